@@ -1,0 +1,803 @@
+/*
+ * CPU oracle for the simulated AllReduce.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or helper with the CUDA
+ * library.
+ *
+ * What it is: a plain, deliberately slow, literal simulation of N ranks that
+ * exchange messages.  Every rank owns a private copy of its buffer; in every
+ * communication step each rank first *posts* a message (a copy of the values it
+ * sends, tagged with the chunk ids it covers), then every rank *receives* the
+ * message addressed to it and applies the elementwise step.  Sent and received
+ * element counts and the number of steps are recorded per rank.
+ *
+ * Sources (page title, section):
+ *  - AllReduce semantics: N processes hold equal-length data, all end with the
+ *    same reduction.  "AllReduce" concept page, §3 技术原理; "AllReduce 集合通信",
+ *    §语义：Reduce 与 Broadcast 的合一.
+ *  - Ring = ReduceScatter (N-1 steps, send one chunk to the next rank, receive
+ *    one from the previous rank, accumulate in place) + AllGather (N-1 steps,
+ *    forward finished chunks, no accumulation).  "Allreduce：大模型分布式训练的
+ *    核心通信算法与优化实践" §2.2; "AllReduce 集合通信" §两阶段流程.
+ *    Reading of the chunk rotation: rank r ends ReduceScatter owning chunk r
+ *    (P0 holds the sum of chunk 0, P1 of chunk 1, ... in §2.2 of the tutorial),
+ *    so in step s rank r sends chunk (r-1-s) mod N and chunk c is folded in the
+ *    order x_{c+1}, x_{c+2}, ..., x_{c+N-1}, x_c.
+ *  - Average: SUM, then divide by the world size once.  Tutorial §3.1;
+ *    "AllReduce 集合通信" §DDP 梯度同步中的地位.
+ *  - Tree / recursive halving: step 1 pairs ranks (0,1), (2,3), ...; step 2
+ *    combines (0/1) with (2/3); log2 N steps.  "【AI Infra小白入门⑩】集合通信
+ *    基础：AllReduce、Ring算法与NCCL全解析" §四 4.1.  Message schedule used here:
+ *    recursive halving (partner r XOR 2^k, k = 0 first) for ReduceScatter, then
+ *    recursive doubling in reverse order for AllGather.
+ *  - Binomial reduce-to-root then broadcast (leaves to root, root to leaves):
+ *    "AllReduce算法详解" §4.3.1-4.3.2 (a second tree schedule; same pairing).
+ *  - Naive central reduce + broadcast: "AllReduce 集合通信" §朴素实现与主节点瓶颈;
+ *    tutorial §2.1.
+ *  - DDP bucketing: buckets of at most bucket_cap (25 MB by default) filled
+ *    with parameters in reverse order.  Tutorial §4.1; "AllReduce 集合通信"
+ *    §DDP 梯度同步中的地位.
+ *
+ * Elementwise step (the pages fix only "sum" / "max"; the arithmetic is IEEE):
+ *  - f32 SUM: IEEE binary32 addition, round to nearest even (C float `+`,
+ *    compiled without contraction or fast-math).
+ *  - bf16 SUM: convert both to binary32 (exact), add, round to bf16 by round-
+ *    to-nearest-even on the dropped 16 bits.  NaN results become 0x7FC0.
+ *  - i32 SUM: two's-complement wrap-around.
+ *  - MAX: IEEE 754-2019 maximum: NaN if either operand is NaN, +0 > -0.
+ *  - AVG: SUM, then the owner of each reduced chunk divides once by N
+ *    (binary32 IEEE division; for bf16 the binary32 quotient is rounded to
+ *    bf16).  AVG on i32 is rejected.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_MAX_RANKS 256
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_I32 = 2 };
+enum { OR_SUM = 0, OR_MAX = 1, OR_AVG = 2 };
+enum { OR_RING = 0, OR_TREE = 1, OR_BINOMIAL = 2, OR_NAIVE = 3 };
+enum { OR_PHASE_RS = 1, OR_PHASE_AG = 2 };
+enum {
+  OR_OK = 0,
+  OR_EINVAL = -1,
+  OR_EUNSUPPORTED = -2,
+  OR_ENOMEM = -3,
+  OR_EMISSING = -4, /* a receiver found no message: a rank dropped out or a message was lost */
+  OR_ESCHEDULE = -5 /* a message arrived with chunks the schedule did not expect */
+};
+
+typedef struct {
+  int32_t steps;     /* communication steps executed */
+  int32_t fail_step; /* step at which a receiver found no message, else -1 */
+  int32_t fail_rank; /* that receiver, else -1 */
+  int32_t pad;
+  int64_t sent[OR_MAX_RANKS]; /* elements each rank sent */
+  int64_t recv[OR_MAX_RANKS]; /* elements each rank received */
+} oracle_stats;
+
+/* Host-side failure injection: kind 1 loses the message that `rank` posts at
+ * global step `step`; kind 2 makes `rank` stop sending from global step `step`
+ * on (it has left the job). */
+typedef struct {
+  int32_t kind;
+  int32_t rank;
+  int32_t step;
+} oracle_fault;
+
+/* ------------------------------------------------------------------------ */
+/* Elementwise arithmetic                                                   */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static int f32_is_nan(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0;
+}
+
+/* Round a binary32 value to bfloat16 (8-bit significand), nearest-even:
+ * keep the upper 16 bits, add one unit if the dropped 16 bits are above half,
+ * or exactly half with the kept part odd.  A carry out of the significand
+ * moves into the exponent, which is what rounding up to the next binade (or to
+ * infinity) means. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u, hi, lo;
+  if (f32_is_nan(f)) return 0x7FC0u;
+  memcpy(&u, &f, 4);
+  hi = u >> 16;
+  lo = u & 0xFFFFu;
+  if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;
+  return (uint16_t)hi;
+}
+
+static float f32_max(float a, float b) {
+  uint32_t ua, ub, r;
+  float out;
+  if (f32_is_nan(a) || f32_is_nan(b)) {
+    r = 0x7FC00000u;
+    memcpy(&out, &r, 4);
+    return out;
+  }
+  if (a > b) return a;
+  if (b > a) return b;
+  /* equal: only +0 / -0 can differ in bits; +0 wins unless both are -0 */
+  memcpy(&ua, &a, 4);
+  memcpy(&ub, &b, 4);
+  r = ua & ub;
+  memcpy(&out, &r, 4);
+  return out;
+}
+
+/* dst[i] = step(first[i], second[i]) */
+static void combine(int dtype, int op, const void* first, const void* second, void* dst, int64_t n) {
+  int64_t i;
+  if (dtype == OR_F32) {
+    const float* a = (const float*)first;
+    const float* b = (const float*)second;
+    float* d = (float*)dst;
+    for (i = 0; i < n; ++i) d[i] = (op == OR_MAX) ? f32_max(a[i], b[i]) : a[i] + b[i];
+  } else if (dtype == OR_BF16) {
+    const uint16_t* a = (const uint16_t*)first;
+    const uint16_t* b = (const uint16_t*)second;
+    uint16_t* d = (uint16_t*)dst;
+    for (i = 0; i < n; ++i) {
+      float fa = bf16_to_f32(a[i]), fb = bf16_to_f32(b[i]);
+      if (op == OR_MAX) {
+        if (f32_is_nan(fa) || f32_is_nan(fb)) d[i] = 0x7FC0u;
+        else if (fa > fb) d[i] = a[i];
+        else if (fb > fa) d[i] = b[i];
+        else d[i] = (uint16_t)(a[i] & b[i]);
+      } else {
+        d[i] = f32_to_bf16_rne(fa + fb);
+      }
+    }
+  } else {
+    const int32_t* a = (const int32_t*)first;
+    const int32_t* b = (const int32_t*)second;
+    int32_t* d = (int32_t*)dst;
+    for (i = 0; i < n; ++i) {
+      if (op == OR_MAX) d[i] = a[i] > b[i] ? a[i] : b[i];
+      else d[i] = (int32_t)((uint32_t)a[i] + (uint32_t)b[i]);
+    }
+  }
+}
+
+static void divide_by(int dtype, void* data, int64_t n, int nranks) {
+  int64_t i;
+  float fn = (float)nranks;
+  if (dtype == OR_F32) {
+    float* d = (float*)data;
+    for (i = 0; i < n; ++i) d[i] = d[i] / fn;
+  } else if (dtype == OR_BF16) {
+    uint16_t* d = (uint16_t*)data;
+    for (i = 0; i < n; ++i) d[i] = f32_to_bf16_rne(bf16_to_f32(d[i]) / fn);
+  }
+}
+
+static int esize_of(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
+
+/* Exported single step, for table checks: out[i] = step(recv[i], local[i]). */
+int oracle_step(int dtype, int op, const void* recv, const void* local, void* out, int64_t n) {
+  if (dtype < 0 || dtype > 2 || op < 0 || op > 1 || n < 0) return OR_EINVAL;
+  combine(dtype, op, recv, local, out, n);
+  return OR_OK;
+}
+
+/* Exported binary32 -> bf16 rounding, for tests of the rounding itself. */
+int oracle_f32_to_bf16(const float* in, uint16_t* out, int64_t n) {
+  int64_t i;
+  for (i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(in[i]);
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunk partition                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Each rank buffer of `count` elements is split into N contiguous chunks,
+ * chunk c = [floor(c*count/N), floor((c+1)*count/N)).  The pages split the data
+ * "evenly into N blocks" without saying what happens when N does not divide
+ * the length; this balanced floor split is the reading used throughout. */
+int oracle_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
+  if (count < 0 || nranks < 1 || c < 0 || c >= nranks || !lo || !hi) return OR_EINVAL;
+  *lo = (int64_t)(((__int128)c * count) / nranks);
+  *hi = (int64_t)(((__int128)(c + 1) * count) / nranks);
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ranks and messages                                                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int present;
+  int src;
+  int nchunks;
+  int chunks[OR_MAX_RANKS];
+  int64_t n;
+  unsigned char* data;
+} message;
+
+typedef struct {
+  int n, dtype, op, es;
+  int64_t m;                      /* positions held per rank */
+  int64_t klo[OR_MAX_RANKS + 1];  /* chunk j = local positions [klo[j], klo[j+1]) */
+  unsigned char* rank[OR_MAX_RANKS];
+  message box[OR_MAX_RANKS];      /* one inbox per rank, emptied every step */
+  oracle_stats* st;
+  const oracle_fault* fault;
+  int step;
+} sim;
+
+static int64_t chunk_len(const sim* s, int j) { return s->klo[j + 1] - s->klo[j]; }
+
+static unsigned char* chunk_ptr(const sim* s, int r, int j) {
+  return s->rank[r] + (size_t)s->klo[j] * (size_t)s->es;
+}
+
+/* Rank `src` posts the listed chunks of its current buffer to `dst`. */
+static int post(sim* s, int src, int dst, const int* chunks, int nchunks) {
+  message* mb = &s->box[dst];
+  int64_t total = 0, off = 0;
+  int i;
+  if (s->fault && s->fault->kind == 2 && s->fault->rank == src && s->step >= s->fault->step)
+    return OR_OK; /* the rank has left: it sends nothing */
+  for (i = 0; i < nchunks; ++i) total += chunk_len(s, chunks[i]);
+  s->st->sent[src] += total;
+  if (s->fault && s->fault->kind == 1 && s->fault->rank == src && s->fault->step == s->step)
+    return OR_OK; /* lost on the wire */
+  if (mb->present) return OR_ESCHEDULE; /* two messages for one receiver in one step */
+  mb->data = (unsigned char*)malloc((size_t)(total > 0 ? total : 1) * (size_t)s->es);
+  if (!mb->data) return OR_ENOMEM;
+  for (i = 0; i < nchunks; ++i) {
+    int64_t len = chunk_len(s, chunks[i]);
+    memcpy(mb->data + (size_t)off * (size_t)s->es, chunk_ptr(s, src, chunks[i]), (size_t)len * (size_t)s->es);
+    off += len;
+    mb->chunks[i] = chunks[i];
+  }
+  mb->present = 1;
+  mb->src = src;
+  mb->nchunks = nchunks;
+  mb->n = total;
+  return OR_OK;
+}
+
+/* Rank `dst` takes the message from `src`, which must cover exactly `chunks`. */
+static int take(sim* s, int dst, int src, const int* chunks, int nchunks, message** out) {
+  message* mb = &s->box[dst];
+  int i;
+  if (!mb->present || mb->src != src) {
+    if (s->st->fail_step < 0) {
+      s->st->fail_step = s->step;
+      s->st->fail_rank = dst;
+    }
+    return OR_EMISSING;
+  }
+  if (mb->nchunks != nchunks) return OR_ESCHEDULE;
+  for (i = 0; i < nchunks; ++i)
+    if (mb->chunks[i] != chunks[i]) return OR_ESCHEDULE;
+  s->st->recv[dst] += mb->n;
+  *out = mb;
+  return OR_OK;
+}
+
+static void drop_box(sim* s, int dst) {
+  if (s->box[dst].present) free(s->box[dst].data);
+  s->box[dst].present = 0;
+  s->box[dst].data = NULL;
+}
+
+static void clear_boxes(sim* s) {
+  int r;
+  for (r = 0; r < s->n; ++r) drop_box(s, r);
+}
+
+static int mod(int a, int n) { return ((a % n) + n) % n; }
+
+/* ------------------------------------------------------------------------ */
+/* Ring                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* ReduceScatter: N-1 steps; in step t rank r sends chunk (r-1-t) mod N to
+ * rank r+1, which folds it into its own copy of that chunk: own = step(recv,
+ * own).  Afterwards rank r holds the reduced chunk r. */
+static int ring_reduce_scatter(sim* s) {
+  int t, r, rc;
+  for (t = 0; t < s->n - 1; ++t) {
+    for (r = 0; r < s->n; ++r) {
+      int j = mod(r - 1 - t, s->n);
+      if ((rc = post(s, r, (r + 1) % s->n, &j, 1))) return rc;
+    }
+    for (r = 0; r < s->n; ++r) {
+      int j = mod(r - 2 - t, s->n);
+      message* mb;
+      if ((rc = take(s, r, mod(r - 1, s->n), &j, 1, &mb))) return rc;
+      combine(s->dtype, s->op, mb->data, chunk_ptr(s, r, j), chunk_ptr(s, r, j), mb->n);
+    }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* AllGather: N-1 steps; in step t rank r sends chunk (r-t) mod N to rank r+1,
+ * which stores it unchanged. */
+static int ring_all_gather(sim* s) {
+  int t, r, rc;
+  for (t = 0; t < s->n - 1; ++t) {
+    for (r = 0; r < s->n; ++r) {
+      int j = mod(r - t, s->n);
+      if ((rc = post(s, r, (r + 1) % s->n, &j, 1))) return rc;
+    }
+    for (r = 0; r < s->n; ++r) {
+      int j = mod(r - 1 - t, s->n);
+      message* mb;
+      if ((rc = take(s, r, mod(r - 1, s->n), &j, 1, &mb))) return rc;
+      memcpy(chunk_ptr(s, r, j), mb->data, (size_t)mb->n * (size_t)s->es);
+    }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tree: recursive halving / recursive doubling                             */
+/* ------------------------------------------------------------------------ */
+
+static int log2_exact(int n) {
+  int k = 0;
+  while ((1 << k) < n) ++k;
+  return (1 << k) == n ? k : -1;
+}
+
+/* Chunks j with j = r (mod 2h): the set rank r keeps after the halving step
+ * of distance h. */
+static int kept_set(int n, int r, int h, int* out) {
+  int j, c = 0;
+  for (j = 0; j < n; ++j)
+    if (j % (2 * h) == r % (2 * h)) out[c++] = j;
+  return c;
+}
+
+/* Step k = 0, 1, ..., log2 N - 1 with distance h = 2^k: rank r and partner
+ * p = r XOR h exchange; each sends the partial values of the chunks the other
+ * keeps, and the receiver folds lower-rank value first: own = step(lower,
+ * upper).  After step k rank r holds, for the chunks j = r (mod 2h), the
+ * reduction over the 2h ranks that agree with r above bit k, combined as a
+ * balanced pairwise tree (ranks 0&1, 2&3, ... then pairs of pairs). */
+static int tree_reduce_scatter(sim* s) {
+  int L = log2_exact(s->n), k, r, rc;
+  int set[OR_MAX_RANKS];
+  for (k = 0; k < L; ++k) {
+    int h = 1 << k;
+    for (r = 0; r < s->n; ++r) {
+      int p = r ^ h;
+      int c = kept_set(s->n, p, h, set);
+      if ((rc = post(s, r, p, set, c))) return rc;
+    }
+    for (r = 0; r < s->n; ++r) {
+      int p = r ^ h, i;
+      int c = kept_set(s->n, r, h, set);
+      int64_t off = 0;
+      message* mb;
+      if ((rc = take(s, r, p, set, c, &mb))) return rc;
+      for (i = 0; i < c; ++i) {
+        unsigned char* own = chunk_ptr(s, r, set[i]);
+        unsigned char* got = mb->data + (size_t)off * (size_t)s->es;
+        int64_t len = chunk_len(s, set[i]);
+        if (r < p) combine(s->dtype, s->op, own, got, own, len);
+        else combine(s->dtype, s->op, got, own, own, len);
+        off += len;
+      }
+    }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* Reverse of the halving: k = log2 N - 1 down to 0; rank r sends the chunks
+ * it holds (j = r mod 2h) to r XOR h, which copies them. */
+static int tree_all_gather(sim* s) {
+  int L = log2_exact(s->n), k, r, rc;
+  int set[OR_MAX_RANKS];
+  for (k = L - 1; k >= 0; --k) {
+    int h = 1 << k;
+    for (r = 0; r < s->n; ++r) {
+      int c = kept_set(s->n, r, h, set);
+      if ((rc = post(s, r, r ^ h, set, c))) return rc;
+    }
+    for (r = 0; r < s->n; ++r) {
+      int p = r ^ h, i;
+      int c = kept_set(s->n, p, h, set);
+      int64_t off = 0;
+      message* mb;
+      if ((rc = take(s, r, p, set, c, &mb))) return rc;
+      for (i = 0; i < c; ++i) {
+        int64_t len = chunk_len(s, set[i]);
+        memcpy(chunk_ptr(s, r, set[i]), mb->data + (size_t)off * (size_t)s->es, (size_t)len * (size_t)s->es);
+        off += len;
+      }
+    }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* Binomial tree: leaves to root, then root to leaves.  Reduce step k
+ * (distance h = 2^k): every rank r = h (mod 2h) sends its whole partial to
+ * r - h, which folds own (lower) first.  Broadcast in reverse: every rank
+ * r = 0 (mod 2h) sends the whole result to r + h. */
+static int binomial_allreduce(sim* s, int avg) {
+  int L = log2_exact(s->n), k, r, rc, j;
+  int all[OR_MAX_RANKS];
+  for (j = 0; j < s->n; ++j) all[j] = j;
+  for (k = 0; k < L; ++k) {
+    int h = 1 << k;
+    for (r = 0; r < s->n; ++r)
+      if (r % (2 * h) == h)
+        if ((rc = post(s, r, r - h, all, s->n))) return rc;
+    for (r = 0; r < s->n; ++r)
+      if (r % (2 * h) == 0) {
+        message* mb;
+        if ((rc = take(s, r, r + h, all, s->n, &mb))) return rc;
+        combine(s->dtype, s->op, s->rank[r], mb->data, s->rank[r], s->m);
+      }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  if (avg) divide_by(s->dtype, s->rank[0], s->m, s->n);
+  for (k = L - 1; k >= 0; --k) {
+    int h = 1 << k;
+    for (r = 0; r < s->n; ++r)
+      if (r % (2 * h) == 0)
+        if ((rc = post(s, r, r + h, all, s->n))) return rc;
+    for (r = 0; r < s->n; ++r)
+      if (r % (2 * h) == h) {
+        message* mb;
+        if ((rc = take(s, r, r - h, all, s->n, &mb))) return rc;
+        memcpy(s->rank[r], mb->data, (size_t)s->m * (size_t)s->es);
+      }
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Naive: rank 0 gathers, reduces, broadcasts                              */
+/* ------------------------------------------------------------------------ */
+
+/* Root-side fold order is x_0, x_1, ..., x_{N-1} (own value first).  The
+ * pages give this schedule only as the bottleneck example; it is compared
+ * only where the result does not depend on order (integers, MAX). */
+static int naive_allreduce(sim* s, int avg) {
+  int r, j, rc;
+  int all[OR_MAX_RANKS];
+  for (j = 0; j < s->n; ++j) all[j] = j;
+  /* gather: one message per non-root rank, received one after another */
+  for (r = 1; r < s->n; ++r) {
+    message* mb;
+    if ((rc = post(s, r, 0, all, s->n))) return rc;
+    if ((rc = take(s, 0, r, all, s->n, &mb))) return rc;
+    combine(s->dtype, s->op, s->rank[0], mb->data, s->rank[0], s->m);
+    clear_boxes(s);
+  }
+  s->step++;
+  s->st->steps++;
+  if (avg) divide_by(s->dtype, s->rank[0], s->m, s->n);
+  for (r = 1; r < s->n; ++r) {
+    message* mb;
+    if ((rc = post(s, 0, r, all, s->n))) return rc;
+    if ((rc = take(s, r, 0, all, s->n, &mb))) return rc;
+    memcpy(s->rank[r], mb->data, (size_t)s->m * (size_t)s->es);
+    clear_boxes(s);
+  }
+  s->step++;
+  s->st->steps++;
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Entry point                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Simulate one collective over N ranks.
+ *
+ *  algo     OR_RING, OR_TREE (recursive halving/doubling), OR_BINOMIAL, OR_NAIVE
+ *  in[r]    rank r's values, out[r] its result (may alias in[r]); npos values
+ *           each when `positions` is given, else `count` values
+ *  positions  NULL, or a strictly increasing list of npos element indices in
+ *           [0, count): the simulation then carries only those positions in
+ *           its messages (elements are independent, and the chunk of each
+ *           position follows from `count`)
+ *  phases   OR_PHASE_RS (ReduceScatter; AVG divides here), OR_PHASE_AG
+ *           (AllGather of the shard each rank owns), or both (AllReduce)
+ *  st       filled with step and volume counts
+ *  fault    NULL or a host-side failure to inject
+ */
+int oracle_collective(int algo, const void* const* in, void* const* out, int nranks, int64_t count,
+                      const int64_t* positions, int64_t npos, int dtype, int op, int phases,
+                      oracle_stats* st, const oracle_fault* fault) {
+  sim* s;
+  int r, j, rc = OR_OK;
+  int64_t i, m;
+  oracle_stats local_st;
+  if (!st) st = &local_st;
+  memset(st, 0, sizeof(*st));
+  st->fail_step = -1;
+  st->fail_rank = -1;
+  if (nranks < 1 || nranks > OR_MAX_RANKS || count < 0 || !in || !out) return OR_EINVAL;
+  if (dtype < 0 || dtype > 2 || op < 0 || op > 2 || phases < 1 || phases > 3) return OR_EINVAL;
+  if (op == OR_AVG && dtype == OR_I32) return OR_EUNSUPPORTED;
+  if (algo < 0 || algo > 3) return OR_EINVAL;
+  if (algo != OR_RING && algo != OR_NAIVE && log2_exact(nranks) < 0) return OR_EUNSUPPORTED;
+  if ((algo == OR_BINOMIAL || algo == OR_NAIVE) && phases != 3) return OR_EUNSUPPORTED;
+  m = positions ? npos : count;
+  if (positions) {
+    for (i = 0; i < npos; ++i)
+      if (positions[i] < 0 || positions[i] >= count || (i > 0 && positions[i] <= positions[i - 1])) return OR_EINVAL;
+  }
+  s = (sim*)calloc(1, sizeof(sim));
+  if (!s) return OR_ENOMEM;
+  s->n = nranks;
+  s->dtype = dtype;
+  s->op = op;
+  s->es = esize_of(dtype);
+  s->m = m;
+  s->st = st;
+  s->fault = fault;
+  /* chunk j covers the local positions whose element index lies in chunk j */
+  for (j = 0; j <= nranks; ++j) {
+    int64_t lo = (int64_t)(((__int128)j * count) / nranks);
+    if (!positions) {
+      s->klo[j] = lo;
+    } else {
+      int64_t k = 0;
+      while (k < npos && positions[k] < lo) ++k;
+      s->klo[j] = k;
+    }
+  }
+  for (r = 0; r < nranks; ++r) {
+    s->rank[r] = (unsigned char*)malloc((size_t)(m > 0 ? m : 1) * (size_t)s->es);
+    if (!s->rank[r]) {
+      rc = OR_ENOMEM;
+      goto done;
+    }
+    memcpy(s->rank[r], in[r], (size_t)m * (size_t)s->es);
+  }
+  if (algo == OR_RING || algo == OR_TREE) {
+    if (phases & OR_PHASE_RS) {
+      rc = algo == OR_RING ? ring_reduce_scatter(s) : tree_reduce_scatter(s);
+      if (rc) goto done;
+      if (op == OR_AVG)
+        for (r = 0; r < nranks; ++r) divide_by(dtype, chunk_ptr(s, r, r), chunk_len(s, r), nranks);
+    }
+    if (phases & OR_PHASE_AG) {
+      rc = algo == OR_RING ? ring_all_gather(s) : tree_all_gather(s);
+      if (rc) goto done;
+    }
+  } else if (algo == OR_BINOMIAL) {
+    rc = binomial_allreduce(s, op == OR_AVG);
+  } else {
+    rc = naive_allreduce(s, op == OR_AVG);
+  }
+  if (rc) goto done;
+  for (r = 0; r < nranks; ++r) memcpy(out[r], s->rank[r], (size_t)m * (size_t)s->es);
+done:
+  clear_boxes(s);
+  for (r = 0; r < nranks; ++r) free(s->rank[r]);
+  free(s);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* DDP buckets                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bucket plan.  Walk the tensors in reverse registration order and add each
+ * to the current bucket while the bucket stays within cap_bytes; a tensor that
+ * does not fit closes the bucket and opens the next one; a tensor larger than
+ * the cap therefore sits alone.  Inside a bucket tensors are laid out in the
+ * order they were added (reverse registration order).  Bucket 0 holds the
+ * last-registered tensors.
+ */
+int oracle_bucket_plan(const int64_t* counts, int ntensors, int dtype, int64_t cap_bytes,
+                       int32_t* bucket_of, int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets) {
+  int t, b = -1;
+  int64_t fill = 0;
+  int es;
+  if (ntensors < 0 || cap_bytes <= 0 || dtype < 0 || dtype > 2 || !nbuckets) return OR_EINVAL;
+  es = esize_of(dtype);
+  for (t = ntensors - 1; t >= 0; --t) {
+    int64_t bytes;
+    if (counts[t] < 0) return OR_EINVAL;
+    bytes = counts[t] * es;
+    if (b < 0 || (fill > 0 && fill + bytes > cap_bytes)) {
+      ++b;
+      bucket_count[b] = 0;
+      fill = 0;
+    }
+    bucket_of[t] = b;
+    offset_in_bucket[t] = bucket_count[b];
+    bucket_count[b] += counts[t];
+    fill += bytes;
+  }
+  *nbuckets = b + 1;
+  return OR_OK;
+}
+
+typedef struct {
+  int64_t pos;
+  int64_t id;
+} pair;
+
+static int cmp_pair(const void* a, const void* b) {
+  int64_t x = ((const pair*)a)->pos, y = ((const pair*)b)->pos;
+  return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/*
+ * Bucketed AllReduce, literally: for each bucket, every rank packs its
+ * tensors into a flat bucket buffer, the ranks run one collective over the
+ * bucket buffers, and every rank copies the result back into its tensors.
+ *
+ *  grads_in / grads_out  [nranks * ntensors] pointers, row-major by rank
+ *  samp_tensor / samp_index / nsamp   when nsamp > 0 only these elements are
+ *           carried (tensor id, element index; all distinct), and results go
+ *           to samp_out[r * nsamp + i]; grads_out is then unused
+ */
+int oracle_bucketed_allreduce(const void* const* grads_in, void* const* grads_out, const int64_t* counts,
+                              int ntensors, int nranks, int dtype, int op, int algo, int64_t cap_bytes,
+                              const int32_t* samp_tensor, const int64_t* samp_index, int64_t nsamp,
+                              void* samp_out, oracle_stats* st_total) {
+  int32_t *bucket_of = NULL, nb = 0;
+  int64_t *off = NULL, *bcount = NULL;
+  int es, b, r, t, rc = OR_OK;
+  oracle_stats st;
+  if (ntensors < 0 || nranks < 1 || nranks > OR_MAX_RANKS || dtype < 0 || dtype > 2) return OR_EINVAL;
+  es = esize_of(dtype);
+  bucket_of = (int32_t*)calloc((size_t)(ntensors + 1), sizeof(int32_t));
+  off = (int64_t*)calloc((size_t)(ntensors + 1), sizeof(int64_t));
+  bcount = (int64_t*)calloc((size_t)(ntensors + 1), sizeof(int64_t));
+  if (!bucket_of || !off || !bcount) {
+    rc = OR_ENOMEM;
+    goto out;
+  }
+  if ((rc = oracle_bucket_plan(counts, ntensors, dtype, cap_bytes, bucket_of, off, bcount, &nb))) goto out;
+  if (st_total) {
+    memset(st_total, 0, sizeof(*st_total));
+    st_total->fail_step = -1;
+    st_total->fail_rank = -1;
+  }
+  for (b = 0; b < nb; ++b) {
+    void* bufs[OR_MAX_RANKS];
+    int64_t* pos = NULL;
+    int64_t* which = NULL; /* sample id of each carried position */
+    int64_t m = 0, i;
+    if (nsamp > 0) {
+      /* this bucket's samples as (bucket offset, sample id), ascending */
+      pair* ps = (pair*)malloc((size_t)(nsamp + 1) * sizeof(pair));
+      pos = (int64_t*)malloc((size_t)(nsamp + 1) * sizeof(int64_t));
+      which = (int64_t*)malloc((size_t)(nsamp + 1) * sizeof(int64_t));
+      if (!ps || !pos || !which) {
+        free(ps);
+        free(pos);
+        free(which);
+        rc = OR_ENOMEM;
+        goto out;
+      }
+      for (i = 0; i < nsamp; ++i) {
+        int32_t ts = samp_tensor[i];
+        if (ts < 0 || ts >= ntensors || samp_index[i] < 0 || samp_index[i] >= counts[ts]) {
+          rc = OR_EINVAL;
+          break;
+        }
+        if (bucket_of[ts] == b) {
+          ps[m].pos = off[ts] + samp_index[i];
+          ps[m].id = i;
+          ++m;
+        }
+      }
+      if (!rc) {
+        qsort(ps, (size_t)m, sizeof(pair), cmp_pair);
+        for (i = 0; i < m; ++i) {
+          if (i > 0 && ps[i].pos == ps[i - 1].pos) rc = OR_EINVAL; /* samples must be distinct */
+          pos[i] = ps[i].pos;
+          which[i] = ps[i].id;
+        }
+      }
+      free(ps);
+      if (rc) {
+        free(pos);
+        free(which);
+        goto out;
+      }
+    } else {
+      m = bcount[b];
+    }
+    for (r = 0; r < nranks; ++r) {
+      bufs[r] = malloc((size_t)(m > 0 ? m : 1) * (size_t)es);
+      if (!bufs[r]) {
+        int q;
+        for (q = 0; q < r; ++q) free(bufs[q]);
+        free(pos);
+        free(which);
+        rc = OR_ENOMEM;
+        goto out;
+      }
+    }
+    /* pack */
+    for (r = 0; r < nranks; ++r) {
+      if (nsamp > 0) {
+        for (i = 0; i < m; ++i) {
+          /* find the tensor holding bucket offset pos[i] */
+          for (t = 0; t < ntensors; ++t)
+            if (bucket_of[t] == b && pos[i] >= off[t] && pos[i] < off[t] + counts[t]) break;
+          memcpy((unsigned char*)bufs[r] + (size_t)i * es,
+                 (const unsigned char*)grads_in[(size_t)r * ntensors + t] + (size_t)(pos[i] - off[t]) * es, (size_t)es);
+        }
+      } else {
+        for (t = 0; t < ntensors; ++t)
+          if (bucket_of[t] == b)
+            memcpy((unsigned char*)bufs[r] + (size_t)off[t] * es, grads_in[(size_t)r * ntensors + t],
+                   (size_t)counts[t] * es);
+      }
+    }
+    rc = oracle_collective(algo, (const void* const*)bufs, bufs, nranks, bcount[b], nsamp > 0 ? pos : NULL, m, dtype, op, 3,
+                           &st, NULL);
+    if (!rc) {
+      if (st_total) {
+        st_total->steps += st.steps;
+        for (r = 0; r < nranks; ++r) {
+          st_total->sent[r] += st.sent[r];
+          st_total->recv[r] += st.recv[r];
+        }
+      }
+      /* unpack */
+      for (r = 0; r < nranks; ++r) {
+        if (nsamp > 0) {
+          for (i = 0; i < m; ++i)
+            memcpy((unsigned char*)samp_out + ((size_t)r * nsamp + which[i]) * es, (unsigned char*)bufs[r] + (size_t)i * es,
+                   (size_t)es);
+        } else {
+          for (t = 0; t < ntensors; ++t)
+            if (bucket_of[t] == b)
+              memcpy(grads_out[(size_t)r * ntensors + t], (unsigned char*)bufs[r] + (size_t)off[t] * es,
+                     (size_t)counts[t] * es);
+        }
+      }
+    }
+    for (r = 0; r < nranks; ++r) free(bufs[r]);
+    free(pos);
+    free(which);
+    if (rc) goto out;
+  }
+out:
+  free(bucket_of);
+  free(off);
+  free(bcount);
+  return rc;
+}
+
+int oracle_max_ranks(void) { return OR_MAX_RANKS; }

@@ -1,0 +1,689 @@
+"""Pins for the CPU oracle: values and invariants fixed by the pages or by
+arithmetic, each chosen so that a plausible mistake in the oracle (a wrong
+chunk rotation, a dropped step, a wrong rounding, a transposed operand, a
+miscounted message) fails at least one of them.  No GPU needed."""
+from fractions import Fraction
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from allreduce_gradient_reduction_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ALL_DTYPES = ("f32", "bf16", "i32")
+
+
+def read_golden(name):
+    spec = {"ranks": {}}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "rank":
+                spec["ranks"][int(vals[0])] = [float(v) for v in vals[1:]]
+            elif key in ("nranks", "count"):
+                spec[key] = int(vals[0])
+            elif key == "op":
+                spec[key] = vals[0]
+            else:
+                spec[key] = [float(v) for v in vals]
+    return spec
+
+
+def to_storage(vals, dtype):
+    a = np.asarray(vals, dtype=np.float32)
+    if dtype == "f32":
+        return a
+    if dtype == "i32":
+        return a.astype(np.int32)
+    return (a.view(np.uint32) >> 16).astype(np.uint16)  # the golden values are exact in bf16
+
+
+def to_f64(x, dtype):
+    x = np.asarray(x)
+    if dtype == "bf16":
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def algos_for(n):
+    out = ["ring", "naive"]
+    if n & (n - 1) == 0:
+        out += ["tree", "binomial"]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Worked examples printed on the pages
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("name", ["three_rank_sum.txt", "four_rank_ones.txt"])
+def test_printed_sum_examples(oracle_lib, name, dtype):
+    g = read_golden(name)
+    x = np.stack([to_storage(g["ranks"][r], dtype) for r in range(g["nranks"])])
+    for algo in algos_for(g["nranks"]):
+        out, st = oracle.allreduce(x, algo=algo, op="sum", dtype=dtype)
+        assert np.all(to_f64(out, dtype) == np.asarray(g["expect"])[None, :]), algo
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_printed_ddp_average(oracle_lib, dtype):
+    g = read_golden("ddp_average.txt")
+    x = np.stack([to_storage(g["ranks"][r], dtype) for r in range(g["nranks"])])
+    for algo in algos_for(g["nranks"]):
+        s, _ = oracle.allreduce(x, algo=algo, op="sum", dtype=dtype)
+        a, _ = oracle.allreduce(x, algo=algo, op="avg", dtype=dtype)
+        assert np.all(to_f64(s, dtype) == g["expect_sum"]), algo
+        assert np.all(to_f64(a, dtype) == g["expect_avg"]), algo
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 8, 16])
+def test_ddp_average_general_n(oracle_lib, n):
+    # ones * rank summed over N ranks is N(N-1)/2; divided by N it is (N-1)/2
+    x = np.stack([np.full(7, r, dtype=np.float32) for r in range(n)])
+    out, _ = oracle.allreduce(x, op="avg", dtype="f32")
+    assert np.all(out == np.float32((n - 1) / 2))
+
+
+# --------------------------------------------------------------------------
+# Chunk partition
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("count,n", [(0, 1), (0, 5), (1, 3), (7, 8), (8, 8), (9, 8), (4096, 4), (1001, 7),
+                                     (67_108_864, 8), ((1 << 40) + 3, 64)])
+def test_chunk_partition(oracle_lib, count, n):
+    rngs = [oracle.chunk_range(count, n, c) for c in range(n)]
+    assert rngs[0][0] == 0 and rngs[-1][1] == count
+    for (lo, hi), (lo2, _) in zip(rngs, rngs[1:]):
+        assert hi == lo2  # contiguous, in order
+    sizes = [hi - lo for lo, hi in rngs]
+    assert min(sizes) >= 0 and max(sizes) - min(sizes) <= 1
+    if count % n == 0:
+        assert all(s == count // n for s in sizes)
+
+
+def test_chunk_partition_three_rank_scalar(oracle_lib):
+    # one element split three ways: the element lies in the last chunk
+    assert [oracle.chunk_range(1, 3, c) for c in range(3)] == [(0, 0), (0, 0), (0, 1)]
+
+
+# --------------------------------------------------------------------------
+# Elementwise arithmetic
+# --------------------------------------------------------------------------
+
+def bf16_round_by_value(v):
+    """Round finite float64 values to bf16 by value: find the bf16 grid
+    spacing of the binade, take the two neighbours, pick the nearer, ties to
+    the even multiple; magnitudes at 2^128 and beyond become infinity."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, e = np.frexp(a)
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    q = a / ulp
+    fl = np.floor(q)
+    rem = q - fl
+    up = (rem > 0.5) | ((rem == 0.5) & (np.fmod(fl, 2.0) == 1.0))
+    r = (fl + up) * ulp
+    r = np.where(r >= 2.0 ** 128, np.inf, r)
+    return np.copysign(r, v)
+
+
+def test_bf16_rounding_edges(oracle_lib):
+    hi = np.arange(1 << 16, dtype=np.uint32)
+    lows = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0xFFFF, 0x4000, 0xC000], dtype=np.uint32)
+    bits = (hi[:, None] << 16 | lows[None, :]).reshape(-1)
+    f = bits.view(np.float32)
+    finite = np.isfinite(f)
+    got = oracle.f32_to_bf16(f)
+    gv = to_f64(got, "bf16")
+    want = bf16_round_by_value(f[finite].astype(np.float64))
+    assert np.array_equal(gv[finite], want)
+    assert np.array_equal(np.signbit(gv[finite]), np.signbit(want))
+    # infinities stay, NaNs stay NaN
+    inf = np.isinf(f)
+    assert np.array_equal(gv[inf], f[inf].astype(np.float64))
+    assert np.all(np.isnan(gv[np.isnan(f)]))
+
+
+def test_bf16_rounding_random(oracle_lib):
+    g = np.random.Generator(np.random.PCG64(7))
+    bits = g.integers(0, 1 << 32, size=2_000_000, dtype=np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    gv = to_f64(oracle.f32_to_bf16(f), "bf16")
+    assert np.array_equal(gv, bf16_round_by_value(f.astype(np.float64)))
+
+
+def _frac_round_bf16(x: Fraction):
+    """Correctly rounded bf16 value of an exact rational (nearest, ties even);
+    returns a float (inf on overflow)."""
+    if x == 0:
+        return 0.0
+    s = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** max(e - 7, -133)
+    q = a / ulp
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * ulp
+    if r >= Fraction(2) ** 128:
+        return s * math.inf
+    return s * float(r)
+
+
+def _bf16_pairs(n, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    a = g.integers(0, 1 << 16, size=n, dtype=np.uint16)
+    # b near a in exponent half the time, so rounding is non-trivial
+    b_near = (a.astype(np.int32) + g.integers(-2000, 2000, size=n)).clip(0, 0xFFFF).astype(np.uint16)
+    b_near ^= (g.integers(0, 2, size=n, dtype=np.uint16) << 15)
+    b_far = g.integers(0, 1 << 16, size=n, dtype=np.uint16)
+    b = np.where(g.random(n) < 0.5, b_near, b_far).astype(np.uint16)
+    fa, fb = to_f64(a, "bf16"), to_f64(b, "bf16")
+    keep = np.isfinite(fa) & np.isfinite(fb)
+    return a[keep], b[keep]
+
+
+def test_bf16_add_is_correctly_rounded(oracle_lib):
+    a, b = _bf16_pairs(30000, 11)
+    got = to_f64(oracle.step(a, b, op="sum", dtype="bf16"), "bf16")
+    fa, fb = to_f64(a, "bf16"), to_f64(b, "bf16")
+    for i in range(a.size):
+        exact = Fraction(float(fa[i])) + Fraction(float(fb[i]))
+        want = _frac_round_bf16(exact)
+        if exact == 0:
+            want = -0.0 if (math.copysign(1, fa[i]) < 0 and math.copysign(1, fb[i]) < 0) else 0.0
+        assert got[i] == want and math.copysign(1, got[i]) == math.copysign(1, want), (hex(a[i]), hex(b[i]))
+
+
+def test_bf16_add_matches_torch_cpu(oracle_lib):
+    torch = pytest.importorskip("torch")
+    a, b = _bf16_pairs(1_000_000, 12)
+    got = oracle.step(a, b, op="sum", dtype="bf16")
+    ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    want = (ta + tb).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(to_f64(want, "bf16"))
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.all(np.isnan(to_f64(got[nan], "bf16")))
+
+
+def test_f32_add_matches_numpy(oracle_lib):
+    a = W.random_bits(1, 500_000, "f32", 3)[0]
+    b = W.random_bits(1, 500_000, "f32", 4)[0]
+    b[::3] = a[::3] * np.float32(-0.75)  # cancellation
+    with np.errstate(all="ignore"):
+        want = a + b
+    got = oracle.step(a, b, op="sum", dtype="f32")
+    nan = np.isnan(want)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    assert np.all(np.isnan(got[nan]))
+
+
+def test_i32_add_wraps(oracle_lib):
+    a = np.array([2**31 - 1, -2**31, 5, -7, 0], dtype=np.int32)
+    b = np.array([1, -1, -5, 7, 0], dtype=np.int32)
+    want = [((int(x) + int(y) + 2**31) % 2**32) - 2**31 for x, y in zip(a, b)]
+    assert oracle.step(a, b, op="sum", dtype="i32").tolist() == want
+
+
+def test_max_special_values(oracle_lib):
+    nan, inf = np.float32("nan"), np.float32("inf")
+    a = np.array([0.0, -0.0, -0.0, nan, 1.0, -inf, 3.0, -2.0], dtype=np.float32)
+    b = np.array([-0.0, 0.0, -0.0, 1.0, nan, 5.0, 2.0, -1.0], dtype=np.float32)
+    got = oracle.step(a, b, op="max", dtype="f32")
+    assert got[0] == 0 and not np.signbit(got[0])
+    assert got[1] == 0 and not np.signbit(got[1])
+    assert got[2] == 0 and np.signbit(got[2])
+    assert np.isnan(got[3]) and np.isnan(got[4])
+    assert got[5:].tolist() == [5.0, 3.0, -1.0]
+    ab, bb = to_storage(a, "f32"), to_storage(b, "f32")
+    ab = (a.view(np.uint32) >> 16).astype(np.uint16)
+    bb = (b.view(np.uint32) >> 16).astype(np.uint16)
+    gb = to_f64(oracle.step(ab, bb, op="max", dtype="bf16"), "bf16")
+    assert gb[0] == 0 and not np.signbit(gb[0])
+    assert gb[2] == 0 and np.signbit(gb[2])
+    assert np.isnan(gb[3]) and np.isnan(gb[4])
+    assert gb[5:].tolist() == [5.0, 3.0, -1.0]
+    ia = np.array([-5, 7, -2**31], dtype=np.int32)
+    ib = np.array([3, -9, 2**31 - 1], dtype=np.int32)
+    assert oracle.step(ia, ib, op="max", dtype="i32").tolist() == [3, 7, 2**31 - 1]
+
+
+# --------------------------------------------------------------------------
+# Brute force on tiny inputs: order-free results must be exact
+# --------------------------------------------------------------------------
+
+SIZES = [0, 1, 2, 3, 5, 7, 8, 9, 31, 257, 1000]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_bruteforce_integers_and_max(oracle_lib, n):
+    g = np.random.Generator(np.random.PCG64(100 + n))
+    for count in SIZES + [n - 1, n, n + 1]:
+        if count < 0:
+            continue
+        xi = g.integers(-2**31, 2**31, size=(n, count), dtype=np.int64).astype(np.int32)
+        exact = ((xi.astype(object).sum(axis=0) + 2**31) % 2**32) - 2**31 if count else np.zeros(0)
+        xf = g.integers(-8, 9, size=(n, count)).astype(np.float32)
+        xb = to_storage(xf.reshape(-1), "bf16").reshape(n, count)
+        xr = g.standard_normal((n, count)).astype(np.float32)
+        for algo in algos_for(n):
+            out, _ = oracle.allreduce(xi, algo=algo, op="sum", dtype="i32")
+            assert [list(map(int, row)) for row in out] == [list(map(int, exact))] * n, (algo, count)
+            out, _ = oracle.allreduce(xi, algo=algo, op="max", dtype="i32")
+            assert np.array_equal(out, np.broadcast_to(xi.max(axis=0), out.shape))
+            out, _ = oracle.allreduce(xf, algo=algo, op="sum", dtype="f32")
+            assert np.array_equal(out, np.broadcast_to(xf.astype(np.float64).sum(axis=0), out.shape))
+            out, _ = oracle.allreduce(xb, algo=algo, op="sum", dtype="bf16")  # |sum| <= 64: exact in bf16
+            assert np.array_equal(to_f64(out, "bf16"), np.broadcast_to(xf.astype(np.float64).sum(axis=0), out.shape))
+            out, _ = oracle.allreduce(xr, algo=algo, op="max", dtype="f32")
+            assert np.array_equal(out, np.broadcast_to(xr.max(axis=0), out.shape))
+
+
+# --------------------------------------------------------------------------
+# Fold order: the message simulation equals the closed-form per-element fold
+# --------------------------------------------------------------------------
+
+def _lib_add(dtype):
+    """Addition by a library routine in the storage type: numpy float32 /
+    int32, torch's CPU bf16 addition."""
+    if dtype == "bf16":
+        import torch
+
+        def add(a, b):
+            ta = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+            tb = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+            return (ta + tb).view(torch.int16).numpy().view(np.uint16)
+        return add
+    return lambda a, b: a + b
+
+
+def ring_closed_form(x, dtype):
+    """Chunk c (balanced floor split) folds x_{c+1}, x_{c+2}, ..., x_c."""
+    n, count = x.shape
+    add = _lib_add(dtype)
+    out = np.empty(count, dtype=x.dtype)
+    for c in range(n):
+        lo, hi = oracle.chunk_range(count, n, c)
+        acc = x[(c + 1) % n, lo:hi].copy()
+        for k in range(2, n + 1):
+            acc = add(acc, x[(c + k) % n, lo:hi])
+        out[lo:hi] = acc
+    return out
+
+
+def tree_closed_form(x, dtype):
+    """Balanced pairwise tree over ranks: (x0+x1), (x2+x3), ... then pairs of
+    pairs, the lower-rank partial first."""
+    add = _lib_add(dtype)
+    level = [x[r] for r in range(x.shape[0])]
+    while len(level) > 1:
+        level = [add(level[2 * i], level[2 * i + 1]) for i in range(len(level) // 2)]
+    return level[0]
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8, 16])
+def test_ring_order_closed_form(oracle_lib, dtype, n):
+    with np.errstate(over="ignore"):
+        for count in [1, n - 1, n, n + 3, 97, 1024 + 5]:
+            if count <= 0:
+                continue
+            x = W.uniform_inputs(n, count, dtype, config=900 + count) if dtype != "f32" else \
+                W.normal_inputs(n, count, 1.0, 900 + count)
+            out, _ = oracle.allreduce(x, algo="ring", op="sum", dtype=dtype)
+            want = ring_closed_form(x, dtype)
+            assert np.array_equal(out, np.broadcast_to(want, out.shape)), count
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32])
+def test_tree_order_closed_form(oracle_lib, dtype, n):
+    with np.errstate(over="ignore"):
+        for count in [1, n + 3, 257]:
+            x = W.uniform_inputs(n, count, dtype, config=700 + count) if dtype != "f32" else \
+                W.normal_inputs(n, count, 1.0, 700 + count)
+            want = tree_closed_form(x, dtype)
+            for algo in ("tree", "binomial"):
+                out, _ = oracle.allreduce(x, algo=algo, op="sum", dtype=dtype)
+                assert np.array_equal(out, np.broadcast_to(want, out.shape)), (algo, count)
+
+
+def test_ring_order_differs_from_other_rotations(oracle_lib):
+    # the fold order is observable in f32: a rotation one rank off gives other bits
+    n, count = 8, 4096
+    x = W.large_inputs(n, count, config=42)
+    out, _ = oracle.allreduce(x, algo="ring", op="sum", dtype="bf16")
+    add = _lib_add("bf16")
+    wrong = np.empty(count, dtype=np.uint16)
+    for c in range(n):
+        lo, hi = oracle.chunk_range(count, n, c)
+        acc = x[c % n, lo:hi].copy()  # starts at x_c instead of x_{c+1}
+        for k in range(1, n):
+            acc = add(acc, x[(c + k) % n, lo:hi])
+        wrong[lo:hi] = acc
+    assert not np.array_equal(out[0], wrong)
+
+
+# --------------------------------------------------------------------------
+# AVG
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 3, 8])
+def test_avg_f32_is_sum_then_divide(oracle_lib, n):
+    x = W.normal_inputs(n, 999, 1e-3, 55)
+    s, _ = oracle.allreduce(x, op="sum", dtype="f32")
+    a, _ = oracle.allreduce(x, op="avg", dtype="f32")
+    assert np.array_equal(a, s / np.float32(n))
+
+
+@pytest.mark.parametrize("n", [3, 8])
+def test_avg_bf16_correctly_rounded_quotient(oracle_lib, n):
+    x = W.uniform_inputs(n, 3000, "bf16", config=66)
+    s, _ = oracle.allreduce(x, op="sum", dtype="bf16")
+    a, _ = oracle.allreduce(x, op="avg", dtype="bf16")
+    sv, av = to_f64(s[0], "bf16"), to_f64(a[0], "bf16")
+    for i in range(sv.size):
+        want = _frac_round_bf16(Fraction(float(sv[i])) / n)
+        assert av[i] == want, i
+
+
+def test_avg_rejects_integers(oracle_lib):
+    x = np.zeros((2, 4), dtype=np.int32)
+    _, st = oracle.allreduce(x, op="avg", dtype="i32", raise_on_error=False)
+    assert st["rc"] == -2
+
+
+# --------------------------------------------------------------------------
+# Invariants of the collective
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+def test_rs_plus_ag_equals_allreduce(oracle_lib, algo, dtype):
+    for n in ([2, 4, 8, 16] if algo == "tree" else [2, 3, 5, 8]):
+        for count in [1, n, 3 * n + 1, 1000]:
+            x = W.random_bits(n, count, dtype, seed=n * 1000 + count)
+            ops = ["sum", "max"] + (["avg"] if dtype != "i32" else [])
+            for op in ops:
+                with np.errstate(all="ignore"):
+                    ar, _ = oracle.allreduce(x, algo=algo, op=op, dtype=dtype)
+                    rs, _ = oracle.reduce_scatter(x, algo=algo, op=op, dtype=dtype)
+                    # AllGather of the owned shards only: fill everything else with junk first
+                    shards = W.random_bits(n, count, dtype, seed=5)
+                    for r in range(n):
+                        lo, hi = oracle.chunk_range(count, n, r)
+                        shards[r, lo:hi] = rs[r, lo:hi]
+                        # after ReduceScatter the owner holds the finished chunk
+                        assert _same(rs[r, lo:hi], ar[r, lo:hi], dtype)
+                    ag, _ = oracle.all_gather(shards, algo=algo, dtype=dtype)
+                assert _same(ag, ar, dtype), (n, count, op)
+                # every rank ends identical
+                assert all(_same(ar[r], ar[0], dtype) for r in range(n))
+
+
+def _same(a, b, dtype):
+    """Bit equality, with all NaNs equal to each other."""
+    a, b = np.asarray(a), np.asarray(b)
+    if dtype == "i32":
+        return np.array_equal(a, b)
+    fa, fb = to_f64(a, dtype), to_f64(b, dtype)
+    na, nb = np.isnan(fa), np.isnan(fb)
+    if not np.array_equal(na, nb):
+        return False
+    ua = a.view(np.uint16 if dtype == "bf16" else np.uint32)
+    ub = b.view(np.uint16 if dtype == "bf16" else np.uint32)
+    return np.array_equal(ua[~na], ub[~nb])
+
+
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+def test_all_gather_copies_bits(oracle_lib, algo):
+    # AllGather forwards finished chunks without arithmetic: NaN payloads,
+    # signed zeros and subnormals arrive bit for bit
+    n, count = 8, 64
+    x = np.zeros((n, count), dtype=np.uint32)
+    special = np.array([0x7FC00001, 0xFFC12345, 0x80000000, 0x00000001, 0x7F800000, 0x807FFFFF], dtype=np.uint32)
+    for r in range(n):
+        lo, hi = oracle.chunk_range(count, n, r)
+        x[r, lo:hi] = np.resize(special + r, hi - lo)
+    out, _ = oracle.all_gather(x.view(np.float32), algo=algo, dtype="f32")
+    want = np.zeros(count, dtype=np.uint32)
+    for r in range(n):
+        lo, hi = oracle.chunk_range(count, n, r)
+        want[lo:hi] = x[r, lo:hi]
+    assert np.array_equal(out.view(np.uint32), np.broadcast_to(want, out.shape))
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16])
+def test_ring_volume_and_steps(oracle_lib, n):
+    count = 64 * n  # N divides D
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="ring", dtype="f32")
+    assert st["steps"] == 2 * (n - 1)
+    assert np.all(st["sent"] == 2 * (n - 1) * count // n)
+    assert np.all(st["recv"] == 2 * (n - 1) * count // n)
+    _, st = oracle.reduce_scatter(x, algo="ring", dtype="f32")
+    assert st["steps"] == n - 1 and np.all(st["sent"] == (n - 1) * count // n)
+    # uneven split: each rank sends every chunk but its own in ReduceScatter
+    # and every chunk but its successor's in AllGather
+    count = 10 * n + 3
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="ring", dtype="f32")
+    size = [oracle.chunk_range(count, n, c)[1] - oracle.chunk_range(count, n, c)[0] for c in range(n)]
+    for r in range(n):
+        assert st["sent"][r] == (count - size[r]) + (count - size[(r + 1) % n])
+    assert st["sent"].sum() == 2 * (n - 1) * count
+
+
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 64])
+def test_tree_volume_and_steps(oracle_lib, n):
+    count = 8 * n
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="tree", dtype="f32")
+    L = int(math.log2(n))
+    assert st["steps"] == 2 * L
+    # halving then doubling moves the bandwidth-optimal 2(N-1)/N * D per rank
+    assert np.all(st["sent"] == 2 * (n - 1) * count // n)
+    _, st = oracle.allreduce(x, algo="binomial", dtype="f32")
+    assert st["steps"] == 2 * L
+    # the root receives log2 N full buffers and sends log2 N full buffers
+    assert st["sent"][0] + st["recv"][0] == 2 * count * L
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_naive_root_volume(oracle_lib, n):
+    count = 12
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="naive", dtype="f32")
+    assert st["recv"][0] == (n - 1) * count and st["sent"][0] == (n - 1) * count
+    assert st["sent"][0] + st["recv"][0] == 2 * (n - 1) * count
+
+
+def test_tree_needs_power_of_two(oracle_lib):
+    x = np.ones((3, 4), dtype=np.float32)
+    for algo in ("tree", "binomial"):
+        _, st = oracle.allreduce(x, algo=algo, dtype="f32", raise_on_error=False)
+        assert st["rc"] == -2
+
+
+# --------------------------------------------------------------------------
+# Error bound against the order-free sum
+# --------------------------------------------------------------------------
+
+def gamma(k, u):
+    return k * u / (1 - k * u)
+
+
+@pytest.mark.parametrize("dtype,u", [("f32", 2.0 ** -24), ("bf16", 2.0 ** -8)])
+@pytest.mark.parametrize("n", [2, 8, 64])
+def test_error_bound(oracle_lib, dtype, u, n):
+    count = 20000 if n < 64 else 2000
+    x = W.uniform_inputs(n, count, dtype, config=300 + n)
+    xv = to_f64(x, dtype)
+    exact = xv.sum(axis=0)  # exact enough: float64 has 29+ spare bits here
+    absum = np.abs(xv).sum(axis=0)
+    for algo, depth in (("ring", n - 1), ("tree", int(math.log2(n)))):
+        out, _ = oracle.allreduce(x, algo=algo, op="sum", dtype=dtype)
+        err = np.abs(to_f64(out[0], dtype) - exact)
+        assert np.all(err <= gamma(depth, u) * absum), algo
+    if dtype == "f32":
+        out, _ = oracle.allreduce(x, algo="ring", op="sum", dtype=dtype)
+        assert np.all(np.abs(out[0] - exact) <= 1e-5 * absum)
+
+
+# --------------------------------------------------------------------------
+# Sampled positions carry the same values as the full run
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo,n", [("ring", 8), ("ring", 5), ("tree", 8)])
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+def test_sampled_positions_match_full(oracle_lib, algo, n, dtype):
+    count = 10_007
+    x = W.random_bits(n, count, dtype, seed=31)
+    g = np.random.Generator(np.random.PCG64(9))
+    pos = np.unique(np.concatenate([g.integers(0, count, 300), [0, count - 1],
+                                    [oracle.chunk_range(count, n, c)[0] for c in range(n)]]))
+    pos = pos[(pos >= 0) & (pos < count)]
+    for op in ["sum", "max"] + (["avg"] if dtype != "i32" else []):
+        with np.errstate(all="ignore"):
+            full, _ = oracle.allreduce(x, algo=algo, op=op, dtype=dtype)
+            part, _ = oracle.allreduce(x[:, pos], algo=algo, op=op, dtype=dtype, count=count, positions=pos)
+        assert _same(part, full[:, pos], dtype)
+
+
+# --------------------------------------------------------------------------
+# DDP buckets
+# --------------------------------------------------------------------------
+
+def greedy_buckets_by_prefix(counts, esize, cap):
+    """Independent formulation of the fill rule: from the current start in the
+    reversed list, a bucket takes the longest run of tensors whose bytes sum
+    to at most the cap (at least one tensor)."""
+    rev = list(range(len(counts)))[::-1]
+    buckets, i = [], 0
+    while i < len(rev):
+        csum = np.cumsum([counts[t] * esize for t in rev[i:]])
+        k = int(np.searchsorted(csum, cap, side="right"))
+        k = max(k, 1)
+        buckets.append(rev[i:i + k])
+        i += k
+    return buckets
+
+
+def test_bucket_plan_gpt2(oracle_lib):
+    counts = W.gpt2_small_counts()
+    assert counts.size == 148 and counts.sum() == 124_439_808
+    bucket_of, offset, bcount = oracle.bucket_plan(counts, dtype="f32", cap_bytes=25 << 20)
+    want = greedy_buckets_by_prefix(counts, 4, 25 << 20)
+    assert len(bcount) == len(want)
+    for b, members in enumerate(want):
+        assert [int(bucket_of[t]) for t in members] == [b] * len(members)
+        off = 0
+        for t in members:  # laid out in reverse registration order
+            assert offset[t] == off
+            off += counts[t]
+        assert bcount[b] == off
+    # by hand: the last block's tail ln_f, then layer 11 from mlp.c_proj.bias back
+    # to attn.c_attn.bias fits (5,318,400 floats); attn.c_attn.weight would overflow
+    assert bcount[0] == 2 * 768 + 768 + 2359296 + 3072 + 2359296 + 2 * 768 + 768 + 589824 + 2304
+    # the embedding table (50257 x 768 floats = 147.2 MiB) sits alone in the last bucket
+    assert bcount[-1] == 50257 * 768 and list(bucket_of).count(len(bcount) - 1) == 1
+    assert np.all(bcount[:-1] * 4 <= 25 << 20)
+
+
+def test_bucket_plan_one_full_bucket(oracle_lib):
+    # 6,553,600 floats are exactly 25 MiB: one bucket, filled to the cap
+    _, _, bcount = oracle.bucket_plan([6_553_600], dtype="f32", cap_bytes=25 << 20)
+    assert bcount.tolist() == [6_553_600]
+    _, _, bcount = oracle.bucket_plan([6_553_600, 1], dtype="f32", cap_bytes=25 << 20)
+    assert bcount.tolist() == [1, 6_553_600]
+    # the same 25 MiB as two tensors still make one full bucket
+    _, _, bcount = oracle.bucket_plan([3_276_800, 3_276_800], dtype="f32", cap_bytes=25 << 20)
+    assert bcount.tolist() == [6_553_600]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_bucket_plan_random(oracle_lib, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    counts = g.integers(0, 5000, size=int(g.integers(1, 60)))
+    counts[g.random(counts.size) < 0.1] = 40000  # oversized
+    cap = 4 * 10000
+    bucket_of, offset, bcount = oracle.bucket_plan(counts, dtype="f32", cap_bytes=cap)
+    want = greedy_buckets_by_prefix(counts, 4, cap)
+    got = [[t for t in range(counts.size)[::-1] if bucket_of[t] == b] for b in range(len(bcount))]
+    assert got == want
+
+
+def test_bucketed_allreduce_equals_per_bucket_collective(oracle_lib):
+    g = np.random.Generator(np.random.PCG64(77))
+    counts = [5, 300, 17, 1024, 3, 999, 64]
+    n = 4
+    grads = [[g.standard_normal(c).astype(np.float32) for c in counts] for _ in range(n)]
+    cap = 4 * 1100
+    out, _ = oracle.bucketed_allreduce(grads, op="avg", dtype="f32", cap_bytes=cap)
+    bucket_of, offset, bcount = oracle.bucket_plan(counts, dtype="f32", cap_bytes=cap)
+    for b in range(len(bcount)):
+        packed = np.zeros((n, bcount[b]), dtype=np.float32)
+        for r in range(n):
+            for t, c in enumerate(counts):
+                if bucket_of[t] == b:
+                    packed[r, offset[t]:offset[t] + c] = grads[r][t]
+        red, _ = oracle.allreduce(packed, op="avg", dtype="f32")
+        for r in range(n):
+            for t, c in enumerate(counts):
+                if bucket_of[t] == b:
+                    assert np.array_equal(out[r][t], red[r, offset[t]:offset[t] + c])
+    # samples carry the same values
+    tid = np.array([0, 1, 1, 3, 6, 5, 2], dtype=np.int32)
+    idx = np.array([4, 0, 299, 512, 63, 0, 16], dtype=np.int64)
+    samp, _ = oracle.bucketed_allreduce(grads, op="avg", dtype="f32", cap_bytes=cap, samples=(tid, idx))
+    for r in range(n):
+        assert np.array_equal(samp[r], [out[r][t][i] for t, i in zip(tid, idx)])
+
+
+def test_bucketed_ddp_average_values(oracle_lib):
+    # every tensor of rank r holds r: the averaged gradients are (N-1)/2 everywhere
+    n = 8
+    counts = [7, 1, 33, 4096]
+    grads = [[np.full(c, r, dtype=np.float32) for c in counts] for r in range(n)]
+    out, _ = oracle.bucketed_allreduce(grads, op="avg", dtype="f32", cap_bytes=4 * 40)
+    for r in range(n):
+        for t in range(len(counts)):
+            assert np.all(out[r][t] == np.float32(3.5))
+
+
+# --------------------------------------------------------------------------
+# Failure detection on the host: a lost message or a departed rank is
+# reported, never waited for
+# --------------------------------------------------------------------------
+
+def test_lost_message_is_detected(oracle_lib):
+    n, count = 4, 16
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="ring", dtype="f32", fault=(1, 2, 1), raise_on_error=False)
+    assert st["rc"] == oracle.ERR_MISSING
+    assert st["fail_step"] == 1 and st["fail_rank"] == 3  # rank 2's successor notices
+
+
+def test_departed_rank_is_detected(oracle_lib):
+    n, count = 8, 64
+    x = np.ones((n, count), dtype=np.float32)
+    for algo in ("ring", "tree"):
+        _, st = oracle.allreduce(x, algo=algo, dtype="f32", fault=(2, 5, 3), raise_on_error=False)
+        assert st["rc"] == oracle.ERR_MISSING and st["fail_step"] == 3, algo
+    _, st = oracle.allreduce(x, algo="ring", dtype="f32", fault=(2, 5, 100), raise_on_error=False)
+    assert st["rc"] == 0  # leaving after the last step harms nobody
