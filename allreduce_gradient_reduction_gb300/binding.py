@@ -1,0 +1,190 @@
+"""Python binding of libar_gb300.so (include/ar.h): argument marshalling only.
+
+Every function takes the same arguments as its C counterpart.  Where the C
+function takes an array of device pointers, this binding accepts a sequence of
+torch CUDA tensors (their data pointers are passed) or plain integers.  Enum
+arguments accept the C value or its lower-case name ("f32", "sum", "ring",
+...).  A stream is a torch.cuda.Stream, an integer cudaStream_t, or None (the
+current torch stream).  Each call returns the C status; ``check()`` raises
+ArError on a non-zero one.
+
+Loading fails loudly: without the compiled library there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libar_gb300.so")
+
+DTYPE = {"f32": 0, "bf16": 1, "i32": 2}
+OP = {"sum": 0, "max": 1, "avg": 2}
+ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3}
+STATUS = {0: "AR_OK", -1: "AR_ERR_INVALID_ARG", -2: "AR_ERR_UNSUPPORTED", -3: "AR_ERR_CUDA",
+          -4: "AR_ERR_TIMEOUT", -5: "AR_ERR_NO_DEVICE", -6: "AR_ERR_TOO_LARGE"}
+AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4
+MAX_RANKS = 64
+DEFAULT_BUCKET_CAP_BYTES = 25 << 20
+
+EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucketed_allreduce",
+           "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
+           "ar_last_cuda_error", "ar_strerror", "ar_version")
+
+
+class ArError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(the CUDA library is required; there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp, cint = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int
+    pp = ctypes.POINTER(vp)
+    L.ar_allreduce.argtypes = [pp, cint, i64, cint, cint, cint, vp]
+    L.ar_reduce_scatter.argtypes = [pp, cint, i64, cint, cint, cint, vp]
+    L.ar_all_gather.argtypes = [pp, cint, i64, cint, cint, vp]
+    L.ar_bucket_plan.argtypes = [ctypes.POINTER(i64), cint, cint, i64, ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                 ctypes.POINTER(i64), ctypes.POINTER(i32)]
+    L.ar_bucketed_allreduce.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, pp, i64, vp]
+    L.ar_chunk_range.argtypes = [i64, cint, cint, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.ar_device_status.argtypes = [vp, ctypes.POINTER(cint)]
+    L.ar_set_barrier_timeout_ns.argtypes = [i64]
+    L.ar_debug_skip_barrier.argtypes = [cint]
+    L.ar_last_cuda_error.argtypes = []
+    L.ar_strerror.argtypes = [cint]
+    L.ar_strerror.restype = ctypes.c_char_p
+    L.ar_version.argtypes = []
+    for name in EXPORTS:
+        if name != "ar_strerror":
+            getattr(L, name).restype = cint
+    return L
+
+
+lib = _load()
+
+
+def _enum(table, v):
+    return table[v] if isinstance(v, str) else int(v)
+
+
+def _ptr(x) -> int:
+    if isinstance(x, int):
+        return x
+    if x is None:
+        return 0
+    return int(x.data_ptr())
+
+
+def _ptr_array(xs):
+    return (ctypes.c_void_p * max(len(xs), 1))(*[_ptr(x) for x in xs])
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _count(bufs, count):
+    if count is not None:
+        return int(count)
+    return int(bufs[0].numel()) if len(bufs) and not isinstance(bufs[0], int) else 0
+
+
+def check(rc: int, what: str = "ar") -> int:
+    if rc != AR_OK:
+        raise ArError(rc, what)
+    return rc
+
+
+def ar_allreduce(bufs, nranks=None, count=None, dtype="f32", op="sum", algo="ring", stream=None) -> int:
+    n = len(bufs) if nranks is None else int(nranks)
+    return lib.ar_allreduce(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), _enum(OP, op),
+                            _enum(ALGO, algo), _stream(stream))
+
+
+def ar_reduce_scatter(bufs, nranks=None, count=None, dtype="f32", op="sum", algo="ring", stream=None) -> int:
+    n = len(bufs) if nranks is None else int(nranks)
+    return lib.ar_reduce_scatter(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), _enum(OP, op),
+                                 _enum(ALGO, algo), _stream(stream))
+
+
+def ar_all_gather(bufs, nranks=None, count=None, dtype="f32", algo="ring", stream=None) -> int:
+    n = len(bufs) if nranks is None else int(nranks)
+    return lib.ar_all_gather(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), _enum(ALGO, algo),
+                             _stream(stream))
+
+
+def ar_bucket_plan(counts, dtype="f32", cap_bytes=DEFAULT_BUCKET_CAP_BYTES):
+    """Returns (status, bucket_of_tensor, offset_in_bucket, bucket_count) as lists."""
+    t = len(counts)
+    c = (ctypes.c_int64 * max(t, 1))(*[int(x) for x in counts])
+    bo = (ctypes.c_int32 * max(t, 1))()
+    off = (ctypes.c_int64 * max(t, 1))()
+    bc = (ctypes.c_int64 * max(t, 1))()
+    nb = ctypes.c_int32()
+    rc = lib.ar_bucket_plan(c, t, _enum(DTYPE, dtype), int(cap_bytes), bo, off, bc, ctypes.byref(nb))
+    return rc, list(bo[:t]), list(off[:t]), list(bc[:nb.value])
+
+
+def ar_bucketed_allreduce(grads, counts=None, ntensors=None, nranks=None, dtype="f32", op="avg", algo="ring",
+                          bucket_cap_bytes=DEFAULT_BUCKET_CAP_BYTES, workspace=None, workspace_bytes=0,
+                          stream=None) -> int:
+    """``grads`` is a list over ranks of lists over tensors (or a flat
+    row-major list with ``ntensors``/``nranks`` given)."""
+    if len(grads) and isinstance(grads[0], (list, tuple)):
+        nr, nt = len(grads), len(grads[0])
+        flat = [g for row in grads for g in row]
+        if counts is None:
+            counts = [int(g.numel()) for g in grads[0]]
+    else:
+        nr, nt, flat = int(nranks), int(ntensors), list(grads)
+    c = (ctypes.c_int64 * max(nt, 1))(*[int(x) for x in counts])
+    ws = _ptr_array(workspace) if workspace is not None else None
+    if workspace is not None and workspace_bytes == 0 and not isinstance(workspace[0], int):
+        workspace_bytes = int(workspace[0].numel() * workspace[0].element_size())
+    return lib.ar_bucketed_allreduce(_ptr_array(flat), c, nt, nr, _enum(DTYPE, dtype), _enum(OP, op),
+                                     _enum(ALGO, algo), int(bucket_cap_bytes), ws, int(workspace_bytes),
+                                     _stream(stream))
+
+
+def ar_chunk_range(count, nranks, c):
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    rc = lib.ar_chunk_range(int(count), int(nranks), int(c), ctypes.byref(lo), ctypes.byref(hi))
+    return rc, lo.value, hi.value
+
+
+def ar_device_status(stream=None):
+    """Returns (status of the call, asynchronous device status)."""
+    st = ctypes.c_int()
+    rc = lib.ar_device_status(_stream(stream), ctypes.byref(st))
+    return rc, st.value
+
+
+def ar_set_barrier_timeout_ns(ns: int) -> int:
+    return lib.ar_set_barrier_timeout_ns(int(ns))
+
+
+def ar_debug_skip_barrier(barrier: int) -> int:
+    return lib.ar_debug_skip_barrier(int(barrier))
+
+
+def ar_last_cuda_error() -> int:
+    return lib.ar_last_cuda_error()
+
+
+def ar_strerror(code: int) -> str:
+    return lib.ar_strerror(int(code)).decode()
+
+
+def ar_version() -> int:
+    return lib.ar_version()

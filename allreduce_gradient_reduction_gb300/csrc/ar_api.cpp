@@ -1,0 +1,491 @@
+// C ABI of the simulated-AllReduce library: argument checks, chunk and bucket
+// planning, descriptor tables, and kernel launches.  Declarations and the
+// contract of every entry point are in include/ar.h.
+#include "../../include/ar.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "ar_internal.h"
+
+namespace {
+
+using ar::Seg;
+using ar::SegTable;
+
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+std::atomic<int64_t> g_timeout_ns{1000000000LL};
+std::atomic<int> g_skip_barrier{-1};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda = e;
+  return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? AR_ERR_NO_DEVICE : AR_ERR_CUDA;
+}
+
+int esize_of(int dtype) { return dtype == AR_BF16 ? 2 : 4; }
+
+bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+// Chunk c of `count` elements split n ways: [floor(c*count/n), floor((c+1)*count/n)).
+int64_t chunk_lo(int64_t count, int n, int c) { return (int64_t)(((__int128)c * count) / n); }
+
+// ---- pointer checks -----------------------------------------------------------
+
+typedef CUresult (*PointerGetAttributeFn)(void*, CUpointer_attribute, CUdeviceptr);
+
+PointerGetAttributeFn pointer_attr_fn() {
+  static PointerGetAttributeFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PointerGetAttributeFn>(p);
+  }();
+  return fn;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+
+// Every range must be non-empty-or-null-free, element aligned, pairwise
+// disjoint, and lie inside device memory of the current device.
+int check_ranges(std::vector<Range>& rs, int esize) {
+  for (const Range& r : rs) {
+    if (r.lo == 0) return AR_ERR_INVALID_ARG;
+    if (r.lo % (uintptr_t)esize) return AR_ERR_INVALID_ARG;
+  }
+  std::sort(rs.begin(), rs.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < rs.size(); ++i)
+    if (rs[i].lo < rs[i - 1].hi || rs[i].lo == rs[i - 1].lo) return AR_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  PointerGetAttributeFn attr = pointer_attr_fn();
+  if (!attr) return cuda_fail(cudaErrorNotSupported);
+  // ranges are sorted: one driver query per allocation they fall into
+  uintptr_t alloc_lo = 0, alloc_hi = 0;
+  for (const Range& r : rs) {
+    if (r.lo >= alloc_lo && r.hi <= alloc_hi && alloc_hi > alloc_lo) continue;
+    unsigned int mtype = 0;
+    int ordinal = -1;
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    if (attr(&mtype, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, (CUdeviceptr)r.lo) != CUDA_SUCCESS) return AR_ERR_INVALID_ARG;
+    if (mtype != CU_MEMORYTYPE_DEVICE) return AR_ERR_INVALID_ARG;
+    if (attr(&ordinal, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL, (CUdeviceptr)r.lo) != CUDA_SUCCESS || ordinal != dev)
+      return AR_ERR_INVALID_ARG;
+    if (attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, (CUdeviceptr)r.lo) != CUDA_SUCCESS ||
+        attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, (CUdeviceptr)r.lo) != CUDA_SUCCESS)
+      return AR_ERR_INVALID_ARG;
+    alloc_lo = (uintptr_t)start;
+    alloc_hi = (uintptr_t)start + size;
+    if (r.hi > alloc_hi) return AR_ERR_INVALID_ARG;
+  }
+  return AR_OK;
+}
+
+int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0) return AR_ERR_INVALID_ARG;
+  if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
+  if (algo < AR_RING || algo > AR_TREE_STEPWISE) return AR_ERR_INVALID_ARG;
+  if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
+  if ((algo == AR_TREE || algo == AR_TREE_STEPWISE) && !is_pow2(nranks)) return AR_ERR_UNSUPPORTED;
+  return AR_OK;
+}
+
+int check_bufs(void* const* bufs, int nranks, int64_t count, int dtype) {
+  if (!bufs) return AR_ERR_INVALID_ARG;
+  std::vector<Range> rs;
+  for (int r = 0; r < nranks; ++r) {
+    uintptr_t p = (uintptr_t)bufs[r];
+    rs.push_back({p, p + (uintptr_t)count * esize_of(dtype)});
+  }
+  return check_ranges(rs, esize_of(dtype));
+}
+
+bool all_aligned16(void* const* p, int n) {
+  for (int i = 0; i < n; ++i)
+    if ((uintptr_t)p[i] % 16) return false;
+  return true;
+}
+
+// ---- per-device barrier block for the step-wise kernels ------------------------
+
+std::mutex g_sync_mu;
+ar::SyncBlock* g_sync[256] = {};
+
+int sync_block(ar::SyncBlock** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 256) return AR_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_sync_mu);
+  if (!g_sync[dev]) {
+    void* p = nullptr;
+    if ((e = cudaMalloc(&p, sizeof(ar::SyncBlock))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemset(p, 0, sizeof(ar::SyncBlock))) != cudaSuccess) {
+      cudaFree(p);
+      return cuda_fail(e);
+    }
+    g_sync[dev] = static_cast<ar::SyncBlock*>(p);
+  }
+  *out = g_sync[dev];
+  return AR_OK;
+}
+
+// ---- one launch over a descriptor table ----------------------------------------
+
+struct Job {
+  int dtype, op, algo, phases;  // phases: 1 RS, 2 AG, 3 both
+  bool avg;
+  bool vec;
+};
+
+int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
+  const int dop = j.op == AR_MAX ? ar::MAX : ar::SUM;
+  const bool stepwise = j.algo == AR_RING_STEPWISE || j.algo == AR_TREE_STEPWISE;
+  const int order = (j.algo == AR_TREE || j.algo == AR_TREE_STEPWISE) ? ar::TREE : ar::RING;
+  cudaError_t e;
+  if (stepwise) {
+    ar::SyncBlock* sb = nullptr;
+    int rc = sync_block(&sb);
+    if (rc) return rc;
+    // counter and abort start at zero for every launch; status stays sticky
+    if ((e = cudaMemsetAsync(sb, 0, 2 * sizeof(int), s)) != cudaSuccess) return cuda_fail(e);
+    ar::StepArgs a;
+    a.tab = tab;
+    a.sync = sb;
+    a.timeout_ns = g_timeout_ns.load();
+    a.order = order;
+    a.phases = j.phases;
+    a.avg = j.avg ? 1 : 0;
+    a.skip_barrier = g_skip_barrier.exchange(-1);
+    a.fn = (float)tab.nranks;
+    e = ar::launch_stepwise(j.dtype, dop, j.vec, a, s);
+  } else if (j.phases == 2) {
+    e = ar::launch_gather(esize_of(j.dtype), j.vec, tab, s);
+  } else {
+    ar::FusedArgs a;
+    a.tab = tab;
+    a.avg = j.avg ? 1 : 0;
+    a.owner_only = j.phases == 1 ? 1 : 0;
+    a.fn = (float)tab.nranks;
+    e = ar::launch_fused(j.dtype, dop, order, j.vec, a, s);
+  }
+  return e == cudaSuccess ? AR_OK : cuda_fail(e);
+}
+
+// Rows (one per tensor: nranks pointers) and their segments, packed into as
+// few descriptor tables as the launch limits allow.
+struct TableBuilder {
+  int nranks;
+  std::vector<const void*> ptrs;  // row-major
+  std::vector<Seg> segs;
+  int add_row(void* const* row_ptrs) {
+    for (int r = 0; r < nranks; ++r) ptrs.push_back(row_ptrs[r]);
+    return (int)(ptrs.size() / nranks) - 1;
+  }
+  void add_seg(int row, int64_t begin, int64_t end, int chunk, int64_t aux = 0) {
+    if (end <= begin) return;
+    Seg s{};
+    s.begin = begin;
+    s.end = end;
+    s.aux = aux;
+    s.tensor = row;
+    s.chunk = chunk;
+    segs.push_back(s);
+  }
+  // Calls fn(table) for consecutive groups of whole rows.
+  template <typename F>
+  int for_each_table(F fn) {
+    const int rows = (int)(ptrs.size() / nranks);
+    const int rows_cap = ar::kPtrCap / nranks;
+    if (rows_cap < 1) return AR_ERR_TOO_LARGE;
+    SegTable t;
+    size_t si = 0;
+    int row0 = 0;
+    while (row0 < rows) {
+      memset(&t, 0, sizeof(t));
+      t.nranks = nranks;
+      int nrow = 0;
+      // take rows while both the pointer and the segment tables have room
+      size_t sj = si;
+      while (row0 + nrow < rows && nrow < rows_cap) {
+        size_t sk = sj;
+        while (sk < segs.size() && segs[sk].tensor == row0 + nrow) ++sk;
+        if ((int)(sk - si) > ar::kSegCap) break;
+        ++nrow;
+        sj = sk;
+      }
+      if (nrow == 0) return AR_ERR_TOO_LARGE;  // one row alone has too many segments
+      for (int r = 0; r < nrow; ++r)
+        for (int k = 0; k < nranks; ++k) t.ptr[r * nranks + k] = ptrs[(size_t)(row0 + r) * nranks + k];
+      t.nseg = (int)(sj - si);
+      for (int k = 0; k < t.nseg; ++k) {
+        t.seg[k] = segs[si + k];
+        t.seg[k].tensor -= row0;
+      }
+      if (t.nseg > 0) {
+        int rc = fn(t);
+        if (rc) return rc;
+      }
+      si = sj;
+      row0 += nrow;
+    }
+    return AR_OK;
+  }
+};
+
+int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases,
+               cudaStream_t stream) {
+  int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
+  if (rc) return rc;
+  if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
+  if (count == 0 || nranks == 1) return AR_OK;
+  TableBuilder tb{nranks, {}, {}};
+  int row = tb.add_row(bufs);
+  for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
+  Job j{dtype, op, algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};
+  return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
+}
+
+int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, int32_t* bucket_of, int64_t* offset,
+                 int64_t* bcount, int32_t* nb) {
+  const int es = esize_of(dtype);
+  int b = -1;
+  int64_t fill = 0;
+  for (int t = ntensors - 1; t >= 0; --t) {
+    if (counts[t] < 0) return AR_ERR_INVALID_ARG;
+    const int64_t bytes = counts[t] * es;
+    if (b < 0 || (fill > 0 && fill + bytes > cap)) {
+      ++b;
+      bcount[b] = 0;
+      fill = 0;
+    }
+    bucket_of[t] = b;
+    offset[t] = bcount[b];
+    bcount[b] += counts[t];
+    fill += bytes;
+  }
+  *nb = b + 1;
+  return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ar_allreduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                 ar_stream_t stream) {
+  return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream);
+}
+
+int ar_reduce_scatter(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                      ar_stream_t stream) {
+  return collective(bufs, nranks, count, dtype, op, algo, 1, (cudaStream_t)stream);
+}
+
+int ar_all_gather(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_algo algo, ar_stream_t stream) {
+  return collective(bufs, nranks, count, dtype, AR_SUM, algo, 2, (cudaStream_t)stream);
+}
+
+int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
+  if (count < 0 || nranks < 1 || c < 0 || c >= nranks || !lo || !hi) return AR_ERR_INVALID_ARG;
+  *lo = chunk_lo(count, nranks, c);
+  *hi = chunk_lo(count, nranks, c + 1);
+  return AR_OK;
+}
+
+int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t cap_bytes, int32_t* bucket_of_tensor,
+                   int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets) {
+  if (ntensors < 0 || cap_bytes <= 0 || dtype < AR_F32 || dtype > AR_I32 || !nbuckets) return AR_ERR_INVALID_ARG;
+  if (ntensors > 0 && (!counts || !bucket_of_tensor || !offset_in_bucket || !bucket_count)) return AR_ERR_INVALID_ARG;
+  return plan_buckets(counts, ntensors, dtype, cap_bytes, bucket_of_tensor, offset_in_bucket, bucket_count, nbuckets);
+}
+
+int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype,
+                          ar_op op, ar_algo algo, int64_t bucket_cap_bytes, void* const* workspace,
+                          int64_t workspace_bytes, ar_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  int rc = check_common(nranks, 0, dtype, op, algo);
+  if (rc) return rc;
+  if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
+  if (ntensors == 0) return AR_OK;
+  if (!grads || !counts) return AR_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  std::vector<int32_t> bucket_of(ntensors);
+  std::vector<int64_t> offset(ntensors), bcount(ntensors);
+  int32_t nb = 0;
+  if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, bucket_of.data(), offset.data(), bcount.data(),
+                         &nb)))
+    return rc;
+  {
+    std::vector<Range> rs;
+    for (int r = 0; r < nranks; ++r)
+      for (int t = 0; t < ntensors; ++t) {
+        if (counts[t] == 0) continue;
+        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+        rs.push_back({p, p + (uintptr_t)counts[t] * es});
+      }
+    if ((rc = check_ranges(rs, es))) return rc;
+  }
+  if (nranks == 1) return AR_OK;
+  const bool avg = op == AR_AVG;
+  // row t of the pointer table: tensor t of every rank
+  std::vector<void*> row(nranks);
+  auto tensor_row = [&](int t) {
+    for (int r = 0; r < nranks; ++r) row[r] = grads[(size_t)r * ntensors + t];
+    return row.data();
+  };
+
+  if (!workspace) {
+    // Fused: every tensor is cut at its bucket's chunk boundaries; each piece
+    // is folded in the order its bucket position implies.
+    TableBuilder tb{nranks, {}, {}};
+    bool vec = true;
+    for (int t = 0; t < ntensors; ++t) {
+      if (counts[t] == 0) continue;
+      void** rp = tensor_row(t);
+      vec = vec && all_aligned16(rp, nranks);
+      const int rw = tb.add_row(rp);
+      const int64_t B = bcount[bucket_of[t]], o = offset[t];
+      for (int c = 0; c < nranks; ++c) {
+        const int64_t lo = std::max(chunk_lo(B, nranks, c), o), hi = std::min(chunk_lo(B, nranks, c + 1), o + counts[t]);
+        tb.add_seg(rw, lo - o, hi - o, c);
+      }
+    }
+    Job j{dtype, op, algo, 3, avg, vec};
+    return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
+  }
+
+  // Literal: pack -> AllReduce the flat buckets -> unpack.
+  int64_t total = 0, largest = 0;
+  std::vector<int64_t> base(nb);
+  for (int b = 0; b < nb; ++b) {
+    base[b] = total;
+    total += bcount[b];
+    largest = std::max(largest, bcount[b]);
+  }
+  if (workspace_bytes < largest * es) return AR_ERR_INVALID_ARG;
+  {
+    std::vector<Range> rs;
+    for (int r = 0; r < nranks; ++r) {
+      uintptr_t p = (uintptr_t)workspace[r];
+      rs.push_back({p, p + (uintptr_t)workspace_bytes});
+    }
+    for (int r = 0; r < nranks; ++r)
+      for (int t = 0; t < ntensors; ++t) {
+        if (counts[t] == 0) continue;
+        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+        rs.push_back({p, p + (uintptr_t)counts[t] * es});
+      }
+    if ((rc = check_ranges(rs, es))) return rc;
+  }
+  const bool whole = workspace_bytes >= total * es;
+  const bool ws_aligned = all_aligned16(workspace, nranks);
+
+  // buckets [b0, b1) at once: pack them, reduce them, unpack them
+  auto run_buckets = [&](int b0, int b1) -> int {
+    const int64_t shift = base[b0];  // packed offset of bucket b0 in the workspace
+    auto copy = [&](int to_packed) -> int {
+      TableBuilder cb{nranks, {}, {}};
+      for (int t = 0; t < ntensors; ++t) {
+        if (counts[t] == 0 || bucket_of[t] < b0 || bucket_of[t] >= b1) continue;
+        void** rp = tensor_row(t);
+        const int64_t aux = base[bucket_of[t]] - shift + offset[t];
+        const bool v = all_aligned16(rp, nranks) && ws_aligned && (aux * es) % 16 == 0;
+        const int rw = cb.add_row(rp);
+        cb.add_seg(rw, 0, counts[t], v ? 1 : 0, aux);
+      }
+      ar::CopyArgs ca;
+      for (int r = 0; r < nranks; ++r) ca.packed[r] = workspace[r];
+      ca.to_packed = to_packed;
+      ca.esize = es;
+      return cb.for_each_table([&](SegTable& t) {
+        ca.tab = t;
+        cudaError_t e = ar::launch_copy(ca, stream);
+        return e == cudaSuccess ? AR_OK : cuda_fail(e);
+      });
+    };
+    auto reduce = [&]() -> int {
+      TableBuilder tb{nranks, {}, {}};
+      bool vec = ws_aligned;
+      std::vector<void*> wrow(nranks);
+      for (int b = b0; b < b1; ++b) {
+        for (int r = 0; r < nranks; ++r) wrow[r] = static_cast<char*>(workspace[r]) + (base[b] - shift) * es;
+        vec = vec && all_aligned16(wrow.data(), nranks);
+        const int rw = tb.add_row(wrow.data());
+        for (int c = 0; c < nranks; ++c)
+          tb.add_seg(rw, chunk_lo(bcount[b], nranks, c), chunk_lo(bcount[b], nranks, c + 1), c);
+      }
+      Job j{dtype, op, algo, 3, avg, vec};
+      return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
+    };
+    int r2 = copy(1);
+    if (!r2) r2 = reduce();
+    if (!r2) r2 = copy(0);
+    return r2;
+  };
+
+  if (whole) return run_buckets(0, nb);
+  for (int b = 0; b < nb; ++b)
+    if ((rc = run_buckets(b, b + 1))) return rc;
+  return AR_OK;
+}
+
+int ar_device_status(ar_stream_t stream, int* status) {
+  if (!status) return AR_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+  *status = AR_OK;
+  ar::SyncBlock* sb = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_sync_mu);
+    if (dev >= 0 && dev < 256) sb = g_sync[dev];
+  }
+  if (!sb) return AR_OK;
+  int v = 0;
+  if ((e = cudaMemcpy(&v, &sb->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemset(&sb->status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+  *status = v;
+  return AR_OK;
+}
+
+int ar_set_barrier_timeout_ns(int64_t ns) {
+  g_timeout_ns.store(ns > 0 ? ns : 1000000000LL);
+  return AR_OK;
+}
+
+int ar_debug_skip_barrier(int barrier) {
+  g_skip_barrier.store(barrier < 0 ? -1 : barrier);
+  return AR_OK;
+}
+
+int ar_last_cuda_error(void) { return (int)g_last_cuda; }
+
+const char* ar_strerror(int status) {
+  switch (status) {
+    case AR_OK: return "AR_OK";
+    case AR_ERR_INVALID_ARG: return "AR_ERR_INVALID_ARG: invalid argument";
+    case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED: unsupported combination";
+    case AR_ERR_CUDA: return "AR_ERR_CUDA: a CUDA call failed";
+    case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a step-wise barrier wait ran out";
+    case AR_ERR_NO_DEVICE: return "AR_ERR_NO_DEVICE: no usable CUDA device";
+    case AR_ERR_TOO_LARGE: return "AR_ERR_TOO_LARGE: descriptor tables too large";
+    default: return "unknown ar_status";
+  }
+}
+
+int ar_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,168 @@
+// Copy kernels (fused AllGather, bucket pack/unpack) and the fused-kernel
+// dispatcher.
+#include "ar_fused.cuh"
+
+namespace ar {
+
+// ---- fused AllGather ---------------------------------------------------------
+// AllGather forwards finished chunks with no arithmetic ("AllReduce" concept
+// page §3; "Allreduce：大模型分布式训练的核心通信算法与优化实践" §2.2 第二阶段):
+// after N-1 forwarding steps every rank holds every owner's chunk bit for bit.
+// One pass: read chunk c of its owner c once, write it to the N-1 others.
+
+constexpr int kGatherUnroll = 4;
+
+template <int ES, bool VECTOR>
+__global__ void __launch_bounds__(kFusedBlock) gather_kernel(const __grid_constant__ SegTable T) {
+  constexpr int VEC = VECTOR ? 16 / ES : 1;
+  constexpr int TILE = kFusedBlock * kGatherUnroll;
+  const int n = T.nranks;
+  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
+    const Seg& s = T.seg[find_seg(T, tile)];
+    const int c = s.chunk;
+    const void* const* P = T.ptr + (size_t)s.tensor * n;
+    const char* src = static_cast<const char*>(P[c]);
+    const int64_t ti = tile - s.tile_begin;
+    if constexpr (VECTOR) {
+      const SegShape sh = seg_shape<VEC>(s);
+      uint4 x[kGatherUnroll];
+      int64_t off[kGatherUnroll];
+      bool ok[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int64_t v = sh.vb + ti * TILE + u * kFusedBlock + threadIdx.x;
+        ok[u] = v < sh.ve;
+        off[u] = v * 16;
+        if (ok[u]) x[u] = ld_stream(src + off[u]);
+      }
+      for (int r = 0; r < n; ++r) {
+        if (r == c) continue;
+        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+#pragma unroll
+        for (int u = 0; u < kGatherUnroll; ++u)
+          if (ok[u]) st_stream(dst + off[u], x[u]);
+      }
+      if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
+        const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
+        const uint32_t v = ld_elem<ES>(src, e);
+        for (int r = 0; r < n; ++r)
+          if (r != c) st_elem<ES>(const_cast<void*>(P[r]), e, v);
+      }
+    } else {
+      const int64_t e = s.begin + ti * TILE + threadIdx.x;
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int64_t eu = e + u * kFusedBlock;
+        if (eu >= s.end) continue;
+        const uint32_t v = ld_elem<ES>(src, eu);
+        for (int r = 0; r < n; ++r)
+          if (r != c) st_elem<ES>(const_cast<void*>(P[r]), eu, v);
+      }
+    }
+  }
+}
+
+template <int ES, bool VECTOR>
+static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
+  if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll) == 0) return cudaSuccess;
+  static const int bps = blocks_per_sm(gather_kernel<ES, VECTOR>, kFusedBlock);
+  const int64_t cap = (int64_t)bps * sm_count();
+  gather_kernel<ES, VECTOR><<<(unsigned)(t.ntiles < cap ? t.ntiles : cap), kFusedBlock, 0, stream>>>(t);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(int esize, bool vec, SegTable& t, cudaStream_t s) {
+  if (esize == 2) return vec ? launch_gather_typed<2, true>(t, s) : launch_gather_typed<2, false>(t, s);
+  return vec ? launch_gather_typed<4, true>(t, s) : launch_gather_typed<4, false>(t, s);
+}
+
+// ---- bucket pack / unpack ----------------------------------------------------
+// The literal DDP path copies every rank's gradients into one flat bucket
+// buffer per rank before the AllReduce and back afterwards ("Allreduce：..."
+// §4.1; "AllReduce 集合通信" §DDP 梯度同步中的地位).  One segment per tensor;
+// seg.aux is the tensor's element offset in the packed buffer; seg.chunk = 1
+// marks a segment whose both sides are 16-byte aligned for every rank.
+
+constexpr int kCopyUnroll = 2;
+
+template <int ES>
+__device__ __forceinline__ void copy_elems(char* dst, const char* src, int64_t e0, int cnt) {
+  for (int i = 0; i < cnt; ++i) st_elem<ES>(dst, e0 + i, ld_elem<ES>(src, e0 + i));
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kFusedBlock) copy_kernel(const __grid_constant__ CopyArgs a) {
+  constexpr int VEC = 16 / ES;
+  constexpr int TILE = kFusedBlock * kCopyUnroll;
+  const SegTable& T = a.tab;
+  const int n = T.nranks;
+  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
+    const Seg& s = T.seg[find_seg(T, tile)];
+    const SegShape sh = seg_shape<VEC>(s);
+    const int64_t ti = tile - s.tile_begin;
+    const bool vec = s.chunk != 0;
+    for (int r = 0; r < n; ++r) {
+      // element e of the tensor sits at element (aux + e) of the packed side
+      const char* tens = static_cast<const char*>(T.ptr[(size_t)s.tensor * n + r]);
+      const char* pack = static_cast<const char*>(a.packed[r]) + s.aux * ES;
+      const char* src = a.to_packed ? tens : pack;
+      char* dst = const_cast<char*>(a.to_packed ? pack : tens);
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t v = sh.vb + ti * TILE + u * kFusedBlock + threadIdx.x;
+        if (v >= sh.ve) continue;
+        if (vec) st_stream(dst + v * 16, ld_stream(src + v * 16));
+        else copy_elems<ES>(dst, src, v * VEC, VEC);
+      }
+      if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
+        const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
+        copy_elems<ES>(dst, src, e, 1);
+      }
+    }
+  }
+}
+
+cudaError_t launch_copy(CopyArgs& a, cudaStream_t stream) {
+  const int es = a.esize;
+  if (fill_tiles(a.tab, 16 / es, (int64_t)kFusedBlock * kCopyUnroll) == 0) return cudaSuccess;
+  if (es == 2) {
+    static const int bps = blocks_per_sm(copy_kernel<2>, kFusedBlock);
+    const int64_t cap = (int64_t)bps * sm_count();
+    copy_kernel<2><<<(unsigned)(a.tab.ntiles < cap ? a.tab.ntiles : cap), kFusedBlock, 0, stream>>>(a);
+  } else {
+    static const int bps = blocks_per_sm(copy_kernel<4>, kFusedBlock);
+    const int64_t cap = (int64_t)bps * sm_count();
+    copy_kernel<4><<<(unsigned)(a.tab.ntiles < cap ? a.tab.ntiles : cap), kFusedBlock, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+// ---- fused dispatch ----------------------------------------------------------
+
+cudaError_t launch_fused_f32_sum(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f32_max(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_bf16_sum(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_bf16_max(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_i32_sum(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_i32_max(int, bool, FusedArgs&, cudaStream_t);
+
+cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& a, cudaStream_t s) {
+  switch (dtype * 2 + op) {
+    case F32 * 2 + SUM: return launch_fused_f32_sum(order, vec, a, s);
+    case F32 * 2 + MAX: return launch_fused_f32_max(order, vec, a, s);
+    case BF16 * 2 + SUM: return launch_fused_bf16_sum(order, vec, a, s);
+    case BF16 * 2 + MAX: return launch_fused_bf16_max(order, vec, a, s);
+    case I32 * 2 + SUM: return launch_fused_i32_sum(order, vec, a, s);
+    case I32 * 2 + MAX: return launch_fused_i32_max(order, vec, a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+  return n;
+}
+
+}  // namespace ar

@@ -1,0 +1,188 @@
+// Device-side building blocks shared by the kernels: the element step for
+// each (dtype, op), 16-byte vector forms of it, streaming loads and stores,
+// and the segment/tile bookkeeping.
+//
+// Element step (the pages ask for sum / max / average; the arithmetic is
+// IEEE): f32 SUM is one binary32 addition rounded to nearest even (compiled
+// without fast-math, so subnormals are kept); bf16 SUM widens both operands to
+// binary32 exactly, adds, and rounds the sum to bf16 nearest-even (the same
+// rounding a step-wise ring applies after every received chunk); i32 SUM wraps;
+// MAX is the IEEE 754-2019 maximum (NaN propagates, +0 > -0).  AVG divides
+// once by N with IEEE binary32 division.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ar_internal.h"
+
+namespace ar {
+
+template <int DT>
+struct ElemSize {
+  static constexpr int value = (DT == BF16) ? 2 : 4;
+};
+
+// ---- one 32-bit word: 1 f32, 2 bf16 or 1 i32 -------------------------------
+
+__device__ __forceinline__ bool f32_nan(uint32_t u) { return (u & 0x7FFFFFFFu) > 0x7F800000u; }
+
+__device__ __forceinline__ uint32_t f32_max_bits(uint32_t a, uint32_t b) {
+  const float fa = __uint_as_float(a), fb = __uint_as_float(b);
+  if (f32_nan(a) || f32_nan(b)) return 0x7FC00000u;
+  if (fa > fb) return a;
+  if (fb > fa) return b;
+  return a & b;  // equal values: only +0 / -0 differ, and +0 wins
+}
+
+__device__ __forceinline__ uint32_t bf16_half_max(uint32_t a, uint32_t b) {  // a, b: bf16 bits in the low half
+  const uint32_t fa = a << 16, fb = b << 16;
+  if (f32_nan(fa) || f32_nan(fb)) return 0x7FC0u;
+  const float xa = __uint_as_float(fa), xb = __uint_as_float(fb);
+  if (xa > xb) return a;
+  if (xb > xa) return b;
+  return a & b;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);  // .x (low 16 bits) = lo
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+template <int DT, int OP>
+__device__ __forceinline__ uint32_t step_word(uint32_t a, uint32_t b) {
+  if constexpr (DT == F32) {
+    if constexpr (OP == SUM) return __float_as_uint(__fadd_rn(__uint_as_float(a), __uint_as_float(b)));
+    else return f32_max_bits(a, b);
+  } else if constexpr (DT == BF16) {
+    if constexpr (OP == SUM) {
+      const float a0 = __uint_as_float(a << 16), a1 = __uint_as_float(a & 0xFFFF0000u);
+      const float b0 = __uint_as_float(b << 16), b1 = __uint_as_float(b & 0xFFFF0000u);
+      return pack_bf16x2_rn(__fadd_rn(a0, b0), __fadd_rn(a1, b1));
+    } else {
+      return bf16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (bf16_half_max(a >> 16, b >> 16) << 16);
+    }
+  } else {
+    if constexpr (OP == SUM) return a + b;  // two's-complement wrap-around
+    else return (uint32_t)max((int32_t)a, (int32_t)b);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t div_word(uint32_t a, float fn) {
+  if constexpr (DT == F32) {
+    return __float_as_uint(__fdiv_rn(__uint_as_float(a), fn));
+  } else if constexpr (DT == BF16) {
+    return pack_bf16x2_rn(__fdiv_rn(__uint_as_float(a << 16), fn), __fdiv_rn(__uint_as_float(a & 0xFFFF0000u), fn));
+  } else {
+    return a;
+  }
+}
+
+// ---- 16-byte vectors --------------------------------------------------------
+
+template <int DT, int OP>
+__device__ __forceinline__ uint4 step_vec(const uint4& a, const uint4& b) {
+  return make_uint4(step_word<DT, OP>(a.x, b.x), step_word<DT, OP>(a.y, b.y), step_word<DT, OP>(a.z, b.z),
+                    step_word<DT, OP>(a.w, b.w));
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 div_vec(const uint4& a, float fn) {
+  return make_uint4(div_word<DT>(a.x, fn), div_word<DT>(a.y, fn), div_word<DT>(a.z, fn), div_word<DT>(a.w, fn));
+}
+
+// Streaming accesses: every byte is touched once, so keep it out of L1 and
+// mark it first in line for L2 eviction.
+__device__ __forceinline__ uint4 ld_stream(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+// L2-coherent accesses for kernels whose phases read what other blocks wrote.
+__device__ __forceinline__ uint4 ld_l2(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void st_l2(void* p, const uint4& v) { __stcg(reinterpret_cast<uint4*>(p), v); }
+
+// ---- single elements --------------------------------------------------------
+
+template <int ES>
+__device__ __forceinline__ uint32_t ld_elem(const void* base, int64_t e) {
+  if constexpr (ES == 2) return __ldcg(reinterpret_cast<const unsigned short*>(base) + e);
+  else return __ldcg(reinterpret_cast<const unsigned int*>(base) + e);
+}
+
+template <int ES>
+__device__ __forceinline__ void st_elem(void* base, int64_t e, uint32_t v) {
+  if constexpr (ES == 2) __stcg(reinterpret_cast<unsigned short*>(base) + e, (unsigned short)v);
+  else __stcg(reinterpret_cast<unsigned int*>(base) + e, v);
+}
+
+// ---- segments and tiles -----------------------------------------------------
+
+// Index of the segment holding `tile`: the last segment whose tile_begin is <= tile.
+__device__ __forceinline__ int find_seg(const SegTable& t, int64_t tile) {
+  int lo = 0, hi = t.nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.seg[mid].tile_begin <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Full 16-byte vectors of a segment: [vb, ve) in units of VEC elements.
+// Elements outside them (at most VEC-1 on each side) are "scalars": with
+// ve > vb they are [begin, vb*VEC) and [ve*VEC, end); otherwise all of
+// [begin, end).
+struct SegShape {
+  int64_t vb, ve;
+  int head, tail;  // scalar counts before / after the vectors
+};
+
+template <int VEC>
+__device__ __forceinline__ SegShape seg_shape(const Seg& s) {
+  SegShape r;
+  r.vb = (s.begin + VEC - 1) / VEC;
+  r.ve = s.end / VEC;
+  if (r.ve > r.vb) {
+    r.head = (int)(r.vb * VEC - s.begin);
+    r.tail = (int)(s.end - r.ve * VEC);
+  } else {
+    r.ve = r.vb;
+    r.head = (int)(s.end - s.begin);
+    r.tail = 0;
+  }
+  return r;
+}
+
+// Element index of scalar k (0 <= k < head + tail) of a segment.
+template <int VEC>
+__device__ __forceinline__ int64_t scalar_elem(const Seg& s, const SegShape& sh, int k) {
+  return k < sh.head ? s.begin + k : sh.ve * VEC + (k - sh.head);
+}
+
+__device__ __forceinline__ int rot(int k, int n) { return k >= n ? k - n : k; }
+
+// ---- scalar folds (runtime N) -----------------------------------------------
+
+// Ring order for element e of chunk c: x[c+1], x[c+2], ..., x[c].
+template <int DT, int OP>
+__device__ uint32_t fold_ring_scalar(const void* const* P, int n, int c, int64_t e) {
+  constexpr int ES = ElemSize<DT>::value;
+  uint32_t acc = ld_elem<ES>(P[rot(c + 1, n)], e);
+  for (int p = 1; p < n; ++p) acc = step_word<DT, OP>(acc, ld_elem<ES>(P[rot(c + 1 + p, n)], e));
+  return acc;
+}
+
+// Balanced pairwise tree over ranks 0..n-1 (n a power of two), lower first.
+template <int DT, int OP>
+__device__ uint32_t fold_tree_scalar(const void* const* P, int n, int64_t e) {
+  constexpr int ES = ElemSize<DT>::value;
+  uint32_t stack[8];
+  int top = 0;
+  for (int r = 0; r < n; ++r) {
+    uint32_t v = ld_elem<ES>(P[r], e);
+    for (int k = r; k & 1; k >>= 1) v = step_word<DT, OP>(stack[--top], v);
+    stack[top++] = v;
+  }
+  return stack[0];
+}
+
+}  // namespace ar

@@ -1,0 +1,275 @@
+// Fused single-pass AllReduce / ReduceScatter kernels.
+//
+// One pass over HBM: each thread owns 16-byte vectors of one segment (a run
+// of elements inside one chunk c), loads the N rank vectors at that position,
+// folds them in the order the schedule would -- ring: x[c+1], x[c+2], ...,
+// x[c] around the ring ("Allreduce：大模型分布式训练的核心通信算法与优化实践"
+// §2.2, "AllReduce 集合通信" §两阶段流程); tree: the balanced pairwise tree
+// (0,1), (2,3), ... ("【AI Infra小白入门⑩】集合通信基础" §四 4.1) -- rounding
+// to the storage type after every step, optionally divides by N (DDP's
+// average, same tutorial §3.1), and stores the finished vector to every rank
+// (AllReduce) or to the chunk owner only (ReduceScatter).  Every element is
+// read once per rank and written once per destination: 2*N*D*b bytes for an
+// AllReduce of D elements of b bytes, the minimum.
+//
+// The fold is per element, so the result is bit-identical to the step-wise
+// schedule (ReduceScatter's N-1 accumulate steps then AllGather's N-1 copies)
+// regardless of how elements are spread over threads.  A thread reads all N
+// values of a vector before it writes any, so working in place is safe.
+#pragma once
+
+#include "ar_device.cuh"
+
+namespace ar {
+
+constexpr int kFusedBlock = 256;
+
+// 16-byte vectors per thread per tile: enough loads in flight to cover HBM
+// latency without spilling (N rank vectors per position).
+__host__ __device__ constexpr int fused_unroll(int order, int nr) {
+  return order == TREE ? (nr <= 4 ? 4 : (nr <= 8 ? 2 : 1)) : (nr == 0 ? 2 : (nr <= 4 ? 4 : 2));
+}
+
+template <int DT, int OP, int NR>
+__device__ __forceinline__ uint4 tree_fold_regs(uint4 (&x)[NR]) {
+#pragma unroll
+  for (int w = 1; w < NR; w <<= 1)
+#pragma unroll
+    for (int i = 0; i < NR; i += 2 * w) x[i] = step_vec<DT, OP>(x[i], x[i + w]);
+  return x[0];
+}
+
+template <int DT, int OP, int ORDER, int NR>
+__global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
+  constexpr int ES = ElemSize<DT>::value;
+  constexpr int VEC = 16 / ES;
+  constexpr int U = fused_unroll(ORDER, NR);
+  constexpr int TILE_V = kFusedBlock * U;
+  const SegTable& T = a.tab;
+  const int n = NR > 0 ? NR : T.nranks;
+
+  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
+    const Seg& s = T.seg[find_seg(T, tile)];
+    const SegShape sh = seg_shape<VEC>(s);
+    const int64_t ti = tile - s.tile_begin;
+    const void* const* P = T.ptr + (size_t)s.tensor * n;
+    const int c = s.chunk;
+
+    int64_t off[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = sh.vb + ti * TILE_V + u * kFusedBlock + threadIdx.x;
+      ok[u] = v < sh.ve;
+      off[u] = v * 16;
+    }
+
+    uint4 acc[U];
+    if constexpr (ORDER == RING && NR > 0) {
+      const char* src[NR];
+#pragma unroll
+      for (int p = 0; p < NR; ++p) src[p] = static_cast<const char*>(P[rot(c + 1 + p, NR)]);
+      uint4 x[U][NR];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int p = 0; p < NR; ++p)
+          if (ok[u]) x[u][p] = ld_stream(src[p] + off[u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        acc[u] = x[u][0];
+#pragma unroll
+        for (int p = 1; p < NR; ++p) acc[u] = step_vec<DT, OP>(acc[u], x[u][p]);
+      }
+    } else if constexpr (ORDER == RING) {
+      // any N: groups of 8 ranks in ring order, folded as they arrive
+      for (int g = 0; g < n; g += 8) {
+        uint4 x[U][8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < n) {
+            const char* src = static_cast<const char*>(P[rot(c + 1 + g + q, n)]);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (ok[u]) x[u][q] = ld_stream(src + off[u]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < n) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] = (g + q == 0) ? x[u][q] : step_vec<DT, OP>(acc[u], x[u][q]);
+          }
+        }
+      }
+    } else if constexpr (NR <= 8) {
+      uint4 x[U][NR];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int p = 0; p < NR; ++p)
+          if (ok[u]) x[u][p] = ld_stream(static_cast<const char*>(P[p]) + off[u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = tree_fold_regs<DT, OP, NR>(x[u]);
+    } else {
+      // N = 16, 32, 64: aligned subtrees of 8 ranks, then a tree over them
+      static_assert(U == 1, "one vector per thread for wide trees");
+      uint4 part[NR / 8];
+#pragma unroll
+      for (int g = 0; g < NR / 8; ++g) {
+        uint4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (ok[0]) x[q] = ld_stream(static_cast<const char*>(P[g * 8 + q]) + off[0]);
+        part[g] = tree_fold_regs<DT, OP, 8>(x);
+      }
+      acc[0] = tree_fold_regs<DT, OP, NR / 8>(part);
+    }
+
+    if (a.avg) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = div_vec<DT>(acc[u], a.fn);
+    }
+    if (a.owner_only) {
+      char* dst = static_cast<char*>(const_cast<void*>(P[c]));
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ok[u]) st_stream(dst + off[u], acc[u]);
+    } else if constexpr (NR > 0) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) st_stream(dst + off[u], acc[u]);
+      }
+    } else {
+      for (int r = 0; r < n; ++r) {
+        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) st_stream(dst + off[u], acc[u]);
+      }
+    }
+
+    // elements of the segment outside its full vectors
+    if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
+      const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
+      uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, c, e) : fold_tree_scalar<DT, OP>(P, n, e);
+      if (a.avg) r = div_word<DT>(r, a.fn);
+      if (a.owner_only) {
+        st_elem<ES>(const_cast<void*>(P[c]), e, r);
+      } else {
+        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+      }
+    }
+  }
+}
+
+// Same computation one element per thread, for buffers that are not all
+// 16-byte aligned.
+template <int DT, int OP, int ORDER>
+__global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_constant__ FusedArgs a) {
+  constexpr int ES = ElemSize<DT>::value;
+  const SegTable& T = a.tab;
+  const int n = T.nranks;
+  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
+    const Seg& s = T.seg[find_seg(T, tile)];
+    const int64_t e = s.begin + (tile - s.tile_begin) * kFusedBlock + threadIdx.x;
+    if (e >= s.end) continue;
+    const void* const* P = T.ptr + (size_t)s.tensor * n;
+    uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, s.chunk, e) : fold_tree_scalar<DT, OP>(P, n, e);
+    if (a.avg) r = div_word<DT>(r, a.fn);
+    if (a.owner_only) {
+      st_elem<ES>(const_cast<void*>(P[s.chunk]), e, r);
+    } else {
+      for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+    }
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+// Tiles of `tile_elems` vectors (or elements) per segment; a segment with
+// leftover scalars but no full vector still gets one tile.
+inline int64_t fill_tiles(SegTable& t, int vec, int64_t tile_units) {
+  int64_t acc = 0;
+  for (int i = 0; i < t.nseg; ++i) {
+    Seg& s = t.seg[i];
+    s.tile_begin = acc;
+    int64_t units, extra;
+    if (vec > 1) {
+      int64_t vb = (s.begin + vec - 1) / vec, ve = s.end / vec;
+      if (ve < vb) ve = vb;
+      units = ve - vb;
+      extra = (s.end - s.begin) - units * vec;
+    } else {
+      units = s.end - s.begin;
+      extra = 0;
+    }
+    int64_t tiles = (units + tile_units - 1) / tile_units;
+    if (tiles == 0 && extra > 0) tiles = 1;
+    acc += tiles;
+  }
+  t.ntiles = acc;
+  return acc;
+}
+
+template <typename K>
+inline int blocks_per_sm(K kernel, int block) {
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, 0) != cudaSuccess || b < 1) b = 1;
+  return b;
+}
+
+template <int DT, int OP, int ORDER, int NR>
+cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
+  constexpr int U = fused_unroll(ORDER, NR);
+  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U) == 0) return cudaSuccess;
+  static const int bps = blocks_per_sm(fused_vec_kernel<DT, OP, ORDER, NR>, kFusedBlock);
+  const int64_t grid = a.tab.ntiles < (int64_t)bps * sm_count() ? a.tab.ntiles : (int64_t)bps * sm_count();
+  fused_vec_kernel<DT, OP, ORDER, NR><<<(unsigned)grid, kFusedBlock, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT, int OP, int ORDER>
+cudaError_t launch_fused_scalar(FusedArgs& a, cudaStream_t stream) {
+  if (fill_tiles(a.tab, 1, kFusedBlock) == 0) return cudaSuccess;
+  static const int bps = blocks_per_sm(fused_scalar_kernel<DT, OP, ORDER>, kFusedBlock);
+  const int64_t grid = a.tab.ntiles < (int64_t)bps * sm_count() ? a.tab.ntiles : (int64_t)bps * sm_count();
+  fused_scalar_kernel<DT, OP, ORDER><<<(unsigned)grid, kFusedBlock, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// Dispatch on order and rank count for one (dtype, op).
+template <int DT, int OP>
+cudaError_t launch_fused_typed(int order, bool vec, FusedArgs& a, cudaStream_t stream) {
+  const int n = a.tab.nranks;
+  if (!vec) return order == RING ? launch_fused_scalar<DT, OP, RING>(a, stream) : launch_fused_scalar<DT, OP, TREE>(a, stream);
+  if (order == RING) {
+    switch (n) {
+      case 2: return launch_fused_vec<DT, OP, RING, 2>(a, stream);
+      case 4: return launch_fused_vec<DT, OP, RING, 4>(a, stream);
+      case 8: return launch_fused_vec<DT, OP, RING, 8>(a, stream);
+      default: return launch_fused_vec<DT, OP, RING, 0>(a, stream);
+    }
+  }
+  switch (n) {
+    case 2: return launch_fused_vec<DT, OP, TREE, 2>(a, stream);
+    case 4: return launch_fused_vec<DT, OP, TREE, 4>(a, stream);
+    case 8: return launch_fused_vec<DT, OP, TREE, 8>(a, stream);
+    case 16: return launch_fused_vec<DT, OP, TREE, 16>(a, stream);
+    case 32: return launch_fused_vec<DT, OP, TREE, 32>(a, stream);
+    case 64: return launch_fused_vec<DT, OP, TREE, 64>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ar
+
+#define AR_DEFINE_FUSED(NAME, DT, OP)                                                              \
+  namespace ar {                                                                                  \
+  cudaError_t NAME(int order, bool vec, FusedArgs& a, cudaStream_t s) {                           \
+    return launch_fused_typed<DT, OP>(order, vec, a, s);                                          \
+  }                                                                                               \
+  }

@@ -1,0 +1,80 @@
+// Internal interface between the C-ABI layer (ar_api.cpp) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ar {
+
+enum Dtype { F32 = 0, BF16 = 1, I32 = 2 };
+enum Op { SUM = 0, MAX = 1 };  // AVG = SUM plus the `avg` flag
+enum Order { RING = 0, TREE = 1 };
+
+constexpr int kMaxRanks = 64;
+constexpr int kPtrCap = 512;  // pointers one launch can describe
+constexpr int kSegCap = 256;  // segments one launch can describe
+
+// A run of elements of one "tensor" (a row of nranks buffers) that lies in a
+// single chunk, so every element of it is reduced in the same rank order.
+struct Seg {
+  int64_t begin;       // first element, relative to the tensor's base pointers
+  int64_t end;         // one past the last element
+  int64_t tile_begin;  // first tile of this segment (filled by the launcher)
+  int64_t aux;         // copy kernels: element offset on the packed side
+  int32_t tensor;      // row in the pointer table: ptr[tensor * nranks + rank]
+  int32_t chunk;       // chunk id c (ring order starts at rank c+1); copy kernels: 1 = vectorisable
+};
+
+struct SegTable {
+  const void* ptr[kPtrCap];
+  Seg seg[kSegCap];
+  int32_t nranks;
+  int32_t nseg;
+  int64_t ntiles;
+};
+
+// Per-device block used by the step-wise kernels' grid barrier.
+struct SyncBlock {
+  unsigned int counter;  // arrivals; reset before each launch
+  int abort;             // set by the first block that gives up; reset before each launch
+  int status;            // sticky: AR_ERR_TIMEOUT until read by ar_device_status
+  int pad;
+};
+
+struct FusedArgs {
+  SegTable tab;
+  int32_t avg;         // divide reduced values by nranks
+  int32_t owner_only;  // ReduceScatter: store to the chunk owner only
+  float fn;            // (float)nranks
+};
+
+struct StepArgs {
+  SegTable tab;
+  SyncBlock* sync;
+  int64_t timeout_ns;
+  int32_t order;      // RING or TREE
+  int32_t phases;     // bit 0 ReduceScatter, bit 1 AllGather
+  int32_t avg;
+  int32_t skip_barrier;  // test hook, -1 = off
+  float fn;
+};
+
+struct CopyArgs {
+  SegTable tab;                  // ptr[tensor * nranks + r] = tensor side
+  const void* packed[kMaxRanks]; // packed side base per rank; seg.aux = element offset there
+  int32_t to_packed;             // 1 = pack (tensor -> packed), 0 = unpack
+  int32_t esize;
+};
+
+// Launchers.  Each fills tab.seg[*].tile_begin and tab.ntiles for its own
+// tile shape, then enqueues on `stream`.  `vec` selects the 16-byte path
+// (every pointer 16-byte aligned); otherwise one element per thread.
+cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& args, cudaStream_t stream);
+cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t stream);
+cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
+cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
+
+int sm_count();
+
+}  // namespace ar

@@ -1,0 +1,181 @@
+// Step-wise kernels: the literal communication schedule, one grid-wide phase
+// per step, in one persistent cooperative kernel.
+//
+// Ring ("Allreduce：大模型分布式训练的核心通信算法与优化实践" §2.2; "AllReduce 集合
+// 通信" §两阶段流程): ReduceScatter step s (s = 0..N-2): rank r sends chunk
+// (r-1-s) mod N to rank r+1, which folds it into its own copy,
+// own = step(received, own) -- so chunk j moves from rank j+1+s to j+2+s.
+// AllGather step s: rank r forwards chunk (r-s) mod N to r+1 unchanged.
+// Tree ("【AI Infra小白入门⑩】集合通信基础" §四 4.1): recursive halving, step k
+// (distance h = 2^k, k = 0 first) pairs rank r with r XOR h; rank r keeps the
+// chunks j = r (mod 2h) and folds lower rank first; then recursive doubling in
+// reverse order copies the halves back.  AVG divides at the owner after the
+// last ReduceScatter step.
+//
+// "Sending" chunk j from rank a to rank b is rank b's threads reading rank
+// a's buffer in HBM: one GPU holds all ranks.  Within a phase no location is
+// both read as a source and written, so a phase needs no intra-phase ordering;
+// between phases a bounded grid barrier orders everything.  Loads and stores
+// go through L2 (.cg), the coherence point for data other blocks wrote.
+#pragma once
+
+#include "ar_device.cuh"
+
+namespace ar {
+
+constexpr int kStepBlock = 256;
+constexpr int kStepUnroll = 2;
+constexpr unsigned kMaxSpin = 1u << 23;  // backstop if the global timer misbehaves
+constexpr int kTimeoutStatus = -4;       // AR_ERR_TIMEOUT
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier with a bounded wait.  Returns false when the kernel must
+// stop: this block timed out (it then raises `abort` for the others and
+// records AR_ERR_TIMEOUT in the sticky status) or another block already did.
+__device__ bool grid_barrier(SyncBlock* sb, unsigned target, bool arrive, int64_t timeout_ns) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();
+    if (arrive) atomicAdd(&sb->counter, 1u);
+    const uint64_t t0 = global_ns();
+    unsigned spins = 0;
+    while (ld_acquire_u32(&sb->counter) < target) {
+      if (ld_relaxed_s32(&sb->abort)) {
+        ok = 0;
+        break;
+      }
+      if (++spins > kMaxSpin || global_ns() - t0 > (uint64_t)timeout_ns) {
+        atomicExch(&sb->abort, 1);
+        atomicCAS(&sb->status, 0, kTimeoutStatus);
+        ok = 0;
+        break;
+      }
+      __nanosleep(128);
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__device__ __forceinline__ int ilog2(int n) { return 31 - __clz(n); }
+
+template <int DT, int OP, bool VECTOR>
+__global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_constant__ StepArgs a) {
+  constexpr int ES = ElemSize<DT>::value;
+  constexpr int VEC = VECTOR ? 16 / ES : 1;
+  constexpr int TILE = kStepBlock * kStepUnroll;
+  const SegTable& T = a.tab;
+  const int n = T.nranks;
+  const bool ring = a.order == RING;
+  const int L = ring ? 0 : ilog2(n);
+  const int n_rs = (a.phases & 1) ? (ring ? n - 1 : L) : 0;
+  const int n_ag = (a.phases & 2) ? (ring ? n - 1 : L) : 0;
+  const int Q = n_rs + n_ag;
+
+  for (int q = 0; q < Q; ++q) {
+    const bool rs = q < n_rs;
+    const int s = rs ? q : q - n_rs;     // step within its half
+    const int k = rs ? s : L - 1 - s;    // tree distance exponent
+    const int h = 1 << k;
+    const int inst = ring ? 1 : (n >> (k + 1));  // rank pairs per chunk in a tree step
+    const bool avg = a.avg && rs && s == n_rs - 1;
+    const int64_t total = (int64_t)inst * T.ntiles;
+
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+      const int m = (int)(w / T.ntiles);
+      const int64_t tile = w - (int64_t)m * T.ntiles;
+      const Seg& sg = T.seg[find_seg(T, tile)];
+      const int j = sg.chunk;
+      int src, dst;
+      if (ring) {
+        src = rs ? (j + 1 + s) % n : (j + s) % n;
+        dst = src + 1 == n ? 0 : src + 1;
+      } else {
+        dst = rs ? ((j & (2 * h - 1)) + m * 2 * h) : (((j ^ h) & (2 * h - 1)) + m * 2 * h);
+        src = dst ^ h;
+      }
+      const bool src_first = ring || src < dst;  // ring: received first; tree: lower rank first
+      const void* const* P = T.ptr + (size_t)sg.tensor * n;
+      const char* ps = static_cast<const char*>(P[src]);
+      char* pd = static_cast<char*>(const_cast<void*>(P[dst]));
+      const int64_t ti = tile - sg.tile_begin;
+
+      if constexpr (VECTOR) {
+        const SegShape sh = seg_shape<VEC>(sg);
+        uint4 xs[kStepUnroll], xd[kStepUnroll];
+        int64_t off[kStepUnroll];
+        bool ok[kStepUnroll];
+#pragma unroll
+        for (int u = 0; u < kStepUnroll; ++u) {
+          const int64_t v = sh.vb + ti * TILE + u * kStepBlock + threadIdx.x;
+          ok[u] = v < sh.ve;
+          off[u] = v * 16;
+          if (ok[u]) {
+            xs[u] = ld_l2(ps + off[u]);
+            if (rs) xd[u] = ld_l2(pd + off[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kStepUnroll; ++u) {
+          if (!ok[u]) continue;
+          uint4 r = xs[u];
+          if (rs) {
+            r = src_first ? step_vec<DT, OP>(xs[u], xd[u]) : step_vec<DT, OP>(xd[u], xs[u]);
+            if (avg) r = div_vec<DT>(r, a.fn);
+          }
+          st_l2(pd + off[u], r);
+        }
+        if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
+          const int64_t e = scalar_elem<VEC>(sg, sh, threadIdx.x);
+          uint32_t r = ld_elem<ES>(ps, e);
+          if (rs) {
+            const uint32_t d = ld_elem<ES>(pd, e);
+            r = src_first ? step_word<DT, OP>(r, d) : step_word<DT, OP>(d, r);
+            if (avg) r = div_word<DT>(r, a.fn);
+          }
+          st_elem<ES>(pd, e, r);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kStepUnroll; ++u) {
+          const int64_t e = sg.begin + ti * TILE + u * kStepBlock + threadIdx.x;
+          if (e >= sg.end) continue;
+          uint32_t r = ld_elem<ES>(ps, e);
+          if (rs) {
+            const uint32_t d = ld_elem<ES>(pd, e);
+            r = src_first ? step_word<DT, OP>(r, d) : step_word<DT, OP>(d, r);
+            if (avg) r = div_word<DT>(r, a.fn);
+          }
+          st_elem<ES>(pd, e, r);
+        }
+      }
+    }
+    if (q + 1 < Q) {
+      const bool arrive = !(blockIdx.x == 0 && q == a.skip_barrier);
+      if (!grid_barrier(a.sync, (unsigned)(q + 1) * gridDim.x, arrive, a.timeout_ns)) return;
+    }
+  }
+}
+
+}  // namespace ar

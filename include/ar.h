@@ -1,0 +1,205 @@
+/*
+ * ar.h -- simulated AllReduce on one GB300 (sm_103a).
+ *
+ * C ABI of the library libar_gb300.so.  N "ranks" are N equal-length buffers
+ * resident in one GPU's HBM; a collective combines them element by element
+ * with SUM, MAX or AVG (SUM, then divide by N) and leaves the result in every
+ * buffer, exactly as the data-parallel gradient AllReduce leaves the same
+ * reduced gradient on every process.
+ *
+ * Sources for the operations (page title, section):
+ *   [concept]  "AllReduce" (concept page), §3 技术原理 and §4 关键参数
+ *   [tutorial] "Allreduce：大模型分布式训练的核心通信算法与优化实践", §2.2, §3.1-3.2,
+ *              §4.1, §4.4
+ *   [chapter]  "AllReduce算法详解：Ring AllReduce原理，Tree AllReduce原理，性能对比与
+ *              选择", §4.2-4.3
+ *   [notes]    "AllReduce 集合通信", §语义, §两阶段流程, §通信量推导, §DDP 梯度同步中的地位
+ *   [primer]   "【AI Infra小白入门⑩】集合通信基础：AllReduce、Ring算法与NCCL全解析",
+ *              §二, §三, §四 4.1
+ *
+ * Common conventions
+ *   - Every function returns AR_OK (0) or a negative ar_status; none throws,
+ *     none keeps a pointer after it returns, none allocates caller-visible
+ *     memory.  Work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and the call returns once it is enqueued; the
+ *     results are valid when the stream reaches that point.
+ *   - Buffers are device pointers of the current CUDA device, one per rank,
+ *     each holding `count` elements of `dtype`, pairwise distinct and
+ *     non-overlapping (checked; AR_ERR_INVALID_ARG otherwise).  They must be
+ *     aligned to the element size; 16-byte alignment of all of them enables
+ *     the vectorised kernels, any other alignment takes a slower scalar path.
+ *   - 1 <= nranks <= AR_MAX_RANKS; count >= 0; count == 0 and nranks == 1 do
+ *     nothing (a single rank already holds the reduction; AVG divides by 1).
+ *   - Chunks: each rank buffer is split into N contiguous chunks,
+ *     chunk c = [floor(c*count/N), floor((c+1)*count/N)); rank c owns chunk c
+ *     after ReduceScatter.  [concept §3], [tutorial §2.2], [notes §两阶段流程].
+ *   - Element step: f32 is IEEE binary32 addition (round to nearest even,
+ *     subnormals kept); bf16 is exact widening to binary32, addition, and
+ *     rounding to nearest even back to bf16 after every step; i32 adds with
+ *     two's-complement wrap-around; MAX is IEEE 754-2019 maximum (NaN
+ *     propagates, +0 > -0).  AVG is SUM followed by one IEEE binary32 division
+ *     by N of each reduced element (for bf16 the quotient is rounded to bf16);
+ *     AVG on i32 is AR_ERR_UNSUPPORTED.  NaN results carry no payload
+ *     guarantee.
+ *   - Orders (bit-exact with a step-wise execution of the same schedule):
+ *       AR_RING / AR_RING_STEPWISE: chunk c is folded in ring order
+ *         x[c+1], x[c+2], ..., x[c+N-1], x[c] (indices mod N), one rounding per
+ *         step -- the order in which ReduceScatter carries chunk c around the
+ *         ring.  [tutorial §2.2], [notes §两阶段流程], [primer §三 3.1].
+ *       AR_TREE / AR_TREE_STEPWISE: balanced pairwise tree over rank indices,
+ *         (x0 (+) x1), (x2 (+) x3), ... then pairs of pairs, lower ranks first;
+ *         N must be a power of two (AR_ERR_UNSUPPORTED otherwise).
+ *         [primer §四 4.1], [chapter §4.3].
+ *     The fused algorithms make one pass over HBM (each element of each rank
+ *     read once and written once); the step-wise ones execute the literal
+ *     schedule, one grid-wide phase per communication step, in a single
+ *     persistent cooperative kernel.
+ */
+#ifndef AR_GB300_H
+#define AR_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st* ar_stream_t;
+
+#define AR_MAX_RANKS 64
+#define AR_DEFAULT_BUCKET_CAP_BYTES (25LL << 20) /* DDP's 25 MB bucket [tutorial §4.1] */
+
+typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2 } ar_dtype;
+typedef enum { AR_SUM = 0, AR_MAX = 1, AR_AVG = 2 } ar_op;
+typedef enum { AR_RING = 0, AR_RING_STEPWISE = 1, AR_TREE = 2, AR_TREE_STEPWISE = 3 } ar_algo;
+
+typedef enum {
+  AR_OK = 0,
+  AR_ERR_INVALID_ARG = -1, /* null/duplicate/overlapping/misaligned pointer, bad size or enum */
+  AR_ERR_UNSUPPORTED = -2, /* AVG on i32, tree order with N not a power of two, ... */
+  AR_ERR_CUDA = -3,        /* a CUDA call failed; ar_last_cuda_error() holds the cause */
+  AR_ERR_TIMEOUT = -4,     /* asynchronous: a step-wise grid barrier gave up (see ar_device_status) */
+  AR_ERR_NO_DEVICE = -5,   /* no usable CUDA device */
+  AR_ERR_TOO_LARGE = -6    /* the call needs more descriptor space than one launch holds */
+} ar_status;
+
+/*
+ * AllReduce: afterwards every bufs[r] holds the reduction of all N inputs.
+ * [concept §3]: every process ends with the same (+)_i D_i; [notes §语义]:
+ * AllReduce = Reduce + Broadcast.
+ *   bufs    host array of nranks device pointers (read and overwritten in place)
+ *   count   elements per rank
+ *   dtype, op, algo   see above
+ *   stream  CUDA stream to enqueue on
+ * Errors: AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_NO_DEVICE.
+ * The step-wise algorithms also use a small per-device synchronisation block
+ * that the library allocates on first use (so the first step-wise call on a
+ * device must not be made during stream capture) and report barrier timeouts
+ * asynchronously through ar_device_status.  Step-wise calls on one device
+ * must not overlap in time (they share that block).
+ */
+int ar_allreduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                 ar_stream_t stream);
+
+/*
+ * ReduceScatter: afterwards chunk r of bufs[r] holds the reduced chunk r (in
+ * the order of `algo`, AVG already divided); the other chunks of each buffer
+ * are left unspecified.  [tutorial §4.4], [concept §3] (each process ends with
+ * exactly 1/N of the global result).
+ * Arguments and errors as ar_allreduce.
+ */
+int ar_reduce_scatter(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                      ar_stream_t stream);
+
+/*
+ * AllGather: on entry chunk r of bufs[r] holds shard r; afterwards every
+ * buffer holds all N shards, copied bit for bit (no arithmetic).
+ * [concept §3], [tutorial §2.2 第二阶段], [notes §两阶段流程].
+ *   algo    AR_RING / AR_TREE: one fused copy pass; AR_RING_STEPWISE /
+ *           AR_TREE_STEPWISE: the literal forwarding schedule.
+ * Arguments and errors as ar_allreduce.
+ */
+int ar_all_gather(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_algo algo, ar_stream_t stream);
+
+/*
+ * DDP bucket plan [tutorial §4.1], [notes §DDP 梯度同步中的地位]: walk the
+ * tensors in reverse registration order; add each to the current bucket while
+ * the bucket's bytes stay <= cap_bytes; a tensor that does not fit opens the
+ * next bucket (so a tensor larger than the cap sits alone).  Inside a bucket
+ * tensors lie in the order they were added.  Bucket 0 holds the
+ * last-registered tensors.
+ *   counts            [ntensors] element counts, registration order
+ *   bucket_of_tensor  [ntensors] out: bucket id of each tensor
+ *   offset_in_bucket  [ntensors] out: element offset of each tensor in its bucket
+ *   bucket_count      [ntensors] out (capacity ntensors): elements per bucket
+ *   nbuckets          out: number of buckets
+ * Host-only; errors: AR_ERR_INVALID_ARG.
+ */
+int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t cap_bytes, int32_t* bucket_of_tensor,
+                   int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets);
+
+/*
+ * Bucketed gradient AllReduce, DDP style: the ntensors gradients of each rank
+ * are grouped into buckets by ar_bucket_plan, every bucket is AllReduced as
+ * one flat buffer (chunks and order follow the bucket, as if the bucket had
+ * been packed), and the result is written back into every rank's tensors.
+ * With op == AR_AVG the 1/N scale is applied inside the reduction.
+ *   grads       host array [nranks * ntensors] of device pointers, row-major by
+ *               rank: grads[r * ntensors + t] is rank r's tensor t
+ *   counts      [ntensors] element counts
+ *   bucket_cap_bytes  cap per bucket (AR_DEFAULT_BUCKET_CAP_BYTES for DDP)
+ *   workspace   NULL: fused path, one pass that reads every gradient element
+ *               of every rank once and writes it once (no packing);
+ *               otherwise host array [nranks] of device buffers of
+ *               workspace_bytes each: the literal path packs into them,
+ *               AllReduces, and unpacks.  workspace_bytes >= total bytes of
+ *               all buckets packs everything at once; >= the largest bucket
+ *               runs bucket by bucket; less is AR_ERR_INVALID_ARG.
+ *   algo        any ar_algo; the step-wise ones run their schedule on every
+ *               bucket at once.
+ * Both paths give bit-identical results.  Errors as ar_allreduce, plus
+ * AR_ERR_TOO_LARGE if one tensor row (nranks pointers) cannot be described.
+ */
+int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype,
+                          ar_op op, ar_algo algo, int64_t bucket_cap_bytes, void* const* workspace,
+                          int64_t workspace_bytes, ar_stream_t stream);
+
+/* Chunk c of a rank buffer of `count` elements split N ways: [*lo, *hi).
+ * Host-only; errors: AR_ERR_INVALID_ARG. */
+int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's
+ * asynchronous status word: *status = AR_OK, or AR_ERR_TIMEOUT when a
+ * step-wise barrier gave up waiting since the last read (the kernel then
+ * stopped early and its buffers hold partial results).
+ * Errors: AR_ERR_INVALID_ARG (status NULL), AR_ERR_CUDA.
+ */
+int ar_device_status(ar_stream_t stream, int* status);
+
+/* Time limit of one step-wise barrier wait, in nanoseconds (default 1e9).
+ * Values <= 0 restore the default. */
+int ar_set_barrier_timeout_ns(int64_t ns);
+
+/* Test hook for failure detection: in the next step-wise launch, block 0
+ * does not arrive at barrier `barrier` (0-based), so every wait on it runs out
+ * and the kernel reports AR_ERR_TIMEOUT through ar_device_status.  -1 clears
+ * the hook.  Nothing faults or hangs: every wait is bounded. */
+int ar_debug_skip_barrier(int barrier);
+
+/* The cudaError_t value behind the calling thread's most recent
+ * AR_ERR_CUDA / AR_ERR_NO_DEVICE return (0 if none). */
+int ar_last_cuda_error(void);
+
+/* Human-readable name of an ar_status value. */
+const char* ar_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_GB300_H */

@@ -1,0 +1,426 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Integers, MAX and the fixed-order f32/bf16 folds must match bit for bit (NaN
+compared as NaN, payload-free); AllGather must copy bits exactly.  Sizes span
+several tiles and ragged tails; the full-size workloads are checked on sampled
+positions (plus every chunk boundary) that the oracle carries through its
+message simulation, and by properties that hold at any size."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from allreduce_gradient_reduction_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+NP_TO_TORCH = {np.dtype(np.float32): torch.float32, np.dtype(np.uint16): torch.int16,
+               np.dtype(np.int32): torch.int32}
+
+
+@pytest.fixture(scope="module")
+def ar():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from allreduce_gradient_reduction_gb300 import build as b
+    b.build()
+    from allreduce_gradient_reduction_gb300 import binding
+    torch.cuda.set_device(0)
+    return binding
+
+
+def to_dev(row: np.ndarray) -> "torch.Tensor":
+    a = np.ascontiguousarray(row)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+def from_dev(bufs, dtype):
+    out = np.stack([b.cpu().numpy() for b in bufs]) if bufs else np.zeros((0, 0))
+    return out.view(np.uint16) if dtype == "bf16" else out
+
+
+def f64(x, dtype):
+    if dtype == "bf16":
+        return (np.asarray(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(x).astype(np.float64)
+
+
+def assert_same(got, want, dtype, what=""):
+    """Bit equality with NaN == NaN."""
+    got, want = np.asarray(got), np.asarray(want)
+    assert got.shape == want.shape, what
+    if dtype == "i32":
+        bad = got != want
+    else:
+        gv, wv = f64(got, dtype), f64(want, dtype)
+        gn, wn = np.isnan(gv), np.isnan(wv)
+        bits = np.uint16 if dtype == "bf16" else np.uint32
+        bad = (gn != wn) | (~gn & ~wn & (got.view(bits) != want.view(bits)))
+    if bad.any():
+        idx = np.argwhere(bad)
+        i = tuple(idx[0])
+        raise AssertionError(f"{what}: {len(idx)} elements differ; first at {i}: got {got[i]!r} want {want[i]!r}")
+
+
+def run_collective(ar, fn_name, x, dtype, count=None, check_status=True, **kw):
+    bufs = [to_dev(x[r]) for r in range(x.shape[0])]
+    rc = getattr(ar, fn_name)(bufs, count=x.shape[1] if count is None else count, dtype=dtype, **kw)
+    ar.check(rc, fn_name)
+    torch.cuda.synchronize()
+    if check_status:
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == 0, (rc, st)
+    return from_dev(bufs, dtype), bufs
+
+
+def inputs(n, count, dtype, kind, seed):
+    if kind == "bits":
+        return W.random_bits(n, count, dtype, seed)
+    if dtype == "i32":
+        return W.uniform_inputs(n, count, "i32", config=seed)
+    if dtype == "bf16":
+        return W.large_inputs(n, count, config=seed)
+    return W.normal_inputs(n, count, 1.0, seed)
+
+
+ALGOS = ["ring", "tree", "ring_stepwise", "tree_stepwise"]
+ORACLE_ALGO = {"ring": "ring", "ring_stepwise": "ring", "tree": "tree", "tree_stepwise": "tree"}
+
+
+def counts_for(n):
+    base = [1, n - 1, n + 1, 1000, 4099, 3 * 2048 * n + 13]
+    if n >= 64:
+        base = [1, n + 1, 4099, 70_001]
+    return [c for c in base if c > 0]
+
+
+# --------------------------------------------------------------------------
+# AllReduce / ReduceScatter / AllGather against the oracle, many shapes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 64])
+def test_allreduce_matches_oracle(ar, algo, dtype, n):
+    if algo.startswith("tree") and n & (n - 1):
+        pytest.skip("tree order needs a power of two")
+    ops = ["sum", "max"] + ([] if dtype == "i32" else ["avg"])
+    for count in counts_for(n):
+        for op in ops:
+            kind = "bits" if (count % 2 and op != "sum") else "values"
+            x = inputs(n, count, dtype, kind, seed=n * 7919 + count)
+            with np.errstate(all="ignore"):
+                want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op=op, dtype=dtype)
+            got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo=algo)
+            assert_same(got, want, dtype, f"{algo} {dtype} {op} n={n} count={count}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_allreduce_special_values(ar, algo, dtype):
+    # NaN, infinities, subnormals, signed zeros in every position
+    for n in (2, 4, 8):
+        for count in (37, 8 * 1024 + 3):
+            x = W.random_bits(n, count, dtype, seed=1000 + n + count)
+            for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+                with np.errstate(all="ignore"):
+                    want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op=op, dtype=dtype)
+                got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo=algo)
+                assert_same(got, want, dtype, f"{algo} {dtype} {op} n={n} count={count}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_reduce_scatter_matches_oracle(ar, algo, dtype):
+    for n in (2, 3, 4, 8, 16):
+        if algo.startswith("tree") and n & (n - 1):
+            continue
+        for count in (n, 4099, 2 * 2048 * n + 5):
+            x = inputs(n, count, dtype, "values", seed=50 + n + count)
+            for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+                want, _ = oracle.reduce_scatter(x, algo=ORACLE_ALGO[algo], op=op, dtype=dtype)
+                got, _ = run_collective(ar, "ar_reduce_scatter", x, dtype, op=op, algo=algo)
+                for r in range(n):
+                    lo, hi = oracle.chunk_range(count, n, r)
+                    assert_same(got[r, lo:hi], want[r, lo:hi], dtype, f"{algo} {op} n={n} count={count} rank {r}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_all_gather_copies_bits(ar, algo, dtype):
+    for n in (2, 3, 4, 8, 16):
+        if algo.startswith("tree") and n & (n - 1):
+            continue
+        for count in (1, n + 1, 4099, 3 * 2048 * n + 7):
+            x = W.random_bits(n, count, dtype, seed=77 + n + count)  # NaN payloads must survive
+            want, _ = oracle.all_gather(x, algo=ORACLE_ALGO[algo], dtype=dtype)
+            bufs = [to_dev(x[r]) for r in range(n)]
+            ar.check(ar.ar_all_gather(bufs, count=count, dtype=dtype, algo=algo), "all_gather")
+            got = from_dev(bufs, dtype)
+            bits = {"bf16": np.uint16, "f32": np.uint32, "i32": np.uint32}[dtype]
+            assert np.array_equal(got.view(bits), want.view(bits)), (algo, n, count)
+
+
+# --------------------------------------------------------------------------
+# Alignment, degenerate sizes, streams
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_buffers_take_scalar_path(ar, algo, dtype):
+    n, count = 8, 5000
+    x = inputs(n, count, dtype, "values", seed=9)
+    want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op="sum", dtype=dtype)
+    for shift in (1, 3):
+        big = [to_dev(np.concatenate([x[r][:shift], x[r]])) for r in range(n)]
+        views = [b[shift:] for b in big]  # element-aligned, not 16-byte aligned
+        ar.check(ar.ar_allreduce(views, count=count, dtype=dtype, op="sum", algo=algo), "unaligned")
+        torch.cuda.synchronize()
+        got = from_dev(views, dtype)
+        assert_same(got, want, dtype, f"{algo} shift {shift}")
+        # the element before each buffer is untouched
+        assert np.array_equal(from_dev([b[:shift] for b in big], dtype), x[:, :shift])
+
+
+def test_degenerate_sizes(ar):
+    x = W.normal_inputs(4, 10, 1.0, 3)
+    bufs = [to_dev(x[r]) for r in range(4)]
+    ar.check(ar.ar_allreduce(bufs, count=0), "count 0")
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev(bufs, "f32"), x)  # nothing moved
+    one = [to_dev(x[0])]
+    for algo in ALGOS:
+        ar.check(ar.ar_allreduce(one, count=10, op="avg", algo=algo), "one rank")
+    torch.cuda.synchronize()
+    assert np.array_equal(one[0].cpu().numpy(), x[0])
+
+
+def test_runs_on_the_given_stream(ar):
+    n, count = 8, 1 << 20
+    x = W.normal_inputs(n, count, 1.0, 4)
+    want, _ = oracle.allreduce(x, op="sum", dtype="f32")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        bufs = [to_dev(x[r]) for r in range(n)]
+        ar.check(ar.ar_allreduce(bufs, dtype="f32", op="sum", stream=s), "stream")
+    s.synchronize()
+    assert_same(from_dev(bufs, "f32"), want, "f32")
+
+
+def test_rejects_memory_it_cannot_use(ar):
+    x = torch.zeros(1024, device="cuda")
+    y = torch.zeros(1024, device="cuda")
+    host = np.zeros(1024, dtype=np.float32)
+    assert ar.ar_allreduce([x, host.ctypes.data], count=1024) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce([x, y], count=1 << 30) == ar.AR_ERR_INVALID_ARG  # past the allocation
+    assert ar.ar_allreduce([x, x[512:]], count=1024) == ar.AR_ERR_INVALID_ARG  # overlap
+
+
+# --------------------------------------------------------------------------
+# The printed examples and the configured workloads
+# --------------------------------------------------------------------------
+
+def test_three_rank_example(ar):
+    x = W.three_rank_example()
+    got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo="ring")
+    assert np.all(got == 6.0)
+    got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo="ring_stepwise")
+    assert np.all(got == 6.0)
+
+
+def test_printed_examples_on_gpu(ar):
+    x = np.stack([np.full(6, r + 1, dtype=np.float32) for r in range(4)])  # ones(2,3)*(rank+1)
+    for algo in ALGOS:
+        got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo=algo)
+        assert np.all(got == 10.0), algo
+    x = np.stack([np.full(4, r, dtype=np.float32) for r in range(4)])   # ones(4)*rank, then / world size
+    for algo in ALGOS:
+        got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="avg", algo=algo)
+        assert np.all(got == 1.5), algo
+
+
+def test_small_workload(ar):
+    x = W.small_inputs()
+    exact = x.astype(np.float64).sum(axis=0)
+    for algo in ALGOS:
+        got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo=algo)
+        assert np.array_equal(got, np.broadcast_to(exact, got.shape)), algo
+
+
+def test_bucket_workload_full_compare(ar):
+    x = W.bucket_inputs()
+    for op in ("avg", "max"):
+        want, _ = oracle.allreduce(x, algo="ring", op=op, dtype="f32")
+        for algo in ("ring", "ring_stepwise"):
+            got, _ = run_collective(ar, "ar_allreduce", x, "f32", op=op, algo=algo)
+            assert_same(got, want, "f32", f"{algo} {op}")
+    # f32 stays inside the stated tolerance against the order-free sum
+    s, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo="ring")
+    xv = x.astype(np.float64)
+    assert np.all(np.abs(s[0] - xv.sum(axis=0)) <= 1e-5 * np.abs(xv).sum(axis=0))
+
+
+def sample_positions(count, n, k, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    pos = [g.integers(0, count, size=k)]
+    for c in range(n + 1):
+        lo = oracle.chunk_range(count, n, c)[0] if c < n else count
+        pos.append(np.arange(lo - 2, lo + 3))
+    p = np.unique(np.concatenate(pos))
+    return p[(p >= 0) & (p < count)]
+
+
+@pytest.mark.slow
+def test_large_workload_sampled(ar):
+    """8 ranks x 67,108,864 bf16, the configuration the benchmark times, in
+    the same call; checked on sampled positions and by whole-buffer
+    properties."""
+    n, count = W.LARGE["nranks"], W.LARGE["count"]
+    x = W.large_inputs(n, count)
+    pos = sample_positions(count, n, 1 << 16, 5)
+    xs = np.ascontiguousarray(x[:, pos])
+    for algo in ("ring", "tree"):
+        want, _ = oracle.allreduce(xs, algo=algo, op="sum", dtype="bf16", count=count, positions=pos)
+        bufs = [to_dev(x[r]) for r in range(n)]
+        ar.check(ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo=algo), algo)
+        torch.cuda.synchronize()
+        for r in range(1, n):
+            assert torch.equal(bufs[r], bufs[0]), (algo, r)  # every rank identical
+        got = bufs[0][torch.from_numpy(pos).cuda()].cpu().numpy().view(np.uint16)
+        assert_same(got, want[0], "bf16", algo)
+        # bf16 error stays within the recursive-summation bound gamma_k * sum|x|
+        xv = f64(xs, "bf16")
+        depth = n - 1 if algo == "ring" else int(math.log2(n))
+        u = 2.0 ** -8
+        err = np.abs(f64(got, "bf16") - xv.sum(axis=0))
+        assert np.all(err <= depth * u / (1 - depth * u) * np.abs(xv).sum(axis=0))
+        del bufs
+
+
+@pytest.mark.slow
+def test_gpt2_bucketed_fused_and_literal(ar):
+    n = W.GPT2["nranks"]
+    counts = W.gpt2_small_counts()
+    host = [W.gpt2_rank_grads(r, counts) for r in range(n)]
+    g = np.random.Generator(np.random.PCG64(8))
+    tid = g.integers(0, counts.size, size=20000).astype(np.int32)
+    idx = (g.random(tid.size) * counts[tid]).astype(np.int64)
+    # every tensor's first and last element too
+    tid = np.concatenate([tid, np.arange(counts.size), np.arange(counts.size)]).astype(np.int32)
+    idx = np.concatenate([idx, np.zeros(counts.size, np.int64), counts - 1])
+    pairs = np.unique(np.stack([tid, idx], axis=1), axis=0)
+    tid, idx = pairs[:, 0].astype(np.int32), pairs[:, 1].astype(np.int64)
+    want, _ = oracle.bucketed_allreduce(host, op="avg", dtype="f32", samples=(tid, idx))
+
+    flat_len = int(counts.sum())
+    results = {}
+    for mode in ("fused", "whole", "per_bucket", "stepwise"):
+        # one flat allocation per rank with the tensors as views into it
+        flats = [torch.from_numpy(np.concatenate(host[r])).cuda() for r in range(n)]
+        offs = np.concatenate([[0], np.cumsum(counts)])
+        grads = [[flats[r][offs[t]:offs[t + 1]] for t in range(counts.size)] for r in range(n)]
+        ws, wbytes = None, 0
+        if mode in ("whole", "per_bucket"):
+            per = flat_len if mode == "whole" else int(max(ar.ar_bucket_plan(counts, "f32")[3]))
+            ws = [torch.empty(per, dtype=torch.float32, device="cuda") for _ in range(n)]
+            wbytes = per * 4
+        algo = "ring_stepwise" if mode == "stepwise" else "ring"
+        rc = ar.ar_bucketed_allreduce(grads, counts=counts, dtype="f32", op="avg", algo=algo, workspace=ws,
+                                      workspace_bytes=wbytes)
+        ar.check(rc, mode)
+        torch.cuda.synchronize()
+        sel = torch.from_numpy(offs[tid] + idx).cuda()
+        got = np.stack([flats[r][sel].cpu().numpy() for r in range(n)])
+        assert_same(got, want, "f32", mode)
+        results[mode] = flats[0].cpu().numpy()
+        del flats, grads, ws
+    for mode in ("whole", "per_bucket", "stepwise"):
+        assert np.array_equal(results[mode].view(np.uint32), results["fused"].view(np.uint32)), mode
+
+
+def test_bucketed_small_full_compare(ar):
+    g = np.random.Generator(np.random.PCG64(21))
+    counts = [5, 300, 17, 1024, 3, 999, 64, 4096 + 3, 1, 2048]
+    for n in (2, 3, 8):
+        for dtype in ("f32", "bf16"):
+            if dtype == "f32":
+                host = [[g.standard_normal(c).astype(np.float32) for c in counts] for _ in range(n)]
+            else:
+                host = [[W.f32_to_bf16_bits_truncate(g.standard_normal(c).astype(np.float32)) for c in counts]
+                        for _ in range(n)]
+            es = 4 if dtype == "f32" else 2
+            cap = es * 1500
+            for algo in ("ring", "tree", "ring_stepwise", "tree_stepwise"):
+                if algo.startswith("tree") and n & (n - 1):
+                    continue
+                want, _ = oracle.bucketed_allreduce(host, op="avg", dtype=dtype, algo=ORACLE_ALGO[algo],
+                                                    cap_bytes=cap)
+                for literal in (False, True):
+                    grads = [[to_dev(t) for t in row] for row in host]
+                    ws = None
+                    if literal:
+                        ws = [torch.empty(sum(counts) + 8, dtype=torch.float32, device="cuda") for _ in range(n)]
+                    rc = ar.ar_bucketed_allreduce(grads, counts=counts, dtype=dtype, op="avg", algo=algo,
+                                                  bucket_cap_bytes=cap, workspace=ws,
+                                                  workspace_bytes=(sum(counts) + 8) * 4 if literal else 0)
+                    ar.check(rc, f"bucketed {algo}")
+                    torch.cuda.synchronize()
+                    for r in range(n):
+                        for t in range(len(counts)):
+                            got = grads[r][t].cpu().numpy()
+                            if dtype == "bf16":
+                                got = got.view(np.uint16)
+                            assert_same(got, want[r][t], dtype, f"{algo} literal={literal} n={n} r={r} t={t}")
+
+
+# --------------------------------------------------------------------------
+# Exhaustive bf16 step: every pair of bf16 values through a 2-rank ring
+# --------------------------------------------------------------------------
+
+@pytest.mark.slow
+def test_bf16_step_exhaustive(ar):
+    all16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    block = 1 << 12  # values of `a` per block: 2^28 pairs
+    a_dev = torch.empty(block << 16, dtype=torch.int16, device="cuda")
+    b_dev = torch.empty(block << 16, dtype=torch.int16, device="cuda")
+    b_row = torch.from_numpy(all16.view(np.int16)).cuda().repeat(block)
+    for a0 in range(0, 1 << 16, block):
+        a_vals = np.repeat(all16[a0:a0 + block], 1 << 16)
+        a_dev.copy_(torch.from_numpy(a_vals.view(np.int16)))
+        b_dev.copy_(b_row)
+        ar.check(ar.ar_allreduce([a_dev, b_dev], count=a_vals.size, dtype="bf16", op="sum", algo="ring"), "pairs")
+        torch.cuda.synchronize()
+        got = a_dev.cpu().numpy().view(np.uint16)
+        want = oracle.step(a_vals, np.tile(all16, block), op="sum", dtype="bf16")
+        assert_same(got, want, "bf16", f"a block {a0}")
+
+
+# --------------------------------------------------------------------------
+# Failure detection without a fault: a barrier nobody completes times out
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ["ring_stepwise", "tree_stepwise"])
+def test_barrier_timeout_is_reported(ar, algo):
+    n, count = 8, 1 << 16
+    x = W.normal_inputs(n, count, 1.0, 12)
+    ar.ar_set_barrier_timeout_ns(50_000_000)  # 50 ms
+    try:
+        bufs = [to_dev(x[r]) for r in range(n)]
+        ar.ar_debug_skip_barrier(1)
+        ar.check(ar.ar_allreduce(bufs, count=count, dtype="f32", op="sum", algo=algo), "launch")
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == ar.AR_ERR_TIMEOUT
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == 0  # read once, then cleared
+        # the context is still usable and the next call is correct
+        want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op="sum", dtype="f32")
+        got, _ = run_collective(ar, "ar_allreduce", x, "f32", op="sum", algo=algo)
+        assert_same(got, want, "f32", algo)
+    finally:
+        ar.ar_debug_skip_barrier(-1)
+        ar.ar_set_barrier_timeout_ns(0)
