@@ -43,6 +43,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--algo", default="ring", help="ring | tree | ring_stepwise | tree_stepwise")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    p.add_argument("--count", type=int, default=0,
+                   help="elements per rank (default: the full workload); smaller counts are for profiling")
     p.add_argument("--variants", action="store_true", help="also time tree and step-wise orders (extra keys)")
     return p.parse_args()
 
@@ -250,13 +253,13 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    n, count = W.LARGE["nranks"], W.LARGE["count"]
+    n, count = W.LARGE["nranks"], (args.count or W.LARGE["count"])
     nbytes_step = 2 * n * count * 2  # every rank element read once, the result written once per rank
 
     # inputs: generated on the host (seeded), pinned, uploaded once
     host = torch.empty((n, count), dtype=torch.int16, pin_memory=True)
     for r in range(n):
-        host[r].copy_(torch.from_numpy(W.large_rank(r).view(np.int16)))
+        host[r].copy_(torch.from_numpy(W.large_rank(r, count).view(np.int16)))
     bufs = [torch.empty(count, dtype=torch.int16, device=dev) for _ in range(n)]
     for r in range(n):
         bufs[r].copy_(host[r], non_blocking=True)
@@ -299,30 +302,32 @@ def main():
     achieved = nbytes_step / (ms_local / 1e3) / 1e9
 
     # end to end through the public call: pinned host -> device, AllReduce, device -> host
-    e2e_steps = max(3, min(args.steps, 20))
-    out_host = torch.empty((n, count), dtype=torch.int16, pin_memory=True)
-    for r in range(n):  # warm the copy path once
-        bufs[r].copy_(host[r], non_blocking=True)
-    step()
-    for r in range(n):
-        out_host[r].copy_(bufs[r], non_blocking=True)
-    torch.cuda.synchronize()
-    barrier(ws)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(e2e_steps):
-        for r in range(n):
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        out_host = torch.empty((n, count), dtype=torch.int16, pin_memory=True)
+        for r in range(n):  # warm the copy path once
             bufs[r].copy_(host[r], non_blocking=True)
         step()
         for r in range(n):
             out_host[r].copy_(bufs[r], non_blocking=True)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
-    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, ws)
-    e2e_value = ws * nbytes_step / (ms_e2e / 1e3) / 1e9
-    # the copied-back result is the reduction of the uploaded inputs
-    ok_e2e = bool(torch.equal(out_host[0], out_host[n - 1]))
+        torch.cuda.synchronize()
+        barrier(ws)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            for r in range(n):
+                bufs[r].copy_(host[r], non_blocking=True)
+            step()
+            for r in range(n):
+                out_host[r].copy_(bufs[r], non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, ws)
+        e2e = {"value": ws * nbytes_step / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": n * count * 2, "d2h_bytes_per_step": n * count * 2, "steps": e2e_steps,
+               "ms_per_step": ms_e2e, "result_ranks_identical": bool(torch.equal(out_host[0], out_host[n - 1]))}
 
     variants = {}
     if args.variants:
@@ -360,9 +365,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
                          "algorithmic_bytes_per_launch": nbytes_step},
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": n * count * 2,
-                    "d2h_bytes_per_step": n * count * 2, "steps": e2e_steps, "ms_per_step": ms_e2e,
-                    "result_ranks_identical": ok_e2e},
+            "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clocks.summary(t_wall0, t_wall1),
             "cpu_baseline": cpu,
