@@ -28,7 +28,7 @@ MAX_RANKS = 64
 DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
 EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucketed_allreduce",
-           "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
+           "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
            "ar_last_cuda_error", "ar_strerror", "ar_version")
 
 
@@ -52,6 +52,7 @@ def _load():
     L.ar_bucket_plan.argtypes = [ctypes.POINTER(i64), cint, cint, i64, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                  ctypes.POINTER(i64), ctypes.POINTER(i32)]
     L.ar_bucketed_allreduce.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, pp, i64, vp]
+    L.ar_bucketed_allreduce_noalloc.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, vp]
     L.ar_chunk_range.argtypes = [i64, cint, cint, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     L.ar_device_status.argtypes = [vp, ctypes.POINTER(cint)]
     L.ar_set_barrier_timeout_ns.argtypes = [i64]
@@ -155,6 +156,26 @@ def ar_bucketed_allreduce(grads, counts=None, ntensors=None, nranks=None, dtype=
     return lib.ar_bucketed_allreduce(_ptr_array(flat), c, nt, nr, _enum(DTYPE, dtype), _enum(OP, op),
                                      _enum(ALGO, algo), int(bucket_cap_bytes), ws, int(workspace_bytes),
                                      _stream(stream))
+
+
+def ar_bucketed_allreduce_noalloc(grads, counts=None, ntensors=None, nranks=None, dtype="f32", op="avg",
+                                  algo="ring", bucket_cap_bytes=DEFAULT_BUCKET_CAP_BYTES, stream=None) -> int:
+    """Same arguments as ar_bucketed_allreduce without the workspace: the
+    library's fixed scratch array stands in for it (see include/ar.h)."""
+    if len(grads) and isinstance(grads[0], (list, tuple)):
+        nr, nt = len(grads), len(grads[0])
+        flat = [g for row in grads for g in row]
+        if counts is None:
+            counts = [int(g.numel()) for g in grads[0]]
+    else:
+        nr, nt, flat = int(nranks), int(ntensors), list(grads)
+    c = (ctypes.c_int64 * max(nt, 1))(*[int(x) for x in counts])
+    return lib.ar_bucketed_allreduce_noalloc(_ptr_array(flat), c, nt, nr, _enum(DTYPE, dtype), _enum(OP, op),
+                                             _enum(ALGO, algo), int(bucket_cap_bytes), _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+NOALLOC_MAX_TENSORS = 1024
 
 
 def ar_chunk_range(count, nranks, c):

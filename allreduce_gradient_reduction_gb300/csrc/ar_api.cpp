@@ -281,6 +281,11 @@ int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, in
 
 }  // namespace
 
+namespace ar {
+// Lets other translation units report a CUDA failure the same way.
+int note_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+}  // namespace ar
+
 extern "C" {
 
 int ar_allreduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,

@@ -165,6 +165,43 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
                           ar_op op, ar_algo algo, int64_t bucket_cap_bytes, void* const* workspace,
                           int64_t workspace_bytes, ar_stream_t stream);
 
+/*
+ * Allocation-free bucketed AllReduce.  The pages have no counterpart: this is
+ * an addition for callers that are not allowed to allocate -- a process whose
+ * device memory is handed out by another allocator or a fixed pool that must
+ * account for every byte, an engine that bans allocation on its hot path
+ * because cudaMalloc can synchronise the device and stall every stream, or a
+ * runtime that must not fail for lack of memory once it has started.
+ *
+ * Same result, bit for bit, as ar_bucketed_allreduce with the same arguments:
+ * the literal path (pack each bucket, AllReduce it, unpack), with the pack
+ * buffers taken from an array of AR_NOALLOC_SCRATCH_BYTES compiled into the
+ * library instead of a caller workspace.  Each rank gets a slice of
+ * AR_NOALLOC_SCRATCH_BYTES / nranks bytes (rounded down to 256); a bucket
+ * larger than that slice, or more than AR_NOALLOC_MAX_TENSORS tensors, is
+ * rejected with AR_ERR_TOO_LARGE before any work is queued.  The call makes
+ * no cudaMalloc/cudaFree and no other allocating call, on the device or the
+ * host heap.
+ *   algo   AR_RING or AR_TREE; the step-wise orders need a barrier block the
+ *          library would allocate, so they return AR_ERR_UNSUPPORTED here.
+ * Other arguments and errors as ar_bucketed_allreduce (without workspace).
+ * The array is shared by all calls and keeps the last call's contents (every
+ * byte this call reads from it, it has written first, so nothing needs
+ * clearing).  Calls that overlap on the GPU -- on different streams, or from
+ * different host threads onto different streams -- race on it and corrupt
+ * each other's results; keep them ordered, e.g. on one stream.  Host-side
+ * calls are serialised by a lock.  The array occupies device memory on every
+ * GPU where the library's device code is loaded, until the process exits
+ * (with CUDA's default lazy module loading, from the first call on that GPU).
+ * The first call on each device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress, no allocation); make that
+ * first call before any stream capture.
+ */
+#define AR_NOALLOC_SCRATCH_BYTES (32 << 20)
+#define AR_NOALLOC_MAX_TENSORS 1024
+int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype,
+                                  ar_op op, ar_algo algo, int64_t bucket_cap_bytes, ar_stream_t stream);
+
 /* Chunk c of a rank buffer of `count` elements split N ways: [*lo, *hi).
  * Host-only; errors: AR_ERR_INVALID_ARG. */
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);
