@@ -20,16 +20,17 @@ LIB_PATH = os.path.join(_HERE, "libar_gb300.so")
 
 DTYPE = {"f32": 0, "bf16": 1, "i32": 2}
 OP = {"sum": 0, "max": 1, "avg": 2}
-ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3}
+ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3, "naive": 4}
 STATUS = {0: "AR_OK", -1: "AR_ERR_INVALID_ARG", -2: "AR_ERR_UNSUPPORTED", -3: "AR_ERR_CUDA",
           -4: "AR_ERR_TIMEOUT", -5: "AR_ERR_NO_DEVICE", -6: "AR_ERR_TOO_LARGE"}
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4
 MAX_RANKS = 64
 DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
-EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_bucket_plan", "ar_bucketed_allreduce",
+EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_bucket_plan",
+           "ar_bucketed_allreduce",
            "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
-           "ar_last_cuda_error", "ar_strerror", "ar_version")
+           "ar_last_cuda_error", "ar_strerror", "ar_version", "ar_kernel_launches")
 
 
 class ArError(RuntimeError):
@@ -49,6 +50,8 @@ def _load():
     L.ar_allreduce.argtypes = [pp, cint, i64, cint, cint, cint, vp]
     L.ar_reduce_scatter.argtypes = [pp, cint, i64, cint, cint, cint, vp]
     L.ar_all_gather.argtypes = [pp, cint, i64, cint, cint, vp]
+    L.ar_reduce.argtypes = [pp, cint, i64, cint, cint, cint, cint, vp]
+    L.ar_broadcast.argtypes = [pp, cint, i64, cint, cint, vp]
     L.ar_bucket_plan.argtypes = [ctypes.POINTER(i64), cint, cint, i64, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                  ctypes.POINTER(i64), ctypes.POINTER(i32)]
     L.ar_bucketed_allreduce.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, pp, i64, vp]
@@ -61,9 +64,11 @@ def _load():
     L.ar_strerror.argtypes = [cint]
     L.ar_strerror.restype = ctypes.c_char_p
     L.ar_version.argtypes = []
+    L.ar_kernel_launches.argtypes = []
     for name in EXPORTS:
         if name != "ar_strerror":
             getattr(L, name).restype = cint
+    L.ar_kernel_launches.restype = i64
     return L
 
 
@@ -123,6 +128,18 @@ def ar_all_gather(bufs, nranks=None, count=None, dtype="f32", algo="ring", strea
     n = len(bufs) if nranks is None else int(nranks)
     return lib.ar_all_gather(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), _enum(ALGO, algo),
                              _stream(stream))
+
+
+def ar_reduce(bufs, nranks=None, count=None, dtype="f32", op="sum", algo="ring", root=0, stream=None) -> int:
+    n = len(bufs) if nranks is None else int(nranks)
+    return lib.ar_reduce(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), _enum(OP, op),
+                         _enum(ALGO, algo), int(root), _stream(stream))
+
+
+def ar_broadcast(bufs, nranks=None, count=None, dtype="f32", root=0, stream=None) -> int:
+    n = len(bufs) if nranks is None else int(nranks)
+    return lib.ar_broadcast(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), int(root),
+                            _stream(stream))
 
 
 def ar_bucket_plan(counts, dtype="f32", cap_bytes=DEFAULT_BUCKET_CAP_BYTES):
@@ -209,3 +226,7 @@ def ar_strerror(code: int) -> str:
 
 def ar_version() -> int:
     return lib.ar_version()
+
+
+def ar_kernel_launches() -> int:
+    return lib.ar_kernel_launches()

@@ -95,7 +95,7 @@ int check_ranges(std::vector<Range>& rs, int esize) {
 int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
   if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0) return AR_ERR_INVALID_ARG;
   if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
-  if (algo < AR_RING || algo > AR_TREE_STEPWISE) return AR_ERR_INVALID_ARG;
+  if (algo < AR_RING || algo > AR_NAIVE) return AR_ERR_INVALID_ARG;
   if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
   if ((algo == AR_TREE || algo == AR_TREE_STEPWISE) && !is_pow2(nranks)) return AR_ERR_UNSUPPORTED;
   return AR_OK;
@@ -147,6 +147,7 @@ struct Job {
   int dtype, op, algo, phases;  // phases: 1 RS, 2 AG, 3 both
   bool avg;
   bool vec;
+  int root = -1;  // Reduce: the rank that receives the result
 };
 
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
@@ -177,6 +178,8 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
     a.tab = tab;
     a.avg = j.avg ? 1 : 0;
     a.owner_only = j.phases == 1 ? 1 : 0;
+    a.to_root = j.root >= 0 ? 1 : 0;
+    a.root = j.root >= 0 ? j.root : 0;
     a.fn = (float)tab.nranks;
     e = ar::launch_fused(j.dtype, dop, order, j.vec, a, s);
   }
@@ -244,16 +247,24 @@ struct TableBuilder {
   }
 };
 
+// phases: 1 ReduceScatter, 2 AllGather, 3 AllReduce; root >= 0: Reduce to root
 int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases,
-               cudaStream_t stream) {
+               cudaStream_t stream, int root = -1) {
   int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
   if (rc) return rc;
+  if (algo == AR_NAIVE && phases != 3) return AR_ERR_UNSUPPORTED;  // no naive ReduceScatter / AllGather
   if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
   if (count == 0 || nranks == 1) return AR_OK;
   TableBuilder tb{nranks, {}, {}};
   int row = tb.add_row(bufs);
-  for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
-  Job j{dtype, op, algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};
+  if (algo == AR_NAIVE) {
+    // index order x[0], x[1], ..., x[N-1] is the ring order of chunk N-1
+    tb.add_seg(row, 0, count, nranks - 1);
+  } else {
+    for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
+  }
+  Job j{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};
+  j.root = root;
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
 }
 
@@ -284,6 +295,9 @@ int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, in
 namespace ar {
 // Lets other translation units report a CUDA failure the same way.
 int note_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
+std::atomic<int64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace ar
 
 extern "C" {
@@ -300,6 +314,26 @@ int ar_reduce_scatter(void* const* bufs, int nranks, int64_t count, ar_dtype dty
 
 int ar_all_gather(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_algo algo, ar_stream_t stream) {
   return collective(bufs, nranks, count, dtype, AR_SUM, algo, 2, (cudaStream_t)stream);
+}
+
+int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo, int root,
+              ar_stream_t stream) {
+  if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+  if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+  return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream, root);
+}
+
+int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, int root, ar_stream_t stream) {
+  if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+  int rc = check_common(nranks, count, dtype, AR_SUM, AR_RING);
+  if (rc) return rc;
+  if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
+  if (count == 0 || nranks == 1) return AR_OK;
+  // one segment owned by the root: the AllGather copy kernel sends it to every other rank
+  TableBuilder tb{nranks, {}, {}};
+  tb.add_seg(tb.add_row(bufs), 0, count, root);
+  Job j{dtype, AR_SUM, AR_RING, 2, false, all_aligned16(bufs, nranks)};
+  return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
 }
 
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
@@ -322,6 +356,7 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
   cudaStream_t stream = (cudaStream_t)stream_;
   int rc = check_common(nranks, 0, dtype, op, algo);
   if (rc) return rc;
+  if (algo == AR_NAIVE) return AR_ERR_UNSUPPORTED;
   if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
   if (ntensors == 0) return AR_OK;
   if (!grads || !counts) return AR_ERR_INVALID_ARG;
@@ -492,5 +527,7 @@ const char* ar_strerror(int status) {
 }
 
 int ar_version(void) { return 100; }
+
+int64_t ar_kernel_launches(void) { return ar::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

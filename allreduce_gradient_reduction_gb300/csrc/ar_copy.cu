@@ -65,9 +65,8 @@ __global__ void __launch_bounds__(kFusedBlock) gather_kernel(const __grid_consta
 template <int ES, bool VECTOR>
 static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
   if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll) == 0) return cudaSuccess;
-  static const int bps = blocks_per_sm(gather_kernel<ES, VECTOR>, kFusedBlock);
-  const int64_t cap = (int64_t)bps * sm_count();
-  gather_kernel<ES, VECTOR><<<(unsigned)(t.ntiles < cap ? t.ntiles : cap), kFusedBlock, 0, stream>>>(t);
+  gather_kernel<ES, VECTOR><<<grid_for(t.ntiles), kFusedBlock, 0, stream>>>(t);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -125,15 +124,9 @@ __global__ void __launch_bounds__(kFusedBlock) copy_kernel(const __grid_constant
 cudaError_t launch_copy(CopyArgs& a, cudaStream_t stream) {
   const int es = a.esize;
   if (fill_tiles(a.tab, 16 / es, (int64_t)kFusedBlock * kCopyUnroll) == 0) return cudaSuccess;
-  if (es == 2) {
-    static const int bps = blocks_per_sm(copy_kernel<2>, kFusedBlock);
-    const int64_t cap = (int64_t)bps * sm_count();
-    copy_kernel<2><<<(unsigned)(a.tab.ntiles < cap ? a.tab.ntiles : cap), kFusedBlock, 0, stream>>>(a);
-  } else {
-    static const int bps = blocks_per_sm(copy_kernel<4>, kFusedBlock);
-    const int64_t cap = (int64_t)bps * sm_count();
-    copy_kernel<4><<<(unsigned)(a.tab.ntiles < cap ? a.tab.ntiles : cap), kFusedBlock, 0, stream>>>(a);
-  }
+  if (es == 2) copy_kernel<2><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  else copy_kernel<4><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 

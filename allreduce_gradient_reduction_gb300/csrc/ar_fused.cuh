@@ -24,11 +24,24 @@ namespace ar {
 
 constexpr int kFusedBlock = 256;
 
-// 16-byte vectors per thread per tile: enough loads in flight to cover HBM
-// latency without spilling (N rank vectors per position).
+// 16-byte vector positions per thread per tile (U), chosen so that each
+// thread keeps about 8 rank loads of 16 bytes in flight (U x min(N, 8)) and
+// stays within 64 registers: 4 blocks of 256 threads per SM.  Measured on
+// GB300 (8 x 128 MiB bf16 ring): U=1 at 4 blocks/SM 309.8 us, U=2 310.7 us,
+// U=3 at 2 blocks/SM 311.3 us, U=4 at 1 block/SM 343.5 us -- occupancy
+// matters more than loads per thread once the grid is one tile per block.
+// (The wide trees, N >= 16, get 128 registers: 2 blocks per SM.)
+__host__ __device__ constexpr int fused_min_blocks(int nr) { return nr > 8 ? 2 : 4; }
 __host__ __device__ constexpr int fused_unroll(int order, int nr) {
-  return order == TREE ? (nr <= 4 ? 4 : (nr <= 8 ? 2 : 1)) : (nr == 0 ? 2 : (nr <= 4 ? 4 : 2));
+  return (nr == 2) ? 2 : 1;
 }
+
+// Grids are sized one tile per block, not persistent: blocks start in index
+// order, so the blocks in flight at any moment cover a compact window of
+// consecutive tiles in all 2N streams, which keeps HBM rows open; on GB300
+// this measured 5-10% faster than a grid of resident blocks striding over
+// the tiles.  The loop in the kernels still strides, for grids at the cap.
+constexpr int64_t kMaxGrid = 1 << 30;
 
 template <int DT, int OP, int NR>
 __device__ __forceinline__ uint4 tree_fold_regs(uint4 (&x)[NR]) {
@@ -40,7 +53,7 @@ __device__ __forceinline__ uint4 tree_fold_regs(uint4 (&x)[NR]) {
 }
 
 template <int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int U = fused_unroll(ORDER, NR);
@@ -55,26 +68,25 @@ __global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_con
     const void* const* P = T.ptr + (size_t)s.tensor * n;
     const int c = s.chunk;
 
-    int64_t off[U];
+    // position u of this thread is byte offset base + u * kStride in every rank
+    const int64_t v0 = sh.vb + ti * TILE_V + threadIdx.x;
+    const int64_t base = v0 * 16;
+    constexpr int64_t kStride = (int64_t)kFusedBlock * 16;
     bool ok[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t v = sh.vb + ti * TILE_V + u * kFusedBlock + threadIdx.x;
-      ok[u] = v < sh.ve;
-      off[u] = v * 16;
-    }
+    for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < sh.ve;
 
     uint4 acc[U];
     if constexpr (ORDER == RING && NR > 0) {
       const char* src[NR];
 #pragma unroll
-      for (int p = 0; p < NR; ++p) src[p] = static_cast<const char*>(P[rot(c + 1 + p, NR)]);
+      for (int p = 0; p < NR; ++p) src[p] = static_cast<const char*>(P[rot(c + 1 + p, NR)]) + base;
       uint4 x[U][NR];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int p = 0; p < NR; ++p)
-          if (ok[u]) x[u][p] = ld_stream(src[p] + off[u]);
+          if (ok[u]) x[u][p] = ld_stream(src[p] + u * kStride);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         acc[u] = x[u][0];
@@ -88,10 +100,10 @@ __global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_con
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (g + q < n) {
-            const char* src = static_cast<const char*>(P[rot(c + 1 + g + q, n)]);
+            const char* src = static_cast<const char*>(P[rot(c + 1 + g + q, n)]) + base;
 #pragma unroll
             for (int u = 0; u < U; ++u)
-              if (ok[u]) x[u][q] = ld_stream(src + off[u]);
+              if (ok[u]) x[u][q] = ld_stream(src + u * kStride);
           }
         }
 #pragma unroll
@@ -105,50 +117,58 @@ __global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_con
     } else if constexpr (NR <= 8) {
       uint4 x[U][NR];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
+      for (int p = 0; p < NR; ++p) {
+        const char* src = static_cast<const char*>(P[p]) + base;
 #pragma unroll
-        for (int p = 0; p < NR; ++p)
-          if (ok[u]) x[u][p] = ld_stream(static_cast<const char*>(P[p]) + off[u]);
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = tree_fold_regs<DT, OP, NR>(x[u]);
     } else {
-      // N = 16, 32, 64: aligned subtrees of 8 ranks, then a tree over them
-      static_assert(U == 1, "one vector per thread for wide trees");
-      uint4 part[NR / 8];
-#pragma unroll
+      // N = 16, 32, 64: aligned subtrees of 8 ranks, each folded as it
+      // arrives and merged with its finished siblings (a binary counter over
+      // the subtree index), which is the same balanced tree.  One group at a
+      // time: 8 loads in flight per thread fit the register budget, N do not.
+      static_assert(U == 1, "one vector position per thread for wide trees");
+      uint4 stk[4];
+      int top = 0;
+#pragma unroll 1
       for (int g = 0; g < NR / 8; ++g) {
         uint4 x[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          if (ok[0]) x[q] = ld_stream(static_cast<const char*>(P[g * 8 + q]) + off[0]);
-        part[g] = tree_fold_regs<DT, OP, 8>(x);
+          if (ok[0]) x[q] = ld_stream(static_cast<const char*>(P[g * 8 + q]) + base);
+        uint4 v = tree_fold_regs<DT, OP, 8>(x);
+        for (int k = g; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[--top], v);
+        stk[top++] = v;
       }
-      acc[0] = tree_fold_regs<DT, OP, NR / 8>(part);
+      acc[0] = stk[0];
     }
 
     if (a.avg) {
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = div_vec<DT>(acc[u], a.fn);
     }
-    if (a.owner_only) {
-      char* dst = static_cast<char*>(const_cast<void*>(P[c]));
+    if (a.owner_only || a.to_root) {
+      char* dst = static_cast<char*>(const_cast<void*>(P[a.owner_only ? c : a.root])) + base;
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (ok[u]) st_stream(dst + off[u], acc[u]);
+        if (ok[u]) st_stream(dst + u * kStride, acc[u]);
     } else if constexpr (NR > 0) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+        char* dst = static_cast<char*>(const_cast<void*>(P[r])) + base;
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (ok[u]) st_stream(dst + off[u], acc[u]);
+          if (ok[u]) st_stream(dst + u * kStride, acc[u]);
       }
     } else {
       for (int r = 0; r < n; ++r) {
-        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+        char* dst = static_cast<char*>(const_cast<void*>(P[r])) + base;
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (ok[u]) st_stream(dst + off[u], acc[u]);
+          if (ok[u]) st_stream(dst + u * kStride, acc[u]);
       }
     }
 
@@ -157,8 +177,8 @@ __global__ void __launch_bounds__(kFusedBlock) fused_vec_kernel(const __grid_con
       const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
       uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, c, e) : fold_tree_scalar<DT, OP>(P, n, e);
       if (a.avg) r = div_word<DT>(r, a.fn);
-      if (a.owner_only) {
-        st_elem<ES>(const_cast<void*>(P[c]), e, r);
+      if (a.owner_only || a.to_root) {
+        st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
       } else {
         for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
       }
@@ -180,8 +200,8 @@ __global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_
     const void* const* P = T.ptr + (size_t)s.tensor * n;
     uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, s.chunk, e) : fold_tree_scalar<DT, OP>(P, n, e);
     if (a.avg) r = div_word<DT>(r, a.fn);
-    if (a.owner_only) {
-      st_elem<ES>(const_cast<void*>(P[s.chunk]), e, r);
+    if (a.owner_only || a.to_root) {
+      st_elem<ES>(const_cast<void*>(P[a.owner_only ? s.chunk : a.root]), e, r);
     } else {
       for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
     }
@@ -222,22 +242,22 @@ inline int blocks_per_sm(K kernel, int block) {
   return b;
 }
 
+inline unsigned grid_for(int64_t ntiles) { return (unsigned)(ntiles < kMaxGrid ? ntiles : kMaxGrid); }
+
 template <int DT, int OP, int ORDER, int NR>
 cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
   constexpr int U = fused_unroll(ORDER, NR);
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U) == 0) return cudaSuccess;
-  static const int bps = blocks_per_sm(fused_vec_kernel<DT, OP, ORDER, NR>, kFusedBlock);
-  const int64_t grid = a.tab.ntiles < (int64_t)bps * sm_count() ? a.tab.ntiles : (int64_t)bps * sm_count();
-  fused_vec_kernel<DT, OP, ORDER, NR><<<(unsigned)grid, kFusedBlock, 0, stream>>>(a);
+  fused_vec_kernel<DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 
 template <int DT, int OP, int ORDER>
 cudaError_t launch_fused_scalar(FusedArgs& a, cudaStream_t stream) {
   if (fill_tiles(a.tab, 1, kFusedBlock) == 0) return cudaSuccess;
-  static const int bps = blocks_per_sm(fused_scalar_kernel<DT, OP, ORDER>, kFusedBlock);
-  const int64_t grid = a.tab.ntiles < (int64_t)bps * sm_count() ? a.tab.ntiles : (int64_t)bps * sm_count();
-  fused_scalar_kernel<DT, OP, ORDER><<<(unsigned)grid, kFusedBlock, 0, stream>>>(a);
+  fused_scalar_kernel<DT, OP, ORDER><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  count_launch();
   return cudaGetLastError();
 }
 

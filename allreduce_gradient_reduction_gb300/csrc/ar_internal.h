@@ -46,6 +46,8 @@ struct FusedArgs {
   SegTable tab;
   int32_t avg;         // divide reduced values by nranks
   int32_t owner_only;  // ReduceScatter: store to the chunk owner only
+  int32_t to_root;     // Reduce: store to rank `root` only
+  int32_t root;
   float fn;            // (float)nranks
 };
 
@@ -76,5 +78,8 @@ cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
 
 int sm_count();
+
+// Counts every kernel launch the library enqueues (ar_kernel_launches).
+void count_launch();
 
 }  // namespace ar

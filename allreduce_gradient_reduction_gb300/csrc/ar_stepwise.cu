@@ -16,6 +16,7 @@ static cudaError_t launch_step_typed(StepArgs& a, cudaStream_t stream) {
   if (grid > widest) grid = widest;
   if (grid < 1) grid = 1;
   void* params[] = {&a};
+  count_launch();
   return cudaLaunchCooperativeKernel((const void*)stepwise_kernel<DT, OP, VECTOR>, dim3((unsigned)grid),
                                      dim3(kStepBlock), params, 0, stream);
 }

@@ -47,6 +47,12 @@ def parse():
     p.add_argument("--count", type=int, default=0,
                    help="elements per rank (default: the full workload); smaller counts are for profiling")
     p.add_argument("--variants", action="store_true", help="also time tree and step-wise orders (extra keys)")
+    p.add_argument("--workload", choices=["large", "bucket", "gpt2"], default="large",
+                   help="large: the headline (default); bucket: 8 x 25 MiB f32 AVG; gpt2: DDP buckets of GPT-2 small")
+    p.add_argument("--sweep", action="store_true",
+                   help="latency/bandwidth sweep (sizes x ranks x dtypes x ops x orders); points go to --sweep-out")
+    p.add_argument("--sweep-out", default="sweep.jsonl")
+    p.add_argument("--sweep-ranks", default="2,4,8,16,64")
     return p.parse_args()
 
 
@@ -230,6 +236,234 @@ def run_reference(args, ws, rank):
 
 
 # ---------------------------------------------------------------------------
+# latency / bandwidth sweep
+# ---------------------------------------------------------------------------
+
+def fit_alpha_beta(points, phases, bw_factor):
+    """Least-squares fit of t = A + B * D over (D bytes per rank, t seconds),
+    relative error weighting; returns alpha = A / phases (seconds per step)
+    and beta = B / bw_factor (seconds per byte), the page's alpha-beta model
+    T = phases * alpha + bw_factor * D * beta."""
+    import numpy as np
+    d = np.array([p[0] for p in points], dtype=np.float64)
+    t = np.array([p[1] for p in points], dtype=np.float64)
+    w = 1.0 / t
+    A = np.stack([np.ones_like(d), d], axis=1) * w[:, None]
+    (a, b), *_ = np.linalg.lstsq(A, t * w, rcond=None)
+    return a / phases, b / bw_factor
+
+
+def run_sweep(args, ws, rank, dev, torch, ar):
+    """Per-rank message 4 KiB .. 1 GiB x N in --sweep-ranks (N x size <= 64 GiB)
+    x {f32, bf16} x {SUM, MAX} x {ring, tree, ring_stepwise, tree_stepwise},
+    uniform(-1, 1) values.  Writes one JSON line per point to --sweep-out and
+    prints one summary line: the alpha-beta fit of every order per (N, dtype)
+    and the ring/tree crossover of the step-wise orders."""
+    import math
+    from allreduce_gradient_reduction_gb300 import workloads as W
+    stream = torch.cuda.current_stream()
+    sid = int(stream.cuda_stream)
+    ranks = [int(x) for x in args.sweep_ranks.split(",")]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(W.BASE_SEED + 1000 * W.CONFIG_SWEEP)
+    fits, crossover, npoints = {}, {}, 0
+    with open(args.sweep_out, "w") as out:
+        for n in ranks:
+            max_bytes = min(W.SWEEP_BYTES[-1], W.SWEEP_CAP_BYTES // n)
+            bufs = [torch.empty(max_bytes, dtype=torch.uint8, device=dev) for _ in range(n)]
+            for dt in ("f32", "bf16"):
+                es = 4 if dt == "f32" else 2
+                tdt = torch.float32 if dt == "f32" else torch.bfloat16
+                for b in bufs:
+                    b.view(tdt).uniform_(-1.0, 1.0, generator=gen)
+                curves = {}
+                for op in ("sum", "max"):
+                    for algo in ("ring", "tree", "ring_stepwise", "tree_stepwise"):
+                        if algo.startswith("tree") and n & (n - 1):
+                            continue
+                        for nbytes in W.SWEEP_BYTES:
+                            if nbytes > max_bytes:
+                                break
+                            count = nbytes // es
+                            views = [b[:nbytes] for b in bufs]
+                            call = lambda: ar.ar_allreduce(views, count=count, dtype=dt, op=op, algo=algo,
+                                                           stream=sid)
+                            for _ in range(3):
+                                ar.check(call(), "sweep")
+                            torch.cuda.synchronize()
+                            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            e0.record(stream)
+                            ar.check(call(), "sweep")
+                            e1.record(stream)
+                            torch.cuda.synchronize()
+                            est = e0.elapsed_time(e1)
+                            k = int(min(200, max(5, 30.0 / max(est, 1e-3))))
+                            e0.record(stream)
+                            for _ in range(k):
+                                call()
+                            e1.record(stream)
+                            torch.cuda.synchronize()
+                            t = e0.elapsed_time(e1) / k / 1e3
+                            rc, st = ar.ar_device_status(sid)
+                            ar.check(rc or st, "sweep status")
+                            rec = {"nranks": n, "bytes_per_rank": nbytes, "dtype": dt, "op": op, "algo": algo,
+                                   "us": t * 1e6, "effective_gbs": 2 * n * nbytes / t / 1e9,
+                                   "algbw_gbs": nbytes / t / 1e9, "l2_resident": 2 * n * nbytes <= 129e6}
+                            out.write(json.dumps(rec) + "\n")
+                            npoints += 1
+                            if op == "sum":
+                                curves.setdefault(algo, []).append((nbytes, t))
+                for algo, pts in curves.items():
+                    stepwise = algo.endswith("stepwise")
+                    steps = (2 * (n - 1) if algo.startswith("ring") else 2 * int(math.log2(n))) if stepwise else 1
+                    # per-rank traffic factor of the page's model: 2(N-1)/N D for ring and halving/doubling
+                    alpha, beta = fit_alpha_beta(pts, steps, 2 * (n - 1) / n)
+                    fits[f"N{n}_{dt}_{algo}"] = {"alpha_us": alpha * 1e6, "beta_ps_per_byte": beta * 1e12,
+                                                 "steps": steps}
+                if "ring_stepwise" in curves and "tree_stepwise" in curves:
+                    rs, ts = dict(curves["ring_stepwise"]), dict(curves["tree_stepwise"])
+                    cross = [d for d in sorted(rs) if rs[d] < ts.get(d, float("inf"))]
+                    # the page's model with a binomial tree (2 D beta) and the fitted ring alpha, beta
+                    f = fits[f"N{n}_{dt}_ring_stepwise"]
+                    model = (n - 1 - math.log2(n)) * n * (f["alpha_us"] * 1e-6) / (f["beta_ps_per_byte"] * 1e-12)
+                    crossover[f"N{n}_{dt}"] = {"measured_first_ring_win_bytes": cross[0] if cross else None,
+                                               "model_binomial_crossover_bytes": model}
+            del bufs
+            torch.cuda.empty_cache()
+    line = {"metric": METRIC + " (sweep)", "points": npoints, "points_file": args.sweep_out, "unit": "us",
+            "alpha_beta": fits, "ring_tree_crossover": crossover, "data": "synthetic uniform(-1,1)"}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# workloads of our arm: host inputs (pinned), device buffers, one step
+# ---------------------------------------------------------------------------
+
+class LargeWorkload:
+    """8 ranks x 67,108,864 bf16, ring SUM: the headline configuration."""
+    dtype, op = "bf16", "sum"
+
+    def __init__(self, args, dev, torch, np, W, ar):
+        self.ar, self.args = ar, args
+        self.n, self.count = W.LARGE["nranks"], (args.count or W.LARGE["count"])
+        self.bytes_step = 2 * self.n * self.count * 2
+        self.host = torch.empty((self.n, self.count), dtype=torch.int16, pin_memory=True)
+        for r in range(self.n):
+            self.host[r].copy_(torch.from_numpy(W.large_rank(r, self.count).view(np.int16)))
+        self.out = torch.empty_like(self.host, pin_memory=True)
+        self.bufs = [torch.empty(self.count, dtype=torch.int16, device=dev) for _ in range(self.n)]
+        self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
+        self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
+        self.workload = WORKLOAD
+        self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
+                       "l2": "inputs larger than L2 (2 GiB touched per step vs 129 MB L2)"}
+
+    def step(self, sid, algo):
+        rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo, stream=sid)
+        if rc:
+            raise self.ar.ArError(rc, "ar_allreduce")
+
+    def cpu_baseline(self):
+        sample = self.count // 4
+        dt, gbs = oracle_sample_time(self.n, sample)
+        return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{self.n} ranks x {sample} bf16 (1/4 of the workload), one literal ring pass, "
+                          f"{dt:.2f} s, one thread"}
+
+
+class BucketWorkload:
+    """8 ranks x 6,553,600 f32 (one 25 MiB DDP bucket), ring AVG."""
+    dtype, op = "f32", "avg"
+
+    def __init__(self, args, dev, torch, np, W, ar):
+        self.ar, self.args = ar, args
+        self.n, self.count = W.BUCKET["nranks"], (args.count or W.BUCKET["count"])
+        self.bytes_step = 2 * self.n * self.count * 4
+        x = W.bucket_inputs(self.n, self.count)
+        self.host = torch.from_numpy(x).pin_memory()
+        self.out = torch.empty_like(self.host, pin_memory=True)
+        self.bufs = [torch.empty(self.count, dtype=torch.float32, device=dev) for _ in range(self.n)]
+        self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
+        self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
+        self.workload = "ring AllReduce AVG, 8 ranks x 6,553,600 f32 (one 25 MiB DDP bucket)"
+        self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
+                       "l2": "409.6 MiB touched per step vs 129 MB L2 (partly L2-resident between steps)"}
+
+    def step(self, sid, algo):
+        rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo, stream=sid)
+        if rc:
+            raise self.ar.ArError(rc, "ar_allreduce")
+
+    def cpu_baseline(self):
+        import oracle
+        from allreduce_gradient_reduction_gb300 import workloads as W
+        oracle.build()
+        x = W.bucket_inputs(self.n, self.count)
+        t0 = time.perf_counter()
+        oracle.allreduce(x, algo="ring", op="avg", dtype="f32")
+        dt = time.perf_counter() - t0
+        return {"value": self.bytes_step / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"the whole workload, one literal ring pass, {dt:.2f} s, one thread"}
+
+
+class Gpt2Workload:
+    """GPT-2 small gradients (148 tensors, 124,439,808 f32 per rank), 8 ranks,
+    DDP buckets of 25 MiB in reverse order, AVG; each rank's gradients are
+    views into one flat allocation."""
+    dtype, op = "f32", "avg"
+
+    def __init__(self, args, dev, torch, np, W, ar):
+        self.ar, self.args = ar, args
+        self.n = W.GPT2["nranks"]
+        self.counts = W.gpt2_small_counts()
+        self.total = int(self.counts.sum())
+        self.bytes_step = 2 * self.n * self.total * 4
+        offs = np.concatenate([[0], np.cumsum(self.counts)])
+        self.host = torch.empty((self.n, self.total), dtype=torch.float32, pin_memory=True)
+        for r in range(self.n):
+            self.host[r].copy_(torch.from_numpy(np.concatenate(W.gpt2_rank_grads(r, self.counts))))
+        self.out = torch.empty_like(self.host, pin_memory=True)
+        self.flats = [torch.empty(self.total, dtype=torch.float32, device=dev) for _ in range(self.n)]
+        self.grads = [[f[offs[t]:offs[t + 1]] for t in range(len(self.counts))] for f in self.flats]
+        self.h2d = [(self.host[r], self.flats[r]) for r in range(self.n)]
+        self.d2h = [(self.flats[r], self.out[r]) for r in range(self.n)]
+        self.ws = None
+        self.workload = "DDP bucketed AllReduce AVG, 8 ranks x GPT-2 small gradients (124,439,808 f32, 25 MiB buckets)"
+        self.config = {"nranks": self.n, "params_per_rank": self.total, "tensors": len(self.counts),
+                       "bucket_cap_bytes": 25 << 20, "algo": args.algo, "op": self.op, "path": "fused",
+                       "l2": "inputs larger than L2 (8 GB touched per step)"}
+
+    def step(self, sid, algo, literal=False):
+        ws, wbytes = None, 0
+        if literal:
+            import torch
+            if self.ws is None:
+                self.ws = [torch.empty(self.total, dtype=torch.float32, device=self.flats[0].device)
+                           for _ in range(self.n)]
+            ws, wbytes = self.ws, self.total * 4
+        rc = self.ar.ar_bucketed_allreduce(self.grads, counts=self.counts, dtype=self.dtype, op=self.op, algo=algo,
+                                           workspace=ws, workspace_bytes=wbytes, stream=sid)
+        if rc:
+            raise self.ar.ArError(rc, "ar_bucketed_allreduce")
+
+    def cpu_baseline(self):
+        import oracle
+        from allreduce_gradient_reduction_gb300 import workloads as W
+        oracle.build()
+        counts = self.counts[-50:]  # the last four blocks and the final norm: the first buckets DDP reduces
+        grads = [W.gpt2_rank_grads(r, self.counts)[-50:] for r in range(self.n)]
+        t0 = time.perf_counter()
+        oracle.bucketed_allreduce(grads, op="avg", dtype="f32")
+        dt = time.perf_counter() - t0
+        nbytes = 2 * self.n * int(counts.sum()) * 4
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"last 50 of 148 tensors ({int(counts.sum())} params per rank), literal pack, "
+                          f"ring, unpack, {dt:.2f} s, one thread"}
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -253,24 +487,19 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    n, count = W.LARGE["nranks"], (args.count or W.LARGE["count"])
-    nbytes_step = 2 * n * count * 2  # every rank element read once, the result written once per rank
-
-    # inputs: generated on the host (seeded), pinned, uploaded once
-    host = torch.empty((n, count), dtype=torch.int16, pin_memory=True)
-    for r in range(n):
-        host[r].copy_(torch.from_numpy(W.large_rank(r, count).view(np.int16)))
-    bufs = [torch.empty(count, dtype=torch.int16, device=dev) for _ in range(n)]
-    for r in range(n):
-        bufs[r].copy_(host[r], non_blocking=True)
+    if args.sweep:
+        return run_sweep(args, ws, rank, dev, torch, ar)
+    wl = {"large": LargeWorkload, "bucket": BucketWorkload, "gpt2": Gpt2Workload}[args.workload](
+        args, dev, torch, np, W, ar)
+    for src, dst in wl.h2d:
+        dst.copy_(src, non_blocking=True)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     sid = int(stream.cuda_stream)
+    nbytes_step = wl.bytes_step
 
-    def step(algo=args.algo):
-        rc = ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo=algo, stream=sid)
-        if rc:
-            raise ar.ArError(rc, "ar_allreduce")
+    def step(algo=args.algo, **kw):
+        wl.step(sid, algo, **kw)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -281,6 +510,7 @@ def main():
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = ar.ar_kernel_launches()
     t_wall0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
@@ -288,6 +518,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    launches = ar.ar_kernel_launches() - launches0
     barrier(ws)
     ms_local = e0.elapsed_time(e1) / args.steps
     clocks.stop()
@@ -297,76 +528,77 @@ def main():
         raise ar.ArError(rc or status, "device status")
 
     value = ws * nbytes_step / (ms / 1e3) / 1e9
-    algbw = count * 2 / (ms / 1e3) / 1e9
+    algbw = nbytes_step / (2 * wl.n) / (ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
+    # one step is `launches / steps` kernels; the roofline is per step of the hot path
     achieved = nbytes_step / (ms_local / 1e3) / 1e9
 
     # end to end through the public call: pinned host -> device, AllReduce, device -> host
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        out_host = torch.empty((n, count), dtype=torch.int16, pin_memory=True)
-        for r in range(n):  # warm the copy path once
-            bufs[r].copy_(host[r], non_blocking=True)
+        for src, dst in wl.h2d:  # warm the copy path once
+            dst.copy_(src, non_blocking=True)
         step()
-        for r in range(n):
-            out_host[r].copy_(bufs[r], non_blocking=True)
+        for src, dst in wl.d2h:
+            dst.copy_(src, non_blocking=True)
         torch.cuda.synchronize()
         barrier(ws)
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(e2e_steps):
-            for r in range(n):
-                bufs[r].copy_(host[r], non_blocking=True)
+            for src, dst in wl.h2d:
+                dst.copy_(src, non_blocking=True)
             step()
-            for r in range(n):
-                out_host[r].copy_(bufs[r], non_blocking=True)
+            for src, dst in wl.d2h:
+                dst.copy_(src, non_blocking=True)
         f1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, ws)
+        io_bytes = sum(src.numel() * src.element_size() for src, _ in wl.h2d)
         e2e = {"value": ws * nbytes_step / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": n * count * 2, "d2h_bytes_per_step": n * count * 2, "steps": e2e_steps,
-               "ms_per_step": ms_e2e, "result_ranks_identical": bool(torch.equal(out_host[0], out_host[n - 1]))}
+               "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes, "steps": e2e_steps,
+               "ms_per_step": ms_e2e, "result_ranks_identical": bool(torch.equal(wl.out[0], wl.out[wl.n - 1]))}
 
     variants = {}
     if args.variants:
-        for algo in ("tree", "ring_stepwise", "tree_stepwise"):
+        todo = [(a, {}) for a in ("ring", "tree", "ring_stepwise", "tree_stepwise") if a != args.algo]
+        if isinstance(wl, Gpt2Workload):
+            todo += [("ring_literal", {"literal": True})]
+        for name, kw in todo:
+            algo = name.replace("_literal", "")
             for _ in range(3):
-                step(algo)
+                step(algo, **kw)
             torch.cuda.synchronize()
             v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             k = max(10, args.steps // 10)
             v0.record(stream)
             for _ in range(k):
-                step(algo)
+                step(algo, **kw)
             v1.record(stream)
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / k
-            variants[algo] = {"ms_per_step": vms, "effective_gbs": nbytes_step / (vms / 1e3) / 1e9}
+            variants[name] = {"ms_per_step": vms, "effective_gbs": nbytes_step / (vms / 1e3) / 1e9}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        sample = count // 4
-        dt, gbs = oracle_sample_time(n, sample)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} ranks x {sample} bf16 (1/4 of the workload), one literal ring pass, "
-                         f"{dt:.2f} s, one thread"}
+        cpu = wl.cpu_baseline()
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "nranks": n, "count_per_rank": count, "algo": args.algo,
-                       "op": "sum", "l2": "inputs larger than L2 (2 GiB touched per step vs 129 MB L2)",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.workload, **wl.config,
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "algbw_gbs": algbw * ws,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": profiled_traffic() if isinstance(wl, LargeWorkload) and not args.count else None,
                          "algorithmic_bytes_per_launch": nbytes_step},
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": launches,
             "clocks": clocks.summary(t_wall0, t_wall1),
             "cpu_baseline": cpu,
         }

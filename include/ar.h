@@ -50,6 +50,9 @@
  *         (x0 (+) x1), (x2 (+) x3), ... then pairs of pairs, lower ranks first;
  *         N must be a power of two (AR_ERR_UNSUPPORTED otherwise).
  *         [primer §四 4.1], [chapter §4.3].
+ *       AR_NAIVE (AllReduce and Reduce only): index order x[0], x[1], ...,
+ *         x[N-1], the order in which a central root folds the buffers it
+ *         gathers ("AllReduce 集合通信" §朴素实现与主节点瓶颈, tutorial §2.1).
  *     The fused algorithms make one pass over HBM (each element of each rank
  *     read once and written once); the step-wise ones execute the literal
  *     schedule, one grid-wide phase per communication step, in a single
@@ -72,7 +75,7 @@ typedef struct CUstream_st* ar_stream_t;
 
 typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2 } ar_dtype;
 typedef enum { AR_SUM = 0, AR_MAX = 1, AR_AVG = 2 } ar_op;
-typedef enum { AR_RING = 0, AR_RING_STEPWISE = 1, AR_TREE = 2, AR_TREE_STEPWISE = 3 } ar_algo;
+typedef enum { AR_RING = 0, AR_RING_STEPWISE = 1, AR_TREE = 2, AR_TREE_STEPWISE = 3, AR_NAIVE = 4 } ar_algo;
 
 typedef enum {
   AR_OK = 0,
@@ -123,6 +126,26 @@ int ar_reduce_scatter(void* const* bufs, int nranks, int64_t count, ar_dtype dty
 int ar_all_gather(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_algo algo, ar_stream_t stream);
 
 /*
+ * Reduce: afterwards bufs[root] holds the reduction of all N inputs (the
+ * order of `algo`: AR_RING, AR_TREE or AR_NAIVE); the other buffers are left
+ * unchanged.  [notes §语义] (Reduce: the result lands at the root only),
+ * [primer §二].  One pass: N reads and one write per element.
+ *   root   0 <= root < nranks (AR_ERR_INVALID_ARG otherwise)
+ * The step-wise orders are AR_ERR_UNSUPPORTED here.  Other arguments and
+ * errors as ar_allreduce.
+ */
+int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo, int root,
+              ar_stream_t stream);
+
+/*
+ * Broadcast: afterwards every buffer holds bufs[root], copied bit for bit.
+ * [notes §语义] (Broadcast: the root's data goes to every process),
+ * [primer §二].  One pass: one read and N-1 writes per element.
+ * Arguments and errors as ar_all_gather, plus root as in ar_reduce.
+ */
+int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, int root, ar_stream_t stream);
+
+/*
  * DDP bucket plan [tutorial §4.1], [notes §DDP 梯度同步中的地位]: walk the
  * tensors in reverse registration order; add each to the current bucket while
  * the bucket's bytes stay <= cap_bytes; a tensor that does not fit opens the
@@ -156,8 +179,8 @@ int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t 
  *               AllReduces, and unpacks.  workspace_bytes >= total bytes of
  *               all buckets packs everything at once; >= the largest bucket
  *               runs bucket by bucket; less is AR_ERR_INVALID_ARG.
- *   algo        any ar_algo; the step-wise ones run their schedule on every
- *               bucket at once.
+ *   algo        any ar_algo but AR_NAIVE; the step-wise ones run their
+ *               schedule on every bucket at once.
  * Both paths give bit-identical results.  Errors as ar_allreduce, plus
  * AR_ERR_TOO_LARGE if one tensor row (nranks pointers) cannot be described.
  */
@@ -231,6 +254,10 @@ int ar_last_cuda_error(void);
 
 /* Human-readable name of an ar_status value. */
 const char* ar_strerror(int status);
+
+/* Number of kernels this library has enqueued since it was loaded, on all
+ * devices and streams (for accounting launches inside a timed region). */
+int64_t ar_kernel_launches(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int ar_version(void);

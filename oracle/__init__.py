@@ -85,6 +85,9 @@ def lib():
                                         ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Stats),
                                         ctypes.POINTER(Fault)]
+        L.oracle_rooted.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int,
+                                    ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.POINTER(Stats)]
         L.oracle_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int64]
         L.oracle_f32_to_bf16.argtypes = [vp, vp, ctypes.c_int64]
         L.oracle_chunk_range.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -162,6 +165,37 @@ def reduce_scatter(x, **kw):
 
 def all_gather(x, **kw):
     return collective(x, phases=PHASE_AG, **kw)
+
+
+def _rooted(kind, x, *, algo="ring", op="sum", dtype="f32", root=0, count=None, positions=None,
+            raise_on_error=True):
+    xs = [_check(np.asarray(a), dtype) for a in x]
+    n = len(xs)
+    m = xs[0].shape[0] if n else 0
+    outs = [np.empty_like(a) for a in xs]
+    pos_arr = None
+    if positions is not None:
+        pos_arr = np.ascontiguousarray(positions, dtype=np.int64)
+    total = m if count is None else int(count)
+    st = Stats()
+    rc = lib().oracle_rooted(kind, ALGOS[algo], _ptrs(xs), _ptrs(outs), n, total,
+                             pos_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if pos_arr is not None else None,
+                             m, DTYPES[dtype], OPS[op], root, ctypes.byref(st))
+    stats = {"rc": rc, "steps": st.steps, "sent": np.array(st.sent[:n], dtype=np.int64),
+             "recv": np.array(st.recv[:n], dtype=np.int64)}
+    if rc != 0 and raise_on_error:
+        raise OracleError(rc, "rooted collective")
+    return np.stack(outs), stats
+
+
+def reduce(x, *, root=0, **kw):
+    """Reduce to `root` (ring, tree or naive order); only out[root] is the result."""
+    return _rooted(0, x, root=root, **kw)
+
+
+def broadcast(x, *, root=0, dtype="f32", **kw):
+    """Copy the root's buffer to every rank."""
+    return _rooted(1, x, root=root, dtype=dtype, **kw)
 
 
 def step(a, b, *, op="sum", dtype="f32"):

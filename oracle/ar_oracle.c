@@ -611,6 +611,146 @@ done:
 }
 
 /* ------------------------------------------------------------------------ */
+/* Reduce and Broadcast (the rest of the collectives table)                 */
+/* ------------------------------------------------------------------------ */
+
+/* Reduce: the reduction lands at `root` only ("AllReduce 集合通信" §语义:
+ * Reduce = reduce to the root; the other ranks' buffers are left as the
+ * schedule leaves them).  Ring / tree: ReduceScatter as in the AllReduce
+ * (AVG at the owners), then every owner r != root sends its finished chunk
+ * to the root, one message per step.  Naive: the root receives every other
+ * buffer and folds x_0, x_1, ..., x_{N-1} in index order. */
+static int reduce_to_root(sim* s, int algo, int root, int avg) {
+  int r, j, rc;
+  int all[OR_MAX_RANKS];
+  if (algo == OR_NAIVE) {
+    unsigned char* got[OR_MAX_RANKS] = {0};
+    for (j = 0; j < s->n; ++j) all[j] = j;
+    for (r = 0; r < s->n; ++r) {
+      message* mb;
+      if (r == root) continue;
+      if ((rc = post(s, r, root, all, s->n))) return rc;
+      if ((rc = take(s, root, r, all, s->n, &mb))) return rc;
+      got[r] = mb->data; /* keep the received copy; the box is emptied by hand */
+      s->box[root].data = NULL;
+      s->box[root].present = 0;
+      s->step++;
+      s->st->steps++;
+    }
+    got[root] = (unsigned char*)malloc((size_t)(s->m > 0 ? s->m : 1) * (size_t)s->es);
+    if (!got[root]) rc = OR_ENOMEM;
+    else {
+      memcpy(got[root], s->rank[root], (size_t)s->m * (size_t)s->es);
+      memcpy(s->rank[root], got[0], (size_t)s->m * (size_t)s->es);
+      for (r = 1; r < s->n; ++r) combine(s->dtype, s->op, s->rank[root], got[r], s->rank[root], s->m);
+      if (avg) divide_by(s->dtype, s->rank[root], s->m, s->n);
+      rc = OR_OK;
+    }
+    for (r = 0; r < s->n; ++r) free(got[r]);
+    return rc;
+  }
+  rc = algo == OR_RING ? ring_reduce_scatter(s) : tree_reduce_scatter(s);
+  if (rc) return rc;
+  if (avg)
+    for (r = 0; r < s->n; ++r) divide_by(s->dtype, chunk_ptr(s, r, r), chunk_len(s, r), s->n);
+  for (r = 0; r < s->n; ++r) {
+    message* mb;
+    if (r == root) continue;
+    if ((rc = post(s, r, root, &r, 1))) return rc;
+    if ((rc = take(s, root, r, &r, 1, &mb))) return rc;
+    memcpy(chunk_ptr(s, root, r), mb->data, (size_t)mb->n * (size_t)s->es);
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+/* Broadcast: the root's buffer is copied to every rank, one message per
+ * receiving rank ("AllReduce 集合通信" §语义; "【AI Infra小白入门⑩】" §二). */
+static int broadcast_from_root(sim* s, int root) {
+  int r, j, rc;
+  int all[OR_MAX_RANKS];
+  for (j = 0; j < s->n; ++j) all[j] = j;
+  for (r = 0; r < s->n; ++r) {
+    message* mb;
+    if (r == root) continue;
+    if ((rc = post(s, root, r, all, s->n))) return rc;
+    if ((rc = take(s, r, root, all, s->n, &mb))) return rc;
+    memcpy(s->rank[r], mb->data, (size_t)s->m * (size_t)s->es);
+    clear_boxes(s);
+    s->step++;
+    s->st->steps++;
+  }
+  return OR_OK;
+}
+
+enum { OR_KIND_REDUCE = 0, OR_KIND_BROADCAST = 1 };
+
+/*
+ * Rooted collectives.  kind OR_KIND_REDUCE (algo ring, tree or naive; op as
+ * for AllReduce) or OR_KIND_BROADCAST (algo and op ignored).  Other
+ * arguments as oracle_collective.  After a Reduce only out[root] is defined
+ * by the operation; the other outputs hold what the schedule left there.
+ */
+int oracle_rooted(int kind, int algo, const void* const* in, void* const* out, int nranks, int64_t count,
+                  const int64_t* positions, int64_t npos, int dtype, int op, int root, oracle_stats* st) {
+  sim* s;
+  int r, j, rc = OR_OK;
+  int64_t i, m;
+  oracle_stats local_st;
+  if (!st) st = &local_st;
+  memset(st, 0, sizeof(*st));
+  st->fail_step = -1;
+  st->fail_rank = -1;
+  if (nranks < 1 || nranks > OR_MAX_RANKS || count < 0 || !in || !out || root < 0 || root >= nranks) return OR_EINVAL;
+  if (dtype < 0 || dtype > 2 || kind < 0 || kind > 1) return OR_EINVAL;
+  if (kind == OR_KIND_REDUCE) {
+    if (op < 0 || op > 2 || (algo != OR_RING && algo != OR_TREE && algo != OR_NAIVE)) return OR_EINVAL;
+    if (op == OR_AVG && dtype == OR_I32) return OR_EUNSUPPORTED;
+    if (algo == OR_TREE && log2_exact(nranks) < 0) return OR_EUNSUPPORTED;
+  }
+  m = positions ? npos : count;
+  if (positions)
+    for (i = 0; i < npos; ++i)
+      if (positions[i] < 0 || positions[i] >= count || (i > 0 && positions[i] <= positions[i - 1])) return OR_EINVAL;
+  s = (sim*)calloc(1, sizeof(sim));
+  if (!s) return OR_ENOMEM;
+  s->n = nranks;
+  s->dtype = dtype;
+  s->op = op == OR_MAX ? OR_MAX : OR_SUM;
+  s->es = esize_of(dtype);
+  s->m = m;
+  s->st = st;
+  for (j = 0; j <= nranks; ++j) {
+    int64_t lo = (int64_t)(((__int128)j * count) / nranks);
+    if (!positions) {
+      s->klo[j] = lo;
+    } else {
+      int64_t k = 0;
+      while (k < npos && positions[k] < lo) ++k;
+      s->klo[j] = k;
+    }
+  }
+  for (r = 0; r < nranks; ++r) {
+    s->rank[r] = (unsigned char*)malloc((size_t)(m > 0 ? m : 1) * (size_t)s->es);
+    if (!s->rank[r]) {
+      rc = OR_ENOMEM;
+      goto done;
+    }
+    memcpy(s->rank[r], in[r], (size_t)m * (size_t)s->es);
+  }
+  rc = kind == OR_KIND_REDUCE ? reduce_to_root(s, algo, root, op == OR_AVG) : broadcast_from_root(s, root);
+  if (rc) goto done;
+  for (r = 0; r < nranks; ++r) memcpy(out[r], s->rank[r], (size_t)m * (size_t)s->es);
+done:
+  clear_boxes(s);
+  for (r = 0; r < nranks; ++r) free(s->rank[r]);
+  free(s);
+  return rc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* DDP buckets                                                              */
 /* ------------------------------------------------------------------------ */
 

@@ -424,3 +424,57 @@ def test_barrier_timeout_is_reported(ar, algo):
     finally:
         ar.ar_debug_skip_barrier(-1)
         ar.ar_set_barrier_timeout_ns(0)
+
+
+# --------------------------------------------------------------------------
+# Reduce, Broadcast and the naive (index) order
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("algo", ["ring", "tree", "naive"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_reduce_matches_oracle(ar, algo, dtype):
+    for n in (2, 3, 5, 8, 16):
+        if algo == "tree" and n & (n - 1):
+            continue
+        for count in (1, n + 1, 4099, 2 * 2048 * n + 9):
+            x = inputs(n, count, dtype, "bits" if count % 2 else "values", seed=900 + n + count)
+            for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+                for root in sorted({0, n - 1, n // 2}):
+                    with np.errstate(all="ignore"):
+                        want, _ = oracle.reduce(x, algo=algo, op=op, dtype=dtype, root=root)
+                    bufs = [to_dev(x[r]) for r in range(n)]
+                    ar.check(ar.ar_reduce(bufs, count=count, dtype=dtype, op=op, algo=algo, root=root), "reduce")
+                    got = from_dev(bufs, dtype)
+                    assert_same(got[root], want[root], dtype, f"{algo} {op} n={n} count={count} root={root}")
+                    others = [r for r in range(n) if r != root]
+                    assert np.array_equal(got[others].view(np.uint8), x[others].view(np.uint8))  # untouched
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_naive_allreduce_matches_oracle(ar, dtype):
+    for n in (2, 3, 8, 64):
+        for count in (1, 4099, 70_001):
+            x = inputs(n, count, dtype, "values", seed=1300 + n + count)
+            for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+                want, _ = oracle.allreduce(x, algo="naive", op=op, dtype=dtype)
+                got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo="naive")
+                assert_same(got, want, dtype, f"naive {op} n={n} count={count}")
+    x = inputs(4, 100, dtype, "values", seed=5)
+    bufs = [to_dev(x[r]) for r in range(4)]
+    assert ar.ar_reduce_scatter(bufs, count=100, dtype=dtype, algo="naive") == ar.AR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_broadcast_copies_bits(ar, dtype):
+    for n in (2, 3, 8, 16):
+        for count in (1, 4099, 3 * 2048 + 7):
+            x = W.random_bits(n, count, dtype, seed=1700 + n + count)
+            for root in sorted({0, n - 1, 1}):
+                want, _ = oracle.broadcast(x, root=root, dtype=dtype)
+                bufs = [to_dev(x[r]) for r in range(n)]
+                ar.check(ar.ar_broadcast(bufs, count=count, dtype=dtype, root=root), "broadcast")
+                got = from_dev(bufs, dtype)
+                assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), (n, count, root)
+    bufs = [to_dev(np.zeros(4, np.float32)) for _ in range(2)]
+    assert ar.ar_broadcast(bufs, count=4, root=2) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_reduce(bufs, count=4, root=-1) == ar.AR_ERR_INVALID_ARG

@@ -687,3 +687,61 @@ def test_departed_rank_is_detected(oracle_lib):
         assert st["rc"] == oracle.ERR_MISSING and st["fail_step"] == 3, algo
     _, st = oracle.allreduce(x, algo="ring", dtype="f32", fault=(2, 5, 100), raise_on_error=False)
     assert st["rc"] == 0  # leaving after the last step harms nobody
+
+
+# --------------------------------------------------------------------------
+# Reduce and Broadcast: AllReduce = Reduce + Broadcast ("AllReduce 集合通信", §语义)
+# --------------------------------------------------------------------------
+
+def naive_closed_form(x, dtype):
+    """Index order x_0, x_1, ..., x_{N-1}, folded with library additions."""
+    add = _lib_add(dtype)
+    acc = x[0].copy()
+    for r in range(1, x.shape[0]):
+        acc = add(acc, x[r])
+    return acc
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("n", [2, 3, 4, 8])
+def test_reduce_then_broadcast_is_allreduce(oracle_lib, dtype, n):
+    for count in (1, n + 1, 517):
+        x = W.random_bits(n, count, dtype, seed=400 + n + count)
+        for algo in ["ring", "naive"] + (["tree"] if n & (n - 1) == 0 else []):
+            for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+                for root in {0, n - 1, n // 2}:
+                    with np.errstate(all="ignore"):
+                        ar, _ = oracle.allreduce(x, algo=algo, op=op, dtype=dtype)
+                        red, _ = oracle.reduce(x, algo=algo, op=op, dtype=dtype, root=root)
+                        bc, _ = oracle.broadcast(red, root=root, dtype=dtype)
+                    assert _same(red[root], ar[0], dtype), (algo, op, root)
+                    assert _same(bc, ar, dtype), (algo, op, root)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_naive_order_closed_form(oracle_lib, dtype):
+    n, count = 5, 300
+    x = W.uniform_inputs(n, count, dtype, config=77) if dtype == "bf16" else W.normal_inputs(n, count, 1.0, 77)
+    for root in (0, 3):
+        red, _ = oracle.reduce(x, algo="naive", op="sum", dtype=dtype, root=root)
+        assert np.array_equal(red[root], naive_closed_form(x, dtype))
+    ar, _ = oracle.allreduce(x, algo="naive", op="sum", dtype=dtype)
+    assert np.array_equal(ar[1], naive_closed_form(x, dtype))
+
+
+def test_broadcast_copies_bits_and_volume(oracle_lib):
+    n, count = 6, 33
+    x = W.random_bits(n, count, "f32", seed=3)
+    out, st = oracle.broadcast(x, root=2, dtype="f32")
+    assert np.array_equal(out.view(np.uint32), np.broadcast_to(x[2].view(np.uint32), out.shape))
+    assert st["sent"][2] == (n - 1) * count and st["steps"] == n - 1
+
+
+def test_reduce_root_volume(oracle_lib):
+    n, count = 8, 64 * 8
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.reduce(x, algo="naive", root=3)
+    assert st["recv"][3] == (n - 1) * count
+    _, st = oracle.reduce(x, algo="ring", root=3)
+    # ReduceScatter (N-1)/N D per rank, then the N-1 foreign chunks to the root
+    assert st["recv"][3] == (n - 1) * count // n + (n - 1) * count // n
