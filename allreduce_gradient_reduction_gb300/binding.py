@@ -30,7 +30,8 @@ DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_bucket_plan",
            "ar_bucketed_allreduce",
            "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
-           "ar_last_cuda_error", "ar_strerror", "ar_version", "ar_kernel_launches")
+           "ar_last_cuda_error", "ar_strerror", "ar_version", "ar_kernel_launches", "ar_reducer_create",
+           "ar_reducer_mark_ready", "ar_reducer_finish", "ar_reducer_destroy", "ar_reducer_buckets")
 
 
 class ArError(RuntimeError):
@@ -65,6 +66,12 @@ def _load():
     L.ar_strerror.restype = ctypes.c_char_p
     L.ar_version.argtypes = []
     L.ar_kernel_launches.argtypes = []
+    L.ar_reducer_create.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, vp,
+                                    ctypes.POINTER(vp)]
+    L.ar_reducer_mark_ready.argtypes = [vp, cint, vp]
+    L.ar_reducer_finish.argtypes = [vp, vp]
+    L.ar_reducer_destroy.argtypes = [vp]
+    L.ar_reducer_buckets.argtypes = [vp]
     for name in EXPORTS:
         if name != "ar_strerror":
             getattr(L, name).restype = cint
@@ -193,6 +200,47 @@ def ar_bucketed_allreduce_noalloc(grads, counts=None, ntensors=None, nranks=None
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
 NOALLOC_MAX_TENSORS = 1024
+
+
+class Reducer:
+    """Overlapped bucket reduction (ar_reducer_*): create once over the
+    gradient tensors, then per iteration ``mark_ready(t, stream)`` for every
+    tensor as its gradients are produced and ``finish(stream)``."""
+
+    def __init__(self, grads, counts=None, dtype="f32", op="avg", algo="ring",
+                 bucket_cap_bytes=DEFAULT_BUCKET_CAP_BYTES, comm_stream=None):
+        nr, nt = len(grads), len(grads[0])
+        flat = [g for row in grads for g in row]
+        if counts is None:
+            counts = [int(g.numel()) for g in grads[0]]
+        c = (ctypes.c_int64 * max(nt, 1))(*[int(x) for x in counts])
+        h = ctypes.c_void_p()
+        check(lib.ar_reducer_create(_ptr_array(flat), c, nt, nr, _enum(DTYPE, dtype), _enum(OP, op),
+                                    _enum(ALGO, algo), int(bucket_cap_bytes), _stream(comm_stream), ctypes.byref(h)),
+              "ar_reducer_create")
+        self.handle = h
+        self.ntensors = nt
+
+    @property
+    def buckets(self) -> int:
+        return lib.ar_reducer_buckets(self.handle)
+
+    def mark_ready(self, tensor: int, stream=None) -> int:
+        return lib.ar_reducer_mark_ready(self.handle, int(tensor), _stream(stream))
+
+    def finish(self, stream=None) -> int:
+        return lib.ar_reducer_finish(self.handle, _stream(stream))
+
+    def close(self):
+        if self.handle:
+            lib.ar_reducer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def ar_chunk_range(count, nranks, c):

@@ -268,6 +268,29 @@ int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, 
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
 }
 
+// Rows of the fused bucketed AllReduce for the tensors `keep(t)` selects: each
+// tensor is cut at its bucket's chunk boundaries, and each piece is folded in
+// the order its bucket position implies (as if the bucket had been packed).
+// Returns whether every row is 16-byte aligned.
+template <typename Keep>
+bool add_bucket_rows(TableBuilder& tb, void* const* grads, const int64_t* counts, int ntensors, int nranks,
+                     const int32_t* bucket_of, const int64_t* offset, const int64_t* bcount, Keep keep) {
+  bool vec = true;
+  std::vector<void*> row(nranks);
+  for (int t = 0; t < ntensors; ++t) {
+    if (counts[t] == 0 || !keep(t)) continue;
+    for (int r = 0; r < nranks; ++r) row[r] = grads[(size_t)r * ntensors + t];
+    vec = vec && all_aligned16(row.data(), nranks);
+    const int rw = tb.add_row(row.data());
+    const int64_t B = bcount[bucket_of[t]], o = offset[t];
+    for (int c = 0; c < nranks; ++c) {
+      const int64_t lo = std::max(chunk_lo(B, nranks, c), o), hi = std::min(chunk_lo(B, nranks, c + 1), o + counts[t]);
+      tb.add_seg(rw, lo - o, hi - o, c);
+    }
+  }
+  return vec;
+}
+
 int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, int32_t* bucket_of, int64_t* offset,
                  int64_t* bcount, int32_t* nb) {
   const int es = esize_of(dtype);
@@ -299,6 +322,48 @@ int note_cuda_failure(cudaError_t e) { return cuda_fail(e); }
 std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace ar
+
+// ---- overlapped bucket reduction (DDP's reducer) --------------------------------
+//
+// DDP does not wait for the whole backward pass: as soon as every gradient of
+// a bucket is ready it starts that bucket's AllReduce asynchronously, so the
+// communication overlaps the rest of the backward computation, and it starts
+// buckets in bucket order ("Allreduce：..." §4.1 通信与计算重叠; "AllReduce 集合
+// 通信" §DDP 梯度同步中的地位).  Here the compute work runs on the caller's
+// compute stream and the bucket reductions on a communication stream; an event
+// recorded when a bucket becomes ready orders the two.
+
+struct ar_reducer {
+  int nranks = 0, ntensors = 0, nbuckets = 0;
+  Job job{};
+  cudaStream_t comm = nullptr;
+  std::vector<int32_t> bucket_of;
+  std::vector<int> left;           // per bucket: tensors not yet marked this iteration
+  std::vector<char> ready;         // per tensor
+  std::vector<std::vector<SegTable>> tables;  // per bucket: launch tables, built once
+  std::vector<cudaEvent_t> ready_ev;          // per bucket
+  cudaEvent_t done_ev = nullptr;
+  int next = 0;                    // next bucket to start (buckets start in order)
+  int64_t ntables = 0;
+};
+
+namespace {
+
+void reducer_reset(ar_reducer* red) {
+  std::fill(red->ready.begin(), red->ready.end(), 0);
+  std::fill(red->left.begin(), red->left.end(), 0);
+  for (int t = 0; t < red->ntensors; ++t) red->left[red->bucket_of[t]]++;
+  red->next = 0;
+}
+
+void reducer_free(ar_reducer* red) {
+  for (cudaEvent_t e : red->ready_ev)
+    if (e) cudaEventDestroy(e);
+  if (red->done_ev) cudaEventDestroy(red->done_ev);
+  delete red;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -387,21 +452,10 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
   };
 
   if (!workspace) {
-    // Fused: every tensor is cut at its bucket's chunk boundaries; each piece
-    // is folded in the order its bucket position implies.
+    // Fused: no packing; one pass reads and writes every gradient element once.
     TableBuilder tb{nranks, {}, {}};
-    bool vec = true;
-    for (int t = 0; t < ntensors; ++t) {
-      if (counts[t] == 0) continue;
-      void** rp = tensor_row(t);
-      vec = vec && all_aligned16(rp, nranks);
-      const int rw = tb.add_row(rp);
-      const int64_t B = bcount[bucket_of[t]], o = offset[t];
-      for (int c = 0; c < nranks; ++c) {
-        const int64_t lo = std::max(chunk_lo(B, nranks, c), o), hi = std::min(chunk_lo(B, nranks, c + 1), o + counts[t]);
-        tb.add_seg(rw, lo - o, hi - o, c);
-      }
-    }
+    const bool vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, bucket_of.data(), offset.data(),
+                                     bcount.data(), [](int) { return true; });
     Job j{dtype, op, algo, 3, avg, vec};
     return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
   }
@@ -480,6 +534,110 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
     if ((rc = run_buckets(b, b + 1))) return rc;
   return AR_OK;
 }
+
+int ar_reducer_create(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype, ar_op op,
+                      ar_algo algo, int64_t bucket_cap_bytes, ar_stream_t comm_stream, ar_reducer** out) {
+  if (!out) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_common(nranks, 0, dtype, op, algo);
+  if (rc) return rc;
+  if (algo == AR_NAIVE) return AR_ERR_UNSUPPORTED;
+  if (ntensors < 1 || bucket_cap_bytes <= 0 || !grads || !counts) return AR_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  ar_reducer* red = new ar_reducer;
+  red->nranks = nranks;
+  red->ntensors = ntensors;
+  red->comm = (cudaStream_t)comm_stream;
+  red->bucket_of.resize(ntensors);
+  std::vector<int64_t> offset(ntensors), bcount(ntensors);
+  int32_t nb = 0;
+  if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, red->bucket_of.data(), offset.data(),
+                         bcount.data(), &nb))) {
+    reducer_free(red);
+    return rc;
+  }
+  {
+    std::vector<Range> rs;
+    for (int r = 0; r < nranks; ++r)
+      for (int t = 0; t < ntensors; ++t) {
+        if (counts[t] == 0) continue;
+        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+        rs.push_back({p, p + (uintptr_t)counts[t] * es});
+      }
+    if ((rc = check_ranges(rs, es))) {
+      reducer_free(red);
+      return rc;
+    }
+  }
+  red->nbuckets = nb;
+  red->left.resize(nb);
+  red->ready.resize(ntensors);
+  red->tables.resize(nb);
+  red->ready_ev.assign(nb, nullptr);
+  bool vec = true;
+  for (int b = 0; b < nb && nranks > 1; ++b) {
+    TableBuilder tb{nranks, {}, {}};
+    vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, red->bucket_of.data(), offset.data(), bcount.data(),
+                          [&](int t) { return red->bucket_of[t] == b; }) && vec;
+    rc = tb.for_each_table([&](SegTable& t) {
+      red->tables[b].push_back(t);
+      return AR_OK;
+    });
+    if (rc) {
+      reducer_free(red);
+      return rc;
+    }
+    red->ntables += (int64_t)red->tables[b].size();
+  }
+  red->job = Job{dtype, op, algo, 3, op == AR_AVG, vec};
+  cudaError_t e = cudaSuccess;
+  for (int b = 0; b < nb && e == cudaSuccess; ++b) e = cudaEventCreateWithFlags(&red->ready_ev[b], cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&red->done_ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    reducer_free(red);
+    return cuda_fail(e);
+  }
+  reducer_reset(red);
+  *out = red;
+  return AR_OK;
+}
+
+int ar_reducer_mark_ready(ar_reducer* red, int tensor, ar_stream_t compute_stream) {
+  if (!red || tensor < 0 || tensor >= red->ntensors || red->ready[tensor]) return AR_ERR_INVALID_ARG;
+  red->ready[tensor] = 1;
+  const int b = red->bucket_of[tensor];
+  cudaError_t e;
+  if (--red->left[b] == 0 && (e = cudaEventRecord(red->ready_ev[b], (cudaStream_t)compute_stream)) != cudaSuccess)
+    return cuda_fail(e);
+  // start every bucket whose turn has come
+  while (red->next < red->nbuckets && red->left[red->next] == 0) {
+    const int nb = red->next++;
+    if ((e = cudaStreamWaitEvent(red->comm, red->ready_ev[nb], 0)) != cudaSuccess) return cuda_fail(e);
+    for (SegTable& t : red->tables[nb]) {
+      int rc = run_table(red->job, t, red->comm);
+      if (rc) return rc;
+    }
+  }
+  return AR_OK;
+}
+
+int ar_reducer_finish(ar_reducer* red, ar_stream_t compute_stream) {
+  if (!red) return AR_ERR_INVALID_ARG;
+  if (red->next < red->nbuckets) return AR_ERR_INVALID_ARG;  // some gradient was never marked ready
+  cudaError_t e;
+  if ((e = cudaEventRecord(red->done_ev, red->comm)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent((cudaStream_t)compute_stream, red->done_ev, 0)) != cudaSuccess) return cuda_fail(e);
+  reducer_reset(red);
+  return AR_OK;
+}
+
+int ar_reducer_destroy(ar_reducer* red) {
+  if (!red) return AR_ERR_INVALID_ARG;
+  reducer_free(red);
+  return AR_OK;
+}
+
+int ar_reducer_buckets(const ar_reducer* red) { return red ? red->nbuckets : AR_ERR_INVALID_ARG; }
 
 int ar_device_status(ar_stream_t stream, int* status) {
   if (!status) return AR_ERR_INVALID_ARG;

@@ -53,6 +53,9 @@ def parse():
                    help="latency/bandwidth sweep (sizes x ranks x dtypes x ops x orders); points go to --sweep-out")
     p.add_argument("--sweep-out", default="sweep.jsonl")
     p.add_argument("--sweep-ranks", default="2,4,8,16,64")
+    p.add_argument("--overlap", action="store_true",
+                   help="gpt2 workload: also time a synthetic backward with and without overlapped bucket reduction")
+    p.add_argument("--overlap-tokens", type=int, default=256)
     return p.parse_args()
 
 
@@ -448,6 +451,68 @@ class Gpt2Workload:
         if rc:
             raise self.ar.ArError(rc, "ar_bucketed_allreduce")
 
+    def overlap(self, sid, tokens, iters=5):
+        """Synthetic backward: for every tensor in reverse registration order and
+        every rank, a GEMM of the shape of its weight gradient (dW = X^T dY over
+        `tokens` tokens; a column sum for vectors) writes the gradient on the
+        compute stream.  Times the backward alone, backward then the bucketed
+        AllReduce, and backward with the reducer starting each bucket as soon
+        as its gradients exist (DDP's overlap)."""
+        import torch
+        shapes = [s for _, s in __import__("allreduce_gradient_reduction_gb300.workloads",
+                                           fromlist=["x"]).gpt2_small_shapes()]
+        dev = self.flats[0].device
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        amax = max(s[0] for s in shapes if len(s) == 2)
+        bmax = max(s[-1] for s in shapes)
+        X = [torch.randn(tokens, amax, device=dev, generator=gen) * 1e-2 for _ in range(self.n)]
+        Y = [torch.randn(tokens, bmax, device=dev, generator=gen) * 1e-2 for _ in range(self.n)]
+        compute = torch.cuda.current_stream()
+        comm = torch.cuda.Stream()
+        red = self.ar.Reducer(self.grads, counts=self.counts, dtype=self.dtype, op=self.op, algo="ring",
+                              comm_stream=comm)
+
+        def backward(mark=None):
+            for t in range(len(shapes) - 1, -1, -1):
+                shp = shapes[t]
+                for r in range(self.n):
+                    g = self.grads[r][t]
+                    if len(shp) == 2:
+                        torch.mm(X[r][:, :shp[0]].t(), Y[r][:, :shp[1]], out=g.view(shp))
+                    else:
+                        torch.sum(Y[r][:, :shp[0]], 0, out=g)
+                if mark:
+                    mark(t)
+
+        def timed(fn):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(compute)
+            for _ in range(iters):
+                fn()
+            e1.record(compute)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / iters
+
+        def seq():
+            backward()
+            self.step(sid, "ring")
+
+        def ovl():
+            backward(lambda t: self.ar.check(red.mark_ready(t, compute), "mark_ready"))
+            self.ar.check(red.finish(compute), "finish")
+
+        t_bwd, t_seq, t_ovl = timed(backward), timed(seq), timed(ovl)
+        nbuckets = red.buckets
+        red.close()
+        t_ar = t_seq - t_bwd
+        return {"tokens": tokens, "backward_ms": t_bwd, "sequential_ms": t_seq, "overlapped_ms": t_ovl,
+                "allreduce_ms_in_sequence": t_ar, "exposed_comm_ms": t_ovl - t_bwd,
+                "hidden_fraction": (t_seq - t_ovl) / t_ar if t_ar > 0 else None, "buckets": nbuckets,
+                "note": "backward = per-rank f32 GEMMs on the compute stream; both streams share one GPU"}
+
     def cpu_baseline(self):
         import oracle
         from allreduce_gradient_reduction_gb300 import workloads as W
@@ -581,6 +646,10 @@ def main():
             vms = v0.elapsed_time(v1) / k
             variants[name] = {"ms_per_step": vms, "effective_gbs": nbytes_step / (vms / 1e3) / 1e9}
 
+    overlap = None
+    if args.overlap and isinstance(wl, Gpt2Workload):
+        overlap = wl.overlap(sid, args.overlap_tokens)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = wl.cpu_baseline()
@@ -604,6 +673,8 @@ def main():
         }
         if variants:
             line["variants"] = variants
+        if overlap:
+            line["overlap"] = overlap
         print(json.dumps(line))
     if ws > 1:
         import torch.distributed as dist

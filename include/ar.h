@@ -225,6 +225,41 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
 int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype,
                                   ar_op op, ar_algo algo, int64_t bucket_cap_bytes, ar_stream_t stream);
 
+/*
+ * Overlapped bucket reduction, the way DDP's reducer runs it: a bucket's
+ * AllReduce starts as soon as all of its gradients are ready, while the rest
+ * of the backward pass is still computing, and buckets start in bucket order.
+ * [tutorial §4.1 通信与计算重叠], [notes §DDP 梯度同步中的地位].
+ *
+ *   ar_reducer_create   plans the buckets of `grads` (as ar_bucketed_allreduce,
+ *                       fused path) and builds their launch tables once.
+ *                       comm_stream carries every bucket reduction.
+ *                       Arguments as ar_bucketed_allreduce (no workspace;
+ *                       AR_NAIVE is AR_ERR_UNSUPPORTED).  *out receives the
+ *                       handle; it allocates host memory and CUDA events only.
+ *   ar_reducer_mark_ready  tensor t's gradients (on every rank) have been
+ *                       produced by the work enqueued so far on
+ *                       compute_stream.  When this completes a bucket, an
+ *                       event is recorded on compute_stream; every bucket
+ *                       whose predecessors have all started is then enqueued
+ *                       on comm_stream behind that event.  Marking a tensor
+ *                       twice in one iteration is AR_ERR_INVALID_ARG.
+ *   ar_reducer_finish   makes compute_stream wait for the iteration's
+ *                       reductions and resets for the next iteration.
+ *                       AR_ERR_INVALID_ARG if some tensor was never marked.
+ *   ar_reducer_destroy  releases the handle (after the streams are idle).
+ * Results are bit-identical to ar_bucketed_allreduce with the same arguments.
+ * A handle is used from one host thread at a time.
+ */
+typedef struct ar_reducer ar_reducer;
+int ar_reducer_create(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype, ar_op op,
+                      ar_algo algo, int64_t bucket_cap_bytes, ar_stream_t comm_stream, ar_reducer** out);
+int ar_reducer_mark_ready(ar_reducer* red, int tensor, ar_stream_t compute_stream);
+int ar_reducer_finish(ar_reducer* red, ar_stream_t compute_stream);
+int ar_reducer_destroy(ar_reducer* red);
+/* Number of buckets of a reducer (or AR_ERR_INVALID_ARG for NULL). */
+int ar_reducer_buckets(const ar_reducer* red);
+
 /* Chunk c of a rank buffer of `count` elements split N ways: [*lo, *hi).
  * Host-only; errors: AR_ERR_INVALID_ARG. */
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);
