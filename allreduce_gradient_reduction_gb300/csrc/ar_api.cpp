@@ -95,7 +95,7 @@ int check_ranges(std::vector<Range>& rs, int esize) {
 int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
   if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0) return AR_ERR_INVALID_ARG;
   if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
-  if (algo < AR_RING || algo > AR_NAIVE) return AR_ERR_INVALID_ARG;
+  if (algo < AR_RING || algo > AR_DBTREE) return AR_ERR_INVALID_ARG;
   if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
   if ((algo == AR_TREE || algo == AR_TREE_STEPWISE) && !is_pow2(nranks)) return AR_ERR_UNSUPPORTED;
   return AR_OK;
@@ -153,7 +153,8 @@ struct Job {
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   const int dop = j.op == AR_MAX ? ar::MAX : ar::SUM;
   const bool stepwise = j.algo == AR_RING_STEPWISE || j.algo == AR_TREE_STEPWISE;
-  const int order = (j.algo == AR_TREE || j.algo == AR_TREE_STEPWISE) ? ar::TREE : ar::RING;
+  const int order = j.algo == AR_DBTREE ? ar::DBTREE
+                    : (j.algo == AR_TREE || j.algo == AR_TREE_STEPWISE) ? ar::TREE : ar::RING;
   cudaError_t e;
   if (stepwise) {
     ar::SyncBlock* sb = nullptr;
@@ -252,7 +253,8 @@ int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, 
                cudaStream_t stream, int root = -1) {
   int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
   if (rc) return rc;
-  if (algo == AR_NAIVE && phases != 3) return AR_ERR_UNSUPPORTED;  // no naive ReduceScatter / AllGather
+  if ((algo == AR_NAIVE || algo == AR_DBTREE) && phases != 3) return AR_ERR_UNSUPPORTED;  // AllReduce / Reduce only
+  if (algo == AR_DBTREE && root >= 0) return AR_ERR_UNSUPPORTED;
   if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
   if (count == 0 || nranks == 1) return AR_OK;
   TableBuilder tb{nranks, {}, {}};
@@ -260,10 +262,14 @@ int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, 
   if (algo == AR_NAIVE) {
     // index order x[0], x[1], ..., x[N-1] is the ring order of chunk N-1
     tb.add_seg(row, 0, count, nranks - 1);
+  } else if (algo == AR_DBTREE) {
+    // tree A reduces the first half (chunk id 0), tree B the second (1)
+    tb.add_seg(row, 0, count / 2, 0);
+    tb.add_seg(row, count / 2, count, 1);
   } else {
     for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
   }
-  Job j{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};
+  Job j{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};  // naive = ring kernel
   j.root = root;
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
 }
@@ -421,7 +427,7 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
   cudaStream_t stream = (cudaStream_t)stream_;
   int rc = check_common(nranks, 0, dtype, op, algo);
   if (rc) return rc;
-  if (algo == AR_NAIVE) return AR_ERR_UNSUPPORTED;
+  if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
   if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
   if (ntensors == 0) return AR_OK;
   if (!grads || !counts) return AR_ERR_INVALID_ARG;
@@ -541,7 +547,7 @@ int ar_reducer_create(void* const* grads, const int64_t* counts, int ntensors, i
   *out = nullptr;
   int rc = check_common(nranks, 0, dtype, op, algo);
   if (rc) return rc;
-  if (algo == AR_NAIVE) return AR_ERR_UNSUPPORTED;
+  if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
   if (ntensors < 1 || bucket_cap_bytes <= 0 || !grads || !counts) return AR_ERR_INVALID_ARG;
   const int es = esize_of(dtype);
   ar_reducer* red = new ar_reducer;

@@ -185,4 +185,41 @@ __device__ uint32_t fold_tree_scalar(const void* const* P, int n, int64_t e) {
   return stack[0];
 }
 
+// Double binary tree: positions 1..N form an in-order binary tree whose root
+// over [lo, hi] is the position with the most trailing zero bits -- hi with
+// every bit below the highest bit in which lo and hi differ cleared; position
+// p holds rank (p - 1 + shift) mod N (tree A: shift 0, tree B: shift 1).  A
+// node folds ((left subtree) (+) own) (+) (right subtree).
+__host__ __device__ constexpr int highest_bit(unsigned v) {
+  int b = -1;
+  while (v) {
+    v >>= 1;
+    ++b;
+  }
+  return b;
+}
+
+__host__ __device__ constexpr int inorder_root(int lo, int hi) {
+  return lo == hi ? lo : (hi & ~((1 << highest_bit((unsigned)(lo ^ hi))) - 1));
+}
+
+template <int DT, int OP>
+__device__ uint32_t fold_dbtree_scalar(const void* const* P, int n, int shift, int64_t e, int lo, int hi) {
+  constexpr int ES = ElemSize<DT>::value;
+  const int root = inorder_root(lo, hi);
+  uint32_t acc = ld_elem<ES>(P[(root - 1 + shift) % n], e);
+  if (lo < root) acc = step_word<DT, OP>(fold_dbtree_scalar<DT, OP>(P, n, shift, e, lo, root - 1), acc);
+  if (root < hi) acc = step_word<DT, OP>(acc, fold_dbtree_scalar<DT, OP>(P, n, shift, e, root + 1, hi));
+  return acc;
+}
+
+// One element in the order of `order` (chunk c selects the ring rotation,
+// and for the double binary tree the tree: 0 = A, 1 = B).
+template <int DT, int OP, int ORDER>
+__device__ __forceinline__ uint32_t fold_scalar(const void* const* P, int n, int c, int64_t e) {
+  if constexpr (ORDER == RING) return fold_ring_scalar<DT, OP>(P, n, c, e);
+  else if constexpr (ORDER == TREE) return fold_tree_scalar<DT, OP>(P, n, e);
+  else return fold_dbtree_scalar<DT, OP>(P, n, c, e, 1, n);
+}
+
 }  // namespace ar

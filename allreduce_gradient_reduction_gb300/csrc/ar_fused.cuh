@@ -52,6 +52,17 @@ __device__ __forceinline__ uint4 tree_fold_regs(uint4 (&x)[NR]) {
   return x[0];
 }
 
+// Double binary tree over register-resident rank vectors x[rank] (see
+// inorder_root): ((left) (+) own) (+) (right), positions LO..HI, shift SH.
+template <int DT, int OP, int NR, int SH, int LO, int HI>
+__device__ __forceinline__ uint4 inorder_fold_regs(const uint4 (&x)[NR]) {
+  constexpr int R = inorder_root(LO, HI);
+  uint4 acc = x[(R - 1 + SH) % NR];
+  if constexpr (LO < R) acc = step_vec<DT, OP>(inorder_fold_regs<DT, OP, NR, SH, LO, R - 1>(x), acc);
+  if constexpr (R < HI) acc = step_vec<DT, OP>(acc, inorder_fold_regs<DT, OP, NR, SH, R + 1, HI>(x));
+  return acc;
+}
+
 template <int DT, int OP, int ORDER, int NR>
 __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
   constexpr int ES = ElemSize<DT>::value;
@@ -114,6 +125,19 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_k
           }
         }
       }
+    } else if constexpr (ORDER == DBTREE) {
+      // chunk 0: tree A over the first half of the elements, chunk 1: tree B
+      uint4 x[U][NR];
+#pragma unroll
+      for (int p = 0; p < NR; ++p) {
+        const char* src = static_cast<const char*>(P[p]) + base;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        acc[u] = c == 0 ? inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]) : inorder_fold_regs<DT, OP, NR, 1, 1, NR>(x[u]);
     } else if constexpr (NR <= 8) {
       uint4 x[U][NR];
 #pragma unroll
@@ -175,7 +199,7 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_k
     // elements of the segment outside its full vectors
     if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
       const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
-      uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, c, e) : fold_tree_scalar<DT, OP>(P, n, e);
+      uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
       if (a.avg) r = div_word<DT>(r, a.fn);
       if (a.owner_only || a.to_root) {
         st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
@@ -198,7 +222,7 @@ __global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_
     const int64_t e = s.begin + (tile - s.tile_begin) * kFusedBlock + threadIdx.x;
     if (e >= s.end) continue;
     const void* const* P = T.ptr + (size_t)s.tensor * n;
-    uint32_t r = ORDER == RING ? fold_ring_scalar<DT, OP>(P, n, s.chunk, e) : fold_tree_scalar<DT, OP>(P, n, e);
+    uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, s.chunk, e);
     if (a.avg) r = div_word<DT>(r, a.fn);
     if (a.owner_only || a.to_root) {
       st_elem<ES>(const_cast<void*>(P[a.owner_only ? s.chunk : a.root]), e, r);
@@ -265,6 +289,18 @@ cudaError_t launch_fused_scalar(FusedArgs& a, cudaStream_t stream) {
 template <int DT, int OP>
 cudaError_t launch_fused_typed(int order, bool vec, FusedArgs& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
+  if (order == DBTREE) {
+    // register-resident trees for the common rank counts, the element-wise
+    // kernel (recursive fold) for the others
+    if (vec) switch (n) {
+        case 2: return launch_fused_vec<DT, OP, DBTREE, 2>(a, stream);
+        case 4: return launch_fused_vec<DT, OP, DBTREE, 4>(a, stream);
+        case 8: return launch_fused_vec<DT, OP, DBTREE, 8>(a, stream);
+        case 16: return launch_fused_vec<DT, OP, DBTREE, 16>(a, stream);
+        default: break;
+      }
+    return launch_fused_scalar<DT, OP, DBTREE>(a, stream);
+  }
   if (!vec) return order == RING ? launch_fused_scalar<DT, OP, RING>(a, stream) : launch_fused_scalar<DT, OP, TREE>(a, stream);
   if (order == RING) {
     switch (n) {

@@ -53,6 +53,13 @@
  *       AR_NAIVE (AllReduce and Reduce only): index order x[0], x[1], ...,
  *         x[N-1], the order in which a central root folds the buffers it
  *         gathers ("AllReduce 集合通信" §朴素实现与主节点瓶颈, tutorial §2.1).
+ *       AR_DBTREE (AllReduce only): double binary tree -- two binary trees
+ *         run at once, each reducing half of the data ([concept §3]; the
+ *         pages give no shape).  Positions 1..N form an in-order binary tree
+ *         (the root of a range is its position with the most trailing zero
+ *         bits); tree A holds rank p-1 at position p and reduces elements
+ *         [0, floor(D/2)); tree B holds rank p mod N and reduces the rest.  A
+ *         node folds ((left subtree) (+) own) (+) (right subtree).
  *     The fused algorithms make one pass over HBM (each element of each rank
  *     read once and written once); the step-wise ones execute the literal
  *     schedule, one grid-wide phase per communication step, in a single
@@ -75,7 +82,14 @@ typedef struct CUstream_st* ar_stream_t;
 
 typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2 } ar_dtype;
 typedef enum { AR_SUM = 0, AR_MAX = 1, AR_AVG = 2 } ar_op;
-typedef enum { AR_RING = 0, AR_RING_STEPWISE = 1, AR_TREE = 2, AR_TREE_STEPWISE = 3, AR_NAIVE = 4 } ar_algo;
+typedef enum {
+  AR_RING = 0,
+  AR_RING_STEPWISE = 1,
+  AR_TREE = 2,
+  AR_TREE_STEPWISE = 3,
+  AR_NAIVE = 4,
+  AR_DBTREE = 5
+} ar_algo;
 
 typedef enum {
   AR_OK = 0,

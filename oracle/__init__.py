@@ -31,7 +31,7 @@ _LIB = os.path.join(_HERE, "libar_oracle.so")
 MAX_RANKS = 256
 DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
 OPS = {"sum": 0, "max": 1, "avg": 2}
-ALGOS = {"ring": 0, "tree": 1, "binomial": 2, "naive": 3}
+ALGOS = {"ring": 0, "tree": 1, "binomial": 2, "naive": 3, "dbtree": 4}
 PHASE_RS, PHASE_AG = 1, 2
 NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}
 

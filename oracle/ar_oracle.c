@@ -59,7 +59,7 @@
 
 enum { OR_F32 = 0, OR_BF16 = 1, OR_I32 = 2 };
 enum { OR_SUM = 0, OR_MAX = 1, OR_AVG = 2 };
-enum { OR_RING = 0, OR_TREE = 1, OR_BINOMIAL = 2, OR_NAIVE = 3 };
+enum { OR_RING = 0, OR_TREE = 1, OR_BINOMIAL = 2, OR_NAIVE = 3, OR_DBTREE = 4 };
 enum { OR_PHASE_RS = 1, OR_PHASE_AG = 2 };
 enum {
   OR_OK = 0,
@@ -237,6 +237,7 @@ typedef struct {
   oracle_stats* st;
   const oracle_fault* fault;
   int step;
+  int64_t khalf; /* first local position of the second half (double binary tree) */
 } sim;
 
 static int64_t chunk_len(const sim* s, int j) { return s->klo[j + 1] - s->klo[j]; }
@@ -517,6 +518,131 @@ static int naive_allreduce(sim* s, int avg) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* Double binary tree                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Two binary trees that run at the same time, each reducing and then
+ * broadcasting half of the data ("AllReduce" concept page §3 技术原理: two
+ * disjoint binary trees; "AllReduce 集合通信" §带宽最优与延迟的取舍).  The pages
+ * give no tree shape; the one used here: positions 1..N form an in-order
+ * binary tree (the root of a range is its position with the most trailing
+ * zero bits; left subtree below it, right subtree above it); tree A puts rank
+ * p-1 at position p, tree B rank p mod N (shifted by one, so for even N every
+ * rank that is a leaf of one tree is inner in the other).  Tree A reduces the
+ * first half of the elements, [0, floor(D/2)), tree B the second.  A node
+ * folds its left child's partial, its own value, then its right child's
+ * partial: ((L (+) own) (+) R). */
+
+typedef struct {
+  int parent[OR_MAX_RANKS + 2], left[OR_MAX_RANKS + 2], right[OR_MAX_RANKS + 2];
+  int sub_h[OR_MAX_RANKS + 2]; /* 0 for a leaf */
+  int depth[OR_MAX_RANKS + 2]; /* 0 for the root */
+  int root;
+} inorder_tree;
+
+static int trailing_zeros(int p) {
+  int k = 0;
+  while (!(p & 1)) {
+    p >>= 1;
+    ++k;
+  }
+  return k;
+}
+
+/* the position with the most trailing zero bits in [lo, hi] */
+static int inorder_root_of(int lo, int hi) {
+  int p, best = lo, bt = -1;
+  for (p = lo; p <= hi; ++p)
+    if (trailing_zeros(p) > bt) {
+      bt = trailing_zeros(p);
+      best = p;
+    }
+  return best;
+}
+
+static int inorder_build(inorder_tree* t, int lo, int hi, int parent, int depth) {
+  int best, hl, hr;
+  if (lo > hi) return -1;
+  best = inorder_root_of(lo, hi);
+  t->parent[best] = parent;
+  t->depth[best] = depth;
+  hl = inorder_build(t, lo, best - 1, best, depth + 1);
+  hr = inorder_build(t, best + 1, hi, best, depth + 1);
+  t->left[best] = lo <= best - 1 ? inorder_root_of(lo, best - 1) : 0;
+  t->right[best] = best + 1 <= hi ? inorder_root_of(best + 1, hi) : 0;
+  t->sub_h[best] = 1 + (hl > hr ? hl : hr);
+  return t->sub_h[best];
+}
+
+/* Reduce then broadcast elements [a, b) of every rank over tree `t`, where
+ * position p holds rank (p - 1 + shift) mod N.  Returns the number of
+ * communication steps (reduce plus broadcast). */
+static int dbtree_half(sim* s, const inorder_tree* t, int shift, int64_t a, int64_t b, int avg) {
+  int n = s->n, p, k, maxh = t->sub_h[t->root], maxd = 0;
+  int64_t len = b - a;
+  size_t bytes = (size_t)(len > 0 ? len : 1) * (size_t)s->es;
+  unsigned char* held[OR_MAX_RANKS + 2][2];
+  memset(held, 0, sizeof(held));
+#define RANK_AT(pos) (((pos) - 1 + shift) % n)
+#define SLICE(pos) (s->rank[RANK_AT(pos)] + (size_t)a * (size_t)s->es)
+  for (k = 0; k <= maxh; ++k) {
+    /* nodes whose subtrees are complete fold what their children sent */
+    for (p = 1; p <= n; ++p) {
+      if (t->sub_h[p] != k) continue;
+      if (held[p][0]) combine(s->dtype, s->op, held[p][0], SLICE(p), SLICE(p), len);
+      if (held[p][1]) combine(s->dtype, s->op, SLICE(p), held[p][1], SLICE(p), len);
+      free(held[p][0]);
+      free(held[p][1]);
+      held[p][0] = held[p][1] = NULL;
+    }
+    /* and send the partial to their parent (copied: the message) */
+    for (p = 1; p <= n; ++p) {
+      int q, side;
+      if (t->sub_h[p] != k || !t->parent[p]) continue;
+      q = t->parent[p];
+      side = t->left[q] == p ? 0 : 1;
+      held[q][side] = (unsigned char*)malloc(bytes);
+      if (!held[q][side]) return OR_ENOMEM;
+      memcpy(held[q][side], SLICE(p), (size_t)len * (size_t)s->es);
+      s->st->sent[RANK_AT(p)] += len;
+      s->st->recv[RANK_AT(q)] += len;
+    }
+  }
+  if (avg) divide_by(s->dtype, SLICE(t->root), len, n);
+  for (p = 1; p <= n; ++p)
+    if (t->depth[p] > maxd) maxd = t->depth[p];
+  for (k = 0; k < maxd; ++k)
+    for (p = 1; p <= n; ++p) {
+      int c;
+      if (t->depth[p] != k) continue;
+      for (c = 0; c < 2; ++c) {
+        int ch = c ? t->right[p] : t->left[p];
+        if (!ch) continue;
+        memcpy(SLICE(ch), SLICE(p), (size_t)len * (size_t)s->es);
+        s->st->sent[RANK_AT(p)] += len;
+        s->st->recv[RANK_AT(ch)] += len;
+      }
+    }
+#undef RANK_AT
+#undef SLICE
+  return maxh + maxd;
+}
+
+static int dbtree_allreduce(sim* s, int avg) {
+  inorder_tree t;
+  int sa, sb;
+  memset(&t, 0, sizeof(t));
+  inorder_build(&t, 1, s->n, 0, 0);
+  t.root = inorder_root_of(1, s->n);
+  sa = dbtree_half(s, &t, 0, 0, s->khalf, avg);
+  if (sa < 0) return sa;
+  sb = dbtree_half(s, &t, 1 % s->n, s->khalf, s->m, avg);
+  if (sb < 0) return sb;
+  s->st->steps += sa > sb ? sa : sb; /* the two trees run at the same time */
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Entry point                                                              */
 /* ------------------------------------------------------------------------ */
 
@@ -549,9 +675,9 @@ int oracle_collective(int algo, const void* const* in, void* const* out, int nra
   if (nranks < 1 || nranks > OR_MAX_RANKS || count < 0 || !in || !out) return OR_EINVAL;
   if (dtype < 0 || dtype > 2 || op < 0 || op > 2 || phases < 1 || phases > 3) return OR_EINVAL;
   if (op == OR_AVG && dtype == OR_I32) return OR_EUNSUPPORTED;
-  if (algo < 0 || algo > 3) return OR_EINVAL;
-  if (algo != OR_RING && algo != OR_NAIVE && log2_exact(nranks) < 0) return OR_EUNSUPPORTED;
-  if ((algo == OR_BINOMIAL || algo == OR_NAIVE) && phases != 3) return OR_EUNSUPPORTED;
+  if (algo < 0 || algo > 4) return OR_EINVAL;
+  if ((algo == OR_TREE || algo == OR_BINOMIAL) && log2_exact(nranks) < 0) return OR_EUNSUPPORTED;
+  if ((algo == OR_BINOMIAL || algo == OR_NAIVE || algo == OR_DBTREE) && phases != 3) return OR_EUNSUPPORTED;
   m = positions ? npos : count;
   if (positions) {
     for (i = 0; i < npos; ++i)
@@ -577,6 +703,12 @@ int oracle_collective(int algo, const void* const* in, void* const* out, int nra
       s->klo[j] = k;
     }
   }
+  s->khalf = count / 2;
+  if (positions) {
+    int64_t k = 0;
+    while (k < npos && positions[k] < count / 2) ++k;
+    s->khalf = k;
+  }
   for (r = 0; r < nranks; ++r) {
     s->rank[r] = (unsigned char*)malloc((size_t)(m > 0 ? m : 1) * (size_t)s->es);
     if (!s->rank[r]) {
@@ -585,7 +717,9 @@ int oracle_collective(int algo, const void* const* in, void* const* out, int nra
     }
     memcpy(s->rank[r], in[r], (size_t)m * (size_t)s->es);
   }
-  if (algo == OR_RING || algo == OR_TREE) {
+  if (algo == OR_DBTREE) {
+    rc = dbtree_allreduce(s, op == OR_AVG);
+  } else if (algo == OR_RING || algo == OR_TREE) {
     if (phases & OR_PHASE_RS) {
       rc = algo == OR_RING ? ring_reduce_scatter(s) : tree_reduce_scatter(s);
       if (rc) goto done;

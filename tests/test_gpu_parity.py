@@ -478,3 +478,27 @@ def test_broadcast_copies_bits(ar, dtype):
     bufs = [to_dev(np.zeros(4, np.float32)) for _ in range(2)]
     assert ar.ar_broadcast(bufs, count=4, root=2) == ar.AR_ERR_INVALID_ARG
     assert ar.ar_reduce(bufs, count=4, root=-1) == ar.AR_ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------------
+# Double binary tree
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 64])
+def test_dbtree_matches_oracle(ar, dtype, n):
+    for count in [c for c in (1, 2, n + 1, 4099, 2 * 2048 * n + 11) if c > 0]:
+        for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+            x = inputs(n, count, dtype, "bits" if (count % 2 and op != "sum") else "values", seed=2100 + n + count)
+            with np.errstate(all="ignore"):
+                want, _ = oracle.allreduce(x, algo="dbtree", op=op, dtype=dtype)
+            got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo="dbtree")
+            assert_same(got, want, dtype, f"dbtree {op} n={n} count={count}")
+
+
+def test_dbtree_only_for_allreduce(ar):
+    x = W.normal_inputs(4, 64, 1.0, 1)
+    bufs = [to_dev(x[r]) for r in range(4)]
+    assert ar.ar_reduce_scatter(bufs, count=64, algo="dbtree") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_all_gather(bufs, count=64, algo="dbtree") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_reduce(bufs, count=64, algo="dbtree", root=1) == ar.AR_ERR_UNSUPPORTED

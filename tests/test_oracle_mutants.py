@@ -57,6 +57,13 @@ MUTANTS = [
     ("buckets filled in registration order",
      [("for (t = ntensors - 1; t >= 0; --t) {\n    int64_t bytes;", "for (t = 0; t < ntensors; ++t) {\n    int64_t bytes;")],
      ["bucket"]),
+    ("double binary tree: both halves on the same tree",
+     [("sb = dbtree_half(s, &t, 1 % s->n, s->khalf, s->m, avg);", "sb = dbtree_half(s, &t, 0, s->khalf, s->m, avg);")],
+     ["dbtree"]),
+    ("double binary tree: a node folds its own value last",
+     [("if (held[p][0]) combine(s->dtype, s->op, held[p][0], SLICE(p), SLICE(p), len);\n      if (held[p][1]) combine(s->dtype, s->op, SLICE(p), held[p][1], SLICE(p), len);",
+       "if (held[p][1]) combine(s->dtype, s->op, SLICE(p), held[p][1], SLICE(p), len);\n      if (held[p][0]) combine(s->dtype, s->op, held[p][0], SLICE(p), SLICE(p), len);")],
+     ["dbtree"]),
     ("ring counts only received volume",
      [("s->st->sent[src] += total;", "(void)total;")],
      ["volume"]),
@@ -93,6 +100,11 @@ def run_pins(which):
         P.test_bucket_plan_gpt2(o)
     if "volume" in which:
         P.test_ring_volume_and_steps(o, 4)
+    if "dbtree" in which:
+        for dt in ("f32", "bf16"):
+            for n in (4, 5, 8):
+                P.test_dbtree_closed_form(o, dt, n)
+        P.test_dbtree_worked_shapes(o)
 
 
 @pytest.mark.parametrize("name,edits,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
@@ -118,4 +130,4 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
 
 def test_real_oracle_passes_the_same_pins():
     run_pins({"ring_order", "tree_order", "bruteforce", "printed", "bf16_round", "avg", "max", "f32_add",
-              "bucket", "volume"})
+              "bucket", "volume", "dbtree"})

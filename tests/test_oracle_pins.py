@@ -52,7 +52,7 @@ def to_f64(x, dtype):
 
 
 def algos_for(n):
-    out = ["ring", "naive"]
+    out = ["ring", "naive", "dbtree"]
     if n & (n - 1) == 0:
         out += ["tree", "binomial"]
     return out
@@ -745,3 +745,75 @@ def test_reduce_root_volume(oracle_lib):
     _, st = oracle.reduce(x, algo="ring", root=3)
     # ReduceScatter (N-1)/N D per rank, then the N-1 foreign chunks to the root
     assert st["recv"][3] == (n - 1) * count // n + (n - 1) * count // n
+
+
+# --------------------------------------------------------------------------
+# Double binary tree
+# --------------------------------------------------------------------------
+
+def inorder_fold(vals, lo, hi, add):
+    """In-order binary tree over positions lo..hi (1-based): the root is the
+    position with the most trailing zero bits; ((left) + own) + (right)."""
+    if lo > hi:
+        return None
+    root = max(range(lo, hi + 1), key=lambda p: (p & -p))
+    acc = vals[root]
+    left = inorder_fold(vals, lo, root - 1, add)
+    right = inorder_fold(vals, root + 1, hi, add)
+    if left is not None:
+        acc = add(left, acc)
+    if right is not None:
+        acc = add(acc, right)
+    return acc
+
+
+def dbtree_closed_form(x, dtype):
+    n, count = x.shape
+    add = _lib_add(dtype)
+    half = count // 2
+    out = np.empty(count, dtype=x.dtype)
+    a = {p: x[p - 1, :half] for p in range(1, n + 1)}        # tree A: rank p-1 at position p
+    b = {p: x[p % n, half:] for p in range(1, n + 1)}        # tree B: rank p mod N at position p
+    out[:half] = inorder_fold(a, 1, n, add)
+    out[half:] = inorder_fold(b, 1, n, add)
+    return out
+
+
+@pytest.mark.parametrize("dtype", ALL_DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 8, 13, 16])
+def test_dbtree_closed_form(oracle_lib, dtype, n):
+    with np.errstate(over="ignore"):
+        for count in (2, 2 * n + 1, 513):
+            x = W.uniform_inputs(n, count, dtype, config=800 + count) if dtype != "f32" else \
+                W.normal_inputs(n, count, 1.0, 800 + count)
+            out, _ = oracle.allreduce(x, algo="dbtree", op="sum", dtype=dtype)
+            assert np.array_equal(out, np.broadcast_to(dbtree_closed_form(x, dtype), out.shape)), count
+
+
+def test_dbtree_worked_shapes(oracle_lib):
+    # by hand from the stated shape, N = 4: tree A reduces ((x0 + x1) + x2) + x3,
+    # tree B (ranks shifted by one) ((x1 + x2) + x3) + x0; distinct f32 values
+    # whose sums round differently in the two orders tell the shapes apart
+    x = np.array([[1e8], [1.0], [-1e8], [1.0]], dtype=np.float32)
+    x = np.repeat(x, 2, axis=1)  # element 0 in half A, element 1 in half B
+    out, _ = oracle.allreduce(x, algo="dbtree", op="sum", dtype="f32")
+    f = np.float32
+    a = ((f(1e8) + f(1.0)) + f(-1e8)) + f(1.0)
+    b = ((f(1.0) + f(-1e8)) + f(1.0)) + f(1e8)
+    assert out[0, 0] == a and out[0, 1] == b and a != b
+
+
+@pytest.mark.parametrize("n", [2, 4, 7, 8, 16])
+def test_dbtree_volume_and_steps(oracle_lib, n):
+    count = 64 * n
+    x = np.ones((n, count), dtype=np.float32)
+    _, st = oracle.allreduce(x, algo="dbtree", dtype="f32")
+    # each tree moves its half up (N-1 messages) and down (N-1 messages)
+    assert st["sent"].sum() == 2 * (n - 1) * count
+    # logarithmic depth: up and down one tree of height floor(log2 N)
+    h = int(math.floor(math.log2(n)))
+    assert st["steps"] <= 2 * (h + 1)
+    if n % 2 == 0:
+        # every rank is a leaf in one of the two trees: no rank relays more
+        # than one half's worth of partials up and down
+        assert st["sent"].max() <= count // 2 * 3 + count // 2
