@@ -27,11 +27,13 @@ AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, 
 MAX_RANKS = 64
 DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
-EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_bucket_plan",
+EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_allreduce_int8_ef",
+           "ar_bucket_plan",
            "ar_bucketed_allreduce",
            "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
            "ar_last_cuda_error", "ar_strerror", "ar_version", "ar_kernel_launches", "ar_reducer_create",
-           "ar_reducer_mark_ready", "ar_reducer_finish", "ar_reducer_destroy", "ar_reducer_buckets")
+           "ar_reducer_mark_ready", "ar_reducer_finish", "ar_reducer_destroy", "ar_reducer_buckets",
+           "ar_reducer_set_max_blocks")
 
 
 class ArError(RuntimeError):
@@ -53,6 +55,7 @@ def _load():
     L.ar_all_gather.argtypes = [pp, cint, i64, cint, cint, vp]
     L.ar_reduce.argtypes = [pp, cint, i64, cint, cint, cint, cint, vp]
     L.ar_broadcast.argtypes = [pp, cint, i64, cint, cint, vp]
+    L.ar_allreduce_int8_ef.argtypes = [pp, pp, cint, i64, cint, vp]
     L.ar_bucket_plan.argtypes = [ctypes.POINTER(i64), cint, cint, i64, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                  ctypes.POINTER(i64), ctypes.POINTER(i32)]
     L.ar_bucketed_allreduce.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, pp, i64, vp]
@@ -72,6 +75,7 @@ def _load():
     L.ar_reducer_finish.argtypes = [vp, vp]
     L.ar_reducer_destroy.argtypes = [vp]
     L.ar_reducer_buckets.argtypes = [vp]
+    L.ar_reducer_set_max_blocks.argtypes = [vp, cint]
     for name in EXPORTS:
         if name != "ar_strerror":
             getattr(L, name).restype = cint
@@ -149,6 +153,12 @@ def ar_broadcast(bufs, nranks=None, count=None, dtype="f32", root=0, stream=None
                             _stream(stream))
 
 
+def ar_allreduce_int8_ef(grads, residuals, nranks=None, count=None, op="sum", stream=None) -> int:
+    n = len(grads) if nranks is None else int(nranks)
+    return lib.ar_allreduce_int8_ef(_ptr_array(grads), _ptr_array(residuals), n, _count(grads, count),
+                                    _enum(OP, op), _stream(stream))
+
+
 def ar_bucket_plan(counts, dtype="f32", cap_bytes=DEFAULT_BUCKET_CAP_BYTES):
     """Returns (status, bucket_of_tensor, offset_in_bucket, bucket_count) as lists."""
     t = len(counts)
@@ -224,6 +234,9 @@ class Reducer:
     @property
     def buckets(self) -> int:
         return lib.ar_reducer_buckets(self.handle)
+
+    def set_max_blocks(self, max_blocks: int) -> int:
+        return lib.ar_reducer_set_max_blocks(self.handle, int(max_blocks))
 
     def mark_ready(self, tensor: int, stream=None) -> int:
         return lib.ar_reducer_mark_ready(self.handle, int(tensor), _stream(stream))

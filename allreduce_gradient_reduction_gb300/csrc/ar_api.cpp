@@ -148,6 +148,7 @@ struct Job {
   bool avg;
   bool vec;
   int root = -1;  // Reduce: the rank that receives the result
+  int max_grid = 0;  // fused kernels: cap on the number of blocks (0 = one per tile)
 };
 
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
@@ -181,6 +182,7 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
     a.owner_only = j.phases == 1 ? 1 : 0;
     a.to_root = j.root >= 0 ? 1 : 0;
     a.root = j.root >= 0 ? j.root : 0;
+    a.max_grid = j.max_grid;
     a.fn = (float)tab.nranks;
     e = ar::launch_fused(j.dtype, dop, order, j.vec, a, s);
   }
@@ -405,6 +407,34 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
   tb.add_seg(tb.add_row(bufs), 0, count, root);
   Job j{dtype, AR_SUM, AR_RING, 2, false, all_aligned16(bufs, nranks)};
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
+}
+
+int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
+                         ar_stream_t stream) {
+  int rc = check_common(nranks, count, AR_F32, op, AR_RING);
+  if (rc) return rc;
+  if (op == AR_MAX) return AR_ERR_UNSUPPORTED;
+  if (!grads || !residuals) return AR_ERR_INVALID_ARG;
+  std::vector<Range> rs;
+  for (int r = 0; r < nranks; ++r) {
+    rs.push_back({(uintptr_t)grads[r], (uintptr_t)grads[r] + (uintptr_t)count * 4});
+    rs.push_back({(uintptr_t)residuals[r], (uintptr_t)residuals[r] + (uintptr_t)count * 4});
+  }
+  if ((rc = check_ranges(rs, 4))) return rc;
+  if (count == 0) return AR_OK;
+  ar::Int8Args a;
+  memset(&a, 0, sizeof(a));
+  for (int r = 0; r < nranks; ++r) {
+    a.x[r] = static_cast<float*>(grads[r]);
+    a.e[r] = static_cast<float*>(residuals[r]);
+  }
+  a.count = count;
+  a.nranks = nranks;
+  a.avg = op == AR_AVG ? 1 : 0;
+  a.vec = all_aligned16(grads, nranks) && all_aligned16(residuals, nranks) ? 1 : 0;
+  a.fn = (float)nranks;
+  cudaError_t e = ar::launch_int8_ef(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? AR_OK : cuda_fail(e);
 }
 
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
@@ -644,6 +674,12 @@ int ar_reducer_destroy(ar_reducer* red) {
 }
 
 int ar_reducer_buckets(const ar_reducer* red) { return red ? red->nbuckets : AR_ERR_INVALID_ARG; }
+
+int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks) {
+  if (!red || max_blocks < 0) return AR_ERR_INVALID_ARG;
+  red->job.max_grid = max_blocks;
+  return AR_OK;
+}
 
 int ar_device_status(ar_stream_t stream, int* status) {
   if (!status) return AR_ERR_INVALID_ARG;

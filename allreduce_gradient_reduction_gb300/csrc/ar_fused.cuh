@@ -266,13 +266,17 @@ inline int blocks_per_sm(K kernel, int block) {
   return b;
 }
 
-inline unsigned grid_for(int64_t ntiles) { return (unsigned)(ntiles < kMaxGrid ? ntiles : kMaxGrid); }
+inline unsigned grid_for(int64_t ntiles, int64_t cap = 0) {
+  int64_t g = ntiles < kMaxGrid ? ntiles : kMaxGrid;
+  if (cap > 0 && g > cap) g = cap;
+  return (unsigned)g;
+}
 
 template <int DT, int OP, int ORDER, int NR>
 cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
   constexpr int U = fused_unroll(ORDER, NR);
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U) == 0) return cudaSuccess;
-  fused_vec_kernel<DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  fused_vec_kernel<DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
@@ -280,7 +284,7 @@ cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
 template <int DT, int OP, int ORDER>
 cudaError_t launch_fused_scalar(FusedArgs& a, cudaStream_t stream) {
   if (fill_tiles(a.tab, 1, kFusedBlock) == 0) return cudaSuccess;
-  fused_scalar_kernel<DT, OP, ORDER><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
+  fused_scalar_kernel<DT, OP, ORDER><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }

@@ -48,6 +48,7 @@ struct FusedArgs {
   int32_t owner_only;  // ReduceScatter: store to the chunk owner only
   int32_t to_root;     // Reduce: store to rank `root` only
   int32_t root;
+  int32_t max_grid;    // > 0: at most this many blocks (they stride over the tiles)
   float fn;            // (float)nranks
 };
 
@@ -69,6 +70,16 @@ struct CopyArgs {
   int32_t esize;
 };
 
+struct Int8Args {
+  float* x[kMaxRanks];  // gradients, reduced in place
+  float* e[kMaxRanks];  // error-feedback residuals, updated in place
+  int64_t count;
+  int32_t nranks;
+  int32_t avg;
+  int32_t vec;          // every pointer 16-byte aligned
+  float fn;
+};
+
 // Launchers.  Each fills tab.seg[*].tile_begin and tab.ntiles for its own
 // tile shape, then enqueues on `stream`.  `vec` selects the 16-byte path
 // (every pointer 16-byte aligned); otherwise one element per thread.
@@ -76,6 +87,7 @@ cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& args
 cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t stream);
 cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
+cudaError_t launch_int8_ef(Int8Args& args, cudaStream_t stream);
 
 int sm_count();
 

@@ -394,8 +394,15 @@ class BucketWorkload:
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
                        "l2": "409.6 MiB touched per step vs 129 MB L2 (partly L2-resident between steps)"}
 
-    def step(self, sid, algo):
-        rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo, stream=sid)
+    def step(self, sid, algo, int8=False):
+        if int8:
+            import torch
+            if getattr(self, "resid", None) is None:
+                self.resid = [torch.zeros_like(b) for b in self.bufs]
+            rc = self.ar.ar_allreduce_int8_ef(self.bufs, self.resid, count=self.count, op=self.op, stream=sid)
+        else:
+            rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo,
+                                      stream=sid)
         if rc:
             raise self.ar.ArError(rc, "ar_allreduce")
 
@@ -514,14 +521,23 @@ class Gpt2Workload:
 
         tf32 = torch.backends.cuda.matmul.allow_tf32
         torch.backends.cuda.matmul.allow_tf32 = True  # mixed-precision-like backward on the tensor cores
+        by_blocks = {}
         try:
-            t_bwd, t_seq, t_ovl = timed(backward), timed(seq), timed(ovl)
+            t_bwd, t_seq = timed(backward), timed(seq)
+            # block caps for the overlapped reductions: none (one block per
+            # tile), then a few "channels" of the GPU's 152 SMs
+            for cap in (0, 304, 152, 76, 38):
+                self.ar.check(red.set_max_blocks(cap), "set_max_blocks")
+                by_blocks[cap] = timed(ovl)
         finally:
             torch.backends.cuda.matmul.allow_tf32 = tf32
         nbuckets = red.buckets
         red.close()
+        best = min(by_blocks, key=by_blocks.get)
+        t_ovl = by_blocks[best]
         t_ar = t_seq - t_bwd
         return {"tokens": tokens, "backward_ms": t_bwd, "sequential_ms": t_seq, "overlapped_ms": t_ovl,
+                "overlapped_ms_by_max_blocks": {str(k): v for k, v in by_blocks.items()}, "best_max_blocks": best,
                 "allreduce_ms_in_sequence": t_ar, "exposed_comm_ms": t_ovl - t_bwd,
                 "hidden_fraction": (t_seq - t_ovl) / t_ar if t_ar > 0 else None, "buckets": nbuckets,
                 "note": "backward = per-rank TF32 GEMMs (dW = X^T dY) on the compute stream, every variant "
@@ -648,8 +664,10 @@ def main():
         todo = [(a, {}) for a in orders if a != args.algo]
         if isinstance(wl, Gpt2Workload):
             todo += [("ring_literal", {"literal": True})]
+        if isinstance(wl, BucketWorkload):
+            todo += [("int8_ef", {"int8": True})]
         for name, kw in todo:
-            algo = name.replace("_literal", "")
+            algo = name.replace("_literal", "") if name != "int8_ef" else "ring"
             for _ in range(3):
                 step(algo, **kw)
             torch.cuda.synchronize()
@@ -662,6 +680,8 @@ def main():
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / k
             variants[name] = {"ms_per_step": vms, "effective_gbs": nbytes_step / (vms / 1e3) / 1e9}
+            if name == "int8_ef":  # reads and writes gradients and residuals: 4 N D floats
+                variants[name]["hbm_gbs"] = 2 * nbytes_step / (vms / 1e3) / 1e9
 
     overlap = None
     if args.overlap and isinstance(wl, Gpt2Workload):

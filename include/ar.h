@@ -160,6 +160,28 @@ int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_o
 int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, int root, ar_stream_t stream);
 
 /*
+ * 8-bit quantised AllReduce with error feedback ([tutorial §4.2]: gradients
+ * travel as 8-bit integers that the receiver dequantises; error feedback
+ * carries the compression error into the next round).  The pages give no
+ * scheme; this one (binary32 throughout, round to nearest):
+ *   every rank r: y = grads[r] + residuals[r]; per block of 128 elements
+ *   from the start of the buffer s = max|y| / 127; q = round-half-even(y / s)
+ *   clamped to [-127, 127] (0 when s = 0); residuals[r] = y - q * s;
+ *   chunk c's owner folds q * s of all ranks in ring order x[c+1], ..., x[c]
+ *   (AVG: divides by N once), requantises with the same rule per block cut at
+ *   the chunk's ends, and every rank's grads receive that requantised value.
+ * On a network this moves 2(N-1)/N * D one-byte codes per rank (plus one
+ * scale per block) instead of 2(N-1)/N * D floats.
+ *   grads, residuals  host arrays of nranks device pointers to count floats
+ *               each (all 2N ranges disjoint); both updated in place.  Start
+ *               training with zeroed residuals.
+ *   op          AR_SUM or AR_AVG (AR_MAX: AR_ERR_UNSUPPORTED)
+ * Inputs must be finite.  Errors as ar_allreduce.
+ */
+int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
+                         ar_stream_t stream);
+
+/*
  * DDP bucket plan [tutorial §4.1], [notes §DDP 梯度同步中的地位]: walk the
  * tensors in reverse registration order; add each to the current bucket while
  * the bucket's bytes stay <= cap_bytes; a tensor that does not fit opens the
@@ -273,6 +295,12 @@ int ar_reducer_finish(ar_reducer* red, ar_stream_t compute_stream);
 int ar_reducer_destroy(ar_reducer* red);
 /* Number of buckets of a reducer (or AR_ERR_INVALID_ARG for NULL). */
 int ar_reducer_buckets(const ar_reducer* red);
+/* Caps the thread blocks of each bucket reduction (fused orders; 0 = no cap,
+ * one block per tile).  On one GPU the reductions share SMs and HBM with the
+ * compute they overlap; a few blocks striding over the tiles leave the rest
+ * of the GPU to that compute, the way a collective library confines itself
+ * to a few channels.  Results do not depend on it. */
+int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks);
 
 /* Chunk c of a rank buffer of `count` elements split N ways: [*lo, *hi).
  * Host-only; errors: AR_ERR_INVALID_ARG. */

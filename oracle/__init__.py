@@ -66,7 +66,7 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
-           "-Wall", "-o", tmp, _SRC]
+           "-Wall", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -88,6 +88,8 @@ def lib():
         L.oracle_rooted.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int,
                                     ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.POINTER(Stats)]
+        L.oracle_int8_ef_allreduce.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.POINTER(Stats)]
         L.oracle_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int64]
         L.oracle_f32_to_bf16.argtypes = [vp, vp, ctypes.c_int64]
         L.oracle_chunk_range.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -196,6 +198,21 @@ def reduce(x, *, root=0, **kw):
 def broadcast(x, *, root=0, dtype="f32", **kw):
     """Copy the root's buffer to every rank."""
     return _rooted(1, x, root=root, dtype=dtype, **kw)
+
+
+def int8_ef_allreduce(x, e, *, op="sum"):
+    """8-bit quantised AllReduce with error feedback (see ar_oracle.c).
+    ``x`` and ``e`` are (N, D) float32: gradients and residuals.  Returns
+    (reduced x, new residuals, stats)."""
+    xs = [np.array(a, dtype=np.float32, copy=True) for a in x]
+    es = [np.array(a, dtype=np.float32, copy=True) for a in e]
+    n = len(xs)
+    st = Stats()
+    rc = lib().oracle_int8_ef_allreduce(_ptrs(xs), _ptrs(es), n, xs[0].size if n else 0, OPS[op], ctypes.byref(st))
+    if rc:
+        raise OracleError(rc, "int8_ef_allreduce")
+    stats = {"steps": st.steps, "sent": np.array(st.sent[:n], dtype=np.int64)}
+    return np.stack(xs), np.stack(es), stats
 
 
 def step(a, b, *, op="sum", dtype="f32"):

@@ -502,3 +502,39 @@ def test_dbtree_only_for_allreduce(ar):
     assert ar.ar_reduce_scatter(bufs, count=64, algo="dbtree") == ar.AR_ERR_UNSUPPORTED
     assert ar.ar_all_gather(bufs, count=64, algo="dbtree") == ar.AR_ERR_UNSUPPORTED
     assert ar.ar_reduce(bufs, count=64, algo="dbtree", root=1) == ar.AR_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------------
+# 8-bit quantised AllReduce with error feedback
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+def test_int8_ef_matches_oracle(ar, n):
+    for count in (1, 127, 128 * n, 128 * 3 * n + 77, 70_001):
+        for op in ("sum", "avg"):
+            x = W.normal_inputs(n, count, 1e-3, 2500 + n + count)
+            e = W.normal_inputs(n, count, 1e-6, 2600 + n + count)
+            for it in range(2):  # the residuals carry over to the next call
+                want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op=op)
+                xd = [to_dev(x[r]) for r in range(n)]
+                ed = [to_dev(e[r]) for r in range(n)]
+                ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op=op), "int8_ef")
+                got_x, got_e = from_dev(xd, "f32"), from_dev(ed, "f32")
+                assert_same(got_x, want_x, "f32", f"x n={n} count={count} {op} it={it}")
+                assert_same(got_e, want_e, "f32", f"e n={n} count={count} {op} it={it}")
+                x, e = W.normal_inputs(n, count, 1e-3, 2700 + it + n + count), got_e
+
+
+def test_int8_ef_unaligned_and_rejects(ar):
+    n, count = 4, 1000
+    x = W.normal_inputs(n, count, 1.0, 31)
+    e = np.zeros_like(x)
+    want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op="avg")
+    bx = [to_dev(np.concatenate([[0.0], x[r]]).astype(np.float32)) for r in range(n)]
+    be = [to_dev(np.concatenate([[0.0], e[r]]).astype(np.float32)) for r in range(n)]
+    xd, ed = [b[1:] for b in bx], [b[1:] for b in be]
+    ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op="avg"), "unaligned int8")
+    assert_same(from_dev(xd, "f32"), want_x, "f32", "x unaligned")
+    assert_same(from_dev(ed, "f32"), want_e, "f32", "e unaligned")
+    assert ar.ar_allreduce_int8_ef(xd, ed, count=count, op="max") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_allreduce_int8_ef(xd, xd, count=count) == ar.AR_ERR_INVALID_ARG  # grads overlap residuals

@@ -39,6 +39,8 @@ def test_reducer_matches_bucketed_allreduce(ar, algo, order):
     grads = make(n, 1)
     red = ar.Reducer(grads, counts=COUNTS, op="avg", algo=algo, bucket_cap_bytes=cap, comm_stream=comm)
     assert red.buckets == len(ar.ar_bucket_plan(COUNTS, "f32", cap)[3])
+    if algo != "ring_stepwise":
+        ar.check(red.set_max_blocks(3), "max blocks")  # few blocks striding: same results
     g = np.random.Generator(np.random.PCG64(2))
     for it in range(3):  # the handle is reused across iterations
         fresh = make(n, 10 + it)

@@ -817,3 +817,72 @@ def test_dbtree_volume_and_steps(oracle_lib, n):
         # every rank is a leaf in one of the two trees: no rank relays more
         # than one half's worth of partials up and down
         assert st["sent"].max() <= count // 2 * 3 + count // 2
+
+
+# --------------------------------------------------------------------------
+# 8-bit quantised AllReduce with error feedback.  The pages give only the idea
+# (8-bit payloads dequantised by the receiver, the compression error fed into
+# the next round); the block scheme is this library's own, pinned by exact
+# cases and error bounds rather than by printed values.
+# --------------------------------------------------------------------------
+
+def test_int8_exact_when_values_sit_on_the_grid(oracle_lib):
+    # every block of both ranks has max |value| = 127, so the scale is exactly 1
+    # and integers quantise without error; the sums stay within 127 as well
+    g = np.random.Generator(np.random.PCG64(5))
+    d = 128 * 6
+    a = g.integers(-63, 64, size=d).astype(np.float32)
+    b = g.integers(-63, 64, size=d).astype(np.float32)
+    a[::128], b[::128] = 127, 0
+    a[1::128], b[1::128] = 0, -127
+    x = np.stack([a, b])
+    e = np.zeros_like(x)
+    out, e_new, _ = oracle.int8_ef_allreduce(x, e, op="sum")
+    assert np.array_equal(out, np.broadcast_to(a + b, out.shape))
+    assert np.all(e_new == 0)
+    out, _, _ = oracle.int8_ef_allreduce(x, e, op="avg")
+    assert np.array_equal(out, np.broadcast_to((a + b) / np.float32(2), out.shape))
+
+
+@pytest.mark.parametrize("n", [2, 3, 8])
+def test_int8_error_bounds(oracle_lib, n):
+    d = 128 * 5 + 37
+    x = W.normal_inputs(n, d, 1e-3, 60 + n)
+    e = W.normal_inputs(n, d, 1e-5, 70 + n)
+    out, e_new, st = oracle.int8_ef_allreduce(x, e, op="sum")
+    y = x.astype(np.float64) + e.astype(np.float64)
+    blocks = [(lo, min(lo + 128, d)) for lo in range(0, d, 128)]
+    scale = np.zeros((n, d))
+    for lo, hi in blocks:
+        scale[:, lo:hi] = np.abs(y[:, lo:hi]).max(axis=1, keepdims=True) / 127
+    # the residual is the rounding error of one 8-bit code: at most half a step
+    assert np.all(np.abs(e_new) <= scale / 2 * (1 + 1e-5) + 1e-12)
+    # every rank gets the same values, within the quantisation errors of the
+    # contributions and of the requantised result of the exact sum
+    exact = y.sum(axis=0)
+    bound = (scale / 2).sum(axis=0) + np.abs(exact).max() / 127 / 2 + 1e-6 * np.abs(y).sum(axis=0)
+    for r in range(n):
+        assert np.all(np.abs(out[r] - exact) <= bound * 1.01 + 1e-9)
+        assert np.array_equal(out[r], out[0])
+
+
+def test_int8_feedback_telescopes(oracle_lib):
+    # one rank, a constant gradient: what the quantiser lets through over K
+    # rounds adds up to K * x minus the residual left at the end
+    d, k = 256, 20
+    x = W.normal_inputs(1, d, 1.0, 9)
+    e = np.zeros_like(x)
+    total = np.zeros(d)
+    for _ in range(k):
+        xe = x[0].astype(np.float64) + e[0]
+        out, e, _ = oracle.int8_ef_allreduce(x, e, op="sum")
+        total += xe - e[0]   # = y^ of this round
+    assert np.allclose(total, k * x[0].astype(np.float64) - e[0], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_int8_payload_volume(oracle_lib, n):
+    d = 128 * n * 3
+    x = np.ones((n, d), dtype=np.float32)
+    _, _, st = oracle.int8_ef_allreduce(x, np.zeros_like(x))
+    assert np.all(st["sent"] == 2 * (n - 1) * d // n) and st["steps"] == 2 * (n - 1)
