@@ -37,16 +37,16 @@ int64_t chunk_lo(int64_t count, int n, int c) { return (int64_t)(((__int128)c * 
 
 // ---- pointer checks -----------------------------------------------------------
 
-typedef CUresult (*PointerGetAttributeFn)(void*, CUpointer_attribute, CUdeviceptr);
+typedef CUresult (*PointerGetAttributesFn)(unsigned int, CUpointer_attribute*, void**, CUdeviceptr);
 
-PointerGetAttributeFn pointer_attr_fn() {
-  static PointerGetAttributeFn fn = [] {
+PointerGetAttributesFn pointer_attrs_fn() {
+  static PointerGetAttributesFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       p = nullptr;
-    return reinterpret_cast<PointerGetAttributeFn>(p);
+    return reinterpret_cast<PointerGetAttributesFn>(p);
   }();
   return fn;
 }
@@ -55,8 +55,8 @@ struct Range {
   uintptr_t lo, hi;
 };
 
-// Every range must be non-empty-or-null-free, element aligned, pairwise
-// disjoint, and lie inside device memory of the current device.
+// Every range must be non-null, element aligned, pairwise disjoint, and lie
+// inside device memory of the current device.
 int check_ranges(std::vector<Range>& rs, int esize) {
   for (const Range& r : rs) {
     if (r.lo == 0) return AR_ERR_INVALID_ARG;
@@ -68,9 +68,9 @@ int check_ranges(std::vector<Range>& rs, int esize) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  PointerGetAttributeFn attr = pointer_attr_fn();
-  if (!attr) return cuda_fail(cudaErrorNotSupported);
-  // ranges are sorted: one driver query per allocation they fall into
+  PointerGetAttributesFn attrs = pointer_attrs_fn();
+  if (!attrs) return cuda_fail(cudaErrorNotSupported);
+  // ranges are sorted: one driver query (four attributes) per allocation they fall into
   uintptr_t alloc_lo = 0, alloc_hi = 0;
   for (const Range& r : rs) {
     if (r.lo >= alloc_lo && r.hi <= alloc_hi && alloc_hi > alloc_lo) continue;
@@ -78,16 +78,14 @@ int check_ranges(std::vector<Range>& rs, int esize) {
     int ordinal = -1;
     CUdeviceptr start = 0;
     size_t size = 0;
-    if (attr(&mtype, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, (CUdeviceptr)r.lo) != CUDA_SUCCESS) return AR_ERR_INVALID_ARG;
-    if (mtype != CU_MEMORYTYPE_DEVICE) return AR_ERR_INVALID_ARG;
-    if (attr(&ordinal, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL, (CUdeviceptr)r.lo) != CUDA_SUCCESS || ordinal != dev)
-      return AR_ERR_INVALID_ARG;
-    if (attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, (CUdeviceptr)r.lo) != CUDA_SUCCESS ||
-        attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, (CUdeviceptr)r.lo) != CUDA_SUCCESS)
-      return AR_ERR_INVALID_ARG;
+    CUpointer_attribute which[4] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL,
+                                    CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+    void* out[4] = {&mtype, &ordinal, &start, &size};
+    if (attrs(4, which, out, (CUdeviceptr)r.lo) != CUDA_SUCCESS) return AR_ERR_INVALID_ARG;
+    if (mtype != CU_MEMORYTYPE_DEVICE || ordinal != dev || size == 0) return AR_ERR_INVALID_ARG;
     alloc_lo = (uintptr_t)start;
     alloc_hi = (uintptr_t)start + size;
-    if (r.hi > alloc_hi) return AR_ERR_INVALID_ARG;
+    if (r.lo < alloc_lo || r.hi > alloc_hi) return AR_ERR_INVALID_ARG;
   }
   return AR_OK;
 }

@@ -256,6 +256,31 @@ def fit_alpha_beta(points, phases, bw_factor):
     return a / phases, b / bw_factor
 
 
+def graph_time(call, torch, stream, reps=20):
+    """Per-call device time of `call` replayed from a CUDA graph, or None if
+    the call cannot be captured."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(reps):
+                if call(int(side.cuda_stream)):
+                    raise RuntimeError("call failed during capture")
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (5 * reps)
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+
+
 def run_sweep(args, ws, rank, dev, torch, ar):
     """Per-rank message 4 KiB .. 1 GiB x N in --sweep-ranks (N x size <= 64 GiB)
     x {f32, bf16} x {SUM, MAX} x {ring, tree, ring_stepwise, tree_stepwise},
@@ -289,8 +314,8 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                                 break
                             count = nbytes // es
                             views = [b[:nbytes] for b in bufs]
-                            call = lambda: ar.ar_allreduce(views, count=count, dtype=dt, op=op, algo=algo,
-                                                           stream=sid)
+                            call = lambda s=None: ar.ar_allreduce(views, count=count, dtype=dt, op=op, algo=algo,
+                                                                  stream=sid if s is None else s)
                             for _ in range(3):
                                 ar.check(call(), "sweep")
                             torch.cuda.synchronize()
@@ -312,6 +337,9 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                             rec = {"nranks": n, "bytes_per_rank": nbytes, "dtype": dt, "op": op, "algo": algo,
                                    "us": t * 1e6, "effective_gbs": 2 * n * nbytes / t / 1e9,
                                    "algbw_gbs": nbytes / t / 1e9, "l2_resident": 2 * n * nbytes <= 129e6}
+                            if nbytes <= (1 << 20):
+                                # device time without the host's per-call cost: 20 calls replayed from a graph
+                                rec["graph_us"] = graph_time(call, torch, stream)
                             out.write(json.dumps(rec) + "\n")
                             npoints += 1
                             if op == "sum":
