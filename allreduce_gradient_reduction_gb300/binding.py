@@ -33,7 +33,7 @@ EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "a
            "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
            "ar_last_cuda_error", "ar_strerror", "ar_version", "ar_kernel_launches", "ar_reducer_create",
            "ar_reducer_mark_ready", "ar_reducer_finish", "ar_reducer_destroy", "ar_reducer_buckets",
-           "ar_reducer_set_max_blocks")
+           "ar_reducer_set_max_blocks", "ar_plan_create", "ar_plan_run", "ar_plan_destroy")
 
 
 class ArError(RuntimeError):
@@ -76,6 +76,9 @@ def _load():
     L.ar_reducer_destroy.argtypes = [vp]
     L.ar_reducer_buckets.argtypes = [vp]
     L.ar_reducer_set_max_blocks.argtypes = [vp, cint]
+    L.ar_plan_create.argtypes = [cint, pp, cint, i64, cint, cint, cint, cint, ctypes.POINTER(vp)]
+    L.ar_plan_run.argtypes = [vp, vp]
+    L.ar_plan_destroy.argtypes = [vp]
     for name in EXPORTS:
         if name != "ar_strerror":
             getattr(L, name).restype = cint
@@ -247,6 +250,35 @@ class Reducer:
     def close(self):
         if self.handle:
             lib.ar_reducer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+PLAN_KIND = {"allreduce": 0, "reduce_scatter": 1, "all_gather": 2, "reduce": 3}
+
+
+class Plan:
+    """A prepared collective (ar_plan_*): arguments checked and launch tables
+    built once; ``run(stream)`` only enqueues the kernels."""
+
+    def __init__(self, kind, bufs, count=None, dtype="f32", op="sum", algo="ring", root=0):
+        h = ctypes.c_void_p()
+        check(lib.ar_plan_create(PLAN_KIND[kind] if isinstance(kind, str) else int(kind), _ptr_array(bufs),
+                                 len(bufs), _count(bufs, count), _enum(DTYPE, dtype), _enum(OP, op), _enum(ALGO, algo),
+                                 int(root), ctypes.byref(h)), "ar_plan_create")
+        self.handle = h
+
+    def run(self, stream=None) -> int:
+        return lib.ar_plan_run(self.handle, _stream(stream))
+
+    def close(self):
+        if self.handle:
+            lib.ar_plan_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -249,15 +249,20 @@ struct TableBuilder {
 };
 
 // phases: 1 ReduceScatter, 2 AllGather, 3 AllReduce; root >= 0: Reduce to root
-int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases,
-               cudaStream_t stream, int root = -1) {
+// Checks the arguments and builds the launch of a collective.  *empty is set
+// when there is nothing to do (count 0 or one rank).
+int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases, int root,
+                     TableBuilder& tb, Job& j, bool* empty) {
+  *empty = false;
   int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
   if (rc) return rc;
   if ((algo == AR_NAIVE || algo == AR_DBTREE) && phases != 3) return AR_ERR_UNSUPPORTED;  // AllReduce / Reduce only
   if (algo == AR_DBTREE && root >= 0) return AR_ERR_UNSUPPORTED;
   if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
-  if (count == 0 || nranks == 1) return AR_OK;
-  TableBuilder tb{nranks, {}, {}};
+  if (count == 0 || nranks == 1) {
+    *empty = true;
+    return AR_OK;
+  }
   int row = tb.add_row(bufs);
   if (algo == AR_NAIVE) {
     // index order x[0], x[1], ..., x[N-1] is the ring order of chunk N-1
@@ -269,8 +274,19 @@ int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, 
   } else {
     for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
   }
-  Job j{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};  // naive = ring kernel
+  j = Job{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};  // naive = ring kernel
   j.root = root;
+  return AR_OK;
+}
+
+// phases: 1 ReduceScatter, 2 AllGather, 3 AllReduce; root >= 0: Reduce to root
+int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases,
+               cudaStream_t stream, int root = -1) {
+  TableBuilder tb{nranks, {}, {}};
+  Job j{};
+  bool empty = false;
+  int rc = build_collective(bufs, nranks, count, dtype, op, algo, phases, root, tb, j, &empty);
+  if (rc || empty) return rc;
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
 }
 
@@ -338,6 +354,13 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 // 通信" §DDP 梯度同步中的地位).  Here the compute work runs on the caller's
 // compute stream and the bucket reductions on a communication stream; an event
 // recorded when a bucket becomes ready orders the two.
+
+// A collective whose arguments were checked and whose launch tables were
+// built once: running it only enqueues the kernels.
+struct ar_plan {
+  Job job{};
+  std::vector<SegTable> tables;
+};
 
 struct ar_reducer {
   int nranks = 0, ntensors = 0, nbuckets = 0;
@@ -676,6 +699,58 @@ int ar_reducer_buckets(const ar_reducer* red) { return red ? red->nbuckets : AR_
 int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks) {
   if (!red || max_blocks < 0) return AR_ERR_INVALID_ARG;
   red->job.max_grid = max_blocks;
+  return AR_OK;
+}
+
+int ar_plan_create(int kind, void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                   int root, ar_plan** out) {
+  if (!out) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  int phases = 3;
+  switch (kind) {
+    case AR_PLAN_ALLREDUCE: root = -1; break;
+    case AR_PLAN_REDUCE_SCATTER: phases = 1, root = -1; break;
+    case AR_PLAN_ALL_GATHER: phases = 2, root = -1, op = AR_SUM; break;
+    case AR_PLAN_REDUCE:
+      if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+      if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+      break;
+    default: return AR_ERR_INVALID_ARG;
+  }
+  TableBuilder tb{nranks, {}, {}};
+  Job j{};
+  bool empty = false;
+  int rc = build_collective(bufs, nranks, count, dtype, op, algo, phases, root, tb, j, &empty);
+  if (rc) return rc;
+  ar_plan* plan = new ar_plan;
+  plan->job = j;
+  if (!empty) {
+    rc = tb.for_each_table([&](SegTable& t) {
+      plan->tables.push_back(t);
+      return AR_OK;
+    });
+    if (rc) {
+      delete plan;
+      return rc;
+    }
+  }
+  *out = plan;
+  return AR_OK;
+}
+
+int ar_plan_run(const ar_plan* plan, ar_stream_t stream) {
+  if (!plan) return AR_ERR_INVALID_ARG;
+  for (const SegTable& t : plan->tables) {
+    SegTable copy = t;  // the launchers fill in the tile layout
+    int rc = run_table(plan->job, copy, (cudaStream_t)stream);
+    if (rc) return rc;
+  }
+  return AR_OK;
+}
+
+int ar_plan_destroy(ar_plan* plan) {
+  if (!plan) return AR_ERR_INVALID_ARG;
+  delete plan;
   return AR_OK;
 }
 

@@ -21,6 +21,7 @@ namespace ar {
 
 constexpr int kQ8 = 128;
 constexpr int kQ8Block = 256;  // threads per block: 8 warps, 8 quantisation blocks
+constexpr int kQ8Group = 8;    // ranks whose loads are in flight together
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -85,7 +86,7 @@ __device__ __forceinline__ Lane4 encode(const Lane4& x, const Lane4& e, float* e
   return yh;
 }
 
-__global__ void __launch_bounds__(kQ8Block) int8_ef_kernel(const __grid_constant__ Int8Args a) {
+__global__ void __launch_bounds__(kQ8Block, 2) int8_ef_kernel(const __grid_constant__ Int8Args a) {
   __shared__ float s_scale[kQ8Block / 32][kMaxRanks];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t count = a.count;
@@ -102,10 +103,10 @@ __global__ void __launch_bounds__(kQ8Block) int8_ef_kernel(const __grid_constant
   if (c_first == c_last) {
     // the whole block is in chunk c: fold the ranks in ring order as they come
     const int c = c_first;
-    for (int p0 = 0; p0 < n; p0 += 4) {
-      Lane4 xs[4], es[4];
+    for (int p0 = 0; p0 < n; p0 += kQ8Group) {
+      Lane4 xs[kQ8Group], es[kQ8Group];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {  // loads of up to 4 ranks in flight
+      for (int g = 0; g < kQ8Group; ++g) {  // loads of up to kQ8Group ranks in flight
         if (p0 + g < n) {
           const int r = rot(c + 1 + p0 + g, n);
           xs[g] = load4(a.x[r], e0, count, vec);
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kQ8Block) int8_ef_kernel(const __grid_constant
         }
       }
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < kQ8Group; ++g) {
         if (p0 + g < n) {
           const int r = rot(c + 1 + p0 + g, n);
           const Lane4 yh = encode(xs[g], es[g], a.e[r], e0, count, vec);

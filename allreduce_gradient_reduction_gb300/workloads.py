@@ -123,6 +123,12 @@ def sweep_points(dtypes=("f32", "bf16")):
     return pts
 
 
+def uniform_rank(rank: int, count: int, dtype: str, config: int = CONFIG_SWEEP) -> np.ndarray:
+    """One rank of uniform_inputs (same draws), for buffers too large to stack."""
+    x = rng(config, rank).uniform(-1.0, 1.0, size=count).astype(np.float32)
+    return f32_to_bf16_bits_truncate(x) if dtype == "bf16" else x
+
+
 def uniform_inputs(nranks: int, count: int, dtype: str, config: int = CONFIG_SWEEP) -> np.ndarray:
     """uniform(-1, 1) values; bf16 as truncated bit patterns."""
     xs = np.stack([rng(config, r).uniform(-1.0, 1.0, size=count).astype(np.float32) for r in range(nranks)])

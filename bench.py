@@ -340,6 +340,18 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                             if nbytes <= (1 << 20):
                                 # device time without the host's per-call cost: 20 calls replayed from a graph
                                 rec["graph_us"] = graph_time(call, torch, stream)
+                                # host cost of a prepared call (checks and tables done once)
+                                plan = ar.Plan("allreduce", views, count=count, dtype=dt, op=op, algo=algo)
+                                for _ in range(3):
+                                    ar.check(plan.run(sid), "plan")
+                                torch.cuda.synchronize()
+                                e0.record(stream)
+                                for _ in range(k):
+                                    plan.run(sid)
+                                e1.record(stream)
+                                torch.cuda.synchronize()
+                                rec["plan_us"] = e0.elapsed_time(e1) * 1e3 / k
+                                plan.close()
                             out.write(json.dumps(rec) + "\n")
                             npoints += 1
                             if op == "sum":

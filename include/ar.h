@@ -302,6 +302,24 @@ int ar_reducer_buckets(const ar_reducer* red);
  * to a few channels.  Results do not depend on it. */
 int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks);
 
+/*
+ * Prepared collectives.  A training loop reduces the same buffers every
+ * step; a plan checks the arguments and builds the launch tables once, and
+ * each run only enqueues the kernels (same results as the direct call).
+ *   kind    AR_PLAN_ALLREDUCE, AR_PLAN_REDUCE_SCATTER, AR_PLAN_ALL_GATHER
+ *           (op ignored) or AR_PLAN_REDUCE (root used; others ignore it)
+ *   other arguments as the corresponding direct call; *out receives the plan
+ * The buffers must stay allocated while the plan is used: a run does not
+ * check them again.  A plan may be run from any thread, on any stream, any
+ * number of times; destroy it when no run is pending.
+ */
+typedef struct ar_plan ar_plan;
+enum { AR_PLAN_ALLREDUCE = 0, AR_PLAN_REDUCE_SCATTER = 1, AR_PLAN_ALL_GATHER = 2, AR_PLAN_REDUCE = 3 };
+int ar_plan_create(int kind, void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
+                   int root, ar_plan** out);
+int ar_plan_run(const ar_plan* plan, ar_stream_t stream);
+int ar_plan_destroy(ar_plan* plan);
+
 /* Chunk c of a rank buffer of `count` elements split N ways: [*lo, *hi).
  * Host-only; errors: AR_ERR_INVALID_ARG. */
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);

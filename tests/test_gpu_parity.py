@@ -538,3 +538,43 @@ def test_int8_ef_unaligned_and_rejects(ar):
     assert_same(from_dev(ed, "f32"), want_e, "f32", "e unaligned")
     assert ar.ar_allreduce_int8_ef(xd, ed, count=count, op="max") == ar.AR_ERR_UNSUPPORTED
     assert ar.ar_allreduce_int8_ef(xd, xd, count=count) == ar.AR_ERR_INVALID_ARG  # grads overlap residuals
+
+
+# --------------------------------------------------------------------------
+# Large sweep points, sampled: the full-size buffers are generated rank by
+# rank; the oracle carries the sampled positions (and every chunk boundary)
+# through its messages
+# --------------------------------------------------------------------------
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n,nbytes,dtype,op,algo", [
+    (16, 256 << 20, "bf16", "sum", "ring"),
+    (64, 64 << 20, "f32", "max", "tree"),
+    (2, 1 << 30, "f32", "sum", "ring"),
+    (8, 512 << 20, "bf16", "sum", "dbtree"),
+])
+def test_large_sweep_points_sampled(ar, n, nbytes, dtype, op, algo):
+    es = 2 if dtype == "bf16" else 4
+    count = nbytes // es
+    pos = sample_positions(count, n, 1 << 14, 11)
+    if algo == "dbtree":
+        pos = np.unique(np.concatenate([pos, [count // 2 - 1, count // 2]]))
+    bufs, xs = [], []
+    for r in range(n):
+        row = W.uniform_rank(r, count, dtype)
+        xs.append(row[pos])
+        bufs.append(to_dev(row))
+        del row
+    xs = np.stack(xs)
+    with np.errstate(all="ignore"):
+        want, _ = oracle.allreduce(xs, algo=algo, op=op, dtype=dtype, count=count, positions=pos)
+    ar.check(ar.ar_allreduce(bufs, count=count, dtype=dtype, op=op, algo=algo), "large sweep point")
+    torch.cuda.synchronize()
+    idx = torch.from_numpy(pos).cuda()
+    for r in (0, n // 2, n - 1):
+        got = bufs[r][idx].cpu().numpy()
+        if dtype == "bf16":
+            got = got.view(np.uint16)
+        assert_same(got, want[r], dtype, f"rank {r}")
+    for r in range(1, n):
+        assert torch.equal(bufs[r], bufs[0]), r
