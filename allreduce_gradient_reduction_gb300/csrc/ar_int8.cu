@@ -15,13 +15,15 @@
 //
 // One warp owns one 128-element block: 4 consecutive floats per lane (one
 // 16-byte access per rank and array), warp shuffles give the block maxima.
+// Ranks are taken one at a time; the latency of their loads is hidden by the
+// 48 warps an SM keeps resident (40 registers a thread).
 #include "ar_fused.cuh"
 
 namespace ar {
 
 constexpr int kQ8 = 128;
 constexpr int kQ8Block = 256;  // threads per block: 8 warps, 8 quantisation blocks
-constexpr int kQ8Group = 8;    // ranks whose loads are in flight together
+constexpr int kQ8MinBlocks = 6; // resident blocks per SM: 48 warps hide the loads of a rank at a time
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -34,6 +36,25 @@ __device__ __forceinline__ float q8_code(float y, float s) {
   if (s == 0.0f) return 0.0f;
   const int q = __float2int_rn(__fdiv_rn(y, s));  // round half to even; |y / s| <= 127 (+ rounding)
   return (float)min(max(q, -127), 127);
+}
+
+// The same code from a reciprocal: t = y * RN(1/s) lies within 1.5 * 2^-23 |y/s|
+// of the correctly rounded quotient RN(y/s) (two roundings of 2^-24 each,
+// plus RN(y/s)'s own).  When t is farther than |t| * 2^-18 from every
+// half-integer, RN(y/s) rounds to the same integer as t, and t is rounded
+// with the classic add-and-subtract of 1.5 * 2^23 (exact round-half-even for
+// |t| < 2^22; a result of zero comes out +0, as the integer path gives).
+// Anything else (near a tie, s = 0 or a non-finite t) takes q8_code itself.
+// Saves the per-element divide and the float-int-float round trip.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ float q8_code_recip(float y, float s, float r) {
+  const float t = __fmul_rn(y, r);
+  const float k = __fsub_rn(__fadd_rn(t, kRoundMagic), kRoundMagic);
+  const float at = fabsf(t);
+  const float slack = __fsub_rn(0.5f, fabsf(__fsub_rn(t, k)));
+  if (!(at < 256.0f) || !(slack > __fmul_rn(at, 0x1p-18f))) return q8_code(y, s);
+  return fminf(fmaxf(k, -127.0f), 127.0f);
 }
 
 __device__ __forceinline__ int chunk_of(int64_t e, int64_t count, int n) {
@@ -77,16 +98,17 @@ __device__ __forceinline__ Lane4 encode(const Lane4& x, const Lane4& e, float* e
     m = fmaxf(m, fabsf(y.v[k]));
   }
   const float s = __fdiv_rn(warp_max(m), 127.0f);
+  const float rs = __frcp_rn(s);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    yh.v[k] = __fmul_rn(q8_code(y.v[k], s), s);
+    yh.v[k] = __fmul_rn(q8_code_recip(y.v[k], s, rs), s);
     en.v[k] = __fsub_rn(y.v[k], yh.v[k]);
   }
   store4(ep, e0, count, vec, en);
   return yh;
 }
 
-__global__ void __launch_bounds__(kQ8Block, 2) int8_ef_kernel(const __grid_constant__ Int8Args a) {
+__global__ void __launch_bounds__(kQ8Block, kQ8MinBlocks) int8_ef_kernel(const __grid_constant__ Int8Args a) {
   __shared__ float s_scale[kQ8Block / 32][kMaxRanks];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t count = a.count;
@@ -103,25 +125,11 @@ __global__ void __launch_bounds__(kQ8Block, 2) int8_ef_kernel(const __grid_const
   if (c_first == c_last) {
     // the whole block is in chunk c: fold the ranks in ring order as they come
     const int c = c_first;
-    for (int p0 = 0; p0 < n; p0 += kQ8Group) {
-      Lane4 xs[kQ8Group], es[kQ8Group];
+    for (int p = 0; p < n; ++p) {
+      const int r = rot(c + 1 + p, n);
+      const Lane4 yh = encode(load4(a.x[r], e0, count, vec), load4(a.e[r], e0, count, vec), a.e[r], e0, count, vec);
 #pragma unroll
-      for (int g = 0; g < kQ8Group; ++g) {  // loads of up to kQ8Group ranks in flight
-        if (p0 + g < n) {
-          const int r = rot(c + 1 + p0 + g, n);
-          xs[g] = load4(a.x[r], e0, count, vec);
-          es[g] = load4(a.e[r], e0, count, vec);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < kQ8Group; ++g) {
-        if (p0 + g < n) {
-          const int r = rot(c + 1 + p0 + g, n);
-          const Lane4 yh = encode(xs[g], es[g], a.e[r], e0, count, vec);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) acc[k] = p0 + g == 0 ? yh.v[k] : __fadd_rn(acc[k], yh.v[k]);
-        }
-      }
+      for (int k = 0; k < 4; ++k) acc[k] = p == 0 ? yh.v[k] : __fadd_rn(acc[k], yh.v[k]);
     }
   } else {
     // the block straddles chunks: first every rank's block scale, then each
@@ -166,10 +174,11 @@ __global__ void __launch_bounds__(kQ8Block, 2) int8_ef_kernel(const __grid_const
     for (int k = 0; k < 4; ++k)
       if (e0 + k < count && (c_first == c_last || chunk_of(e0 + k, count, n) == c)) m = fmaxf(m, fabsf(acc[k]));
     const float s = __fdiv_rn(warp_max(m), 127.0f);
+    const float rs = __frcp_rn(s);
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       if (c_first == c_last || (e0 + k < count && chunk_of(e0 + k, count, n) == c))
-        res.v[k] = __fmul_rn(q8_code(acc[k], s), s);
+        res.v[k] = __fmul_rn(q8_code_recip(acc[k], s, rs), s);
   }
   for (int r = 0; r < n; ++r) store4(a.x[r], e0, count, vec, res);
   __syncwarp();  // s_scale is reused by the warp's next block

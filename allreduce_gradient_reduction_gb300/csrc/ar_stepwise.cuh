@@ -46,16 +46,22 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   return v;
 }
 
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Grid-wide barrier with a bounded wait.  Returns false when the kernel must
 // stop: this block timed out (it then raises `abort` for the others and
 // records AR_ERR_TIMEOUT in the sticky status) or another block already did.
+// The block's stores are ordered before its arrival by the CTA barrier and
+// the gpu-scope release of the arrival (release is cumulative); the acquire
+// load that sees the last arrival orders every later load after all of them.
 __device__ bool grid_barrier(SyncBlock* sb, unsigned target, bool arrive, int64_t timeout_ns) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    __threadfence();
-    if (arrive) atomicAdd(&sb->counter, 1u);
+    if (arrive) red_release_add(&sb->counter, 1u);
     const uint64_t t0 = global_ns();
     unsigned spins = 0;
     while (ld_acquire_u32(&sb->counter) < target) {
@@ -69,9 +75,8 @@ __device__ bool grid_barrier(SyncBlock* sb, unsigned target, bool arrive, int64_
         ok = 0;
         break;
       }
-      __nanosleep(128);
+      if (spins > 32) __nanosleep(64);
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();

@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--algo", default="ring", help="ring | tree | ring_stepwise | tree_stepwise")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-procs", type=int, default=0,
+                   help="processes for the CPU oracle baseline (default: every host core)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--count", type=int, default=0,
                    help="elements per rank (default: the full workload); smaller counts are for profiling")
@@ -192,18 +194,94 @@ def profiled_traffic():
 # the CPU oracle as the baseline
 # ---------------------------------------------------------------------------
 
-def oracle_sample_time(n: int, count: int, steps: int = 1):
-    """Time the oracle's ring AllReduce (single thread) on n x count bf16 of
-    the same input recipe.  Returns (seconds per pass, GB/s in the metric)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(conn):
+    """One process of OraclePool: holds its element range of the input and
+    runs the oracle's ring AllReduce on it on request, through the oracle's
+    sampled-positions mode (an element's fold depends only on its own column
+    and its chunk)."""
+    import numpy as np
+    import oracle
+    oracle.lib()
+    x = pos = count = None
+    while True:
+        msg = conn.recv()
+        if msg[0] == "load":
+            _, x, lo, count = msg
+            pos = np.arange(lo, lo + x.shape[1], dtype=np.int64)
+            conn.send(0.0)
+        elif msg[0] == "run":
+            t0 = time.perf_counter()
+            oracle.allreduce(x, algo="ring", op="sum", dtype="bf16", count=count, positions=pos)
+            conn.send(time.perf_counter() - t0)
+        else:
+            return
+
+
+class OraclePool:
+    """The oracle, as it stands, on every host core: each spawned process (never
+    forked, so no CUDA state is inherited) keeps one element range of the
+    input, loaded before any timing, so a timed pass moves no data between
+    processes."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for _ in range(procs):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b,), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+
+    def load(self, x):
+        import numpy as np
+        count = x.shape[1]
+        b = np.linspace(0, count, len(self.conns) + 1).astype(np.int64)
+        for i, c in enumerate(self.conns):
+            c.send(("load", np.ascontiguousarray(x[:, b[i]:b[i + 1]]), int(b[i]), count))
+        for c in self.conns:
+            c.recv()
+        return [int(b[i + 1] - b[i]) for i in range(len(self.conns))]
+
+    def run(self):
+        """One pass over the whole input; returns (wall seconds, per-process seconds)."""
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(("run",))
+        per = [c.recv() for c in self.conns]
+        return time.perf_counter() - t0, per
+
+    def close(self):
+        for c in self.conns:
+            c.send(("stop",))
+        for p in self.procs:
+            p.join(timeout=60)
+
+
+def oracle_sample_time(n: int, count: int, procs: int):
+    """Time the oracle's ring AllReduce on n x count bf16 of the same input
+    recipe, split over `procs` processes.  Returns (seconds per pass, GB/s in
+    the metric, median GB/s of one process on its own range)."""
     import oracle
     from allreduce_gradient_reduction_gb300 import workloads as W
     oracle.build()
     x = W.large_inputs(n, count)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle.allreduce(x, algo="ring", op="sum", dtype="bf16")
-    dt = (time.perf_counter() - t0) / steps
-    return dt, 2 * n * count * 2 / dt / 1e9
+    pool = OraclePool(procs)
+    try:
+        widths = pool.load(x)
+        dt, per = pool.run()
+    finally:
+        pool.close()
+    per_gbs = sorted(2 * n * w * 2 / max(p, 1e-9) / 1e9 for w, p in zip(widths, per))
+    return dt, 2 * n * count * 2 / dt / 1e9, per_gbs[len(per_gbs) // 2]
 
 
 def run_reference(args, ws, rank):
@@ -216,12 +294,18 @@ def run_reference(args, ws, rank):
     import oracle
     oracle.build()
     x = W.large_inputs(n, sample)
-    for _ in range(args.warmup):
-        oracle.allreduce(x, algo="ring", op="sum", dtype="bf16")
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.allreduce(x, algo="ring", op="sum", dtype="bf16")
-    dt = (time.perf_counter() - t0) / args.steps
+    procs = args.cpu_procs or host_cores()
+    pool = OraclePool(procs)
+    try:
+        pool.load(x)
+        for _ in range(args.warmup):
+            pool.run()
+        total = 0.0
+        for _ in range(args.steps):
+            total += pool.run()[0]
+    finally:
+        pool.close()
+    dt = total / max(args.steps, 1)
     value = 2 * n * sample * 2 / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -229,9 +313,10 @@ def run_reference(args, ws, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "nranks": n, "count_per_rank": W.LARGE["count"],
                    "sample_count_per_rank": sample, "algo": "ring", "op": "sum"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "kind": "oracle",
                          "sample": f"{n} ranks x {sample} bf16 per step (1/{W.LARGE['count'] // sample} of the "
-                                   "workload), literal message simulation, one thread"},
+                                   f"workload), literal message simulation, element ranges split over {procs} "
+                                   "processes"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -424,10 +509,11 @@ class LargeWorkload:
 
     def cpu_baseline(self):
         sample = self.count // 4
-        dt, gbs = oracle_sample_time(self.n, sample)
-        return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        procs = self.args.cpu_procs or host_cores()
+        dt, gbs, one = oracle_sample_time(self.n, sample, procs)
+        return {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle", "one_process_gbs": one,
                 "sample": f"{self.n} ranks x {sample} bf16 (1/4 of the workload), one literal ring pass, "
-                          f"{dt:.2f} s, one thread"}
+                          f"{dt:.2f} s, element ranges split over {procs} processes"}
 
 
 class BucketWorkload:

@@ -525,6 +525,45 @@ def test_int8_ef_matches_oracle(ar, n):
                 x, e = W.normal_inputs(n, count, 1e-3, 2700 + it + n + count), got_e
 
 
+def int8_tie_inputs(n, count, seed):
+    """Per 128-block: one element at the block maximum m, the others at, or a
+    hair beside, the quantisation ties (j + 1/2) * s with s = m / 127 -- some
+    within two ulps, some a relative 2^-24 .. 2^-12 away -- so that the code
+    rounding meets ties and near-ties of every kind."""
+    g = np.random.default_rng(seed)
+    x = np.zeros((n, count), np.float32)
+    for r in range(n):
+        for b0 in range(0, count, 128):
+            w = min(128, count - b0)
+            m = np.float32(g.uniform(0.5, 2.0) * 2.0 ** int(g.integers(-30, 30)))
+            s = np.float32(m / np.float32(127.0))
+            j = g.integers(-127, 127, size=w).astype(np.float64)
+            rel = np.where(g.random(w) < 0.5, 0.0, g.choice([-1, 1], w) * 2.0 ** g.uniform(-24, -12, w))
+            y = ((j + 0.5) * (1.0 + rel) * np.float64(s)).astype(np.float32)
+            ulps = g.integers(-2, 3, size=w)
+            for k in range(2):
+                y = np.where(ulps > k, np.nextafter(y, np.float32(np.inf)), y)
+                y = np.where(ulps < -k, np.nextafter(y, np.float32(-np.inf)), y)
+            y = np.clip(y, -m, m)
+            y[int(g.integers(0, w))] = m if g.random() < 0.5 else -m
+            x[r, b0:b0 + w] = y
+    return x
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_int8_ef_rounding_ties(ar, n):
+    for count in (128 * 8 * n, 128 * 5 * n + 45):
+        x = int8_tie_inputs(n, count, 90 + n + count)
+        e = np.zeros_like(x)
+        for op in ("sum", "avg"):
+            want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op=op)
+            xd = [to_dev(x[r]) for r in range(n)]
+            ed = [to_dev(e[r]) for r in range(n)]
+            ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op=op), "int8_ef ties")
+            assert_same(from_dev(xd, "f32"), want_x, "f32", f"x ties n={n} count={count} {op}")
+            assert_same(from_dev(ed, "f32"), want_e, "f32", f"e ties n={n} count={count} {op}")
+
+
 def test_int8_ef_unaligned_and_rejects(ar):
     n, count = 4, 1000
     x = W.normal_inputs(n, count, 1.0, 31)
