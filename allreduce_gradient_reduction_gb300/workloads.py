@@ -129,6 +129,19 @@ def uniform_rank(rank: int, count: int, dtype: str, config: int = CONFIG_SWEEP) 
     return f32_to_bf16_bits_truncate(x) if dtype == "bf16" else x
 
 
+def uniform_rank_device(rank: int, count: int, dtype: str, torch, config: int = CONFIG_SWEEP, device="cuda"):
+    """uniform(-1, 1) drawn on the device by torch's seeded generator, for
+    buffers too large to draw on the host (not the same values as
+    uniform_rank).  f32 as is; bf16 rounded to nearest and returned as int16
+    bit patterns."""
+    g = torch.Generator(device=device)
+    g.manual_seed(BASE_SEED + 1000 * config + rank)
+    x = torch.rand(count, generator=g, device=device, dtype=torch.float32).mul_(2.0).sub_(1.0)
+    if dtype == "bf16":
+        return x.to(torch.bfloat16).view(torch.int16)
+    return x
+
+
 def uniform_inputs(nranks: int, count: int, dtype: str, config: int = CONFIG_SWEEP) -> np.ndarray:
     """uniform(-1, 1) values; bf16 as truncated bit patterns."""
     xs = np.stack([rng(config, r).uniform(-1.0, 1.0, size=count).astype(np.float32) for r in range(nranks)])

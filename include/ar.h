@@ -176,7 +176,12 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
  *               each (all 2N ranges disjoint); both updated in place.  Start
  *               training with zeroed residuals.
  *   op          AR_SUM or AR_AVG (AR_MAX: AR_ERR_UNSUPPORTED)
- * Inputs must be finite.  Errors as ar_allreduce.
+ * Inputs must be finite.  Errors as ar_allreduce.  With 16-byte aligned
+ * buffers and N <= 8 the kernel streams the inputs through shared memory
+ * with bulk asynchronous copies; its waits on them are bounded like the
+ * step-wise barriers (ar_set_barrier_timeout_ns) and report AR_ERR_TIMEOUT
+ * through ar_device_status.  So this call, too, uses the per-device block the
+ * library allocates on first use (first call outside stream capture).
  */
 int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
                          ar_stream_t stream);
@@ -311,7 +316,14 @@ int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks);
  *   other arguments as the corresponding direct call; *out receives the plan
  * The buffers must stay allocated while the plan is used: a run does not
  * check them again.  A plan may be run from any thread, on any stream, any
- * number of times; destroy it when no run is pending.
+ * number of times, and captured into a CUDA graph (the first step-wise call
+ * on a device, plan or direct, must be made outside capture).  Each launch
+ * copies the plan's tables into its kernel parameters, so a plan may be
+ * destroyed as soon as its last run has returned, with kernels still pending.
+ * Step-wise runs on one device must not overlap in time (the shared barrier
+ * block, as for the direct calls).
+ * Errors: as the direct calls, at create; a run returns AR_ERR_CUDA on a
+ * launch failure and AR_ERR_INVALID_ARG for a NULL plan.
  */
 typedef struct ar_plan ar_plan;
 enum { AR_PLAN_ALLREDUCE = 0, AR_PLAN_REDUCE_SCATTER = 1, AR_PLAN_ALL_GATHER = 2, AR_PLAN_REDUCE = 3 };
@@ -327,20 +339,22 @@ int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);
 /*
  * Synchronises `stream`, then reads and clears the current device's
  * asynchronous status word: *status = AR_OK, or AR_ERR_TIMEOUT when a
- * step-wise barrier gave up waiting since the last read (the kernel then
- * stopped early and its buffers hold partial results).
+ * step-wise barrier or a wait of the 8-bit kernel gave up since the last read
+ * (the kernel then stopped early and its buffers hold partial results).
  * Errors: AR_ERR_INVALID_ARG (status NULL), AR_ERR_CUDA.
  */
 int ar_device_status(ar_stream_t stream, int* status);
 
-/* Time limit of one step-wise barrier wait, in nanoseconds (default 1e9).
- * Values <= 0 restore the default. */
+/* Time limit of one step-wise barrier wait (and of one wait of the 8-bit
+ * kernel), in nanoseconds (default 1e9).  Values <= 0 restore the default. */
 int ar_set_barrier_timeout_ns(int64_t ns);
 
 /* Test hook for failure detection: in the next step-wise launch, block 0
- * does not arrive at barrier `barrier` (0-based), so every wait on it runs out
- * and the kernel reports AR_ERR_TIMEOUT through ar_device_status.  -1 clears
- * the hook.  Nothing faults or hangs: every wait is bounded. */
+ * does not arrive at barrier `barrier` (0-based); in the next 8-bit call that
+ * streams through shared memory, block 0 skips its fill number `barrier`.
+ * Either way every wait on it runs out and the kernel reports AR_ERR_TIMEOUT
+ * through ar_device_status.  -1 clears the hook.  Nothing faults or hangs:
+ * every wait is bounded, and no copy is left in flight. */
 int ar_debug_skip_barrier(int barrier);
 
 /* The cudaError_t value behind the calling thread's most recent

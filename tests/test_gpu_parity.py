@@ -564,6 +564,38 @@ def test_int8_ef_rounding_ties(ar, n):
             assert_same(from_dev(ed, "f32"), want_e, "f32", f"e ties n={n} count={count} {op}")
 
 
+@pytest.mark.parametrize("skip", [0, 5])
+def test_int8_ef_staged_wait_timeout_is_reported(ar, skip):
+    """Block 0 of the staged 8-bit kernel skips one fill of its shared-memory
+    ring (test hook): its consumers' bounded waits run out, the kernel stops
+    with AR_ERR_TIMEOUT in the device status, no copy is left in flight, and
+    the next call is correct."""
+    n, count = 8, 1024 * 400
+    x = W.normal_inputs(n, count, 1e-3, 77)
+    e = np.zeros_like(x)
+    ar.ar_set_barrier_timeout_ns(50_000_000)  # 50 ms
+    try:
+        xd = [to_dev(x[r]) for r in range(n)]
+        ed = [to_dev(e[r]) for r in range(n)]
+        ar.ar_debug_skip_barrier(skip)
+        ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op="avg"), "launch")
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == ar.AR_ERR_TIMEOUT
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == 0
+        want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op="avg")
+        xd = [to_dev(x[r]) for r in range(n)]
+        ed = [to_dev(e[r]) for r in range(n)]
+        ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op="avg"), "after the timeout")
+        assert_same(from_dev(xd, "f32"), want_x, "f32", "x after timeout")
+        assert_same(from_dev(ed, "f32"), want_e, "f32", "e after timeout")
+        rc, st = ar.ar_device_status()
+        assert rc == 0 and st == 0
+    finally:
+        ar.ar_debug_skip_barrier(-1)
+        ar.ar_set_barrier_timeout_ns(0)
+
+
 def test_int8_ef_unaligned_and_rejects(ar):
     n, count = 4, 1000
     x = W.normal_inputs(n, count, 1.0, 31)
@@ -617,3 +649,36 @@ def test_large_sweep_points_sampled(ar, n, nbytes, dtype, op, algo):
         assert_same(got, want[r], dtype, f"rank {r}")
     for r in range(1, n):
         assert torch.equal(bufs[r], bufs[0]), r
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype,op,algo", [("f32", "sum", "ring"), ("bf16", "max", "tree")])
+def test_largest_sweep_point_sampled(ar, dtype, op, algo):
+    """The sweep's largest point: 64 ranks x 1 GiB (64 GiB of rank buffers),
+    drawn on the device; sampled positions and every chunk boundary go
+    through the oracle."""
+    n, nbytes = 64, 1 << 30
+    free, _ = torch.cuda.mem_get_info()
+    if free < n * nbytes + (8 << 30):
+        pytest.skip("needs about 72 GiB of free device memory")
+    es = 2 if dtype == "bf16" else 4
+    count = nbytes // es
+    pos = sample_positions(count, n, 1 << 14, 12)
+    idx = torch.from_numpy(pos).cuda()
+    bufs = [W.uniform_rank_device(r, count, dtype, torch) for r in range(n)]
+    xs = np.stack([b[idx].cpu().numpy() for b in bufs])
+    if dtype == "bf16":
+        xs = xs.view(np.uint16)
+    with np.errstate(all="ignore"):
+        want, _ = oracle.allreduce(xs, algo=algo, op=op, dtype=dtype, count=count, positions=pos)
+    ar.check(ar.ar_allreduce(bufs, count=count, dtype=dtype, op=op, algo=algo), "largest sweep point")
+    torch.cuda.synchronize()
+    for r in (0, 1, n // 2, n - 1):
+        got = bufs[r][idx].cpu().numpy()
+        if dtype == "bf16":
+            got = got.view(np.uint16)
+        assert_same(got, want[r], dtype, f"rank {r}")
+    for r in range(1, n):
+        assert torch.equal(bufs[r], bufs[0]), r
+    del bufs
+    torch.cuda.empty_cache()
