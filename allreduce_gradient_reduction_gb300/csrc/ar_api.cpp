@@ -454,11 +454,6 @@ int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks,
   a.avg = op == AR_AVG ? 1 : 0;
   a.vec = all_aligned16(grads, nranks) && all_aligned16(residuals, nranks) ? 1 : 0;
   a.fn = (float)nranks;
-  ar::SyncBlock* sb = nullptr;
-  if ((rc = sync_block(&sb))) return rc;
-  a.status = &sb->status;
-  a.timeout_ns = g_timeout_ns.load();
-  a.skip_fill = g_skip_barrier.exchange(-1);
   cudaError_t e = ar::launch_int8_ef(a, (cudaStream_t)stream);
   return e == cudaSuccess ? AR_OK : cuda_fail(e);
 }

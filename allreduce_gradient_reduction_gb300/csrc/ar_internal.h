@@ -78,10 +78,6 @@ struct Int8Args {
   int32_t avg;
   int32_t vec;          // every pointer 16-byte aligned
   float fn;
-  int64_t qb_begin;     // first 128-element block the launch covers (set by the launcher)
-  int* status;          // sticky device status: AR_ERR_TIMEOUT when a bounded wait gave up
-  int64_t timeout_ns;   // limit of one wait in the staged kernel
-  int32_t skip_fill;    // test hook: block 0 of the staged kernel skips this fill (-1: none)
 };
 
 // Launchers.  Each fills tab.seg[*].tile_begin and tab.ntiles for its own

@@ -880,27 +880,46 @@ def main():
         orders = ("ring", "tree", "ring_stepwise", "tree_stepwise")
         if not isinstance(wl, Gpt2Workload):
             orders += ("dbtree", "naive")
-        todo = [(a, {}) for a in orders if a != args.algo]
+        # (name, one call, algorithmic bytes of that call)
+        todo = [(a, (lambda a=a: step(a)), nbytes_step) for a in orders if a != args.algo]
         if isinstance(wl, Gpt2Workload):
-            todo += [("ring_literal", {"literal": True})]
+            todo += [("ring_literal", lambda: step("ring", literal=True), nbytes_step)]
         if isinstance(wl, BucketWorkload):
-            todo += [("int8_ef", {"int8": True}), ("ring_max", {"op": "max"})]  # MAX on the same data
-        for name, kw in todo:
-            algo = {"int8_ef": "ring", "ring_max": "ring"}.get(name, name.replace("_literal", ""))
+            # the residuals are read and written too: 4 N D floats
+            todo += [("int8_ef", lambda: step("ring", int8=True), 2 * nbytes_step),
+                     ("ring_max", lambda: step("ring", op="max"), nbytes_step)]  # MAX on the same data
+        if not isinstance(wl, Gpt2Workload):
+            # the other collectives on the same buffers, each against its own bytes:
+            # ReduceScatter and Reduce read N D and write D, AllGather and
+            # Broadcast read D and write (N - 1) D
+            per = nbytes_step // (2 * wl.n)  # D * b
+            c = dict(count=wl.count, dtype=wl.dtype, stream=sid)
+
+            def chk(rc):
+                if rc:
+                    raise ar.ArError(rc, "collective variant")
+
+            todo += [
+                ("reduce_scatter", lambda: chk(ar.ar_reduce_scatter(wl.bufs, op=wl.op, **c)), (wl.n + 1) * per),
+                ("all_gather", lambda: chk(ar.ar_all_gather(wl.bufs, **c)), wl.n * per),
+                ("reduce", lambda: chk(ar.ar_reduce(wl.bufs, op=wl.op, root=0, **c)), (wl.n + 1) * per),
+                ("broadcast", lambda: chk(ar.ar_broadcast(wl.bufs, root=0, **c)), wl.n * per),
+            ]
+        for name, call, nbytes in todo:
             for _ in range(3):
-                step(algo, **kw)
+                call()
             torch.cuda.synchronize()
             v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             k = max(10, args.steps // 10)
             v0.record(stream)
             for _ in range(k):
-                step(algo, **kw)
+                call()
             v1.record(stream)
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / k
-            variants[name] = {"ms_per_step": vms, "effective_gbs": nbytes_step / (vms / 1e3) / 1e9}
-            if name == "int8_ef":  # reads and writes gradients and residuals: 4 N D floats
-                variants[name]["hbm_gbs"] = 2 * nbytes_step / (vms / 1e3) / 1e9
+            variants[name] = {"ms_per_step": vms, "effective_gbs": nbytes / (vms / 1e3) / 1e9}
+            if nbytes != nbytes_step:
+                variants[name]["algorithmic_bytes"] = nbytes
 
     overlap = None
     if args.overlap and isinstance(wl, Gpt2Workload):

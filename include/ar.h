@@ -176,12 +176,7 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
  *               each (all 2N ranges disjoint); both updated in place.  Start
  *               training with zeroed residuals.
  *   op          AR_SUM or AR_AVG (AR_MAX: AR_ERR_UNSUPPORTED)
- * Inputs must be finite.  Errors as ar_allreduce.  With 16-byte aligned
- * buffers and N <= 8 the kernel streams the inputs through shared memory
- * with bulk asynchronous copies; its waits on them are bounded like the
- * step-wise barriers (ar_set_barrier_timeout_ns) and report AR_ERR_TIMEOUT
- * through ar_device_status.  So this call, too, uses the per-device block the
- * library allocates on first use (first call outside stream capture).
+ * Inputs must be finite.  Errors as ar_allreduce.
  */
 int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
                          ar_stream_t stream);
@@ -339,22 +334,20 @@ int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi);
 /*
  * Synchronises `stream`, then reads and clears the current device's
  * asynchronous status word: *status = AR_OK, or AR_ERR_TIMEOUT when a
- * step-wise barrier or a wait of the 8-bit kernel gave up since the last read
- * (the kernel then stopped early and its buffers hold partial results).
+ * step-wise barrier gave up waiting since the last read (the kernel then
+ * stopped early and its buffers hold partial results).
  * Errors: AR_ERR_INVALID_ARG (status NULL), AR_ERR_CUDA.
  */
 int ar_device_status(ar_stream_t stream, int* status);
 
-/* Time limit of one step-wise barrier wait (and of one wait of the 8-bit
- * kernel), in nanoseconds (default 1e9).  Values <= 0 restore the default. */
+/* Time limit of one step-wise barrier wait, in nanoseconds (default 1e9).
+ * Values <= 0 restore the default. */
 int ar_set_barrier_timeout_ns(int64_t ns);
 
 /* Test hook for failure detection: in the next step-wise launch, block 0
- * does not arrive at barrier `barrier` (0-based); in the next 8-bit call that
- * streams through shared memory, block 0 skips its fill number `barrier`.
- * Either way every wait on it runs out and the kernel reports AR_ERR_TIMEOUT
- * through ar_device_status.  -1 clears the hook.  Nothing faults or hangs:
- * every wait is bounded, and no copy is left in flight. */
+ * does not arrive at barrier `barrier` (0-based), so every wait on it runs out
+ * and the kernel reports AR_ERR_TIMEOUT through ar_device_status.  -1 clears
+ * the hook.  Nothing faults or hangs: every wait is bounded. */
 int ar_debug_skip_barrier(int barrier);
 
 /* The cudaError_t value behind the calling thread's most recent

@@ -564,38 +564,6 @@ def test_int8_ef_rounding_ties(ar, n):
             assert_same(from_dev(ed, "f32"), want_e, "f32", f"e ties n={n} count={count} {op}")
 
 
-@pytest.mark.parametrize("skip", [0, 5])
-def test_int8_ef_staged_wait_timeout_is_reported(ar, skip):
-    """Block 0 of the staged 8-bit kernel skips one fill of its shared-memory
-    ring (test hook): its consumers' bounded waits run out, the kernel stops
-    with AR_ERR_TIMEOUT in the device status, no copy is left in flight, and
-    the next call is correct."""
-    n, count = 8, 1024 * 400
-    x = W.normal_inputs(n, count, 1e-3, 77)
-    e = np.zeros_like(x)
-    ar.ar_set_barrier_timeout_ns(50_000_000)  # 50 ms
-    try:
-        xd = [to_dev(x[r]) for r in range(n)]
-        ed = [to_dev(e[r]) for r in range(n)]
-        ar.ar_debug_skip_barrier(skip)
-        ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op="avg"), "launch")
-        rc, st = ar.ar_device_status()
-        assert rc == 0 and st == ar.AR_ERR_TIMEOUT
-        rc, st = ar.ar_device_status()
-        assert rc == 0 and st == 0
-        want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op="avg")
-        xd = [to_dev(x[r]) for r in range(n)]
-        ed = [to_dev(e[r]) for r in range(n)]
-        ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op="avg"), "after the timeout")
-        assert_same(from_dev(xd, "f32"), want_x, "f32", "x after timeout")
-        assert_same(from_dev(ed, "f32"), want_e, "f32", "e after timeout")
-        rc, st = ar.ar_device_status()
-        assert rc == 0 and st == 0
-    finally:
-        ar.ar_debug_skip_barrier(-1)
-        ar.ar_set_barrier_timeout_ns(0)
-
-
 def test_int8_ef_unaligned_and_rejects(ar):
     n, count = 4, 1000
     x = W.normal_inputs(n, count, 1.0, 31)
