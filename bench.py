@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--overlap", action="store_true",
                    help="gpt2 workload: also time a synthetic backward with and without overlapped bucket reduction")
     p.add_argument("--overlap-tokens", type=int, default=256)
+    p.add_argument("--overlap-eager", action="store_true",
+                   help="time the overlap variants with direct launches instead of CUDA-graph replays")
     return p.parse_args()
 
 
@@ -637,7 +639,7 @@ class Gpt2Workload:
                 raise self.ar.ArError(rc, "ar_bucketed_allreduce")
         return flats, step
 
-    def overlap(self, sid, tokens, iters=5):
+    def overlap(self, sid, tokens, iters=5, eager=False):
         """Synthetic backward: for every tensor in reverse registration order and
         every rank, a GEMM of the shape of its weight gradient (dW = X^T dY over
         `tokens` tokens; a column sum for vectors) writes the gradient on the
@@ -655,9 +657,14 @@ class Gpt2Workload:
         X = [torch.randn(tokens, amax, device=dev, generator=gen) * 1e-2 for _ in range(self.n)]
         Y = [torch.randn(tokens, bmax, device=dev, generator=gen) * 1e-2 for _ in range(self.n)]
         compute = torch.cuda.current_stream()
-        comm = torch.cuda.Stream()
-        red = self.ar.Reducer(self.grads, counts=self.counts, dtype=self.dtype, op=self.op, algo="ring",
-                              comm_stream=comm)
+        # the reducer's stream at normal priority and at the highest (as a
+        # collective library's would be), so its blocks go first as GEMM blocks retire
+        reducers = {}
+        for prio in (0, -1):
+            comm = torch.cuda.Stream(priority=prio)
+            reducers[prio] = (comm, self.ar.Reducer(self.grads, counts=self.counts, dtype=self.dtype, op=self.op,
+                                                    algo="ring", comm_stream=comm))
+        red = reducers[0][1]
 
         def backward(mark=None):
             for t in range(len(shapes) - 1, -1, -1):
@@ -675,16 +682,28 @@ class Gpt2Workload:
             backward()
             self.step(int(torch.cuda.current_stream().cuda_stream), "ring")
 
-        def ovl():
-            s = torch.cuda.current_stream()
-            backward(lambda t: self.ar.check(red.mark_ready(t, s), "mark_ready"))
-            self.ar.check(red.finish(s), "finish")
+        def ovl_with(rd):
+            def ovl():
+                s = torch.cuda.current_stream()
+                backward(lambda t: self.ar.check(rd.mark_ready(t, s), "mark_ready"))
+                self.ar.check(rd.finish(s), "finish")
+            return ovl
 
         # each variant is captured once into a CUDA graph and replayed, so the
-        # numbers are GPU time, not the host's launch rate (1184 GEMM launches)
+        # numbers are GPU time, not the host's launch rate (1184 GEMM launches);
+        # eager=True launches them directly (graphs drop stream priorities), for
+        # token counts whose GEMMs outlast their launches
         def timed(fn):
             fn()
             torch.cuda.synchronize()
+            if eager:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(compute)
+                for _ in range(iters):
+                    fn()
+                e1.record(compute)
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / iters
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
@@ -705,22 +724,25 @@ class Gpt2Workload:
             t_bwd, t_seq = timed(backward), timed(seq)
             # block caps for the overlapped reductions: none (one block per
             # tile), then a few "channels" of the GPU's 152 SMs
-            for cap in (0, 304, 152, 76, 38):
-                self.ar.check(red.set_max_blocks(cap), "set_max_blocks")
-                by_blocks[cap] = timed(ovl)
+            for prio, (_, rd) in reducers.items():
+                for cap in (0, 304, 152, 76, 38):
+                    self.ar.check(rd.set_max_blocks(cap), "set_max_blocks")
+                    by_blocks[f"prio{prio}_blocks{cap}"] = timed(ovl_with(rd))
         finally:
             torch.backends.cuda.matmul.allow_tf32 = tf32
         nbuckets = red.buckets
-        red.close()
+        for _, rd in reducers.values():
+            rd.close()
         best = min(by_blocks, key=by_blocks.get)
         t_ovl = by_blocks[best]
         t_ar = t_seq - t_bwd
         return {"tokens": tokens, "backward_ms": t_bwd, "sequential_ms": t_seq, "overlapped_ms": t_ovl,
-                "overlapped_ms_by_max_blocks": {str(k): v for k, v in by_blocks.items()}, "best_max_blocks": best,
+                "overlapped_ms_by_stream_priority_and_max_blocks": by_blocks, "best": best,
                 "allreduce_ms_in_sequence": t_ar, "exposed_comm_ms": t_ovl - t_bwd,
                 "hidden_fraction": (t_seq - t_ovl) / t_ar if t_ar > 0 else None, "buckets": nbuckets,
-                "note": "backward = per-rank TF32 GEMMs (dW = X^T dY) on the compute stream, every variant "
-                        "replayed from a CUDA graph; both streams share one GPU"}
+                "launch": "eager" if eager else "cuda graph",
+                "note": "backward = per-rank TF32 GEMMs (dW = X^T dY) on the compute stream; both streams share "
+                        "one GPU"}
 
     def cpu_baseline(self):
         import oracle
@@ -924,7 +946,7 @@ def main():
     overlap = None
     if args.overlap and isinstance(wl, Gpt2Workload):
         try:
-            overlap = wl.overlap(sid, args.overlap_tokens)
+            overlap = wl.overlap(sid, args.overlap_tokens, eager=args.overlap_eager)
         except Exception as exc:  # reported in the line; the headline numbers above stand
             overlap = {"error": f"{type(exc).__name__}: {exc}"}
 
