@@ -31,7 +31,12 @@ constexpr int kFusedBlock = 256;
 // U=3 at 2 blocks/SM 311.3 us, U=4 at 1 block/SM 343.5 us -- occupancy
 // matters more than loads per thread once the grid is one tile per block.
 // (The wide trees, N >= 16, get 128 registers: 2 blocks per SM.)
-__host__ __device__ constexpr int fused_min_blocks(int nr) { return nr > 8 ? 2 : 4; }
+// Resident blocks per SM the register budget is cut for: 4 (64 registers) for
+// up to 8 ranks, 2 beyond; the in-order double-binary-tree fold of 8 ranks
+// keeps more partial sums live and gets 3 (80 registers), without spills.
+__host__ __device__ constexpr int fused_min_blocks(int order, int nr) {
+  return nr > 8 ? 2 : (order == DBTREE && nr == 8 ? 3 : 4);
+}
 __host__ __device__ constexpr int fused_unroll(int order, int nr) {
   return (nr == 2) ? 2 : 1;
 }
@@ -64,7 +69,7 @@ __device__ __forceinline__ uint4 inorder_fold_regs(const uint4 (&x)[NR]) {
 }
 
 template <int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int U = fused_unroll(ORDER, NR);
@@ -126,18 +131,20 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(NR)) fused_vec_k
         }
       }
     } else if constexpr (ORDER == DBTREE) {
-      // chunk 0: tree A over the first half of the elements, chunk 1: tree B
+      // chunk 0: tree A over the first half of the elements, chunk 1: tree B.
+      // Tree B is tree A over the ranks shifted by one, so the shift goes
+      // into which buffer lands in x[p], and one tree is compiled.
+      const int shift = c == 0 ? 0 : 1;
       uint4 x[U][NR];
 #pragma unroll
       for (int p = 0; p < NR; ++p) {
-        const char* src = static_cast<const char*>(P[p]) + base;
+        const char* src = static_cast<const char*>(P[rot(p + shift, NR)]) + base;
 #pragma unroll
         for (int u = 0; u < U; ++u)
           if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        acc[u] = c == 0 ? inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]) : inorder_fold_regs<DT, OP, NR, 1, 1, NR>(x[u]);
+      for (int u = 0; u < U; ++u) acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
     } else if constexpr (NR <= 8) {
       uint4 x[U][NR];
 #pragma unroll
