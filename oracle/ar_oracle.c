@@ -39,6 +39,14 @@
  *  - DDP bucketing: buckets of at most bucket_cap (25 MB by default) filled
  *    with parameters in reverse order.  Tutorial §4.1; "AllReduce 集合通信"
  *    §DDP 梯度同步中的地位.
+ *  - Double binary tree (two complementary trees, half the data each) and
+ *    the 8-bit quantised AllReduce with error feedback: see their functions.
+ *
+ * PARITY UNPINNED by the pages, for three choices: the ring's chunk rotation
+ * (every example the pages print is integer-valued, hence order-free), the
+ * double binary tree's shape, and the 8-bit scheme.  Each is pinned here
+ * only by the reading stated at its function and by closed forms and worked
+ * cases of that reading, never by a value the pages print.
  *
  * Elementwise step (the pages fix only "sum" / "max"; the arithmetic is IEEE):
  *  - f32 SUM: IEEE binary32 addition, round to nearest even (C float `+`,

@@ -650,3 +650,64 @@ def test_largest_sweep_point_sampled(ar, dtype, op, algo):
         assert torch.equal(bufs[r], bufs[0]), r
     del bufs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("algo", ["ring", "tree", "dbtree"])
+def test_more_than_2g_elements_sampled(ar, algo):
+    """2 ranks x (2^31 + 12,345) bf16 (4.3 GB each): element indices and byte
+    offsets past 32 bits, on sampled positions, chunk boundaries and the
+    double binary tree's half boundary."""
+    n, count = 2, (1 << 31) + 12_345
+    free, _ = torch.cuda.mem_get_info()
+    if free < 3 * n * count * 2:
+        pytest.skip("needs about 26 GB of free device memory")
+    pos = sample_positions(count, n, 1 << 14, 13)
+    pos = np.unique(np.concatenate([pos, count // 2 + np.arange(-2, 3), [(1 << 31) - 1, 1 << 31, count - 1]]))
+    pos = pos[(pos >= 0) & (pos < count)]
+    idx = torch.from_numpy(pos).cuda()
+    bufs = [W.uniform_rank_device(r, count, "bf16", torch, config=21) for r in range(n)]
+    xs = np.stack([b[idx].cpu().numpy() for b in bufs]).view(np.uint16)
+    want, _ = oracle.allreduce(xs, algo=algo, op="sum", dtype="bf16", count=count, positions=pos)
+    ar.check(ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo=algo), "2G elements")
+    torch.cuda.synchronize()
+    for r in range(n):
+        assert_same(bufs[r][idx].cpu().numpy().view(np.uint16), want[r], "bf16", f"rank {r}")
+    assert torch.equal(bufs[0], bufs[1])
+    del bufs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_int8_ef_more_than_2g_elements_sampled(ar):
+    """8-bit path on 2 ranks x (2^31 + 300) f32: quantisation blocks and
+    chunks past 32-bit indices.  A block that lies in one chunk depends only
+    on its own elements and that chunk, so the oracle checks it on a small
+    buffer that puts the same block, in the same chunk, at a block boundary
+    (the other block of that buffer is zero filler)."""
+    n, count = 2, (1 << 31) + 300
+    free, _ = torch.cuda.mem_get_info()
+    if free < 2 * n * count * 4 + (8 << 30):
+        pytest.skip("needs about 44 GB of free device memory")
+    x = [W.uniform_rank_device(r, count, "f32", torch, config=22) for r in range(n)]
+    e = [torch.zeros(count, dtype=torch.float32, device="cuda") for _ in range(n)]
+    starts = [0, 128 * 1000, (1 << 31) - 128, 1 << 31, (count - 1) // 128 * 128]
+    blocks = [np.arange(b, min(b + 128, count), dtype=np.int64) for b in starts]
+    before = [np.stack([t[torch.from_numpy(b).cuda()].cpu().numpy() for t in x]) for b in blocks]
+    ar.check(ar.ar_allreduce_int8_ef(x, e, count=count, op="avg"), "int8 2G")
+    torch.cuda.synchronize()
+    for b, x0 in zip(blocks, before):
+        chunks = {((int(el) + 1) * n - 1) // count for el in b}
+        assert len(chunks) == 1
+        c, m = chunks.pop(), len(b)
+        off = 0 if c == 0 else 128  # chunk 0 = [0, 128) of 256; chunk 1 starts at or before 128 of 128 + m
+        small = np.zeros((n, 256 if c == 0 else 128 + m), np.float32)
+        small[:, off:off + m] = x0
+        wx, we, _ = oracle.int8_ef_allreduce(small, np.zeros_like(small), op="avg")
+        idx = torch.from_numpy(b).cuda()
+        got_x = np.stack([t[idx].cpu().numpy() for t in x])
+        got_e = np.stack([t[idx].cpu().numpy() for t in e])
+        assert_same(got_x, wx[:, off:off + m], "f32", f"x block at {b[0]}")
+        assert_same(got_e, we[:, off:off + m], "f32", f"e block at {b[0]}")
+    del x, e
+    torch.cuda.empty_cache()
