@@ -147,6 +147,7 @@ struct Job {
   bool vec;
   int root = -1;  // Reduce: the rank that receives the result
   int max_grid = 0;  // fused kernels: cap on the number of blocks (0 = one per tile)
+  int64_t row_count = 0;  // plain collectives: elements per rank of their single buffer row (0: several rows)
 };
 
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
@@ -155,7 +156,26 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   const int order = j.algo == AR_DBTREE ? ar::DBTREE
                     : (j.algo == AR_TREE || j.algo == AR_TREE_STEPWISE) ? ar::TREE : ar::RING;
   cudaError_t e;
-  if (stepwise) {
+  // element updates in the busiest phase: the chunk's count for the ring,
+  // N/2 pairs of it in the first tree step
+  const int64_t phase_elems = j.row_count * (order == ar::TREE ? tab.nranks / 2 : 1);
+  if (stepwise && j.row_count > 0 && phase_elems <= ar::kSmemStepMaxPhaseElems &&
+      ar::smem_step_bytes(tab.nranks, j.row_count, esize_of(j.dtype)) <= ar::kSmemStepBytes) {
+    // a small row: the whole schedule in one block's shared memory (no grid
+    // barrier, so the barrier test hook is consumed without effect)
+    g_skip_barrier.exchange(-1);
+    ar::SmemStepArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int r = 0; r < tab.nranks; ++r) a.ptr[r] = tab.ptr[r];
+    a.count = j.row_count;
+    a.nranks = tab.nranks;
+    a.order = order;
+    a.phases = j.phases;
+    a.avg = j.avg ? 1 : 0;
+    a.vec = j.vec ? 1 : 0;
+    a.fn = (float)tab.nranks;
+    e = ar::launch_stepwise_smem(j.dtype, dop, a, s);
+  } else if (stepwise) {
     ar::SyncBlock* sb = nullptr;
     int rc = sync_block(&sb);
     if (rc) return rc;
@@ -276,6 +296,7 @@ int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, in
   }
   j = Job{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};  // naive = ring kernel
   j.root = root;
+  j.row_count = count;
   return AR_OK;
 }
 

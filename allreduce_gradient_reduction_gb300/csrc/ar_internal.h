@@ -63,6 +63,27 @@ struct StepArgs {
   float fn;
 };
 
+// The step-wise schedule of one buffer row small enough to live in one
+// block's shared memory (each rank's count elements, padded to 16 bytes).
+struct SmemStepArgs {
+  const void* ptr[kMaxRanks];
+  int64_t count;
+  int32_t nranks;
+  int32_t order;   // RING or TREE
+  int32_t phases;  // bit 0 ReduceScatter, bit 1 AllGather
+  int32_t avg;
+  int32_t vec;     // every pointer 16-byte aligned
+  float fn;
+};
+constexpr int64_t kSmemStepBytes = 160 * 1024;  // shared memory the small step-wise kernel may use
+// One block does a phase's element updates at about 0.45 ns each, a grid
+// barrier plus phase of the multi-block kernel costs about 2.2 us: the block
+// path is taken while a phase has at most this many element updates.
+constexpr int64_t kSmemStepMaxPhaseElems = 3072;
+inline int64_t smem_step_bytes(int nranks, int64_t count, int esize) {
+  return (int64_t)nranks * ((count * esize + 15) / 16 * 16);
+}
+
 struct CopyArgs {
   SegTable tab;                  // ptr[tensor * nranks + r] = tensor side
   const void* packed[kMaxRanks]; // packed side base per rank; seg.aux = element offset there
@@ -87,6 +108,7 @@ cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& args
 cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t stream);
 cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
+cudaError_t launch_stepwise_smem(int dtype, int op, SmemStepArgs& args, cudaStream_t stream);
 cudaError_t launch_int8_ef(Int8Args& args, cudaStream_t stream);
 
 int sm_count();

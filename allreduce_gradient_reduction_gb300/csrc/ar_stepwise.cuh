@@ -183,4 +183,113 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
   }
 }
 
+// The same schedule for a small buffer row, in one block: every rank's
+// buffer is staged in shared memory (elements at their own size, each rank's
+// region padded to 16 bytes), the phases run there with a block barrier
+// between them, and the final state is written back.  Same per-element
+// operations in the same order as stepwise_kernel, so the same bits; a phase
+// costs a block barrier instead of a grid barrier and an L2 round trip.
+// Sizes here are small enough for 32-bit index arithmetic.
+constexpr int kSmemStepBlock = 1024;
+constexpr int kSmemStepUnroll = 4;  // 16-byte copies in flight per thread while staging
+
+template <int ES>
+struct SmemWord;
+template <>
+struct SmemWord<2> {
+  using type = unsigned short;
+};
+template <>
+struct SmemWord<4> {
+  using type = unsigned int;
+};
+
+// Moves every rank's buffer between global memory and its shared-memory
+// region (to_smem: global -> shared).  16-byte pieces when the buffers are
+// 16-byte aligned, then the last count * ES % 16 bytes element by element.
+template <int ES, bool TO_SMEM>
+__device__ __forceinline__ void smem_stage(const SmemStepArgs& a, unsigned char* S, int stride, int n, int count) {
+  using Wd = typename SmemWord<ES>::type;
+  const int nvec = a.vec ? count * ES / 16 : 0;
+  const int total = n * nvec;
+  for (int i0 = threadIdx.x; i0 < total; i0 += kSmemStepUnroll * kSmemStepBlock) {
+    uint4 v[kSmemStepUnroll];
+#pragma unroll
+    for (int u = 0; u < kSmemStepUnroll; ++u) {
+      const int i = i0 + u * kSmemStepBlock;
+      if (i < total) {
+        const int r = i / nvec, k = i - r * nvec;
+        uint4* sp = reinterpret_cast<uint4*>(S + r * stride) + k;
+        if constexpr (TO_SMEM) v[u] = ld_l2(static_cast<const uint4*>(a.ptr[r]) + k);
+        else v[u] = *sp;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kSmemStepUnroll; ++u) {
+      const int i = i0 + u * kSmemStepBlock;
+      if (i < total) {
+        const int r = i / nvec, k = i - r * nvec;
+        uint4* sp = reinterpret_cast<uint4*>(S + r * stride) + k;
+        if constexpr (TO_SMEM) *sp = v[u];
+        else st_l2(static_cast<uint4*>(const_cast<void*>(a.ptr[r])) + k, v[u]);
+      }
+    }
+  }
+  const int done = nvec * 16 / ES, rest = count - done;  // elements left per rank
+  for (int i = threadIdx.x; i < n * rest; i += kSmemStepBlock) {
+    const int r = i / rest, e = done + (i - r * rest);
+    Wd* sp = reinterpret_cast<Wd*>(S + r * stride) + e;
+    if constexpr (TO_SMEM) *sp = (Wd)ld_elem<ES>(a.ptr[r], e);
+    else st_elem<ES>(const_cast<void*>(a.ptr[r]), e, *sp);
+  }
+}
+
+template <int DT, int OP>
+__global__ void __launch_bounds__(kSmemStepBlock) stepwise_smem_kernel(const __grid_constant__ SmemStepArgs a) {
+  constexpr int ES = ElemSize<DT>::value;
+  using Wd = typename SmemWord<ES>::type;
+  extern __shared__ __align__(16) unsigned char S[];  // rank r's elements at S + r * stride
+  const int n = a.nranks;
+  const int count = (int)a.count;
+  const int stride = (count * ES + 15) / 16 * 16;
+  smem_stage<ES, true>(a, S, stride, n, count);
+  __syncthreads();
+  const bool ring = a.order == RING;
+  const int L = ring ? 0 : ilog2(n);
+  const int n_rs = (a.phases & 1) ? (ring ? n - 1 : L) : 0;
+  const int n_ag = (a.phases & 2) ? (ring ? n - 1 : L) : 0;
+  for (int q = 0; q < n_rs + n_ag; ++q) {
+    const bool rs = q < n_rs;
+    const int s = rs ? q : q - n_rs;
+    const int k = rs ? s : L - 1 - s;
+    const int h = 1 << k;
+    const int inst = ring ? 1 : (n >> (k + 1));
+    const bool avg = a.avg && rs && s == n_rs - 1;
+    for (int w = threadIdx.x; w < inst * count; w += kSmemStepBlock) {
+      const int m = w / count;
+      const int e = w - m * count;
+      const int j = ((e + 1) * n - 1) / count;  // chunk [floor(jD/N), floor((j+1)D/N)) holding e
+      int src, dst;
+      if (ring) {
+        src = rs ? (j + 1 + s) % n : (j + s) % n;
+        dst = src + 1 == n ? 0 : src + 1;
+      } else {
+        dst = rs ? ((j & (2 * h - 1)) + m * 2 * h) : (((j ^ h) & (2 * h - 1)) + m * 2 * h);
+        src = dst ^ h;
+      }
+      Wd* ps = reinterpret_cast<Wd*>(S + src * stride) + e;
+      Wd* pd = reinterpret_cast<Wd*>(S + dst * stride) + e;
+      uint32_t r = *ps;
+      if (rs) {
+        const uint32_t d = *pd;
+        r = (ring || src < dst) ? step_word<DT, OP>(r, d) : step_word<DT, OP>(d, r);
+        if (avg) r = div_word<DT>(r, a.fn);
+      }
+      *pd = (Wd)r;
+    }
+    __syncthreads();
+  }
+  smem_stage<ES, false>(a, S, stride, n, count);
+}
+
 }  // namespace ar

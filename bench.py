@@ -886,6 +886,18 @@ def main():
     if rc or status:
         raise ar.ArError(rc or status, "device status")
 
+    # the spread of single steps (outside the timed region): each one bracketed
+    # by its own events, so launch gaps count against it
+    singles = []
+    for _ in range(20):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        singles.append((a, b))
+    torch.cuda.synchronize()
+    single_ms = sorted(a.elapsed_time(b) for a, b in singles)
+
     value = ws * nbytes_step / (ms / 1e3) / 1e9
     algbw = nbytes_step / (2 * wl.n) / (ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -962,6 +974,8 @@ def main():
             "config": {"workload": wl.workload, **wl.config,
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "algbw_gbs": algbw * ws,
+            "single_step_ms": {"median": statistics.median(single_ms), "best": single_ms[0],
+                               "worst": single_ms[-1], "samples": len(single_ms)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": profiled_traffic() if isinstance(wl, LargeWorkload) and not args.count else None,

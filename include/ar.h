@@ -63,7 +63,11 @@
  *     The fused algorithms make one pass over HBM (each element of each rank
  *     read once and written once); the step-wise ones execute the literal
  *     schedule, one grid-wide phase per communication step, in a single
- *     persistent cooperative kernel.
+ *     persistent cooperative kernel.  A small plain (one-buffer-per-rank)
+ *     step-wise call -- at most 3072 element updates in a phase, N buffers
+ *     within 160 KiB -- runs the same schedule in one thread block, the
+ *     buffers staged in its shared memory and a block barrier between
+ *     phases: same results, no grid barrier.
  */
 #ifndef AR_GB300_H
 #define AR_GB300_H
