@@ -1,5 +1,5 @@
-"""Out-of-bounds writes, caught with guard bands (compute-sanitizer is not
-available on this pool).  Every rank buffer sits inside a larger allocation
+"""Out-of-bounds writes, caught with guard bands instead of a memory
+sanitizer.  Every rank buffer sits inside a larger allocation
 between guard bands filled with a byte pattern; after each call the bands
 must be untouched.  Sizes are odd, ragged and unaligned (element-aligned but
 not 16-byte aligned), so every tail and scalar path runs."""
