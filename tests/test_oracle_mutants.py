@@ -64,6 +64,18 @@ MUTANTS = [
      [("if (held[p][0]) combine(s->dtype, s->op, held[p][0], SLICE(p), SLICE(p), len);\n      if (held[p][1]) combine(s->dtype, s->op, SLICE(p), held[p][1], SLICE(p), len);",
        "if (held[p][1]) combine(s->dtype, s->op, SLICE(p), held[p][1], SLICE(p), len);\n      if (held[p][0]) combine(s->dtype, s->op, held[p][0], SLICE(p), SLICE(p), len);")],
      ["dbtree"]),
+    ("int8 codes round half away from zero",
+     [("q = nearbyintf(y / s); /* default rounding mode: to nearest, ties to even */", "q = roundf(y / s);")],
+     ["int8"]),
+    ("int8 compression error not fed back",
+     [("e[lo + i] = y[i] - (float)q[lo + i] * scale[b];", "e[lo + i] = 0.0f;")],
+     ["int8"]),
+    ("int8 scale over 128 steps",
+     [("  return m / 127.0f;\n}", "  return m / 128.0f;\n}")],
+     ["int8"]),
+    ("int8 owner folds in index order",
+     [("int rr = (c + 1 + p) % nranks;", "int rr = p;")],
+     ["int8"]),
     ("ring counts only received volume",
      [("s->st->sent[src] += total;", "(void)total;")],
      ["volume"]),
@@ -100,6 +112,14 @@ def run_pins(which):
         P.test_bucket_plan_gpt2(o)
     if "volume" in which:
         P.test_ring_volume_and_steps(o, 4)
+    if "int8" in which:
+        P.test_int8_exact_when_values_sit_on_the_grid(o)
+        P.test_int8_codes_round_half_to_even(o)
+        P.test_int8_feedback_is_unbiased(o)
+        for n, d in ((2, 128 * 3 + 5), (3, 1000), (5, 128 * 5 + 77)):
+            P.test_int8_messages_realise_the_definition(o, n, d)
+        for n in (2, 3):
+            P.test_int8_error_bounds(o, n)
     if "dbtree" in which:
         for dt in ("f32", "bf16"):
             for n in (4, 5, 8):
@@ -121,7 +141,7 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
     real = oracle.lib()
     mutant = ctypes.CDLL(str(so))
     for fname in ("oracle_collective", "oracle_step", "oracle_f32_to_bf16", "oracle_chunk_range",
-                  "oracle_bucket_plan", "oracle_bucketed_allreduce"):
+                  "oracle_bucket_plan", "oracle_bucketed_allreduce", "oracle_int8_ef_allreduce"):
         getattr(mutant, fname).argtypes = getattr(real, fname).argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)
     with pytest.raises((AssertionError, oracle.OracleError)):
@@ -130,4 +150,4 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
 
 def test_real_oracle_passes_the_same_pins():
     run_pins({"ring_order", "tree_order", "bruteforce", "printed", "bf16_round", "avg", "max", "f32_add",
-              "bucket", "volume", "dbtree"})
+              "bucket", "volume", "dbtree", "int8"})

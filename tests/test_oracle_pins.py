@@ -880,6 +880,92 @@ def test_int8_feedback_telescopes(oracle_lib):
     assert np.allclose(total, k * x[0].astype(np.float64) - e[0], rtol=0, atol=1e-4)
 
 
+def test_int8_codes_round_half_to_even(oracle_lib):
+    # one rank, one block whose maximum is 127: the scale is exactly 1, so the
+    # codes are the values rounded to integers, ties to even, and the
+    # residual is what rounding dropped
+    y = np.zeros(128, dtype=np.float32)
+    ties = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -126.5, 0.25, 0.75, -0.75], dtype=np.float32)
+    y[:ties.size] = ties
+    y[-1] = 127.0
+    _, e_new, _ = oracle.int8_ef_allreduce(y[None, :], np.zeros((1, 128), np.float32), op="sum")
+    codes = y - e_new[0]
+    want = np.array([0, 2, 2, 4, 0, -2, -2, 126, -126, 0, 1, -1], dtype=np.float32)
+    assert np.array_equal(codes[:ties.size], want)
+    assert codes[-1] == 127.0
+
+
+def test_int8_feedback_is_unbiased(oracle_lib):
+    # one rank, the same gradient every round: with the compression error fed
+    # back, the results of K rounds average to the gradient within one code
+    # step over K; without feedback every round would return the same rounded
+    # value, off by up to half a step
+    d, k = 256, 64
+    x = W.normal_inputs(1, d, 1.0, 19)
+    e = np.zeros_like(x)
+    outs = []
+    for _ in range(k):
+        out, e, _ = oracle.int8_ef_allreduce(x, e, op="sum")
+        outs.append(out[0].astype(np.float64))
+    mean = np.mean(outs, axis=0)
+    step = np.repeat([np.abs(x[0, lo:lo + 128]).max() / 127 for lo in range(0, d, 128)], 128)
+    assert np.all(np.abs(mean - x[0]) <= 1.5 * step / k)
+    # and the plain rounding error it removes is far larger somewhere
+    assert np.abs(outs[0] - x[0]).max() > 10 * (1.5 * step / k).max()
+
+
+def int8_by_definition(x, e, op):
+    """The 8-bit scheme written out per chunk in numpy binary32 (each step one
+    IEEE operation): codes per 128-block, the owner's fold in ring order,
+    requantisation per block cut at the chunk's ends."""
+    n, d = x.shape
+    f = np.float32
+    y = (x.astype(f) + e.astype(f)).astype(f)
+    yh = np.zeros_like(y)
+    for lo in range(0, d, 128):
+        blk = y[:, lo:lo + 128]
+        s = (np.abs(blk).max(axis=1) / f(127)).astype(f)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.where(s[:, None] > 0, np.clip(np.rint(blk / s[:, None]), -127, 127), f(0))
+        q = q.astype(np.int8).astype(f)  # an 8-bit integer code: a zero code is +0
+        yh[:, lo:lo + 128] = (q * s[:, None]).astype(f)
+    e_new = (y - yh).astype(f)
+    out = np.zeros_like(y)
+    for c in range(n):
+        lo, hi = c * d // n, (c + 1) * d // n
+        if hi == lo:
+            continue
+        a = yh[(c + 1) % n, lo:hi].copy()
+        for p in range(1, n):
+            a = (a + yh[(c + 1 + p) % n, lo:hi]).astype(f)
+        if op == "avg":
+            a = (a / f(n)).astype(f)
+        res = np.zeros_like(a)
+        b = lo // 128 * 128
+        while b < hi:
+            plo, phi = max(b, lo), min(b + 128, hi)
+            piece = a[plo - lo:phi - lo]
+            s = f(np.abs(piece).max() / f(127))
+            q = np.clip(np.rint(piece / s), -127, 127).astype(np.int8).astype(f) if s > 0 else np.zeros_like(piece)
+            res[plo - lo:phi - lo] = (q * s).astype(f)
+            b += 128
+        out[:, lo:hi] = res
+    return out, e_new
+
+
+@pytest.mark.parametrize("n,d", [(1, 300), (2, 128 * 3 + 5), (3, 1000), (5, 128 * 5 + 77), (8, 128 * 24 + 3)])
+def test_int8_messages_realise_the_definition(oracle_lib, n, d):
+    # the literal simulation (codes and scales routed to chunk owners, then
+    # requantised chunks broadcast) equals the scheme written out per chunk
+    x = W.normal_inputs(n, d, 1e-2, 40 + n)
+    e = W.normal_inputs(n, d, 1e-4, 50 + n)
+    for op in ("sum", "avg"):
+        got_x, got_e, _ = oracle.int8_ef_allreduce(x, e, op=op)
+        want_x, want_e = int8_by_definition(x, e, op)
+        assert np.array_equal(got_x.view(np.uint32), want_x.view(np.uint32)), (n, d, op)
+        assert np.array_equal(got_e.view(np.uint32), want_e.view(np.uint32)), (n, d, op)
+
+
 @pytest.mark.parametrize("n", [2, 4, 8])
 def test_int8_payload_volume(oracle_lib, n):
     d = 128 * n * 3
