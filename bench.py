@@ -763,6 +763,52 @@ class Gpt2Workload:
 # end to end: host inputs in, host results out
 # ---------------------------------------------------------------------------
 
+# The pages' own figures, other hardware: quoted as context, never as a target.
+PAGES_CONTEXT = {
+    "nvlink_h100_gbs_bidirectional": 900, "nvlink_a100_gbs_per_gpu": 600, "infiniband_hdr_gbs": 25,
+    "ddp_bucket_mb": 25, "note": "figures printed on the pages for other hardware; context only",
+}
+
+
+def accuracy(wl, step, torch, np, dev):
+    """Fresh inputs, one step, then sampled positions against the order-free
+    float64 reduction: the largest |error| / sum|x|, the tolerance stated for
+    the dtype (1e-5 f32, 2^-7 bf16) and the fraction of positions above it,
+    and the recursive-summation bound gamma_{N-1} of the ring's N-1 rounded
+    additions."""
+    for src, dst in wl.h2d:
+        dst.copy_(src)
+    torch.cuda.synchronize()
+    step()
+    torch.cuda.synchronize()
+    count = wl.h2d[0][0].numel()
+    pos = np.unique(np.random.default_rng(12345).integers(0, count, 1 << 16))
+    idx = torch.from_numpy(pos).to(dev)
+    x = np.stack([src.numpy()[pos] for src, _ in wl.h2d])
+    got = np.stack([dst[idx].cpu().numpy() for _, dst in wl.h2d])
+    if wl.dtype == "bf16":
+        def f64(a):
+            return (a.view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        u, tol = 2.0 ** -8, 2.0 ** -7
+    else:
+        def f64(a):
+            return a.astype(np.float64)
+        u, tol = 2.0 ** -24, 1e-5
+    xs = f64(x)
+    scale = 1.0 / wl.n if wl.op == "avg" else 1.0
+    ref, absum = xs.sum(axis=0) * scale, np.abs(xs).sum(axis=0) * scale
+    err = np.abs(f64(got) - ref).max(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(absum > 0, err / absum, 0.0)
+    k = wl.n - 1
+    gamma = k * u / (1 - k * u)
+    return {"vs": "float64 order-free reduction", "positions": int(pos.size),
+            "max_err_over_abs_sum": float(ratio.max()), "tolerance": tol,
+            "frac_above_tolerance": float((ratio > tol).mean()), "gamma_bound": gamma,
+            "within_gamma_bound": bool((ratio <= gamma * (1 + 1e-9)).all()),
+            "ranks_identical": bool(all(np.array_equal(got[r], got[0]) for r in range(wl.n)))}
+
+
 def end_to_end(wl, args, ws, stream, torch):
     """The same metric through the public call with the step's inputs copied
     from pinned host memory and its results copied back inside the timed
@@ -962,6 +1008,8 @@ def main():
         except Exception as exc:  # reported in the line; the headline numbers above stand
             overlap = {"error": f"{type(exc).__name__}: {exc}"}
 
+    acc = accuracy(wl, step, torch, np, dev) if rank == 0 else None
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = wl.cpu_baseline()
@@ -976,6 +1024,7 @@ def main():
             "algbw_gbs": algbw * ws,
             "single_step_ms": {"median": statistics.median(single_ms), "best": single_ms[0],
                                "worst": single_ms[-1], "samples": len(single_ms)},
+            "accuracy": acc, "context": PAGES_CONTEXT,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": profiled_traffic() if isinstance(wl, LargeWorkload) and not args.count else None,
