@@ -11,7 +11,7 @@ namespace ar {
 // One pass: read chunk c of its owner c once, write it to the N-1 others.
 
 // Two 16-byte positions per thread and 4 resident blocks per SM (64
-// registers): 1-4% faster than four positions without the register cap.
+// registers): 1-4% faster alone than four positions without the cap.
 constexpr int kGatherUnroll = 2;
 
 template <int ES, bool VECTOR>
