@@ -109,6 +109,16 @@ int check_bufs(void* const* bufs, int nranks, int64_t count, int dtype) {
   return check_ranges(rs, esize_of(dtype));
 }
 
+// The fused, gather and step-wise kernels move a row in 16-byte vectors
+// when all its buffers have the same address modulo 16 (they cut the
+// vectors at that offset); true 16-byte alignment is needed only where
+// shared or packed staging assumes it.
+bool same_phase16(void* const* p, int n) {
+  for (int i = 1; i < n; ++i)
+    if (((uintptr_t)p[i] & 15) != ((uintptr_t)p[0] & 15)) return false;
+  return true;
+}
+
 bool all_aligned16(void* const* p, int n) {
   for (int i = 0; i < n; ++i)
     if ((uintptr_t)p[i] % 16) return false;
@@ -148,6 +158,7 @@ struct Job {
   int root = -1;  // Reduce: the rank that receives the result
   int max_grid = 0;  // fused kernels: cap on the number of blocks (0 = one per tile)
   int64_t row_count = 0;  // plain collectives: elements per rank of their single buffer row (0: several rows)
+  bool aligned = false;   // every buffer 16-byte aligned (the single-block step-wise form stages with it)
 };
 
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
@@ -172,7 +183,7 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
     a.order = order;
     a.phases = j.phases;
     a.avg = j.avg ? 1 : 0;
-    a.vec = j.vec ? 1 : 0;
+    a.vec = j.aligned ? 1 : 0;
     a.fn = (float)tab.nranks;
     e = ar::launch_stepwise_smem(j.dtype, dop, a, s);
   } else if (stepwise) {
@@ -294,9 +305,10 @@ int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, in
   } else {
     for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
   }
-  j = Job{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, all_aligned16(bufs, nranks)};  // naive = ring kernel
+  j = Job{dtype, op, algo == AR_NAIVE ? AR_RING : algo, phases, op == AR_AVG, same_phase16(bufs, nranks)};  // naive = ring kernel
   j.root = root;
   j.row_count = count;
+  j.aligned = all_aligned16(bufs, nranks);
   return AR_OK;
 }
 
@@ -314,7 +326,7 @@ int collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, 
 // Rows of the fused bucketed AllReduce for the tensors `keep(t)` selects: each
 // tensor is cut at its bucket's chunk boundaries, and each piece is folded in
 // the order its bucket position implies (as if the bucket had been packed).
-// Returns whether every row is 16-byte aligned.
+// Returns whether every row can move in 16-byte vectors (same_phase16).
 template <typename Keep>
 bool add_bucket_rows(TableBuilder& tb, void* const* grads, const int64_t* counts, int ntensors, int nranks,
                      const int32_t* bucket_of, const int64_t* offset, const int64_t* bcount, Keep keep) {
@@ -323,7 +335,7 @@ bool add_bucket_rows(TableBuilder& tb, void* const* grads, const int64_t* counts
   for (int t = 0; t < ntensors; ++t) {
     if (counts[t] == 0 || !keep(t)) continue;
     for (int r = 0; r < nranks; ++r) row[r] = grads[(size_t)r * ntensors + t];
-    vec = vec && all_aligned16(row.data(), nranks);
+    vec = vec && same_phase16(row.data(), nranks);
     const int rw = tb.add_row(row.data());
     const int64_t B = bcount[bucket_of[t]], o = offset[t];
     for (int c = 0; c < nranks; ++c) {
@@ -447,7 +459,7 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
   // one segment owned by the root: the AllGather copy kernel sends it to every other rank
   TableBuilder tb{nranks, {}, {}};
   tb.add_seg(tb.add_row(bufs), 0, count, root);
-  Job j{dtype, AR_SUM, AR_RING, 2, false, all_aligned16(bufs, nranks)};
+  Job j{dtype, AR_SUM, AR_RING, 2, false, same_phase16(bufs, nranks)};
   return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
 }
 

@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
     const char* src = static_cast<const char*>(P[c]);
     const int64_t ti = tile - s.tile_begin;
     if constexpr (VECTOR) {
-      const SegShape sh = seg_shape<VEC>(s);
+      const int shift = row_shift(P[0], ES);  // the row's buffers share it
+      const SegShape sh = seg_shape<VEC>(s, shift);
       uint4 x[kGatherUnroll];
       int64_t off[kGatherUnroll];
       bool ok[kGatherUnroll];
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
       for (int u = 0; u < kGatherUnroll; ++u) {
         const int64_t v = sh.vb + ti * TILE + u * kFusedBlock + threadIdx.x;
         ok[u] = v < sh.ve;
-        off[u] = v * 16;
+        off[u] = v * 16 - shift * ES;
         if (ok[u]) x[u] = ld_stream(src + off[u]);
       }
       for (int r = 0; r < n; ++r) {
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
           if (ok[u]) st_stream(dst + off[u], x[u]);
       }
       if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
-        const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
+        const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x, shift);
         const uint32_t v = ld_elem<ES>(src, e);
         for (int r = 0; r < n; ++r)
           if (r != c) st_elem<ES>(const_cast<void*>(P[r]), e, v);
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
 
 template <int ES, bool VECTOR>
 static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
-  if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll) == 0) return cudaSuccess;
+  if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll, VECTOR) == 0) return cudaSuccess;
   gather_kernel<ES, VECTOR><<<grid_for(t.ntiles), kFusedBlock, 0, stream>>>(t);
   count_launch();
   return cudaGetLastError();

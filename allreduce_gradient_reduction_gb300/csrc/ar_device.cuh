@@ -129,21 +129,30 @@ __device__ __forceinline__ int find_seg(const SegTable& t, int64_t tile) {
 
 // Full 16-byte vectors of a segment: [vb, ve) in units of VEC elements.
 // Elements outside them (at most VEC-1 on each side) are "scalars": with
-// ve > vb they are [begin, vb*VEC) and [ve*VEC, end); otherwise all of
-// [begin, end).
+// ve > vb they are [begin, vb*VEC - shift) and [ve*VEC - shift, end);
+// otherwise all of [begin, end).
 struct SegShape {
   int64_t vb, ve;
   int head, tail;  // scalar counts before / after the vectors
 };
 
+// Rows whose N buffers share the same address modulo 16 (not necessarily 0)
+// still move in 16-byte vectors: with `shift` = (address mod 16) / element
+// size, vector v of the row covers elements [v*VEC - shift, (v+1)*VEC -
+// shift), at byte offset v*16 - shift*ES from every buffer of the row, which
+// is 16-byte aligned in all of them.  shift = 0 for aligned rows.
+__host__ __device__ __forceinline__ int row_shift(const void* p0, int es) {
+  return (int)(((uintptr_t)p0 & 15) / (uintptr_t)es);
+}
+
 template <int VEC>
-__device__ __forceinline__ SegShape seg_shape(const Seg& s) {
+__device__ __forceinline__ SegShape seg_shape(const Seg& s, int shift = 0) {
   SegShape r;
-  r.vb = (s.begin + VEC - 1) / VEC;
-  r.ve = s.end / VEC;
+  r.vb = (s.begin + shift + VEC - 1) / VEC;
+  r.ve = (s.end + shift) / VEC;
   if (r.ve > r.vb) {
-    r.head = (int)(r.vb * VEC - s.begin);
-    r.tail = (int)(s.end - r.ve * VEC);
+    r.head = (int)(r.vb * VEC - shift - s.begin);
+    r.tail = (int)(s.end - (r.ve * VEC - shift));
   } else {
     r.ve = r.vb;
     r.head = (int)(s.end - s.begin);
@@ -154,8 +163,8 @@ __device__ __forceinline__ SegShape seg_shape(const Seg& s) {
 
 // Element index of scalar k (0 <= k < head + tail) of a segment.
 template <int VEC>
-__device__ __forceinline__ int64_t scalar_elem(const Seg& s, const SegShape& sh, int k) {
-  return k < sh.head ? s.begin + k : sh.ve * VEC + (k - sh.head);
+__device__ __forceinline__ int64_t scalar_elem(const Seg& s, const SegShape& sh, int k, int shift = 0) {
+  return k < sh.head ? s.begin + k : sh.ve * VEC - shift + (k - sh.head);
 }
 
 __device__ __forceinline__ int rot(int k, int n) { return k >= n ? k - n : k; }

@@ -79,14 +79,16 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
 
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
-    const SegShape sh = seg_shape<VEC>(s);
-    const int64_t ti = tile - s.tile_begin;
     const void* const* P = T.ptr + (size_t)s.tensor * n;
+    const int shift = row_shift(P[0], ES);  // the row's buffers share it
+    const SegShape sh = seg_shape<VEC>(s, shift);
+    const int64_t ti = tile - s.tile_begin;
     const int c = s.chunk;
 
-    // position u of this thread is byte offset base + u * kStride in every rank
+    // position u of this thread is byte offset base + u * kStride in every
+    // rank, 16-byte aligned in all of them
     const int64_t v0 = sh.vb + ti * TILE_V + threadIdx.x;
-    const int64_t base = v0 * 16;
+    const int64_t base = v0 * 16 - shift * ES;
     constexpr int64_t kStride = (int64_t)kFusedBlock * 16;
     bool ok[U];
 #pragma unroll
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
 
     // elements of the segment outside its full vectors
     if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
-      const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x);
+      const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x, shift);
       uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
       if (a.avg) r = div_word<DT>(r, a.fn);
       if (a.owner_only || a.to_root) {
@@ -242,15 +244,18 @@ __global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_
 // ---- host side ---------------------------------------------------------------
 
 // Tiles of `tile_elems` vectors (or elements) per segment; a segment with
-// leftover scalars but no full vector still gets one tile.
-inline int64_t fill_tiles(SegTable& t, int vec, int64_t tile_units) {
+// leftover scalars but no full vector still gets one tile.  `shifted`: the
+// kernel cuts vectors at the row's shift (row_shift of its first pointer),
+// as the fused, gather and step-wise kernels do; the copy kernels do not.
+inline int64_t fill_tiles(SegTable& t, int vec, int64_t tile_units, bool shifted = false) {
   int64_t acc = 0;
   for (int i = 0; i < t.nseg; ++i) {
     Seg& s = t.seg[i];
     s.tile_begin = acc;
     int64_t units, extra;
     if (vec > 1) {
-      int64_t vb = (s.begin + vec - 1) / vec, ve = s.end / vec;
+      const int sh = shifted ? row_shift(t.ptr[(size_t)s.tensor * t.nranks], 16 / vec) : 0;
+      int64_t vb = (s.begin + sh + vec - 1) / vec, ve = (s.end + sh) / vec;
       if (ve < vb) ve = vb;
       units = ve - vb;
       extra = (s.end - s.begin) - units * vec;
@@ -282,7 +287,7 @@ inline unsigned grid_for(int64_t ntiles, int64_t cap = 0) {
 template <int DT, int OP, int ORDER, int NR>
 cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
   constexpr int U = fused_unroll(ORDER, NR);
-  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U) == 0) return cudaSuccess;
+  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U, true) == 0) return cudaSuccess;
   fused_vec_kernel<DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();

@@ -9,7 +9,7 @@ namespace ar {
 template <int DT, int OP, bool VECTOR>
 static cudaError_t launch_step_typed(StepArgs& a, cudaStream_t stream) {
   constexpr int VEC = VECTOR ? 16 / ElemSize<DT>::value : 1;
-  if (fill_tiles(a.tab, VEC, (int64_t)kStepBlock * kStepUnroll) == 0) return cudaSuccess;
+  if (fill_tiles(a.tab, VEC, (int64_t)kStepBlock * kStepUnroll, VECTOR) == 0) return cudaSuccess;
   static const int bps = blocks_per_sm(stepwise_kernel<DT, OP, VECTOR>, kStepBlock);
   // persistent: every block must be resident at once (the launch checks it);
   // more blocks than the widest phase has tiles would only wait at barriers

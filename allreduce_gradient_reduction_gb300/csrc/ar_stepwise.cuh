@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
       const int64_t ti = tile - sg.tile_begin;
 
       if constexpr (VECTOR) {
-        const SegShape sh = seg_shape<VEC>(sg);
+        const int shift = row_shift(P[0], ES);  // the row's buffers share it
+        const SegShape sh = seg_shape<VEC>(sg, shift);
         uint4 xs[kStepUnroll], xd[kStepUnroll];
         int64_t off[kStepUnroll];
         bool ok[kStepUnroll];
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
         for (int u = 0; u < kStepUnroll; ++u) {
           const int64_t v = sh.vb + ti * TILE + u * kStepBlock + threadIdx.x;
           ok[u] = v < sh.ve;
-          off[u] = v * 16;
+          off[u] = v * 16 - shift * ES;
           if (ok[u]) {
             xs[u] = ld_l2(ps + off[u]);
             if (rs) xd[u] = ld_l2(pd + off[u]);
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
           st_l2(pd + off[u], r);
         }
         if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
-          const int64_t e = scalar_elem<VEC>(sg, sh, threadIdx.x);
+          const int64_t e = scalar_elem<VEC>(sg, sh, threadIdx.x, shift);
           uint32_t r = ld_elem<ES>(ps, e);
           if (rs) {
             const uint32_t d = ld_elem<ES>(pd, e);

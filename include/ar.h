@@ -26,8 +26,11 @@
  *   - Buffers are device pointers of the current CUDA device, one per rank,
  *     each holding `count` elements of `dtype`, pairwise distinct and
  *     non-overlapping (checked; AR_ERR_INVALID_ARG otherwise).  They must be
- *     aligned to the element size; 16-byte alignment of all of them enables
- *     the vectorised kernels, any other alignment takes a slower scalar path.
+ *     aligned to the element size.  When all of them sit at the same address
+ *     modulo 16 (16-byte aligned or not) the kernels move 16-byte vectors,
+ *     cut at that offset; buffers at different offsets modulo 16 take a
+ *     slower one-element-per-thread path.  (For a bucketed call this holds
+ *     per tensor: each tensor's N buffers.)
  *   - 1 <= nranks <= AR_MAX_RANKS; count >= 0; count == 0 and nranks == 1 do
  *     nothing (a single rank already holds the reduction; AVG divides by 1).
  *   - Chunks: each rank buffer is split into N contiguous chunks,

@@ -32,13 +32,14 @@ class Guarded:
 
     def __init__(self, n, count, dtype, shift, seed):
         es = ES[dtype]
-        self.lo, self.hi = GUARD + shift, GUARD + shift + count * es
-        self.raw = [torch.full((self.hi + GUARD,), PATTERN, dtype=torch.uint8, device="cuda") for _ in range(n)]
+        shifts = shift if isinstance(shift, (list, tuple)) else [shift] * n  # bytes, per rank
+        self.span = [(GUARD + sh, GUARD + sh + count * es) for sh in shifts]
+        self.raw = [torch.full((hi + GUARD,), PATTERN, dtype=torch.uint8, device="cuda") for _, hi in self.span]
         g = torch.Generator(device="cuda")
         g.manual_seed(seed)
         self.bufs = []
-        for r in self.raw:
-            v = r[self.lo:self.hi].view(TORCH[dtype])
+        for r, (lo, hi) in zip(self.raw, self.span):
+            v = r[lo:hi].view(TORCH[dtype])
             if dtype == "f32":
                 v.copy_(torch.randn(count, device="cuda", generator=g))
             else:
@@ -47,8 +48,8 @@ class Guarded:
 
     def check(self, what):
         torch.cuda.synchronize()
-        for i, r in enumerate(self.raw):
-            head, tail = r[:self.lo].cpu().numpy(), r[self.hi:].cpu().numpy()
+        for i, (r, (lo, hi)) in enumerate(zip(self.raw, self.span)):
+            head, tail = r[:lo].cpu().numpy(), r[hi:].cpu().numpy()
             assert (head == PATTERN).all(), f"{what}: rank {i} wrote before its buffer"
             assert (tail == PATTERN).all(), f"{what}: rank {i} wrote past its buffer"
 
@@ -62,8 +63,10 @@ def sizes(n):
 def test_collectives_stay_inside_their_buffers(ar, n, dtype):
     algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
     for count in [c for c in sizes(n) if c > 0]:
-        for shift in (0, ES[dtype]):
-            G = Guarded(n, count, dtype, shift, seed=count + shift)
+        # aligned; the same offset in every rank (vectors cut at it); offsets
+        # differing by rank (one element per thread)
+        for shift in (0, ES[dtype], [(r * ES[dtype]) % 16 for r in range(n)]):
+            G = Guarded(n, count, dtype, shift, seed=count + n)
             for algo in algos:
                 ar.check(ar.ar_allreduce(G.bufs, count=count, dtype=dtype, op="max", algo=algo), "allreduce")
                 G.check(f"allreduce {algo} n={n} count={count} shift={shift}")
@@ -83,7 +86,7 @@ def test_collectives_stay_inside_their_buffers(ar, n, dtype):
 @pytest.mark.parametrize("n", [2, 3, 8])
 def test_int8_ef_stays_inside_its_buffers(ar, n):
     for count in (1, 127, 129, 1000, 128 * 3 * n + 77):
-        for shift in (0, 4):
+        for shift in (0, 4, [(4 * r) % 16 for r in range(n)]):
             X = Guarded(n, count, "f32", shift, seed=5 + count)
             E = Guarded(n, count, "f32", shift, seed=6 + count)
             ar.check(ar.ar_allreduce_int8_ef(X.bufs, E.bufs, count=count, op="avg"), "int8_ef")

@@ -170,21 +170,54 @@ def test_all_gather_copies_bits(ar, algo, dtype):
 # Alignment, degenerate sizes, streams
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_unaligned_buffers_take_scalar_path(ar, algo, dtype):
-    n, count = 8, 5000
+@pytest.mark.parametrize("algo", ALGOS + ["dbtree", "naive"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_unaligned_buffers(ar, algo, dtype):
+    """Element-aligned but not 16-byte aligned buffers.  The same offset in
+    every rank takes the vector path cut at that offset; different offsets
+    per rank take the one-element-per-thread path.  Both must give the same
+    bits, and nothing before a buffer is touched."""
+    n, count = 8, 5000 + 2048 * 8 + 3
     x = inputs(n, count, dtype, "values", seed=9)
-    want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op="sum", dtype=dtype)
-    for shift in (1, 3):
-        big = [to_dev(np.concatenate([x[r][:shift], x[r]])) for r in range(n)]
-        views = [b[shift:] for b in big]  # element-aligned, not 16-byte aligned
+    want, _ = oracle.allreduce(x, algo=ORACLE_ALGO.get(algo, algo), op="sum", dtype=dtype)
+    vec = 8 if dtype == "bf16" else 4
+    layouts = [[s] * n for s in range(1, vec)] + [[r % vec for r in range(n)], [(3 * r + 1) % vec for r in range(n)]]
+    for shifts in layouts:
+        big = [to_dev(np.concatenate([x[r][:shifts[r]], x[r]])) for r in range(n)]
+        views = [b[s:] for b, s in zip(big, shifts)]
         ar.check(ar.ar_allreduce(views, count=count, dtype=dtype, op="sum", algo=algo), "unaligned")
         torch.cuda.synchronize()
         got = from_dev(views, dtype)
-        assert_same(got, want, dtype, f"{algo} shift {shift}")
-        # the element before each buffer is untouched
-        assert np.array_equal(from_dev([b[:shift] for b in big], dtype), x[:, :shift])
+        assert_same(got, want, dtype, f"{algo} shifts {shifts}")
+        for r in range(n):
+            assert np.array_equal(from_dev([big[r][:shifts[r]]], dtype)[0], x[r, :shifts[r]])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_reduce_scatter_all_gather_broadcast(ar, dtype):
+    n, count = 4, 3 * 2048 * 4 + 77
+    x = inputs(n, count, dtype, "values", seed=19)
+    vec = 8 if dtype == "bf16" else 4
+    for shifts in ([3] * n, [r % vec for r in range(n)]):
+        def views_of(data):
+            big = [to_dev(np.concatenate([data[r][:shifts[r]], data[r]])) for r in range(n)]
+            return [b[s:] for b, s in zip(big, shifts)]
+        for algo in ("ring", "tree", "ring_stepwise"):
+            want, _ = oracle.reduce_scatter(x, algo=ORACLE_ALGO[algo], op="sum", dtype=dtype)
+            v = views_of(x)
+            ar.check(ar.ar_reduce_scatter(v, count=count, dtype=dtype, op="sum", algo=algo), "rs")
+            got = from_dev(v, dtype)
+            for r in range(n):
+                lo, hi = oracle.chunk_range(count, n, r)
+                assert_same(got[r, lo:hi], want[r, lo:hi], dtype, f"rs {algo} {shifts}")
+            want, _ = oracle.all_gather(x, algo=ORACLE_ALGO[algo], dtype=dtype)
+            v = views_of(x)
+            ar.check(ar.ar_all_gather(v, count=count, dtype=dtype, algo=algo), "ag")
+            assert_same(from_dev(v, dtype), want, dtype, f"ag {algo} {shifts}")
+        want, _ = oracle.broadcast(x, root=2, dtype=dtype)
+        v = views_of(x)
+        ar.check(ar.ar_broadcast(v, count=count, dtype=dtype, root=2), "broadcast")
+        assert_same(from_dev(v, dtype), want, dtype, f"broadcast {shifts}")
 
 
 def test_degenerate_sizes(ar):
