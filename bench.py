@@ -211,7 +211,7 @@ def _oracle_worker(conn):
     import numpy as np
     import oracle
     oracle.lib()
-    x = pos = count = None
+    x = pos = count = out = None
     while True:
         msg = conn.recv()
         if msg[0] == "load":
@@ -220,8 +220,14 @@ def _oracle_worker(conn):
             conn.send(0.0)
         elif msg[0] == "run":
             t0 = time.perf_counter()
-            oracle.allreduce(x, algo="ring", op="sum", dtype="bf16", count=count, positions=pos)
+            out, _ = oracle.allreduce(x, algo="ring", op="sum", dtype="bf16", count=count, positions=pos)
             conn.send(time.perf_counter() - t0)
+        elif msg[0] == "digest":
+            # the last pass's result on this range: digest of rank 0's values
+            # and whether every rank holds the same
+            import hashlib
+            conn.send((hashlib.sha256(np.ascontiguousarray(out[0]).tobytes()).hexdigest(),
+                       bool(all(np.array_equal(out[r], out[0]) for r in range(out.shape[0])))))
         else:
             return
 
@@ -253,6 +259,12 @@ class OraclePool:
             c.recv()
         return [int(b[i + 1] - b[i]) for i in range(len(self.conns))]
 
+    def digests(self):
+        """Per process: (sha256 of rank 0's result on its range, ranks identical)."""
+        for c in self.conns:
+            c.send(("digest",))
+        return [c.recv() for c in self.conns]
+
     def run(self):
         """One pass over the whole input; returns (wall seconds, per-process seconds)."""
         t0 = time.perf_counter()
@@ -268,15 +280,20 @@ class OraclePool:
             p.join(timeout=60)
 
 
-def oracle_pass_time(x, procs: int, passes: int):
+def oracle_pass_time(x, procs: int, passes: int, gpu_result=None):
     """Time the oracle's ring AllReduce over the bf16 bit patterns x (n x count)
     on `procs` processes: one untimed pass, then `passes` timed ones.  Returns
     (seconds per pass, GB/s in the metric, median GB/s of one process on its
-    own range)."""
+    own range, parity) -- parity compares the oracle's result with
+    `gpu_result` (rank 0's result of the same inputs on the GPU, or None) by
+    digest, range by range."""
+    import hashlib
+    import numpy as np
     import oracle
     oracle.build()
     n, count = x.shape
     pool = OraclePool(procs)
+    parity = None
     try:
         widths = pool.load(x)
         pool.run()
@@ -285,11 +302,19 @@ def oracle_pass_time(x, procs: int, passes: int):
             dt, p = pool.run()
             total += dt
             per = [a + b for a, b in zip(per, p)]
+        if gpu_result is not None:
+            got = pool.digests()
+            lo, same = 0, True
+            for w, (digest, ranks_equal) in zip(widths, got):
+                mine = hashlib.sha256(np.ascontiguousarray(gpu_result[lo:lo + w]).tobytes()).hexdigest()
+                same = same and ranks_equal and mine == digest
+                lo += w
+            parity = {"vs": "oracle", "elements": int(count), "ranges": len(widths), "bit_identical": bool(same)}
     finally:
         pool.close()
     per_gbs = sorted(2 * n * w * 2 * passes / max(t, 1e-9) / 1e9 for w, t in zip(widths, per))
     dt = total / passes
-    return dt, 2 * n * count * 2 / dt / 1e9, per_gbs[len(per_gbs) // 2]
+    return dt, 2 * n * count * 2 / dt / 1e9, per_gbs[len(per_gbs) // 2], parity
 
 
 def run_reference(args, ws, rank):
@@ -515,15 +540,17 @@ class LargeWorkload:
                 raise self.ar.ArError(rc, "ar_allreduce")
         return bufs, step
 
-    def cpu_baseline(self):
+    def cpu_baseline(self, gpu_result=None):
         import numpy as np
         procs = self.args.cpu_procs or host_cores()
         passes = 3
-        dt, gbs, one = oracle_pass_time(self.host.numpy().view(np.uint16), procs, passes)
+        res = gpu_result.view(np.uint16) if gpu_result is not None else None
+        dt, gbs, one, parity = oracle_pass_time(self.host.numpy().view(np.uint16), procs, passes, res)
         return {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle", "one_process_gbs": one,
                 "sample": f"the whole workload ({self.n} ranks x {self.count} bf16), literal ring passes: "
                           f"1 untimed + {passes} timed at {dt:.3f} s each, element ranges split over "
-                          f"{procs} processes"}
+                          f"{procs} processes",
+                "parity": parity}
 
 
 class BucketWorkload:
@@ -570,16 +597,21 @@ class BucketWorkload:
                 raise self.ar.ArError(rc, "ar_allreduce")
         return bufs, step
 
-    def cpu_baseline(self):
+    def cpu_baseline(self, gpu_result=None):
+        import numpy as np
         import oracle
         from allreduce_gradient_reduction_gb300 import workloads as W
         oracle.build()
         x = W.bucket_inputs(self.n, self.count)
         t0 = time.perf_counter()
-        oracle.allreduce(x, algo="ring", op="avg", dtype="f32")
+        out, _ = oracle.allreduce(x, algo="ring", op="avg", dtype="f32")
         dt = time.perf_counter() - t0
+        parity = None
+        if gpu_result is not None:
+            same = all(np.array_equal(out[r].view(np.uint32), gpu_result.view(np.uint32)) for r in range(self.n))
+            parity = {"vs": "oracle", "elements": int(self.count), "bit_identical": bool(same)}
         return {"value": self.bytes_step / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"the whole workload, one literal ring pass, {dt:.2f} s, one thread"}
+                "sample": f"the whole workload, one literal ring pass, {dt:.2f} s, one thread", "parity": parity}
 
 
 class Gpt2Workload:
@@ -744,7 +776,7 @@ class Gpt2Workload:
                 "note": "backward = per-rank TF32 GEMMs (dW = X^T dY) on the compute stream; both streams share "
                         "one GPU"}
 
-    def cpu_baseline(self):
+    def cpu_baseline(self, gpu_result=None):
         import oracle
         from allreduce_gradient_reduction_gb300 import workloads as W
         oracle.build()
@@ -1012,7 +1044,13 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = wl.cpu_baseline()
+        # the accuracy step left the result of fresh inputs on the device:
+        # the oracle's own pass over the same inputs checks it bit for bit
+        rows = [dst for _, dst in wl.h2d]
+        gpu_result = rows[0].cpu().numpy() if all(torch.equal(r, rows[0]) for r in rows[1:]) else None
+        cpu = wl.cpu_baseline(gpu_result)
+        if gpu_result is None and cpu is not None:
+            cpu["parity"] = {"vs": "oracle", "bit_identical": False, "note": "ranks differ on the device"}
 
     if rank == 0:
         line = {
