@@ -517,9 +517,11 @@ class LargeWorkload:
         self.bufs = [torch.empty(self.count, dtype=torch.int16, device=dev) for _ in range(self.n)]
         self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
         self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
-        self.workload = WORKLOAD
+        self.workload = WORKLOAD if self.count == W.LARGE["count"] else (
+            f"ring AllReduce SUM, {self.n} ranks x {self.count:,} bf16 ({self.count * 2 / 2**20:g} MiB per rank)")
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
-                       "l2": "inputs larger than L2 (2 GiB touched per step vs 129 MB L2)"}
+                       "l2": ("inputs larger than L2" if self.n * self.count * 2 > 129e6 else "inputs partly L2-resident")
+                       + f" ({2 * self.n * self.count * 2 / 2**30:g} GiB touched per step vs 129 MB L2)"}
 
     def step(self, sid, algo):
         rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo, stream=sid)
