@@ -920,12 +920,18 @@ def main():
     import torch
 
     import __graft_entry__
-    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # one process per node compiles (a no-op when the library is up to date);
+    # the others wait, then only load it
+    if local == 0:
+        __graft_entry__.build()
+    barrier(ws)
+    if local != 0:
+        __graft_entry__.build()
     from allreduce_gradient_reduction_gb300 import binding as ar
     from allreduce_gradient_reduction_gb300 import workloads as W
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     if args.sweep:
         return run_sweep(args, ws, rank, dev, torch, ar)
     wl = {"large": LargeWorkload, "bucket": BucketWorkload, "gpt2": Gpt2Workload}[args.workload](
