@@ -76,6 +76,18 @@ MUTANTS = [
     ("int8 owner folds in index order",
      [("int rr = (c + 1 + p) % nranks;", "int rr = p;")],
      ["int8"]),
+    ("naive Reduce folds the root's own value first",
+     [("memcpy(s->rank[root], got[0], (size_t)s->m * (size_t)s->es);\n      for (r = 1; r < s->n; ++r) combine(s->dtype, s->op, s->rank[root], got[r], s->rank[root], s->m);",
+       "memcpy(s->rank[root], got[root], (size_t)s->m * (size_t)s->es);\n      for (r = 0; r < s->n; ++r) if (r != root) combine(s->dtype, s->op, s->rank[root], got[r], s->rank[root], s->m);")],
+     ["rooted"]),
+    ("Broadcast skips the last rank",
+     [("    if (r == root) continue;\n    if ((rc = post(s, root, r, all, s->n))) return rc;",
+       "    if (r == root || r == s->n - 1) continue;\n    if ((rc = post(s, root, r, all, s->n))) return rc;")],
+     ["rooted"]),
+    ("Reduce files gathered chunks one slot off",
+     [("memcpy(chunk_ptr(s, root, r), mb->data, (size_t)mb->n * (size_t)s->es);",
+       "memcpy(chunk_ptr(s, root, (r + 1) % s->n), mb->data, (size_t)mb->n * (size_t)s->es);")],
+     ["rooted"]),
     ("ring counts only received volume",
      [("s->st->sent[src] += total;", "(void)total;")],
      ["volume"]),
@@ -112,6 +124,12 @@ def run_pins(which):
         P.test_bucket_plan_gpt2(o)
     if "volume" in which:
         P.test_ring_volume_and_steps(o, 4)
+    if "rooted" in which:
+        for dt in ("f32", "bf16"):
+            P.test_naive_order_closed_form(o, dt)
+        for n in (3, 4):
+            P.test_reduce_then_broadcast_is_allreduce(o, "f32", n)
+        P.test_broadcast_copies_bits_and_volume(o)
     if "int8" in which:
         P.test_int8_exact_when_values_sit_on_the_grid(o)
         P.test_int8_codes_round_half_to_even(o)
@@ -141,7 +159,7 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
     real = oracle.lib()
     mutant = ctypes.CDLL(str(so))
     for fname in ("oracle_collective", "oracle_step", "oracle_f32_to_bf16", "oracle_chunk_range",
-                  "oracle_bucket_plan", "oracle_bucketed_allreduce", "oracle_int8_ef_allreduce"):
+                  "oracle_bucket_plan", "oracle_bucketed_allreduce", "oracle_int8_ef_allreduce", "oracle_rooted"):
         getattr(mutant, fname).argtypes = getattr(real, fname).argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)
     with pytest.raises((AssertionError, oracle.OracleError)):
@@ -150,4 +168,4 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
 
 def test_real_oracle_passes_the_same_pins():
     run_pins({"ring_order", "tree_order", "bruteforce", "printed", "bf16_round", "avg", "max", "f32_add",
-              "bucket", "volume", "dbtree", "int8"})
+              "bucket", "volume", "dbtree", "int8", "rooted"})
