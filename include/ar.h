@@ -183,7 +183,9 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
  *               each (all 2N ranges disjoint); both updated in place.  Start
  *               training with zeroed residuals.
  *   op          AR_SUM or AR_AVG (AR_MAX: AR_ERR_UNSUPPORTED)
- * Inputs must be finite.  Errors as ar_allreduce.
+ * Inputs must be finite.  Errors as ar_allreduce.  All 2N buffers 16-byte
+ * aligned: 16-byte accesses; otherwise each lane's four elements are loaded
+ * one by one (same results).
  */
 int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
                          ar_stream_t stream);
