@@ -1087,6 +1087,7 @@ def main():
         print(json.dumps(line))
     if ws > 1:
         import torch.distributed as dist
+        barrier(ws)  # rank 0's accuracy and printing come last: leave together
         dist.destroy_process_group()
     return 0
 
