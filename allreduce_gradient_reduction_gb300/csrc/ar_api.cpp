@@ -161,6 +161,22 @@ struct Job {
   bool aligned = false;   // every buffer 16-byte aligned (the single-block step-wise form stages with it)
 };
 
+// A table whose rows fit the small launch form (see ar::SmallSegTable).
+bool fits_small(const SegTable& tab) {
+  if (tab.nseg < 1 || tab.nseg > ar::kSmallSegCap) return false;
+  return (int64_t)(tab.seg[tab.nseg - 1].tensor + 1) * tab.nranks <= ar::kMaxRanks;
+}
+
+template <class ARGS>
+void fill_fused(const Job& j, int nranks, ARGS& a) {
+  a.avg = j.avg ? 1 : 0;
+  a.owner_only = j.phases == 1 ? 1 : 0;
+  a.to_root = j.root >= 0 ? 1 : 0;
+  a.root = j.root >= 0 ? j.root : 0;
+  a.max_grid = j.max_grid;
+  a.fn = (float)nranks;
+}
+
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   const int dop = j.op == AR_MAX ? ar::MAX : ar::SUM;
   const bool stepwise = j.algo == AR_RING_STEPWISE || j.algo == AR_TREE_STEPWISE;
@@ -204,15 +220,20 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
     e = ar::launch_stepwise(j.dtype, dop, j.vec, a, s);
   } else if (j.phases == 2) {
     e = ar::launch_gather(esize_of(j.dtype), j.vec, tab, s);
+  } else if (fits_small(tab)) {
+    ar::SmallFusedArgs a;
+    const int nptr = (tab.seg[tab.nseg - 1].tensor + 1) * tab.nranks;
+    memcpy(a.tab.ptr, tab.ptr, sizeof(void*) * (size_t)nptr);
+    memcpy(a.tab.seg, tab.seg, sizeof(Seg) * (size_t)tab.nseg);
+    a.tab.nranks = tab.nranks;
+    a.tab.nseg = tab.nseg;
+    a.tab.ntiles = 0;
+    fill_fused(j, tab.nranks, a);
+    e = ar::launch_fused(j.dtype, dop, order, j.vec, a, s);
   } else {
     ar::FusedArgs a;
     a.tab = tab;
-    a.avg = j.avg ? 1 : 0;
-    a.owner_only = j.phases == 1 ? 1 : 0;
-    a.to_root = j.root >= 0 ? 1 : 0;
-    a.root = j.root >= 0 ? j.root : 0;
-    a.max_grid = j.max_grid;
-    a.fn = (float)tab.nranks;
+    fill_fused(j, tab.nranks, a);
     e = ar::launch_fused(j.dtype, dop, order, j.vec, a, s);
   }
   return e == cudaSuccess ? AR_OK : cuda_fail(e);

@@ -141,8 +141,15 @@ cudaError_t launch_fused_bf16_sum(int, bool, FusedArgs&, cudaStream_t);
 cudaError_t launch_fused_bf16_max(int, bool, FusedArgs&, cudaStream_t);
 cudaError_t launch_fused_i32_sum(int, bool, FusedArgs&, cudaStream_t);
 cudaError_t launch_fused_i32_max(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f32_sum(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f32_max(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_bf16_sum(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_bf16_max(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_i32_sum(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_i32_max(int, bool, SmallFusedArgs&, cudaStream_t);
 
-cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& a, cudaStream_t s) {
+template <class ARGS>
+static cudaError_t launch_fused_any(int dtype, int op, int order, bool vec, ARGS& a, cudaStream_t s) {
   switch (dtype * 2 + op) {
     case F32 * 2 + SUM: return launch_fused_f32_sum(order, vec, a, s);
     case F32 * 2 + MAX: return launch_fused_f32_max(order, vec, a, s);
@@ -152,6 +159,14 @@ cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& a, c
     case I32 * 2 + MAX: return launch_fused_i32_max(order, vec, a, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& a, cudaStream_t s) {
+  return launch_fused_any(dtype, op, order, vec, a, s);
+}
+
+cudaError_t launch_fused(int dtype, int op, int order, bool vec, SmallFusedArgs& a, cudaStream_t s) {
+  return launch_fused_any(dtype, op, order, vec, a, s);
 }
 
 int sm_count() {

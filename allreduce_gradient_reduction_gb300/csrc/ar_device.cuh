@@ -117,7 +117,8 @@ __device__ __forceinline__ void st_elem(void* base, int64_t e, uint32_t v) {
 // ---- segments and tiles -----------------------------------------------------
 
 // Index of the segment holding `tile`: the last segment whose tile_begin is <= tile.
-__device__ __forceinline__ int find_seg(const SegTable& t, int64_t tile) {
+template <class TABLE>
+__device__ __forceinline__ int find_seg(const TABLE& t, int64_t tile) {
   int lo = 0, hi = t.nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;

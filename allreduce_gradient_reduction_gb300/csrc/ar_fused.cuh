@@ -68,13 +68,13 @@ __device__ __forceinline__ uint4 inorder_fold_regs(const uint4 (&x)[NR]) {
   return acc;
 }
 
-template <int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ FusedArgs a) {
+template <class ARGS, int DT, int OP, int ORDER, int NR>
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int U = fused_unroll(ORDER, NR);
   constexpr int TILE_V = kFusedBlock * U;
-  const SegTable& T = a.tab;
+  const auto& T = a.tab;
   const int n = NR > 0 ? NR : T.nranks;
 
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
@@ -221,10 +221,10 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
 
 // Same computation one element per thread, for buffers that are not all
 // 16-byte aligned.
-template <int DT, int OP, int ORDER>
-__global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_constant__ FusedArgs a) {
+template <class ARGS, int DT, int OP, int ORDER>
+__global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
-  const SegTable& T = a.tab;
+  const auto& T = a.tab;
   const int n = T.nranks;
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
@@ -247,7 +247,8 @@ __global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_
 // leftover scalars but no full vector still gets one tile.  `shifted`: the
 // kernel cuts vectors at the row's shift (row_shift of its first pointer),
 // as the fused, gather and step-wise kernels do; the copy kernels do not.
-inline int64_t fill_tiles(SegTable& t, int vec, int64_t tile_units, bool shifted = false) {
+template <class TABLE>
+inline int64_t fill_tiles(TABLE& t, int vec, int64_t tile_units, bool shifted = false) {
   int64_t acc = 0;
   for (int i = 0; i < t.nseg; ++i) {
     Seg& s = t.seg[i];
@@ -284,26 +285,26 @@ inline unsigned grid_for(int64_t ntiles, int64_t cap = 0) {
   return (unsigned)g;
 }
 
-template <int DT, int OP, int ORDER, int NR>
-cudaError_t launch_fused_vec(FusedArgs& a, cudaStream_t stream) {
+template <int DT, int OP, int ORDER, int NR, class ARGS>
+cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
   constexpr int U = fused_unroll(ORDER, NR);
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U, true) == 0) return cudaSuccess;
-  fused_vec_kernel<DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
+  fused_vec_kernel<ARGS, DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
 
-template <int DT, int OP, int ORDER>
-cudaError_t launch_fused_scalar(FusedArgs& a, cudaStream_t stream) {
+template <int DT, int OP, int ORDER, class ARGS>
+cudaError_t launch_fused_scalar(ARGS& a, cudaStream_t stream) {
   if (fill_tiles(a.tab, 1, kFusedBlock) == 0) return cudaSuccess;
-  fused_scalar_kernel<DT, OP, ORDER><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
+  fused_scalar_kernel<ARGS, DT, OP, ORDER><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
 }
 
 // Dispatch on order and rank count for one (dtype, op).
-template <int DT, int OP>
-cudaError_t launch_fused_typed(int order, bool vec, FusedArgs& a, cudaStream_t stream) {
+template <int DT, int OP, class ARGS>
+cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
   if (order == DBTREE) {
     // register-resident trees for the common rank counts, the element-wise
@@ -342,6 +343,9 @@ cudaError_t launch_fused_typed(int order, bool vec, FusedArgs& a, cudaStream_t s
 #define AR_DEFINE_FUSED(NAME, DT, OP)                                                              \
   namespace ar {                                                                                  \
   cudaError_t NAME(int order, bool vec, FusedArgs& a, cudaStream_t s) {                           \
+    return launch_fused_typed<DT, OP>(order, vec, a, s);                                          \
+  }                                                                                               \
+  cudaError_t NAME(int order, bool vec, SmallFusedArgs& a, cudaStream_t s) {                      \
     return launch_fused_typed<DT, OP>(order, vec, a, s);                                          \
   }                                                                                               \
   }

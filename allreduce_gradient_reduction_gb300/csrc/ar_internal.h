@@ -26,13 +26,20 @@ struct Seg {
   int32_t chunk;       // chunk id c (ring order starts at rank c+1); copy kernels: 1 = vectorisable
 };
 
-struct SegTable {
-  const void* ptr[kPtrCap];
-  Seg seg[kSegCap];
+template <int PTRS, int SEGS>
+struct SegTableT {
+  const void* ptr[PTRS];
+  Seg seg[SEGS];
   int32_t nranks;
   int32_t nseg;
   int64_t ntiles;
 };
+// Launch tables travel as kernel parameters, and a launch costs more the
+// larger they are (16 KB: about 0.9 us more per call than 3 KB).  Calls
+// whose rows fit use the small form.
+using SegTable = SegTableT<kPtrCap, kSegCap>;
+constexpr int kSmallSegCap = 72;
+using SmallSegTable = SegTableT<kMaxRanks, kSmallSegCap>;
 
 // Per-device block used by the step-wise kernels' grid barrier.
 struct SyncBlock {
@@ -42,8 +49,9 @@ struct SyncBlock {
   int pad;
 };
 
-struct FusedArgs {
-  SegTable tab;
+template <class TABLE>
+struct FusedArgsT {
+  TABLE tab;
   int32_t avg;         // divide reduced values by nranks
   int32_t owner_only;  // ReduceScatter: store to the chunk owner only
   int32_t to_root;     // Reduce: store to rank `root` only
@@ -51,6 +59,8 @@ struct FusedArgs {
   int32_t max_grid;    // > 0: at most this many blocks (they stride over the tiles)
   float fn;            // (float)nranks
 };
+using FusedArgs = FusedArgsT<SegTable>;
+using SmallFusedArgs = FusedArgsT<SmallSegTable>;
 
 struct StepArgs {
   SegTable tab;
@@ -105,6 +115,7 @@ struct Int8Args {
 // tile shape, then enqueues on `stream`.  `vec` selects the 16-byte path
 // (every pointer 16-byte aligned); otherwise one element per thread.
 cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& args, cudaStream_t stream);
+cudaError_t launch_fused(int dtype, int op, int order, bool vec, SmallFusedArgs& args, cudaStream_t stream);
 cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t stream);
 cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
