@@ -571,7 +571,7 @@ class BucketWorkload:
         self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
         self.workload = "ring AllReduce AVG, 8 ranks x 6,553,600 f32 (one 25 MiB DDP bucket)"
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
-                       "l2": "409.6 MiB touched per step vs 129 MB L2 (partly L2-resident between steps)"}
+                       "l2": "inputs larger than L2 (409.6 MiB touched per step vs 129 MB L2)"}
 
     def step(self, sid, algo, int8=False, op=None):
         if int8:
