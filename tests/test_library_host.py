@@ -115,3 +115,50 @@ def test_strerror_and_version(ar):
     for code, name in ar.STATUS.items():
         assert ar.ar_strerror(code).startswith(name)
     assert ar.ar_version() >= 100
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "ar.h"
+
+int main(void) {
+  int64_t lo = -1, hi = -1;
+  int64_t counts[4] = {10, 300, 7, 2000};
+  int32_t bucket_of[4];
+  int64_t offset[4], bcount[4];
+  int32_t nb = 0;
+  int rc;
+  void* none[2] = {0, 0};
+  if (ar_version() <= 0) return 1;
+  if (ar_chunk_range(10, 3, 2, &lo, &hi) != AR_OK || lo != 6 || hi != 10) return 2;
+  rc = ar_bucket_plan(counts, 4, AR_F32, 4096, bucket_of, offset, bcount, &nb);
+  if (rc != AR_OK) return 3;
+  printf("%d", nb);
+  for (int i = 0; i < nb; ++i) printf(" %lld", (long long)bcount[i]);
+  printf("\n");
+  /* argument checks run on the host, before any CUDA call */
+  if (ar_allreduce(none, 0, 16, AR_F32, AR_SUM, AR_RING, 0) != AR_ERR_INVALID_ARG) return 4;
+  if (ar_allreduce(none, 2, 16, AR_I32, AR_AVG, AR_RING, 0) != AR_ERR_UNSUPPORTED) return 5;
+  if (strncmp(ar_strerror(AR_ERR_TIMEOUT), "AR_ERR_TIMEOUT", 14) != 0) return 6;
+  return 0;
+}
+"""
+
+
+def test_c_program_compiles_links_and_runs_against_the_header(ar, tmp_path):
+    """The boundary is plain C: a C11 program includes include/ar.h, links
+    libar_gb300.so and calls the host-side entry points (no GPU needed)."""
+    src = tmp_path / "use_ar.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_ar"
+    libdir = os.path.dirname(ar.LIB_PATH) if hasattr(ar, "LIB_PATH") else os.path.join(
+        ROOT, "allreduce_gradient_reduction_gb300")
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-lar_gb300", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, env=dict(os.environ, LD_LIBRARY_PATH=libdir))
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    want = oracle.bucket_plan([10, 300, 7, 2000], dtype="f32", cap_bytes=4096)
+    fields = r.stdout.split()
+    assert int(fields[0]) == len(want[2])
+    assert [int(v) for v in fields[1:]] == [int(v) for v in want[2]]
