@@ -101,6 +101,7 @@ int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
 
 int check_bufs(void* const* bufs, int nranks, int64_t count, int dtype) {
   if (!bufs) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;  // nothing is accessed: any pointers (NULL included) will do
   std::vector<Range> rs;
   for (int r = 0; r < nranks; ++r) {
     uintptr_t p = (uintptr_t)bufs[r];
@@ -490,6 +491,7 @@ int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks,
   if (rc) return rc;
   if (op == AR_MAX) return AR_ERR_UNSUPPORTED;
   if (!grads || !residuals) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;  // nothing is accessed
   std::vector<Range> rs;
   for (int r = 0; r < nranks; ++r) {
     rs.push_back({(uintptr_t)grads[r], (uintptr_t)grads[r] + (uintptr_t)count * 4});

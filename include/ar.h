@@ -33,6 +33,8 @@
  *     per tensor: each tensor's N buffers.)
  *   - 1 <= nranks <= AR_MAX_RANKS; count >= 0; count == 0 and nranks == 1 do
  *     nothing (a single rank already holds the reduction; AVG divides by 1).
+ *     With count == 0 the buffer pointers are not examined (NULL is fine,
+ *     as an empty tensor's is); the host array itself must not be NULL.
  *   - Chunks: each rank buffer is split into N contiguous chunks,
  *     chunk c = [floor(c*count/N), floor((c+1)*count/N)); rank c owns chunk c
  *     after ReduceScatter.  [concept §3], [tutorial §2.2], [notes §两阶段流程].

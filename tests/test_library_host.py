@@ -162,3 +162,18 @@ def test_c_program_compiles_links_and_runs_against_the_header(ar, tmp_path):
     fields = r.stdout.split()
     assert int(fields[0]) == len(want[2])
     assert [int(v) for v in fields[1:]] == [int(v) for v in want[2]]
+
+
+def test_count_zero_is_a_no_op_with_any_pointers(ar):
+    # an empty tensor's data pointer is NULL; with nothing to move the calls
+    # succeed without looking at the pointers (and without touching CUDA)
+    nulls = [0, 0, 0, 0]
+    assert ar.ar_allreduce(nulls, count=0, dtype="bf16", algo="ring", stream=0) == ar.AR_OK
+    assert ar.ar_reduce_scatter(nulls, count=0, algo="tree", stream=0) == ar.AR_OK
+    assert ar.ar_all_gather(nulls, count=0, stream=0) == ar.AR_OK
+    assert ar.ar_reduce(nulls, count=0, root=2, stream=0) == ar.AR_OK
+    assert ar.ar_broadcast(nulls, count=0, root=1, stream=0) == ar.AR_OK
+    assert ar.ar_allreduce_int8_ef(nulls, nulls, count=0, op="avg", stream=0) == ar.AR_OK
+    # argument checks still apply
+    assert ar.ar_reduce(nulls, count=0, root=7, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce(nulls, count=0, dtype="i32", op="avg", stream=0) == ar.AR_ERR_UNSUPPORTED
