@@ -62,10 +62,10 @@ def shifts_for(rng, n, dtype):
     return [int(rng.integers(0, vec)) for _ in range(n)]
 
 
-@pytest.mark.parametrize("block", range(6))
+@pytest.mark.parametrize("block", range(12))
 def test_random_collectives(ar, block):
     rng = np.random.default_rng(7000 + block)
-    for case in range(40):
+    for case in range(50):
         n = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 16, 32, 64]))
         count = int(rng.choice([0, 1, n - 1, n, n + 1, int(rng.integers(1, 300)), int(rng.integers(300, 20000))]))
         count = max(count, 0)
@@ -120,7 +120,7 @@ def test_random_collectives(ar, block):
         assert rc == 0 and st == 0, what
 
 
-@pytest.mark.parametrize("block", range(3))
+@pytest.mark.parametrize("block", range(6))
 def test_random_bucketed(ar, block):
     rng = np.random.default_rng(8000 + block)
     for case in range(12):
