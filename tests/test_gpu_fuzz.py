@@ -147,3 +147,79 @@ def test_random_bucketed(ar, block):
         for r in range(n):
             for i in range(t):
                 assert same_bits(host(dg[r][i], "f32"), want[r][i], "f32"), f"{what} rank {r} tensor {i}"
+
+
+@pytest.mark.parametrize("block", range(4))
+def test_random_int8_ef(ar, block):
+    rng = np.random.default_rng(9000 + block)
+    for case in range(15):
+        n = int(rng.choice([1, 2, 3, 4, 5, 8, 13, 16]))
+        count = int(rng.choice([0, 1, 127, 128, 129, int(rng.integers(1, 3000)), int(rng.integers(3000, 40000))]))
+        op = str(rng.choice(["sum", "avg"]))
+        shift = int(rng.choice([0, 0, 1, 3]))  # elements, the same for every buffer
+        x = W.normal_inputs(n, count, float(rng.choice([1e-3, 1.0, 50.0])), int(rng.integers(1 << 20)))
+        e = W.normal_inputs(n, count, 1e-5, int(rng.integers(1 << 20)))
+        what = f"int8 case {block}/{case}: n={n} count={count} {op} shift={shift}"
+        for it in range(2):  # the residuals carry over
+            want_x, want_e, _ = oracle.int8_ef_allreduce(x, e, op=op)
+            xd = [place(x[r], "f32", shift) for r in range(n)]
+            ed = [place(e[r], "f32", shift) for r in range(n)]
+            ar.check(ar.ar_allreduce_int8_ef(xd, ed, count=count, op=op), what)
+            torch.cuda.synchronize()
+            for r in range(n):
+                assert same_bits(host(xd[r], "f32"), want_x[r], "f32"), f"{what} it={it} x rank {r}"
+                assert same_bits(host(ed[r], "f32"), want_e[r], "f32"), f"{what} it={it} e rank {r}"
+            e = np.stack([host(t, "f32") for t in ed]) if count else e
+            x = W.normal_inputs(n, count, 1e-3, int(rng.integers(1 << 20)))
+
+
+@pytest.mark.parametrize("block", range(2))
+def test_random_plans(ar, block):
+    """Prepared calls, each run three times on new data, against the oracle."""
+    rng = np.random.default_rng(9500 + block)
+    for case in range(10):
+        n = int(rng.choice([2, 3, 4, 8, 16]))
+        count = int(rng.integers(1, 20000))
+        dtype = str(rng.choice(["f32", "bf16", "i32"]))
+        kind = str(rng.choice(["allreduce", "reduce_scatter", "all_gather", "reduce"]))
+        algos = ["ring", "ring_stepwise"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
+        if kind == "allreduce":
+            algos += ["naive", "dbtree"]
+        if kind == "reduce":
+            algos = [a for a in algos if not a.endswith("stepwise")] + ["naive"]
+        algo = str(rng.choice(algos))
+        op = str(rng.choice(["sum", "max"] + ([] if dtype == "i32" else ["avg"])))
+        root = int(rng.integers(0, n))
+        shifts = shifts_for(rng, n, dtype)
+        bufs = [place(np.zeros(count, dtype={"f32": np.float32, "bf16": np.uint16, "i32": np.int32}[dtype]),
+                      dtype, shifts[r]) for r in range(n)]
+        plan = ar.Plan(kind, bufs, count=count, dtype=dtype, op=op, algo=algo, root=root)
+        oa = {"ring_stepwise": "ring", "tree_stepwise": "tree"}.get(algo, algo)
+        what = f"plan case {block}/{case}: {kind} {algo} {dtype} {op} n={n} count={count}"
+        for it in range(3):
+            x = W.uniform_inputs(n, count, dtype, config=int(rng.integers(1 << 20)))
+            for r in range(n):
+                src = np.ascontiguousarray(x[r])
+                bufs[r].copy_(torch.from_numpy(src.view(np.int16) if dtype == "bf16" else src))
+            ar.check(plan.run(), what)
+            torch.cuda.synchronize()
+            with np.errstate(all="ignore"):
+                if kind == "allreduce":
+                    want, _ = oracle.allreduce(x, algo=oa, op=op, dtype=dtype)
+                elif kind == "reduce_scatter":
+                    want, _ = oracle.reduce_scatter(x, algo=oa, op=op, dtype=dtype)
+                elif kind == "all_gather":
+                    want, _ = oracle.all_gather(x, algo=oa, dtype=dtype)
+                else:
+                    want, _ = oracle.reduce(x, algo=oa, op=op, dtype=dtype, root=root)
+            for r in range(n):
+                got = host(bufs[r], dtype)
+                if kind == "reduce_scatter":
+                    lo, hi = oracle.chunk_range(count, n, r)
+                    assert same_bits(got[lo:hi], want[r][lo:hi], dtype), f"{what} it={it} rank {r}"
+                elif kind == "reduce":
+                    if r == root:
+                        assert same_bits(got, want[r], dtype), f"{what} it={it} root"
+                else:
+                    assert same_bits(got, want[r], dtype), f"{what} it={it} rank {r}"
+        plan.close()
