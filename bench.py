@@ -38,7 +38,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fused_ring_bf16_8x128MiB.md")
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=2000)  # about 0.6 s timed: several clock samples
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--algo", default="ring", help="ring | tree | ring_stepwise | tree_stepwise")
