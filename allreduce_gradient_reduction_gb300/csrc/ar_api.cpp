@@ -449,69 +449,92 @@ void reducer_free(ar_reducer* red) {
 
 }  // namespace
 
+// Nothing may unwind through the C ABI: a host allocation failure (or any
+// other exception) in an entry point becomes AR_ERR_HOST.
+template <class F>
+int guarded(F f) noexcept {
+  try {
+    return f();
+  } catch (...) {
+    return AR_ERR_HOST;
+  }
+}
+
 extern "C" {
 
 int ar_allreduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
                  ar_stream_t stream) {
-  return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream);
+  return guarded([&]() -> int {
+    return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream);
+  });
 }
 
 int ar_reduce_scatter(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
                       ar_stream_t stream) {
-  return collective(bufs, nranks, count, dtype, op, algo, 1, (cudaStream_t)stream);
+  return guarded([&]() -> int {
+    return collective(bufs, nranks, count, dtype, op, algo, 1, (cudaStream_t)stream);
+  });
 }
 
 int ar_all_gather(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_algo algo, ar_stream_t stream) {
-  return collective(bufs, nranks, count, dtype, AR_SUM, algo, 2, (cudaStream_t)stream);
+  return guarded([&]() -> int {
+    return collective(bufs, nranks, count, dtype, AR_SUM, algo, 2, (cudaStream_t)stream);
+  });
 }
 
 int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo, int root,
               ar_stream_t stream) {
-  if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
-  if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
-  return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream, root);
+  return guarded([&]() -> int {
+    if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+    if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+    return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream, root);
+  });
 }
 
 int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, int root, ar_stream_t stream) {
-  if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
-  int rc = check_common(nranks, count, dtype, AR_SUM, AR_RING);
-  if (rc) return rc;
-  if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
-  if (count == 0 || nranks == 1) return AR_OK;
-  // one segment owned by the root: the AllGather copy kernel sends it to every other rank
-  TableBuilder tb{nranks, {}, {}};
-  tb.add_seg(tb.add_row(bufs), 0, count, root);
-  Job j{dtype, AR_SUM, AR_RING, 2, false, same_phase16(bufs, nranks)};
-  return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
+  return guarded([&]() -> int {
+    if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+    int rc = check_common(nranks, count, dtype, AR_SUM, AR_RING);
+    if (rc) return rc;
+    if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
+    if (count == 0 || nranks == 1) return AR_OK;
+    // one segment owned by the root: the AllGather copy kernel sends it to every other rank
+    TableBuilder tb{nranks, {}, {}};
+    tb.add_seg(tb.add_row(bufs), 0, count, root);
+    Job j{dtype, AR_SUM, AR_RING, 2, false, same_phase16(bufs, nranks)};
+    return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
+  });
 }
 
 int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks, int64_t count, ar_op op,
                          ar_stream_t stream) {
-  int rc = check_common(nranks, count, AR_F32, op, AR_RING);
-  if (rc) return rc;
-  if (op == AR_MAX) return AR_ERR_UNSUPPORTED;
-  if (!grads || !residuals) return AR_ERR_INVALID_ARG;
-  if (count == 0) return AR_OK;  // nothing is accessed
-  std::vector<Range> rs;
-  for (int r = 0; r < nranks; ++r) {
-    rs.push_back({(uintptr_t)grads[r], (uintptr_t)grads[r] + (uintptr_t)count * 4});
-    rs.push_back({(uintptr_t)residuals[r], (uintptr_t)residuals[r] + (uintptr_t)count * 4});
-  }
-  if ((rc = check_ranges(rs, 4))) return rc;
-  if (count == 0) return AR_OK;
-  ar::Int8Args a;
-  memset(&a, 0, sizeof(a));
-  for (int r = 0; r < nranks; ++r) {
-    a.x[r] = static_cast<float*>(grads[r]);
-    a.e[r] = static_cast<float*>(residuals[r]);
-  }
-  a.count = count;
-  a.nranks = nranks;
-  a.avg = op == AR_AVG ? 1 : 0;
-  a.vec = all_aligned16(grads, nranks) && all_aligned16(residuals, nranks) ? 1 : 0;
-  a.fn = (float)nranks;
-  cudaError_t e = ar::launch_int8_ef(a, (cudaStream_t)stream);
-  return e == cudaSuccess ? AR_OK : cuda_fail(e);
+  return guarded([&]() -> int {
+    int rc = check_common(nranks, count, AR_F32, op, AR_RING);
+    if (rc) return rc;
+    if (op == AR_MAX) return AR_ERR_UNSUPPORTED;
+    if (!grads || !residuals) return AR_ERR_INVALID_ARG;
+    if (count == 0) return AR_OK;  // nothing is accessed
+    std::vector<Range> rs;
+    for (int r = 0; r < nranks; ++r) {
+      rs.push_back({(uintptr_t)grads[r], (uintptr_t)grads[r] + (uintptr_t)count * 4});
+      rs.push_back({(uintptr_t)residuals[r], (uintptr_t)residuals[r] + (uintptr_t)count * 4});
+    }
+    if ((rc = check_ranges(rs, 4))) return rc;
+    if (count == 0) return AR_OK;
+    ar::Int8Args a;
+    memset(&a, 0, sizeof(a));
+    for (int r = 0; r < nranks; ++r) {
+      a.x[r] = static_cast<float*>(grads[r]);
+      a.e[r] = static_cast<float*>(residuals[r]);
+    }
+    a.count = count;
+    a.nranks = nranks;
+    a.avg = op == AR_AVG ? 1 : 0;
+    a.vec = all_aligned16(grads, nranks) && all_aligned16(residuals, nranks) ? 1 : 0;
+    a.fn = (float)nranks;
+    cudaError_t e = ar::launch_int8_ef(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? AR_OK : cuda_fail(e);
+  });
 }
 
 int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
@@ -523,231 +546,243 @@ int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
 
 int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t cap_bytes, int32_t* bucket_of_tensor,
                    int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets) {
-  if (ntensors < 0 || cap_bytes <= 0 || dtype < AR_F32 || dtype > AR_I32 || !nbuckets) return AR_ERR_INVALID_ARG;
-  if (ntensors > 0 && (!counts || !bucket_of_tensor || !offset_in_bucket || !bucket_count)) return AR_ERR_INVALID_ARG;
-  return plan_buckets(counts, ntensors, dtype, cap_bytes, bucket_of_tensor, offset_in_bucket, bucket_count, nbuckets);
+  return guarded([&]() -> int {
+    if (ntensors < 0 || cap_bytes <= 0 || dtype < AR_F32 || dtype > AR_I32 || !nbuckets) return AR_ERR_INVALID_ARG;
+    if (ntensors > 0 && (!counts || !bucket_of_tensor || !offset_in_bucket || !bucket_count)) return AR_ERR_INVALID_ARG;
+    return plan_buckets(counts, ntensors, dtype, cap_bytes, bucket_of_tensor, offset_in_bucket, bucket_count, nbuckets);
+  });
 }
 
 int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype,
                           ar_op op, ar_algo algo, int64_t bucket_cap_bytes, void* const* workspace,
                           int64_t workspace_bytes, ar_stream_t stream_) {
-  cudaStream_t stream = (cudaStream_t)stream_;
-  int rc = check_common(nranks, 0, dtype, op, algo);
-  if (rc) return rc;
-  if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
-  if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
-  if (ntensors == 0) return AR_OK;
-  if (!grads || !counts) return AR_ERR_INVALID_ARG;
-  const int es = esize_of(dtype);
-  std::vector<int32_t> bucket_of(ntensors);
-  std::vector<int64_t> offset(ntensors), bcount(ntensors);
-  int32_t nb = 0;
-  if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, bucket_of.data(), offset.data(), bcount.data(),
-                         &nb)))
-    return rc;
-  {
-    std::vector<Range> rs;
-    for (int r = 0; r < nranks; ++r)
-      for (int t = 0; t < ntensors; ++t) {
-        if (counts[t] == 0) continue;
-        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
-        rs.push_back({p, p + (uintptr_t)counts[t] * es});
-      }
-    if ((rc = check_ranges(rs, es))) return rc;
-  }
-  if (nranks == 1) return AR_OK;
-  const bool avg = op == AR_AVG;
-  // row t of the pointer table: tensor t of every rank
-  std::vector<void*> row(nranks);
-  auto tensor_row = [&](int t) {
-    for (int r = 0; r < nranks; ++r) row[r] = grads[(size_t)r * ntensors + t];
-    return row.data();
-  };
-
-  if (!workspace) {
-    // Fused: no packing; one pass reads and writes every gradient element once.
-    TableBuilder tb{nranks, {}, {}};
-    const bool vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, bucket_of.data(), offset.data(),
-                                     bcount.data(), [](int) { return true; });
-    Job j{dtype, op, algo, 3, avg, vec};
-    return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
-  }
-
-  // Literal: pack -> AllReduce the flat buckets -> unpack.
-  int64_t total = 0, largest = 0;
-  std::vector<int64_t> base(nb);
-  for (int b = 0; b < nb; ++b) {
-    base[b] = total;
-    total += bcount[b];
-    largest = std::max(largest, bcount[b]);
-  }
-  if (workspace_bytes < largest * es) return AR_ERR_INVALID_ARG;
-  {
-    std::vector<Range> rs;
-    for (int r = 0; r < nranks; ++r) {
-      uintptr_t p = (uintptr_t)workspace[r];
-      rs.push_back({p, p + (uintptr_t)workspace_bytes});
+  return guarded([&]() -> int {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    int rc = check_common(nranks, 0, dtype, op, algo);
+    if (rc) return rc;
+    if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
+    if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
+    if (ntensors == 0) return AR_OK;
+    if (!grads || !counts) return AR_ERR_INVALID_ARG;
+    const int es = esize_of(dtype);
+    std::vector<int32_t> bucket_of(ntensors);
+    std::vector<int64_t> offset(ntensors), bcount(ntensors);
+    int32_t nb = 0;
+    if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, bucket_of.data(), offset.data(), bcount.data(),
+                           &nb)))
+      return rc;
+    {
+      std::vector<Range> rs;
+      for (int r = 0; r < nranks; ++r)
+        for (int t = 0; t < ntensors; ++t) {
+          if (counts[t] == 0) continue;
+          uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+          rs.push_back({p, p + (uintptr_t)counts[t] * es});
+        }
+      if ((rc = check_ranges(rs, es))) return rc;
     }
-    for (int r = 0; r < nranks; ++r)
-      for (int t = 0; t < ntensors; ++t) {
-        if (counts[t] == 0) continue;
-        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
-        rs.push_back({p, p + (uintptr_t)counts[t] * es});
-      }
-    if ((rc = check_ranges(rs, es))) return rc;
-  }
-  const bool whole = workspace_bytes >= total * es;
-  const bool ws_aligned = all_aligned16(workspace, nranks);
-
-  // buckets [b0, b1) at once: pack them, reduce them, unpack them
-  auto run_buckets = [&](int b0, int b1) -> int {
-    const int64_t shift = base[b0];  // packed offset of bucket b0 in the workspace
-    auto copy = [&](int to_packed) -> int {
-      TableBuilder cb{nranks, {}, {}};
-      for (int t = 0; t < ntensors; ++t) {
-        if (counts[t] == 0 || bucket_of[t] < b0 || bucket_of[t] >= b1) continue;
-        void** rp = tensor_row(t);
-        const int64_t aux = base[bucket_of[t]] - shift + offset[t];
-        const bool v = all_aligned16(rp, nranks) && ws_aligned && (aux * es) % 16 == 0;
-        const int rw = cb.add_row(rp);
-        cb.add_seg(rw, 0, counts[t], v ? 1 : 0, aux);
-      }
-      ar::CopyArgs ca;
-      for (int r = 0; r < nranks; ++r) ca.packed[r] = workspace[r];
-      ca.to_packed = to_packed;
-      ca.esize = es;
-      return cb.for_each_table([&](SegTable& t) {
-        ca.tab = t;
-        cudaError_t e = ar::launch_copy(ca, stream);
-        return e == cudaSuccess ? AR_OK : cuda_fail(e);
-      });
+    if (nranks == 1) return AR_OK;
+    const bool avg = op == AR_AVG;
+    // row t of the pointer table: tensor t of every rank
+    std::vector<void*> row(nranks);
+    auto tensor_row = [&](int t) {
+      for (int r = 0; r < nranks; ++r) row[r] = grads[(size_t)r * ntensors + t];
+      return row.data();
     };
-    auto reduce = [&]() -> int {
+
+    if (!workspace) {
+      // Fused: no packing; one pass reads and writes every gradient element once.
       TableBuilder tb{nranks, {}, {}};
-      bool vec = ws_aligned;
-      std::vector<void*> wrow(nranks);
-      for (int b = b0; b < b1; ++b) {
-        for (int r = 0; r < nranks; ++r) wrow[r] = static_cast<char*>(workspace[r]) + (base[b] - shift) * es;
-        vec = vec && all_aligned16(wrow.data(), nranks);
-        const int rw = tb.add_row(wrow.data());
-        for (int c = 0; c < nranks; ++c)
-          tb.add_seg(rw, chunk_lo(bcount[b], nranks, c), chunk_lo(bcount[b], nranks, c + 1), c);
-      }
+      const bool vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, bucket_of.data(), offset.data(),
+                                       bcount.data(), [](int) { return true; });
       Job j{dtype, op, algo, 3, avg, vec};
       return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
-    };
-    int r2 = copy(1);
-    if (!r2) r2 = reduce();
-    if (!r2) r2 = copy(0);
-    return r2;
-  };
+    }
 
-  if (whole) return run_buckets(0, nb);
-  for (int b = 0; b < nb; ++b)
-    if ((rc = run_buckets(b, b + 1))) return rc;
-  return AR_OK;
+    // Literal: pack -> AllReduce the flat buckets -> unpack.
+    int64_t total = 0, largest = 0;
+    std::vector<int64_t> base(nb);
+    for (int b = 0; b < nb; ++b) {
+      base[b] = total;
+      total += bcount[b];
+      largest = std::max(largest, bcount[b]);
+    }
+    if (workspace_bytes < largest * es) return AR_ERR_INVALID_ARG;
+    {
+      std::vector<Range> rs;
+      for (int r = 0; r < nranks; ++r) {
+        uintptr_t p = (uintptr_t)workspace[r];
+        rs.push_back({p, p + (uintptr_t)workspace_bytes});
+      }
+      for (int r = 0; r < nranks; ++r)
+        for (int t = 0; t < ntensors; ++t) {
+          if (counts[t] == 0) continue;
+          uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+          rs.push_back({p, p + (uintptr_t)counts[t] * es});
+        }
+      if ((rc = check_ranges(rs, es))) return rc;
+    }
+    const bool whole = workspace_bytes >= total * es;
+    const bool ws_aligned = all_aligned16(workspace, nranks);
+
+    // buckets [b0, b1) at once: pack them, reduce them, unpack them
+    auto run_buckets = [&](int b0, int b1) -> int {
+      const int64_t shift = base[b0];  // packed offset of bucket b0 in the workspace
+      auto copy = [&](int to_packed) -> int {
+        TableBuilder cb{nranks, {}, {}};
+        for (int t = 0; t < ntensors; ++t) {
+          if (counts[t] == 0 || bucket_of[t] < b0 || bucket_of[t] >= b1) continue;
+          void** rp = tensor_row(t);
+          const int64_t aux = base[bucket_of[t]] - shift + offset[t];
+          const bool v = all_aligned16(rp, nranks) && ws_aligned && (aux * es) % 16 == 0;
+          const int rw = cb.add_row(rp);
+          cb.add_seg(rw, 0, counts[t], v ? 1 : 0, aux);
+        }
+        ar::CopyArgs ca;
+        for (int r = 0; r < nranks; ++r) ca.packed[r] = workspace[r];
+        ca.to_packed = to_packed;
+        ca.esize = es;
+        return cb.for_each_table([&](SegTable& t) {
+          ca.tab = t;
+          cudaError_t e = ar::launch_copy(ca, stream);
+          return e == cudaSuccess ? AR_OK : cuda_fail(e);
+        });
+      };
+      auto reduce = [&]() -> int {
+        TableBuilder tb{nranks, {}, {}};
+        bool vec = ws_aligned;
+        std::vector<void*> wrow(nranks);
+        for (int b = b0; b < b1; ++b) {
+          for (int r = 0; r < nranks; ++r) wrow[r] = static_cast<char*>(workspace[r]) + (base[b] - shift) * es;
+          vec = vec && all_aligned16(wrow.data(), nranks);
+          const int rw = tb.add_row(wrow.data());
+          for (int c = 0; c < nranks; ++c)
+            tb.add_seg(rw, chunk_lo(bcount[b], nranks, c), chunk_lo(bcount[b], nranks, c + 1), c);
+        }
+        Job j{dtype, op, algo, 3, avg, vec};
+        return tb.for_each_table([&](SegTable& t) { return run_table(j, t, stream); });
+      };
+      int r2 = copy(1);
+      if (!r2) r2 = reduce();
+      if (!r2) r2 = copy(0);
+      return r2;
+    };
+
+    if (whole) return run_buckets(0, nb);
+    for (int b = 0; b < nb; ++b)
+      if ((rc = run_buckets(b, b + 1))) return rc;
+    return AR_OK;
+  });
 }
 
 int ar_reducer_create(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype, ar_op op,
                       ar_algo algo, int64_t bucket_cap_bytes, ar_stream_t comm_stream, ar_reducer** out) {
-  if (!out) return AR_ERR_INVALID_ARG;
-  *out = nullptr;
-  int rc = check_common(nranks, 0, dtype, op, algo);
-  if (rc) return rc;
-  if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
-  if (ntensors < 1 || bucket_cap_bytes <= 0 || !grads || !counts) return AR_ERR_INVALID_ARG;
-  const int es = esize_of(dtype);
-  ar_reducer* red = new ar_reducer;
-  red->nranks = nranks;
-  red->ntensors = ntensors;
-  red->comm = (cudaStream_t)comm_stream;
-  red->bucket_of.resize(ntensors);
-  std::vector<int64_t> offset(ntensors), bcount(ntensors);
-  int32_t nb = 0;
-  if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, red->bucket_of.data(), offset.data(),
-                         bcount.data(), &nb))) {
-    reducer_free(red);
-    return rc;
-  }
-  {
-    std::vector<Range> rs;
-    for (int r = 0; r < nranks; ++r)
-      for (int t = 0; t < ntensors; ++t) {
-        if (counts[t] == 0) continue;
-        uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
-        rs.push_back({p, p + (uintptr_t)counts[t] * es});
+  return guarded([&]() -> int {
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_common(nranks, 0, dtype, op, algo);
+    if (rc) return rc;
+    if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
+    if (ntensors < 1 || bucket_cap_bytes <= 0 || !grads || !counts) return AR_ERR_INVALID_ARG;
+    const int es = esize_of(dtype);
+    ar_reducer* red = new ar_reducer;
+    red->nranks = nranks;
+    red->ntensors = ntensors;
+    red->comm = (cudaStream_t)comm_stream;
+    red->bucket_of.resize(ntensors);
+    std::vector<int64_t> offset(ntensors), bcount(ntensors);
+    int32_t nb = 0;
+    if ((rc = plan_buckets(counts, ntensors, dtype, bucket_cap_bytes, red->bucket_of.data(), offset.data(),
+                           bcount.data(), &nb))) {
+      reducer_free(red);
+      return rc;
+    }
+    {
+      std::vector<Range> rs;
+      for (int r = 0; r < nranks; ++r)
+        for (int t = 0; t < ntensors; ++t) {
+          if (counts[t] == 0) continue;
+          uintptr_t p = (uintptr_t)grads[(size_t)r * ntensors + t];
+          rs.push_back({p, p + (uintptr_t)counts[t] * es});
+        }
+      if ((rc = check_ranges(rs, es))) {
+        reducer_free(red);
+        return rc;
       }
-    if ((rc = check_ranges(rs, es))) {
-      reducer_free(red);
-      return rc;
     }
-  }
-  red->nbuckets = nb;
-  red->left.resize(nb);
-  red->ready.resize(ntensors);
-  red->tables.resize(nb);
-  red->ready_ev.assign(nb, nullptr);
-  bool vec = true;
-  for (int b = 0; b < nb && nranks > 1; ++b) {
-    TableBuilder tb{nranks, {}, {}};
-    vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, red->bucket_of.data(), offset.data(), bcount.data(),
-                          [&](int t) { return red->bucket_of[t] == b; }) && vec;
-    rc = tb.for_each_table([&](SegTable& t) {
-      red->tables[b].push_back(t);
-      return AR_OK;
-    });
-    if (rc) {
-      reducer_free(red);
-      return rc;
+    red->nbuckets = nb;
+    red->left.resize(nb);
+    red->ready.resize(ntensors);
+    red->tables.resize(nb);
+    red->ready_ev.assign(nb, nullptr);
+    bool vec = true;
+    for (int b = 0; b < nb && nranks > 1; ++b) {
+      TableBuilder tb{nranks, {}, {}};
+      vec = add_bucket_rows(tb, grads, counts, ntensors, nranks, red->bucket_of.data(), offset.data(), bcount.data(),
+                            [&](int t) { return red->bucket_of[t] == b; }) && vec;
+      rc = tb.for_each_table([&](SegTable& t) {
+        red->tables[b].push_back(t);
+        return AR_OK;
+      });
+      if (rc) {
+        reducer_free(red);
+        return rc;
+      }
+      red->ntables += (int64_t)red->tables[b].size();
     }
-    red->ntables += (int64_t)red->tables[b].size();
-  }
-  red->job = Job{dtype, op, algo, 3, op == AR_AVG, vec};
-  cudaError_t e = cudaSuccess;
-  for (int b = 0; b < nb && e == cudaSuccess; ++b) e = cudaEventCreateWithFlags(&red->ready_ev[b], cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&red->done_ev, cudaEventDisableTiming);
-  if (e != cudaSuccess) {
-    reducer_free(red);
-    return cuda_fail(e);
-  }
-  reducer_reset(red);
-  *out = red;
-  return AR_OK;
+    red->job = Job{dtype, op, algo, 3, op == AR_AVG, vec};
+    cudaError_t e = cudaSuccess;
+    for (int b = 0; b < nb && e == cudaSuccess; ++b) e = cudaEventCreateWithFlags(&red->ready_ev[b], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&red->done_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      reducer_free(red);
+      return cuda_fail(e);
+    }
+    reducer_reset(red);
+    *out = red;
+    return AR_OK;
+  });
 }
 
 int ar_reducer_mark_ready(ar_reducer* red, int tensor, ar_stream_t compute_stream) {
-  if (!red || tensor < 0 || tensor >= red->ntensors || red->ready[tensor]) return AR_ERR_INVALID_ARG;
-  red->ready[tensor] = 1;
-  const int b = red->bucket_of[tensor];
-  cudaError_t e;
-  if (--red->left[b] == 0 && (e = cudaEventRecord(red->ready_ev[b], (cudaStream_t)compute_stream)) != cudaSuccess)
-    return cuda_fail(e);
-  // start every bucket whose turn has come
-  while (red->next < red->nbuckets && red->left[red->next] == 0) {
-    const int nb = red->next++;
-    if ((e = cudaStreamWaitEvent(red->comm, red->ready_ev[nb], 0)) != cudaSuccess) return cuda_fail(e);
-    for (SegTable& t : red->tables[nb]) {
-      int rc = run_table(red->job, t, red->comm);
-      if (rc) return rc;
+  return guarded([&]() -> int {
+    if (!red || tensor < 0 || tensor >= red->ntensors || red->ready[tensor]) return AR_ERR_INVALID_ARG;
+    red->ready[tensor] = 1;
+    const int b = red->bucket_of[tensor];
+    cudaError_t e;
+    if (--red->left[b] == 0 && (e = cudaEventRecord(red->ready_ev[b], (cudaStream_t)compute_stream)) != cudaSuccess)
+      return cuda_fail(e);
+    // start every bucket whose turn has come
+    while (red->next < red->nbuckets && red->left[red->next] == 0) {
+      const int nb = red->next++;
+      if ((e = cudaStreamWaitEvent(red->comm, red->ready_ev[nb], 0)) != cudaSuccess) return cuda_fail(e);
+      for (SegTable& t : red->tables[nb]) {
+        int rc = run_table(red->job, t, red->comm);
+        if (rc) return rc;
+      }
     }
-  }
-  return AR_OK;
+    return AR_OK;
+  });
 }
 
 int ar_reducer_finish(ar_reducer* red, ar_stream_t compute_stream) {
-  if (!red) return AR_ERR_INVALID_ARG;
-  if (red->next < red->nbuckets) return AR_ERR_INVALID_ARG;  // some gradient was never marked ready
-  cudaError_t e;
-  if ((e = cudaEventRecord(red->done_ev, red->comm)) != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaStreamWaitEvent((cudaStream_t)compute_stream, red->done_ev, 0)) != cudaSuccess) return cuda_fail(e);
-  reducer_reset(red);
-  return AR_OK;
+  return guarded([&]() -> int {
+    if (!red) return AR_ERR_INVALID_ARG;
+    if (red->next < red->nbuckets) return AR_ERR_INVALID_ARG;  // some gradient was never marked ready
+    cudaError_t e;
+    if ((e = cudaEventRecord(red->done_ev, red->comm)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent((cudaStream_t)compute_stream, red->done_ev, 0)) != cudaSuccess) return cuda_fail(e);
+    reducer_reset(red);
+    return AR_OK;
+  });
 }
 
 int ar_reducer_destroy(ar_reducer* red) {
-  if (!red) return AR_ERR_INVALID_ARG;
-  reducer_free(red);
-  return AR_OK;
+  return guarded([&]() -> int {
+    if (!red) return AR_ERR_INVALID_ARG;
+    reducer_free(red);
+    return AR_OK;
+  });
 }
 
 int ar_reducer_buckets(const ar_reducer* red) { return red ? red->nbuckets : AR_ERR_INVALID_ARG; }
@@ -760,74 +795,82 @@ int ar_reducer_set_max_blocks(ar_reducer* red, int max_blocks) {
 
 int ar_plan_create(int kind, void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_op op, ar_algo algo,
                    int root, ar_plan** out) {
-  if (!out) return AR_ERR_INVALID_ARG;
-  *out = nullptr;
-  int phases = 3;
-  switch (kind) {
-    case AR_PLAN_ALLREDUCE: root = -1; break;
-    case AR_PLAN_REDUCE_SCATTER: phases = 1, root = -1; break;
-    case AR_PLAN_ALL_GATHER: phases = 2, root = -1, op = AR_SUM; break;
-    case AR_PLAN_REDUCE:
-      if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
-      if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
-      break;
-    default: return AR_ERR_INVALID_ARG;
-  }
-  TableBuilder tb{nranks, {}, {}};
-  Job j{};
-  bool empty = false;
-  int rc = build_collective(bufs, nranks, count, dtype, op, algo, phases, root, tb, j, &empty);
-  if (rc) return rc;
-  ar_plan* plan = new ar_plan;
-  plan->job = j;
-  if (!empty) {
-    rc = tb.for_each_table([&](SegTable& t) {
-      plan->tables.push_back(t);
-      return AR_OK;
-    });
-    if (rc) {
-      delete plan;
-      return rc;
+  return guarded([&]() -> int {
+    if (!out) return AR_ERR_INVALID_ARG;
+    *out = nullptr;
+    int phases = 3;
+    switch (kind) {
+      case AR_PLAN_ALLREDUCE: root = -1; break;
+      case AR_PLAN_REDUCE_SCATTER: phases = 1, root = -1; break;
+      case AR_PLAN_ALL_GATHER: phases = 2, root = -1, op = AR_SUM; break;
+      case AR_PLAN_REDUCE:
+        if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
+        if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+        break;
+      default: return AR_ERR_INVALID_ARG;
     }
-  }
-  *out = plan;
-  return AR_OK;
+    TableBuilder tb{nranks, {}, {}};
+    Job j{};
+    bool empty = false;
+    int rc = build_collective(bufs, nranks, count, dtype, op, algo, phases, root, tb, j, &empty);
+    if (rc) return rc;
+    ar_plan* plan = new ar_plan;
+    plan->job = j;
+    if (!empty) {
+      rc = tb.for_each_table([&](SegTable& t) {
+        plan->tables.push_back(t);
+        return AR_OK;
+      });
+      if (rc) {
+        delete plan;
+        return rc;
+      }
+    }
+    *out = plan;
+    return AR_OK;
+  });
 }
 
 int ar_plan_run(const ar_plan* plan, ar_stream_t stream) {
-  if (!plan) return AR_ERR_INVALID_ARG;
-  for (const SegTable& t : plan->tables) {
-    SegTable copy = t;  // the launchers fill in the tile layout
-    int rc = run_table(plan->job, copy, (cudaStream_t)stream);
-    if (rc) return rc;
-  }
-  return AR_OK;
+  return guarded([&]() -> int {
+    if (!plan) return AR_ERR_INVALID_ARG;
+    for (const SegTable& t : plan->tables) {
+      SegTable copy = t;  // the launchers fill in the tile layout
+      int rc = run_table(plan->job, copy, (cudaStream_t)stream);
+      if (rc) return rc;
+    }
+    return AR_OK;
+  });
 }
 
 int ar_plan_destroy(ar_plan* plan) {
-  if (!plan) return AR_ERR_INVALID_ARG;
-  delete plan;
-  return AR_OK;
+  return guarded([&]() -> int {
+    if (!plan) return AR_ERR_INVALID_ARG;
+    delete plan;
+    return AR_OK;
+  });
 }
 
 int ar_device_status(ar_stream_t stream, int* status) {
-  if (!status) return AR_ERR_INVALID_ARG;
-  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e);
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
-  *status = AR_OK;
-  ar::SyncBlock* sb = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_sync_mu);
-    if (dev >= 0 && dev < 256) sb = g_sync[dev];
-  }
-  if (!sb) return AR_OK;
-  int v = 0;
-  if ((e = cudaMemcpy(&v, &sb->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaMemset(&sb->status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
-  *status = v;
-  return AR_OK;
+  return guarded([&]() -> int {
+    if (!status) return AR_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    *status = AR_OK;
+    ar::SyncBlock* sb = nullptr;
+    {
+      std::lock_guard<std::mutex> lk(g_sync_mu);
+      if (dev >= 0 && dev < 256) sb = g_sync[dev];
+    }
+    if (!sb) return AR_OK;
+    int v = 0;
+    if ((e = cudaMemcpy(&v, &sb->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemset(&sb->status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    *status = v;
+    return AR_OK;
+  });
 }
 
 int ar_set_barrier_timeout_ns(int64_t ns) {
@@ -850,6 +893,7 @@ const char* ar_strerror(int status) {
     case AR_ERR_CUDA: return "AR_ERR_CUDA: a CUDA call failed";
     case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a step-wise barrier wait ran out";
     case AR_ERR_NO_DEVICE: return "AR_ERR_NO_DEVICE: no usable CUDA device";
+    case AR_ERR_HOST: return "AR_ERR_HOST: host-side failure (out of host memory)";
     case AR_ERR_TOO_LARGE: return "AR_ERR_TOO_LARGE: descriptor tables too large";
     default: return "unknown ar_status";
   }

@@ -107,7 +107,8 @@ typedef enum {
   AR_ERR_CUDA = -3,        /* a CUDA call failed; ar_last_cuda_error() holds the cause */
   AR_ERR_TIMEOUT = -4,     /* asynchronous: a step-wise grid barrier gave up (see ar_device_status) */
   AR_ERR_NO_DEVICE = -5,   /* no usable CUDA device */
-  AR_ERR_TOO_LARGE = -6    /* the call needs more descriptor space than one launch holds */
+  AR_ERR_TOO_LARGE = -6,   /* the call needs more descriptor space than one launch holds */
+  AR_ERR_HOST = -7         /* host-side failure (out of host memory) */
 } ar_status;
 
 /*
