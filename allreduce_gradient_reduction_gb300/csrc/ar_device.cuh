@@ -63,7 +63,14 @@ __device__ __forceinline__ uint32_t step_word(uint32_t a, uint32_t b) {
       return bf16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (bf16_half_max(a >> 16, b >> 16) << 16);
     }
   } else {
-    if constexpr (OP == SUM) return a + b;  // two's-complement wrap-around
+    if constexpr (OP == SUM) {
+      // two's-complement wrap-around, as one opaque instruction: the
+      // compiler must not reassociate a long fold of them (that would keep
+      // every loaded value live at once and spill)
+      uint32_t r;
+      asm("add.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+      return r;
+    }
     else return (uint32_t)max((int32_t)a, (int32_t)b);
   }
 }
@@ -213,14 +220,42 @@ __host__ __device__ constexpr int inorder_root(int lo, int hi) {
   return lo == hi ? lo : (hi & ~((1 << highest_bit((unsigned)(lo ^ hi))) - 1));
 }
 
+// The fold over positions 1..n, without recursion (a device stack whose
+// depth the compiler cannot bound could overflow the per-thread stack): an
+// explicit frame stack of at most log2(n) + 2 entries emulates it.
 template <int DT, int OP>
-__device__ uint32_t fold_dbtree_scalar(const void* const* P, int n, int shift, int64_t e, int lo, int hi) {
+__device__ uint32_t fold_dbtree_scalar(const void* const* P, int n, int shift, int64_t e) {
   constexpr int ES = ElemSize<DT>::value;
-  const int root = inorder_root(lo, hi);
-  uint32_t acc = ld_elem<ES>(P[(root - 1 + shift) % n], e);
-  if (lo < root) acc = step_word<DT, OP>(fold_dbtree_scalar<DT, OP>(P, n, shift, e, lo, root - 1), acc);
-  if (root < hi) acc = step_word<DT, OP>(acc, fold_dbtree_scalar<DT, OP>(P, n, shift, e, root + 1, hi));
-  return acc;
+  struct Frame {
+    int lo, hi, r, stage;  // stage 0: new, 1: left subtree folded, 2: right subtree folded
+    uint32_t acc;
+  };
+  Frame f[10];  // n <= 64: ranges at least halve on each push
+  int sp = 0;
+  f[0] = {1, n, inorder_root(1, n), 0, 0u};
+  uint32_t ret = 0u;  // value of the subtree that finished last
+  for (;;) {
+    Frame& t = f[sp];
+    const uint32_t own = t.stage == 2 ? 0u : ld_elem<ES>(P[(t.r - 1 + shift) % n], e);
+    if (t.stage == 0 && t.lo < t.r) {
+      t.stage = 1;
+      f[sp + 1] = {t.lo, t.r - 1, inorder_root(t.lo, t.r - 1), 0, 0u};
+      ++sp;
+      continue;
+    }
+    if (t.stage == 0) t.acc = own;
+    else if (t.stage == 1) t.acc = step_word<DT, OP>(ret, own);
+    else t.acc = step_word<DT, OP>(t.acc, ret);
+    if (t.stage != 2 && t.r < t.hi) {
+      t.stage = 2;
+      f[sp + 1] = {t.r + 1, t.hi, inorder_root(t.r + 1, t.hi), 0, 0u};
+      ++sp;
+      continue;
+    }
+    ret = t.acc;
+    if (sp == 0) return ret;
+    --sp;
+  }
 }
 
 // One element in the order of `order` (chunk c selects the ring rotation,
@@ -229,7 +264,7 @@ template <int DT, int OP, int ORDER>
 __device__ __forceinline__ uint32_t fold_scalar(const void* const* P, int n, int c, int64_t e) {
   if constexpr (ORDER == RING) return fold_ring_scalar<DT, OP>(P, n, c, e);
   else if constexpr (ORDER == TREE) return fold_tree_scalar<DT, OP>(P, n, e);
-  else return fold_dbtree_scalar<DT, OP>(P, n, c, e, 1, n);
+  else return fold_dbtree_scalar<DT, OP>(P, n, c, e);
 }
 
 }  // namespace ar

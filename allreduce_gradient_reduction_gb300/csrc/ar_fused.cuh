@@ -68,6 +68,47 @@ __device__ __forceinline__ uint4 inorder_fold_regs(const uint4 (&x)[NR]) {
   return acc;
 }
 
+// Double binary tree over many ranks.  The in-order fold of positions LO..HI
+// visits them in increasing order (left subtree, own, right subtree), so the
+// rank vectors can be streamed eight positions at a time: the loads of a
+// group go out together when its first position is needed, and only that
+// group and the pending partial sums live in registers.  Position p holds
+// rank p - 1 + rank_shift (mod NR).
+template <int NR>
+struct DbtStream {
+  const void* const* P;
+  int64_t base;
+  int rank_shift;
+  bool ok;
+  uint4 g[8];
+  template <int POS>
+  __device__ __forceinline__ uint4 at() {
+    if constexpr ((POS - 1) % 8 == 0) {
+      // keep each group's loads here: hoisting all of them (integer adds may
+      // be reassociated freely) would need NR vectors of registers at once
+      asm volatile("" ::: "memory");
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (ok) g[q] = ld_stream(static_cast<const char*>(P[rot(POS - 1 + q + rank_shift, NR)]) + base);
+    }
+    return g[(POS - 1) % 8];
+  }
+};
+
+template <int DT, int OP, int NR, int LO, int HI>
+__device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
+  constexpr int R = inorder_root(LO, HI);
+  uint4 acc;
+  if constexpr (LO < R) {
+    const uint4 left = inorder_fold_stream<DT, OP, NR, LO, R - 1>(st);
+    acc = step_vec<DT, OP>(left, st.template at<R>());
+  } else {
+    acc = st.template at<R>();
+  }
+  if constexpr (R < HI) acc = step_vec<DT, OP>(acc, inorder_fold_stream<DT, OP, NR, R + 1, HI>(st));
+  return acc;
+}
+
 template <class ARGS, int DT, int OP, int ORDER, int NR>
 __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
@@ -135,18 +176,24 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
     } else if constexpr (ORDER == DBTREE) {
       // chunk 0: tree A over the first half of the elements, chunk 1: tree B.
       // Tree B is tree A over the ranks shifted by one, so the shift goes
-      // into which buffer lands in x[p], and one tree is compiled.
-      const int shift = c == 0 ? 0 : 1;
-      uint4 x[U][NR];
+      // into which buffer lands at each position, and one tree is compiled.
+      const int rank_shift = c == 0 ? 0 : 1;
+      if constexpr (NR <= 8) {
+        uint4 x[U][NR];
 #pragma unroll
-      for (int p = 0; p < NR; ++p) {
-        const char* src = static_cast<const char*>(P[rot(p + shift, NR)]) + base;
+        for (int p = 0; p < NR; ++p) {
+          const char* src = static_cast<const char*>(P[rot(p + rank_shift, NR)]) + base;
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+          for (int u = 0; u < U; ++u)
+            if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
+      } else {
+        static_assert(U == 1, "one vector position per thread for wide trees");
+        DbtStream<NR> st{P, base, rank_shift, ok[0], {}};
+        acc[0] = inorder_fold_stream<DT, OP, NR, 1, NR>(st);
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
     } else if constexpr (NR <= 8) {
       uint4 x[U][NR];
 #pragma unroll
@@ -314,6 +361,8 @@ cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream
         case 4: return launch_fused_vec<DT, OP, DBTREE, 4>(a, stream);
         case 8: return launch_fused_vec<DT, OP, DBTREE, 8>(a, stream);
         case 16: return launch_fused_vec<DT, OP, DBTREE, 16>(a, stream);
+        case 32: return launch_fused_vec<DT, OP, DBTREE, 32>(a, stream);
+        case 64: return launch_fused_vec<DT, OP, DBTREE, 64>(a, stream);
         default: break;
       }
     return launch_fused_scalar<DT, OP, DBTREE>(a, stream);
