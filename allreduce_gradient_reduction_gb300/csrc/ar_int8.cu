@@ -15,15 +15,18 @@
 //
 // One warp owns one 128-element block: 4 consecutive floats per lane (one
 // 16-byte access per rank and array), warp shuffles give the block maxima.
-// Ranks are taken one at a time; the latency of their loads is hidden by the
-// 48 warps an SM keeps resident (40 registers a thread).
+// Ranks are taken one at a time.  Their loads run ahead of the arithmetic:
+// each lane copies its 16 bytes of x and e for the next ranks straight into
+// its own shared-memory slots with cp.async, so the copies in flight hold no
+// registers and 48 warps per SM still fit (40 registers a thread).
 #include "ar_fused.cuh"
 
 namespace ar {
 
 constexpr int kQ8 = 128;
 constexpr int kQ8Block = 256;  // threads per block: 8 warps, 8 quantisation blocks
-constexpr int kQ8MinBlocks = 6; // resident blocks per SM: 48 warps hide the loads of a rank at a time
+constexpr int kQ8MinBlocks = 6; // resident blocks per SM: 48 warps
+constexpr int kQ8Stages = 3;    // ranks whose x and e a warp has in flight or waiting in shared memory
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -59,6 +62,18 @@ __device__ __forceinline__ float q8_code_recip(float y, float s, float r) {
 
 __device__ __forceinline__ int chunk_of(int64_t e, int64_t count, int n) {
   return (int)(((e + 1) * n - 1) / count);  // the chunk [floor(cD/N), floor((c+1)D/N)) holding e
+}
+
+// 16-byte global -> shared copy that bypasses L1; both addresses 16-byte aligned
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most K of this thread's committed groups are still in flight
+template <int K>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
 }
 
 struct Lane4 {
@@ -110,6 +125,7 @@ __device__ __forceinline__ Lane4 encode(const Lane4& x, const Lane4& e, float* e
 
 __global__ void __launch_bounds__(kQ8Block, kQ8MinBlocks) int8_ef_kernel(const __grid_constant__ Int8Args a) {
   __shared__ float s_scale[kQ8Block / 32][kMaxRanks];
+  __shared__ float4 s_stage[kQ8Block / 32][kQ8Stages][2][32];  // [warp][slot][x or e][lane]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t count = a.count;
   const int n = a.nranks;
@@ -122,8 +138,41 @@ __global__ void __launch_bounds__(kQ8Block, kQ8MinBlocks) int8_ef_kernel(const _
   const int c_first = chunk_of(b0, count, n), c_last = chunk_of(blast, count, n);
   float acc[4];
 
-  if (c_first == c_last) {
-    // the whole block is in chunk c: fold the ranks in ring order as they come
+  if (c_first == c_last && vec && b0 + kQ8 <= count) {
+    // a whole aligned block in chunk c: fold the ranks in ring order as they
+    // come, the copies of the next kQ8Stages - 1 ranks in flight.  Each lane
+    // reads back only the 16 bytes it copied itself, so waiting on its own
+    // groups is enough; the slot refilled in step p was read in step p - 1,
+    // whose results were stored before this copy is issued.
+    const int c = c_first;
+    float4 (*st)[2][32] = s_stage[warp];
+#pragma unroll
+    for (int j = 0; j < kQ8Stages - 1; ++j) {
+      if (j < n) {
+        const int r = rot(c + 1 + j, n);
+        cp_async16(&st[j][0][lane], a.x[r] + e0);
+        cp_async16(&st[j][1][lane], a.e[r] + e0);
+      }
+      cp_async_commit();
+    }
+    for (int p = 0; p < n; ++p) {
+      const int j = p + kQ8Stages - 1;
+      if (j < n) {
+        const int r = rot(c + 1 + j, n);
+        cp_async16(&st[j % kQ8Stages][0][lane], a.x[r] + e0);
+        cp_async16(&st[j % kQ8Stages][1][lane], a.e[r] + e0);
+      }
+      cp_async_commit();  // possibly empty, so that group p is always kQ8Stages - 1 behind
+      cp_async_wait<kQ8Stages - 1>();
+      const int r = rot(c + 1 + p, n);
+      const float4 xv = st[p % kQ8Stages][0][lane], ev = st[p % kQ8Stages][1][lane];
+      const Lane4 yh = encode(Lane4{{xv.x, xv.y, xv.z, xv.w}}, Lane4{{ev.x, ev.y, ev.z, ev.w}}, a.e[r], e0, count,
+                              true);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = p == 0 ? yh.v[k] : __fadd_rn(acc[k], yh.v[k]);
+    }
+  } else if (c_first == c_last) {
+    // the same from registers: unaligned rows and the ragged last block
     const int c = c_first;
     for (int p = 0; p < n; ++p) {
       const int r = rot(c + 1 + p, n);

@@ -541,7 +541,7 @@ def test_dbtree_only_for_allreduce(ar):
 # 8-bit quantised AllReduce with error feedback
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 16, 64])
 def test_int8_ef_matches_oracle(ar, n):
     for count in (1, 127, 128 * n, 128 * 3 * n + 77, 70_001):
         for op in ("sum", "avg"):
