@@ -30,12 +30,17 @@ constexpr int kFusedBlock = 256;
 // GB300 (8 x 128 MiB bf16 ring): U=1 at 4 blocks/SM 309.8 us, U=2 310.7 us,
 // U=3 at 2 blocks/SM 311.3 us, U=4 at 1 block/SM 343.5 us -- occupancy
 // matters more than loads per thread once the grid is one tile per block.
-// (The wide trees, N >= 16, get 128 registers: 2 blocks per SM.)
 // Resident blocks per SM the register budget is cut for: 4 (64 registers) for
-// up to 8 ranks, 2 beyond; the in-order double-binary-tree fold of 8 ranks
-// keeps more partial sums live and gets 3 (80 registers), without spills.
-__host__ __device__ constexpr int fused_min_blocks(int order, int nr) {
-  return nr > 8 ? 2 : (order == DBTREE && nr == 8 ? 3 : 4);
+// up to 8 ranks; the in-order double-binary-tree fold of 8 ranks keeps more
+// partial sums live and gets 3 (80 registers), without spills.  Beyond 8
+// ranks every order keeps two groups of 8 rank loads in flight.  The ring
+// then gets 3 (at 2 it was 1.9% slower on 64 x 64 MiB; at 3 as fast as one
+// group at a time at 4 blocks per SM, and twice as fast for calls of
+// 4-64 KiB).  The trees, which also hold finished subtrees, and the bf16
+// maximum, which needs more temporaries, get 2 (128 registers), without
+// spills.
+__host__ __device__ constexpr int fused_min_blocks(int order, int nr, int dt, int op) {
+  return nr > 8 ? (order == RING && !(dt == BF16 && op == MAX) ? 3 : 2) : (order == DBTREE && nr == 8 ? 3 : 4);
 }
 __host__ __device__ constexpr int fused_unroll(int order, int nr) {
   return (nr == 2) ? 2 : 1;
@@ -110,7 +115,7 @@ __device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
 }
 
 template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ ARGS a) {
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR, DT, OP)) fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int U = fused_unroll(ORDER, NR);
@@ -136,7 +141,33 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
     for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < sh.ve;
 
     uint4 acc[U];
-    if constexpr (ORDER == RING && NR > 0) {
+    if constexpr (ORDER == RING && NR > 8) {
+      // 16, 32 or 64 ranks: groups of 8 in ring order, the loads of group
+      // g + 1 in flight while group g is folded (16 vectors of registers)
+      static_assert(U == 1, "one vector position per thread for wide rings");
+      constexpr int G = 8;
+      uint4 cur[G], nxt[G];
+#pragma unroll
+      for (int q = 0; q < G; ++q)
+        if (ok[0]) cur[q] = ld_stream(static_cast<const char*>(P[rot(c + 1 + q, NR)]) + base);
+#pragma unroll
+      for (int g = 0; g < NR; g += G) {
+        // keep group g + 2's loads behind group g's fold (integer adds may
+        // be reassociated, which would let every load hoist)
+        asm volatile("" ::: "memory");
+        if (g + G < NR) {
+#pragma unroll
+          for (int q = 0; q < G; ++q)
+            if (ok[0]) nxt[q] = ld_stream(static_cast<const char*>(P[rot(c + 1 + g + G + q, NR)]) + base);
+        }
+#pragma unroll
+        for (int q = 0; q < G; ++q) acc[0] = (g + q == 0) ? cur[q] : step_vec<DT, OP>(acc[0], cur[q]);
+        if (g + G < NR) {
+#pragma unroll
+          for (int q = 0; q < G; ++q) cur[q] = nxt[q];
+        }
+      }
+    } else if constexpr (ORDER == RING && NR > 0) {
       const char* src[NR];
 #pragma unroll
       for (int p = 0; p < NR; ++p) src[p] = static_cast<const char*>(P[rot(c + 1 + p, NR)]) + base;
@@ -208,20 +239,31 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
     } else {
       // N = 16, 32, 64: aligned subtrees of 8 ranks, each folded as it
       // arrives and merged with its finished siblings (a binary counter over
-      // the subtree index), which is the same balanced tree.  One group at a
-      // time: 8 loads in flight per thread fit the register budget, N do not.
+      // the subtree index), which is the same balanced tree.  The loads of
+      // subtree g + 1 are in flight while subtree g is folded.
       static_assert(U == 1, "one vector position per thread for wide trees");
-      uint4 stk[4];
+      constexpr int G = 8;
+      uint4 cur[G], nxt[G], stk[4];
       int top = 0;
-#pragma unroll 1
-      for (int g = 0; g < NR / 8; ++g) {
-        uint4 x[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (ok[0]) x[q] = ld_stream(static_cast<const char*>(P[g * 8 + q]) + base);
-        uint4 v = tree_fold_regs<DT, OP, 8>(x);
+      for (int q = 0; q < G; ++q)
+        if (ok[0]) cur[q] = ld_stream(static_cast<const char*>(P[q]) + base);
+#pragma unroll
+      for (int g = 0; g < NR / G; ++g) {
+        asm volatile("" ::: "memory");  // subtree g + 2's loads stay behind this fold
+        if (g + 1 < NR / G) {
+#pragma unroll
+          for (int q = 0; q < G; ++q)
+            if (ok[0]) nxt[q] = ld_stream(static_cast<const char*>(P[(g + 1) * G + q]) + base);
+        }
+        uint4 v = tree_fold_regs<DT, OP, G>(cur);
+#pragma unroll
         for (int k = g; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[--top], v);
         stk[top++] = v;
+        if (g + 1 < NR / G) {
+#pragma unroll
+          for (int q = 0; q < G; ++q) cur[q] = nxt[q];
+        }
       }
       acc[0] = stk[0];
     }
@@ -255,7 +297,9 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
     // elements of the segment outside its full vectors
     if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
       const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x, shift);
-      uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
+      // beyond 8 ranks the fold runs over the table's runtime rank count: a
+      // loop unrolled over 32 or 64 ranks would hoist every load and spill
+      uint32_t r = fold_scalar<DT, OP, ORDER>(P, NR > 8 ? T.nranks : n, c, e);
       if (a.avg) r = div_word<DT>(r, a.fn);
       if (a.owner_only || a.to_root) {
         st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
@@ -373,6 +417,9 @@ cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream
       case 2: return launch_fused_vec<DT, OP, RING, 2>(a, stream);
       case 4: return launch_fused_vec<DT, OP, RING, 4>(a, stream);
       case 8: return launch_fused_vec<DT, OP, RING, 8>(a, stream);
+      case 16: return launch_fused_vec<DT, OP, RING, 16>(a, stream);
+      case 32: return launch_fused_vec<DT, OP, RING, 32>(a, stream);
+      case 64: return launch_fused_vec<DT, OP, RING, 64>(a, stream);
       default: return launch_fused_vec<DT, OP, RING, 0>(a, stream);
     }
   }

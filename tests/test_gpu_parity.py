@@ -105,7 +105,7 @@ def counts_for(n):
 
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
-@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 64])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 32, 64])
 def test_allreduce_matches_oracle(ar, algo, dtype, n):
     if algo.startswith("tree") and n & (n - 1):
         pytest.skip("tree order needs a power of two")
@@ -191,6 +191,33 @@ def test_unaligned_buffers(ar, algo, dtype):
         assert_same(got, want, dtype, f"{algo} shifts {shifts}")
         for r in range(n):
             assert np.array_equal(from_dev([big[r][:shifts[r]]], dtype)[0], x[r, :shifts[r]])
+
+
+@pytest.mark.parametrize("n", [16, 32, 64])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+def test_unaligned_wide_rings(ar, n, dtype):
+    """The 16-, 32- and 64-rank ring kernels with every buffer at the same
+    offset from 16 bytes (vectors cut at that offset, scalar head and tail),
+    and the ReduceScatter form that stores to the chunk owner only."""
+    count = 2048 * n + 4099
+    x = inputs(n, count, dtype, "values", seed=31 + n)
+    want, _ = oracle.allreduce(x, algo="ring", op="sum", dtype=dtype)
+    want_rs, _ = oracle.reduce_scatter(x, algo="ring", op="sum", dtype=dtype)
+    shift = 3 if dtype == "bf16" else 1
+    for fn in ("ar_allreduce", "ar_reduce_scatter"):
+        big = [to_dev(np.concatenate([x[r][:shift], x[r]])) for r in range(n)]
+        views = [b[shift:] for b in big]
+        ar.check(getattr(ar, fn)(views, count=count, dtype=dtype, op="sum", algo="ring"), fn)
+        torch.cuda.synchronize()
+        got = from_dev(views, dtype)
+        if fn == "ar_allreduce":
+            assert_same(got, want, dtype, f"wide ring n={n}")
+        else:
+            for r in range(n):
+                lo, hi = oracle.chunk_range(count, n, r)
+                assert_same(got[r, lo:hi], want_rs[r, lo:hi], dtype, f"wide ring RS n={n} rank {r}")
+        for r in range(n):
+            assert np.array_equal(from_dev([big[r][:shift]], dtype)[0], x[r, :shift])
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
