@@ -59,7 +59,7 @@ struct Range {
 // inside device memory of the current device.
 int check_ranges(std::vector<Range>& rs, int esize) {
   for (const Range& r : rs) {
-    if (r.lo == 0) return AR_ERR_INVALID_ARG;
+    if (r.lo == 0 || r.hi < r.lo) return AR_ERR_INVALID_ARG;  // NULL, or an end past the address space
     if (r.lo % (uintptr_t)esize) return AR_ERR_INVALID_ARG;
   }
   std::sort(rs.begin(), rs.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
@@ -91,7 +91,7 @@ int check_ranges(std::vector<Range>& rs, int esize) {
 }
 
 int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
-  if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0) return AR_ERR_INVALID_ARG;
+  if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0 || count > AR_MAX_COUNT) return AR_ERR_INVALID_ARG;
   if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
   if (algo < AR_RING || algo > AR_DBTREE) return AR_ERR_INVALID_ARG;
   if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
@@ -372,9 +372,10 @@ int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, in
                  int64_t* bcount, int32_t* nb) {
   const int es = esize_of(dtype);
   int b = -1;
-  int64_t fill = 0;
+  int64_t fill = 0, total = 0;
   for (int t = ntensors - 1; t >= 0; --t) {
-    if (counts[t] < 0) return AR_ERR_INVALID_ARG;
+    if (counts[t] < 0 || counts[t] > AR_MAX_COUNT - total) return AR_ERR_INVALID_ARG;
+    total += counts[t];
     const int64_t bytes = counts[t] * es;
     if (b < 0 || (fill > 0 && fill + bytes > cap)) {
       ++b;

@@ -70,7 +70,8 @@ PointerGetAttributeFn attr_fn() {
 // device memory of the current device.  Sorts g_ranges[0..n) in place.
 int check_ranges(int n, int esize, int dev) {
   for (int i = 0; i < n; ++i)
-    if (g_ranges[i].lo == 0 || g_ranges[i].lo % (uintptr_t)esize) return AR_ERR_INVALID_ARG;
+    if (g_ranges[i].lo == 0 || g_ranges[i].hi < g_ranges[i].lo || g_ranges[i].lo % (uintptr_t)esize)
+      return AR_ERR_INVALID_ARG;
   std::sort(g_ranges, g_ranges + n, [](const Range& a, const Range& b) { return a.lo < b.lo; });
   for (int i = 1; i < n; ++i)
     if (g_ranges[i].lo < g_ranges[i - 1].hi || g_ranges[i].lo == g_ranges[i - 1].lo) return AR_ERR_INVALID_ARG;

@@ -31,7 +31,9 @@
  *     cut at that offset; buffers at different offsets modulo 16 take a
  *     slower one-element-per-thread path.  (For a bucketed call this holds
  *     per tensor: each tensor's N buffers.)
- *   - 1 <= nranks <= AR_MAX_RANKS; count >= 0; count == 0 and nranks == 1 do
+ *   - 1 <= nranks <= AR_MAX_RANKS; 0 <= count <= AR_MAX_COUNT (else
+ *     AR_ERR_INVALID_ARG, as for a buffer whose end would pass the top of the
+ *     address space); count == 0 and nranks == 1 do
  *     nothing (a single rank already holds the reduction; AVG divides by 1).
  *     With count == 0 the buffer pointers are not examined (NULL is fine,
  *     as an empty tensor's is); the host array itself must not be NULL.
@@ -87,6 +89,11 @@ extern "C" {
 typedef struct CUstream_st* ar_stream_t;
 
 #define AR_MAX_RANKS 64
+/* Largest element count a call accepts (per buffer; for bucketed calls also
+ * per tensor and for the sum over tensors).  2^56 elements is far beyond any
+ * device allocation; the limit keeps every byte offset and buffer end
+ * representable, so the range checks cannot be defeated by wrap-around. */
+#define AR_MAX_COUNT (1LL << 56)
 #define AR_DEFAULT_BUCKET_CAP_BYTES (25LL << 20) /* DDP's 25 MB bucket [tutorial §4.1] */
 
 typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2 } ar_dtype;
@@ -205,7 +212,8 @@ int ar_allreduce_int8_ef(void* const* grads, void* const* residuals, int nranks,
  *   offset_in_bucket  [ntensors] out: element offset of each tensor in its bucket
  *   bucket_count      [ntensors] out (capacity ntensors): elements per bucket
  *   nbuckets          out: number of buckets
- * Host-only; errors: AR_ERR_INVALID_ARG.
+ * Host-only; errors: AR_ERR_INVALID_ARG (also for a negative count, or
+ * counts whose sum exceeds AR_MAX_COUNT).
  */
 int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t cap_bytes, int32_t* bucket_of_tensor,
                    int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets);

@@ -102,6 +102,28 @@ def test_argument_checks_without_device(ar):
     assert rc == ar.AR_ERR_INVALID_ARG
 
 
+def test_counts_that_overflow_byte_ranges_are_refused(ar):
+    """Element counts whose byte size would wrap past 2^64 (or past the
+    documented ceiling, 2^56 elements) and buffers whose end passes the top
+    of the address space are argument errors, found before any device work:
+    a wrapped end could otherwise pass the range checks."""
+    limit = 1 << 56
+    ptrs = [1 << 20, 1 << 40]
+    assert ar.ar_allreduce(ptrs, count=limit + 1, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce(ptrs, count=1 << 62, stream=0) == ar.AR_ERR_INVALID_ARG  # 4 * 2^62 = 2^64
+    assert ar.ar_reduce_scatter(ptrs, count=(1 << 63) - 1, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_all_gather(ptrs, count=1 << 62, dtype="bf16", stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce_int8_ef(ptrs, [1 << 44, 1 << 45], count=1 << 62, stream=0) == ar.AR_ERR_INVALID_ARG
+    top = (1 << 64) - 64  # 16 f32 from here would end past 2^64
+    assert ar.ar_allreduce([top, 1 << 20], count=32, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_bucket_plan([1 << 62], "f32", 25 << 20)[0] == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_bucket_plan([1 << 55] * 3, "f32", 25 << 20)[0] == ar.AR_ERR_INVALID_ARG  # sum > 2^56
+    rc, bo, off, bc = ar.ar_bucket_plan([1 << 55] * 2, "f32", 25 << 20)  # sum = 2^56: accepted
+    assert rc == ar.AR_OK and list(bc) == [1 << 55, 1 << 55]
+    header = open(os.path.join(ROOT, "include", "ar.h")).read()
+    assert "#define AR_MAX_COUNT (1LL << 56)" in header
+
+
 def test_no_device_is_reported_not_faked(ar):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
