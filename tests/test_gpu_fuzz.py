@@ -124,7 +124,7 @@ def test_random_collectives(ar, block):
 def test_random_bucketed(ar, block):
     rng = np.random.default_rng(8000 + block)
     for case in range(12):
-        n = int(rng.choice([2, 3, 4, 8]))
+        n = int(rng.choice([2, 3, 4, 8, 16, 32, 64]))  # 16-64: several launch tables per bucketed call
         t = int(rng.integers(1, 12))
         counts = [int(rng.choice([0, 1, 7, int(rng.integers(1, 5000))])) for _ in range(t)]
         if sum(counts) == 0:
