@@ -25,6 +25,7 @@ STATUS = {0: "AR_OK", -1: "AR_ERR_INVALID_ARG", -2: "AR_ERR_UNSUPPORTED", -3: "A
           -4: "AR_ERR_TIMEOUT", -5: "AR_ERR_NO_DEVICE", -6: "AR_ERR_TOO_LARGE", -7: "AR_ERR_HOST"}
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4
 MAX_RANKS = 64
+MAX_COUNT = 1 << 56  # AR_MAX_COUNT
 DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
 EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_allreduce_int8_ef",

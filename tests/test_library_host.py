@@ -108,6 +108,7 @@ def test_counts_that_overflow_byte_ranges_are_refused(ar):
     of the address space are argument errors, found before any device work:
     a wrapped end could otherwise pass the range checks."""
     limit = 1 << 56
+    assert ar.MAX_COUNT == limit
     ptrs = [1 << 20, 1 << 40]
     assert ar.ar_allreduce(ptrs, count=limit + 1, stream=0) == ar.AR_ERR_INVALID_ARG
     assert ar.ar_allreduce(ptrs, count=1 << 62, stream=0) == ar.AR_ERR_INVALID_ARG  # 4 * 2^62 = 2^64
