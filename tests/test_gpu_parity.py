@@ -464,9 +464,10 @@ def test_bf16_step_exhaustive(ar):
 # Failure detection without a fault: a barrier nobody completes times out
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("count", [1 << 16, 1 << 22])  # grids of at most 128 blocks (one counter) and more (groups)
 @pytest.mark.parametrize("algo", ["ring_stepwise", "tree_stepwise"])
-def test_barrier_timeout_is_reported(ar, algo):
-    n, count = 8, 1 << 16
+def test_barrier_timeout_is_reported(ar, algo, count):
+    n = 8
     x = W.normal_inputs(n, count, 1.0, 12)
     ar.ar_set_barrier_timeout_ns(50_000_000)  # 50 ms
     try:
