@@ -29,6 +29,7 @@ MAX_COUNT = 1 << 56  # AR_MAX_COUNT
 DEFAULT_BUCKET_CAP_BYTES = 25 << 20
 
 EXPORTS = ("ar_allreduce", "ar_reduce_scatter", "ar_all_gather", "ar_reduce", "ar_broadcast", "ar_allreduce_int8_ef",
+           "ar_allreduce_host",
            "ar_bucket_plan",
            "ar_bucketed_allreduce",
            "ar_bucketed_allreduce_noalloc", "ar_chunk_range", "ar_device_status", "ar_set_barrier_timeout_ns", "ar_debug_skip_barrier",
@@ -57,6 +58,7 @@ def _load():
     L.ar_reduce.argtypes = [pp, cint, i64, cint, cint, cint, cint, vp]
     L.ar_broadcast.argtypes = [pp, cint, i64, cint, cint, vp]
     L.ar_allreduce_int8_ef.argtypes = [pp, pp, cint, i64, cint, vp]
+    L.ar_allreduce_host.argtypes = [pp, pp, cint, i64, cint, cint, cint, i64, vp]
     L.ar_bucket_plan.argtypes = [ctypes.POINTER(i64), cint, cint, i64, ctypes.POINTER(i32), ctypes.POINTER(i64),
                                  ctypes.POINTER(i64), ctypes.POINTER(i32)]
     L.ar_bucketed_allreduce.argtypes = [pp, ctypes.POINTER(i64), cint, cint, cint, cint, cint, i64, pp, i64, vp]
@@ -155,6 +157,17 @@ def ar_broadcast(bufs, nranks=None, count=None, dtype="f32", root=0, stream=None
     n = len(bufs) if nranks is None else int(nranks)
     return lib.ar_broadcast(_ptr_array(bufs), n, _count(bufs, count), _enum(DTYPE, dtype), int(root),
                             _stream(stream))
+
+
+def ar_allreduce_host(host_bufs, dev_bufs=None, nranks=None, count=None, dtype="f32", op="sum", algo="ring",
+                      piece_elems=0, stream=None) -> int:
+    """host_bufs: CPU tensors or host addresses.  dev_bufs None: zero-copy on
+    page-locked host buffers; else device working buffers (staged pieces)."""
+    n = len(host_bufs) if nranks is None else int(nranks)
+    return lib.ar_allreduce_host(_ptr_array(host_bufs), None if dev_bufs is None else _ptr_array(dev_bufs), n,
+                                 _count(host_bufs, count),
+                                 _enum(DTYPE, dtype), _enum(OP, op), _enum(ALGO, algo), int(piece_elems),
+                                 _stream(stream))
 
 
 def ar_allreduce_int8_ef(grads, residuals, nranks=None, count=None, op="sum", stream=None) -> int:

@@ -55,9 +55,8 @@ struct Range {
   uintptr_t lo, hi;
 };
 
-// Every range must be non-null, element aligned, pairwise disjoint, and lie
-// inside device memory of the current device.
-int check_ranges(std::vector<Range>& rs, int esize) {
+// Every range must be non-null, element aligned and pairwise disjoint (sorts rs).
+int check_disjoint(std::vector<Range>& rs, int esize) {
   for (const Range& r : rs) {
     if (r.lo == 0 || r.hi < r.lo) return AR_ERR_INVALID_ARG;  // NULL, or an end past the address space
     if (r.lo % (uintptr_t)esize) return AR_ERR_INVALID_ARG;
@@ -65,6 +64,13 @@ int check_ranges(std::vector<Range>& rs, int esize) {
   std::sort(rs.begin(), rs.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
   for (size_t i = 1; i < rs.size(); ++i)
     if (rs[i].lo < rs[i - 1].hi || rs[i].lo == rs[i - 1].lo) return AR_ERR_INVALID_ARG;
+  return AR_OK;
+}
+
+// ... and lie inside device memory of the current device.
+int check_ranges(std::vector<Range>& rs, int esize) {
+  int rc = check_disjoint(rs, esize);
+  if (rc) return rc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -86,6 +92,28 @@ int check_ranges(std::vector<Range>& rs, int esize) {
     alloc_lo = (uintptr_t)start;
     alloc_hi = (uintptr_t)start + size;
     if (r.lo < alloc_lo || r.hi > alloc_hi) return AR_ERR_INVALID_ARG;
+  }
+  return AR_OK;
+}
+
+// Every range must be non-null, element aligned, pairwise disjoint, and lie
+// inside page-locked host memory that kernels on the current device reach at
+// the same address (a mapped allocation under unified addressing).
+int check_mapped_host(std::vector<Range>& rs, int esize) {
+  int rc = check_disjoint(rs, esize);
+  if (rc) return rc;
+  PointerGetAttributesFn attrs = pointer_attrs_fn();
+  if (!attrs) return cuda_fail(cudaErrorNotSupported);
+  for (const Range& r : rs) {
+    unsigned int mtype = 0;
+    CUdeviceptr devptr = 0, start = 0;
+    size_t size = 0;
+    CUpointer_attribute which[4] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_POINTER,
+                                    CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+    void* out[4] = {&mtype, &devptr, &start, &size};
+    if (attrs(4, which, out, (CUdeviceptr)r.lo) != CUDA_SUCCESS) return AR_ERR_INVALID_ARG;
+    if (mtype != CU_MEMORYTYPE_HOST || devptr != (CUdeviceptr)r.lo || size == 0) return AR_ERR_INVALID_ARG;
+    if (r.lo < (uintptr_t)start || r.hi > (uintptr_t)start + size) return AR_ERR_INVALID_ARG;
   }
   return AR_OK;
 }
@@ -148,6 +176,76 @@ int sync_block(ar::SyncBlock** out) {
   }
   *out = g_sync[dev];
   return AR_OK;
+}
+
+// ---- per-device copy streams of the host-buffer AllReduce ------------------------
+
+struct HostPipe {
+  std::mutex mu;  // one call at a time enqueues on this device's streams and events
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, uploaded = nullptr, reduced = nullptr, done = nullptr;
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[256];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 256) return AR_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& p = g_pipe[dev];
+  if (!p.done) {
+    cudaStream_t st[2] = {nullptr, nullptr};
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+      for (cudaStream_t x : st)
+        if (x) cudaStreamDestroy(x);
+      return cuda_fail(e);
+    }
+    p.up = st[0], p.down = st[1];
+    p.start = ev[0], p.uploaded = ev[1], p.reduced = ev[2], p.done = ev[3];
+  }
+  *out = &p;
+  return AR_OK;
+}
+
+// First element of every piece of the host-buffer AllReduce.  An explicit
+// piece size is used as given (rounded up to 64 elements).  By default the
+// pieces hold count / 8 elements, between 1 MiB and 16 MiB per rank, and the
+// first and last three are 1/8, 1/4 and 1/2 of that: the time when only the
+// first upload or only the last download is running is what the overlap
+// cannot hide, so those pieces are small, and the rest are large, which the
+// copy engines move most efficiently.
+std::vector<int64_t> host_pieces(int64_t count, int es, int64_t piece_elems) {
+  auto round64 = [](int64_t v) { return std::max<int64_t>(64, (v + 63) / 64 * 64); };
+  std::vector<int64_t> starts;
+  if (piece_elems > 0) {
+    const int64_t p = round64(piece_elems);
+    for (int64_t a = 0; a < count; a += p) starts.push_back(a);
+    return starts;
+  }
+  const int64_t lo = ((int64_t)1 << 20) / es, hi = ((int64_t)16 << 20) / es;
+  const int64_t p = round64(std::min(hi, std::max(lo, count / 8)));
+  const int64_t ramp[3] = {round64(p / 8), round64(p / 4), round64(p / 2)};
+  const int64_t ramp_total = 2 * (ramp[0] + ramp[1] + ramp[2]);
+  int64_t a = 0;
+  if (count >= ramp_total + p) {
+    const int64_t tail = (count - ramp_total / 2) / 64 * 64;  // first of the last three pieces
+    for (int i = 0; i < 3; ++i) starts.push_back(a), a += ramp[i];
+    const int64_t mid = tail - a;
+    const int64_t nmid = (mid + p - 1) / p, step = round64((mid + nmid - 1) / nmid);
+    for (; a < tail; a += step) starts.push_back(a);
+    a = tail;
+    for (int i = 2; i >= 0; --i) starts.push_back(a), a += ramp[i];
+  } else {
+    for (; a < count; a += p) starts.push_back(a);
+  }
+  return starts;
 }
 
 // ---- one launch over a descriptor table ----------------------------------------
@@ -305,13 +403,13 @@ struct TableBuilder {
 // Checks the arguments and builds the launch of a collective.  *empty is set
 // when there is nothing to do (count 0 or one rank).
 int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, int op, int algo, int phases, int root,
-                     TableBuilder& tb, Job& j, bool* empty) {
+                     TableBuilder& tb, Job& j, bool* empty, bool bufs_checked = false) {
   *empty = false;
   int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
   if (rc) return rc;
   if ((algo == AR_NAIVE || algo == AR_DBTREE) && phases != 3) return AR_ERR_UNSUPPORTED;  // AllReduce / Reduce only
   if (algo == AR_DBTREE && root >= 0) return AR_ERR_UNSUPPORTED;
-  if ((rc = check_bufs(bufs, nranks, count, dtype))) return rc;
+  if (!bufs_checked && (rc = check_bufs(bufs, nranks, count, dtype))) return rc;
   if (count == 0 || nranks == 1) {
     *empty = true;
     return AR_OK;
@@ -504,6 +602,86 @@ int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, i
     tb.add_seg(tb.add_row(bufs), 0, count, root);
     Job j{dtype, AR_SUM, AR_RING, 2, false, same_phase16(bufs, nranks)};
     return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream); });
+  });
+}
+
+int ar_allreduce_host(void* const* host_bufs, void* const* dev_bufs, int nranks, int64_t count, ar_dtype dtype,
+                      ar_op op, ar_algo algo, int64_t piece_elems, ar_stream_t stream_) {
+  return guarded([&]() -> int {
+    int rc = check_common(nranks, count, dtype, op, algo);
+    if (rc) return rc;
+    if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+    if (!host_bufs || piece_elems < 0) return AR_ERR_INVALID_ARG;
+    if (count == 0) return AR_OK;  // nothing is accessed
+    const int es = esize_of(dtype);
+    if (!dev_bufs) {
+      // zero-copy: one fused launch reads and writes the mapped host buffers
+      std::vector<Range> rs;
+      for (int r = 0; r < nranks; ++r) {
+        const uintptr_t h = (uintptr_t)host_bufs[r];
+        rs.push_back({h, h + (uintptr_t)count * es});
+      }
+      if ((rc = check_mapped_host(rs, es))) return rc;
+      TableBuilder tb{nranks, {}, {}};
+      Job j{};
+      bool empty = false;
+      if ((rc = build_collective(host_bufs, nranks, count, dtype, op, algo, 3, -1, tb, j, &empty, true)) || empty)
+        return rc;
+      return tb.for_each_table([&](SegTable& t) { return run_table(j, t, (cudaStream_t)stream_); });
+    }
+    {
+      std::vector<Range> all;
+      for (int r = 0; r < nranks; ++r) {
+        const uintptr_t h = (uintptr_t)host_bufs[r], d = (uintptr_t)dev_bufs[r];
+        all.push_back({h, h + (uintptr_t)count * es});
+        all.push_back({d, d + (uintptr_t)count * es});
+      }
+      if ((rc = check_disjoint(all, es))) return rc;
+    }
+    if ((rc = check_bufs(dev_bufs, nranks, count, dtype))) return rc;
+    if (nranks == 1) return AR_OK;  // a single rank already holds the reduction
+    HostPipe* hp = nullptr;
+    if ((rc = host_pipe(&hp))) return rc;
+    std::lock_guard<std::mutex> lk(hp->mu);
+    const std::vector<int64_t> starts = host_pieces(count, es, piece_elems);
+    // every piece is folded in the order of its elements' chunks of the whole buffer
+    Job j{dtype, op, algo == AR_NAIVE ? AR_RING : algo, 3, op == AR_AVG, same_phase16(dev_bufs, nranks)};
+    j.aligned = all_aligned16(dev_bufs, nranks);
+    cudaStream_t s = (cudaStream_t)stream_;
+    cudaError_t e;
+    if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(hp->up, hp->start, 0)) != cudaSuccess) return cuda_fail(e);
+    for (size_t k = 0; k < starts.size(); ++k) {
+      const int64_t a = starts[k], b = k + 1 < starts.size() ? starts[k + 1] : count;
+      const size_t off = (size_t)a * es, bytes = (size_t)(b - a) * es;
+      for (int r = 0; r < nranks; ++r)
+        if ((e = cudaMemcpyAsync(static_cast<char*>(dev_bufs[r]) + off, static_cast<const char*>(host_bufs[r]) + off,
+                                 bytes, cudaMemcpyHostToDevice, hp->up)) != cudaSuccess)
+          return cuda_fail(e);
+      if ((e = cudaEventRecord(hp->uploaded, hp->up)) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaStreamWaitEvent(s, hp->uploaded, 0)) != cudaSuccess) return cuda_fail(e);
+      TableBuilder tb{nranks, {}, {}};
+      const int row = tb.add_row(dev_bufs);
+      if (algo == AR_NAIVE) {
+        tb.add_seg(row, a, b, nranks - 1);
+      } else if (algo == AR_DBTREE) {
+        tb.add_seg(row, a, std::min(b, count / 2), 0);
+        tb.add_seg(row, std::max(a, count / 2), b, 1);
+      } else {
+        for (int c = 0; c < nranks; ++c)
+          tb.add_seg(row, std::max(a, chunk_lo(count, nranks, c)), std::min(b, chunk_lo(count, nranks, c + 1)), c);
+      }
+      if ((rc = tb.for_each_table([&](SegTable& t) { return run_table(j, t, s); }))) return rc;
+      if ((e = cudaEventRecord(hp->reduced, s)) != cudaSuccess) return cuda_fail(e);
+      if ((e = cudaStreamWaitEvent(hp->down, hp->reduced, 0)) != cudaSuccess) return cuda_fail(e);
+      for (int r = 0; r < nranks; ++r)
+        if ((e = cudaMemcpyAsync(static_cast<char*>(host_bufs[r]) + off, static_cast<const char*>(dev_bufs[r]) + off,
+                                 bytes, cudaMemcpyDeviceToHost, hp->down)) != cudaSuccess)
+          return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(hp->done, hp->down)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(s, hp->done, 0)) != cudaSuccess) return cuda_fail(e);
+    return AR_OK;
   });
 }
 

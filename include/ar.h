@@ -177,6 +177,48 @@ int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_o
 int ar_broadcast(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, int root, ar_stream_t stream);
 
 /*
+ * AllReduce of rank buffers held in host memory, through the GPU (an addition
+ * with no counterpart on the pages, which keep gradients on the devices: the
+ * end-to-end call for data that starts and ends on the host).  Either way the
+ * result is the one ar_allreduce gives with this algo, bit for bit.
+ *   dev_bufs == NULL (zero-copy): the host buffers must be page-locked memory
+ *     mapped for the current device at the same address (cudaHostAlloc, or
+ *     cudaHostRegister with mapping, under unified addressing; checked, else
+ *     AR_ERR_INVALID_ARG).  One fused launch on `stream` reads every rank's
+ *     elements across the CPU-GPU link and writes the result back across it.
+ *     piece_elems is ignored.
+ *   dev_bufs != NULL (staged): the buffers are cut into pieces of
+ *     `piece_elems` elements.  Each piece is copied into the device buffers,
+ *     AllReduced there by the fused kernel, and copied back.  The upload of
+ *     the next piece, the reduction of this one and the download of the
+ *     previous one run at the same time: the copies on two streams the
+ *     library keeps per device, the reductions on `stream`, ordered by events.
+ *     Page-locked host memory lets the copies overlap; pageable memory gives
+ *     the same result, but the CUDA runtime stages and mostly serialises its
+ *     copies.
+ *   host_bufs   host array of nranks host pointers, `count` elements each;
+ *               overwritten with the result
+ *   dev_bufs    NULL, or a host array of nranks device pointers of the current
+ *               device, `count` elements each: working space, overwritten
+ *   piece_elems elements per staged piece, rounded up to a multiple of 64;
+ *               0 = count / 8 clamped to 1-16 MiB per rank, with the first
+ *               and last three pieces 1/8, 1/4 and 1/2 of that
+ *   algo        AR_RING, AR_TREE, AR_NAIVE or AR_DBTREE (the step-wise
+ *               orders: AR_ERR_UNSUPPORTED)
+ * The call returns once everything is enqueued; the host buffers hold the
+ * result once `stream` reaches that point (e.g. after
+ * cudaStreamSynchronize(stream)) and must not be touched before.  The work
+ * starts after the work already on `stream`.  Staged calls on one device are
+ * serialised on the host and share its two copy streams; they are not for
+ * stream capture.
+ * Errors as ar_allreduce; all 2N ranges must be pairwise disjoint.  A CUDA
+ * failure part-way returns AR_ERR_CUDA with some pieces already enqueued:
+ * synchronise the device before reusing the buffers.
+ */
+int ar_allreduce_host(void* const* host_bufs, void* const* dev_bufs, int nranks, int64_t count, ar_dtype dtype,
+                      ar_op op, ar_algo algo, int64_t piece_elems, ar_stream_t stream);
+
+/*
  * 8-bit quantised AllReduce with error feedback ([tutorial §4.2]: gradients
  * travel as 8-bit integers that the receiver dequantises; error feedback
  * carries the compression error into the next round).  The pages give no

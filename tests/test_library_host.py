@@ -125,6 +125,20 @@ def test_counts_that_overflow_byte_ranges_are_refused(ar):
     assert "#define AR_MAX_COUNT (1LL << 56)" in header
 
 
+def test_host_buffer_allreduce_checks_without_device(ar):
+    h, d = [1 << 20, 1 << 21], [1 << 40, 1 << 41]
+    assert ar.ar_allreduce_host(h, d, count=4, algo="ring_stepwise", stream=0) == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_allreduce_host(h, d, count=4, dtype="i32", op="avg", stream=0) == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_allreduce_host([1 << 20, 1 << 20], d, count=4, stream=0) == ar.AR_ERR_INVALID_ARG  # duplicate
+    assert ar.ar_allreduce_host(h, [1 << 20, 1 << 41], count=4, stream=0) == ar.AR_ERR_INVALID_ARG  # host = device
+    assert ar.ar_allreduce_host(h, d, count=4, piece_elems=-1, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce_host(h, d, count=1 << 62, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.lib.ar_allreduce_host(None, None, 2, 4, 0, 0, 0, 0, None) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce_host([0, 0], [0, 0], count=0, stream=0) == ar.AR_OK  # nothing to move
+    # zero-copy needs mapped page-locked memory: unbacked addresses are refused, never computed on the host
+    assert ar.ar_allreduce_host(h, None, count=4, stream=0) in (ar.AR_ERR_INVALID_ARG, ar.AR_ERR_CUDA, -5)
+
+
 def test_no_device_is_reported_not_faked(ar):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
