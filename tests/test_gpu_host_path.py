@@ -139,6 +139,37 @@ def test_host_allreduce_completes_with_the_callers_stream(ar):
     assert same_bits(as_np(hb, "f32"), want2, "f32")
 
 
+@pytest.mark.parametrize("mode", ["staged", "zero_copy"])
+def test_host_allreduce_stays_inside_its_buffers(ar, mode):
+    """Rows carved out of one page-locked block between guard bands, at
+    offsets that are element-aligned but not all 16-byte aligned: the bands
+    (host and device side) must come back untouched and the rows correct."""
+    guard, n = 4096, 3
+    for count, shifts in ((1, [0, 1, 2]), (1001, [1, 1, 1]), (3 * 2048 + 7, [0, 3, 1]), (70_001, [2, 2, 2])):
+        x = W.normal_inputs(n, count, 1.0, 60 + count)
+        want, _ = oracle.allreduce(x, algo="ring", op="sum", dtype="f32")
+        span = guard + count + 8 + guard
+        block = torch.full((n, span), 7.5, dtype=torch.float32).pin_memory()
+        rows = []
+        for r in range(n):
+            o = guard + shifts[r]
+            block[r, o:o + count] = torch.from_numpy(x[r])
+            rows.append(block[r, o:o + count])
+        devblock = torch.full((n, span), -3.0, device="cuda")
+        dv = None if mode == "zero_copy" else [devblock[r, guard + shifts[r]:guard + shifts[r] + count]
+                                               for r in range(n)]
+        ar.check(ar.ar_allreduce_host(rows, dv, count=count, dtype="f32", op="sum", algo="ring", piece_elems=640),
+                 "host allreduce")
+        torch.cuda.synchronize()
+        for r in range(n):
+            o = guard + shifts[r]
+            assert same_bits(rows[r].numpy(), want[r], "f32"), (mode, count, shifts, r)
+            assert bool((block[r, :o] == 7.5).all()) and bool((block[r, o + count:] == 7.5).all()), (mode, count, r)
+            if dv is not None:
+                d = devblock[r].cpu()
+                assert bool((d[:o] == -3.0).all()) and bool((d[o + count:] == -3.0).all()), (mode, count, r)
+
+
 def test_zero_copy_needs_mapped_page_locked_memory(ar):
     n, count = 4, 1000
     x = W.normal_inputs(n, count, 1.0, 21)
