@@ -9,8 +9,10 @@ with 1% of entries scaled by 100, ring order, SUM.  A step is one
 
 Prints one JSON line.  ``value`` is effective HBM GB/s (2*N*D*b bytes per
 step / time, summed over replicas for N GPUs; each GPU runs an independent
-replica, there is no cross-GPU data path).  ``--impl reference`` times the CPU
-oracle on this host's cores on a bounded sample of the same workload.
+replica, there is no cross-GPU data path).  ``e2e`` is the same metric for
+``ar_allreduce_host`` on page-locked host buffers (every step's inputs come
+from host memory and its result goes back there).  ``--impl reference`` times
+the CPU oracle on this host's cores on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
