@@ -223,3 +223,41 @@ def test_random_plans(ar, block):
                 else:
                     assert same_bits(got, want[r], dtype), f"{what} it={it} rank {r}"
         plan.close()
+
+
+@pytest.mark.parametrize("block", range(4))
+def test_random_host_buffer_calls(ar, block):
+    """ar_allreduce_host with random shapes, orders, piece sizes, host-row
+    offsets, page-locked or pageable rows, zero-copy or staged."""
+    rng = np.random.default_rng(9500 + block)
+    for case in range(10):
+        n = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
+        count = int(rng.choice([1, n + 1, int(rng.integers(1, 3000)), int(rng.integers(3000, 60000))]))
+        dtype = str(rng.choice(["f32", "bf16", "i32"]))
+        algos = ["ring", "naive", "dbtree"] + (["tree"] if n & (n - 1) == 0 else [])
+        algo = str(rng.choice(algos))
+        op = str(rng.choice(["sum", "max"] + ([] if dtype == "i32" else ["avg"])))
+        pinned = bool(rng.integers(0, 2))
+        mode = str(rng.choice(["zero_copy", "staged"])) if pinned else "staged"
+        piece = int(rng.choice([0, 64, int(rng.integers(1, 5000))]))
+        x = (W.random_bits(n, count, dtype, int(rng.integers(1 << 20))) if op != "sum" or dtype == "i32"
+             else W.normal_inputs(n, count, 1.0, int(rng.integers(1 << 20))) if dtype == "f32"
+             else W.large_inputs(n, count, config=int(rng.integers(1 << 20))))
+        with np.errstate(all="ignore"):
+            want, _ = oracle.allreduce(x, algo=algo, op=op, dtype=dtype)
+        shifts = shifts_for(rng, n, dtype)
+        a = np.ascontiguousarray(x).view(np.int16) if dtype == "bf16" else np.ascontiguousarray(x)
+        block_t = torch.zeros((n, count + 8), dtype=TORCH[dtype])
+        if pinned:
+            block_t = block_t.pin_memory()
+        rows = []
+        for r in range(n):
+            block_t[r, shifts[r]:shifts[r] + count] = torch.from_numpy(a[r])
+            rows.append(block_t[r, shifts[r]:shifts[r] + count])
+        dv = None if mode == "zero_copy" else [place(np.zeros(count, dtype=a.dtype), dtype, s) for s in shifts]
+        what = f"host case {block}/{case}: n={n} count={count} {dtype} {op} {algo} {mode} pinned={pinned} piece={piece}"
+        ar.check(ar.ar_allreduce_host(rows, dv, count=count, dtype=dtype, op=op, algo=algo, piece_elems=piece), what)
+        torch.cuda.synchronize()
+        for r in range(n):
+            got = rows[r].numpy()
+            assert same_bits(got.view(np.uint16) if dtype == "bf16" else got, want[r], dtype), f"{what} rank {r}"
