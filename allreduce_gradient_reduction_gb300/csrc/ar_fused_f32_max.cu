@@ -1,4 +1,10 @@
-// Fused kernels for f32 max: one translation unit per (dtype, op) so the
+// Fused kernels for f32 max, large launch tables.  The maximum's kernels take
+// longest to compile, so each table form has its own translation unit and the
 // build compiles them in parallel.
 #include "ar_fused.cuh"
-AR_DEFINE_FUSED(launch_fused_f32_max, F32, MAX)
+
+namespace ar {
+cudaError_t launch_fused_f32_max(int order, bool vec, FusedArgs& a, cudaStream_t s) {
+  return launch_fused_typed<F32, MAX>(order, vec, a, s);
+}
+}  // namespace ar
