@@ -143,10 +143,13 @@ def uniform_rank_device(rank: int, count: int, dtype: str, torch, config: int = 
 
 
 def uniform_inputs(nranks: int, count: int, dtype: str, config: int = CONFIG_SWEEP) -> np.ndarray:
-    """uniform(-1, 1) values; bf16 as truncated bit patterns."""
+    """uniform(-1, 1) values; bf16 as truncated bit patterns, f16 as numpy's
+    binary16 conversion of the binary32 draw."""
     xs = np.stack([rng(config, r).uniform(-1.0, 1.0, size=count).astype(np.float32) for r in range(nranks)])
     if dtype == "bf16":
         return f32_to_bf16_bits_truncate(xs)
+    if dtype == "f16":
+        return xs.astype(np.float16).view(np.uint16)
     if dtype == "i32":
         return np.stack([rng(config, r).integers(-(1 << 20), 1 << 20, size=count, dtype=np.int32)
                          for r in range(nranks)])
@@ -157,7 +160,7 @@ def random_bits(nranks: int, count: int, dtype: str, seed: int) -> np.ndarray:
     """Arbitrary bit patterns (including NaN, infinities, subnormals, -0) for
     edge-case tests."""
     g = np.random.Generator(np.random.PCG64(seed))
-    if dtype == "bf16":
+    if dtype in ("bf16", "f16"):
         return g.integers(0, 1 << 16, size=(nranks, count), dtype=np.uint16)
     bits = g.integers(0, 1 << 32, size=(nranks, count), dtype=np.uint32)
     return bits.view(np.float32) if dtype == "f32" else bits.view(np.int32)

@@ -29,11 +29,11 @@ _SRC = os.path.join(_HERE, "ar_oracle.c")
 _LIB = os.path.join(_HERE, "libar_oracle.so")
 
 MAX_RANKS = 256
-DTYPES = {"f32": 0, "bf16": 1, "i32": 2}
+DTYPES = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 OPS = {"sum": 0, "max": 1, "avg": 2}
 ALGOS = {"ring": 0, "tree": 1, "binomial": 2, "naive": 3, "dbtree": 4}
 PHASE_RS, PHASE_AG = 1, 2
-NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32}
+NP_STORAGE = {"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.uint16}
 
 ERR_MISSING = -4
 
@@ -92,6 +92,8 @@ def lib():
                                                ctypes.c_int, ctypes.POINTER(Stats)]
         L.oracle_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int64]
         L.oracle_f32_to_bf16.argtypes = [vp, vp, ctypes.c_int64]
+        L.oracle_f32_to_f16.argtypes = [vp, vp, ctypes.c_int64]
+        L.oracle_f16_to_f32.argtypes = [vp, vp, ctypes.c_int64]
         L.oracle_chunk_range.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
         L.oracle_bucket_plan.argtypes = [ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int, ctypes.c_int64,
@@ -230,6 +232,22 @@ def f32_to_bf16(x):
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.shape, dtype=np.uint16)
     lib().oracle_f32_to_bf16(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def f32_to_f16(x):
+    """binary32 -> binary16 bit patterns, round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f32_to_f16(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def f16_to_f32(h):
+    """binary16 bit patterns -> binary32 values (exact)."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_f16_to_f32(h.ctypes.data, out.ctypes.data, h.size)
     return out
 
 

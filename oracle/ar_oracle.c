@@ -53,11 +53,16 @@
  *    compiled without contraction or fast-math).
  *  - bf16 SUM: convert both to binary32 (exact), add, round to bf16 by round-
  *    to-nearest-even on the dropped 16 bits.  NaN results become 0x7FC0.
+ *  - f16 SUM (IEEE binary16; the tutorial §4.2 names FP16 beside BF16 as the
+ *    half-size gradient type): convert both to binary32 (exact), add, round
+ *    to binary16 nearest-even.  Both roundings together equal one correct
+ *    rounding of the exact sum, because binary32 carries 24 >= 2*11 + 2
+ *    significand bits.  NaN results become 0x7E00.
  *  - i32 SUM: two's-complement wrap-around.
  *  - MAX: IEEE 754-2019 maximum: NaN if either operand is NaN, +0 > -0.
  *  - AVG: SUM, then the owner of each reduced chunk divides once by N
- *    (binary32 IEEE division; for bf16 the binary32 quotient is rounded to
- *    bf16).  AVG on i32 is rejected.
+ *    (binary32 IEEE division; for bf16 and f16 the binary32 quotient is
+ *    rounded to the storage type).  AVG on i32 is rejected.
  */
 #include <math.h>
 #include <stdint.h>
@@ -66,7 +71,7 @@
 
 #define OR_MAX_RANKS 256
 
-enum { OR_F32 = 0, OR_BF16 = 1, OR_I32 = 2 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_I32 = 2, OR_F16 = 3 };
 enum { OR_SUM = 0, OR_MAX = 1, OR_AVG = 2 };
 enum { OR_RING = 0, OR_TREE = 1, OR_BINOMIAL = 2, OR_NAIVE = 3, OR_DBTREE = 4 };
 enum { OR_PHASE_RS = 1, OR_PHASE_AG = 2 };
@@ -129,6 +134,58 @@ static uint16_t f32_to_bf16_rne(float f) {
   return (uint16_t)hi;
 }
 
+/* IEEE binary16: sign, 5 exponent bits (bias 15), 10 fraction bits.  Every
+ * binary16 value is exactly a binary32 value. */
+static float f16_to_f32(uint16_t h) {
+  const int e = (h >> 10) & 0x1F, m = h & 0x3FF;
+  float v;
+  if (e == 0x1F) {
+    uint32_t u = (h & 0x8000u) ? 0xFF800000u : 0x7F800000u;
+    if (m) u = 0x7FC00000u;
+    memcpy(&v, &u, 4);
+    return v;
+  }
+  v = e ? ldexpf((float)(1024 + m), e - 25) : ldexpf((float)m, -24);
+  return (h & 0x8000u) ? -v : v;
+}
+
+/* Round a binary32 value to binary16, nearest-even.  The significand with its
+ * hidden bit is shifted right to the binary16 unit of the value's exponent
+ * (2^-24 below the normal range), rounding on the bits shifted out; a carry
+ * into the next binade, or past the largest finite value, is what rounding up
+ * there means. */
+static uint16_t f32_to_f16_rne(float f) {
+  uint32_t u, sign, e, m, shift, q, rem, half;
+  uint64_t sig;
+  int E;
+  if (f32_is_nan(f)) return 0x7E00u;
+  memcpy(&u, &f, 4);
+  sign = (u >> 16) & 0x8000u;
+  e = (u >> 23) & 0xFFu;
+  m = u & 0x7FFFFFu;
+  if (e == 0xFFu) return (uint16_t)(sign | 0x7C00u); /* infinity */
+  if (e == 0 && m == 0) return (uint16_t)sign;       /* zero */
+  sig = e ? (uint64_t)(m | 0x800000u) : (uint64_t)m;  /* value = sig * 2^(E - 23) */
+  E = e ? (int)e - 127 : -126;
+  /* binary16 unit at exponent E: 2^(E-10) for E >= -14, else 2^-24 */
+  shift = (uint32_t)(E >= -14 ? 13 : (-E - 1)); /* 23 - 10, or 23 - (E + 24) */
+  if (shift > 24) return (uint16_t)sign; /* sig < 2^24: less than half a unit, and never a tie */
+  q = (uint32_t)(sig >> shift);
+  rem = (uint32_t)(sig & ((1ull << shift) - 1));
+  half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) q += 1u;
+  if (E >= -14) {
+    /* q holds the significand with its hidden bit: 1024..2048 */
+    if (q == 2048u) {
+      q = 1024u;
+      E += 1;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | ((uint32_t)(E + 15) << 10) | (q - 1024u));
+  }
+  return (uint16_t)(sign | q); /* subnormal; q == 1024 is the smallest normal */
+}
+
 static float f32_max(float a, float b) {
   uint32_t ua, ub, r;
   float out;
@@ -170,6 +227,21 @@ static void combine(int dtype, int op, const void* first, const void* second, vo
         d[i] = f32_to_bf16_rne(fa + fb);
       }
     }
+  } else if (dtype == OR_F16) {
+    const uint16_t* a = (const uint16_t*)first;
+    const uint16_t* b = (const uint16_t*)second;
+    uint16_t* d = (uint16_t*)dst;
+    for (i = 0; i < n; ++i) {
+      float fa = f16_to_f32(a[i]), fb = f16_to_f32(b[i]);
+      if (op == OR_MAX) {
+        if (f32_is_nan(fa) || f32_is_nan(fb)) d[i] = 0x7E00u;
+        else if (fa > fb) d[i] = a[i];
+        else if (fb > fa) d[i] = b[i];
+        else d[i] = (uint16_t)(a[i] & b[i]);
+      } else {
+        d[i] = f32_to_f16_rne(fa + fb);
+      }
+    }
   } else {
     const int32_t* a = (const int32_t*)first;
     const int32_t* b = (const int32_t*)second;
@@ -190,14 +262,17 @@ static void divide_by(int dtype, void* data, int64_t n, int nranks) {
   } else if (dtype == OR_BF16) {
     uint16_t* d = (uint16_t*)data;
     for (i = 0; i < n; ++i) d[i] = f32_to_bf16_rne(bf16_to_f32(d[i]) / fn);
+  } else if (dtype == OR_F16) {
+    uint16_t* d = (uint16_t*)data;
+    for (i = 0; i < n; ++i) d[i] = f32_to_f16_rne(f16_to_f32(d[i]) / fn);
   }
 }
 
-static int esize_of(int dtype) { return dtype == OR_BF16 ? 2 : 4; }
+static int esize_of(int dtype) { return (dtype == OR_BF16 || dtype == OR_F16) ? 2 : 4; }
 
 /* Exported single step, for table checks: out[i] = step(recv[i], local[i]). */
 int oracle_step(int dtype, int op, const void* recv, const void* local, void* out, int64_t n) {
-  if (dtype < 0 || dtype > 2 || op < 0 || op > 1 || n < 0) return OR_EINVAL;
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 1 || n < 0) return OR_EINVAL;
   combine(dtype, op, recv, local, out, n);
   return OR_OK;
 }
@@ -206,6 +281,19 @@ int oracle_step(int dtype, int op, const void* recv, const void* local, void* ou
 int oracle_f32_to_bf16(const float* in, uint16_t* out, int64_t n) {
   int64_t i;
   for (i = 0; i < n; ++i) out[i] = f32_to_bf16_rne(in[i]);
+  return OR_OK;
+}
+
+/* Exported binary32 <-> binary16 conversions, for tests of them. */
+int oracle_f32_to_f16(const float* in, uint16_t* out, int64_t n) {
+  int64_t i;
+  for (i = 0; i < n; ++i) out[i] = f32_to_f16_rne(in[i]);
+  return OR_OK;
+}
+
+int oracle_f16_to_f32(const uint16_t* in, float* out, int64_t n) {
+  int64_t i;
+  for (i = 0; i < n; ++i) out[i] = f16_to_f32(in[i]);
   return OR_OK;
 }
 
@@ -682,7 +770,7 @@ int oracle_collective(int algo, const void* const* in, void* const* out, int nra
   st->fail_step = -1;
   st->fail_rank = -1;
   if (nranks < 1 || nranks > OR_MAX_RANKS || count < 0 || !in || !out) return OR_EINVAL;
-  if (dtype < 0 || dtype > 2 || op < 0 || op > 2 || phases < 1 || phases > 3) return OR_EINVAL;
+  if (dtype < 0 || dtype > 3 || op < 0 || op > 2 || phases < 1 || phases > 3) return OR_EINVAL;
   if (op == OR_AVG && dtype == OR_I32) return OR_EUNSUPPORTED;
   if (algo < 0 || algo > 4) return OR_EINVAL;
   if ((algo == OR_TREE || algo == OR_BINOMIAL) && log2_exact(nranks) < 0) return OR_EUNSUPPORTED;
@@ -847,7 +935,7 @@ int oracle_rooted(int kind, int algo, const void* const* in, void* const* out, i
   st->fail_step = -1;
   st->fail_rank = -1;
   if (nranks < 1 || nranks > OR_MAX_RANKS || count < 0 || !in || !out || root < 0 || root >= nranks) return OR_EINVAL;
-  if (dtype < 0 || dtype > 2 || kind < 0 || kind > 1) return OR_EINVAL;
+  if (dtype < 0 || dtype > 3 || kind < 0 || kind > 1) return OR_EINVAL;
   if (kind == OR_KIND_REDUCE) {
     if (op < 0 || op > 2 || (algo != OR_RING && algo != OR_TREE && algo != OR_NAIVE)) return OR_EINVAL;
     if (op == OR_AVG && dtype == OR_I32) return OR_EUNSUPPORTED;
@@ -1110,7 +1198,7 @@ int oracle_bucket_plan(const int64_t* counts, int ntensors, int dtype, int64_t c
   int t, b = -1;
   int64_t fill = 0;
   int es;
-  if (ntensors < 0 || cap_bytes <= 0 || dtype < 0 || dtype > 2 || !nbuckets) return OR_EINVAL;
+  if (ntensors < 0 || cap_bytes <= 0 || dtype < 0 || dtype > 3 || !nbuckets) return OR_EINVAL;
   es = esize_of(dtype);
   for (t = ntensors - 1; t >= 0; --t) {
     int64_t bytes;
@@ -1158,7 +1246,7 @@ int oracle_bucketed_allreduce(const void* const* grads_in, void* const* grads_ou
   int64_t *off = NULL, *bcount = NULL;
   int es, b, r, t, rc = OR_OK;
   oracle_stats st;
-  if (ntensors < 0 || nranks < 1 || nranks > OR_MAX_RANKS || dtype < 0 || dtype > 2) return OR_EINVAL;
+  if (ntensors < 0 || nranks < 1 || nranks > OR_MAX_RANKS || dtype < 0 || dtype > 3) return OR_EINVAL;
   es = esize_of(dtype);
   bucket_of = (int32_t*)calloc((size_t)(ntensors + 1), sizeof(int32_t));
   off = (int64_t*)calloc((size_t)(ntensors + 1), sizeof(int64_t));

@@ -32,6 +32,13 @@ MUTANTS = [
     ("bf16 truncates",
      [("if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;", "(void)lo;")],
      ["bf16_round"]),
+    ("f16 ties round away from zero",
+     [("if (rem > half || (rem == half && (q & 1u))) q += 1u;", "if (rem >= half) q += 1u;")],
+     ["f16_round"]),
+    ("f16 subnormals flushed to zero",
+     [("return (uint16_t)(sign | q); /* subnormal; q == 1024 is the smallest normal */",
+       "return (uint16_t)(q == 1024u ? (sign | q) : sign);")],
+     ["f16_round"]),
     ("tree pairs the farthest ranks first",
      [("for (k = 0; k < L; ++k) {\n    int h = 1 << k;\n    for (r = 0; r < s->n; ++r) {\n      int p = r ^ h;\n      int c = kept_set(s->n, p, h, set);",
        "for (k = 0; k < L; ++k) {\n    int h = s->n >> (k + 1);\n    for (r = 0; r < s->n; ++r) {\n      int p = r ^ h;\n      int c = kept_set(s->n, p, h, set);"),
@@ -112,6 +119,9 @@ def run_pins(which):
     if "bf16_round" in which:
         P.test_bf16_rounding_edges(o)
         P.test_bf16_add_is_correctly_rounded(o)
+    if "f16_round" in which:
+        P.test_f16_rounding_by_value(o)
+        P.test_f16_add_is_correctly_rounded(o)
     if "avg" in which:
         P.test_printed_ddp_average(o, "f32")
         P.test_avg_f32_is_sum_then_divide(o, 8)
@@ -167,5 +177,5 @@ def test_pins_catch_mutant(tmp_path, monkeypatch, name, edits, pins):
 
 
 def test_real_oracle_passes_the_same_pins():
-    run_pins({"ring_order", "tree_order", "bruteforce", "printed", "bf16_round", "avg", "max", "f32_add",
+    run_pins({"ring_order", "tree_order", "bruteforce", "printed", "bf16_round", "f16_round", "avg", "max", "f32_add",
               "bucket", "volume", "dbtree", "int8", "rooted"})

@@ -13,7 +13,7 @@ import oracle
 from allreduce_gradient_reduction_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-ALL_DTYPES = ("f32", "bf16", "i32")
+ALL_DTYPES = ("f32", "bf16", "i32", "f16")
 
 
 def read_golden(name):
@@ -41,6 +41,8 @@ def to_storage(vals, dtype):
         return a
     if dtype == "i32":
         return a.astype(np.int32)
+    if dtype == "f16":
+        return a.astype(np.float16).view(np.uint16)  # the golden values are exact in binary16
     return (a.view(np.uint32) >> 16).astype(np.uint16)  # the golden values are exact in bf16
 
 
@@ -48,6 +50,8 @@ def to_f64(x, dtype):
     x = np.asarray(x)
     if dtype == "bf16":
         return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype == "f16":
+        return np.ascontiguousarray(x, dtype=np.uint16).view(np.float16).astype(np.float64)
     return x.astype(np.float64)
 
 
@@ -264,6 +268,127 @@ def test_max_special_values(oracle_lib):
 
 
 # --------------------------------------------------------------------------
+# binary16 (f16): conversions and the SUM / AVG / MAX steps
+# --------------------------------------------------------------------------
+
+def _frac_round_f16(x: Fraction):
+    """Correctly rounded binary16 value of an exact rational (nearest, ties to
+    even; 10 fraction bits, unit 2^-24 below the normal range); a float, inf
+    when the rounded magnitude reaches 2^16."""
+    if x == 0:
+        return 0.0
+    s = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** max(e - 10, -24)
+    q = a / ulp
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * ulp
+    if r >= 2 ** 16:
+        return s * math.inf
+    return s * float(r)
+
+
+def test_f16_decodes_every_pattern(oracle_lib):
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f16_to_f32(h)
+    want = h.view(np.float16).astype(np.float32)  # numpy's binary16 widening
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    # and every non-NaN pattern survives the trip back
+    assert np.array_equal(oracle.f32_to_f16(got[~nan]), h[~nan])
+
+
+def test_f16_rounding_by_value(oracle_lib):
+    # ties and near-ties at the subnormal unit, the normal/subnormal boundary,
+    # the top binade and the overflow threshold, plus their neighbours
+    base = [2.0 ** -25, 3 * 2.0 ** -25, 2.0 ** -24, 1.5 * 2.0 ** -24, 2.0 ** -14 - 2.0 ** -25,
+            2.0 ** -14 - 2.0 ** -26, 2.0 ** -14, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 2049.0, 2051.0,
+            65504.0, 65505.0, 65519.0, 65520.0, 65536.0, 1e-9, 0.1, 1.0 / 3.0, 1e5]
+    f = np.array(base, dtype=np.float32)
+    f = np.concatenate([f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(0))])
+    f = np.concatenate([f, -f])
+    got = to_f64(oracle.f32_to_f16(f), "f16")
+    for v, g in zip(f.tolist(), got.tolist()):
+        want = _frac_round_f16(Fraction(v))
+        assert g == want and math.copysign(1, g) == math.copysign(1, v if want == 0 else want), (v, g, want)
+
+
+def test_f16_rounding_matches_numpy(oracle_lib):
+    g = np.random.Generator(np.random.PCG64(16))
+    # magnitudes from far below the smallest subnormal to past the overflow threshold
+    f = (g.standard_normal(2_000_000) * np.exp2(g.uniform(-30, 18, 2_000_000))).astype(np.float32)
+    with np.errstate(over="ignore"):
+        want = f.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.f32_to_f16(f), want)
+
+
+def _f16_pairs(n, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    a = g.integers(0, 1 << 16, size=n, dtype=np.uint16)
+    b_near = (a.astype(np.int32) + g.integers(-1500, 1500, size=n)).clip(0, 0xFFFF).astype(np.uint16)
+    b_near ^= (g.integers(0, 2, size=n, dtype=np.uint16) << 15)
+    b_far = g.integers(0, 1 << 16, size=n, dtype=np.uint16)
+    b = np.where(g.random(n) < 0.5, b_near, b_far).astype(np.uint16)
+    fa, fb = to_f64(a, "f16"), to_f64(b, "f16")
+    keep = np.isfinite(fa) & np.isfinite(fb)
+    return a[keep], b[keep]
+
+
+def test_f16_add_is_correctly_rounded(oracle_lib):
+    a, b = _f16_pairs(30000, 21)
+    got = to_f64(oracle.step(a, b, op="sum", dtype="f16"), "f16")
+    fa, fb = to_f64(a, "f16"), to_f64(b, "f16")
+    for i in range(a.size):
+        exact = Fraction(float(fa[i])) + Fraction(float(fb[i]))
+        want = _frac_round_f16(exact)
+        if exact == 0:
+            want = -0.0 if (math.copysign(1, fa[i]) < 0 and math.copysign(1, fb[i]) < 0) else 0.0
+        assert got[i] == want and math.copysign(1, got[i]) == math.copysign(1, want), (hex(a[i]), hex(b[i]))
+
+
+def test_f16_add_matches_numpy(oracle_lib):
+    a, b = _f16_pairs(1_000_000, 22)
+    got = oracle.step(a, b, op="sum", dtype="f16")
+    with np.errstate(over="ignore"):
+        want = (a.view(np.float16) + b.view(np.float16)).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_f16_avg_is_the_correctly_rounded_quotient(oracle_lib):
+    for n in (2, 3, 5, 8, 13, 64):
+        x = W.uniform_inputs(n, 3000, "f16", config=40 + n)
+        s, _ = oracle.allreduce(x, algo="ring", op="sum", dtype="f16")
+        a, _ = oracle.allreduce(x, algo="ring", op="avg", dtype="f16")
+        sv, av = to_f64(s[0], "f16"), to_f64(a[0], "f16")
+        for i in range(sv.size):
+            want = _frac_round_f16(Fraction(float(sv[i])) / n)
+            if want == 0:
+                want = math.copysign(0.0, sv[i])
+            assert av[i] == want and math.copysign(1, av[i]) == math.copysign(1, want), (n, i, sv[i])
+
+
+def test_f16_max_special_values(oracle_lib):
+    nan, inf = np.float16("nan"), np.float16("inf")
+    a = np.array([0.0, -0.0, -0.0, nan, 1.0, -inf, 3.0, -2.0, 6e-8], dtype=np.float16)
+    b = np.array([-0.0, 0.0, -0.0, 1.0, nan, 5.0, 2.0, -1.0, -6e-8], dtype=np.float16)
+    got = to_f64(oracle.step(a.view(np.uint16), b.view(np.uint16), op="max", dtype="f16"), "f16")
+    assert got[0] == 0 and not np.signbit(got[0])
+    assert got[1] == 0 and not np.signbit(got[1])
+    assert got[2] == 0 and np.signbit(got[2])
+    assert np.isnan(got[3]) and np.isnan(got[4])
+    assert got[5:].tolist() == [5.0, 3.0, -1.0, float(np.float16(6e-8))]
+
+
+# --------------------------------------------------------------------------
 # Brute force on tiny inputs: order-free results must be exact
 # --------------------------------------------------------------------------
 
@@ -290,6 +415,9 @@ def test_bruteforce_integers_and_max(oracle_lib, n):
             assert np.array_equal(out, np.broadcast_to(xf.astype(np.float64).sum(axis=0), out.shape))
             out, _ = oracle.allreduce(xb, algo=algo, op="sum", dtype="bf16")  # |sum| <= 64: exact in bf16
             assert np.array_equal(to_f64(out, "bf16"), np.broadcast_to(xf.astype(np.float64).sum(axis=0), out.shape))
+            out, _ = oracle.allreduce(to_storage(xf.reshape(-1), "f16").reshape(n, count), algo=algo, op="sum",
+                                      dtype="f16")  # exact in binary16 too
+            assert np.array_equal(to_f64(out, "f16"), np.broadcast_to(xf.astype(np.float64).sum(axis=0), out.shape))
             out, _ = oracle.allreduce(xr, algo=algo, op="max", dtype="f32")
             assert np.array_equal(out, np.broadcast_to(xr.max(axis=0), out.shape))
 
@@ -309,6 +437,9 @@ def _lib_add(dtype):
             tb = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
             return (ta + tb).view(torch.int16).numpy().view(np.uint16)
         return add
+    if dtype == "f16":
+        return lambda a, b: (np.ascontiguousarray(a).view(np.float16) +
+                             np.ascontiguousarray(b).view(np.float16)).view(np.uint16)
     return lambda a, b: a + b
 
 
@@ -445,8 +576,8 @@ def _same(a, b, dtype):
     na, nb = np.isnan(fa), np.isnan(fb)
     if not np.array_equal(na, nb):
         return False
-    ua = a.view(np.uint16 if dtype == "bf16" else np.uint32)
-    ub = b.view(np.uint16 if dtype == "bf16" else np.uint32)
+    ua = a.view(np.uint16 if dtype in ("bf16", "f16") else np.uint32)
+    ub = b.view(np.uint16 if dtype in ("bf16", "f16") else np.uint32)
     return np.array_equal(ua[~na], ub[~nb])
 
 
@@ -528,7 +659,7 @@ def gamma(k, u):
     return k * u / (1 - k * u)
 
 
-@pytest.mark.parametrize("dtype,u", [("f32", 2.0 ** -24), ("bf16", 2.0 ** -8)])
+@pytest.mark.parametrize("dtype,u", [("f32", 2.0 ** -24), ("bf16", 2.0 ** -8), ("f16", 2.0 ** -11)])
 @pytest.mark.parametrize("n", [2, 8, 64])
 def test_error_bound(oracle_lib, dtype, u, n):
     count = 20000 if n < 64 else 2000
