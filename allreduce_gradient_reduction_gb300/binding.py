@@ -18,7 +18,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libar_gb300.so")
 
-DTYPE = {"f32": 0, "bf16": 1, "i32": 2}
+DTYPE = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 OP = {"sum": 0, "max": 1, "avg": 2}
 ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3, "naive": 4, "dbtree": 5}
 STATUS = {0: "AR_OK", -1: "AR_ERR_INVALID_ARG", -2: "AR_ERR_UNSUPPORTED", -3: "AR_ERR_CUDA",

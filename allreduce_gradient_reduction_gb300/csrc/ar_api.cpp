@@ -28,7 +28,7 @@ int cuda_fail(cudaError_t e) {
   return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? AR_ERR_NO_DEVICE : AR_ERR_CUDA;
 }
 
-int esize_of(int dtype) { return dtype == AR_BF16 ? 2 : 4; }
+int esize_of(int dtype) { return (dtype == AR_BF16 || dtype == AR_F16) ? 2 : 4; }
 
 bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
@@ -120,7 +120,7 @@ int check_mapped_host(std::vector<Range>& rs, int esize) {
 
 int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
   if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0 || count > AR_MAX_COUNT) return AR_ERR_INVALID_ARG;
-  if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
+  if (dtype < AR_F32 || dtype > AR_F16 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
   if (algo < AR_RING || algo > AR_DBTREE) return AR_ERR_INVALID_ARG;
   if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
   if ((algo == AR_TREE || algo == AR_TREE_STEPWISE) && !is_pow2(nranks)) return AR_ERR_UNSUPPORTED;
@@ -726,7 +726,7 @@ int ar_chunk_range(int64_t count, int nranks, int c, int64_t* lo, int64_t* hi) {
 int ar_bucket_plan(const int64_t* counts, int ntensors, ar_dtype dtype, int64_t cap_bytes, int32_t* bucket_of_tensor,
                    int64_t* offset_in_bucket, int64_t* bucket_count, int32_t* nbuckets) {
   return guarded([&]() -> int {
-    if (ntensors < 0 || cap_bytes <= 0 || dtype < AR_F32 || dtype > AR_I32 || !nbuckets) return AR_ERR_INVALID_ARG;
+    if (ntensors < 0 || cap_bytes <= 0 || dtype < AR_F32 || dtype > AR_F16 || !nbuckets) return AR_ERR_INVALID_ARG;
     if (ntensors > 0 && (!counts || !bucket_of_tensor || !offset_in_bucket || !bucket_count)) return AR_ERR_INVALID_ARG;
     return plan_buckets(counts, ntensors, dtype, cap_bytes, bucket_of_tensor, offset_in_bucket, bucket_count, nbuckets);
   });

@@ -147,6 +147,10 @@ cudaError_t launch_fused_bf16_sum(int, bool, SmallFusedArgs&, cudaStream_t);
 cudaError_t launch_fused_bf16_max(int, bool, SmallFusedArgs&, cudaStream_t);
 cudaError_t launch_fused_i32_sum(int, bool, SmallFusedArgs&, cudaStream_t);
 cudaError_t launch_fused_i32_max(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f16_sum(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f16_max(int, bool, FusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f16_sum(int, bool, SmallFusedArgs&, cudaStream_t);
+cudaError_t launch_fused_f16_max(int, bool, SmallFusedArgs&, cudaStream_t);
 
 template <class ARGS>
 static cudaError_t launch_fused_any(int dtype, int op, int order, bool vec, ARGS& a, cudaStream_t s) {
@@ -157,6 +161,8 @@ static cudaError_t launch_fused_any(int dtype, int op, int order, bool vec, ARGS
     case BF16 * 2 + MAX: return launch_fused_bf16_max(order, vec, a, s);
     case I32 * 2 + SUM: return launch_fused_i32_sum(order, vec, a, s);
     case I32 * 2 + MAX: return launch_fused_i32_max(order, vec, a, s);
+    case F16 * 2 + SUM: return launch_fused_f16_sum(order, vec, a, s);
+    case F16 * 2 + MAX: return launch_fused_f16_max(order, vec, a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -4,14 +4,16 @@
 //
 // Element step (the pages ask for sum / max / average; the arithmetic is
 // IEEE): f32 SUM is one binary32 addition rounded to nearest even (compiled
-// without fast-math, so subnormals are kept); bf16 SUM widens both operands to
-// binary32 exactly, adds, and rounds the sum to bf16 nearest-even (the same
-// rounding a step-wise ring applies after every received chunk); i32 SUM wraps;
+// without fast-math, so subnormals are kept); bf16 and f16 SUM widen both
+// operands to binary32 exactly, add, and round the sum to the storage type
+// nearest-even (the same rounding a step-wise ring applies after every
+// received chunk); i32 SUM wraps;
 // MAX is the IEEE 754-2019 maximum (NaN propagates, +0 > -0).  AVG divides
 // once by N with IEEE binary32 division.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "ar_internal.h"
@@ -20,10 +22,10 @@ namespace ar {
 
 template <int DT>
 struct ElemSize {
-  static constexpr int value = (DT == BF16) ? 2 : 4;
+  static constexpr int value = (DT == BF16 || DT == F16) ? 2 : 4;
 };
 
-// ---- one 32-bit word: 1 f32, 2 bf16 or 1 i32 -------------------------------
+// ---- one 32-bit word: 1 f32, 2 bf16, 2 f16 or 1 i32 ------------------------
 
 __device__ __forceinline__ bool f32_nan(uint32_t u) { return (u & 0x7FFFFFFFu) > 0x7F800000u; }
 
@@ -49,6 +51,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+__device__ __forceinline__ float f16_to_float(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)h)); }
+
+__device__ __forceinline__ uint32_t f16_half_max(uint32_t a, uint32_t b) {  // a, b: f16 bits in the low half
+  if ((a & 0x7FFFu) > 0x7C00u || (b & 0x7FFFu) > 0x7C00u) return 0x7E00u;
+  const float xa = f16_to_float(a), xb = f16_to_float(b);
+  if (xa > xb) return a;
+  if (xb > xa) return b;
+  return a & b;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2_rn(float lo, float hi) {
+  __half2 r = __floats2half2_rn(lo, hi);  // .x (low 16 bits) = lo
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 template <int DT, int OP>
 __device__ __forceinline__ uint32_t step_word(uint32_t a, uint32_t b) {
   if constexpr (DT == F32) {
@@ -61,6 +78,13 @@ __device__ __forceinline__ uint32_t step_word(uint32_t a, uint32_t b) {
       return pack_bf16x2_rn(__fadd_rn(a0, b0), __fadd_rn(a1, b1));
     } else {
       return bf16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (bf16_half_max(a >> 16, b >> 16) << 16);
+    }
+  } else if constexpr (DT == F16) {
+    if constexpr (OP == SUM) {
+      return pack_f16x2_rn(__fadd_rn(f16_to_float(a & 0xFFFFu), f16_to_float(b & 0xFFFFu)),
+                           __fadd_rn(f16_to_float(a >> 16), f16_to_float(b >> 16)));
+    } else {
+      return f16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (f16_half_max(a >> 16, b >> 16) << 16);
     }
   } else {
     if constexpr (OP == SUM) {
@@ -81,6 +105,8 @@ __device__ __forceinline__ uint32_t div_word(uint32_t a, float fn) {
     return __float_as_uint(__fdiv_rn(__uint_as_float(a), fn));
   } else if constexpr (DT == BF16) {
     return pack_bf16x2_rn(__fdiv_rn(__uint_as_float(a << 16), fn), __fdiv_rn(__uint_as_float(a & 0xFFFF0000u), fn));
+  } else if constexpr (DT == F16) {
+    return pack_f16x2_rn(__fdiv_rn(f16_to_float(a & 0xFFFFu), fn), __fdiv_rn(f16_to_float(a >> 16), fn));
   } else {
     return a;
   }

@@ -37,10 +37,11 @@ constexpr int kFusedBlock = 256;
 // then gets 3 (at 2 it was 1.9% slower on 64 x 64 MiB; at 3 as fast as one
 // group at a time at 4 blocks per SM, and twice as fast for calls of
 // 4-64 KiB).  The trees, which also hold finished subtrees, and the bf16
-// maximum, which needs more temporaries, get 2 (128 registers), without
-// spills.
+// and f16 maximum, which need more temporaries, get 2 (128 registers),
+// without spills.
 __host__ __device__ constexpr int fused_min_blocks(int order, int nr, int dt, int op) {
-  return nr > 8 ? (order == RING && !(dt == BF16 && op == MAX) ? 3 : 2) : (order == DBTREE && nr == 8 ? 3 : 4);
+  return nr > 8 ? (order == RING && !((dt == BF16 || dt == F16) && op == MAX) ? 3 : 2)
+                : (order == DBTREE && nr == 8 ? 3 : 4);
 }
 __host__ __device__ constexpr int fused_unroll(int order, int nr) {
   return (nr == 2) ? 2 : 1;

@@ -7,7 +7,7 @@
 
 namespace ar {
 
-enum Dtype { F32 = 0, BF16 = 1, I32 = 2 };
+enum Dtype { F32 = 0, BF16 = 1, I32 = 2, F16 = 3 };
 enum Op { SUM = 0, MAX = 1 };  // AVG = SUM plus the `avg` flag
 enum Order { RING = 0, TREE = 1, DBTREE = 2 };
 

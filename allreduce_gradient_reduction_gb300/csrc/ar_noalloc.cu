@@ -126,7 +126,7 @@ extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* 
                                              ar_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   if (nranks < 1 || nranks > AR_MAX_RANKS || ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
-  if (dtype < AR_F32 || dtype > AR_I32 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
+  if (dtype < AR_F32 || dtype > AR_F16 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
   if (algo < AR_RING || algo > AR_TREE_STEPWISE) return AR_ERR_INVALID_ARG;
   // the step-wise kernels need a barrier block the library would allocate
   if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
@@ -135,7 +135,7 @@ extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* 
   if (ntensors == 0) return AR_OK;
   if (!grads || !counts) return AR_ERR_INVALID_ARG;
   if (ntensors > kMaxTensors) return AR_ERR_TOO_LARGE;
-  const int es = dtype == AR_BF16 ? 2 : 4;
+  const int es = (dtype == AR_BF16 || dtype == AR_F16) ? 2 : 4;
 
   std::lock_guard<std::mutex> lk(g_mu);
   int32_t nb = 0;

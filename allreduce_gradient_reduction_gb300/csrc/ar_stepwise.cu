@@ -49,7 +49,8 @@ static cudaError_t launch_smem_typed(SmemStepArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_stepwise_smem(int dtype, int op, SmemStepArgs& a, cudaStream_t s) {
-  if (smem_step_bytes(a.nranks, a.count, dtype == BF16 ? 2 : 4) > kSmemStepBytes) return cudaErrorInvalidValue;
+  if (smem_step_bytes(a.nranks, a.count, (dtype == BF16 || dtype == F16) ? 2 : 4) > kSmemStepBytes)
+    return cudaErrorInvalidValue;
   switch (dtype * 2 + op) {
     case F32 * 2 + SUM: return launch_smem_typed<F32, SUM>(a, s);
     case F32 * 2 + MAX: return launch_smem_typed<F32, MAX>(a, s);
@@ -57,6 +58,8 @@ cudaError_t launch_stepwise_smem(int dtype, int op, SmemStepArgs& a, cudaStream_
     case BF16 * 2 + MAX: return launch_smem_typed<BF16, MAX>(a, s);
     case I32 * 2 + SUM: return launch_smem_typed<I32, SUM>(a, s);
     case I32 * 2 + MAX: return launch_smem_typed<I32, MAX>(a, s);
+    case F16 * 2 + SUM: return launch_smem_typed<F16, SUM>(a, s);
+    case F16 * 2 + MAX: return launch_smem_typed<F16, MAX>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -69,6 +72,8 @@ cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& a, cudaStream
     case BF16 * 2 + MAX: return launch_step_op<BF16, MAX>(vec, a, s);
     case I32 * 2 + SUM: return launch_step_op<I32, SUM>(vec, a, s);
     case I32 * 2 + MAX: return launch_step_op<I32, MAX>(vec, a, s);
+    case F16 * 2 + SUM: return launch_step_op<F16, SUM>(vec, a, s);
+    case F16 * 2 + MAX: return launch_step_op<F16, MAX>(vec, a, s);
     default: return cudaErrorInvalidValue;
   }
 }

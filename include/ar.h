@@ -41,13 +41,14 @@
  *     chunk c = [floor(c*count/N), floor((c+1)*count/N)); rank c owns chunk c
  *     after ReduceScatter.  [concept §3], [tutorial §2.2], [notes §两阶段流程].
  *   - Element step: f32 is IEEE binary32 addition (round to nearest even,
- *     subnormals kept); bf16 is exact widening to binary32, addition, and
- *     rounding to nearest even back to bf16 after every step; i32 adds with
+ *     subnormals kept); bf16 and f16 (IEEE binary16, the FP16 of [tutorial
+ *     §4.2]) are exact widening to binary32, addition, and rounding to nearest
+ *     even back to the storage type after every step; i32 adds with
  *     two's-complement wrap-around; MAX is IEEE 754-2019 maximum (NaN
  *     propagates, +0 > -0).  AVG is SUM followed by one IEEE binary32 division
- *     by N of each reduced element (for bf16 the quotient is rounded to bf16);
- *     AVG on i32 is AR_ERR_UNSUPPORTED.  NaN results carry no payload
- *     guarantee.
+ *     by N of each reduced element (for bf16 and f16 the quotient is rounded
+ *     to the storage type); AVG on i32 is AR_ERR_UNSUPPORTED.  NaN results
+ *     carry no payload guarantee.
  *   - Orders (bit-exact with a step-wise execution of the same schedule):
  *       AR_RING / AR_RING_STEPWISE: chunk c is folded in ring order
  *         x[c+1], x[c+2], ..., x[c+N-1], x[c] (indices mod N), one rounding per
@@ -96,7 +97,7 @@ typedef struct CUstream_st* ar_stream_t;
 #define AR_MAX_COUNT (1LL << 56)
 #define AR_DEFAULT_BUCKET_CAP_BYTES (25LL << 20) /* DDP's 25 MB bucket [tutorial §4.1] */
 
-typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2 } ar_dtype;
+typedef enum { AR_F32 = 0, AR_BF16 = 1, AR_I32 = 2, AR_F16 = 3 } ar_dtype;
 typedef enum { AR_SUM = 0, AR_MAX = 1, AR_AVG = 2 } ar_op;
 typedef enum {
   AR_RING = 0,

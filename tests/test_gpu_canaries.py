@@ -11,8 +11,8 @@ torch = pytest.importorskip("torch")
 
 GUARD = 4096
 PATTERN = 0xA5
-ES = {"f32": 4, "bf16": 2, "i32": 4}
-TORCH = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32}
+ES = {"f32": 4, "bf16": 2, "i32": 4, "f16": 2}
+TORCH = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32, "f16": torch.int16}
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +58,7 @@ def sizes(n):
     return [1, n - 1, n + 1, 127, 1000, 4099, 3 * 2048 * n + 13]
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 @pytest.mark.parametrize("n", [2, 3, 8])
 def test_collectives_stay_inside_their_buffers(ar, n, dtype):
     algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])

@@ -11,8 +11,9 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-ES = {"f32": 4, "bf16": 2, "i32": 4}
-TORCH = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32}
+ES = {"f32": 4, "bf16": 2, "i32": 4, "f16": 2}
+TORCH = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32, "f16": torch.int16}
+HALF = ("bf16", "f16")
 
 
 @pytest.fixture(scope="module")
@@ -29,7 +30,7 @@ def ar():
 def place(row, dtype, shift):
     """A device buffer holding `row`, starting `shift` elements into its allocation."""
     a = np.ascontiguousarray(row)
-    if dtype == "bf16":
+    if dtype in HALF:
         a = a.view(np.int16)
     big = torch.zeros(a.size + shift + 8, dtype=TORCH[dtype], device="cuda")
     v = big[shift:shift + a.size]
@@ -39,15 +40,21 @@ def place(row, dtype, shift):
 
 def host(v, dtype):
     out = v.cpu().numpy()
-    return out.view(np.uint16) if dtype == "bf16" else out
+    return out.view(np.uint16) if dtype in HALF else out
 
 
 def same_bits(got, want, dtype):
     if dtype == "i32":
         return np.array_equal(got, want)
-    bits = np.uint16 if dtype == "bf16" else np.uint32
-    f = (got.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else got
-    g = (want.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else want
+    bits = np.uint16 if dtype in HALF else np.uint32
+
+    def val(x):
+        if dtype == "bf16":
+            return (x.astype(np.uint32) << 16).view(np.float32)
+        if dtype == "f16":
+            return np.ascontiguousarray(x, dtype=np.uint16).view(np.float16)
+        return x
+    f, g = val(got), val(want)
     nan = np.isnan(f) & np.isnan(g)
     return bool(np.all(nan | (got.view(bits) == want.view(bits))))
 
@@ -69,7 +76,7 @@ def test_random_collectives(ar, block):
         n = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 16, 32, 64]))
         count = int(rng.choice([0, 1, n - 1, n, n + 1, int(rng.integers(1, 300)), int(rng.integers(300, 20000))]))
         count = max(count, 0)
-        dtype = str(rng.choice(["f32", "bf16", "i32"]))
+        dtype = str(rng.choice(["f32", "bf16", "i32", "f16"]))
         kind = str(rng.choice(["allreduce", "reduce_scatter", "all_gather", "reduce", "broadcast"]))
         algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
         if kind in ("reduce_scatter", "all_gather"):
@@ -82,7 +89,7 @@ def test_random_collectives(ar, block):
         root = int(rng.integers(0, n))
         x = W.random_bits(n, count, dtype, seed=int(rng.integers(1 << 30))) if rng.random() < 0.3 else (
             W.uniform_inputs(n, count, dtype, config=int(rng.integers(1 << 20))) if count else
-            np.zeros((n, 0), dtype=np.uint16 if dtype == "bf16" else (np.int32 if dtype == "i32" else np.float32)))
+            np.zeros((n, 0), dtype=np.uint16 if dtype in HALF else (np.int32 if dtype == "i32" else np.float32)))
         shifts = shifts_for(rng, n, dtype)
         bufs = [place(x[r], dtype, shifts[r]) for r in range(n)]
         oa = {"ring_stepwise": "ring", "tree_stepwise": "tree"}.get(algo, algo)
@@ -180,7 +187,7 @@ def test_random_plans(ar, block):
     for case in range(10):
         n = int(rng.choice([2, 3, 4, 8, 16]))
         count = int(rng.integers(1, 20000))
-        dtype = str(rng.choice(["f32", "bf16", "i32"]))
+        dtype = str(rng.choice(["f32", "bf16", "i32", "f16"]))
         kind = str(rng.choice(["allreduce", "reduce_scatter", "all_gather", "reduce"]))
         algos = ["ring", "ring_stepwise"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
         if kind == "allreduce":
@@ -191,7 +198,7 @@ def test_random_plans(ar, block):
         op = str(rng.choice(["sum", "max"] + ([] if dtype == "i32" else ["avg"])))
         root = int(rng.integers(0, n))
         shifts = shifts_for(rng, n, dtype)
-        bufs = [place(np.zeros(count, dtype={"f32": np.float32, "bf16": np.uint16, "i32": np.int32}[dtype]),
+        bufs = [place(np.zeros(count, dtype={"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.uint16}[dtype]),
                       dtype, shifts[r]) for r in range(n)]
         plan = ar.Plan(kind, bufs, count=count, dtype=dtype, op=op, algo=algo, root=root)
         oa = {"ring_stepwise": "ring", "tree_stepwise": "tree"}.get(algo, algo)
@@ -200,7 +207,7 @@ def test_random_plans(ar, block):
             x = W.uniform_inputs(n, count, dtype, config=int(rng.integers(1 << 20)))
             for r in range(n):
                 src = np.ascontiguousarray(x[r])
-                bufs[r].copy_(torch.from_numpy(src.view(np.int16) if dtype == "bf16" else src))
+                bufs[r].copy_(torch.from_numpy(src.view(np.int16) if dtype in HALF else src))
             ar.check(plan.run(), what)
             torch.cuda.synchronize()
             with np.errstate(all="ignore"):
@@ -233,7 +240,7 @@ def test_random_host_buffer_calls(ar, block):
     for case in range(10):
         n = int(rng.choice([1, 2, 3, 4, 8, 16, 64]))
         count = int(rng.choice([1, n + 1, int(rng.integers(1, 3000)), int(rng.integers(3000, 60000))]))
-        dtype = str(rng.choice(["f32", "bf16", "i32"]))
+        dtype = str(rng.choice(["f32", "bf16", "i32", "f16"]))
         algos = ["ring", "naive", "dbtree"] + (["tree"] if n & (n - 1) == 0 else [])
         algo = str(rng.choice(algos))
         op = str(rng.choice(["sum", "max"] + ([] if dtype == "i32" else ["avg"])))
@@ -242,11 +249,12 @@ def test_random_host_buffer_calls(ar, block):
         piece = int(rng.choice([0, 64, int(rng.integers(1, 5000))]))
         x = (W.random_bits(n, count, dtype, int(rng.integers(1 << 20))) if op != "sum" or dtype == "i32"
              else W.normal_inputs(n, count, 1.0, int(rng.integers(1 << 20))) if dtype == "f32"
-             else W.large_inputs(n, count, config=int(rng.integers(1 << 20))))
+             else W.large_inputs(n, count, config=int(rng.integers(1 << 20))) if dtype == "bf16"
+             else W.uniform_inputs(n, count, "f16", config=int(rng.integers(1 << 20))))
         with np.errstate(all="ignore"):
             want, _ = oracle.allreduce(x, algo=algo, op=op, dtype=dtype)
         shifts = shifts_for(rng, n, dtype)
-        a = np.ascontiguousarray(x).view(np.int16) if dtype == "bf16" else np.ascontiguousarray(x)
+        a = np.ascontiguousarray(x).view(np.int16) if dtype in HALF else np.ascontiguousarray(x)
         block_t = torch.zeros((n, count + 8), dtype=TORCH[dtype])
         if pinned:
             block_t = block_t.pin_memory()
@@ -260,4 +268,4 @@ def test_random_host_buffer_calls(ar, block):
         torch.cuda.synchronize()
         for r in range(n):
             got = rows[r].numpy()
-            assert same_bits(got.view(np.uint16) if dtype == "bf16" else got, want[r], dtype), f"{what} rank {r}"
+            assert same_bits(got.view(np.uint16) if dtype in HALF else got, want[r], dtype), f"{what} rank {r}"

@@ -24,12 +24,13 @@ def ar():
     return binding
 
 
-TORCH_DT = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32}
+TORCH_DT = {"f32": torch.float32, "bf16": torch.int16, "i32": torch.int32, "f16": torch.int16}
+HALF = ("bf16", "f16")
 
 
 def host_rows(x, dtype, pinned):
     a = np.ascontiguousarray(x)
-    if dtype == "bf16":
+    if dtype in HALF:
         a = a.view(np.int16)
     t = torch.from_numpy(a.copy())
     return t.pin_memory() if pinned else t
@@ -37,7 +38,7 @@ def host_rows(x, dtype, pinned):
 
 def as_np(t, dtype):
     a = t.numpy()
-    return a.view(np.uint16) if dtype == "bf16" else a
+    return a.view(np.uint16) if dtype in HALF else a
 
 
 def inputs(n, count, dtype, seed):
@@ -45,17 +46,19 @@ def inputs(n, count, dtype, seed):
         return W.uniform_inputs(n, count, "i32", config=seed)
     if dtype == "bf16":
         return W.large_inputs(n, count, config=seed)
+    if dtype == "f16":
+        return W.uniform_inputs(n, count, "f16", config=seed)
     return W.normal_inputs(n, count, 1.0, seed)
 
 
 def same_bits(got, want, dtype):
-    bits = {"bf16": np.uint16, "f32": np.uint32, "i32": np.uint32}[dtype]
+    bits = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32, "i32": np.uint32}[dtype]
     return np.array_equal(np.asarray(got).view(bits), np.asarray(want).view(bits))
 
 
 @pytest.mark.parametrize("mode", ["staged", "zero_copy"])
 @pytest.mark.parametrize("algo", ["ring", "tree", "naive", "dbtree"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_host_allreduce_matches_oracle(ar, algo, dtype, mode):
     for n in (2, 3, 8, 16):
         if algo == "tree" and n & (n - 1):

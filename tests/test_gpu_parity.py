@@ -41,10 +41,15 @@ def to_dev(row: np.ndarray) -> "torch.Tensor":
 
 def from_dev(bufs, dtype):
     out = np.stack([b.cpu().numpy() for b in bufs]) if bufs else np.zeros((0, 0))
-    return out.view(np.uint16) if dtype == "bf16" else out
+    return out.view(np.uint16) if dtype in HALF else out
+
+
+HALF = ("bf16", "f16")  # dtypes stored as 16-bit patterns
 
 
 def f64(x, dtype):
+    if dtype == "f16":
+        return np.ascontiguousarray(x, dtype=np.uint16).view(np.float16).astype(np.float64)
     if dtype == "bf16":
         return (np.asarray(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return np.asarray(x).astype(np.float64)
@@ -59,7 +64,7 @@ def assert_same(got, want, dtype, what=""):
     else:
         gv, wv = f64(got, dtype), f64(want, dtype)
         gn, wn = np.isnan(gv), np.isnan(wv)
-        bits = np.uint16 if dtype == "bf16" else np.uint32
+        bits = np.uint16 if dtype in HALF else np.uint32
         bad = (gn != wn) | (~gn & ~wn & (got.view(bits) != want.view(bits)))
     if bad.any():
         idx = np.argwhere(bad)
@@ -85,6 +90,8 @@ def inputs(n, count, dtype, kind, seed):
         return W.uniform_inputs(n, count, "i32", config=seed)
     if dtype == "bf16":
         return W.large_inputs(n, count, config=seed)
+    if dtype == "f16":
+        return W.normal_inputs(n, count, 1.0, seed).astype(np.float16).view(np.uint16)
     return W.normal_inputs(n, count, 1.0, seed)
 
 
@@ -104,7 +111,7 @@ def counts_for(n):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 @pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 32, 64])
 def test_allreduce_matches_oracle(ar, algo, dtype, n):
     if algo.startswith("tree") and n & (n - 1):
@@ -121,7 +128,7 @@ def test_allreduce_matches_oracle(ar, algo, dtype, n):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_allreduce_special_values(ar, algo, dtype):
     # NaN, infinities, subnormals, signed zeros in every position
     for n in (2, 4, 8):
@@ -135,7 +142,7 @@ def test_allreduce_special_values(ar, algo, dtype):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_reduce_scatter_matches_oracle(ar, algo, dtype):
     for n in (2, 3, 4, 8, 16):
         if algo.startswith("tree") and n & (n - 1):
@@ -151,7 +158,7 @@ def test_reduce_scatter_matches_oracle(ar, algo, dtype):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_all_gather_copies_bits(ar, algo, dtype):
     for n in (2, 3, 4, 8, 16):
         if algo.startswith("tree") and n & (n - 1):
@@ -162,7 +169,7 @@ def test_all_gather_copies_bits(ar, algo, dtype):
             bufs = [to_dev(x[r]) for r in range(n)]
             ar.check(ar.ar_all_gather(bufs, count=count, dtype=dtype, algo=algo), "all_gather")
             got = from_dev(bufs, dtype)
-            bits = {"bf16": np.uint16, "f32": np.uint32, "i32": np.uint32}[dtype]
+            bits = {"bf16": np.uint16, "f16": np.uint16, "f32": np.uint32, "i32": np.uint32}[dtype]
             assert np.array_equal(got.view(bits), want.view(bits)), (algo, n, count)
 
 
@@ -171,7 +178,7 @@ def test_all_gather_copies_bits(ar, algo, dtype):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("algo", ALGOS + ["dbtree", "naive"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_unaligned_buffers(ar, algo, dtype):
     """Element-aligned but not 16-byte aligned buffers.  The same offset in
     every rank takes the vector path cut at that offset; different offsets
@@ -180,7 +187,7 @@ def test_unaligned_buffers(ar, algo, dtype):
     n, count = 8, 5000 + 2048 * 8 + 3
     x = inputs(n, count, dtype, "values", seed=9)
     want, _ = oracle.allreduce(x, algo=ORACLE_ALGO.get(algo, algo), op="sum", dtype=dtype)
-    vec = 8 if dtype == "bf16" else 4
+    vec = 8 if dtype in HALF else 4
     layouts = [[s] * n for s in range(1, vec)] + [[r % vec for r in range(n)], [(3 * r + 1) % vec for r in range(n)]]
     for shifts in layouts:
         big = [to_dev(np.concatenate([x[r][:shifts[r]], x[r]])) for r in range(n)]
@@ -194,7 +201,7 @@ def test_unaligned_buffers(ar, algo, dtype):
 
 
 @pytest.mark.parametrize("n", [16, 32, 64])
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_unaligned_wide_rings(ar, n, dtype):
     """The 16-, 32- and 64-rank ring kernels with every buffer at the same
     offset from 16 bytes (vectors cut at that offset, scalar head and tail),
@@ -203,7 +210,7 @@ def test_unaligned_wide_rings(ar, n, dtype):
     x = inputs(n, count, dtype, "values", seed=31 + n)
     want, _ = oracle.allreduce(x, algo="ring", op="sum", dtype=dtype)
     want_rs, _ = oracle.reduce_scatter(x, algo="ring", op="sum", dtype=dtype)
-    shift = 3 if dtype == "bf16" else 1
+    shift = 3 if dtype in HALF else 1
     for fn in ("ar_allreduce", "ar_reduce_scatter"):
         big = [to_dev(np.concatenate([x[r][:shift], x[r]])) for r in range(n)]
         views = [b[shift:] for b in big]
@@ -220,11 +227,11 @@ def test_unaligned_wide_rings(ar, n, dtype):
             assert np.array_equal(from_dev([big[r][:shift]], dtype)[0], x[r, :shift])
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_unaligned_reduce_scatter_all_gather_broadcast(ar, dtype):
     n, count = 4, 3 * 2048 * 4 + 77
     x = inputs(n, count, dtype, "values", seed=19)
-    vec = 8 if dtype == "bf16" else 4
+    vec = 8 if dtype in HALF else 4
     for shifts in ([3] * n, [r % vec for r in range(n)]):
         def views_of(data):
             big = [to_dev(np.concatenate([data[r][:shifts[r]], data[r]])) for r in range(n)]
@@ -443,6 +450,23 @@ def test_bucketed_small_full_compare(ar):
 # --------------------------------------------------------------------------
 
 @pytest.mark.slow
+def test_f16_step_exhaustive(ar):
+    all16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    block = 1 << 12  # values of `a` per block: 2^28 pairs
+    a_dev = torch.empty(block << 16, dtype=torch.int16, device="cuda")
+    b_dev = torch.empty(block << 16, dtype=torch.int16, device="cuda")
+    b_row = torch.from_numpy(all16.view(np.int16)).cuda().repeat(block)
+    for a0 in range(0, 1 << 16, block):
+        a_vals = np.repeat(all16[a0:a0 + block], 1 << 16)
+        a_dev.copy_(torch.from_numpy(a_vals.view(np.int16)))
+        b_dev.copy_(b_row)
+        ar.check(ar.ar_allreduce([a_dev, b_dev], count=a_vals.size, dtype="f16", op="sum", algo="ring"), "pairs")
+        torch.cuda.synchronize()
+        got = a_dev.cpu().numpy().view(np.uint16)
+        want = oracle.step(a_vals, np.tile(all16, block), op="sum", dtype="f16")
+        assert_same(got, want, "f16", f"a block {a0}")
+
+
 def test_bf16_step_exhaustive(ar):
     all16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     block = 1 << 12  # values of `a` per block: 2^28 pairs
@@ -492,7 +516,7 @@ def test_barrier_timeout_is_reported(ar, algo, count):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("algo", ["ring", "tree", "naive"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_reduce_matches_oracle(ar, algo, dtype):
     for n in (2, 3, 5, 8, 16):
         if algo == "tree" and n & (n - 1):
@@ -511,7 +535,7 @@ def test_reduce_matches_oracle(ar, algo, dtype):
                     assert np.array_equal(got[others].view(np.uint8), x[others].view(np.uint8))  # untouched
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_naive_allreduce_matches_oracle(ar, dtype):
     for n in (2, 3, 8, 64):
         for count in (1, 4099, 70_001):
@@ -525,7 +549,7 @@ def test_naive_allreduce_matches_oracle(ar, dtype):
     assert ar.ar_reduce_scatter(bufs, count=100, dtype=dtype, algo="naive") == ar.AR_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_broadcast_copies_bits(ar, dtype):
     for n in (2, 3, 8, 16):
         for count in (1, 4099, 3 * 2048 + 7):
@@ -545,7 +569,7 @@ def test_broadcast_copies_bits(ar, dtype):
 # Double binary tree
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 @pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 64])
 def test_dbtree_matches_oracle(ar, dtype, n):
     for count in [c for c in (1, 2, n + 1, 4099, 2 * 2048 * n + 11) if c > 0]:
