@@ -414,9 +414,11 @@ def test_bucketed_small_full_compare(ar):
     g = np.random.Generator(np.random.PCG64(21))
     counts = [5, 300, 17, 1024, 3, 999, 64, 4096 + 3, 1, 2048]
     for n in (2, 3, 8):
-        for dtype in ("f32", "bf16"):
+        for dtype in ("f32", "bf16", "f16"):
             if dtype == "f32":
                 host = [[g.standard_normal(c).astype(np.float32) for c in counts] for _ in range(n)]
+            elif dtype == "f16":
+                host = [[g.standard_normal(c).astype(np.float16).view(np.uint16) for c in counts] for _ in range(n)]
             else:
                 host = [[W.f32_to_bf16_bits_truncate(g.standard_normal(c).astype(np.float32)) for c in counts]
                         for _ in range(n)]
@@ -440,7 +442,7 @@ def test_bucketed_small_full_compare(ar):
                     for r in range(n):
                         for t in range(len(counts)):
                             got = grads[r][t].cpu().numpy()
-                            if dtype == "bf16":
+                            if dtype in HALF:
                                 got = got.view(np.uint16)
                             assert_same(got, want[r][t], dtype, f"{algo} literal={literal} n={n} r={r} t={t}")
 

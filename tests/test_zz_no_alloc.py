@@ -42,6 +42,8 @@ def make_grads(seed, dtype):
             x = g.standard_normal(c).astype(np.float32) * np.float32(1e-3)
             if dtype == "bf16":
                 x = (x.view(np.uint32) >> 16).astype(np.uint16).view(np.int16)
+            elif dtype == "f16":
+                x = x.astype(np.float16).view(np.int16)
             row.append(torch.from_numpy(x).cuda())
         out.append(row)
     return out
@@ -52,7 +54,7 @@ def bits(t):
     return a.view(np.uint16) if a.dtype == np.int16 else a.view(np.uint32)
 
 
-@pytest.mark.parametrize("dtype,op,algo", [("f32", "avg", "ring"), ("bf16", "sum", "tree")])
+@pytest.mark.parametrize("dtype,op,algo", [("f32", "avg", "ring"), ("bf16", "sum", "tree"), ("f16", "avg", "ring")])
 def test_noalloc_matches_bucketed_allreduce_twice(ar, dtype, op, algo):
     for call in range(2):
         grads = make_grads(100 + call, dtype)
