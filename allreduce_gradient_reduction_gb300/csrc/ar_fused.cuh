@@ -36,12 +36,10 @@ constexpr int kFusedBlock = 256;
 // ranks every order keeps two groups of 8 rank loads in flight.  The ring
 // then gets 3 (at 2 it was 1.9% slower on 64 x 64 MiB; at 3 as fast as one
 // group at a time at 4 blocks per SM, and twice as fast for calls of
-// 4-64 KiB).  The trees, which also hold finished subtrees, and the bf16
-// and f16 maximum, which need more temporaries, get 2 (128 registers),
-// without spills.
-__host__ __device__ constexpr int fused_min_blocks(int order, int nr, int dt, int op) {
-  return nr > 8 ? (order == RING && !((dt == BF16 || dt == F16) && op == MAX) ? 3 : 2)
-                : (order == DBTREE && nr == 8 ? 3 : 4);
+// 4-64 KiB).  The trees, which also hold finished subtrees, get 2 (128
+// registers), without spills.
+__host__ __device__ constexpr int fused_min_blocks(int order, int nr) {
+  return nr > 8 ? (order == RING ? 3 : 2) : (order == DBTREE && nr == 8 ? 3 : 4);
 }
 __host__ __device__ constexpr int fused_unroll(int order, int nr) {
   return (nr == 2) ? 2 : 1;
@@ -116,7 +114,7 @@ __device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
 }
 
 template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR, DT, OP)) fused_vec_kernel(const __grid_constant__ ARGS a) {
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int U = fused_unroll(ORDER, NR);
