@@ -96,6 +96,9 @@ def test_argument_checks_without_device(ar):
     assert ar.ar_allreduce([(1 << 20) + 2, 1 << 21], count=4, stream=0) == ar.AR_ERR_INVALID_ARG  # misaligned f32
     assert ar.ar_allreduce([0, 1 << 21], count=4, stream=0) == ar.AR_ERR_INVALID_ARG
     assert ar.ar_allreduce([1 << 20, 1 << 21], count=4, dtype=7, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce([1 << 20, 1 << 21], count=4, dtype=4, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.DTYPE["f16"] == 3 and "AR_F16 = 3" in open(HEADER).read()
+    assert ar.ar_allreduce([1 << 20, (1 << 20) + 4], count=4, dtype="f16", stream=0) == ar.AR_ERR_INVALID_ARG  # overlap
     assert ar.ar_allreduce([1 << 20, 1 << 21], count=4, algo=9, stream=0) == ar.AR_ERR_INVALID_ARG
     assert ar.lib.ar_device_status(None, None) == ar.AR_ERR_INVALID_ARG
     rc = ar.ar_bucket_plan([5, 6], "f32", 0)[0]
