@@ -309,24 +309,59 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
   }
 }
 
-// Same computation one element per thread, for buffers that are not all
-// 16-byte aligned.
+// Same computation element by element, for rows whose buffers sit at
+// different addresses modulo 16.  Each thread takes kScalarUnroll elements of
+// a tile, kFusedBlock apart.  In ring order (the naive order too) it walks the
+// ranks once for all of them, so their loads from each rank are in flight
+// together; the trees fold each element on its own.  Measured with every rank
+// at a different offset: 8 x 128 MiB bf16 SUM 1030 us at one element per
+// thread, 623 at two, 560 at four, 1052 at eight; 8 x 25 MiB f32 AVG 118.8,
+// 86.0, 83.0 and 139.6 us.
+constexpr int kScalarUnroll = 4;
+
 template <class ARGS, int DT, int OP, int ORDER>
 __global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
+  constexpr int SU = kScalarUnroll;
   const auto& T = a.tab;
   const int n = T.nranks;
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
-    const int64_t e = s.begin + (tile - s.tile_begin) * kFusedBlock + threadIdx.x;
-    if (e >= s.end) continue;
+    const int64_t e0 = s.begin + (tile - s.tile_begin) * (int64_t)kFusedBlock * SU + threadIdx.x;
+    if (e0 >= s.end) continue;
     const void* const* P = T.ptr + (size_t)s.tensor * n;
-    uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, s.chunk, e);
-    if (a.avg) r = div_word<DT>(r, a.fn);
-    if (a.owner_only || a.to_root) {
-      st_elem<ES>(const_cast<void*>(P[a.owner_only ? s.chunk : a.root]), e, r);
+    uint32_t r[SU];
+    bool ok[SU];
+#pragma unroll
+    for (int u = 0; u < SU; ++u) ok[u] = e0 + (int64_t)u * kFusedBlock < s.end;
+    if constexpr (ORDER == RING) {
+      const void* src = P[rot(s.chunk + 1, n)];
+#pragma unroll
+      for (int u = 0; u < SU; ++u)
+        if (ok[u]) r[u] = ld_elem<ES>(src, e0 + (int64_t)u * kFusedBlock);
+#pragma unroll 1
+      for (int p = 1; p < n; ++p) {
+        src = P[rot(s.chunk + 1 + p, n)];
+#pragma unroll
+        for (int u = 0; u < SU; ++u)
+          if (ok[u]) r[u] = step_word<DT, OP>(r[u], ld_elem<ES>(src, e0 + (int64_t)u * kFusedBlock));
+      }
     } else {
-      for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+#pragma unroll
+      for (int u = 0; u < SU; ++u)
+        if (ok[u]) r[u] = fold_scalar<DT, OP, ORDER>(P, n, s.chunk, e0 + (int64_t)u * kFusedBlock);
+    }
+#pragma unroll
+    for (int u = 0; u < SU; ++u) {
+      if (!ok[u]) continue;
+      const int64_t e = e0 + (int64_t)u * kFusedBlock;
+      uint32_t v = r[u];
+      if (a.avg) v = div_word<DT>(v, a.fn);
+      if (a.owner_only || a.to_root) {
+        st_elem<ES>(const_cast<void*>(P[a.owner_only ? s.chunk : a.root]), e, v);
+      } else {
+        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, v);
+      }
     }
   }
 }
@@ -386,7 +421,7 @@ cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
 
 template <int DT, int OP, int ORDER, class ARGS>
 cudaError_t launch_fused_scalar(ARGS& a, cudaStream_t stream) {
-  if (fill_tiles(a.tab, 1, kFusedBlock) == 0) return cudaSuccess;
+  if (fill_tiles(a.tab, 1, (int64_t)kFusedBlock * kScalarUnroll) == 0) return cudaSuccess;
   fused_scalar_kernel<ARGS, DT, OP, ORDER><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
