@@ -154,18 +154,57 @@ bool all_aligned16(void* const* p, int n) {
   return true;
 }
 
+// ---- the current context's identity --------------------------------------------
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class FN>
+FN driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    p = nullptr;
+  return reinterpret_cast<FN>(p);
+}
+
+int context_id(unsigned long long* id) {
+  static CtxGetCurrentFn cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn getid = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  *id = 0;
+  if (!cur || !getid) return cuda_fail(cudaErrorNotSupported);
+  CUcontext c = nullptr;
+  if (cur(&c) != CUDA_SUCCESS) return cuda_fail(cudaErrorDeviceUninitialized);
+  if (c && getid(c, id) != CUDA_SUCCESS) return cuda_fail(cudaErrorDeviceUninitialized);
+  return AR_OK;
+}
+
 // ---- per-device barrier block for the step-wise kernels ------------------------
 
+// One block per device, allocated on first use and tagged with the context it
+// was allocated in: a context that was torn down (cudaDeviceReset) took the
+// block with it, so a new context gets a new one.
 std::mutex g_sync_mu;
 ar::SyncBlock* g_sync[256] = {};
+unsigned long long g_sync_ctx[256] = {};
 
 int sync_block(ar::SyncBlock** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= 256) return AR_ERR_NO_DEVICE;
+  unsigned long long ctx = 0;
+  int rc = context_id(&ctx);
+  if (rc) return rc;
+  if (ctx == 0) {
+    // no context current on this thread yet: let the runtime bind its own
+    // (cudaFree of NULL frees nothing), then ask again
+    if ((e = cudaFree(nullptr)) != cudaSuccess) return cuda_fail(e);
+    if ((rc = context_id(&ctx))) return rc;
+  }
   std::lock_guard<std::mutex> lk(g_sync_mu);
-  if (!g_sync[dev]) {
+  if (!g_sync[dev] || g_sync_ctx[dev] != ctx) {
     void* p = nullptr;
     if ((e = cudaMalloc(&p, sizeof(ar::SyncBlock))) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemset(p, 0, sizeof(ar::SyncBlock))) != cudaSuccess) {
@@ -173,6 +212,7 @@ int sync_block(ar::SyncBlock** out) {
       return cuda_fail(e);
     }
     g_sync[dev] = static_cast<ar::SyncBlock*>(p);
+    g_sync_ctx[dev] = ctx;
   }
   *out = g_sync[dev];
   return AR_OK;
@@ -494,6 +534,10 @@ int plan_buckets(const int64_t* counts, int ntensors, int dtype, int64_t cap, in
 namespace ar {
 // Lets other translation units report a CUDA failure the same way.
 int note_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
+  return ::check_common(nranks, count, dtype, op, algo);
+}
+int current_context_id(unsigned long long* id) { return context_id(id); }
 
 std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -1039,9 +1083,13 @@ int ar_device_status(ar_stream_t stream, int* status) {
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
     *status = AR_OK;
     ar::SyncBlock* sb = nullptr;
+    unsigned long long ctx = 0;
+    int rc = context_id(&ctx);
+    if (rc) return rc;
     {
+      // a block from a context that no longer exists holds no status
       std::lock_guard<std::mutex> lk(g_sync_mu);
-      if (dev >= 0 && dev < 256) sb = g_sync[dev];
+      if (dev >= 0 && dev < 256 && g_sync_ctx[dev] == ctx) sb = g_sync[dev];
     }
     if (!sb) return AR_OK;
     int v = 0;

@@ -124,6 +124,18 @@ cudaError_t launch_int8_ef(Int8Args& args, cudaStream_t stream);
 
 int sm_count();
 
+// ar_api.cpp helpers that other translation units share.
+// The argument rules every collective entry point applies (ranges of nranks,
+// count, dtype, op and algo; AVG on i32 and trees of other than 2^k ranks are
+// AR_ERR_UNSUPPORTED).
+int check_common(int nranks, int64_t count, int dtype, int op, int algo);
+// Records a CUDA failure for ar_last_cuda_error and maps it to a status.
+int note_cuda_failure(cudaError_t e);
+// Unique id of the context current on this thread (0 if none is current).
+// Device addresses the library caches per device are keyed by it, so a
+// context that was torn down (cudaDeviceReset) and replaced is noticed.
+int current_context_id(unsigned long long* id);
+
 // Counts every kernel launch the library enqueues (ar_kernel_launches).
 void count_launch();
 

@@ -27,10 +27,6 @@
 // (rounded down to 256 bytes) that holds the packed buckets of that rank.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[AR_NOALLOC_SCRATCH_BYTES];
 
-namespace ar {
-int note_cuda_failure(cudaError_t e);  // ar_api.cpp: records the error for ar_last_cuda_error
-}
-
 namespace {
 
 using ar::Seg;
@@ -50,7 +46,10 @@ int32_t g_bucket_of[kMaxTensors];
 int64_t g_offset[kMaxTensors];
 int64_t g_bcount[kMaxTensors];
 int64_t g_base[kMaxTensors];
-unsigned char* g_scratch_addr[256];  // device address of the scratch, per device ordinal
+// Device address of the scratch, per device ordinal, and the context it was
+// looked up in (the address belongs to that context's copy of the module).
+unsigned char* g_scratch_addr[256];
+unsigned long long g_scratch_ctx[256];
 
 typedef CUresult (*PointerGetAttributeFn)(void*, CUpointer_attribute, CUdeviceptr);
 
@@ -102,14 +101,22 @@ int check_ranges(int n, int esize, int dev) {
 
 // Set-up, once per device, with that device current: the device address of
 // the scratch array.  (In host code the array's name is only a host-side
-// stand-in, not a device address.)
+// stand-in, not a device address.)  The address is cached per device together
+// with the id of the context it was looked up in; if that context has since
+// been torn down and replaced (cudaDeviceReset), the module was loaded again,
+// possibly elsewhere, and the address is looked up anew.
 int scratch_address(int dev, unsigned char** out) {
   if (dev < 0 || dev >= 256) return AR_ERR_NO_DEVICE;
-  if (!g_scratch_addr[dev]) {
+  unsigned long long ctx = 0;
+  int rc = ar::current_context_id(&ctx);
+  if (rc) return rc;
+  if (ctx == 0 || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // binds the device's context if none is current
     if (e != cudaSuccess) return ar::note_cuda_failure(e);
+    if ((rc = ar::current_context_id(&ctx))) return rc;
     g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return AR_OK;
@@ -119,19 +126,18 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
 int64_t chunk_lo(int64_t count, int n, int c) { return (int64_t)(((__int128)c * count) / n); }
 
-}  // namespace
-
-extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* counts, int ntensors, int nranks,
-                                             ar_dtype dtype, ar_op op, ar_algo algo, int64_t bucket_cap_bytes,
-                                             ar_stream_t stream_) {
-  cudaStream_t stream = (cudaStream_t)stream_;
-  if (nranks < 1 || nranks > AR_MAX_RANKS || ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
-  if (dtype < AR_F32 || dtype > AR_F16 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
-  if (algo < AR_RING || algo > AR_TREE_STEPWISE) return AR_ERR_INVALID_ARG;
+int noalloc_body(void* const* grads, const int64_t* counts, int ntensors, int nranks, ar_dtype dtype, ar_op op,
+                 ar_algo algo, int64_t bucket_cap_bytes, cudaStream_t stream) {
+  // the argument rules of ar_bucketed_allreduce: out-of-range values are
+  // AR_ERR_INVALID_ARG; AVG on i32, trees of other than 2^k ranks, and the
+  // orders the bucketed call does not take (naive, double binary tree) are
+  // AR_ERR_UNSUPPORTED
+  int rc = ar::check_common(nranks, 0, dtype, op, algo);
+  if (rc) return rc;
+  if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
   // the step-wise kernels need a barrier block the library would allocate
   if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
-  if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
-  if (algo == AR_TREE && (nranks & (nranks - 1))) return AR_ERR_UNSUPPORTED;
+  if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
   if (ntensors == 0) return AR_OK;
   if (!grads || !counts) return AR_ERR_INVALID_ARG;
   if (ntensors > kMaxTensors) return AR_ERR_TOO_LARGE;
@@ -139,7 +145,7 @@ extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* 
 
   std::lock_guard<std::mutex> lk(g_mu);
   int32_t nb = 0;
-  int rc = ar_bucket_plan(counts, ntensors, dtype, bucket_cap_bytes, g_bucket_of, g_offset, g_bcount, &nb);
+  rc = ar_bucket_plan(counts, ntensors, dtype, bucket_cap_bytes, g_bucket_of, g_offset, g_bcount, &nb);
   if (rc) return rc;
   // per-rank slice of the scratch, and whether the largest bucket fits in it
   const int64_t slice = ((int64_t)AR_NOALLOC_SCRATCH_BYTES / nranks) & ~(int64_t)255;
@@ -264,4 +270,18 @@ extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* 
     b0 = b1;
   }
   return AR_OK;
+}
+
+}  // namespace
+
+// Nothing may unwind through the C ABI: an exception (the lock can throw)
+// becomes AR_ERR_HOST, as in every other entry point.
+extern "C" int ar_bucketed_allreduce_noalloc(void* const* grads, const int64_t* counts, int ntensors, int nranks,
+                                             ar_dtype dtype, ar_op op, ar_algo algo, int64_t bucket_cap_bytes,
+                                             ar_stream_t stream) {
+  try {
+    return noalloc_body(grads, counts, ntensors, nranks, dtype, op, algo, bucket_cap_bytes, (cudaStream_t)stream);
+  } catch (...) {
+    return AR_ERR_HOST;
+  }
 }

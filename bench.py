@@ -20,7 +20,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -34,8 +33,10 @@ METRIC = "simulated-AllReduce algbw & effective HBM GB/s (frac of GB300 peak), 1
 WORKLOAD = "ring AllReduce SUM, 8 ranks x 67,108,864 bf16 (128 MiB per rank)"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("ar_fused.cuh", "ar_device.cuh", "ar_fused_bf16_sum.cu")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fused_ring_bf16_8x128MiB.md")
-
+# DRAM bytes per launch of the headline kernel from one ncu capture, with the
+# hash of the kernel sources it was taken on (machine-readable; the summary
+# beside it gives the command)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "headline_traffic.json")
 
 def parse():
     p = argparse.ArgumentParser()
@@ -48,6 +49,8 @@ def parse():
     p.add_argument("--cpu-procs", type=int, default=0,
                    help="processes for the CPU oracle baseline (default: every host core)")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip timing the small, bucket and GPT-2 configurations beside the headline")
     p.add_argument("--count", type=int, default=0,
                    help="elements per rank (default: the full workload); smaller counts are for profiling")
     p.add_argument("--variants", action="store_true", help="also time tree and step-wise orders (extra keys)")
@@ -181,17 +184,17 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    """DRAM bytes per launch from the committed ncu capture, if it was taken
     on the kernel source as it is now."""
     try:
-        text = open(PROFILE_SUMMARY, encoding="utf-8").read()
-    except OSError:
+        with open(TRAFFIC_FILE, encoding="utf-8") as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return int(m_bytes.group(1))
+    v = rec.get("dram_bytes_per_launch")
+    return int(v) if isinstance(v, int) else None
 
 
 # ---------------------------------------------------------------------------
@@ -205,99 +208,41 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def _oracle_worker(conn):
-    """One process of OraclePool: holds its element range of the input and
-    runs the oracle's ring AllReduce on it on request, through the oracle's
-    sampled-positions mode (an element's fold depends only on its own column
-    and its chunk)."""
-    import numpy as np
-    import oracle
-    oracle.lib()
-    x = pos = count = out = None
-    while True:
-        msg = conn.recv()
-        if msg[0] == "load":
-            _, x, lo, count = msg
-            pos = np.arange(lo, lo + x.shape[1], dtype=np.int64)
-            conn.send(0.0)
-        elif msg[0] == "run":
-            t0 = time.perf_counter()
-            out, _ = oracle.allreduce(x, algo="ring", op="sum", dtype="bf16", count=count, positions=pos)
-            conn.send(time.perf_counter() - t0)
-        elif msg[0] == "digest":
-            # the last pass's result on this range: digest of rank 0's values
-            # and whether every rank holds the same
-            import hashlib
-            conn.send((hashlib.sha256(np.ascontiguousarray(out[0]).tobytes()).hexdigest(),
-                       bool(all(np.array_equal(out[r], out[0]) for r in range(out.shape[0])))))
-        else:
-            return
-
-
-class OraclePool:
-    """The oracle, as it stands, on every host core: each spawned process (never
-    forked, so no CUDA state is inherited) keeps one element range of the
-    input, loaded before any timing, so a timed pass moves no data between
-    processes."""
-
-    def __init__(self, procs: int):
-        import multiprocessing as mp
-        ctx = mp.get_context("spawn")
-        self.conns, self.procs = [], []
-        for _ in range(procs):
-            a, b = ctx.Pipe()
-            p = ctx.Process(target=_oracle_worker, args=(b,), daemon=True)
-            p.start()
-            self.conns.append(a)
-            self.procs.append(p)
-
-    def load(self, x):
-        import numpy as np
-        count = x.shape[1]
-        b = np.linspace(0, count, len(self.conns) + 1).astype(np.int64)
-        for i, c in enumerate(self.conns):
-            c.send(("load", np.ascontiguousarray(x[:, b[i]:b[i + 1]]), int(b[i]), count))
-        for c in self.conns:
-            c.recv()
-        return [int(b[i + 1] - b[i]) for i in range(len(self.conns))]
-
-    def digests(self):
-        """Per process: (sha256 of rank 0's result on its range, ranks identical)."""
-        for c in self.conns:
-            c.send(("digest",))
-        return [c.recv() for c in self.conns]
-
-    def run(self):
-        """One pass over the whole input; returns (wall seconds, per-process seconds)."""
-        t0 = time.perf_counter()
-        for c in self.conns:
-            c.send(("run",))
-        per = [c.recv() for c in self.conns]
-        return time.perf_counter() - t0, per
-
-    def close(self):
-        for c in self.conns:
-            c.send(("stop",))
-        for p in self.procs:
-            p.join(timeout=60)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def oracle_pass_time(x, procs: int, passes: int, gpu_result=None):
     """Time the oracle's ring AllReduce over the bf16 bit patterns x (n x count)
-    on `procs` processes: one untimed pass, then `passes` timed ones.  Returns
-    (seconds per pass, GB/s in the metric, median GB/s of one process on its
-    own range, parity) -- parity compares the oracle's result with
-    `gpu_result` (rank 0's result of the same inputs on the GPU, or None) by
-    digest, range by range."""
-    import hashlib
-    import numpy as np
+    on `procs` processes (each holding one element range): one untimed pass,
+    then `passes` timed ones.  Returns (seconds per pass, GB/s in the metric,
+    median GB/s of one process on its own range, parity) -- parity compares
+    the oracle's result with `gpu_result` (rank 0's result of the same inputs
+    on the GPU, or None) range by range."""
     import oracle
+    from oracle import parallel as oracle_parallel
     oracle.build()
     n, count = x.shape
-    pool = OraclePool(procs)
     parity = None
-    try:
-        widths = pool.load(x)
+    with oracle_parallel.Pool(procs) as pool:
+        widths = pool.load(x, algo="ring", op="sum", dtype="bf16")
         pool.run()
         total, per = 0.0, [0.0] * procs
         for _ in range(passes):
@@ -305,15 +250,8 @@ def oracle_pass_time(x, procs: int, passes: int, gpu_result=None):
             total += dt
             per = [a + b for a, b in zip(per, p)]
         if gpu_result is not None:
-            got = pool.digests()
-            lo, same = 0, True
-            for w, (digest, ranks_equal) in zip(widths, got):
-                mine = hashlib.sha256(np.ascontiguousarray(gpu_result[lo:lo + w]).tobytes()).hexdigest()
-                same = same and ranks_equal and mine == digest
-                lo += w
-            parity = {"vs": "oracle", "elements": int(count), "ranges": len(widths), "bit_identical": bool(same)}
-    finally:
-        pool.close()
+            parity = pool.compare(gpu_result)
+            parity.pop("differing_ranges", None)
     per_gbs = sorted(2 * n * w * 2 * passes / max(t, 1e-9) / 1e9 for w, t in zip(widths, per))
     dt = total / passes
     return dt, 2 * n * count * 2 / dt / 1e9, per_gbs[len(per_gbs) // 2], parity
@@ -330,16 +268,14 @@ def run_reference(args, ws, rank):
     oracle.build()
     x = W.large_inputs(n, sample)
     procs = args.cpu_procs or host_cores()
-    pool = OraclePool(procs)
-    try:
-        pool.load(x)
+    from oracle import parallel as oracle_parallel
+    with oracle_parallel.Pool(procs) as pool:
+        pool.load(x, algo="ring", op="sum", dtype="bf16")
         for _ in range(args.warmup):
             pool.run()
         total = 0.0
         for _ in range(args.steps):
             total += pool.run()[0]
-    finally:
-        pool.close()
     dt = total / max(args.steps, 1)
     value = 2 * n * sample * 2 / dt / 1e9
     line = {
@@ -348,7 +284,7 @@ def run_reference(args, ws, rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "nranks": n, "count_per_rank": W.LARGE["count"],
                    "sample_count_per_rank": sample, "algo": "ring", "op": "sum"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": procs, "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"{n} ranks x {sample} bf16 per step (1/{W.LARGE['count'] // sample} of the "
                                    f"workload), literal message simulation, element ranges split over {procs} "
                                    "processes"},
@@ -550,7 +486,8 @@ class LargeWorkload:
         passes = 3
         res = gpu_result.view(np.uint16) if gpu_result is not None else None
         dt, gbs, one, parity = oracle_pass_time(self.host.numpy().view(np.uint16), procs, passes, res)
-        return {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle", "one_process_gbs": one,
+        return {"value": gbs, "unit": "GB/s", "cores": procs, "kind": "oracle", "cpu_model": cpu_model(),
+                "one_process_gbs": one,
                 "sample": f"the whole workload ({self.n} ranks x {self.count} bf16), literal ring passes: "
                           f"1 untimed + {passes} timed at {dt:.3f} s each, element ranges split over "
                           f"{procs} processes",
@@ -615,6 +552,7 @@ class BucketWorkload:
             same = all(np.array_equal(out[r].view(np.uint32), gpu_result.view(np.uint32)) for r in range(self.n))
             parity = {"vs": "oracle", "elements": int(self.count), "bit_identical": bool(same)}
         return {"value": self.bytes_step / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "cpu_model": cpu_model(),
                 "sample": f"the whole workload, one literal ring pass, {dt:.2f} s, one thread", "parity": parity}
 
 
@@ -781,18 +719,33 @@ class Gpt2Workload:
                         "one GPU"}
 
     def cpu_baseline(self, gpu_result=None):
+        """The oracle's literal bucketed AllReduce (pack, ring, unpack) over the
+        whole workload, one bucket per process at a time on every host core;
+        its per-tensor digests check the GPU's result of the same inputs."""
+        import numpy as np
         import oracle
-        from allreduce_gradient_reduction_gb300 import workloads as W
+        from oracle import parallel as oracle_parallel
         oracle.build()
-        counts = self.counts[-50:]  # the last four blocks and the final norm: the first buckets DDP reduces
-        grads = [W.gpt2_rank_grads(r, self.counts)[-50:] for r in range(self.n)]
+        host = self.host.numpy()
+        offs = np.concatenate([[0], np.cumsum(self.counts)])
+        grads = [[host[r, offs[t]:offs[t + 1]] for t in range(len(self.counts))] for r in range(self.n)]
+        procs = self.args.cpu_procs or host_cores()
         t0 = time.perf_counter()
-        oracle.bucketed_allreduce(grads, op="avg", dtype="f32")
+        with oracle_parallel.Pool(procs) as pool:
+            want, slowest = pool.bucketed_digests(grads, op="avg", dtype="f32", cap_bytes=25 << 20)
         dt = time.perf_counter() - t0
-        nbytes = 2 * self.n * int(counts.sum()) * 4
-        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"last 50 of 148 tensors ({int(counts.sum())} params per rank), literal pack, "
-                          f"ring, unpack, {dt:.2f} s, one thread"}
+        parity = None
+        if gpu_result is not None:
+            same = all(oracle_parallel.digest(gpu_result[offs[t]:offs[t + 1]]) == want[0][t]
+                       for t in range(len(self.counts)))
+            parity = {"vs": "oracle", "elements": int(self.total), "tensors": len(self.counts),
+                      "bit_identical": bool(same)}
+        return {"value": self.bytes_step / dt / 1e9, "unit": "GB/s", "cores": procs, "kind": "oracle",
+                "cpu_model": cpu_model(),
+                "sample": f"the whole workload (8 ranks x {self.total} f32, 17 buckets), literal pack, ring, unpack, "
+                          f"buckets spread over {procs} processes: {dt:.2f} s wall (includes sending the inputs), "
+                          f"slowest process {slowest:.2f} s",
+                "parity": parity}
 
 
 # ---------------------------------------------------------------------------
@@ -963,6 +916,109 @@ def end_to_end(wl, args, ws, stream, torch):
 
 
 # ---------------------------------------------------------------------------
+# the other configurations, timed beside the headline
+# ---------------------------------------------------------------------------
+
+def timed_calls(call, k, stream, torch, warm=3):
+    """Milliseconds per call over k back-to-back calls (CUDA events on the
+    launching stream, after `warm` untimed calls), and the wall window."""
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(k):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / k, (t0, time.time())
+
+
+def other_workloads(dev, torch, np, W, ar, stream, clocks, peak):
+    """The small, bucket and GPT-2 configurations, each timed the way the
+    headline is (CUDA events over back-to-back calls on the launching stream),
+    with the clocks sampled during each window."""
+    sid = int(stream.cuda_stream)
+    out = {}
+
+    def chk(rc, what):
+        if rc:
+            raise ar.ArError(rc, what)
+
+    # small: 4 ranks x 4096 f32 integers, ring SUM -- latency bound (L2 resident)
+    n, count = W.SMALL["nranks"], W.SMALL["count"]
+    x = W.small_inputs(n, count)
+    bufs = [torch.from_numpy(x[r]).to(dev) for r in range(n)]
+    call = lambda s=sid: chk(ar.ar_allreduce(bufs, count=count, dtype="f32", op="sum", algo="ring", stream=s), "small")
+    eager_ms, win = timed_calls(call, 2000, stream, torch)
+    plan = ar.Plan("allreduce", bufs, count=count, dtype="f32", op="sum", algo="ring")
+    plan_ms, _ = timed_calls(lambda: chk(plan.run(sid), "small plan"), 2000, stream, torch)
+    plan.close()
+    graph_us = graph_time(lambda s: ar.ar_allreduce(bufs, count=count, dtype="f32", op="sum", algo="ring", stream=s),
+                          torch, stream, reps=50)
+    nbytes = 2 * n * count * 4
+    out["small"] = {"workload": "ring AllReduce SUM, 4 ranks x 4096 f32 (integers in [-8, 8])",
+                    "us_per_call_eager": eager_ms * 1e3, "us_per_call_prepared": plan_ms * 1e3,
+                    "us_per_call_graph": graph_us, "algorithmic_bytes": nbytes,
+                    "note": "latency bound and L2 resident: eager = one ar_allreduce through the binding per call "
+                            "(host-bound), prepared = ar_plan_run, graph = 50 calls replayed from a CUDA graph "
+                            "(device time)", "clocks": clocks.summary(*win)}
+    del bufs
+
+    # bucket: 8 ranks x 6,553,600 f32 (one 25 MiB DDP bucket), ring AVG, then MAX on the same data
+    n, count = W.BUCKET["nranks"], W.BUCKET["count"]
+    x = W.bucket_inputs(n, count)
+    bufs = [torch.from_numpy(x[r]).to(dev) for r in range(n)]
+    nbytes = 2 * n * count * 4
+    for op in ("avg", "max"):
+        ms, win = timed_calls(lambda: chk(ar.ar_allreduce(bufs, count=count, dtype="f32", op=op, algo="ring",
+                                                          stream=sid), "bucket"), 200, stream, torch)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[f"bucket_{op}"] = {"workload": f"ring AllReduce {op.upper()}, 8 ranks x 6,553,600 f32 (one 25 MiB bucket)",
+                               "ms_per_step": ms, "effective_gbs": gbs, "frac": gbs / peak,
+                               "algorithmic_bytes": nbytes, "clocks": clocks.summary(*win)}
+    del bufs
+
+    # GPT-2 small gradients in 25 MiB reverse-order buckets, AVG: fused and literal
+    counts = W.gpt2_small_counts()
+    total = int(counts.sum())
+    n = W.GPT2["nranks"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(W.BASE_SEED + 1000 * W.CONFIG_GPT2)
+    flats = [torch.randn(total, device=dev, generator=gen).mul_(1e-4) for _ in range(n)]
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    grads = [[f[offs[t]:offs[t + 1]] for t in range(len(counts))] for f in flats]
+    ws = [torch.empty(total, device=dev) for _ in range(n)]
+    nbytes = 2 * n * total * 4
+    for mode in ("fused", "literal"):
+        w, wb = (ws, total * 4) if mode == "literal" else (None, 0)
+        launches0 = ar.ar_kernel_launches()
+        chk(ar.ar_bucketed_allreduce(grads, counts=counts, dtype="f32", op="avg", algo="ring", workspace=w,
+                                     workspace_bytes=wb, stream=sid), "gpt2")
+        per_step = ar.ar_kernel_launches() - launches0
+        ms, win = timed_calls(lambda: chk(ar.ar_bucketed_allreduce(grads, counts=counts, dtype="f32", op="avg",
+                                                                   algo="ring", workspace=w, workspace_bytes=wb,
+                                                                   stream=sid), "gpt2"),
+                              40 if mode == "fused" else 20, stream, torch)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        rec = {"workload": "DDP bucketed AllReduce AVG, 8 ranks x GPT-2 small gradients (148 tensors, "
+                           f"{total:,} f32, 17 buckets of <= 25 MiB), {mode}",
+               "ms_per_step": ms, "effective_gbs": gbs, "frac": gbs / peak, "algorithmic_bytes": nbytes,
+               "launches_per_step": per_step, "clocks": clocks.summary(*win)}
+        if mode == "literal":
+            rec["moved_bytes"] = 3 * nbytes  # pack, AllReduce, unpack: each 2 N P b
+            rec["moved_gbs"] = 3 * gbs
+        out[f"gpt2_{mode}"] = rec
+    del flats, grads, ws
+    torch.cuda.empty_cache()
+    out["note"] = ("each timed like the headline (CUDA events over back-to-back calls); bucket and small inputs "
+                   "from the seeded host recipe, GPT-2 gradients drawn on the device (normal(0, 1e-4)); frac is "
+                   "of the measured copy bandwidth")
+    return out
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -1026,7 +1082,6 @@ def main():
     launches = ar.ar_kernel_launches() - launches0
     barrier(ws)
     ms_local = e0.elapsed_time(e1) / args.steps
-    clocks.stop()
     ms = max_over_ranks(ms_local, ws)
     rc, status = ar.ar_device_status(sid)
     if rc or status:
@@ -1046,7 +1101,6 @@ def main():
 
     value = ws * nbytes_step / (ms / 1e3) / 1e9
     algbw = nbytes_step / (2 * wl.n) / (ms / 1e3) / 1e9
-    peak, peak_kind = hbm_peak()
     # one step is `launches / steps` kernels; the roofline is per step of the hot path
     achieved = nbytes_step / (ms_local / 1e3) / 1e9
 
@@ -1057,6 +1111,13 @@ def main():
             e2e = end_to_end_host_call(wl, args, ws, stream, torch)
         else:  # bucketed and step-wise calls: device-buffer calls with the copies around them
             e2e = end_to_end(wl, args, ws, stream, torch)
+
+    peak, peak_kind = hbm_peak()
+    others = None
+    if (isinstance(wl, LargeWorkload) and not args.count and not args.no_workloads and rank == 0
+            and args.algo == "ring"):
+        others = other_workloads(dev, torch, np, W, ar, stream, clocks, peak)
+    clocks.stop()
 
     variants = {}
     if args.variants:
@@ -1143,6 +1204,8 @@ def main():
             "clocks": clocks.summary(t_wall0, t_wall1),
             "cpu_baseline": cpu,
         }
+        if others:
+            line["workloads"] = others
         if variants:
             line["variants"] = variants
         if overlap:

@@ -305,7 +305,9 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
  * no cudaMalloc/cudaFree and no other allocating call, on the device or the
  * host heap.
  *   algo   AR_RING or AR_TREE; the step-wise orders need a barrier block the
- *          library would allocate, so they return AR_ERR_UNSUPPORTED here.
+ *          library would allocate, so they return AR_ERR_UNSUPPORTED here, as
+ *          do AR_NAIVE and AR_DBTREE (which ar_bucketed_allreduce does not
+ *          take either); a value outside ar_algo is AR_ERR_INVALID_ARG.
  * Other arguments and errors as ar_bucketed_allreduce (without workspace).
  * The array is shared by all calls and keeps the last call's contents (every
  * byte this call reads from it, it has written first, so nothing needs
@@ -317,7 +319,10 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
  * (with CUDA's default lazy module loading, from the first call on that GPU).
  * The first call on each device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress, no allocation); make that
- * first call before any stream capture.
+ * first call before any stream capture.  The address is remembered together
+ * with the context it belongs to: after the device's context has been torn
+ * down and replaced (cudaDeviceReset), the next call looks it up again (that
+ * call, too, should come before any capture).
  */
 #define AR_NOALLOC_SCRATCH_BYTES (32 << 20)
 #define AR_NOALLOC_MAX_TENSORS 1024

@@ -2,16 +2,20 @@
 
 Integers, MAX and the fixed-order f32/bf16 folds must match bit for bit (NaN
 compared as NaN, payload-free); AllGather must copy bits exactly.  Sizes span
-several tiles and ragged tails; the full-size workloads are checked on sampled
-positions (plus every chunk boundary) that the oracle carries through its
-message simulation, and by properties that hold at any size."""
+several tiles and ragged tails.  The full-size workloads (8 x 128 MiB bf16 in
+ring and tree order, GPT-2 small's gradients in 25 MiB buckets) are compared
+with the oracle on every element (the oracle's runs split over host
+processes), and element by element on sampled positions plus every chunk
+boundary."""
 import math
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
 
 import oracle
 from allreduce_gradient_reduction_gb300 import workloads as W
+from oracle import parallel as oracle_parallel
 
 pytestmark = pytest.mark.gpu
 
@@ -343,57 +347,92 @@ def sample_positions(count, n, k, seed):
 
 
 @pytest.mark.slow
-def test_large_workload_sampled(ar):
+def test_large_workload_full_compare(ar):
     """8 ranks x 67,108,864 bf16, the configuration the benchmark times, in
-    the same call; checked on sampled positions and by whole-buffer
-    properties."""
+    ring and in tree order: every element of the result compared with the
+    oracle (oracle processes on every host core, each carrying one element
+    range through the full simulation, compared by digests of the ranges),
+    every rank identical, and on sampled positions plus every chunk boundary
+    +-2 the values one by one and the bf16 error bound."""
     n, count = W.LARGE["nranks"], W.LARGE["count"]
     x = W.large_inputs(n, count)
     pos = sample_positions(count, n, 1 << 16, 5)
     xs = np.ascontiguousarray(x[:, pos])
-    for algo in ("ring", "tree"):
-        want, _ = oracle.allreduce(xs, algo=algo, op="sum", dtype="bf16", count=count, positions=pos)
-        bufs = [to_dev(x[r]) for r in range(n)]
-        ar.check(ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo=algo), algo)
-        torch.cuda.synchronize()
-        for r in range(1, n):
-            assert torch.equal(bufs[r], bufs[0]), (algo, r)  # every rank identical
-        got = bufs[0][torch.from_numpy(pos).cuda()].cpu().numpy().view(np.uint16)
-        assert_same(got, want[0], "bf16", algo)
-        # bf16 error stays within the recursive-summation bound gamma_k * sum|x|
-        xv = f64(xs, "bf16")
-        depth = n - 1 if algo == "ring" else int(math.log2(n))
-        u = 2.0 ** -8
-        err = np.abs(f64(got, "bf16") - xv.sum(axis=0))
-        assert np.all(err <= depth * u / (1 - depth * u) * np.abs(xv).sum(axis=0))
-        del bufs
+    with oracle_parallel.Pool() as pool:
+        pool.load(x, op="sum", dtype="bf16")
+        for algo in ("ring", "tree"):
+            want, _ = oracle.allreduce(xs, algo=algo, op="sum", dtype="bf16", count=count, positions=pos)
+            bufs = [to_dev(x[r]) for r in range(n)]
+            ar.check(ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo=algo), algo)
+            torch.cuda.synchronize()
+            for r in range(1, n):
+                assert torch.equal(bufs[r], bufs[0]), (algo, r)  # every rank identical
+            got = bufs[0][torch.from_numpy(pos).cuda()].cpu().numpy().view(np.uint16)
+            assert_same(got, want[0], "bf16", algo)
+            # bf16 error stays within the recursive-summation bound gamma_k * sum|x|
+            xv = f64(xs, "bf16")
+            depth = n - 1 if algo == "ring" else int(math.log2(n))
+            u = 2.0 ** -8
+            err = np.abs(f64(got, "bf16") - xv.sum(axis=0))
+            assert np.all(err <= depth * u / (1 - depth * u) * np.abs(xv).sum(axis=0))
+            # every element against the oracle's full run
+            res0 = bufs[0].cpu().numpy().view(np.uint16)
+            del bufs
+            pool.run(algo=algo)
+            cmp = pool.compare(res0)
+            assert cmp["bit_identical"] and cmp["elements"] == count, (algo, cmp)
+
+
+def bucket_boundary_samples(counts, n, cap=25 << 20, dtype="f32"):
+    """(tensor, index) of every bucket chunk boundary +-2 and every tensor's
+    first and last two elements, from the oracle's bucket plan: the places
+    where the fused bucketed kernel switches segments and rank order."""
+    bucket_of, offset, bcount = oracle.bucket_plan(counts, dtype=dtype, cap_bytes=cap)
+    tid, idx = [], []
+    for t, c in enumerate(counts):
+        if c == 0:
+            continue
+        B, o = int(bcount[bucket_of[t]]), int(offset[t])
+        cand = [0, 1, c - 2, c - 1]
+        for k in range(n + 1):
+            lo = oracle.chunk_range(B, n, k)[0] if k < n else B
+            cand += list(range(lo - o - 2, lo - o + 3))
+        for i in sorted(set(cand)):
+            if 0 <= i < c:
+                tid.append(t)
+                idx.append(i)
+    return np.array(tid, dtype=np.int32), np.array(idx, dtype=np.int64)
 
 
 @pytest.mark.slow
-def test_gpt2_bucketed_fused_and_literal(ar):
+def test_gpt2_bucketed_full_compare(ar):
+    """GPT-2 small gradients, 8 ranks, 25 MiB buckets, AVG: the fused,
+    literal (whole and per-bucket workspace) and step-wise paths, each compared
+    with the oracle's bucketed AllReduce on every element of every tensor of
+    every rank (the oracle split by bucket over host processes, compared by
+    digests), and element by element on every bucket chunk boundary +-2."""
     n = W.GPT2["nranks"]
     counts = W.gpt2_small_counts()
     host = [W.gpt2_rank_grads(r, counts) for r in range(n)]
+    with oracle_parallel.Pool() as pool:
+        want_digest, _ = pool.bucketed_digests(host, op="avg", dtype="f32", cap_bytes=25 << 20)
+    tid, idx = bucket_boundary_samples(counts, n)
     g = np.random.Generator(np.random.PCG64(8))
-    tid = g.integers(0, counts.size, size=20000).astype(np.int32)
-    idx = (g.random(tid.size) * counts[tid]).astype(np.int64)
-    # every tensor's first and last element too
-    tid = np.concatenate([tid, np.arange(counts.size), np.arange(counts.size)]).astype(np.int32)
-    idx = np.concatenate([idx, np.zeros(counts.size, np.int64), counts - 1])
-    pairs = np.unique(np.stack([tid, idx], axis=1), axis=0)
+    rt = g.integers(0, counts.size, size=4000).astype(np.int32)
+    ri = (g.random(rt.size) * counts[rt]).astype(np.int64)
+    pairs = np.unique(np.stack([np.concatenate([tid, rt]), np.concatenate([idx, ri])], axis=1), axis=0)
     tid, idx = pairs[:, 0].astype(np.int32), pairs[:, 1].astype(np.int64)
     want, _ = oracle.bucketed_allreduce(host, op="avg", dtype="f32", samples=(tid, idx))
 
     flat_len = int(counts.sum())
-    results = {}
+    offs = np.concatenate([[0], np.cumsum(counts)])
     for mode in ("fused", "whole", "per_bucket", "stepwise"):
         # one flat allocation per rank with the tensors as views into it
         flats = [torch.from_numpy(np.concatenate(host[r])).cuda() for r in range(n)]
-        offs = np.concatenate([[0], np.cumsum(counts)])
         grads = [[flats[r][offs[t]:offs[t + 1]] for t in range(counts.size)] for r in range(n)]
         ws, wbytes = None, 0
         if mode in ("whole", "per_bucket"):
-            per = flat_len if mode == "whole" else int(max(ar.ar_bucket_plan(counts, "f32")[3]))
+            per = flat_len if mode == "whole" else int(max(oracle.bucket_plan(counts, dtype="f32")[2]))
             ws = [torch.empty(per, dtype=torch.float32, device="cuda") for _ in range(n)]
             wbytes = per * 4
         algo = "ring_stepwise" if mode == "stepwise" else "ring"
@@ -404,10 +443,16 @@ def test_gpt2_bucketed_fused_and_literal(ar):
         sel = torch.from_numpy(offs[tid] + idx).cuda()
         got = np.stack([flats[r][sel].cpu().numpy() for r in range(n)])
         assert_same(got, want, "f32", mode)
-        results[mode] = flats[0].cpu().numpy()
+        host_res = [f.cpu().numpy() for f in flats]
         del flats, grads, ws
-    for mode in ("whole", "per_bucket", "stepwise"):
-        assert np.array_equal(results[mode].view(np.uint32), results["fused"].view(np.uint32)), mode
+
+        def rank_digests(r):
+            return [oracle_parallel.digest(host_res[r][offs[t]:offs[t + 1]]) for t in range(counts.size)]
+        with ThreadPoolExecutor(max_workers=n) as ex:
+            got_digest = list(ex.map(rank_digests, range(n)))
+        bad = [(r, t) for r in range(n) for t in range(counts.size) if got_digest[r][t] != want_digest[r][t]]
+        assert not bad, (mode, f"{len(bad)} (rank, tensor) results differ from the oracle, first {bad[:5]}")
+        del host_res
 
 
 def test_bucketed_small_full_compare(ar):
