@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_HERE, "libar_gb300.so")
 
 DTYPE = {"f32": 0, "bf16": 1, "i32": 2, "f16": 3}
 OP = {"sum": 0, "max": 1, "avg": 2}
-ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3, "naive": 4, "dbtree": 5}
+ALGO = {"ring": 0, "ring_stepwise": 1, "tree": 2, "tree_stepwise": 3, "naive": 4, "dbtree": 5,
+        "binomial_stepwise": 6}
 STATUS = {0: "AR_OK", -1: "AR_ERR_INVALID_ARG", -2: "AR_ERR_UNSUPPORTED", -3: "AR_ERR_CUDA",
           -4: "AR_ERR_TIMEOUT", -5: "AR_ERR_NO_DEVICE", -6: "AR_ERR_TOO_LARGE", -7: "AR_ERR_HOST"}
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4

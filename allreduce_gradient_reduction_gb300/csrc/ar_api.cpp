@@ -32,6 +32,10 @@ int esize_of(int dtype) { return (dtype == AR_BF16 || dtype == AR_F16) ? 2 : 4; 
 
 bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
+bool is_stepwise(int algo) {
+  return algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE || algo == AR_BINOMIAL_STEPWISE;
+}
+
 // Chunk c of `count` elements split n ways: [floor(c*count/n), floor((c+1)*count/n)).
 int64_t chunk_lo(int64_t count, int n, int c) { return (int64_t)(((__int128)c * count) / n); }
 
@@ -121,9 +125,10 @@ int check_mapped_host(std::vector<Range>& rs, int esize) {
 int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
   if (nranks < 1 || nranks > AR_MAX_RANKS || count < 0 || count > AR_MAX_COUNT) return AR_ERR_INVALID_ARG;
   if (dtype < AR_F32 || dtype > AR_F16 || op < AR_SUM || op > AR_AVG) return AR_ERR_INVALID_ARG;
-  if (algo < AR_RING || algo > AR_DBTREE) return AR_ERR_INVALID_ARG;
+  if (algo < AR_RING || algo > AR_BINOMIAL_STEPWISE) return AR_ERR_INVALID_ARG;
   if (op == AR_AVG && dtype == AR_I32) return AR_ERR_UNSUPPORTED;
-  if ((algo == AR_TREE || algo == AR_TREE_STEPWISE) && !is_pow2(nranks)) return AR_ERR_UNSUPPORTED;
+  if ((algo == AR_TREE || algo == AR_TREE_STEPWISE || algo == AR_BINOMIAL_STEPWISE) && !is_pow2(nranks))
+    return AR_ERR_UNSUPPORTED;
   return AR_OK;
 }
 
@@ -318,13 +323,14 @@ void fill_fused(const Job& j, int nranks, ARGS& a) {
 
 int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   const int dop = j.op == AR_MAX ? ar::MAX : ar::SUM;
-  const bool stepwise = j.algo == AR_RING_STEPWISE || j.algo == AR_TREE_STEPWISE;
+  const bool stepwise = is_stepwise(j.algo);
   const int order = j.algo == AR_DBTREE ? ar::DBTREE
+                    : j.algo == AR_BINOMIAL_STEPWISE ? ar::BINOMIAL
                     : (j.algo == AR_TREE || j.algo == AR_TREE_STEPWISE) ? ar::TREE : ar::RING;
   cudaError_t e;
   // element updates in the busiest phase: the chunk's count for the ring,
-  // N/2 pairs of it in the first tree step
-  const int64_t phase_elems = j.row_count * (order == ar::TREE ? tab.nranks / 2 : 1);
+  // N/2 pairs of it in the first tree or binomial step
+  const int64_t phase_elems = j.row_count * (order == ar::TREE || order == ar::BINOMIAL ? tab.nranks / 2 : 1);
   if (stepwise && j.row_count > 0 && phase_elems <= ar::kSmemStepMaxPhaseElems &&
       ar::smem_step_bytes(tab.nranks, j.row_count, esize_of(j.dtype)) <= ar::kSmemStepBytes) {
     // a small row: the whole schedule in one block's shared memory (no grid
@@ -447,8 +453,9 @@ int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, in
   *empty = false;
   int rc = check_common(nranks, count, dtype, phases == 2 ? AR_SUM : op, algo);
   if (rc) return rc;
-  if ((algo == AR_NAIVE || algo == AR_DBTREE) && phases != 3) return AR_ERR_UNSUPPORTED;  // AllReduce / Reduce only
-  if (algo == AR_DBTREE && root >= 0) return AR_ERR_UNSUPPORTED;
+  if ((algo == AR_NAIVE || algo == AR_DBTREE || algo == AR_BINOMIAL_STEPWISE) && phases != 3)
+    return AR_ERR_UNSUPPORTED;  // AllReduce / Reduce only
+  if ((algo == AR_DBTREE || algo == AR_BINOMIAL_STEPWISE) && root >= 0) return AR_ERR_UNSUPPORTED;  // AllReduce only
   if (!bufs_checked && (rc = check_bufs(bufs, nranks, count, dtype))) return rc;
   if (count == 0 || nranks == 1) {
     *empty = true;
@@ -462,6 +469,9 @@ int build_collective(void* const* bufs, int nranks, int64_t count, int dtype, in
     // tree A reduces the first half (chunk id 0), tree B the second (1)
     tb.add_seg(row, 0, count / 2, 0);
     tb.add_seg(row, count / 2, count, 1);
+  } else if (algo == AR_BINOMIAL_STEPWISE) {
+    // whole buffers move in every step: one segment
+    tb.add_seg(row, 0, count, 0);
   } else {
     for (int c = 0; c < nranks; ++c) tb.add_seg(row, chunk_lo(count, nranks, c), chunk_lo(count, nranks, c + 1), c);
   }
@@ -629,7 +639,7 @@ int ar_reduce(void* const* bufs, int nranks, int64_t count, ar_dtype dtype, ar_o
               ar_stream_t stream) {
   return guarded([&]() -> int {
     if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
-    if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+    if (is_stepwise(algo)) return AR_ERR_UNSUPPORTED;
     return collective(bufs, nranks, count, dtype, op, algo, 3, (cudaStream_t)stream, root);
   });
 }
@@ -654,7 +664,7 @@ int ar_allreduce_host(void* const* host_bufs, void* const* dev_bufs, int nranks,
   return guarded([&]() -> int {
     int rc = check_common(nranks, count, dtype, op, algo);
     if (rc) return rc;
-    if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+    if (is_stepwise(algo)) return AR_ERR_UNSUPPORTED;
     if (!host_bufs || piece_elems < 0) return AR_ERR_INVALID_ARG;
     if (count == 0) return AR_OK;  // nothing is accessed
     const int es = esize_of(dtype);
@@ -783,7 +793,7 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
     cudaStream_t stream = (cudaStream_t)stream_;
     int rc = check_common(nranks, 0, dtype, op, algo);
     if (rc) return rc;
-    if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
+    if (algo == AR_NAIVE || algo == AR_DBTREE || algo == AR_BINOMIAL_STEPWISE) return AR_ERR_UNSUPPORTED;
     if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
     if (ntensors == 0) return AR_OK;
     if (!grads || !counts) return AR_ERR_INVALID_ARG;
@@ -905,7 +915,7 @@ int ar_reducer_create(void* const* grads, const int64_t* counts, int ntensors, i
     *out = nullptr;
     int rc = check_common(nranks, 0, dtype, op, algo);
     if (rc) return rc;
-    if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
+    if (algo == AR_NAIVE || algo == AR_DBTREE || algo == AR_BINOMIAL_STEPWISE) return AR_ERR_UNSUPPORTED;
     if (ntensors < 1 || bucket_cap_bytes <= 0 || !grads || !counts) return AR_ERR_INVALID_ARG;
     const int es = esize_of(dtype);
     ar_reducer* red = new ar_reducer;
@@ -1028,7 +1038,7 @@ int ar_plan_create(int kind, void* const* bufs, int nranks, int64_t count, ar_dt
       case AR_PLAN_ALL_GATHER: phases = 2, root = -1, op = AR_SUM; break;
       case AR_PLAN_REDUCE:
         if (root < 0 || root >= nranks) return AR_ERR_INVALID_ARG;
-        if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+        if (is_stepwise(algo)) return AR_ERR_UNSUPPORTED;
         break;
       default: return AR_ERR_INVALID_ARG;
     }

@@ -113,31 +113,165 @@ __device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
   return acc;
 }
 
-template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fused_vec_kernel(const __grid_constant__ ARGS a) {
+// ---- rows whose buffers sit at different addresses modulo 16 -----------------
+//
+// The row's first buffer sets the frame: vector v covers elements
+// [v*VEC - shift, (v+1)*VEC - shift), shift = row_shift(P[0]).  In buffer p
+// those elements begin `off_p` = (P[p] - P[0]) mod 16 bytes into an aligned
+// 16-byte word and run into the next word.  Every lane of a warp loads, from
+// every buffer, the aligned word holding the start of its vector and takes
+// the next word from the lane above (a shuffle); lanes 0..30 fold, lane 31
+// only loads.  Results go back the same way: the aligned word of buffer q
+// that begins off_q bytes before vector v holds the end of vector v-1 (from
+// the lane below, a shuffle) and the start of v.  Warps start 30 vectors
+// apart, so neighbouring warps of a block both fold the vector where they
+// meet; a warp writes its vectors 0..29 to the buffers at the frame's phase,
+// and the words that begin in its vectors 1..30 to the others, whole.  A
+// block barrier between the folds and the stores keeps every warp's reads
+// before any warp's writes.  A block writes only the elements of its own
+// tile: the words at a tile's two ends are written in part, the rest of
+// each by the neighbouring tile (or, at a segment's ends, by the element-wise
+// edge code).  Bytes of a loaded word outside the tile are never used, so no
+// value a block uses was written by another block.
+constexpr int kShiftWarpVecs = 30;  // vectors a warp owns (it folds one more)
+constexpr int kShiftTileVecs = (kFusedBlock / 32) * kShiftWarpVecs;
+
+__device__ __forceinline__ int byte_phase(const void* p, const void* p0) {
+  return (int)(((uintptr_t)p - (uintptr_t)p0) & 15);
+}
+
+// Bytes [OFF, OFF + 16) of the 32 bytes lo:hi (little-endian).
+template <int OFF>
+__device__ __forceinline__ uint4 bytes_at_c(const uint4& lo, const uint4& hi) {
+  constexpr int K = OFF >> 2, SH = (OFF & 3) * 8;
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  if constexpr (SH == 0) {
+    return make_uint4(w[K], w[K + 1], w[K + 2], w[K + 3]);
+  } else {
+    return make_uint4(__funnelshift_r(w[K], w[K + 1], SH), __funnelshift_r(w[K + 1], w[K + 2], SH),
+                      __funnelshift_r(w[K + 2], w[K + 3], SH), __funnelshift_r(w[K + 3], w[K + 4], SH));
+  }
+}
+
+// The same for a runtime offset (a multiple of the element size in [0, 16),
+// the same in every lane of the warp): one branch to a fixed shift.
+template <int ES>
+__device__ __forceinline__ uint4 bytes_at(const uint4& lo, const uint4& hi, int off) {
+  switch (off) {
+    case 4: return bytes_at_c<4>(lo, hi);
+    case 8: return bytes_at_c<8>(lo, hi);
+    case 12: return bytes_at_c<12>(lo, hi);
+    default: break;
+  }
+  if constexpr (ES == 2) {
+    switch (off) {
+      case 2: return bytes_at_c<2>(lo, hi);
+      case 6: return bytes_at_c<6>(lo, hi);
+      case 10: return bytes_at_c<10>(lo, hi);
+      case 14: return bytes_at_c<14>(lo, hi);
+      default: break;
+    }
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, int k) {
+  return k < 2 ? (k == 0 ? a0 : a1) : (k == 2 ? a2 : a3);
+}
+
+__device__ __forceinline__ uint4 shfl_down4(const uint4& v) {
+  return make_uint4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                    __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+}
+__device__ __forceinline__ uint4 shfl_up4(const uint4& v) {
+  return make_uint4(__shfl_up_sync(0xffffffffu, v.x, 1), __shfl_up_sync(0xffffffffu, v.y, 1),
+                    __shfl_up_sync(0xffffffffu, v.z, 1), __shfl_up_sync(0xffffffffu, v.w, 1));
+}
+
+// Bytes [lo, hi) of the aligned 16-byte word at `w` get bytes [lo, hi) of v
+// (lo, hi multiples of 2), as naturally aligned 8-, 4- and 2-byte stores.
+__device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, int hi) {
+  int pos = lo;
+  while (pos < hi) {
+    const int k = pos >> 2;
+    if ((pos & 7) == 0 && pos + 8 <= hi) {
+      __stcs(reinterpret_cast<uint2*>(w + pos), make_uint2(pick4(v.x, v.y, v.z, v.w, k), pick4(v.y, v.z, v.w, v.w, k)));
+      pos += 8;
+    } else if ((pos & 3) == 0 && pos + 4 <= hi) {
+      __stcs(reinterpret_cast<unsigned int*>(w + pos), pick4(v.x, v.y, v.z, v.w, k));
+      pos += 4;
+    } else {
+      __stcs(reinterpret_cast<unsigned short*>(w + pos),
+             (unsigned short)(pick4(v.x, v.y, v.z, v.w, k) >> ((pos & 2) * 8)));
+      pos += 2;
+    }
+  }
+}
+
+__host__ __device__ constexpr int fused_min_blocks_shift(int order, int nr) {
+  return order == DBTREE && nr == 8 ? 2 : 3;
+}
+
+// SHIFT: the row's buffers need not share their address modulo 16 (see
+// above); otherwise they do, and every rank is read and written in aligned
+// 16-byte vectors at the same offset.
+template <class ARGS, int DT, int OP, int ORDER, int NR, bool SHIFT>
+__global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(ORDER, NR) : fused_min_blocks(ORDER, NR))
+    fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
-  constexpr int U = fused_unroll(ORDER, NR);
-  constexpr int TILE_V = kFusedBlock * U;
+  constexpr int U = SHIFT ? 1 : fused_unroll(ORDER, NR);
+  constexpr int TILE_V = SHIFT ? kShiftTileVecs : kFusedBlock * U;
+  static_assert(!SHIFT || NR <= 8, "mixed-phase rows of more than 8 ranks take the runtime-N ring");
   const auto& T = a.tab;
   const int n = NR > 0 ? NR : T.nranks;
+  const int lane = threadIdx.x & 31;
 
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
     const void* const* P = T.ptr + (size_t)s.tensor * n;
-    const int shift = row_shift(P[0], ES);  // the row's buffers share it
+    const int shift = row_shift(P[0], ES);  // the row's frame (all its buffers share it unless SHIFT)
     const SegShape sh = seg_shape<VEC>(s, shift);
     const int64_t ti = tile - s.tile_begin;
     const int c = s.chunk;
 
     // position u of this thread is byte offset base + u * kStride in every
-    // rank, 16-byte aligned in all of them
-    const int64_t v0 = sh.vb + ti * TILE_V + threadIdx.x;
+    // rank, 16-byte aligned in all of them (SHIFT: in the first buffer)
+    const int64_t v0 = sh.vb + ti * TILE_V + (SHIFT ? (threadIdx.x >> 5) * kShiftWarpVecs + lane : threadIdx.x);
     const int64_t base = v0 * 16 - shift * ES;
     constexpr int64_t kStride = (int64_t)kFusedBlock * 16;
+    // SHIFT: the tile's vectors are [t0, t1)
+    const int64_t t0 = sh.vb + ti * TILE_V;
+    const int64_t t1 = SHIFT ? (t0 + TILE_V < sh.ve ? t0 + TILE_V : sh.ve) : sh.ve;
+    // ok: this lane folds position u (SHIFT: lanes 0..30, inside the tile)
     bool ok[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < sh.ve;
+    for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < t1 && (!SHIFT || lane <= kShiftWarpVecs);
+    // SHIFT: a lane also loads when the lane below folds a vector whose end
+    // lies in this lane's word
+    const bool edge = SHIFT && lane >= 1 && v0 <= t1;
+
+    // rank rk's 16 bytes at position u (SHIFT: the aligned word holding the
+    // start of the vector), whether this lane loads them, and the vector
+    // itself once loaded (SHIFT: realigned with the word of the lane above)
+    auto ld = [&](int rk, int u) -> uint4 {
+      const char* p = static_cast<const char*>(P[rk]) + base + u * kStride;
+      if constexpr (SHIFT) p = reinterpret_cast<const char*>((uintptr_t)p & ~(uintptr_t)15);
+      return ld_stream(p);
+    };
+    auto may_ld = [&](int rk, int u) -> bool {
+      if constexpr (SHIFT) return ok[0] || (edge && byte_phase(P[rk], P[0]) != 0);
+      else return ok[u];
+    };
+    auto fix = [&](const uint4& raw, int rk) -> uint4 {
+      if constexpr (SHIFT) {
+        const int off = byte_phase(P[rk], P[0]);  // the same in every lane
+        if (off == 0) return raw;
+        return bytes_at<ES>(raw, shfl_down4(raw), off);
+      } else {
+        return raw;
+      }
+    };
 
     uint4 acc[U];
     if constexpr (ORDER == RING && NR > 8) {
@@ -167,20 +301,17 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
         }
       }
     } else if constexpr (ORDER == RING && NR > 0) {
-      const char* src[NR];
-#pragma unroll
-      for (int p = 0; p < NR; ++p) src[p] = static_cast<const char*>(P[rot(c + 1 + p, NR)]) + base;
       uint4 x[U][NR];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int p = 0; p < NR; ++p)
-          if (ok[u]) x[u][p] = ld_stream(src[p] + u * kStride);
+          if (may_ld(rot(c + 1 + p, NR), u)) x[u][p] = ld(rot(c + 1 + p, NR), u);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        acc[u] = x[u][0];
+        acc[u] = fix(x[u][0], rot(c + 1, NR));
 #pragma unroll
-        for (int p = 1; p < NR; ++p) acc[u] = step_vec<DT, OP>(acc[u], x[u][p]);
+        for (int p = 1; p < NR; ++p) acc[u] = step_vec<DT, OP>(acc[u], fix(x[u][p], rot(c + 1 + p, NR)));
       }
     } else if constexpr (ORDER == RING) {
       // any N: groups of 8 ranks in ring order, folded as they arrive
@@ -189,17 +320,21 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (g + q < n) {
-            const char* src = static_cast<const char*>(P[rot(c + 1 + g + q, n)]) + base;
+            const int rk = rot(c + 1 + g + q, n);
 #pragma unroll
             for (int u = 0; u < U; ++u)
-              if (ok[u]) x[u][q] = ld_stream(src + u * kStride);
+              if (may_ld(rk, u)) x[u][q] = ld(rk, u);
           }
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (g + q < n) {
+            const int rk = rot(c + 1 + g + q, n);
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = (g + q == 0) ? x[u][q] : step_vec<DT, OP>(acc[u], x[u][q]);
+            for (int u = 0; u < U; ++u) {
+              const uint4 v = fix(x[u][q], rk);
+              acc[u] = (g + q == 0) ? v : step_vec<DT, OP>(acc[u], v);
+            }
           }
         }
       }
@@ -212,13 +347,17 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
         uint4 x[U][NR];
 #pragma unroll
         for (int p = 0; p < NR; ++p) {
-          const char* src = static_cast<const char*>(P[rot(p + rank_shift, NR)]) + base;
+          const int rk = rot(p + rank_shift, NR);
 #pragma unroll
           for (int u = 0; u < U; ++u)
-            if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+            if (may_ld(rk, u)) x[u][p] = ld(rk, u);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int p = 0; p < NR; ++p) x[u][p] = fix(x[u][p], rot(p + rank_shift, NR));
+          acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
+        }
       } else {
         static_assert(U == 1, "one vector position per thread for wide trees");
         DbtStream<NR> st{P, base, rank_shift, ok[0], {}};
@@ -228,13 +367,16 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
       uint4 x[U][NR];
 #pragma unroll
       for (int p = 0; p < NR; ++p) {
-        const char* src = static_cast<const char*>(P[p]) + base;
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (ok[u]) x[u][p] = ld_stream(src + u * kStride);
+          if (may_ld(p, u)) x[u][p] = ld(p, u);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) acc[u] = tree_fold_regs<DT, OP, NR>(x[u]);
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int p = 0; p < NR; ++p) x[u][p] = fix(x[u][p], p);
+        acc[u] = tree_fold_regs<DT, OP, NR>(x[u]);
+      }
     } else {
       // N = 16, 32, 64: aligned subtrees of 8 ranks, each folded as it
       // arrives and merged with its finished siblings (a binary counter over
@@ -271,7 +413,34 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR)) fuse
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = div_vec<DT>(acc[u], a.fn);
     }
-    if (a.owner_only || a.to_root) {
+    if constexpr (SHIFT) {
+      // rank rk's aligned word that begins off bytes before this vector gets
+      // the end of the vector below (prev) and the start of this one
+      const uint4 prev = shfl_up4(acc[0]);
+      const bool own = ok[0] && lane < kShiftWarpVecs;  // vectors 0..29 of the warp
+      __syncthreads();  // every warp of the block has read its inputs
+      auto put = [&](int rk) {
+        char* d = static_cast<char*>(const_cast<void*>(P[rk])) + base;
+        const int off = byte_phase(P[rk], P[0]);
+        if (off == 0) {
+          if (own) st_stream(d, acc[0]);
+          return;
+        }
+        char* w = d - off;
+        if (ok[0] && lane >= 1) st_stream(w, bytes_at<ES>(prev, acc[0], 16 - off));
+        // the tile's first and last words hold elements outside it
+        if (own && v0 == t0) st_stream_part(w, bytes_at<ES>(prev, acc[0], 16 - off), off, 16);
+        if (own && v0 + 1 == t1) st_stream_part(w + 16, bytes_at<ES>(acc[0], acc[0], 16 - off), 0, off);
+      };
+      if (a.owner_only || a.to_root) {
+        put(a.owner_only ? c : a.root);
+      } else if constexpr (NR > 0) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) put(r);
+      } else {
+        for (int r = 0; r < n; ++r) put(r);
+      }
+    } else if (a.owner_only || a.to_root) {
       char* dst = static_cast<char*>(const_cast<void*>(P[a.owner_only ? c : a.root])) + base;
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -410,13 +579,41 @@ inline unsigned grid_for(int64_t ntiles, int64_t cap = 0) {
   return (unsigned)g;
 }
 
-template <int DT, int OP, int ORDER, int NR, class ARGS>
+template <int DT, int OP, int ORDER, int NR, class ARGS, bool SHIFT = false>
 cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
-  constexpr int U = fused_unroll(ORDER, NR);
-  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, (int64_t)kFusedBlock * U, true) == 0) return cudaSuccess;
-  fused_vec_kernel<ARGS, DT, OP, ORDER, NR><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
+  constexpr int U = SHIFT ? 1 : fused_unroll(ORDER, NR);
+  constexpr int64_t kTile = SHIFT ? kShiftTileVecs : (int64_t)kFusedBlock * U;
+  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kTile, true) == 0) return cudaSuccess;
+  fused_vec_kernel<ARGS, DT, OP, ORDER, NR, SHIFT><<<grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, 0, stream>>>(a);
   count_launch();
   return cudaGetLastError();
+}
+
+// Rows whose buffers sit at different addresses modulo 16 (every order up to
+// 8 ranks; rings of any size through the runtime-N form).  Returns
+// cudaErrorNotSupported where no such form is compiled (trees of 16 or more
+// ranks), for the element-wise kernel to take.
+__host__ __forceinline__ bool shift_form_exists(int order, int n) {
+  return order == RING || n == 2 || n == 4 || n == 8;
+}
+
+template <int DT, int OP, class ARGS>
+cudaError_t launch_fused_shift_typed(int order, ARGS& a, cudaStream_t stream) {
+  const int n = a.tab.nranks;
+  switch (order * 100 + n) {
+    case RING * 100 + 2: return launch_fused_vec<DT, OP, RING, 2, ARGS, true>(a, stream);
+    case RING * 100 + 4: return launch_fused_vec<DT, OP, RING, 4, ARGS, true>(a, stream);
+    case RING * 100 + 8: return launch_fused_vec<DT, OP, RING, 8, ARGS, true>(a, stream);
+    case TREE * 100 + 2: return launch_fused_vec<DT, OP, TREE, 2, ARGS, true>(a, stream);
+    case TREE * 100 + 4: return launch_fused_vec<DT, OP, TREE, 4, ARGS, true>(a, stream);
+    case TREE * 100 + 8: return launch_fused_vec<DT, OP, TREE, 8, ARGS, true>(a, stream);
+    case DBTREE * 100 + 2: return launch_fused_vec<DT, OP, DBTREE, 2, ARGS, true>(a, stream);
+    case DBTREE * 100 + 4: return launch_fused_vec<DT, OP, DBTREE, 4, ARGS, true>(a, stream);
+    case DBTREE * 100 + 8: return launch_fused_vec<DT, OP, DBTREE, 8, ARGS, true>(a, stream);
+    default: break;
+  }
+  if (order == RING) return launch_fused_vec<DT, OP, RING, 0, ARGS, true>(a, stream);
+  return cudaErrorNotSupported;
 }
 
 template <int DT, int OP, int ORDER, class ARGS>
@@ -469,6 +666,14 @@ cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream
 }
 
 }  // namespace ar
+
+#define AR_DEFINE_FUSED_SHIFT(NAME, DT, OP)                                                        \
+  namespace ar {                                                                                  \
+  cudaError_t NAME(int order, FusedArgs& a, cudaStream_t s) { return launch_fused_shift_typed<DT, OP>(order, a, s); } \
+  cudaError_t NAME(int order, SmallFusedArgs& a, cudaStream_t s) {                                \
+    return launch_fused_shift_typed<DT, OP>(order, a, s);                                         \
+  }                                                                                               \
+  }
 
 #define AR_DEFINE_FUSED(NAME, DT, OP)                                                              \
   namespace ar {                                                                                  \

@@ -9,7 +9,7 @@ namespace ar {
 
 enum Dtype { F32 = 0, BF16 = 1, I32 = 2, F16 = 3 };
 enum Op { SUM = 0, MAX = 1 };  // AVG = SUM plus the `avg` flag
-enum Order { RING = 0, TREE = 1, DBTREE = 2 };
+enum Order { RING = 0, TREE = 1, DBTREE = 2, BINOMIAL = 3 };  // BINOMIAL: step-wise kernels only
 
 constexpr int kMaxRanks = 64;
 constexpr int kPtrCap = 512;  // pointers one launch can describe
@@ -66,8 +66,8 @@ struct StepArgs {
   SegTable tab;
   SyncBlock* sync;
   int64_t timeout_ns;
-  int32_t order;      // RING or TREE
-  int32_t phases;     // bit 0 ReduceScatter, bit 1 AllGather
+  int32_t order;      // RING, TREE or BINOMIAL
+  int32_t phases;     // bit 0 ReduceScatter (BINOMIAL: reduce to rank 0), bit 1 AllGather (BINOMIAL: broadcast)
   int32_t avg;
   int32_t skip_barrier;  // test hook, -1 = off
   float fn;
@@ -79,8 +79,8 @@ struct SmemStepArgs {
   const void* ptr[kMaxRanks];
   int64_t count;
   int32_t nranks;
-  int32_t order;   // RING or TREE
-  int32_t phases;  // bit 0 ReduceScatter, bit 1 AllGather
+  int32_t order;   // RING, TREE or BINOMIAL
+  int32_t phases;  // bit 0 ReduceScatter (BINOMIAL: reduce to rank 0), bit 1 AllGather (BINOMIAL: broadcast)
   int32_t avg;
   int32_t vec;     // every pointer 16-byte aligned
   float fn;

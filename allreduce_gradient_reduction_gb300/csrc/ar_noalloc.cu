@@ -136,7 +136,7 @@ int noalloc_body(void* const* grads, const int64_t* counts, int ntensors, int nr
   if (rc) return rc;
   if (algo == AR_NAIVE || algo == AR_DBTREE) return AR_ERR_UNSUPPORTED;
   // the step-wise kernels need a barrier block the library would allocate
-  if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE) return AR_ERR_UNSUPPORTED;
+  if (algo == AR_RING_STEPWISE || algo == AR_TREE_STEPWISE || algo == AR_BINOMIAL_STEPWISE) return AR_ERR_UNSUPPORTED;
   if (ntensors < 0 || bucket_cap_bytes <= 0) return AR_ERR_INVALID_ARG;
   if (ntensors == 0) return AR_OK;
   if (!grads || !counts) return AR_ERR_INVALID_ARG;

@@ -13,7 +13,7 @@ static cudaError_t launch_step_typed(StepArgs& a, cudaStream_t stream) {
   static const int bps = blocks_per_sm(stepwise_kernel<DT, OP, VECTOR>, kStepBlock);
   // persistent: every block must be resident at once (the launch checks it);
   // more blocks than the widest phase has tiles would only wait at barriers
-  int64_t widest = a.tab.ntiles * (a.order == TREE ? a.tab.nranks / 2 : 1);
+  int64_t widest = a.tab.ntiles * (a.order == TREE || a.order == BINOMIAL ? a.tab.nranks / 2 : 1);
   int64_t grid = (int64_t)bps * sm_count();
   if (grid > widest) grid = widest;
   if (grid < 1) grid = 1;

@@ -11,6 +11,12 @@
 // chunks j = r (mod 2h) and folds lower rank first; then recursive doubling in
 // reverse order copies the halves back.  AVG divides at the owner after the
 // last ReduceScatter step.
+// Binomial ("4、AllReduce算法详解" §4.3, reduce to a root then broadcast; nearest
+// ranks first as in the primer's §四 4.1): reduce step k (h = 2^k, k = 0
+// first) has rank r = h (mod 2h) send its whole buffer to r - h, which folds
+// it in (lower rank first); broadcast step k (k = log2 N - 1 first) has rank
+// r = 0 (mod 2h) send its whole buffer to r + h.  AVG divides at rank 0 after
+// the last reduce step.  Whole buffers move, so the table has one segment.
 //
 // "Sending" chunk j from rank a to rank b is rank b's threads reading rank
 // a's buffer in HBM: one GPU holds all ranks.  Within a phase no location is
@@ -93,6 +99,7 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
   const SegTable& T = a.tab;
   const int n = T.nranks;
   const bool ring = a.order == RING;
+  const bool binom = a.order == BINOMIAL;
   const int L = ring ? 0 : ilog2(n);
   const int n_rs = (a.phases & 1) ? (ring ? n - 1 : L) : 0;
   const int n_ag = (a.phases & 2) ? (ring ? n - 1 : L) : 0;
@@ -103,7 +110,7 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
     const int s = rs ? q : q - n_rs;     // step within its half
     const int k = rs ? s : L - 1 - s;    // tree distance exponent
     const int h = 1 << k;
-    const int inst = ring ? 1 : (n >> (k + 1));  // rank pairs per chunk in a tree step
+    const int inst = ring ? 1 : (n >> (k + 1));  // rank pairs per chunk in a tree or binomial step
     const bool avg = a.avg && rs && s == n_rs - 1;
     const int64_t total = (int64_t)inst * T.ntiles;
 
@@ -116,11 +123,14 @@ __global__ void __launch_bounds__(kStepBlock) stepwise_kernel(const __grid_const
       if (ring) {
         src = rs ? (j + 1 + s) % n : (j + s) % n;
         dst = src + 1 == n ? 0 : src + 1;
+      } else if (binom) {
+        dst = m * 2 * h + (rs ? 0 : h);
+        src = dst ^ h;
       } else {
         dst = rs ? ((j & (2 * h - 1)) + m * 2 * h) : (((j ^ h) & (2 * h - 1)) + m * 2 * h);
         src = dst ^ h;
       }
-      const bool src_first = ring || src < dst;  // ring: received first; tree: lower rank first
+      const bool src_first = ring || src < dst;  // ring: received first; trees: lower rank first
       const void* const* P = T.ptr + (size_t)sg.tensor * n;
       const char* ps = static_cast<const char*>(P[src]);
       char* pd = static_cast<char*>(const_cast<void*>(P[dst]));
@@ -256,6 +266,7 @@ __global__ void __launch_bounds__(kSmemStepBlock) stepwise_smem_kernel(const __g
   smem_stage<ES, true>(a, S, stride, n, count);
   __syncthreads();
   const bool ring = a.order == RING;
+  const bool binom = a.order == BINOMIAL;
   const int L = ring ? 0 : ilog2(n);
   const int n_rs = (a.phases & 1) ? (ring ? n - 1 : L) : 0;
   const int n_ag = (a.phases & 2) ? (ring ? n - 1 : L) : 0;
@@ -274,6 +285,9 @@ __global__ void __launch_bounds__(kSmemStepBlock) stepwise_smem_kernel(const __g
       if (ring) {
         src = rs ? (j + 1 + s) % n : (j + s) % n;
         dst = src + 1 == n ? 0 : src + 1;
+      } else if (binom) {
+        dst = m * 2 * h + (rs ? 0 : h);
+        src = dst ^ h;
       } else {
         dst = rs ? ((j & (2 * h - 1)) + m * 2 * h) : (((j ^ h) & (2 * h - 1)) + m * 2 * h);
         src = dst ^ h;

@@ -339,10 +339,12 @@ def graph_time(call, torch, stream, reps=20):
 
 def run_sweep(args, ws, rank, dev, torch, ar):
     """Per-rank message 4 KiB .. 1 GiB x N in --sweep-ranks (N x size <= 64 GiB)
-    x {f32, bf16} x {SUM, MAX} x {ring, tree, ring_stepwise, tree_stepwise},
-    uniform(-1, 1) values.  Writes one JSON line per point to --sweep-out and
-    prints one summary line: the alpha-beta fit of every order per (N, dtype)
-    and the ring/tree crossover of the step-wise orders."""
+    x {f32, bf16} x {SUM, MAX} x {ring, tree, ring_stepwise, tree_stepwise,
+    binomial_stepwise}, uniform(-1, 1) values.  Writes one JSON line per point
+    to --sweep-out and prints one summary line: the alpha-beta fit of every
+    order per (N, dtype), and the ring/tree crossover measured between the
+    step-wise ring and the step-wise binomial (and halving/doubling) trees,
+    beside where the pages' alpha-beta model puts it."""
     import math
     from allreduce_gradient_reduction_gb300 import workloads as W
     stream = torch.cuda.current_stream()
@@ -362,8 +364,8 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                     b.view(tdt).uniform_(-1.0, 1.0, generator=gen)
                 curves = {}
                 for op in ("sum", "max"):
-                    for algo in ("ring", "tree", "ring_stepwise", "tree_stepwise"):
-                        if algo.startswith("tree") and n & (n - 1):
+                    for algo in ("ring", "tree", "ring_stepwise", "tree_stepwise", "binomial_stepwise"):
+                        if (algo.startswith("tree") or algo.startswith("binomial")) and n & (n - 1):
                             continue
                         for nbytes in W.SWEEP_BYTES:
                             if nbytes > max_bytes:
@@ -412,21 +414,36 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                             npoints += 1
                             if op == "sum":
                                 curves.setdefault(algo, []).append((nbytes, t))
+                L = math.log2(n)
                 for algo, pts in curves.items():
                     stepwise = algo.endswith("stepwise")
-                    steps = (2 * (n - 1) if algo.startswith("ring") else 2 * int(math.log2(n))) if stepwise else 1
-                    # per-rank traffic factor of the page's model: 2(N-1)/N D for ring and halving/doubling
-                    alpha, beta = fit_alpha_beta(pts, steps, 2 * (n - 1) / n)
+                    steps = (2 * (n - 1) if algo.startswith("ring") else 2 * int(L)) if stepwise else 1
+                    # per-rank traffic factor of the pages' model: 2(N-1)/N D for ring and
+                    # halving/doubling; the binomial tree's root moves 2 log2(N) D
+                    factor = 2 * L if algo.startswith("binomial") else 2 * (n - 1) / n
+                    alpha, beta = fit_alpha_beta(pts, steps, factor)
                     fits[f"N{n}_{dt}_{algo}"] = {"alpha_us": alpha * 1e6, "beta_ps_per_byte": beta * 1e12,
                                                  "steps": steps}
-                if "ring_stepwise" in curves and "tree_stepwise" in curves:
-                    rs, ts = dict(curves["ring_stepwise"]), dict(curves["tree_stepwise"])
-                    cross = [d for d in sorted(rs) if rs[d] < ts.get(d, float("inf"))]
-                    # the page's model with a binomial tree (2 D beta) and the fitted ring alpha, beta
+                if "ring_stepwise" in curves and "binomial_stepwise" in curves:
+                    rs = dict(curves["ring_stepwise"])
+
+                    def first_ring_win(other):
+                        os_ = dict(curves[other])
+                        wins = [d for d in sorted(rs) if rs[d] < os_.get(d, float("inf"))]
+                        return wins[0] if wins else None
                     f = fits[f"N{n}_{dt}_ring_stepwise"]
-                    model = (n - 1 - math.log2(n)) * n * (f["alpha_us"] * 1e-6) / (f["beta_ps_per_byte"] * 1e-12)
-                    crossover[f"N{n}_{dt}"] = {"measured_first_ring_win_bytes": cross[0] if cross else None,
-                                               "model_binomial_crossover_bytes": model}
+                    a_, b_ = f["alpha_us"] * 1e-6, f["beta_ps_per_byte"] * 1e-12
+                    # where the pages' alpha-beta model puts the ring/tree crossover, with the
+                    # fitted ring alpha and beta: against a binomial tree whose root moves
+                    # 2 log2(N) D, and against a pipelined tree moving 2 D
+                    model_binom = ((n - 1 - L) * a_ / ((L - (n - 1) / n) * b_)) if n > 2 else None
+                    model_pipe = (n - 1 - L) * n * a_ / b_
+                    crossover[f"N{n}_{dt}"] = {
+                        "crossover_measured_ring_vs_binomial_bytes": first_ring_win("binomial_stepwise"),
+                        "crossover_measured_ring_vs_halving_doubling_bytes": first_ring_win("tree_stepwise"),
+                        "model_ring_vs_binomial_bytes": model_binom,
+                        "model_ring_vs_pipelined_tree_bytes": model_pipe,
+                        "sizes_measured": [int(d) for d in sorted(rs)]}
             del bufs
             torch.cuda.empty_cache()
     line = {"metric": METRIC + " (sweep)", "points": npoints, "points_file": args.sweep_out, "unit": "us",

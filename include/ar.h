@@ -28,9 +28,13 @@
  *     non-overlapping (checked; AR_ERR_INVALID_ARG otherwise).  They must be
  *     aligned to the element size.  When all of them sit at the same address
  *     modulo 16 (16-byte aligned or not) the kernels move 16-byte vectors,
- *     cut at that offset; buffers at different offsets modulo 16 take a
- *     slower one-element-per-thread path.  (For a bucketed call this holds
- *     per tensor: each tensor's N buffers.)
+ *     cut at that offset.  Buffers at different offsets modulo 16 still move
+ *     in aligned 16-byte words in the fused kernels (each rank read and
+ *     written at its own offset, the words realigned in registers) for every
+ *     order of up to 8 ranks and for rings of any size; trees of 16 or more
+ *     ranks and the step-wise, gather and copy kernels then take a slower
+ *     one-element-per-thread path.  (For a bucketed call this holds per
+ *     tensor: each tensor's N buffers.)
  *   - 1 <= nranks <= AR_MAX_RANKS; 0 <= count <= AR_MAX_COUNT (else
  *     AR_ERR_INVALID_ARG, as for a buffer whose end would pass the top of the
  *     address space); count == 0 and nranks == 1 do
@@ -61,6 +65,18 @@
  *       AR_NAIVE (AllReduce and Reduce only): index order x[0], x[1], ...,
  *         x[N-1], the order in which a central root folds the buffers it
  *         gathers ("AllReduce 集合通信" §朴素实现与主节点瓶颈, tutorial §2.1).
+ *       AR_BINOMIAL_STEPWISE (AllReduce only): the tree that reduces to a
+ *         root and then broadcasts ([chapter §4.3]), executed literally:
+ *         reduce step k = 0 .. log2(N)-1 (distance h = 2^k, nearest ranks
+ *         first as in [primer §四 4.1]) has every rank r = h (mod 2h) send
+ *         its whole buffer to rank r-h, which folds it in (lower rank first);
+ *         rank 0 then holds the result (and divides it by N for AVG);
+ *         broadcast step k = log2(N)-1 .. 0 has every rank r = 0 (mod 2h)
+ *         send it to rank r+h.  2 log2(N) steps, each moving whole buffers
+ *         (the root sends and receives D elements per level: 2 D log2(N) at
+ *         the root, [chapter §4.3]).  Every element is folded in the
+ *         balanced pairwise order of AR_TREE, so the values equal AR_TREE's.
+ *         N must be a power of two.
  *       AR_DBTREE (AllReduce only): double binary tree -- two binary trees
  *         run at once, each reducing half of the data ([concept §3]; the
  *         pages give no shape).  Positions 1..N form an in-order binary tree
@@ -105,7 +121,8 @@ typedef enum {
   AR_TREE = 2,
   AR_TREE_STEPWISE = 3,
   AR_NAIVE = 4,
-  AR_DBTREE = 5
+  AR_DBTREE = 5,
+  AR_BINOMIAL_STEPWISE = 6
 } ar_algo;
 
 typedef enum {

@@ -78,9 +78,10 @@ def test_random_collectives(ar, block):
         count = max(count, 0)
         dtype = str(rng.choice(["f32", "bf16", "i32", "f16"]))
         kind = str(rng.choice(["allreduce", "reduce_scatter", "all_gather", "reduce", "broadcast"]))
-        algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
+        algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (
+            ["tree", "tree_stepwise", "binomial_stepwise"] if n & (n - 1) == 0 else [])
         if kind in ("reduce_scatter", "all_gather"):
-            algos = [a for a in algos if a not in ("naive", "dbtree")]
+            algos = [a for a in algos if a not in ("naive", "dbtree", "binomial_stepwise")]
         if kind == "reduce":
             algos = [a for a in algos if a in ("ring", "tree", "naive")]
         algo = str(rng.choice(algos))
@@ -92,7 +93,7 @@ def test_random_collectives(ar, block):
             np.zeros((n, 0), dtype=np.uint16 if dtype in HALF else (np.int32 if dtype == "i32" else np.float32)))
         shifts = shifts_for(rng, n, dtype)
         bufs = [place(x[r], dtype, shifts[r]) for r in range(n)]
-        oa = {"ring_stepwise": "ring", "tree_stepwise": "tree"}.get(algo, algo)
+        oa = {"ring_stepwise": "ring", "tree_stepwise": "tree", "binomial_stepwise": "binomial"}.get(algo, algo)
         what = f"case {block}/{case}: {kind} {algo} {dtype} {op} n={n} count={count} shifts={shifts}"
         with np.errstate(all="ignore"):
             if kind == "allreduce":
@@ -201,7 +202,7 @@ def test_random_plans(ar, block):
         bufs = [place(np.zeros(count, dtype={"f32": np.float32, "bf16": np.uint16, "i32": np.int32, "f16": np.uint16}[dtype]),
                       dtype, shifts[r]) for r in range(n)]
         plan = ar.Plan(kind, bufs, count=count, dtype=dtype, op=op, algo=algo, root=root)
-        oa = {"ring_stepwise": "ring", "tree_stepwise": "tree"}.get(algo, algo)
+        oa = {"ring_stepwise": "ring", "tree_stepwise": "tree", "binomial_stepwise": "binomial"}.get(algo, algo)
         what = f"plan case {block}/{case}: {kind} {algo} {dtype} {op} n={n} count={count}"
         for it in range(3):
             x = W.uniform_inputs(n, count, dtype, config=int(rng.integers(1 << 20)))

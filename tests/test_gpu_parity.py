@@ -100,7 +100,8 @@ def inputs(n, count, dtype, kind, seed):
 
 
 ALGOS = ["ring", "tree", "ring_stepwise", "tree_stepwise"]
-ORACLE_ALGO = {"ring": "ring", "ring_stepwise": "ring", "tree": "tree", "tree_stepwise": "tree"}
+ORACLE_ALGO = {"ring": "ring", "ring_stepwise": "ring", "tree": "tree", "tree_stepwise": "tree",
+               "binomial_stepwise": "binomial"}
 
 
 def counts_for(n):
@@ -177,6 +178,42 @@ def test_all_gather_copies_bits(ar, algo, dtype):
             assert np.array_equal(got.view(bits), want.view(bits)), (algo, n, count)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 32, 64])
+def test_binomial_stepwise_matches_oracle(ar, n, dtype):
+    """The literal binomial reduce-to-root-then-broadcast schedule against the
+    oracle's message simulation of the same schedule, bit for bit, in the
+    one-block form (small rows) and the grid-barrier form; its values must
+    equal the tree order's (the same pairwise fold)."""
+    for count in counts_for(n):
+        x = inputs(n, count, dtype, "bits" if count % 2 else "values", seed=700 + n + count)
+        for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
+            with np.errstate(all="ignore"):
+                want, st = oracle.allreduce(x, algo="binomial", op=op, dtype=dtype)
+                tree, _ = oracle.allreduce(x, algo="tree", op=op, dtype=dtype)
+            assert st["steps"] == 2 * int(math.log2(n))
+            got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo="binomial_stepwise")
+            assert_same(got, want, dtype, f"binomial n={n} count={count} {op}")
+            assert_same(got, tree, dtype, f"binomial = tree n={n} count={count} {op}")
+
+
+def test_binomial_stepwise_takes_allreduce_only(ar):
+    bufs = [torch.zeros(64, device="cuda") for _ in range(4)]
+    assert ar.ar_allreduce(bufs[:3], count=64, algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_reduce_scatter(bufs, count=64, algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_all_gather(bufs, count=64, algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_reduce(bufs, count=64, algo="binomial_stepwise", root=0) == ar.AR_ERR_UNSUPPORTED
+    grads = [[b] for b in bufs]
+    assert ar.ar_bucketed_allreduce(grads, counts=[64], algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    assert ar.ar_bucketed_allreduce_noalloc(grads, counts=[64], algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    host = [torch.zeros(64).pin_memory() for _ in range(4)]
+    assert ar.ar_allreduce_host(host, None, count=64, algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
+    plan = ar.Plan("allreduce", bufs, count=64, algo="binomial_stepwise")  # prepared AllReduce is fine
+    ar.check(plan.run(), "plan")
+    torch.cuda.synchronize()
+    plan.close()
+
+
 # --------------------------------------------------------------------------
 # Alignment, degenerate sizes, streams
 # --------------------------------------------------------------------------
@@ -202,6 +239,53 @@ def test_unaligned_buffers(ar, algo, dtype):
         assert_same(got, want, dtype, f"{algo} shifts {shifts}")
         for r in range(n):
             assert np.array_equal(from_dev([big[r][:shifts[r]]], dtype)[0], x[r, :shifts[r]])
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 16, 64])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
+def test_mixed_phase_rows(ar, n, dtype):
+    """Rank buffers at different addresses modulo 16 (the realigning vector
+    kernel: aligned words at each rank's own phase, shuffled into the first
+    buffer's frame, stored back at each rank's phase), in every order the
+    rank count allows, for AllReduce, ReduceScatter (owner store) and Reduce
+    (root store), over a size that spans many tiles and ends ragged.  Nothing
+    outside the buffers may change."""
+    vec = 8 if dtype in HALF else 4
+    count = 3 * 248 * vec + 2048 * n + 13
+    x = inputs(n, count, dtype, "values", seed=41 + n)
+    shifts = [(5 * r + 1) % vec for r in range(n)]
+    algos = ["ring", "naive", "dbtree"] + (["tree"] if n & (n - 1) == 0 else [])
+    ops = ["sum", "max"] + ([] if dtype == "i32" else ["avg"])
+    for algo in algos:
+        for op in ops:
+            kinds = ("allreduce", "reduce_scatter", "reduce") if algo in ("ring", "tree") else ("allreduce",)
+            for kind in kinds:
+                big = [to_dev(np.concatenate([x[r][:shifts[r]], x[r], x[r][:7]])) for r in range(n)]
+                views = [b[s:s + count] for b, s in zip(big, shifts)]
+                oa = ORACLE_ALGO.get(algo, algo)
+                what = f"{kind} {algo} {op} n={n} shifts={shifts}"
+                if kind == "allreduce":
+                    want, _ = oracle.allreduce(x, algo=oa, op=op, dtype=dtype)
+                    ar.check(ar.ar_allreduce(views, count=count, dtype=dtype, op=op, algo=algo), what)
+                elif kind == "reduce_scatter":
+                    want, _ = oracle.reduce_scatter(x, algo=oa, op=op, dtype=dtype)
+                    ar.check(ar.ar_reduce_scatter(views, count=count, dtype=dtype, op=op, algo=algo), what)
+                else:
+                    want, _ = oracle.reduce(x, algo=oa, op=op, dtype=dtype, root=n - 1)
+                    ar.check(ar.ar_reduce(views, count=count, dtype=dtype, op=op, algo=algo, root=n - 1), what)
+                torch.cuda.synchronize()
+                got = from_dev(views, dtype)
+                for r in range(n):
+                    if kind == "reduce_scatter":
+                        lo, hi = oracle.chunk_range(count, n, r)
+                        assert_same(got[r, lo:hi], want[r, lo:hi], dtype, f"{what} rank {r}")
+                    elif kind == "reduce" and r != n - 1:
+                        assert_same(got[r], x[r], dtype, f"{what} non-root {r}")
+                    else:
+                        assert_same(got[r], want[r], dtype, f"{what} rank {r}")
+                    edge = from_dev([big[r]], dtype)[0]
+                    assert np.array_equal(edge[:shifts[r]], x[r, :shifts[r]]), f"{what} before rank {r}"
+                    assert np.array_equal(edge[shifts[r] + count:], x[r, :7]), f"{what} after rank {r}"
 
 
 @pytest.mark.parametrize("n", [16, 32, 64])
@@ -536,7 +620,7 @@ def test_bf16_step_exhaustive(ar):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("count", [1 << 16, 1 << 22])  # grids of at most 128 blocks (one counter) and more (groups)
-@pytest.mark.parametrize("algo", ["ring_stepwise", "tree_stepwise"])
+@pytest.mark.parametrize("algo", ["ring_stepwise", "tree_stepwise", "binomial_stepwise"])
 def test_barrier_timeout_is_reported(ar, algo, count):
     n = 8
     x = W.normal_inputs(n, count, 1.0, 12)

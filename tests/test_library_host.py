@@ -100,6 +100,10 @@ def test_argument_checks_without_device(ar):
     assert ar.DTYPE["f16"] == 3 and "AR_F16 = 3" in open(HEADER).read()
     assert ar.ar_allreduce([1 << 20, (1 << 20) + 4], count=4, dtype="f16", stream=0) == ar.AR_ERR_INVALID_ARG  # overlap
     assert ar.ar_allreduce([1 << 20, 1 << 21], count=4, algo=9, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ar_allreduce([1 << 20, 1 << 21], count=4, algo=7, stream=0) == ar.AR_ERR_INVALID_ARG
+    assert ar.ALGO["binomial_stepwise"] == 6 and "AR_BINOMIAL_STEPWISE = 6" in open(HEADER).read()
+    assert ar.ar_allreduce([1 << 20, 1 << 21, 1 << 22], count=4, algo="binomial_stepwise",
+                           stream=0) == ar.AR_ERR_UNSUPPORTED  # not a power of two
     assert ar.lib.ar_device_status(None, None) == ar.AR_ERR_INVALID_ARG
     rc = ar.ar_bucket_plan([5, 6], "f32", 0)[0]
     assert rc == ar.AR_ERR_INVALID_ARG
