@@ -18,6 +18,7 @@ template <int ES, bool VECTOR>
 __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_constant__ SegTable T) {
   constexpr int VEC = VECTOR ? 16 / ES : 1;
   constexpr int TILE = kFusedBlock * kGatherUnroll;
+  pdl_prologue();
   const int n = T.nranks;
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
@@ -68,9 +69,8 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
 template <int ES, bool VECTOR>
 static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
   if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll, VECTOR) == 0) return cudaSuccess;
-  gather_kernel<ES, VECTOR><<<grid_for(t.ntiles), kFusedBlock, 0, stream>>>(t);
   count_launch();
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel<ES, VECTOR>, grid_for(t.ntiles), kFusedBlock, stream, t);
 }
 
 cudaError_t launch_gather(int esize, bool vec, SegTable& t, cudaStream_t s) {
@@ -96,6 +96,7 @@ template <int ES>
 __global__ void __launch_bounds__(kFusedBlock) copy_kernel(const __grid_constant__ CopyArgs a) {
   constexpr int VEC = 16 / ES;
   constexpr int TILE = kFusedBlock * kCopyUnroll;
+  pdl_prologue();
   const SegTable& T = a.tab;
   const int n = T.nranks;
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
@@ -127,10 +128,9 @@ __global__ void __launch_bounds__(kFusedBlock) copy_kernel(const __grid_constant
 cudaError_t launch_copy(CopyArgs& a, cudaStream_t stream) {
   const int es = a.esize;
   if (fill_tiles(a.tab, 16 / es, (int64_t)kFusedBlock * kCopyUnroll) == 0) return cudaSuccess;
-  if (es == 2) copy_kernel<2><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
-  else copy_kernel<4><<<grid_for(a.tab.ntiles), kFusedBlock, 0, stream>>>(a);
   count_launch();
-  return cudaGetLastError();
+  if (es == 2) return launch_pdl(copy_kernel<2>, grid_for(a.tab.ntiles), kFusedBlock, stream, a);
+  return launch_pdl(copy_kernel<4>, grid_for(a.tab.ntiles), kFusedBlock, stream, a);
 }
 
 // ---- fused dispatch ----------------------------------------------------------

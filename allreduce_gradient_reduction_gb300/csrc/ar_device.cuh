@@ -21,6 +21,21 @@
 
 namespace ar {
 
+// ---- programmatic dependent launch ------------------------------------------
+// The fused, gather and copy kernels are launched so that the next kernel on
+// the stream may start while this one drains: every block first allows its
+// dependents to launch, then waits until the kernels it depends on have
+// completed and their writes are visible.  Nothing touches global memory
+// before that wait, so a kernel never sees a predecessor's data half
+// written; what overlaps is the next launch and its blocks' start-up with
+// the last blocks of this one.  (The launch attribute is what makes the
+// dependency programmatic; launched without it, both instructions do
+// nothing.)
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int DT>
 struct ElemSize {
   static constexpr int value = (DT == BF16 || DT == F16) ? 2 : 4;
