@@ -331,10 +331,15 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   // element updates in the busiest phase: the chunk's count for the ring,
   // N/2 pairs of it in the first tree or binomial step
   const int64_t phase_elems = j.row_count * (order == ar::TREE || order == ar::BINOMIAL ? tab.nranks / 2 : 1);
-  if (stepwise && j.row_count > 0 && phase_elems <= ar::kSmemStepMaxPhaseElems &&
-      ar::smem_step_bytes(tab.nranks, j.row_count, esize_of(j.dtype)) <= ar::kSmemStepBytes) {
-    // a small row: the whole schedule in one block's shared memory (no grid
-    // barrier, so the barrier test hook is consumed without effect)
+  const bool one_block = stepwise && j.row_count > 0 && phase_elems <= ar::kSmemStepMaxPhaseElems &&
+                         ar::smem_step_bytes(tab.nranks, j.row_count, esize_of(j.dtype)) <= ar::kSmemStepBytes;
+  int csize = 0;
+  if (stepwise && !one_block && j.row_count > 0 && phase_elems <= ar::kClusterStepMaxPhaseElems)
+    csize = ar::cluster_step_size(tab.nranks, j.row_count, esize_of(j.dtype), ar::cluster_step_max_size());
+  if (one_block || csize > 0) {
+    // a small row: the whole schedule in one block's shared memory, or in
+    // one thread-block cluster's (no grid barrier, so the barrier test hook
+    // is consumed without effect)
     g_skip_barrier.exchange(-1);
     ar::SmemStepArgs a;
     memset(&a, 0, sizeof(a));
@@ -346,7 +351,7 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
     a.avg = j.avg ? 1 : 0;
     a.vec = j.aligned ? 1 : 0;
     a.fn = (float)tab.nranks;
-    e = ar::launch_stepwise_smem(j.dtype, dop, a, s);
+    e = one_block ? ar::launch_stepwise_smem(j.dtype, dop, a, s) : ar::launch_stepwise_cluster(j.dtype, dop, a, csize, s);
   } else if (stepwise) {
     ar::SyncBlock* sb = nullptr;
     int rc = sync_block(&sb);

@@ -93,6 +93,18 @@ constexpr int64_t kSmemStepMaxPhaseElems = 3072;
 inline int64_t smem_step_bytes(int nranks, int64_t count, int esize) {
   return (int64_t)nranks * ((count * esize + 15) / 16 * 16);
 }
+// The cluster form spreads the ranks over the blocks of one thread-block
+// cluster (at most kSmemStepBytes of each block's shared memory); it is taken
+// while a step has at most this many element updates.
+constexpr int64_t kClusterStepMaxPhaseElems = 32768;
+// Blocks in the smallest cluster (a power of two, at most max_size and at
+// most nranks) whose blocks hold the row; 0 if none does.
+inline int cluster_step_size(int nranks, int64_t count, int esize, int max_size) {
+  const int64_t stride = (count * esize + 15) / 16 * 16;
+  for (int c = 2; c <= max_size && c <= nranks; c *= 2)
+    if ((nranks + c - 1) / c * stride <= kSmemStepBytes) return c;
+  return 0;
+}
 
 struct CopyArgs {
   SegTable tab;                  // ptr[tensor * nranks + r] = tensor side
@@ -120,6 +132,8 @@ cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t strea
 cudaError_t launch_copy(CopyArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise(int dtype, int op, bool vec, StepArgs& args, cudaStream_t stream);
 cudaError_t launch_stepwise_smem(int dtype, int op, SmemStepArgs& args, cudaStream_t stream);
+cudaError_t launch_stepwise_cluster(int dtype, int op, SmemStepArgs& args, int cluster_size, cudaStream_t stream);
+int cluster_step_max_size();
 cudaError_t launch_int8_ef(Int8Args& args, cudaStream_t stream);
 
 int sm_count();

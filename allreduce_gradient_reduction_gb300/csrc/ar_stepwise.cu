@@ -48,6 +48,80 @@ static cudaError_t launch_smem_typed(SmemStepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// ---- cluster form -----------------------------------------------------------
+
+template <int DT, int OP>
+static cudaError_t launch_cluster_typed(SmemStepArgs& a, int csize, cudaStream_t stream) {
+  static std::atomic<bool> opened[256];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  auto kernel = stepwise_cluster_kernel<DT, OP>;
+  if (!opened[dev].load()) {
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemStepBytes)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
+    opened[dev].store(true);
+  }
+  const int es = ElemSize<DT>::value;
+  const int64_t stride = (a.count * es + 15) / 16 * 16;
+  const size_t bytes = (size_t)(((int64_t)a.nranks + csize - 1) / csize * stride);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)csize);
+  cfg.blockDim = dim3(kClusterStepBlock);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)csize;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// The largest cluster the cluster kernel can be launched with on the current
+// device with a full shared-memory budget per block (0 if none).
+int cluster_step_max_size() {
+  static std::atomic<int> cached[256];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+  int v = cached[dev].load();
+  if (v) return v > 0 ? v : 0;
+  auto kernel = stepwise_cluster_kernel<F32, SUM>;
+  int best = -1;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemStepBytes) == cudaSuccess &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(kClusterStepBlock);
+    cfg.dynamicSmemBytes = (size_t)kSmemStepBytes;
+    int sz = 0;
+    if (cudaOccupancyMaxPotentialClusterSize(&sz, (const void*)kernel, &cfg) == cudaSuccess && sz >= 2) best = sz;
+  }
+  (void)cudaGetLastError();  // a refused query leaves nothing behind
+  cached[dev].store(best);
+  return best > 0 ? best : 0;
+}
+
+cudaError_t launch_stepwise_cluster(int dtype, int op, SmemStepArgs& a, int csize, cudaStream_t s) {
+  switch (dtype * 2 + op) {
+    case F32 * 2 + SUM: return launch_cluster_typed<F32, SUM>(a, csize, s);
+    case F32 * 2 + MAX: return launch_cluster_typed<F32, MAX>(a, csize, s);
+    case BF16 * 2 + SUM: return launch_cluster_typed<BF16, SUM>(a, csize, s);
+    case BF16 * 2 + MAX: return launch_cluster_typed<BF16, MAX>(a, csize, s);
+    case I32 * 2 + SUM: return launch_cluster_typed<I32, SUM>(a, csize, s);
+    case I32 * 2 + MAX: return launch_cluster_typed<I32, MAX>(a, csize, s);
+    case F16 * 2 + SUM: return launch_cluster_typed<F16, SUM>(a, csize, s);
+    case F16 * 2 + MAX: return launch_cluster_typed<F16, MAX>(a, csize, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_stepwise_smem(int dtype, int op, SmemStepArgs& a, cudaStream_t s) {
   if (smem_step_bytes(a.nranks, a.count, (dtype == BF16 || dtype == F16) ? 2 : 4) > kSmemStepBytes)
     return cudaErrorInvalidValue;

@@ -25,6 +25,8 @@
 // go through L2 (.cg), the coherence point for data other blocks wrote.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "ar_device.cuh"
 
 namespace ar {
@@ -305,6 +307,133 @@ __global__ void __launch_bounds__(kSmemStepBlock) stepwise_smem_kernel(const __g
     __syncthreads();
   }
   smem_stage<ES, false>(a, S, stride, n, count);
+}
+
+// ---- the same schedule in one thread-block cluster ---------------------------
+//
+// For rows too large for one block's shared memory but small enough that a
+// grid-wide barrier per step would dominate: the C blocks of one cluster
+// hold the N rank buffers between them (rank r in block r mod C, at
+// (r / C) * stride of its shared memory).  In a step each block folds the
+// elements its own ranks receive, reading the sender's values straight from
+// the sender block's shared memory (distributed shared memory), and the
+// steps are separated by the cluster's hardware barrier, whose release /
+// acquire order the writes of one step before the reads of the next.  Same
+// per-element operations in the same order as stepwise_kernel, so the same
+// bits.  Each block moves only its own ranks in and out of global memory.
+constexpr int kClusterStepBlock = 512;
+
+// What rank r receives in step s of its half (rs: the reduce half), k the
+// tree distance exponent: `nch` chunks j0, j0 + jstep, ... from rank `src`
+// (binomial: the whole buffer as one range), or nothing (nch = 0).
+struct StepRecv {
+  int src, j0, jstep, nch;
+  bool whole;
+};
+
+__device__ __forceinline__ StepRecv step_recv(int order, bool rs, int s, int k, int n, int r) {
+  StepRecv v{0, 0, 1, 0, false};
+  const int h = order == RING ? 1 : 1 << k;  // (the ring has no distance)
+  if (order == RING) {
+    v.src = r == 0 ? n - 1 : r - 1;
+    v.j0 = ((r - (rs ? 2 : 1) - s) % n + n) % n;
+    v.nch = 1;
+  } else if (order == BINOMIAL) {
+    const bool recv = rs ? (r & (2 * h - 1)) == 0 : (r & (2 * h - 1)) == h;
+    if (recv) {
+      v.src = r ^ h;
+      v.nch = 1;
+      v.whole = true;
+    }
+  } else {
+    v.src = r ^ h;
+    v.j0 = (rs ? r : (r ^ h)) & (2 * h - 1);
+    v.jstep = 2 * h;
+    v.nch = n / (2 * h);
+  }
+  return v;
+}
+
+template <int DT, int OP>
+__global__ void __launch_bounds__(kClusterStepBlock) stepwise_cluster_kernel(const __grid_constant__ SmemStepArgs a) {
+  namespace cg = cooperative_groups;
+  constexpr int ES = ElemSize<DT>::value;
+  using Wd = typename SmemWord<ES>::type;
+  extern __shared__ __align__(16) unsigned char S[];
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = (int)cl.num_blocks();
+  const int me = (int)cl.block_rank();
+  const int n = a.nranks;
+  const int count = (int)a.count;
+  const int stride = (count * ES + 15) / 16 * 16;
+  const int nloc = (n - me + C - 1) / C;  // ranks me, me + C, ...
+  const int maxch = (count + n - 1) / n;  // elements of the largest chunk
+
+  // stage this block's ranks in (16-byte pieces when aligned, then the tail)
+  const int nvec = a.vec ? count * ES / 16 : 0;
+  for (int i = threadIdx.x; i < nloc * nvec; i += kClusterStepBlock) {
+    const int l = i / nvec, kk = i - l * nvec;
+    reinterpret_cast<uint4*>(S + l * stride)[kk] = ld_l2(static_cast<const uint4*>(a.ptr[me + l * C]) + kk);
+  }
+  const int done = nvec * 16 / ES, rest = count - done;
+  for (int i = threadIdx.x; i < nloc * rest; i += kClusterStepBlock) {
+    const int l = i / rest, e = done + (i - l * rest);
+    reinterpret_cast<Wd*>(S + l * stride)[e] = (Wd)ld_elem<ES>(a.ptr[me + l * C], e);
+  }
+  cl.sync();
+
+  const bool ring = a.order == RING;
+  const int L = ring ? 0 : ilog2(n);
+  const int n_rs = (a.phases & 1) ? (ring ? n - 1 : L) : 0;
+  const int n_ag = (a.phases & 2) ? (ring ? n - 1 : L) : 0;
+  for (int q = 0; q < n_rs + n_ag; ++q) {
+    const bool rs = q < n_rs;
+    const int s = rs ? q : q - n_rs;
+    const int k = rs ? s : L - 1 - s;
+    const bool avg = a.avg && rs && s == n_rs - 1;
+    // items: (local rank, chunk of its list, offset in the chunk)
+    const bool whole = a.order == BINOMIAL;
+    const int per_ch = whole ? count : maxch;
+    const int nch_max = ring || whole ? 1 : n / (2 << k);
+    const int items = nloc * nch_max * per_ch;
+    for (int w = threadIdx.x; w < items; w += kClusterStepBlock) {
+      const int l = w / (nch_max * per_ch);
+      const int rem = w - l * (nch_max * per_ch);
+      const int ci = rem / per_ch, off = rem - ci * per_ch;
+      const int r = me + l * C;
+      const StepRecv v = step_recv(a.order, rs, s, k, n, r);
+      if (ci >= v.nch) continue;
+      int e;
+      if (v.whole) {
+        e = off;
+      } else {
+        const int j = v.j0 + ci * v.jstep;
+        const int lo = (int)(((int64_t)j * count) / n), hi = (int)(((int64_t)(j + 1) * count) / n);
+        e = lo + off;
+        if (e >= hi) continue;
+      }
+      Wd* pd = reinterpret_cast<Wd*>(S + l * stride) + e;
+      const Wd* ps = cl.map_shared_rank(reinterpret_cast<Wd*>(S + (v.src / C) * stride) + e, v.src % C);
+      uint32_t x = *ps;
+      if (rs) {
+        const uint32_t d = *pd;
+        x = (ring || v.src < r) ? step_word<DT, OP>(x, d) : step_word<DT, OP>(d, x);
+        if (avg) x = div_word<DT>(x, a.fn);
+      }
+      *pd = (Wd)x;
+    }
+    cl.sync();
+  }
+
+  // stage this block's ranks out
+  for (int i = threadIdx.x; i < nloc * nvec; i += kClusterStepBlock) {
+    const int l = i / nvec, kk = i - l * nvec;
+    st_l2(static_cast<uint4*>(const_cast<void*>(a.ptr[me + l * C])) + kk, reinterpret_cast<const uint4*>(S + l * stride)[kk]);
+  }
+  for (int i = threadIdx.x; i < nloc * rest; i += kClusterStepBlock) {
+    const int l = i / rest, e = done + (i - l * rest);
+    st_elem<ES>(const_cast<void*>(a.ptr[me + l * C]), e, reinterpret_cast<const Wd*>(S + l * stride)[e]);
+  }
 }
 
 }  // namespace ar

@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip timing the small, bucket and GPT-2 configurations beside the headline")
+    p.add_argument("--rank-offsets", choices=["aligned", "mixed"], default="aligned",
+                   help="large and bucket workloads: 'mixed' starts rank r's buffer (3r+1) mod (16/element size) "
+                        "elements into its allocation, so the ranks sit at different addresses modulo 16")
     p.add_argument("--count", type=int, default=0,
                    help="elements per rank (default: the full workload); smaller counts are for profiling")
     p.add_argument("--variants", action="store_true", help="also time tree and step-wise orders (extra keys)")
@@ -457,6 +460,19 @@ def run_sweep(args, ws, rank, dev, torch, ar):
 # workloads of our arm: host inputs (pinned), device buffers, one step
 # ---------------------------------------------------------------------------
 
+def rank_offsets(n: int, esize: int, kind: str) -> list:
+    """Element offset of each rank's buffer inside its allocation."""
+    vec = 16 // esize
+    return [0] * n if kind == "aligned" else [(3 * r + 1) % vec for r in range(n)]
+
+
+def rank_buffers(n, count, dtype, dev, esize, kind):
+    """One device allocation per rank (16 elements of slack), each rank's
+    buffer a view at its offset (all 0 unless kind == 'mixed')."""
+    import torch
+    return [torch.empty(count + 16, dtype=dtype, device=dev)[o:o + count] for o in rank_offsets(n, esize, kind)]
+
+
 class LargeWorkload:
     """8 ranks x 67,108,864 bf16, ring SUM: the headline configuration."""
     dtype, op = "bf16", "sum"
@@ -469,14 +485,17 @@ class LargeWorkload:
         for r in range(self.n):
             self.host[r].copy_(torch.from_numpy(W.large_rank(r, self.count).view(np.int16)))
         self.out = torch.empty_like(self.host, pin_memory=True)
-        self.bufs = [torch.empty(self.count, dtype=torch.int16, device=dev) for _ in range(self.n)]
+        self.bufs = rank_buffers(self.n, self.count, torch.int16, dev, 2, args.rank_offsets)
         self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
         self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
         self.workload = WORKLOAD if self.count == W.LARGE["count"] else (
             f"ring AllReduce SUM, {self.n} ranks x {self.count:,} bf16 ({self.count * 2 / 2**20:g} MiB per rank)")
+        if args.rank_offsets == "mixed":
+            self.workload += ", rank buffers at different addresses modulo 16"
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
                        "l2": ("inputs larger than L2" if self.n * self.count * 2 > 129e6 else "inputs partly L2-resident")
-                       + f" ({2 * self.n * self.count * 2 / 2**30:g} GiB touched per step vs 129 MB L2)"}
+                       + f" ({2 * self.n * self.count * 2 / 2**30:g} GiB touched per step vs 129 MB L2)",
+                       "rank_offset_elements": rank_offsets(self.n, 2, args.rank_offsets)}
 
     def step(self, sid, algo):
         rc = self.ar.ar_allreduce(self.bufs, count=self.count, dtype=self.dtype, op=self.op, algo=algo, stream=sid)
@@ -488,7 +507,7 @@ class LargeWorkload:
 
     def second_set(self):
         import torch
-        bufs = [torch.empty_like(b) for b in self.bufs]
+        bufs = rank_buffers(self.n, self.count, self.bufs[0].dtype, self.bufs[0].device, 2, self.args.rank_offsets)
 
         def step(sid):
             rc = self.ar.ar_allreduce(bufs, count=self.count, dtype=self.dtype, op=self.op, algo=self.args.algo,
@@ -522,12 +541,15 @@ class BucketWorkload:
         x = W.bucket_inputs(self.n, self.count)
         self.host = torch.from_numpy(x).pin_memory()
         self.out = torch.empty_like(self.host, pin_memory=True)
-        self.bufs = [torch.empty(self.count, dtype=torch.float32, device=dev) for _ in range(self.n)]
+        self.bufs = rank_buffers(self.n, self.count, torch.float32, dev, 4, args.rank_offsets)
         self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
         self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
         self.workload = "ring AllReduce AVG, 8 ranks x 6,553,600 f32 (one 25 MiB DDP bucket)"
+        if args.rank_offsets == "mixed":
+            self.workload += ", rank buffers at different addresses modulo 16"
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
-                       "l2": "inputs larger than L2 (409.6 MiB touched per step vs 129 MB L2)"}
+                       "l2": "inputs larger than L2 (409.6 MiB touched per step vs 129 MB L2)",
+                       "rank_offset_elements": rank_offsets(self.n, 4, args.rank_offsets)}
 
     def step(self, sid, algo, int8=False, op=None):
         if int8:
@@ -545,8 +567,7 @@ class BucketWorkload:
         return self.bufs, lambda sid: self.step(sid, self.args.algo)
 
     def second_set(self):
-        import torch
-        bufs = [torch.empty_like(b) for b in self.bufs]
+        bufs = rank_buffers(self.n, self.count, self.bufs[0].dtype, self.bufs[0].device, 4, self.args.rank_offsets)
 
         def step(sid):
             rc = self.ar.ar_allreduce(bufs, count=self.count, dtype=self.dtype, op=self.op, algo=self.args.algo,

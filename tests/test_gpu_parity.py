@@ -197,6 +197,39 @@ def test_binomial_stepwise_matches_oracle(ar, n, dtype):
             assert_same(got, tree, dtype, f"binomial = tree n={n} count={count} {op}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 64])
+def test_stepwise_cluster_form(ar, n, dtype):
+    """Rows too large for one block's shared memory (or with more than 3072
+    element updates in a step) but with at most 32768 updates per step run
+    the literal schedule in one thread-block cluster, ranks spread over its
+    blocks' shared memory: ring, tree and binomial, AllReduce, ReduceScatter
+    and AllGather, against the oracle bit for bit."""
+    es = 4 if dtype == "f32" else 2
+    ring_counts = [c for c in (3073, 8191, 20000, 32768) if n * ((c * es + 15) // 16 * 16) <= 16 * 160 * 1024]
+    for algo in ("ring_stepwise", "tree_stepwise", "binomial_stepwise"):
+        if not algo.startswith("ring") and n & (n - 1):
+            continue
+        counts = ring_counts if algo.startswith("ring") else [c for c in (3073 // (n // 2) + 1, 32768 // (n // 2))
+                                                              if n // 2 * c > 3072 or n * c * es > 160 * 1024]
+        for count in counts:
+            x = inputs(n, count, dtype, "values", seed=1300 + n + count)
+            for op in ("sum", "avg"):
+                want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op=op, dtype=dtype)
+                got, _ = run_collective(ar, "ar_allreduce", x, dtype, op=op, algo=algo)
+                assert_same(got, want, dtype, f"cluster {algo} n={n} count={count} {op}")
+            if algo == "binomial_stepwise":
+                continue
+            want, _ = oracle.reduce_scatter(x, algo=ORACLE_ALGO[algo], op="max", dtype=dtype)
+            got, _ = run_collective(ar, "ar_reduce_scatter", x, dtype, op="max", algo=algo)
+            for r in range(n):
+                lo, hi = oracle.chunk_range(count, n, r)
+                assert_same(got[r, lo:hi], want[r, lo:hi], dtype, f"cluster RS {algo} n={n} count={count}")
+            want, _ = oracle.all_gather(x, algo=ORACLE_ALGO[algo], dtype=dtype)
+            got, _ = run_collective(ar, "ar_all_gather", x, dtype, algo=algo)
+            assert_same(got, want, dtype, f"cluster AG {algo} n={n} count={count}")
+
+
 def test_binomial_stepwise_takes_allreduce_only(ar):
     bufs = [torch.zeros(64, device="cuda") for _ in range(4)]
     assert ar.ar_allreduce(bufs[:3], count=64, algo="binomial_stepwise") == ar.AR_ERR_UNSUPPORTED
