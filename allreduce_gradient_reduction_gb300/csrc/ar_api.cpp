@@ -334,8 +334,8 @@ int run_table(const Job& j, SegTable& tab, cudaStream_t s) {
   const bool one_block = stepwise && j.row_count > 0 && phase_elems <= ar::kSmemStepMaxPhaseElems &&
                          ar::smem_step_bytes(tab.nranks, j.row_count, esize_of(j.dtype)) <= ar::kSmemStepBytes;
   int csize = 0;
-  if (stepwise && !one_block && j.row_count > 0 && phase_elems <= ar::kClusterStepMaxPhaseElems)
-    csize = ar::cluster_step_size(tab.nranks, j.row_count, esize_of(j.dtype), ar::cluster_step_max_size());
+  if (stepwise && !one_block && j.row_count > 0)
+    csize = ar::cluster_step_size(tab.nranks, j.row_count, esize_of(j.dtype), order, ar::cluster_step_max_size());
   if (one_block || csize > 0) {
     // a small row: the whole schedule in one block's shared memory, or in
     // one thread-block cluster's (no grid barrier, so the barrier test hook

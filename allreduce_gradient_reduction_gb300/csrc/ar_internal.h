@@ -94,16 +94,28 @@ inline int64_t smem_step_bytes(int nranks, int64_t count, int esize) {
   return (int64_t)nranks * ((count * esize + 15) / 16 * 16);
 }
 // The cluster form spreads the ranks over the blocks of one thread-block
-// cluster (at most kSmemStepBytes of each block's shared memory); it is taken
-// while a step has at most this many element updates.
-constexpr int64_t kClusterStepMaxPhaseElems = 32768;
-// Blocks in the smallest cluster (a power of two, at most max_size and at
-// most nranks) whose blocks hold the row; 0 if none does.
-inline int cluster_step_size(int nranks, int64_t count, int esize, int max_size) {
+// cluster (at most kSmemStepBytes of each block's shared memory).  It pays
+// while each block has little to fold per step: measured on GB300 against
+// the grid-barrier form (bf16, CUDA-graph replay), it won up to the point
+// where the busiest block folds about this many elements in its heaviest
+// step (64 ranks x 4 KiB ring: 274.6 -> 140 us, 16 x 16 KiB ring 65.6 ->
+// 44.3 us, 8- and 16-rank trees at 4 KiB 16.2 -> 12.2 and 20.5 -> 14.5 us;
+// 1,024 elements per block tied, 2,048 and more lost).
+constexpr int64_t kClusterStepMaxBlockElems = 1024;
+// Blocks in the cluster for a row: the largest power of two that is at
+// least 2 and at most max_size and nranks, if its blocks hold the row and
+// no block folds more than kClusterStepMaxBlockElems elements in a step
+// (ring: a chunk per rank; tree: half a buffer per rank in its first step;
+// binomial: a whole buffer); 0 otherwise.
+inline int cluster_step_size(int nranks, int64_t count, int esize, int order, int max_size) {
   const int64_t stride = (count * esize + 15) / 16 * 16;
-  for (int c = 2; c <= max_size && c <= nranks; c *= 2)
-    if ((nranks + c - 1) / c * stride <= kSmemStepBytes) return c;
-  return 0;
+  int c = 2;
+  while (c * 2 <= max_size && c * 2 <= nranks) c *= 2;
+  if (c > nranks || c > max_size) return 0;
+  const int64_t nloc = (nranks + c - 1) / c;
+  if (nloc * stride > kSmemStepBytes) return 0;
+  const int64_t per_rank = order == RING ? (count + nranks - 1) / nranks : order == TREE ? (count + 1) / 2 : count;
+  return nloc * per_rank <= kClusterStepMaxBlockElems ? c : 0;
 }
 
 struct CopyArgs {

@@ -391,36 +391,66 @@ __global__ void __launch_bounds__(kClusterStepBlock) stepwise_cluster_kernel(con
     const int s = rs ? q : q - n_rs;
     const int k = rs ? s : L - 1 - s;
     const bool avg = a.avg && rs && s == n_rs - 1;
-    // items: (local rank, chunk of its list, offset in the chunk)
+    // items: (local rank, chunk of its list, offset in the chunk), four
+    // per thread at a time so their remote loads are in flight together;
+    // index arithmetic in 32 bits (count * nranks < 2^31 for rows this size)
     const bool whole = a.order == BINOMIAL;
     const int per_ch = whole ? count : maxch;
     const int nch_max = ring || whole ? 1 : n / (2 << k);
-    const int items = nloc * nch_max * per_ch;
-    for (int w = threadIdx.x; w < items; w += kClusterStepBlock) {
-      const int l = w / (nch_max * per_ch);
-      const int rem = w - l * (nch_max * per_ch);
-      const int ci = rem / per_ch, off = rem - ci * per_ch;
-      const int r = me + l * C;
-      const StepRecv v = step_recv(a.order, rs, s, k, n, r);
-      if (ci >= v.nch) continue;
-      int e;
-      if (v.whole) {
-        e = off;
-      } else {
-        const int j = v.j0 + ci * v.jstep;
-        const int lo = (int)(((int64_t)j * count) / n), hi = (int)(((int64_t)(j + 1) * count) / n);
-        e = lo + off;
-        if (e >= hi) continue;
+    const int span = nch_max * per_ch;
+    const int items = nloc * span;
+    constexpr int CU = 4;
+    for (int w0 = threadIdx.x; w0 < items; w0 += CU * kClusterStepBlock) {
+      Wd* pd[CU];
+      const Wd* ps[CU];
+      bool go[CU], src_first[CU];
+#pragma unroll
+      for (int u = 0; u < CU; ++u) {
+        const int w = w0 + u * kClusterStepBlock;
+        go[u] = false;
+        pd[u] = nullptr;
+        ps[u] = nullptr;
+        src_first[u] = true;
+        if (w < items) {
+          const int l = w / span;
+          const int rem = w - l * span;
+          const int ci = rem / per_ch, off = rem - ci * per_ch;
+          const int r = me + l * C;
+          const StepRecv v = step_recv(a.order, rs, s, k, n, r);
+          int e = off;
+          bool in = ci < v.nch;
+          if (in && !v.whole) {
+            const int j = v.j0 + ci * v.jstep;
+            const int lo = j * count / n, hi = (j + 1) * count / n;
+            e = lo + off;
+            in = e < hi;
+          }
+          if (in) {
+            go[u] = true;
+            pd[u] = reinterpret_cast<Wd*>(S + l * stride) + e;
+            ps[u] = cl.map_shared_rank(reinterpret_cast<Wd*>(S + (v.src / C) * stride) + e, v.src % C);
+            src_first[u] = ring || v.src < r;
+          }
+        }
       }
-      Wd* pd = reinterpret_cast<Wd*>(S + l * stride) + e;
-      const Wd* ps = cl.map_shared_rank(reinterpret_cast<Wd*>(S + (v.src / C) * stride) + e, v.src % C);
-      uint32_t x = *ps;
-      if (rs) {
-        const uint32_t d = *pd;
-        x = (ring || v.src < r) ? step_word<DT, OP>(x, d) : step_word<DT, OP>(d, x);
-        if (avg) x = div_word<DT>(x, a.fn);
+      uint32_t x[CU], d[CU];
+#pragma unroll
+      for (int u = 0; u < CU; ++u) {
+        if (go[u]) {
+          x[u] = *ps[u];
+          d[u] = rs ? (uint32_t)*pd[u] : 0u;
+        }
       }
-      *pd = (Wd)x;
+#pragma unroll
+      for (int u = 0; u < CU; ++u) {
+        if (!go[u]) continue;
+        uint32_t y = x[u];
+        if (rs) {
+          y = src_first[u] ? step_word<DT, OP>(x[u], d[u]) : step_word<DT, OP>(d[u], x[u]);
+          if (avg) y = div_word<DT>(y, a.fn);
+        }
+        *pd[u] = (Wd)y;
+      }
     }
     cl.sync();
   }

@@ -197,22 +197,42 @@ def test_binomial_stepwise_matches_oracle(ar, n, dtype):
             assert_same(got, tree, dtype, f"binomial = tree n={n} count={count} {op}")
 
 
+def cluster_form_counts(n, algo, es):
+    """Counts whose plain step-wise call takes the cluster form: more than
+    3072 element updates in a step or more than 160 KiB in all (so not one
+    block), the busiest block folding at most 1024 elements in a step, the
+    ranks spread over the largest power-of-two cluster of at most 16 blocks."""
+    c = 2
+    while c * 2 <= 16 and c * 2 <= n:
+        c *= 2
+    if c > n:
+        return []
+    nloc = -(-n // c)
+    out = []
+    for count in range(1, 40000, 7):
+        stride = -(-count * es // 16) * 16
+        step = count * (1 if algo.startswith("ring") else n // 2)
+        one_block = step <= 3072 and n * stride <= 160 * 1024
+        per_rank = -(-count // n) if algo.startswith("ring") else (-(-count // 2) if algo.startswith("tree") else count)
+        if not one_block and nloc * stride <= 160 * 1024 and nloc * per_rank <= 1024:
+            out.append(count)
+    return [out[0], out[len(out) // 2], out[-1]] if out else []
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("n", [2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("n", [4, 8, 16, 32, 64])
 def test_stepwise_cluster_form(ar, n, dtype):
     """Rows too large for one block's shared memory (or with more than 3072
-    element updates in a step) but with at most 32768 updates per step run
-    the literal schedule in one thread-block cluster, ranks spread over its
+    element updates in a step) whose steps are small run the literal
+    schedule in one thread-block cluster, ranks spread over its blocks'
+    shared memory, each step reading the senders' values from the other
     blocks' shared memory: ring, tree and binomial, AllReduce, ReduceScatter
     and AllGather, against the oracle bit for bit."""
     es = 4 if dtype == "f32" else 2
-    ring_counts = [c for c in (3073, 8191, 20000, 32768) if n * ((c * es + 15) // 16 * 16) <= 16 * 160 * 1024]
+    tested = 0
     for algo in ("ring_stepwise", "tree_stepwise", "binomial_stepwise"):
-        if not algo.startswith("ring") and n & (n - 1):
-            continue
-        counts = ring_counts if algo.startswith("ring") else [c for c in (3073 // (n // 2) + 1, 32768 // (n // 2))
-                                                              if n // 2 * c > 3072 or n * c * es > 160 * 1024]
-        for count in counts:
+        for count in cluster_form_counts(n, algo, es):
+            tested += 1
             x = inputs(n, count, dtype, "values", seed=1300 + n + count)
             for op in ("sum", "avg"):
                 want, _ = oracle.allreduce(x, algo=ORACLE_ALGO[algo], op=op, dtype=dtype)
@@ -228,6 +248,7 @@ def test_stepwise_cluster_form(ar, n, dtype):
             want, _ = oracle.all_gather(x, algo=ORACLE_ALGO[algo], dtype=dtype)
             got, _ = run_collective(ar, "ar_all_gather", x, dtype, algo=algo)
             assert_same(got, want, dtype, f"cluster AG {algo} n={n} count={count}")
+    assert tested > 0
 
 
 def test_binomial_stepwise_takes_allreduce_only(ar):
