@@ -126,6 +126,7 @@ __device__ __forceinline__ Lane4 encode(const Lane4& x, const Lane4& e, float* e
 __global__ void __launch_bounds__(kQ8Block, kQ8MinBlocks) int8_ef_kernel(const __grid_constant__ Int8Args a) {
   __shared__ float s_scale[kQ8Block / 32][kMaxRanks];
   __shared__ float4 s_stage[kQ8Block / 32][kQ8Stages][2][32];  // [warp][slot][x or e][lane]
+  pdl_prologue();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t count = a.count;
   const int n = a.nranks;
@@ -238,9 +239,8 @@ cudaError_t launch_int8_ef(Int8Args& a, cudaStream_t stream) {
   const int64_t nq = (a.count + kQ8 - 1) / kQ8;
   if (nq == 0) return cudaSuccess;
   const int64_t grid = (nq + kQ8Block / 32 - 1) / (kQ8Block / 32);
-  int8_ef_kernel<<<grid_for(grid), kQ8Block, 0, stream>>>(a);
   count_launch();
-  return cudaGetLastError();
+  return launch_pdl(int8_ef_kernel, grid_for(grid), kQ8Block, stream, a);
 }
 
 }  // namespace ar

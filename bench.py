@@ -431,9 +431,21 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                     rs = dict(curves["ring_stepwise"])
 
                     def first_ring_win(other):
+                        # the smallest size from which the ring is faster by 2% or more at that size
+                        # and at every larger one measured (None: the ring never pulls ahead)
                         os_ = dict(curves[other])
-                        wins = [d for d in sorted(rs) if rs[d] < os_.get(d, float("inf"))]
-                        return wins[0] if wins else None
+                        sizes = sorted(d for d in rs if d in os_)
+                        win = None
+                        for d in reversed(sizes):
+                            if rs[d] < 0.98 * os_[d]:
+                                win = d
+                            else:
+                                break
+                        return win
+
+                    def ratios(other):
+                        os_ = dict(curves[other])
+                        return {str(d): round(rs[d] / os_[d], 3) for d in sorted(rs) if d in os_}
                     f = fits[f"N{n}_{dt}_ring_stepwise"]
                     a_, b_ = f["alpha_us"] * 1e-6, f["beta_ps_per_byte"] * 1e-12
                     # where the pages' alpha-beta model puts the ring/tree crossover, with the
@@ -446,7 +458,7 @@ def run_sweep(args, ws, rank, dev, torch, ar):
                         "crossover_measured_ring_vs_halving_doubling_bytes": first_ring_win("tree_stepwise"),
                         "model_ring_vs_binomial_bytes": model_binom,
                         "model_ring_vs_pipelined_tree_bytes": model_pipe,
-                        "sizes_measured": [int(d) for d in sorted(rs)]}
+                        "ring_over_binomial_time_by_bytes": ratios("binomial_stepwise")}
             del bufs
             torch.cuda.empty_cache()
     line = {"metric": METRIC + " (sweep)", "points": npoints, "points_file": args.sweep_out, "unit": "us",

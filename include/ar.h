@@ -91,7 +91,11 @@
  *     step-wise call -- at most 3072 element updates in a phase, N buffers
  *     within 160 KiB -- runs the same schedule in one thread block, the
  *     buffers staged in its shared memory and a block barrier between
- *     phases: same results, no grid barrier.
+ *     phases: same results, no grid barrier.  A somewhat larger one runs it
+ *     in one thread-block cluster (up to 16 blocks, each holding some ranks'
+ *     buffers in at most 160 KiB of shared memory), senders read through
+ *     distributed shared memory and a cluster barrier between phases, while
+ *     no block folds more than 1024 elements in a phase: same results.
  */
 #ifndef AR_GB300_H
 #define AR_GB300_H
