@@ -57,8 +57,14 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
 
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
+    """Compile every source under csrc/ for sm_103a and link libar_gb300.so
+    (skipped when the library is newer than every source and header).
+    Prints one line saying which it did."""
     if not force and up_to_date():
+        print(f"[build] {os.path.basename(OUT)} is up to date (sm_103a)", file=sys.stderr)
         return OUT
+    import time
+    t0 = time.time()
     os.makedirs(BUILD, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
@@ -69,6 +75,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, OUT)
+    print(f"[build] compiled {len(srcs)} sources for sm_103a and linked {os.path.basename(OUT)} "
+          f"in {time.time() - t0:.1f} s", file=sys.stderr)
     return OUT
 
 

@@ -59,18 +59,20 @@ def sizes(n):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
-@pytest.mark.parametrize("n", [2, 3, 8])
+@pytest.mark.parametrize("n", [2, 3, 8, 16])
 def test_collectives_stay_inside_their_buffers(ar, n, dtype):
-    algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (["tree", "tree_stepwise"] if n & (n - 1) == 0 else [])
+    algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (
+        ["tree", "tree_stepwise", "binomial_stepwise"] if n & (n - 1) == 0 else [])
     for count in [c for c in sizes(n) if c > 0]:
         # aligned; the same offset in every rank (vectors cut at it); offsets
-        # differing by rank (one element per thread)
+        # differing by rank (the realigning vector kernel, or one element per
+        # thread)
         for shift in (0, ES[dtype], [(r * ES[dtype]) % 16 for r in range(n)]):
             G = Guarded(n, count, dtype, shift, seed=count + n)
             for algo in algos:
                 ar.check(ar.ar_allreduce(G.bufs, count=count, dtype=dtype, op="max", algo=algo), "allreduce")
                 G.check(f"allreduce {algo} n={n} count={count} shift={shift}")
-                if algo in ("naive", "dbtree"):
+                if algo in ("naive", "dbtree", "binomial_stepwise"):
                     continue
                 ar.check(ar.ar_reduce_scatter(G.bufs, count=count, dtype=dtype, op="max", algo=algo), "rs")
                 G.check(f"reduce_scatter {algo} n={n} count={count} shift={shift}")
