@@ -855,6 +855,45 @@ def test_int8_ef_unaligned_and_rejects(ar):
 # through its messages
 # --------------------------------------------------------------------------
 
+@pytest.fixture(scope="module")
+def pool():
+    with oracle_parallel.Pool() as p:
+        yield p
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [2, 4, 8, 16, 64])
+def test_sweep_points_full_compare(ar, pool, n, dtype):
+    """The latency/bandwidth sweep's points with N x size <= 2 GiB are
+    compared with the oracle on every element: 1 MiB per rank and the
+    largest such size (2 GiB / N), uniform(-1, 1) inputs as the sweep draws
+    them, SUM and MAX in the fused and step-wise orders, every rank identical
+    and rank 0 against the oracle's full run (element ranges over host
+    processes, compared by digests)."""
+    es = 2 if dtype == "bf16" else 4
+    orders = ["ring", "ring_stepwise"] + (["tree", "tree_stepwise", "binomial_stepwise"] if n & (n - 1) == 0 else [])
+    for nbytes in (1 << 20, (2 << 30) // n):
+        count = nbytes // es
+        x = np.stack([W.uniform_rank(r, count, dtype) for r in range(n)])
+        pool.load(x, dtype=dtype)
+        for i, algo in enumerate(orders):
+            op = "sum" if i % 2 == 0 else "max"
+            bufs = [to_dev(x[r]) for r in range(n)]
+            ar.check(ar.ar_allreduce(bufs, count=count, dtype=dtype, op=op, algo=algo), "sweep point")
+            torch.cuda.synchronize()
+            for r in range(1, n):
+                assert torch.equal(bufs[r], bufs[0]), (algo, r)
+            res0 = bufs[0].cpu().numpy()
+            if dtype == "bf16":
+                res0 = res0.view(np.uint16)
+            del bufs
+            pool.run(algo=ORACLE_ALGO.get(algo, algo), op=op)
+            cmp = pool.compare(res0)
+            assert cmp["bit_identical"], (n, nbytes, algo, op, cmp["differing_ranges"][:3])
+        del x
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("n,nbytes,dtype,op,algo", [
     (16, 256 << 20, "bf16", "sum", "ring"),
@@ -863,9 +902,11 @@ def test_int8_ef_unaligned_and_rejects(ar):
     (8, 512 << 20, "bf16", "sum", "dbtree"),
 ])
 def test_large_sweep_points_sampled(ar, n, nbytes, dtype, op, algo):
+    """Sweep points beyond 2 GiB in all: 2^20 seeded sample positions and
+    every chunk boundary +-2 carried through the oracle's messages."""
     es = 2 if dtype == "bf16" else 4
     count = nbytes // es
-    pos = sample_positions(count, n, 1 << 14, 11)
+    pos = sample_positions(count, n, 1 << 20, 11)
     if algo == "dbtree":
         pos = np.unique(np.concatenate([pos, [count // 2 - 1, count // 2]]))
     bufs, xs = [], []
@@ -901,7 +942,7 @@ def test_largest_sweep_point_sampled(ar, dtype, op, algo):
         pytest.skip("needs about 72 GiB of free device memory")
     es = 2 if dtype == "bf16" else 4
     count = nbytes // es
-    pos = sample_positions(count, n, 1 << 14, 12)
+    pos = sample_positions(count, n, 1 << 20, 12)
     idx = torch.from_numpy(pos).cuda()
     bufs = [W.uniform_rank_device(r, count, dtype, torch) for r in range(n)]
     xs = np.stack([b[idx].cpu().numpy() for b in bufs])
