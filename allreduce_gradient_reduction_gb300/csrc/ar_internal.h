@@ -102,6 +102,12 @@ inline int64_t smem_step_bytes(int nranks, int64_t count, int esize) {
 // 44.3 us, 8- and 16-rank trees at 4 KiB 16.2 -> 12.2 and 20.5 -> 14.5 us;
 // 1,024 elements per block tied, 2,048 and more lost).
 constexpr int64_t kClusterStepMaxBlockElems = 1024;
+// The same limit when every chunk is cut on a 16-byte boundary (count a
+// multiple of nranks * 16 / element size), so a step moves 16-byte vectors:
+// measured to win up to 4096 elements (8 x 64 KiB ring 28.8 -> 24.7 us,
+// 16 x 128 KiB ring 67.5 -> 51.3 us, 64 x 4 KiB tree 66.0 -> 18.6 us) and to
+// lose at 8192 (4 x 64 KiB ring 14.4 -> 18.3 us, 8 x 128 KiB 32.8 -> 38.7).
+constexpr int64_t kClusterStepMaxBlockElemsVec = 4096;
 // Blocks in the cluster for a row: the largest power of two that is at
 // least 2 and at most max_size and nranks, if its blocks hold the row and
 // no block folds more than kClusterStepMaxBlockElems elements in a step
@@ -115,7 +121,8 @@ inline int cluster_step_size(int nranks, int64_t count, int esize, int order, in
   const int64_t nloc = (nranks + c - 1) / c;
   if (nloc * stride > kSmemStepBytes) return 0;
   const int64_t per_rank = order == RING ? (count + nranks - 1) / nranks : order == TREE ? (count + 1) / 2 : count;
-  return nloc * per_rank <= kClusterStepMaxBlockElems ? c : 0;
+  const bool vec = count % ((int64_t)nranks * (16 / esize)) == 0;
+  return nloc * per_rank <= (vec ? kClusterStepMaxBlockElemsVec : kClusterStepMaxBlockElems) ? c : 0;
 }
 
 struct CopyArgs {

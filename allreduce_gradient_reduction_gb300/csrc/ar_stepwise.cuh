@@ -368,6 +368,9 @@ __global__ void __launch_bounds__(kClusterStepBlock) stepwise_cluster_kernel(con
   const int stride = (count * ES + 15) / 16 * 16;
   const int nloc = (n - me + C - 1) / C;  // ranks me, me + C, ...
   const int maxch = (count + n - 1) / n;  // elements of the largest chunk
+  constexpr int VEC = 16 / ES;
+  // chunks (and whole buffers) cut on 16-byte boundaries of the staged rows
+  const bool vmode = count % (n * VEC) == 0;
 
   // stage this block's ranks in (16-byte pieces when aligned, then the tail)
   const int nvec = a.vec ? count * ES / 16 : 0;
@@ -395,11 +398,64 @@ __global__ void __launch_bounds__(kClusterStepBlock) stepwise_cluster_kernel(con
     // per thread at a time so their remote loads are in flight together;
     // index arithmetic in 32 bits (count * nranks < 2^31 for rows this size)
     const bool whole = a.order == BINOMIAL;
-    const int per_ch = whole ? count : maxch;
     const int nch_max = ring || whole ? 1 : n / (2 << k);
+    constexpr int CU = 4;
+    if (vmode) {
+      // every chunk starts and ends on a 16-byte boundary: 16-byte items
+      const int per_ch = (whole ? count : maxch) / VEC;
+      const int span = nch_max * per_ch;
+      const int items = nloc * span;
+      for (int w0 = threadIdx.x; w0 < items; w0 += CU * kClusterStepBlock) {
+        uint4* pd[CU];
+        const uint4* ps[CU];
+        bool go[CU], src_first[CU];
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+          const int w = w0 + u * kClusterStepBlock;
+          go[u] = false;
+          pd[u] = nullptr;
+          ps[u] = nullptr;
+          src_first[u] = true;
+          if (w < items) {
+            const int l = w / span;
+            const int rem = w - l * span;
+            const int ci = rem / per_ch, offv = rem - ci * per_ch;
+            const int r = me + l * C;
+            const StepRecv v = step_recv(a.order, rs, s, k, n, r);
+            if (ci < v.nch) {
+              const int e = (v.whole ? 0 : (v.j0 + ci * v.jstep) * (count / n)) + offv * VEC;
+              go[u] = true;
+              pd[u] = reinterpret_cast<uint4*>(S + l * stride + e * ES);
+              ps[u] = cl.map_shared_rank(reinterpret_cast<uint4*>(S + (v.src / C) * stride + e * ES), v.src % C);
+              src_first[u] = ring || v.src < r;
+            }
+          }
+        }
+        uint4 x[CU], d[CU];
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+          if (go[u]) {
+            x[u] = *ps[u];
+            if (rs) d[u] = *pd[u];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+          if (!go[u]) continue;
+          uint4 y = x[u];
+          if (rs) {
+            y = src_first[u] ? step_vec<DT, OP>(x[u], d[u]) : step_vec<DT, OP>(d[u], x[u]);
+            if (avg) y = div_vec<DT>(y, a.fn);
+          }
+          *pd[u] = y;
+        }
+      }
+      cl.sync();
+      continue;
+    }
+    const int per_ch = whole ? count : maxch;
     const int span = nch_max * per_ch;
     const int items = nloc * span;
-    constexpr int CU = 4;
     for (int w0 = threadIdx.x; w0 < items; w0 += CU * kClusterStepBlock) {
       Wd* pd[CU];
       const Wd* ps[CU];

@@ -200,23 +200,29 @@ def test_binomial_stepwise_matches_oracle(ar, n, dtype):
 def cluster_form_counts(n, algo, es):
     """Counts whose plain step-wise call takes the cluster form: more than
     3072 element updates in a step or more than 160 KiB in all (so not one
-    block), the busiest block folding at most 1024 elements in a step, the
-    ranks spread over the largest power-of-two cluster of at most 16 blocks."""
+    block), the busiest block folding at most 1024 elements in a step (4096
+    when every chunk is cut on a 16-byte boundary and the steps move 16-byte
+    vectors), the ranks spread over the largest power-of-two cluster of at
+    most 16 blocks.  Both kinds of count are returned."""
     c = 2
     while c * 2 <= 16 and c * 2 <= n:
         c *= 2
     if c > n:
         return []
     nloc = -(-n // c)
-    out = []
-    for count in range(1, 40000, 7):
+    vec = 16 // es
+    out, out_vec = [], []
+    for count in list(range(1, 40000, 7)) + list(range(n * vec, 200000, n * vec)):
         stride = -(-count * es // 16) * 16
         step = count * (1 if algo.startswith("ring") else n // 2)
         one_block = step <= 3072 and n * stride <= 160 * 1024
         per_rank = -(-count // n) if algo.startswith("ring") else (-(-count // 2) if algo.startswith("tree") else count)
-        if not one_block and nloc * stride <= 160 * 1024 and nloc * per_rank <= 1024:
-            out.append(count)
-    return [out[0], out[len(out) // 2], out[-1]] if out else []
+        aligned = count % (n * vec) == 0
+        limit = 4096 if aligned else 1024
+        if not one_block and nloc * stride <= 160 * 1024 and nloc * per_rank <= limit:
+            (out_vec if aligned else out).append(count)
+    pick = lambda v: sorted({v[0], v[len(v) // 2], v[-1]}) if v else []
+    return pick(out) + pick(out_vec)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
