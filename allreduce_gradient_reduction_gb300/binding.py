@@ -12,6 +12,7 @@ Loading fails loudly: without the compiled library there is no fallback.
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 
@@ -105,8 +106,22 @@ def _ptr(x) -> int:
     return int(x.data_ptr())
 
 
+_ARRAY_TYPES = {}
+
+
 def _ptr_array(xs):
-    return (ctypes.c_void_p * max(len(xs), 1))(*[_ptr(x) for x in xs])
+    """A C array of the addresses of xs (tensors, addresses or None), built
+    over an array of 64-bit words: at 64 ranks about half the cost of ctypes'
+    element-by-element constructor."""
+    n = max(len(xs), 1)
+    t = _ARRAY_TYPES.get(n)
+    if t is None:
+        t = _ARRAY_TYPES[n] = ctypes.c_void_p * n
+    try:
+        addrs = [x.data_ptr() for x in xs]
+    except AttributeError:
+        addrs = [_ptr(x) for x in xs]
+    return t.from_buffer(array.array("Q", addrs or [0]))
 
 
 def _stream(s) -> int:

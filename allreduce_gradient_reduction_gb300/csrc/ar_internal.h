@@ -94,25 +94,39 @@ inline int64_t smem_step_bytes(int nranks, int64_t count, int esize) {
   return (int64_t)nranks * ((count * esize + 15) / 16 * 16);
 }
 // The cluster form spreads the ranks over the blocks of one thread-block
-// cluster (at most kSmemStepBytes of each block's shared memory).  It pays
-// while each block has little to fold per step: measured on GB300 against
-// the grid-barrier form (bf16, CUDA-graph replay), it won up to the point
-// where the busiest block folds about this many elements in its heaviest
-// step (64 ranks x 4 KiB ring: 274.6 -> 140 us, 16 x 16 KiB ring 65.6 ->
-// 44.3 us, 8- and 16-rank trees at 4 KiB 16.2 -> 12.2 and 20.5 -> 14.5 us;
-// 1,024 elements per block tied, 2,048 and more lost).
+// cluster (at most kSmemStepBytes of each block's shared memory).  A step
+// there costs a cluster barrier (about 1 us) plus the busiest block's folds
+// (about 0.22 ns per element with 16-byte vectors); a step of the
+// grid-barrier form costs 2-5.5 us whatever its size.  So the cluster form
+// pays while the busiest block folds few elements in an average step of the
+// schedule.  Measured on GB300 against the grid-barrier form (bf16,
+// CUDA-graph replay of 20 calls): with chunks cut on 16-byte boundaries
+// (count a multiple of nranks * 16 / element size) it won up to about 6144
+// elements per block per step (64 ranks x 16 KiB tree 66.0 -> 28.2 us,
+// 16 x 128 KiB ring 67.6 -> 51.2 us, 8 x 16 KiB tree 14.4 -> 11.2 us) and
+// lost from 7680 on (16 x 64 KiB tree 19.2 -> 23.8 us, 4 x 64 KiB ring
+// 14.4 -> 18.3 us, 8 x 128 KiB ring 32.8 -> 38.8 us).  Otherwise a step
+// moves one element at a time and the limit is the lower one.
 constexpr int64_t kClusterStepMaxBlockElems = 1024;
-// The same limit when every chunk is cut on a 16-byte boundary (count a
-// multiple of nranks * 16 / element size), so a step moves 16-byte vectors:
-// measured to win up to 4096 elements (8 x 64 KiB ring 28.8 -> 24.7 us,
-// 16 x 128 KiB ring 67.5 -> 51.3 us, 64 x 4 KiB tree 66.0 -> 18.6 us) and to
-// lose at 8192 (4 x 64 KiB ring 14.4 -> 18.3 us, 8 x 128 KiB 32.8 -> 38.7).
-constexpr int64_t kClusterStepMaxBlockElemsVec = 4096;
+constexpr int64_t kClusterStepMaxBlockElemsVec = 6144;
+// Elements the busiest of the cluster's blocks folds in an average step,
+// each block holding nloc ranks: ring, one chunk per rank in every step;
+// tree, count * (1 - 1/N) per rank over the log2(N) halving steps (and the
+// same over the doubling steps); binomial, up to a whole buffer per rank
+// in every step.
+inline int64_t cluster_step_mean_elems(int nranks, int64_t count, int order, int64_t nloc) {
+  if (order == RING) return nloc * ((count + nranks - 1) / nranks);
+  if (order == TREE) {
+    int levels = 0;
+    while ((2 << levels) <= nranks) ++levels;
+    return nloc * (count - count / nranks) / levels;
+  }
+  return nloc * count;
+}
 // Blocks in the cluster for a row: the largest power of two that is at
 // least 2 and at most max_size and nranks, if its blocks hold the row and
-// no block folds more than kClusterStepMaxBlockElems elements in a step
-// (ring: a chunk per rank; tree: half a buffer per rank in its first step;
-// binomial: a whole buffer); 0 otherwise.
+// the busiest block folds at most the limit above in an average step; 0
+// otherwise.
 inline int cluster_step_size(int nranks, int64_t count, int esize, int order, int max_size) {
   const int64_t stride = (count * esize + 15) / 16 * 16;
   int c = 2;
@@ -120,9 +134,9 @@ inline int cluster_step_size(int nranks, int64_t count, int esize, int order, in
   if (c > nranks || c > max_size) return 0;
   const int64_t nloc = (nranks + c - 1) / c;
   if (nloc * stride > kSmemStepBytes) return 0;
-  const int64_t per_rank = order == RING ? (count + nranks - 1) / nranks : order == TREE ? (count + 1) / 2 : count;
   const bool vec = count % ((int64_t)nranks * (16 / esize)) == 0;
-  return nloc * per_rank <= (vec ? kClusterStepMaxBlockElemsVec : kClusterStepMaxBlockElems) ? c : 0;
+  const int64_t limit = vec ? kClusterStepMaxBlockElemsVec : kClusterStepMaxBlockElems;
+  return cluster_step_mean_elems(nranks, count, order, nloc) <= limit ? c : 0;
 }
 
 struct CopyArgs {

@@ -200,10 +200,10 @@ def test_binomial_stepwise_matches_oracle(ar, n, dtype):
 def cluster_form_counts(n, algo, es):
     """Counts whose plain step-wise call takes the cluster form: more than
     3072 element updates in a step or more than 160 KiB in all (so not one
-    block), the busiest block folding at most 1024 elements in a step (4096
-    when every chunk is cut on a 16-byte boundary and the steps move 16-byte
-    vectors), the ranks spread over the largest power-of-two cluster of at
-    most 16 blocks.  Both kinds of count are returned."""
+    block), the busiest block folding at most 1024 elements in an average
+    step (6144 when every chunk is cut on a 16-byte boundary and the steps
+    move 16-byte vectors), the ranks spread over the largest power-of-two
+    cluster of at most 16 blocks.  Both kinds of count are returned."""
     c = 2
     while c * 2 <= 16 and c * 2 <= n:
         c *= 2
@@ -216,10 +216,15 @@ def cluster_form_counts(n, algo, es):
         stride = -(-count * es // 16) * 16
         step = count * (1 if algo.startswith("ring") else n // 2)
         one_block = step <= 3072 and n * stride <= 160 * 1024
-        per_rank = -(-count // n) if algo.startswith("ring") else (-(-count // 2) if algo.startswith("tree") else count)
+        if algo.startswith("ring"):
+            work = nloc * -(-count // n)
+        elif algo.startswith("tree"):
+            work = nloc * (count - count // n) // (n.bit_length() - 1)
+        else:
+            work = nloc * count
         aligned = count % (n * vec) == 0
-        limit = 4096 if aligned else 1024
-        if not one_block and nloc * stride <= 160 * 1024 and nloc * per_rank <= limit:
+        limit = 6144 if aligned else 1024
+        if not one_block and nloc * stride <= 160 * 1024 and work <= limit:
             (out_vec if aligned else out).append(count)
     pick = lambda v: sorted({v[0], v[len(v) // 2], v[-1]}) if v else []
     return pick(out) + pick(out_vec)
@@ -304,14 +309,15 @@ def test_unaligned_buffers(ar, algo, dtype):
 @pytest.mark.parametrize("n", [2, 3, 4, 5, 16, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_mixed_phase_rows(ar, n, dtype):
-    """Rank buffers at different addresses modulo 16 (the realigning vector
-    kernel: aligned words at each rank's own phase, shuffled into the first
-    buffer's frame, stored back at each rank's phase), in every order the
-    rank count allows, for AllReduce, ReduceScatter (owner store) and Reduce
-    (root store), over a size that spans many tiles and ends ragged.  Nothing
-    outside the buffers may change."""
+    """Rank buffers at different addresses modulo 16 (up to 8 ranks the
+    staged kernel: aligned words of every rank copied to shared memory,
+    folded in the first buffer's frame, stored back at each rank's phase;
+    more ranks the register-realigning ring), in every order the rank count
+    allows, for AllReduce, ReduceScatter (owner store) and Reduce (root
+    store), over a size whose chunks span several tiles and end ragged.
+    Nothing outside the buffers may change."""
     vec = 8 if dtype in HALF else 4
-    count = 3 * 248 * vec + 2048 * n + 13
+    count = 3 * 512 * vec * min(n, 8) + 2048 * n + 13
     x = inputs(n, count, dtype, "values", seed=41 + n)
     shifts = [(5 * r + 1) % vec for r in range(n)]
     algos = ["ring", "naive", "dbtree"] + (["tree"] if n & (n - 1) == 0 else [])
