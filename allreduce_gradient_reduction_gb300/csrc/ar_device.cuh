@@ -154,6 +154,14 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) { __stcs(rein
 __device__ __forceinline__ uint4 ld_l2(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ void st_l2(void* p, const uint4& v) { __stcg(reinterpret_cast<uint4*>(p), v); }
 
+// 16-byte global -> shared copy that bypasses L1; both addresses 16-byte
+// aligned.  cp_async_wait_all waits for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- single elements --------------------------------------------------------
 
 template <int ES>

@@ -18,6 +18,8 @@
 // values of a vector before it writes any, so working in place is safe.
 #pragma once
 
+#include <atomic>
+
 #include "ar_device.cuh"
 
 namespace ar {
@@ -496,6 +498,176 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
   }
 }
 
+// ---- rows whose buffers sit at different addresses modulo 16: staged form ----
+//
+// The same fold with the realignment done in shared memory instead of
+// registers.  A block takes a tile of kStageTileVecs vectors of the row's
+// frame (the first buffer's 16-byte grid).  (1) Every thread copies aligned
+// 16-byte words of every rank straight into shared memory (cp.async, no
+// registers), rank r's words from the one holding the tile's first byte in
+// buffer r: the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes
+// into rank r's slot.  (2) Each thread folds 4-byte words of the frame,
+// kFusedBlock apart (consecutive threads, consecutive words: no bank
+// conflicts): word w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its
+// slot, two word loads and a funnel shift when off_r is 2 mod 4, one load
+// otherwise.  (3) The results go to shared memory four times, the k-th copy
+// shifted by k words, so that for a destination at off = 4k + h bytes the
+// 16-byte word it needs at position i is one aligned 16-byte load of copy k
+// (plus, when h = 2, the last word of the position below, from the lane
+// below, and a funnel shift).  (4) Each thread stores whole aligned 16-byte
+// words of every destination; a destination's first and last word also hold
+// bytes of the neighbouring tiles and are written in part.  A block reads all
+// its inputs before its first store and writes only its tile's bytes, so
+// working in place is safe: bytes of a staged word outside the tile are never
+// used.
+constexpr int kStageTileVecs = 512;
+constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
+constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
+__host__ __device__ constexpr int stage_smem_bytes(int nr) {
+  return nr * kStageSlotBytes > 4 * kStageCopyBytes ? nr * kStageSlotBytes : 4 * kStageCopyBytes;
+}
+
+template <class ARGS, int DT, int OP, int ORDER, int NR>
+__global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kernel(const __grid_constant__ ARGS a) {
+  constexpr int ES = ElemSize<DT>::value;
+  constexpr int VEC = 16 / ES;
+  constexpr int TV = kStageTileVecs;
+  constexpr int G = TV * 4 / kFusedBlock / 4;  // groups of 4 frame words per thread
+  static_assert(G * 4 * kFusedBlock == TV * 4, "tile is a whole number of word groups");
+  extern __shared__ __align__(16) unsigned char S[];
+  pdl_prologue();
+  const auto& T = a.tab;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+
+  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
+    const Seg& s = T.seg[find_seg(T, tile)];
+    const void* const* P = T.ptr + (size_t)s.tensor * NR;
+    const int shift = row_shift(P[0], ES);
+    const SegShape sh = seg_shape<VEC>(s, shift);
+    const int64_t ti = tile - s.tile_begin;
+    const int c = s.chunk;
+    const int64_t t0 = sh.vb + ti * TV;
+    const int nv = (int)(sh.ve - t0 < TV ? sh.ve - t0 : TV);  // vectors in this tile (<= 0: scalars only)
+    const int64_t base = t0 * 16 - shift * ES;                 // vector t0 in every buffer, aligned in P[0]
+
+    if (nv > 0) {
+      // (1) rank r's aligned words [0, nv + (off_r != 0)) into slot r
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const int off = byte_phase(P[r], P[0]);
+        const char* g = static_cast<const char*>(P[r]) + base - off;
+        const int nw = nv + (off != 0);
+        for (int i = tid; i < nw; i += kFusedBlock) cp_async16(S + r * kStageSlotBytes + i * 16, g + i * 16);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+
+      // (2) fold frame words w = tid + (4j + k) * kFusedBlock, k = 0..3, of group j
+      auto word = [&](int r, int w) -> uint32_t {
+        const int off = byte_phase(P[r], P[0]);
+        const uint32_t* sl = reinterpret_cast<const uint32_t*>(S + r * kStageSlotBytes) + (off >> 2) + w;
+        if constexpr (ES == 4) {
+          return sl[0];
+        } else {
+          return __funnelshift_r(sl[0], sl[1], (uint32_t)(off & 2) * 8);
+        }
+      };
+      auto group = [&](int r, int j) -> uint4 {
+        const int w = tid + 4 * j * kFusedBlock;
+        return make_uint4(word(r, w), word(r, w + kFusedBlock), word(r, w + 2 * kFusedBlock),
+                          word(r, w + 3 * kFusedBlock));
+      };
+      uint4 res[G];
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        if constexpr (ORDER == RING) {
+          res[j] = group(rot(c + 1, NR), j);
+#pragma unroll
+          for (int p = 1; p < NR; ++p) res[j] = step_vec<DT, OP>(res[j], group(rot(c + 1 + p, NR), j));
+        } else if constexpr (ORDER == DBTREE) {
+          const int rank_shift = c == 0 ? 0 : 1;
+          uint4 x[NR];
+#pragma unroll
+          for (int p = 0; p < NR; ++p) x[p] = group(rot(p + rank_shift, NR), j);
+          res[j] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x);
+        } else {
+          uint4 x[NR];
+#pragma unroll
+          for (int p = 0; p < NR; ++p) x[p] = group(p, j);
+          res[j] = tree_fold_regs<DT, OP, NR>(x);
+        }
+        if (a.avg) res[j] = div_vec<DT>(res[j], a.fn);
+      }
+      __syncthreads();  // every slot has been read
+
+      // (3) copy k holds frame word m at word index m + k + 4
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t* cp = reinterpret_cast<uint32_t*>(S + k * kStageCopyBytes) + k + 4 + tid;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          cp[(4 * j + 0) * kFusedBlock] = res[j].x;
+          cp[(4 * j + 1) * kFusedBlock] = res[j].y;
+          cp[(4 * j + 2) * kFusedBlock] = res[j].z;
+          cp[(4 * j + 3) * kFusedBlock] = res[j].w;
+        }
+      }
+      __syncthreads();
+
+      // (4) destination word i of rank r: bytes [16i, 16i + 16) from the
+      // aligned word holding the tile's first byte, i.e. frame bytes
+      // [16i - off, 16i + 16 - off): words 4i - k .. 4i - k + 3 (entry i + 1
+      // of copy k) and, for h = 2, word 4i - k - 1 (entry i of copy k, .w)
+      auto put = [&](int r) {
+        const int off = byte_phase(P[r], P[0]);
+        const int k = off >> 2;
+        const uint32_t hs = (uint32_t)(off & 2) * 8;
+        const uint4* cp = reinterpret_cast<const uint4*>(S + k * kStageCopyBytes);
+        char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
+        const int nw = nv + (off != 0);
+        for (int i0 = tid - lane; i0 < nw; i0 += kFusedBlock) {  // whole warps: the shuffle needs every lane
+          const int i = i0 + lane;
+          const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
+          const uint4 cur = cp[ic + 1];
+          uint4 v = cur;
+          if (ES == 2 && hs) {
+            uint32_t prev = __shfl_up_sync(0xffffffffu, cur.w, 1);
+            if (lane == 0) prev = cp[ic].w;
+            v = make_uint4(__funnelshift_l(prev, cur.x, 16), __funnelshift_l(cur.x, cur.y, 16),
+                           __funnelshift_l(cur.y, cur.z, 16), __funnelshift_l(cur.z, cur.w, 16));
+          }
+          if (i >= nw) continue;
+          if (off != 0 && i == 0) st_stream_part(g, v, off, 16);
+          else if (off != 0 && i == nv) st_stream_part(g + 16 * (int64_t)i, v, 0, off);
+          else st_stream(g + 16 * (int64_t)i, v);
+        }
+      };
+      if (a.owner_only || a.to_root) {
+        put(a.owner_only ? c : a.root);
+      } else {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) put(r);
+      }
+    }
+
+    // elements of the segment outside its full vectors
+    if (ti == 0 && tid < sh.head + sh.tail) {
+      const int64_t e = scalar_elem<VEC>(s, sh, tid, shift);
+      uint32_t r = fold_scalar<DT, OP, ORDER>(P, NR, c, e);
+      if (a.avg) r = div_word<DT>(r, a.fn);
+      if (a.owner_only || a.to_root) {
+        st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
+      } else {
+        for (int q = 0; q < NR; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+      }
+    }
+    // the next tile's copies overwrite shared memory every thread has
+    // finished reading
+    if (tile + gridDim.x < T.ntiles) __syncthreads();
+  }
+}
+
 // Same computation element by element, for rows whose buffers sit at
 // different addresses modulo 16.  Each thread takes kScalarUnroll elements of
 // a tile, kFusedBlock apart.  In ring order (the naive order too) it walks the
@@ -592,11 +764,12 @@ inline int64_t fill_tiles(TABLE& t, int vec, int64_t tile_units, bool shifted = 
 // 34.9 -> 32.7 us and Broadcast 34.8 -> 32.5 us; a 4 x 16 KiB call replayed
 // from a CUDA graph 1.65 -> 1.78 us.
 template <typename K, typename ARGS>
-inline cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, cudaStream_t stream, const ARGS& a) {
+inline cudaError_t launch_pdl(K kernel, unsigned grid, unsigned block, cudaStream_t stream, const ARGS& a,
+                              size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -629,6 +802,26 @@ cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
                     stream, a);
 }
 
+template <int DT, int OP, int ORDER, int NR, class ARGS>
+cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
+  constexpr int kSmem = stage_smem_bytes(NR);
+  auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR>;
+  // opened once per device to the shared memory the kernel uses
+  static std::atomic<bool> opened[256];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  if (!opened[dev].load()) {
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
+      return e;
+    opened[dev].store(true);
+  }
+  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kStageTileVecs, true) == 0) return cudaSuccess;
+  count_launch();
+  return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, stream, a, (size_t)kSmem);
+}
+
 // Rows whose buffers sit at different addresses modulo 16 (every order up to
 // 8 ranks; rings of any size through the runtime-N form).  Returns
 // cudaErrorNotSupported where no such form is compiled (trees of 16 or more
@@ -641,15 +834,15 @@ template <int DT, int OP, class ARGS>
 cudaError_t launch_fused_shift_typed(int order, ARGS& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
   switch (order * 100 + n) {
-    case RING * 100 + 2: return launch_fused_vec<DT, OP, RING, 2, ARGS, true>(a, stream);
-    case RING * 100 + 4: return launch_fused_vec<DT, OP, RING, 4, ARGS, true>(a, stream);
-    case RING * 100 + 8: return launch_fused_vec<DT, OP, RING, 8, ARGS, true>(a, stream);
-    case TREE * 100 + 2: return launch_fused_vec<DT, OP, TREE, 2, ARGS, true>(a, stream);
-    case TREE * 100 + 4: return launch_fused_vec<DT, OP, TREE, 4, ARGS, true>(a, stream);
-    case TREE * 100 + 8: return launch_fused_vec<DT, OP, TREE, 8, ARGS, true>(a, stream);
-    case DBTREE * 100 + 2: return launch_fused_vec<DT, OP, DBTREE, 2, ARGS, true>(a, stream);
-    case DBTREE * 100 + 4: return launch_fused_vec<DT, OP, DBTREE, 4, ARGS, true>(a, stream);
-    case DBTREE * 100 + 8: return launch_fused_vec<DT, OP, DBTREE, 8, ARGS, true>(a, stream);
+    case RING * 100 + 2: return launch_fused_stage<DT, OP, RING, 2>(a, stream);
+    case RING * 100 + 4: return launch_fused_stage<DT, OP, RING, 4>(a, stream);
+    case RING * 100 + 8: return launch_fused_stage<DT, OP, RING, 8>(a, stream);
+    case TREE * 100 + 2: return launch_fused_stage<DT, OP, TREE, 2>(a, stream);
+    case TREE * 100 + 4: return launch_fused_stage<DT, OP, TREE, 4>(a, stream);
+    case TREE * 100 + 8: return launch_fused_stage<DT, OP, TREE, 8>(a, stream);
+    case DBTREE * 100 + 2: return launch_fused_stage<DT, OP, DBTREE, 2>(a, stream);
+    case DBTREE * 100 + 4: return launch_fused_stage<DT, OP, DBTREE, 4>(a, stream);
+    case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
     default: break;
   }
   if (order == RING) return launch_fused_vec<DT, OP, RING, 0, ARGS, true>(a, stream);

@@ -64,11 +64,6 @@ __device__ __forceinline__ int chunk_of(int64_t e, int64_t count, int n) {
   return (int)(((e + 1) * n - 1) / count);  // the chunk [floor(cD/N), floor((c+1)D/N)) holding e
 }
 
-// 16-byte global -> shared copy that bypasses L1; both addresses 16-byte aligned
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // waits until at most K of this thread's committed groups are still in flight
 template <int K>
