@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 // registers), rank r's words from the one holding the tile's first byte in
 // buffer r: the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes
 // into rank r's slot.  (2) Each thread folds 4-byte words of the frame,
-// kFusedBlock apart (consecutive threads, consecutive words: no bank
+// kStageBlock apart (consecutive threads, consecutive words: no bank
 // conflicts): word w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its
 // slot, two word loads and a funnel shift when off_r is 2 mod 4, one load
 // otherwise.  (3) The results go to shared memory four times, the k-th copy
@@ -520,6 +520,8 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 // its inputs before its first store and writes only its tile's bytes, so
 // working in place is safe: bytes of a staged word outside the tile are never
 // used.
+constexpr int kStageBlock = 256;
+__host__ __device__ constexpr int stage_min_blocks(int nr) { return nr == 8 ? 3 : 4; }
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
@@ -528,12 +530,12 @@ __host__ __device__ constexpr int stage_smem_bytes(int nr) {
 }
 
 template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kernel(const __grid_constant__ ARGS a) {
+__global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int TV = kStageTileVecs;
-  constexpr int G = TV * 4 / kFusedBlock / 4;  // groups of 4 frame words per thread
-  static_assert(G * 4 * kFusedBlock == TV * 4, "tile is a whole number of word groups");
+  constexpr int G = TV * 4 / kStageBlock / 4;  // groups of 4 frame words per thread
+  static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
   const auto& T = a.tab;
@@ -552,18 +554,25 @@ __global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kern
     const int64_t base = t0 * 16 - shift * ES;                 // vector t0 in every buffer, aligned in P[0]
 
     if (nv > 0) {
-      // (1) rank r's aligned words [0, nv + (off_r != 0)) into slot r
+      // (1) rank r's aligned words [0, nv + (off_r != 0)) into slot r, one
+      // commit group per rank in the order the fold takes them
+      const int rank_shift = ORDER == DBTREE && c != 0 ? 1 : 0;
+      auto rank_at = [&](int p) -> int {
+        if constexpr (ORDER == RING) return rot(c + 1 + p, NR);
+        else if constexpr (ORDER == DBTREE) return rot(p + rank_shift, NR);
+        else return p;
+      };
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
+      for (int p = 0; p < NR; ++p) {
+        const int r = rank_at(p);
         const int off = byte_phase(P[r], P[0]);
         const char* g = static_cast<const char*>(P[r]) + base - off;
         const int nw = nv + (off != 0);
-        for (int i = tid; i < nw; i += kFusedBlock) cp_async16(S + r * kStageSlotBytes + i * 16, g + i * 16);
+        for (int i = tid; i < nw; i += kStageBlock) cp_async16(S + r * kStageSlotBytes + i * 16, g + i * 16);
+        cp_async_commit();
       }
-      cp_async_wait_all();
-      __syncthreads();
 
-      // (2) fold frame words w = tid + (4j + k) * kFusedBlock, k = 0..3, of group j
+      // (2) fold frame words w = tid + (4j + k) * kStageBlock, k = 0..3, of group j
       auto word = [&](int r, int w) -> uint32_t {
         const int off = byte_phase(P[r], P[0]);
         const uint32_t* sl = reinterpret_cast<const uint32_t*>(S + r * kStageSlotBytes) + (off >> 2) + w;
@@ -574,30 +583,57 @@ __global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kern
         }
       };
       auto group = [&](int r, int j) -> uint4 {
-        const int w = tid + 4 * j * kFusedBlock;
-        return make_uint4(word(r, w), word(r, w + kFusedBlock), word(r, w + 2 * kFusedBlock),
-                          word(r, w + 3 * kFusedBlock));
+        const int w = tid + 4 * j * kStageBlock;
+        return make_uint4(word(r, w), word(r, w + kStageBlock), word(r, w + 2 * kStageBlock),
+                          word(r, w + 3 * kStageBlock));
       };
       uint4 res[G];
+      if constexpr (ORDER == DBTREE) {
+        // the in-order tree needs every rank at once
+        cp_async_wait_all();
+        __syncthreads();
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        if constexpr (ORDER == RING) {
-          res[j] = group(rot(c + 1, NR), j);
-#pragma unroll
-          for (int p = 1; p < NR; ++p) res[j] = step_vec<DT, OP>(res[j], group(rot(c + 1 + p, NR), j));
-        } else if constexpr (ORDER == DBTREE) {
-          const int rank_shift = c == 0 ? 0 : 1;
+        for (int j = 0; j < G; ++j) {
           uint4 x[NR];
 #pragma unroll
-          for (int p = 0; p < NR; ++p) x[p] = group(rot(p + rank_shift, NR), j);
+          for (int p = 0; p < NR; ++p) x[p] = group(rank_at(p), j);
           res[j] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x);
-        } else {
-          uint4 x[NR];
-#pragma unroll
-          for (int p = 0; p < NR; ++p) x[p] = group(p, j);
-          res[j] = tree_fold_regs<DT, OP, NR>(x);
         }
-        if (a.avg) res[j] = div_vec<DT>(res[j], a.fn);
+      } else {
+        // rank p is folded as soon as its copies have landed, while the
+        // later ranks' copies are still in flight; the tree keeps finished
+        // subtrees on a stack (a binary counter over the rank index), which
+        // is the same balanced pairwise tree
+        uint4 stk[G][ORDER == RING ? 1 : 4];
+        int top = 0;
+#pragma unroll
+        for (int p = 0; p < NR; ++p) {
+          cp_async_wait_pending(NR - 1 - p);
+          __syncthreads();
+          const int r = rank_at(p);
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            uint4 v = group(r, j);
+            if constexpr (ORDER == RING) {
+              stk[j][0] = p == 0 ? v : step_vec<DT, OP>(stk[j][0], v);
+            } else {
+              int t = top;
+#pragma unroll
+              for (int k = p; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[j][--t], v);
+              stk[j][t] = v;
+            }
+          }
+          if constexpr (ORDER != RING) {
+            for (int k = p; k & 1; k >>= 1) --top;
+            ++top;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) res[j] = stk[j][0];
+      }
+      if (a.avg) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) res[j] = div_vec<DT>(res[j], a.fn);
       }
       __syncthreads();  // every slot has been read
 
@@ -607,10 +643,10 @@ __global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kern
         uint32_t* cp = reinterpret_cast<uint32_t*>(S + k * kStageCopyBytes) + k + 4 + tid;
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-          cp[(4 * j + 0) * kFusedBlock] = res[j].x;
-          cp[(4 * j + 1) * kFusedBlock] = res[j].y;
-          cp[(4 * j + 2) * kFusedBlock] = res[j].z;
-          cp[(4 * j + 3) * kFusedBlock] = res[j].w;
+          cp[(4 * j + 0) * kStageBlock] = res[j].x;
+          cp[(4 * j + 1) * kStageBlock] = res[j].y;
+          cp[(4 * j + 2) * kStageBlock] = res[j].z;
+          cp[(4 * j + 3) * kStageBlock] = res[j].w;
         }
       }
       __syncthreads();
@@ -626,7 +662,7 @@ __global__ void __launch_bounds__(kFusedBlock, NR == 8 ? 3 : 4) fused_stage_kern
         const uint4* cp = reinterpret_cast<const uint4*>(S + k * kStageCopyBytes);
         char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
         const int nw = nv + (off != 0);
-        for (int i0 = tid - lane; i0 < nw; i0 += kFusedBlock) {  // whole warps: the shuffle needs every lane
+        for (int i0 = tid - lane; i0 < nw; i0 += kStageBlock) {  // whole warps: the shuffle needs every lane
           const int i = i0 + lane;
           const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
           const uint4 cur = cp[ic + 1];
@@ -819,7 +855,7 @@ cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
   }
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kStageTileVecs, true) == 0) return cudaSuccess;
   count_launch();
-  return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, stream, a, (size_t)kSmem);
+  return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kStageBlock, stream, a, (size_t)kSmem);
 }
 
 // Rows whose buffers sit at different addresses modulo 16 (every order up to

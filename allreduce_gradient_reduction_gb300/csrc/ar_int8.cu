@@ -64,12 +64,6 @@ __device__ __forceinline__ int chunk_of(int64_t e, int64_t count, int n) {
   return (int)(((e + 1) * n - 1) / count);  // the chunk [floor(cD/N), floor((c+1)D/N)) holding e
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// waits until at most K of this thread's committed groups are still in flight
-template <int K>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
-}
 
 struct Lane4 {
   float v[4];
