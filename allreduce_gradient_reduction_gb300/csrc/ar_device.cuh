@@ -181,6 +181,23 @@ __device__ __forceinline__ void cp_async_wait_pending(int k) {
   }
 }
 
+// Bulk shared -> global copy (the tensor-memory-access engine, no tensor
+// map): both addresses 16-byte aligned, a size that is a multiple of 16.
+// The shared data must be made visible to the async proxy first
+// (fence_proxy_async_shared by the threads that wrote it, then a block
+// barrier).  bulk_commit closes this thread's group of bulk copies;
+// bulk_wait_read waits until they have read their shared memory,
+// bulk_wait_all until their writes are done.
+__device__ __forceinline__ void bulk_store(void* gmem, const void* smem, uint32_t bytes) {
+  const unsigned sa = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem), "r"(sa), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- single elements --------------------------------------------------------
 
 template <int ES>

@@ -514,9 +514,11 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 // shifted by k words, so that for a destination at off = 4k + h bytes the
 // 16-byte word it needs at position i is one aligned 16-byte load of copy k
 // (plus, when h = 2, the last word of the position below, from the lane
-// below, and a funnel shift).  (4) Each thread stores whole aligned 16-byte
-// words of every destination; a destination's first and last word also hold
-// bytes of the neighbouring tiles and are written in part.  A block reads all
+// below, and a funnel shift).  (4) A destination with h = 0 is a run of
+// whole entries of copy k: one bulk copy (cp.async.bulk, the
+// tensor-memory-access engine) writes it; with h = 2 each thread stores
+// whole aligned 16-byte words it shifted.  A destination's first and last
+// word also hold bytes of the neighbouring tiles and are written in part.  A block reads all
 // its inputs before its first store and writes only its tile's bytes, so
 // working in place is safe: bytes of a staged word outside the tile are never
 // used.
@@ -649,6 +651,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           cp[(4 * j + 3) * kStageBlock] = res[j].w;
         }
       }
+      fence_proxy_async_shared();  // the bulk copies read them through the async proxy
       __syncthreads();
 
       // (4) destination word i of rank r: bytes [16i, 16i + 16) from the
@@ -662,21 +665,30 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         const uint4* cp = reinterpret_cast<const uint4*>(S + k * kStageCopyBytes);
         char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
         const int nw = nv + (off != 0);
-        for (int i0 = tid - lane; i0 < nw; i0 += kStageBlock) {  // whole warps: the shuffle needs every lane
-          const int i = i0 + lane;
-          const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
-          const uint4 cur = cp[ic + 1];
-          uint4 v = cur;
-          if (ES == 2 && hs) {
+        if (ES == 4 || hs == 0) {
+          // a whole number of words off: destination word i is entry i + 1
+          // of copy k, so its whole words leave in one bulk copy; the two
+          // partial words by plain stores
+          const int lo = off != 0;
+          if (tid == 0 && nv > lo) bulk_store(g + 16 * lo, cp + lo + 1, 16 * (nv - lo));
+          if (off != 0 && tid == 32) st_stream_part(g, cp[1], off, 16);
+          if (off != 0 && tid == 64) st_stream_part(g + 16 * (int64_t)nv, cp[nv + 1], 0, off);
+          return;
+        }
+        if constexpr (ES == 2) {  // 2 mod 4 bytes off: each word shifted by one element
+          for (int i0 = tid - lane; i0 < nw; i0 += kStageBlock) {  // whole warps: the shuffle needs every lane
+            const int i = i0 + lane;
+            const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
+            const uint4 cur = cp[ic + 1];
             uint32_t prev = __shfl_up_sync(0xffffffffu, cur.w, 1);
             if (lane == 0) prev = cp[ic].w;
-            v = make_uint4(__funnelshift_l(prev, cur.x, 16), __funnelshift_l(cur.x, cur.y, 16),
-                           __funnelshift_l(cur.y, cur.z, 16), __funnelshift_l(cur.z, cur.w, 16));
+            const uint4 v = make_uint4(__funnelshift_l(prev, cur.x, 16), __funnelshift_l(cur.x, cur.y, 16),
+                                       __funnelshift_l(cur.y, cur.z, 16), __funnelshift_l(cur.z, cur.w, 16));
+            if (i >= nw) continue;
+            if (i == 0) st_stream_part(g, v, off, 16);
+            else if (i == nv) st_stream_part(g + 16 * (int64_t)i, v, 0, off);
+            else st_stream(g + 16 * (int64_t)i, v);
           }
-          if (i >= nw) continue;
-          if (off != 0 && i == 0) st_stream_part(g, v, off, 16);
-          else if (off != 0 && i == nv) st_stream_part(g + 16 * (int64_t)i, v, 0, off);
-          else st_stream(g + 16 * (int64_t)i, v);
         }
       };
       if (a.owner_only || a.to_root) {
@@ -685,6 +697,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
 #pragma unroll
         for (int r = 0; r < NR; ++r) put(r);
       }
+      if (tid == 0) bulk_commit();
     }
 
     // elements of the segment outside its full vectors
@@ -698,10 +711,14 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         for (int q = 0; q < NR; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
       }
     }
-    // the next tile's copies overwrite shared memory every thread has
-    // finished reading
-    if (tile + gridDim.x < T.ntiles) __syncthreads();
+    // the next tile's copies overwrite shared memory every thread and every
+    // bulk copy has finished reading
+    if (tile + gridDim.x < T.ntiles) {
+      if (tid == 0) bulk_wait_read();
+      __syncthreads();
+    }
   }
+  if (tid == 0) bulk_wait_all();
 }
 
 // Same computation element by element, for rows whose buffers sit at
