@@ -527,8 +527,13 @@ __host__ __device__ constexpr int stage_min_blocks(int nr) { return nr == 8 ? 3 
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
-__host__ __device__ constexpr int stage_smem_bytes(int nr) {
-  return nr * kStageSlotBytes > 4 * kStageCopyBytes ? nr * kStageSlotBytes : 4 * kStageCopyBytes;
+// Eight copies (the four word shifts of the result and of the result moved
+// by one 2-byte element) for 8-rank rows of 2-byte elements, whose slots
+// leave room for them; four otherwise.
+__host__ __device__ constexpr int stage_copies(int es, int nr) { return es == 2 && nr == 8 ? 8 : 4; }
+__host__ __device__ constexpr int stage_smem_bytes(int nr, int es) {
+  return nr * kStageSlotBytes > stage_copies(es, nr) * kStageCopyBytes ? nr * kStageSlotBytes
+                                                                         : stage_copies(es, nr) * kStageCopyBytes;
 }
 
 template <class ARGS, int DT, int OP, int ORDER, int NR>
@@ -651,6 +656,36 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           cp[(4 * j + 3) * kStageBlock] = res[j].w;
         }
       }
+      constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
+      if constexpr (kHalfCopies) {
+        // copies 4..7: the same with frame word m replaced by its last
+        // element followed by the first of word m + 1 ... that is, word m
+        // of the stream one element earlier: funnel(word m - 1, word m)
+        __syncthreads();  // lane 0 reads the word below from copy 0
+        const uint32_t* c0 = reinterpret_cast<const uint32_t*>(S) + 4 + tid;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          uint32_t f[4] = {res[j].x, res[j].y, res[j].z, res[j].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int m_off = (4 * j + q) * kStageBlock;  // this thread's word m = tid + m_off
+            uint32_t below = __shfl_up_sync(0xffffffffu, f[q], 1);
+            if (lane == 0) below = c0[m_off - 1];
+            const uint32_t h = __funnelshift_l(below, f[q], 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              reinterpret_cast<uint32_t*>(S + (4 + k) * kStageCopyBytes)[k + 4 + tid + m_off] = h;
+          }
+        }
+        // one word past the tile: a full tile's last destination word starts
+        // with the last element of its last frame word
+        if (tid == kStageBlock - 1) {
+          const uint32_t h = __funnelshift_l(res[G - 1].w, 0u, 16);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            reinterpret_cast<uint32_t*>(S + (4 + k) * kStageCopyBytes)[k + 4 + 4 * TV] = h;
+        }
+      }
       fence_proxy_async_shared();  // the bulk copies read them through the async proxy
       __syncthreads();
 
@@ -662,10 +697,10 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         const int off = byte_phase(P[r], P[0]);
         const int k = off >> 2;
         const uint32_t hs = (uint32_t)(off & 2) * 8;
-        const uint4* cp = reinterpret_cast<const uint4*>(S + k * kStageCopyBytes);
+        const uint4* cp = reinterpret_cast<const uint4*>(S + ((kHalfCopies && hs ? 4 : 0) + k) * kStageCopyBytes);
         char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
         const int nw = nv + (off != 0);
-        if (ES == 4 || hs == 0) {
+        if (ES == 4 || hs == 0 || kHalfCopies) {
           // a whole number of words off: destination word i is entry i + 1
           // of copy k, so its whole words leave in one bulk copy; the two
           // partial words by plain stores
@@ -675,7 +710,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           if (off != 0 && tid == 64) st_stream_part(g + 16 * (int64_t)nv, cp[nv + 1], 0, off);
           return;
         }
-        if constexpr (ES == 2) {  // 2 mod 4 bytes off: each word shifted by one element
+        if constexpr (ES == 2 && !kHalfCopies) {  // 2 mod 4 bytes off: each word shifted by one element
           for (int i0 = tid - lane; i0 < nw; i0 += kStageBlock) {  // whole warps: the shuffle needs every lane
             const int i = i0 + lane;
             const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
@@ -857,7 +892,7 @@ cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
 
 template <int DT, int OP, int ORDER, int NR, class ARGS>
 cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
-  constexpr int kSmem = stage_smem_bytes(NR);
+  constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value);
   auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR>;
   // opened once per device to the shared memory the kernel uses
   static std::atomic<bool> opened[256];
