@@ -523,7 +523,13 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 // working in place is safe: bytes of a staged word outside the tile are never
 // used.
 constexpr int kStageBlock = 256;
-__host__ __device__ constexpr int stage_min_blocks(int nr) { return nr == 8 ? 3 : 4; }
+// Resident blocks per SM: as many as shared memory allows, since the tiles
+// in flight are what keeps HBM busy (three at 8 ranks, 66 KB each; six below,
+// 33 KB each, at 40 registers without spills).  Measured, 2-byte elements at
+// eight offsets: 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 /
+// 89.3 / 83.9 us at four / five / six blocks; 8 x 128 MiB 446.7 us at two,
+// 351.4 at three (before the bulk stores).
+__host__ __device__ constexpr int stage_min_blocks(int nr) { return nr == 8 ? 3 : 6; }
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
