@@ -180,8 +180,8 @@ static cudaError_t launch_fused_shift_any(int dtype, int op, int order, ARGS& a,
 }
 
 // `vec`: every row's buffers share their address modulo 16.  Rows that do
-// not take the realigning vector form where one is compiled, else the
-// element-wise kernel.
+// not take the staged kernel where its form exists (shift_form_exists),
+// else the element-wise kernel.
 template <class ARGS>
 static cudaError_t launch_fused_any(int dtype, int op, int order, bool vec, ARGS& a, cudaStream_t s) {
   if (!vec && shift_form_exists(order, a.tab.nranks)) return launch_fused_shift_any(dtype, op, order, a, s);

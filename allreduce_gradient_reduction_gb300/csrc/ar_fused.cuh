@@ -115,92 +115,15 @@ __device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
   return acc;
 }
 
-// ---- rows whose buffers sit at different addresses modulo 16 -----------------
-//
-// The row's first buffer sets the frame: vector v covers elements
-// [v*VEC - shift, (v+1)*VEC - shift), shift = row_shift(P[0]).  In buffer p
-// those elements begin `off_p` = (P[p] - P[0]) mod 16 bytes into an aligned
-// 16-byte word and run into the next word.  Every lane of a warp loads, from
-// every buffer, the aligned word holding the start of its vector and takes
-// the next word from the lane above (a shuffle); lanes 0..30 fold, lane 31
-// only loads.  Results go back the same way: the aligned word of buffer q
-// that begins off_q bytes before vector v holds the end of vector v-1 (from
-// the lane below, a shuffle) and the start of v.  Warps start 30 vectors
-// apart, so neighbouring warps of a block both fold the vector where they
-// meet; a warp writes its vectors 0..29 to the buffers at the frame's phase,
-// and the words that begin in its vectors 1..30 to the others, whole.  A
-// block barrier between the folds and the stores keeps every warp's reads
-// before any warp's writes.  A block writes only the elements of its own
-// tile: the words at a tile's two ends are written in part, the rest of
-// each by the neighbouring tile (or, at a segment's ends, by the element-wise
-// edge code).  Bytes of a loaded word outside the tile are never used, so no
-// value a block uses was written by another block.
-constexpr int kShiftWarpVecs = 30;  // vectors a warp owns (it folds one more)
-constexpr int kShiftTileVecs = (kFusedBlock / 32) * kShiftWarpVecs;
+// ---- helpers for rows whose buffers sit at different addresses modulo 16 ------
 
+// Offset of buffer p from the row's first buffer within a 16-byte word.
 __device__ __forceinline__ int byte_phase(const void* p, const void* p0) {
   return (int)(((uintptr_t)p - (uintptr_t)p0) & 15);
 }
 
-// The five consecutive words c[0..4] of a stream starting K words into a
-// lane's own 16 bytes (w), continuing into the next lane's (a shuffle each:
-// only the words the case needs are exchanged), and the bytes [sh/8, sh/8 +
-// 16) of c as one vector.  K and sh are the same in every lane of the warp.
-__device__ __forceinline__ uint32_t fs(uint32_t lo, uint32_t hi, uint32_t sh) { return __funnelshift_r(lo, hi, sh); }
-__device__ __forceinline__ uint32_t shd(uint32_t v) { return __shfl_down_sync(0xffffffffu, v, 1); }
-
-// This lane's 16 bytes of a stream whose elements begin `off` bytes into
-// the lane's aligned word w (off a multiple of the element size, 0 < off <
-// 16, the same in every lane), the rest coming from the lane above.
-template <int ES>
-__device__ __forceinline__ uint4 realign_from_next(const uint4& w, int off) {
-  const uint32_t sh = ES == 2 ? (uint32_t)(off & 2) * 8 : 0u;
-  uint32_t c0, c1, c2, c3, c4 = 0;
-  switch (off >> 2) {
-    case 0:
-      c0 = w.x, c1 = w.y, c2 = w.z, c3 = w.w;
-      if (ES == 2) c4 = shd(w.x);
-      break;
-    case 1:
-      c0 = w.y, c1 = w.z, c2 = w.w, c3 = shd(w.x);
-      if (ES == 2) c4 = shd(w.y);
-      break;
-    case 2:
-      c0 = w.z, c1 = w.w, c2 = shd(w.x), c3 = shd(w.y);
-      if (ES == 2) c4 = shd(w.z);
-      break;
-    default:
-      c0 = w.w, c1 = shd(w.x), c2 = shd(w.y), c3 = shd(w.z);
-      if (ES == 2) c4 = shd(w.w);
-      break;
-  }
-  if constexpr (ES == 4) return make_uint4(c0, c1, c2, c3);
-  else return make_uint4(fs(c0, c1, sh), fs(c1, c2, sh), fs(c2, c3, sh), fs(c3, c4, sh));
-}
-
-// Bytes [off, off + 16) of the 32 bytes lo:hi (little-endian; off a
-// multiple of the element size in [0, 16), the same in every lane).
-template <int ES>
-__device__ __forceinline__ uint4 bytes_at(const uint4& lo, const uint4& hi, int off) {
-  const uint32_t sh = ES == 2 ? (uint32_t)(off & 2) * 8 : 0u;
-  uint32_t c0, c1, c2, c3, c4;
-  switch (off >> 2) {
-    case 0: c0 = lo.x, c1 = lo.y, c2 = lo.z, c3 = lo.w, c4 = hi.x; break;
-    case 1: c0 = lo.y, c1 = lo.z, c2 = lo.w, c3 = hi.x, c4 = hi.y; break;
-    case 2: c0 = lo.z, c1 = lo.w, c2 = hi.x, c3 = hi.y, c4 = hi.z; break;
-    default: c0 = lo.w, c1 = hi.x, c2 = hi.y, c3 = hi.z, c4 = hi.w; break;
-  }
-  if constexpr (ES == 4) return make_uint4(c0, c1, c2, c3);
-  else return make_uint4(fs(c0, c1, sh), fs(c1, c2, sh), fs(c2, c3, sh), fs(c3, c4, sh));
-}
-
 __device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, int k) {
   return k < 2 ? (k == 0 ? a0 : a1) : (k == 2 ? a2 : a3);
-}
-
-__device__ __forceinline__ uint4 shfl_up4(const uint4& v) {
-  return make_uint4(__shfl_up_sync(0xffffffffu, v.x, 1), __shfl_up_sync(0xffffffffu, v.y, 1),
-                    __shfl_up_sync(0xffffffffu, v.z, 1), __shfl_up_sync(0xffffffffu, v.w, 1));
 }
 
 // Bytes [lo, hi) of the aligned 16-byte word at `w` get bytes [lo, hi) of v
@@ -223,75 +146,35 @@ __device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, 
   }
 }
 
-// Mixed-phase rows: 4 blocks per SM (64 registers), the 8-rank double
-// binary tree 2.  Measured on 8 x 128 MiB bf16 with eight phases and
-// 8 x 25 MiB f32 with four: 397 / 76.4 us at 4 blocks, 438 / 86.2 us at 3.
-__host__ __device__ constexpr int fused_min_blocks_shift(int order, int nr, int es) {
-  return order == DBTREE && nr == 8 ? 2 : 4;
-}
-
-// SHIFT: the row's buffers need not share their address modulo 16 (see
-// above); otherwise they do, and every rank is read and written in aligned
-// 16-byte vectors at the same offset.
-template <class ARGS, int DT, int OP, int ORDER, int NR, bool SHIFT>
-__global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(ORDER, NR, ElemSize<DT>::value)
-                                                    : fused_min_blocks(ORDER, NR))
+// The row's buffers share their address modulo 16: every rank is read and
+// written in aligned 16-byte vectors at the same offset.
+template <class ARGS, int DT, int OP, int ORDER, int NR>
+__global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR))
     fused_vec_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
-  constexpr int U = SHIFT ? 1 : fused_unroll(ORDER, NR);
-  constexpr int TILE_V = SHIFT ? kShiftTileVecs : kFusedBlock * U;
-  static_assert(!SHIFT || NR <= 8, "mixed-phase rows of more than 8 ranks take the runtime-N ring");
+  constexpr int U = fused_unroll(ORDER, NR);
   pdl_prologue();
   const auto& T = a.tab;
   const int n = NR > 0 ? NR : T.nranks;
-  const int lane = threadIdx.x & 31;
 
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
     const void* const* P = T.ptr + (size_t)s.tensor * n;
-    const int shift = row_shift(P[0], ES);  // the row's frame (all its buffers share it unless SHIFT)
+    const int shift = row_shift(P[0], ES);  // all the row's buffers share it
     const SegShape sh = seg_shape<VEC>(s, shift);
     const int64_t ti = tile - s.tile_begin;
     const int c = s.chunk;
 
     // position u of this thread is byte offset base + u * kStride in every
-    // rank, 16-byte aligned in all of them (SHIFT: in the first buffer)
-    const int64_t v0 = sh.vb + ti * TILE_V + (SHIFT ? (threadIdx.x >> 5) * kShiftWarpVecs + lane : threadIdx.x);
+    // rank, 16-byte aligned in all of them
+    const int64_t v0 = sh.vb + ti * (kFusedBlock * U) + threadIdx.x;
     const int64_t base = v0 * 16 - shift * ES;
     constexpr int64_t kStride = (int64_t)kFusedBlock * 16;
-    // SHIFT: the tile's vectors are [t0, t1)
-    const int64_t t0 = sh.vb + ti * TILE_V;
-    const int64_t t1 = SHIFT ? (t0 + TILE_V < sh.ve ? t0 + TILE_V : sh.ve) : sh.ve;
-    // ok: this lane folds position u (SHIFT: lanes 0..30, inside the tile)
-    bool ok[U];
+    bool ok[U];  // this thread folds position u
 #pragma unroll
-    for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < t1 && (!SHIFT || lane <= kShiftWarpVecs);
-    // SHIFT: a lane also loads when the lane below folds a vector whose end
-    // lies in this lane's word
-    const bool edge = SHIFT && lane >= 1 && v0 <= t1;
-
-    // rank rk's 16 bytes at position u (SHIFT: the aligned word holding the
-    // start of the vector), whether this lane loads them, and the vector
-    // itself once loaded (SHIFT: realigned with the word of the lane above)
-    auto ld = [&](int rk, int u) -> uint4 {
-      const char* p = static_cast<const char*>(P[rk]) + base + u * kStride;
-      if constexpr (SHIFT) p = reinterpret_cast<const char*>((uintptr_t)p & ~(uintptr_t)15);
-      return ld_stream(p);
-    };
-    auto may_ld = [&](int rk, int u) -> bool {
-      if constexpr (SHIFT) return ok[0] || (edge && byte_phase(P[rk], P[0]) != 0);
-      else return ok[u];
-    };
-    auto fix = [&](const uint4& raw, int rk) -> uint4 {
-      if constexpr (SHIFT) {
-        const int off = byte_phase(P[rk], P[0]);  // the same in every lane
-        if (off == 0) return raw;
-        return realign_from_next<ES>(raw, off);
-      } else {
-        return raw;
-      }
-    };
+    for (int u = 0; u < U; ++u) ok[u] = v0 + u * kFusedBlock < sh.ve;
+    auto ld = [&](int rk, int u) -> uint4 { return ld_stream(static_cast<const char*>(P[rk]) + base + u * kStride); };
 
     uint4 acc[U];
     if constexpr (ORDER == RING && NR > 8) {
@@ -326,12 +209,12 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
       for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int p = 0; p < NR; ++p)
-          if (may_ld(rot(c + 1 + p, NR), u)) x[u][p] = ld(rot(c + 1 + p, NR), u);
+          if (ok[u]) x[u][p] = ld(rot(c + 1 + p, NR), u);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        acc[u] = fix(x[u][0], rot(c + 1, NR));
+        acc[u] = x[u][0];
 #pragma unroll
-        for (int p = 1; p < NR; ++p) acc[u] = step_vec<DT, OP>(acc[u], fix(x[u][p], rot(c + 1 + p, NR)));
+        for (int p = 1; p < NR; ++p) acc[u] = step_vec<DT, OP>(acc[u], x[u][p]);
       }
     } else if constexpr (ORDER == RING) {
       // any N: groups of 8 ranks in ring order, folded as they arrive
@@ -343,7 +226,7 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
             const int rk = rot(c + 1 + g + q, n);
 #pragma unroll
             for (int u = 0; u < U; ++u)
-              if (may_ld(rk, u)) x[u][q] = ld(rk, u);
+              if (ok[u]) x[u][q] = ld(rk, u);
           }
         }
 #pragma unroll
@@ -352,7 +235,7 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
             const int rk = rot(c + 1 + g + q, n);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-              const uint4 v = fix(x[u][q], rk);
+              const uint4 v = x[u][q];
               acc[u] = (g + q == 0) ? v : step_vec<DT, OP>(acc[u], v);
             }
           }
@@ -370,12 +253,10 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
           const int rk = rot(p + rank_shift, NR);
 #pragma unroll
           for (int u = 0; u < U; ++u)
-            if (may_ld(rk, u)) x[u][p] = ld(rk, u);
+            if (ok[u]) x[u][p] = ld(rk, u);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int p = 0; p < NR; ++p) x[u][p] = fix(x[u][p], rot(p + rank_shift, NR));
           acc[u] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x[u]);
         }
       } else {
@@ -389,12 +270,10 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
       for (int p = 0; p < NR; ++p) {
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (may_ld(p, u)) x[u][p] = ld(p, u);
+          if (ok[u]) x[u][p] = ld(p, u);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-#pragma unroll
-        for (int p = 0; p < NR; ++p) x[u][p] = fix(x[u][p], p);
         acc[u] = tree_fold_regs<DT, OP, NR>(x[u]);
       }
     } else {
@@ -433,34 +312,7 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = div_vec<DT>(acc[u], a.fn);
     }
-    if constexpr (SHIFT) {
-      // rank rk's aligned word that begins off bytes before this vector gets
-      // the end of the vector below (prev) and the start of this one
-      const uint4 prev = shfl_up4(acc[0]);
-      const bool own = ok[0] && lane < kShiftWarpVecs;  // vectors 0..29 of the warp
-      __syncthreads();  // every warp of the block has read its inputs
-      auto put = [&](int rk) {
-        char* d = static_cast<char*>(const_cast<void*>(P[rk])) + base;
-        const int off = byte_phase(P[rk], P[0]);
-        if (off == 0) {
-          if (own) st_stream(d, acc[0]);
-          return;
-        }
-        char* w = d - off;
-        if (ok[0] && lane >= 1) st_stream(w, bytes_at<ES>(prev, acc[0], 16 - off));
-        // the tile's first and last words hold elements outside it
-        if (own && v0 == t0) st_stream_part(w, bytes_at<ES>(prev, acc[0], 16 - off), off, 16);
-        if (own && v0 + 1 == t1) st_stream_part(w + 16, bytes_at<ES>(acc[0], acc[0], 16 - off), 0, off);
-      };
-      if (a.owner_only || a.to_root) {
-        put(a.owner_only ? c : a.root);
-      } else if constexpr (NR > 0) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) put(r);
-      } else {
-        for (int r = 0; r < n; ++r) put(r);
-      }
-    } else if (a.owner_only || a.to_root) {
+    if (a.owner_only || a.to_root) {
       char* dst = static_cast<char*>(const_cast<void*>(P[a.owner_only ? c : a.root])) + base;
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -500,48 +352,57 @@ __global__ void __launch_bounds__(kFusedBlock, SHIFT ? fused_min_blocks_shift(OR
 
 // ---- rows whose buffers sit at different addresses modulo 16: staged form ----
 //
-// The same fold with the realignment done in shared memory instead of
-// registers.  A block takes a tile of kStageTileVecs vectors of the row's
-// frame (the first buffer's 16-byte grid).  (1) Every thread copies aligned
-// 16-byte words of every rank straight into shared memory (cp.async, no
-// registers), rank r's words from the one holding the tile's first byte in
-// buffer r: the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes
-// into rank r's slot.  (2) Each thread folds 4-byte words of the frame,
-// kStageBlock apart (consecutive threads, consecutive words: no bank
-// conflicts): word w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its
-// slot, two word loads and a funnel shift when off_r is 2 mod 4, one load
-// otherwise.  (3) The results go to shared memory four times, the k-th copy
-// shifted by k words, so that for a destination at off = 4k + h bytes the
-// 16-byte word it needs at position i is one aligned 16-byte load of copy k
-// (plus, when h = 2, the last word of the position below, from the lane
-// below, and a funnel shift).  (4) A destination with h = 0 is a run of
-// whole entries of copy k: one bulk copy (cp.async.bulk, the
-// tensor-memory-access engine) writes it; with h = 2 each thread stores
-// whole aligned 16-byte words it shifted.  A destination's first and last
-// word also hold bytes of the neighbouring tiles and are written in part.  A block reads all
-// its inputs before its first store and writes only its tile's bytes, so
-// working in place is safe: bytes of a staged word outside the tile are never
-// used.
+// The fold of the fused kernel with the realignment done in shared memory.
+// A block takes a tile of kStageTileVecs vectors of the row's frame (the
+// first buffer's 16-byte grid).  (1) Every thread copies aligned 16-byte
+// words of the ranks straight into shared memory (cp.async, no registers),
+// rank r's words from the one holding the tile's first byte in buffer r:
+// the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes into its
+// slot.  One commit group per rank, in the order the fold takes them; up to
+// eight ranks each have a slot, more stream through eight slots, a slot
+// refilled as soon as its rank is folded.  (2) Each thread folds 4-byte
+// words of the frame, kStageBlock apart (consecutive threads, consecutive
+// words: no bank conflicts), a rank as soon as its copies have landed: word
+// w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its slot, two word
+// loads and a funnel shift when off_r is 2 mod 4, one load otherwise.
+// (3) The results go to shared memory four times, the k-th copy shifted by
+// k words, and for 2-byte elements (with eight slots) four more times moved
+// by one element, so that the 16-byte words a destination at off = 4k + h
+// bytes needs are consecutive entries of one copy.  (4) One bulk copy
+// (cp.async.bulk, the tensor-memory-access engine) per destination writes
+// its whole words; its first and last word also hold bytes of the
+// neighbouring tiles and are written in part by plain stores.  (Rows of 2
+// or 4 ranks of 2-byte elements keep four copies, for occupancy, and store
+// their 2 mod 4 byte destinations word by word, shifted in registers.)  A
+// block reads all its inputs before its first store and writes only its
+// tile's bytes, so working in place is safe: bytes of a staged word outside
+// the tile are never used.
 constexpr int kStageBlock = 256;
+constexpr int kStageSlots = 8;
+// Rank slots a block holds: one per rank up to eight ranks; NR = 0 (a
+// runtime rank count) and more ranks stream through eight.
+__host__ __device__ constexpr int stage_slots(int nr) { return nr > 0 && nr < kStageSlots ? nr : kStageSlots; }
 // Resident blocks per SM: as many as shared memory allows, since the tiles
-// in flight are what keeps HBM busy (three at 8 ranks, 66 KB each; six below,
-// 33 KB each, at 40 registers without spills).  Measured, 2-byte elements at
-// eight offsets: 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 /
-// 89.3 / 83.9 us at four / five / six blocks; 8 x 128 MiB 446.7 us at two,
-// 351.4 at three (before the bulk stores).
-__host__ __device__ constexpr int stage_min_blocks(int nr) { return nr == 8 ? 3 : 6; }
+// in flight are what keeps HBM busy (three with eight slots, 66 KB each; six
+// below, 33 KB each, at 40 registers without spills).  Measured, 2-byte
+// elements at eight offsets: 4 x 128 MiB 162.8 / 158.5 / 157.5 us and
+// 2 x 128 MiB 98.1 / 89.3 / 83.9 us at four / five / six blocks;
+// 8 x 128 MiB 446.7 us at two, 351.4 at three (before the bulk stores).
+__host__ __device__ constexpr int stage_min_blocks(int nr) { return stage_slots(nr) == kStageSlots ? 3 : 6; }
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
-// Eight copies (the four word shifts of the result and of the result moved
-// by one 2-byte element) for 8-rank rows of 2-byte elements, whose slots
-// leave room for them; four otherwise.
-__host__ __device__ constexpr int stage_copies(int es, int nr) { return es == 2 && nr == 8 ? 8 : 4; }
+__host__ __device__ constexpr int stage_copies(int es, int nr) {
+  return es == 2 && stage_slots(nr) == kStageSlots ? 8 : 4;
+}
 __host__ __device__ constexpr int stage_smem_bytes(int nr, int es) {
-  return nr * kStageSlotBytes > stage_copies(es, nr) * kStageCopyBytes ? nr * kStageSlotBytes
-                                                                         : stage_copies(es, nr) * kStageCopyBytes;
+  return stage_slots(nr) * kStageSlotBytes > stage_copies(es, nr) * kStageCopyBytes
+             ? stage_slots(nr) * kStageSlotBytes
+             : stage_copies(es, nr) * kStageCopyBytes;
 }
 
+// NR: 2, 4 or 8 ranks (every order), 16, 32 or 64 (ring and tree), 0 = the
+// table's rank count (ring).
 template <class ARGS, int DT, int OP, int ORDER, int NR>
 __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
@@ -549,15 +410,20 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
   constexpr int TV = kStageTileVecs;
   constexpr int G = TV * 4 / kStageBlock / 4;  // groups of 4 frame words per thread
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
+  constexpr int NS = stage_slots(NR);
+  constexpr bool kStream = NR == 0 || NR > kStageSlots;  // ranks stream through the slots
+  static_assert(NR == 0 ? ORDER == RING : (ORDER != DBTREE || NR <= kStageSlots), "no staged form");
+  constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
   const auto& T = a.tab;
+  const int n = NR > 0 ? NR : T.nranks;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
 
   for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
     const Seg& s = T.seg[find_seg(T, tile)];
-    const void* const* P = T.ptr + (size_t)s.tensor * NR;
+    const void* const* P = T.ptr + (size_t)s.tensor * n;
     const int shift = row_shift(P[0], ES);
     const SegShape sh = seg_shape<VEC>(s, shift);
     const int64_t ti = tile - s.tile_begin;
@@ -567,38 +433,41 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
     const int64_t base = t0 * 16 - shift * ES;                 // vector t0 in every buffer, aligned in P[0]
 
     if (nv > 0) {
-      // (1) rank r's aligned words [0, nv + (off_r != 0)) into slot r, one
-      // commit group per rank in the order the fold takes them
+      // (1) the rank at fold position p, its aligned words [0, nv + (off != 0))
+      // into slot p (mod the slot count), one commit group each
       const int rank_shift = ORDER == DBTREE && c != 0 ? 1 : 0;
       auto rank_at = [&](int p) -> int {
-        if constexpr (ORDER == RING) return rot(c + 1 + p, NR);
-        else if constexpr (ORDER == DBTREE) return rot(p + rank_shift, NR);
+        if constexpr (ORDER == RING) return rot(c + 1 + p, n);
+        else if constexpr (ORDER == DBTREE) return rot(p + rank_shift, n);
         else return p;
       };
-#pragma unroll
-      for (int p = 0; p < NR; ++p) {
+      auto slot = [&](int p) -> unsigned char* { return S + (p % NS) * kStageSlotBytes; };
+      auto issue = [&](int p) {
         const int r = rank_at(p);
         const int off = byte_phase(P[r], P[0]);
         const char* g = static_cast<const char*>(P[r]) + base - off;
         const int nw = nv + (off != 0);
-        for (int i = tid; i < nw; i += kStageBlock) cp_async16(S + r * kStageSlotBytes + i * 16, g + i * 16);
+        unsigned char* d = slot(p);
+        for (int i = tid; i < nw; i += kStageBlock) cp_async16(d + i * 16, g + i * 16);
         cp_async_commit();
+      };
+      if constexpr (kStream) {
+        const int first = n < NS ? n : NS;
+        for (int p = 0; p < first; ++p) issue(p);
+      } else {
+#pragma unroll
+        for (int p = 0; p < NR; ++p) issue(p);
       }
 
       // (2) fold frame words w = tid + (4j + k) * kStageBlock, k = 0..3, of group j
-      auto word = [&](int r, int w) -> uint32_t {
-        const int off = byte_phase(P[r], P[0]);
-        const uint32_t* sl = reinterpret_cast<const uint32_t*>(S + r * kStageSlotBytes) + (off >> 2) + w;
-        if constexpr (ES == 4) {
-          return sl[0];
-        } else {
-          return __funnelshift_r(sl[0], sl[1], (uint32_t)(off & 2) * 8);
-        }
-      };
-      auto group = [&](int r, int j) -> uint4 {
-        const int w = tid + 4 * j * kStageBlock;
-        return make_uint4(word(r, w), word(r, w + kStageBlock), word(r, w + 2 * kStageBlock),
-                          word(r, w + 3 * kStageBlock));
+      auto group = [&](int p, int j) -> uint4 {
+        const int off = byte_phase(P[rank_at(p)], P[0]);
+        const uint32_t* sl = reinterpret_cast<const uint32_t*>(slot(p)) + (off >> 2) + tid + 4 * j * kStageBlock;
+        auto word = [&](int q) -> uint32_t {
+          if constexpr (ES == 4) return sl[q * kStageBlock];
+          else return __funnelshift_r(sl[q * kStageBlock], sl[q * kStageBlock + 1], (uint32_t)(off & 2) * 8);
+        };
+        return make_uint4(word(0), word(1), word(2), word(3));
       };
       uint4 res[G];
       if constexpr (ORDER == DBTREE) {
@@ -609,7 +478,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         for (int j = 0; j < G; ++j) {
           uint4 x[NR];
 #pragma unroll
-          for (int p = 0; p < NR; ++p) x[p] = group(rank_at(p), j);
+          for (int p = 0; p < NR; ++p) x[p] = group(p, j);
           res[j] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x);
         }
       } else {
@@ -617,16 +486,17 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         // later ranks' copies are still in flight; the tree keeps finished
         // subtrees on a stack (a binary counter over the rank index), which
         // is the same balanced pairwise tree
-        uint4 stk[G][ORDER == RING ? 1 : 4];
+        constexpr int kDepth = ORDER == RING ? 1 : (NR >= 64 ? 7 : NR >= 32 ? 6 : NR >= 16 ? 5 : 4);
+        uint4 stk[G][kDepth];
         int top = 0;
-#pragma unroll
-        for (int p = 0; p < NR; ++p) {
-          cp_async_wait_pending(NR - 1 - p);
+        auto fold = [&](int p) {
+          // copies still allowed in flight: those issued after rank p's
+          const int later = (kStream ? (n < p + NS ? n : p + NS) : n) - 1 - p;
+          cp_async_wait_pending(later);
           __syncthreads();
-          const int r = rank_at(p);
 #pragma unroll
           for (int j = 0; j < G; ++j) {
-            uint4 v = group(r, j);
+            uint4 v = group(p, j);
             if constexpr (ORDER == RING) {
               stk[j][0] = p == 0 ? v : step_vec<DT, OP>(stk[j][0], v);
             } else {
@@ -640,6 +510,17 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
             for (int k = p; k & 1; k >>= 1) --top;
             ++top;
           }
+          if (kStream && p + NS < n) {
+            __syncthreads();  // every thread has read the slot rank p + NS takes
+            issue(p + NS);
+          }
+        };
+        if constexpr (NR > 0) {
+#pragma unroll
+          for (int p = 0; p < NR; ++p) fold(p);
+        } else {
+#pragma unroll 1
+          for (int p = 0; p < n; ++p) fold(p);
         }
 #pragma unroll
         for (int j = 0; j < G; ++j) res[j] = stk[j][0];
@@ -662,11 +543,9 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           cp[(4 * j + 3) * kStageBlock] = res[j].w;
         }
       }
-      constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
       if constexpr (kHalfCopies) {
-        // copies 4..7: the same with frame word m replaced by its last
-        // element followed by the first of word m + 1 ... that is, word m
-        // of the stream one element earlier: funnel(word m - 1, word m)
+        // copies 4..7 the same for the stream one element earlier: its word
+        // m is the last element of frame word m - 1 and the first of word m
         __syncthreads();  // lane 0 reads the word below from copy 0
         const uint32_t* c0 = reinterpret_cast<const uint32_t*>(S) + 4 + tid;
 #pragma unroll
@@ -707,9 +586,8 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
         const int nw = nv + (off != 0);
         if (ES == 4 || hs == 0 || kHalfCopies) {
-          // a whole number of words off: destination word i is entry i + 1
-          // of copy k, so its whole words leave in one bulk copy; the two
-          // partial words by plain stores
+          // destination word i is entry i + 1 of the copy: its whole words
+          // leave in one bulk copy, the two partial words by plain stores
           const int lo = off != 0;
           if (tid == 0 && nv > lo) bulk_store(g + 16 * lo, cp + lo + 1, 16 * (nv - lo));
           if (off != 0 && tid == 32) st_stream_part(g, cp[1], off, 16);
@@ -734,9 +612,12 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
       };
       if (a.owner_only || a.to_root) {
         put(a.owner_only ? c : a.root);
-      } else {
+      } else if constexpr (NR > 0 && NR <= kStageSlots) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) put(r);
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < n; ++r) put(r);
       }
       if (tid == 0) bulk_commit();
     }
@@ -744,12 +625,12 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
     // elements of the segment outside its full vectors
     if (ti == 0 && tid < sh.head + sh.tail) {
       const int64_t e = scalar_elem<VEC>(s, sh, tid, shift);
-      uint32_t r = fold_scalar<DT, OP, ORDER>(P, NR, c, e);
+      uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
       if (a.avg) r = div_word<DT>(r, a.fn);
       if (a.owner_only || a.to_root) {
         st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
       } else {
-        for (int q = 0; q < NR; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
       }
     }
     // the next tile's copies overwrite shared memory every thread and every
@@ -886,13 +767,12 @@ inline unsigned grid_for(int64_t ntiles, int64_t cap = 0) {
   return (unsigned)g;
 }
 
-template <int DT, int OP, int ORDER, int NR, class ARGS, bool SHIFT = false>
+template <int DT, int OP, int ORDER, int NR, class ARGS>
 cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
-  constexpr int U = SHIFT ? 1 : fused_unroll(ORDER, NR);
-  constexpr int64_t kTile = SHIFT ? kShiftTileVecs : (int64_t)kFusedBlock * U;
+  constexpr int64_t kTile = (int64_t)kFusedBlock * fused_unroll(ORDER, NR);
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kTile, true) == 0) return cudaSuccess;
   count_launch();
-  return launch_pdl(fused_vec_kernel<ARGS, DT, OP, ORDER, NR, SHIFT>, grid_for(a.tab.ntiles, a.max_grid), kFusedBlock,
+  return launch_pdl(fused_vec_kernel<ARGS, DT, OP, ORDER, NR>, grid_for(a.tab.ntiles, a.max_grid), kFusedBlock,
                     stream, a);
 }
 
@@ -916,12 +796,12 @@ cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
   return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kStageBlock, stream, a, (size_t)kSmem);
 }
 
-// Rows whose buffers sit at different addresses modulo 16 (every order up to
-// 8 ranks; rings of any size through the runtime-N form).  Returns
-// cudaErrorNotSupported where no such form is compiled (trees of 16 or more
-// ranks), for the element-wise kernel to take.
+// Rows whose buffers sit at different addresses modulo 16: the staged
+// kernel for rings of any size, trees of 2 to 64 ranks and double binary
+// trees of 2, 4 or 8.  Returns cudaErrorNotSupported otherwise (wider double
+// binary trees), for the element-wise kernel to take.
 __host__ __forceinline__ bool shift_form_exists(int order, int n) {
-  return order == RING || n == 2 || n == 4 || n == 8;
+  return order == RING || order == TREE || n == 2 || n == 4 || n == 8;
 }
 
 template <int DT, int OP, class ARGS>
@@ -934,12 +814,15 @@ cudaError_t launch_fused_shift_typed(int order, ARGS& a, cudaStream_t stream) {
     case TREE * 100 + 2: return launch_fused_stage<DT, OP, TREE, 2>(a, stream);
     case TREE * 100 + 4: return launch_fused_stage<DT, OP, TREE, 4>(a, stream);
     case TREE * 100 + 8: return launch_fused_stage<DT, OP, TREE, 8>(a, stream);
+    case TREE * 100 + 16: return launch_fused_stage<DT, OP, TREE, 16>(a, stream);
+    case TREE * 100 + 32: return launch_fused_stage<DT, OP, TREE, 32>(a, stream);
+    case TREE * 100 + 64: return launch_fused_stage<DT, OP, TREE, 64>(a, stream);
     case DBTREE * 100 + 2: return launch_fused_stage<DT, OP, DBTREE, 2>(a, stream);
     case DBTREE * 100 + 4: return launch_fused_stage<DT, OP, DBTREE, 4>(a, stream);
     case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
     default: break;
   }
-  if (order == RING) return launch_fused_vec<DT, OP, RING, 0, ARGS, true>(a, stream);
+  if (order == RING) return launch_fused_stage<DT, OP, RING, 0>(a, stream);
   return cudaErrorNotSupported;
 }
 
