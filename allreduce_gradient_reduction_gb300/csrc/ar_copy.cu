@@ -1,6 +1,6 @@
 // Copy kernels (fused AllGather, bucket pack/unpack) and the fused-kernel
 // dispatcher.
-#include "ar_fused.cuh"
+#include "ar_stage.cuh"
 
 namespace ar {
 
@@ -152,39 +152,39 @@ cudaError_t launch_fused_f16_max(int, bool, FusedArgs&, cudaStream_t);
 cudaError_t launch_fused_f16_sum(int, bool, SmallFusedArgs&, cudaStream_t);
 cudaError_t launch_fused_f16_max(int, bool, SmallFusedArgs&, cudaStream_t);
 
-#define AR_DECLARE_SHIFT(NAME)                           \
+#define AR_DECLARE_STAGE(NAME)                           \
   cudaError_t NAME(int, FusedArgs&, cudaStream_t);       \
   cudaError_t NAME(int, SmallFusedArgs&, cudaStream_t);
-AR_DECLARE_SHIFT(launch_fused_shift_f32_sum)
-AR_DECLARE_SHIFT(launch_fused_shift_f32_max)
-AR_DECLARE_SHIFT(launch_fused_shift_bf16_sum)
-AR_DECLARE_SHIFT(launch_fused_shift_bf16_max)
-AR_DECLARE_SHIFT(launch_fused_shift_f16_sum)
-AR_DECLARE_SHIFT(launch_fused_shift_f16_max)
-AR_DECLARE_SHIFT(launch_fused_shift_i32_sum)
-AR_DECLARE_SHIFT(launch_fused_shift_i32_max)
+AR_DECLARE_STAGE(launch_stage_f32_sum)
+AR_DECLARE_STAGE(launch_stage_f32_max)
+AR_DECLARE_STAGE(launch_stage_bf16_sum)
+AR_DECLARE_STAGE(launch_stage_bf16_max)
+AR_DECLARE_STAGE(launch_stage_f16_sum)
+AR_DECLARE_STAGE(launch_stage_f16_max)
+AR_DECLARE_STAGE(launch_stage_i32_sum)
+AR_DECLARE_STAGE(launch_stage_i32_max)
 
 template <class ARGS>
-static cudaError_t launch_fused_shift_any(int dtype, int op, int order, ARGS& a, cudaStream_t s) {
+static cudaError_t launch_stage_any(int dtype, int op, int order, ARGS& a, cudaStream_t s) {
   switch (dtype * 2 + op) {
-    case F32 * 2 + SUM: return launch_fused_shift_f32_sum(order, a, s);
-    case F32 * 2 + MAX: return launch_fused_shift_f32_max(order, a, s);
-    case BF16 * 2 + SUM: return launch_fused_shift_bf16_sum(order, a, s);
-    case BF16 * 2 + MAX: return launch_fused_shift_bf16_max(order, a, s);
-    case I32 * 2 + SUM: return launch_fused_shift_i32_sum(order, a, s);
-    case I32 * 2 + MAX: return launch_fused_shift_i32_max(order, a, s);
-    case F16 * 2 + SUM: return launch_fused_shift_f16_sum(order, a, s);
-    case F16 * 2 + MAX: return launch_fused_shift_f16_max(order, a, s);
+    case F32 * 2 + SUM: return launch_stage_f32_sum(order, a, s);
+    case F32 * 2 + MAX: return launch_stage_f32_max(order, a, s);
+    case BF16 * 2 + SUM: return launch_stage_bf16_sum(order, a, s);
+    case BF16 * 2 + MAX: return launch_stage_bf16_max(order, a, s);
+    case I32 * 2 + SUM: return launch_stage_i32_sum(order, a, s);
+    case I32 * 2 + MAX: return launch_stage_i32_max(order, a, s);
+    case F16 * 2 + SUM: return launch_stage_f16_sum(order, a, s);
+    case F16 * 2 + MAX: return launch_stage_f16_max(order, a, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 // `vec`: every row's buffers share their address modulo 16.  Rows that do
-// not take the staged kernel where its form exists (shift_form_exists),
+// not take the staged kernel where its form exists (stage_form_exists),
 // else the element-wise kernel.
 template <class ARGS>
 static cudaError_t launch_fused_any(int dtype, int op, int order, bool vec, ARGS& a, cudaStream_t s) {
-  if (!vec && shift_form_exists(order, a.tab.nranks)) return launch_fused_shift_any(dtype, op, order, a, s);
+  if (!vec && stage_form_exists(order, a.tab.nranks)) return launch_stage_any(dtype, op, order, a, s);
   switch (dtype * 2 + op) {
     case F32 * 2 + SUM: return launch_fused_f32_sum(order, vec, a, s);
     case F32 * 2 + MAX: return launch_fused_f32_max(order, vec, a, s);

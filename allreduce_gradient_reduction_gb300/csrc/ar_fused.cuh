@@ -18,8 +18,6 @@
 // values of a vector before it writes any, so working in place is safe.
 #pragma once
 
-#include <atomic>
-
 #include "ar_device.cuh"
 
 namespace ar {
@@ -113,37 +111,6 @@ __device__ __forceinline__ uint4 inorder_fold_stream(DbtStream<NR>& st) {
   }
   if constexpr (R < HI) acc = step_vec<DT, OP>(acc, inorder_fold_stream<DT, OP, NR, R + 1, HI>(st));
   return acc;
-}
-
-// ---- helpers for rows whose buffers sit at different addresses modulo 16 ------
-
-// Offset of buffer p from the row's first buffer within a 16-byte word.
-__device__ __forceinline__ int byte_phase(const void* p, const void* p0) {
-  return (int)(((uintptr_t)p - (uintptr_t)p0) & 15);
-}
-
-__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, int k) {
-  return k < 2 ? (k == 0 ? a0 : a1) : (k == 2 ? a2 : a3);
-}
-
-// Bytes [lo, hi) of the aligned 16-byte word at `w` get bytes [lo, hi) of v
-// (lo, hi multiples of 2), as naturally aligned 8-, 4- and 2-byte stores.
-__device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, int hi) {
-  int pos = lo;
-  while (pos < hi) {
-    const int k = pos >> 2;
-    if ((pos & 7) == 0 && pos + 8 <= hi) {
-      __stcs(reinterpret_cast<uint2*>(w + pos), make_uint2(pick4(v.x, v.y, v.z, v.w, k), pick4(v.y, v.z, v.w, v.w, k)));
-      pos += 8;
-    } else if ((pos & 3) == 0 && pos + 4 <= hi) {
-      __stcs(reinterpret_cast<unsigned int*>(w + pos), pick4(v.x, v.y, v.z, v.w, k));
-      pos += 4;
-    } else {
-      __stcs(reinterpret_cast<unsigned short*>(w + pos),
-             (unsigned short)(pick4(v.x, v.y, v.z, v.w, k) >> ((pos & 2) * 8)));
-      pos += 2;
-    }
-  }
 }
 
 // The row's buffers share their address modulo 16: every rank is read and
@@ -350,299 +317,6 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR))
   }
 }
 
-// ---- rows whose buffers sit at different addresses modulo 16: staged form ----
-//
-// The fold of the fused kernel with the realignment done in shared memory.
-// A block takes a tile of kStageTileVecs vectors of the row's frame (the
-// first buffer's 16-byte grid).  (1) Every thread copies aligned 16-byte
-// words of the ranks straight into shared memory (cp.async, no registers),
-// rank r's words from the one holding the tile's first byte in buffer r:
-// the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes into its
-// slot.  One commit group per rank, in the order the fold takes them; up to
-// eight ranks each have a slot, more stream through eight slots, a slot
-// refilled as soon as its rank is folded.  (2) Each thread folds 4-byte
-// words of the frame, kStageBlock apart (consecutive threads, consecutive
-// words: no bank conflicts), a rank as soon as its copies have landed: word
-// w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its slot, two word
-// loads and a funnel shift when off_r is 2 mod 4, one load otherwise.
-// (3) The results go to shared memory four times, the k-th copy shifted by
-// k words, and for 2-byte elements (with eight slots) four more times moved
-// by one element, so that the 16-byte words a destination at off = 4k + h
-// bytes needs are consecutive entries of one copy.  (4) One bulk copy
-// (cp.async.bulk, the tensor-memory-access engine) per destination writes
-// its whole words; its first and last word also hold bytes of the
-// neighbouring tiles and are written in part by plain stores.  (Rows of 2
-// or 4 ranks of 2-byte elements keep four copies, for occupancy, and store
-// their 2 mod 4 byte destinations word by word, shifted in registers.)  A
-// block reads all its inputs before its first store and writes only its
-// tile's bytes, so working in place is safe: bytes of a staged word outside
-// the tile are never used.
-constexpr int kStageBlock = 256;
-constexpr int kStageSlots = 8;
-// Rank slots a block holds: one per rank up to eight ranks; NR = 0 (a
-// runtime rank count) and more ranks stream through eight.
-__host__ __device__ constexpr int stage_slots(int nr) { return nr > 0 && nr < kStageSlots ? nr : kStageSlots; }
-// Resident blocks per SM: as many as shared memory allows, since the tiles
-// in flight are what keeps HBM busy (three with eight slots, 66 KB each; six
-// below, 33 KB each, at 40 registers without spills).  Measured, 2-byte
-// elements at eight offsets: 4 x 128 MiB 162.8 / 158.5 / 157.5 us and
-// 2 x 128 MiB 98.1 / 89.3 / 83.9 us at four / five / six blocks;
-// 8 x 128 MiB 446.7 us at two, 351.4 at three (before the bulk stores).
-__host__ __device__ constexpr int stage_min_blocks(int nr) { return stage_slots(nr) == kStageSlots ? 3 : 6; }
-constexpr int kStageTileVecs = 512;
-constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
-constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
-__host__ __device__ constexpr int stage_copies(int es, int nr) {
-  return es == 2 && stage_slots(nr) == kStageSlots ? 8 : 4;
-}
-__host__ __device__ constexpr int stage_smem_bytes(int nr, int es) {
-  return stage_slots(nr) * kStageSlotBytes > stage_copies(es, nr) * kStageCopyBytes
-             ? stage_slots(nr) * kStageSlotBytes
-             : stage_copies(es, nr) * kStageCopyBytes;
-}
-
-// NR: 2, 4 or 8 ranks (every order), 16, 32 or 64 (ring and tree), 0 = the
-// table's rank count (ring).
-template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage_kernel(const __grid_constant__ ARGS a) {
-  constexpr int ES = ElemSize<DT>::value;
-  constexpr int VEC = 16 / ES;
-  constexpr int TV = kStageTileVecs;
-  constexpr int G = TV * 4 / kStageBlock / 4;  // groups of 4 frame words per thread
-  static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
-  constexpr int NS = stage_slots(NR);
-  constexpr bool kStream = NR == 0 || NR > kStageSlots;  // ranks stream through the slots
-  static_assert(NR == 0 ? ORDER == RING : (ORDER != DBTREE || NR <= kStageSlots), "no staged form");
-  constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
-  extern __shared__ __align__(16) unsigned char S[];
-  pdl_prologue();
-  const auto& T = a.tab;
-  const int n = NR > 0 ? NR : T.nranks;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-
-  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
-    const Seg& s = T.seg[find_seg(T, tile)];
-    const void* const* P = T.ptr + (size_t)s.tensor * n;
-    const int shift = row_shift(P[0], ES);
-    const SegShape sh = seg_shape<VEC>(s, shift);
-    const int64_t ti = tile - s.tile_begin;
-    const int c = s.chunk;
-    const int64_t t0 = sh.vb + ti * TV;
-    const int nv = (int)(sh.ve - t0 < TV ? sh.ve - t0 : TV);  // vectors in this tile (<= 0: scalars only)
-    const int64_t base = t0 * 16 - shift * ES;                 // vector t0 in every buffer, aligned in P[0]
-
-    if (nv > 0) {
-      // (1) the rank at fold position p, its aligned words [0, nv + (off != 0))
-      // into slot p (mod the slot count), one commit group each
-      const int rank_shift = ORDER == DBTREE && c != 0 ? 1 : 0;
-      auto rank_at = [&](int p) -> int {
-        if constexpr (ORDER == RING) return rot(c + 1 + p, n);
-        else if constexpr (ORDER == DBTREE) return rot(p + rank_shift, n);
-        else return p;
-      };
-      auto slot = [&](int p) -> unsigned char* { return S + (p % NS) * kStageSlotBytes; };
-      auto issue = [&](int p) {
-        const int r = rank_at(p);
-        const int off = byte_phase(P[r], P[0]);
-        const char* g = static_cast<const char*>(P[r]) + base - off;
-        const int nw = nv + (off != 0);
-        unsigned char* d = slot(p);
-        for (int i = tid; i < nw; i += kStageBlock) cp_async16(d + i * 16, g + i * 16);
-        cp_async_commit();
-      };
-      if constexpr (kStream) {
-        const int first = n < NS ? n : NS;
-        for (int p = 0; p < first; ++p) issue(p);
-      } else {
-#pragma unroll
-        for (int p = 0; p < NR; ++p) issue(p);
-      }
-
-      // (2) fold frame words w = tid + (4j + k) * kStageBlock, k = 0..3, of group j
-      auto group = [&](int p, int j) -> uint4 {
-        const int off = byte_phase(P[rank_at(p)], P[0]);
-        const uint32_t* sl = reinterpret_cast<const uint32_t*>(slot(p)) + (off >> 2) + tid + 4 * j * kStageBlock;
-        auto word = [&](int q) -> uint32_t {
-          if constexpr (ES == 4) return sl[q * kStageBlock];
-          else return __funnelshift_r(sl[q * kStageBlock], sl[q * kStageBlock + 1], (uint32_t)(off & 2) * 8);
-        };
-        return make_uint4(word(0), word(1), word(2), word(3));
-      };
-      uint4 res[G];
-      if constexpr (ORDER == DBTREE) {
-        // the in-order tree needs every rank at once
-        cp_async_wait_all();
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          uint4 x[NR];
-#pragma unroll
-          for (int p = 0; p < NR; ++p) x[p] = group(p, j);
-          res[j] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x);
-        }
-      } else {
-        // rank p is folded as soon as its copies have landed, while the
-        // later ranks' copies are still in flight; the tree keeps finished
-        // subtrees on a stack (a binary counter over the rank index), which
-        // is the same balanced pairwise tree
-        constexpr int kDepth = ORDER == RING ? 1 : (NR >= 64 ? 7 : NR >= 32 ? 6 : NR >= 16 ? 5 : 4);
-        uint4 stk[G][kDepth];
-        int top = 0;
-        auto fold = [&](int p) {
-          // copies still allowed in flight: those issued after rank p's
-          const int later = (kStream ? (n < p + NS ? n : p + NS) : n) - 1 - p;
-          cp_async_wait_pending(later);
-          __syncthreads();
-#pragma unroll
-          for (int j = 0; j < G; ++j) {
-            uint4 v = group(p, j);
-            if constexpr (ORDER == RING) {
-              stk[j][0] = p == 0 ? v : step_vec<DT, OP>(stk[j][0], v);
-            } else {
-              int t = top;
-#pragma unroll
-              for (int k = p; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[j][--t], v);
-              stk[j][t] = v;
-            }
-          }
-          if constexpr (ORDER != RING) {
-            for (int k = p; k & 1; k >>= 1) --top;
-            ++top;
-          }
-          if (kStream && p + NS < n) {
-            __syncthreads();  // every thread has read the slot rank p + NS takes
-            issue(p + NS);
-          }
-        };
-        if constexpr (NR > 0) {
-#pragma unroll
-          for (int p = 0; p < NR; ++p) fold(p);
-        } else {
-#pragma unroll 1
-          for (int p = 0; p < n; ++p) fold(p);
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j) res[j] = stk[j][0];
-      }
-      if (a.avg) {
-#pragma unroll
-        for (int j = 0; j < G; ++j) res[j] = div_vec<DT>(res[j], a.fn);
-      }
-      __syncthreads();  // every slot has been read
-
-      // (3) copy k holds frame word m at word index m + k + 4
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t* cp = reinterpret_cast<uint32_t*>(S + k * kStageCopyBytes) + k + 4 + tid;
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          cp[(4 * j + 0) * kStageBlock] = res[j].x;
-          cp[(4 * j + 1) * kStageBlock] = res[j].y;
-          cp[(4 * j + 2) * kStageBlock] = res[j].z;
-          cp[(4 * j + 3) * kStageBlock] = res[j].w;
-        }
-      }
-      if constexpr (kHalfCopies) {
-        // copies 4..7 the same for the stream one element earlier: its word
-        // m is the last element of frame word m - 1 and the first of word m
-        __syncthreads();  // lane 0 reads the word below from copy 0
-        const uint32_t* c0 = reinterpret_cast<const uint32_t*>(S) + 4 + tid;
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          uint32_t f[4] = {res[j].x, res[j].y, res[j].z, res[j].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int m_off = (4 * j + q) * kStageBlock;  // this thread's word m = tid + m_off
-            uint32_t below = __shfl_up_sync(0xffffffffu, f[q], 1);
-            if (lane == 0) below = c0[m_off - 1];
-            const uint32_t h = __funnelshift_l(below, f[q], 16);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              reinterpret_cast<uint32_t*>(S + (4 + k) * kStageCopyBytes)[k + 4 + tid + m_off] = h;
-          }
-        }
-        // one word past the tile: a full tile's last destination word starts
-        // with the last element of its last frame word
-        if (tid == kStageBlock - 1) {
-          const uint32_t h = __funnelshift_l(res[G - 1].w, 0u, 16);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            reinterpret_cast<uint32_t*>(S + (4 + k) * kStageCopyBytes)[k + 4 + 4 * TV] = h;
-        }
-      }
-      fence_proxy_async_shared();  // the bulk copies read them through the async proxy
-      __syncthreads();
-
-      // (4) destination word i of rank r: bytes [16i, 16i + 16) from the
-      // aligned word holding the tile's first byte, i.e. frame bytes
-      // [16i - off, 16i + 16 - off): words 4i - k .. 4i - k + 3 (entry i + 1
-      // of copy k) and, for h = 2, word 4i - k - 1 (entry i of copy k, .w)
-      auto put = [&](int r) {
-        const int off = byte_phase(P[r], P[0]);
-        const int k = off >> 2;
-        const uint32_t hs = (uint32_t)(off & 2) * 8;
-        const uint4* cp = reinterpret_cast<const uint4*>(S + ((kHalfCopies && hs ? 4 : 0) + k) * kStageCopyBytes);
-        char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
-        const int nw = nv + (off != 0);
-        if (ES == 4 || hs == 0 || kHalfCopies) {
-          // destination word i is entry i + 1 of the copy: its whole words
-          // leave in one bulk copy, the two partial words by plain stores
-          const int lo = off != 0;
-          if (tid == 0 && nv > lo) bulk_store(g + 16 * lo, cp + lo + 1, 16 * (nv - lo));
-          if (off != 0 && tid == 32) st_stream_part(g, cp[1], off, 16);
-          if (off != 0 && tid == 64) st_stream_part(g + 16 * (int64_t)nv, cp[nv + 1], 0, off);
-          return;
-        }
-        if constexpr (ES == 2 && !kHalfCopies) {  // 2 mod 4 bytes off: each word shifted by one element
-          for (int i0 = tid - lane; i0 < nw; i0 += kStageBlock) {  // whole warps: the shuffle needs every lane
-            const int i = i0 + lane;
-            const int ic = i < TV ? i : TV;  // lanes past the end read an entry that exists and store nothing
-            const uint4 cur = cp[ic + 1];
-            uint32_t prev = __shfl_up_sync(0xffffffffu, cur.w, 1);
-            if (lane == 0) prev = cp[ic].w;
-            const uint4 v = make_uint4(__funnelshift_l(prev, cur.x, 16), __funnelshift_l(cur.x, cur.y, 16),
-                                       __funnelshift_l(cur.y, cur.z, 16), __funnelshift_l(cur.z, cur.w, 16));
-            if (i >= nw) continue;
-            if (i == 0) st_stream_part(g, v, off, 16);
-            else if (i == nv) st_stream_part(g + 16 * (int64_t)i, v, 0, off);
-            else st_stream(g + 16 * (int64_t)i, v);
-          }
-        }
-      };
-      if (a.owner_only || a.to_root) {
-        put(a.owner_only ? c : a.root);
-      } else if constexpr (NR > 0 && NR <= kStageSlots) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) put(r);
-      } else {
-#pragma unroll 1
-        for (int r = 0; r < n; ++r) put(r);
-      }
-      if (tid == 0) bulk_commit();
-    }
-
-    // elements of the segment outside its full vectors
-    if (ti == 0 && tid < sh.head + sh.tail) {
-      const int64_t e = scalar_elem<VEC>(s, sh, tid, shift);
-      uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
-      if (a.avg) r = div_word<DT>(r, a.fn);
-      if (a.owner_only || a.to_root) {
-        st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
-      } else {
-        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
-      }
-    }
-    // the next tile's copies overwrite shared memory every thread and every
-    // bulk copy has finished reading
-    if (tile + gridDim.x < T.ntiles) {
-      if (tid == 0) bulk_wait_read();
-      __syncthreads();
-    }
-  }
-  if (tid == 0) bulk_wait_all();
-}
-
 // Same computation element by element, for rows whose buffers sit at
 // different addresses modulo 16.  Each thread takes kScalarUnroll elements of
 // a tile, kFusedBlock apart.  In ring order (the naive order too) it walks the
@@ -776,56 +450,6 @@ cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
                     stream, a);
 }
 
-template <int DT, int OP, int ORDER, int NR, class ARGS>
-cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
-  constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value);
-  auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR>;
-  // opened once per device to the shared memory the kernel uses
-  static std::atomic<bool> opened[256];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-  if (!opened[dev].load()) {
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
-      return e;
-    opened[dev].store(true);
-  }
-  if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kStageTileVecs, true) == 0) return cudaSuccess;
-  count_launch();
-  return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kStageBlock, stream, a, (size_t)kSmem);
-}
-
-// Rows whose buffers sit at different addresses modulo 16: the staged
-// kernel for rings of any size, trees of 2 to 64 ranks and double binary
-// trees of 2, 4 or 8.  Returns cudaErrorNotSupported otherwise (wider double
-// binary trees), for the element-wise kernel to take.
-__host__ __forceinline__ bool shift_form_exists(int order, int n) {
-  return order == RING || order == TREE || n == 2 || n == 4 || n == 8;
-}
-
-template <int DT, int OP, class ARGS>
-cudaError_t launch_fused_shift_typed(int order, ARGS& a, cudaStream_t stream) {
-  const int n = a.tab.nranks;
-  switch (order * 100 + n) {
-    case RING * 100 + 2: return launch_fused_stage<DT, OP, RING, 2>(a, stream);
-    case RING * 100 + 4: return launch_fused_stage<DT, OP, RING, 4>(a, stream);
-    case RING * 100 + 8: return launch_fused_stage<DT, OP, RING, 8>(a, stream);
-    case TREE * 100 + 2: return launch_fused_stage<DT, OP, TREE, 2>(a, stream);
-    case TREE * 100 + 4: return launch_fused_stage<DT, OP, TREE, 4>(a, stream);
-    case TREE * 100 + 8: return launch_fused_stage<DT, OP, TREE, 8>(a, stream);
-    case TREE * 100 + 16: return launch_fused_stage<DT, OP, TREE, 16>(a, stream);
-    case TREE * 100 + 32: return launch_fused_stage<DT, OP, TREE, 32>(a, stream);
-    case TREE * 100 + 64: return launch_fused_stage<DT, OP, TREE, 64>(a, stream);
-    case DBTREE * 100 + 2: return launch_fused_stage<DT, OP, DBTREE, 2>(a, stream);
-    case DBTREE * 100 + 4: return launch_fused_stage<DT, OP, DBTREE, 4>(a, stream);
-    case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
-    default: break;
-  }
-  if (order == RING) return launch_fused_stage<DT, OP, RING, 0>(a, stream);
-  return cudaErrorNotSupported;
-}
-
 template <int DT, int OP, int ORDER, class ARGS>
 cudaError_t launch_fused_scalar(ARGS& a, cudaStream_t stream) {
   if (fill_tiles(a.tab, 1, (int64_t)kFusedBlock * kScalarUnroll) == 0) return cudaSuccess;
@@ -876,14 +500,6 @@ cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream
 }
 
 }  // namespace ar
-
-#define AR_DEFINE_FUSED_SHIFT(NAME, DT, OP)                                                        \
-  namespace ar {                                                                                  \
-  cudaError_t NAME(int order, FusedArgs& a, cudaStream_t s) { return launch_fused_shift_typed<DT, OP>(order, a, s); } \
-  cudaError_t NAME(int order, SmallFusedArgs& a, cudaStream_t s) {                                \
-    return launch_fused_shift_typed<DT, OP>(order, a, s);                                         \
-  }                                                                                               \
-  }
 
 #define AR_DEFINE_FUSED(NAME, DT, OP)                                                              \
   namespace ar {                                                                                  \

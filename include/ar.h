@@ -29,10 +29,11 @@
  *     aligned to the element size.  When all of them sit at the same address
  *     modulo 16 (16-byte aligned or not) the kernels move 16-byte vectors,
  *     cut at that offset.  Buffers at different offsets modulo 16 still move
- *     in aligned 16-byte words in the fused kernels (each rank read and
- *     written at its own offset, the words realigned in registers) for every
- *     order of up to 8 ranks and for rings of any size; trees of 16 or more
- *     ranks and the step-wise, gather and copy kernels then take a slower
+ *     in aligned 16-byte words in the fused kernels (each rank's words staged
+ *     in shared memory, folded there in the first buffer's frame and written
+ *     back at each rank's own offset) for rings of any size, trees of up to
+ *     64 ranks and double binary trees of 2, 4 or 8; wider double binary
+ *     trees and the step-wise, gather and copy kernels then take a slower
  *     one-element-per-thread path.  (For a bucketed call this holds per
  *     tensor: each tensor's N buffers.)
  *   - 1 <= nranks <= AR_MAX_RANKS; 0 <= count <= AR_MAX_COUNT (else

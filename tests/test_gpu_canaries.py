@@ -65,8 +65,7 @@ def test_collectives_stay_inside_their_buffers(ar, n, dtype):
         ["tree", "tree_stepwise", "binomial_stepwise"] if n & (n - 1) == 0 else [])
     for count in [c for c in sizes(n) if c > 0]:
         # aligned; the same offset in every rank (vectors cut at it); offsets
-        # differing by rank (the realigning vector kernel, or one element per
-        # thread)
+        # differing by rank (the staged kernel, or one element per thread)
         for shift in (0, ES[dtype], [(r * ES[dtype]) % 16 for r in range(n)]):
             G = Guarded(n, count, dtype, shift, seed=count + n)
             for algo in algos:
