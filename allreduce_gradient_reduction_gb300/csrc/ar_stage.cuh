@@ -182,9 +182,14 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         int top = 0;
         auto fold = [&](int p) {
           // copies still allowed in flight: those issued after rank p's
-          const int later = (kStream ? (n < p + NS ? n : p + NS) : n) - 1 - p;
+          // (streaming: ranks up to p + NS - 2, issued one step late, below)
+          int later = n - 1 - p;
+          if (kStream && p > 0 && later > NS - 2) later = NS - 2;
+          if (kStream && p == 0 && later > NS - 1) later = NS - 1;
           cp_async_wait_pending(later);
-          __syncthreads();
+          __syncthreads();  // rank p has landed; every thread has folded rank p - 1
+          // streaming: rank p - 1's slot is free, refill it
+          if (kStream && p > 0 && p - 1 + NS < n) issue(p - 1 + NS);
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             uint4 v = group(p, j);
@@ -200,10 +205,6 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           if constexpr (ORDER != RING) {
             for (int k = p; k & 1; k >>= 1) --top;
             ++top;
-          }
-          if (kStream && p + NS < n) {
-            __syncthreads();  // every thread has read the slot rank p + NS takes
-            issue(p + NS);
           }
         };
         if constexpr (NR > 0) {
