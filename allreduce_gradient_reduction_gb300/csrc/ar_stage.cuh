@@ -92,8 +92,32 @@ __host__ __device__ constexpr int stage_smem_bytes(int nr, int es) {
              : stage_copies(es, nr) * kStageCopyBytes;
 }
 
-// NR: 2, 4 or 8 ranks (every order), 16, 32 or 64 (ring and tree), 0 = the
-// table's rank count (ring).
+// The double binary tree's in-order fold (see inorder_root) over G groups
+// of words at once: positions LO..HI in increasing order, `take(p, v)`
+// handing over position p + 1's words when they have landed.
+template <int DT, int OP, int G, int LO, int HI, class TAKE>
+__device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
+  constexpr int R = inorder_root(LO, HI);
+  if constexpr (LO < R) {
+    stage_inorder<DT, OP, G, LO, R - 1>(acc, take);
+    uint4 own[G];
+    take(R - 1, own);
+#pragma unroll
+    for (int j = 0; j < G; ++j) acc[j] = step_vec<DT, OP>(acc[j], own[j]);
+  } else {
+    take(R - 1, acc);
+  }
+  if constexpr (R < HI) {
+    uint4 right[G];
+    stage_inorder<DT, OP, G, R + 1, HI>(right, take);
+#pragma unroll
+    for (int j = 0; j < G; ++j) acc[j] = step_vec<DT, OP>(acc[j], right[j]);
+  }
+}
+
+// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 0 = the table's rank count
+// (ring).  Every order folds the ranks in increasing position order, so
+// each is folded as soon as its copies have landed.
 template <class ARGS, int DT, int OP, int ORDER, int NR>
 __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
@@ -103,7 +127,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
   constexpr int NS = stage_slots(NR);
   constexpr bool kStream = NR == 0 || NR > kStageSlots;  // ranks stream through the slots
-  static_assert(NR == 0 ? ORDER == RING : (ORDER != DBTREE || NR <= kStageSlots), "no staged form");
+  static_assert(NR == 0 ? ORDER == RING : NR <= 64 && (NR & (NR - 1)) == 0, "no staged form");
   constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
@@ -161,17 +185,25 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         return make_uint4(word(0), word(1), word(2), word(3));
       };
       uint4 res[G];
+      // copies allowed in flight when position p is needed: those issued
+      // after it (streaming: up to p + NS - 2, a slot being refilled one
+      // step late, after the next position's barrier)
+      auto later_than = [&](int p) -> int {
+        int later = n - 1 - p;
+        if (kStream && p > 0 && later > NS - 2) later = NS - 2;
+        if (kStream && p == 0 && later > NS - 1) later = NS - 1;
+        return later;
+      };
       if constexpr (ORDER == DBTREE) {
-        // the in-order tree needs every rank at once
-        cp_async_wait_all();
-        __syncthreads();
+        // the in-order tree visits positions in increasing order too
+        auto take = [&](int p, uint4 (&v)[G]) {
+          cp_async_wait_pending(later_than(p));
+          __syncthreads();  // position p has landed; every thread has folded position p - 1
+          if (kStream && p > 0 && p - 1 + NS < n) issue(p - 1 + NS);
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-          uint4 x[NR];
-#pragma unroll
-          for (int p = 0; p < NR; ++p) x[p] = group(p, j);
-          res[j] = inorder_fold_regs<DT, OP, NR, 0, 1, NR>(x);
-        }
+          for (int j = 0; j < G; ++j) v[j] = group(p, j);
+        };
+        stage_inorder<DT, OP, G, 1, (NR > 0 ? NR : 1)>(res, take);
       } else {
         // rank p is folded as soon as its copies have landed, while the
         // later ranks' copies are still in flight; the tree keeps finished
@@ -181,12 +213,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         uint4 stk[G][kDepth];
         int top = 0;
         auto fold = [&](int p) {
-          // copies still allowed in flight: those issued after rank p's
-          // (streaming: ranks up to p + NS - 2, issued one step late, below)
-          int later = n - 1 - p;
-          if (kStream && p > 0 && later > NS - 2) later = NS - 2;
-          if (kStream && p == 0 && later > NS - 1) later = NS - 1;
-          cp_async_wait_pending(later);
+          cp_async_wait_pending(later_than(p));
           __syncthreads();  // rank p has landed; every thread has folded rank p - 1
           // streaming: rank p - 1's slot is free, refill it
           if (kStream && p > 0 && p - 1 + NS < n) issue(p - 1 + NS);
@@ -356,11 +383,11 @@ cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
 }
 
 // Rows whose buffers sit at different addresses modulo 16: the staged
-// kernel for rings of any size, trees of 2 to 64 ranks and double binary
-// trees of 2, 4 or 8.  Returns cudaErrorNotSupported otherwise (wider double
-// binary trees), for the element-wise kernel to take.
+// kernel for rings of any size and trees and double binary trees of 2 to 64
+// ranks.  Returns cudaErrorNotSupported otherwise (double binary trees of
+// other rank counts), for the element-wise kernel to take.
 __host__ __forceinline__ bool stage_form_exists(int order, int n) {
-  return order == RING || order == TREE || n == 2 || n == 4 || n == 8;
+  return order == RING || order == TREE || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
 }
 
 template <int DT, int OP, class ARGS>
@@ -379,6 +406,9 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
     case DBTREE * 100 + 2: return launch_fused_stage<DT, OP, DBTREE, 2>(a, stream);
     case DBTREE * 100 + 4: return launch_fused_stage<DT, OP, DBTREE, 4>(a, stream);
     case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
+    case DBTREE * 100 + 16: return launch_fused_stage<DT, OP, DBTREE, 16>(a, stream);
+    case DBTREE * 100 + 32: return launch_fused_stage<DT, OP, DBTREE, 32>(a, stream);
+    case DBTREE * 100 + 64: return launch_fused_stage<DT, OP, DBTREE, 64>(a, stream);
     default: break;
   }
   if (order == RING) return launch_fused_stage<DT, OP, RING, 0>(a, stream);

@@ -312,8 +312,8 @@ def test_mixed_phase_rows(ar, n, dtype):
     """Rank buffers at different addresses modulo 16 (the staged kernel:
     aligned words of every rank copied to shared memory, through eight slots
     beyond eight ranks, folded in the first buffer's frame, stored back at
-    each rank's phase; double binary trees of 16 or more ranks one element
-    per thread), in every order the rank count allows, for AllReduce,
+    each rank's phase; double binary trees of 3 or 5 ranks one element per
+    thread), in every order the rank count allows, for AllReduce,
     ReduceScatter (owner store) and Reduce (root store), over a size whose
     chunks span several tiles and end ragged.  Nothing outside the buffers
     may change."""
