@@ -73,9 +73,24 @@ static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
   return launch_pdl(gather_kernel<ES, VECTOR>, grid_for(t.ntiles), kFusedBlock, stream, t);
 }
 
+cudaError_t launch_stage_gather4(FusedArgs&, cudaStream_t);
+cudaError_t launch_stage_gather2(FusedArgs&, cudaStream_t);
+
+// Rows whose buffers share their address modulo 16 take the vector copy
+// kernel; the others the staged kernel's gather form (the owner's words
+// staged in shared memory, each destination written by bulk copies at its
+// own offset).
 cudaError_t launch_gather(int esize, bool vec, SegTable& t, cudaStream_t s) {
-  if (esize == 2) return vec ? launch_gather_typed<2, true>(t, s) : launch_gather_typed<2, false>(t, s);
-  return vec ? launch_gather_typed<4, true>(t, s) : launch_gather_typed<4, false>(t, s);
+  if (vec) return esize == 2 ? launch_gather_typed<2, true>(t, s) : launch_gather_typed<4, true>(t, s);
+  FusedArgs a;
+  a.tab = t;
+  a.avg = 0;
+  a.owner_only = 0;
+  a.to_root = 0;
+  a.root = 0;
+  a.max_grid = 0;
+  a.fn = 1.0f;
+  return esize == 2 ? launch_stage_gather2(a, s) : launch_stage_gather4(a, s);
 }
 
 // ---- bucket pack / unpack ----------------------------------------------------

@@ -71,25 +71,31 @@ __device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, 
 constexpr int kStageBlock = 256;
 constexpr int kStageSlots = 8;
 // Rank slots a block holds: one per rank up to eight ranks; NR = 0 (a
-// runtime rank count) and more ranks stream through eight.
-__host__ __device__ constexpr int stage_slots(int nr) { return nr > 0 && nr < kStageSlots ? nr : kStageSlots; }
-// Resident blocks per SM: as many as shared memory allows, since the tiles
-// in flight are what keeps HBM busy (three with eight slots, 66 KB each; six
-// below, 33 KB each, at 40 registers without spills).  Measured, 2-byte
-// elements at eight offsets: 4 x 128 MiB 162.8 / 158.5 / 157.5 us and
-// 2 x 128 MiB 98.1 / 89.3 / 83.9 us at four / five / six blocks;
-// 8 x 128 MiB 446.7 us at two, 351.4 at three (before the bulk stores).
-__host__ __device__ constexpr int stage_min_blocks(int nr) { return stage_slots(nr) == kStageSlots ? 3 : 6; }
+// runtime rank count) and more ranks stream through eight.  The gather form
+// (AllGather, Broadcast: one owner's words copied to the other ranks) holds
+// one.
+__host__ __device__ constexpr int stage_slots(int nr, bool gather) {
+  return gather ? 1 : nr > 0 && nr < kStageSlots ? nr : kStageSlots;
+}
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
-__host__ __device__ constexpr int stage_copies(int es, int nr) {
-  return es == 2 && stage_slots(nr) == kStageSlots ? 8 : 4;
+__host__ __device__ constexpr int stage_copies(int es, int nr, bool gather) {
+  return es == 2 && (gather || stage_slots(nr, gather) == kStageSlots) ? 8 : 4;
 }
-__host__ __device__ constexpr int stage_smem_bytes(int nr, int es) {
-  return stage_slots(nr) * kStageSlotBytes > stage_copies(es, nr) * kStageCopyBytes
-             ? stage_slots(nr) * kStageSlotBytes
-             : stage_copies(es, nr) * kStageCopyBytes;
+__host__ __device__ constexpr int stage_smem_bytes(int nr, int es, bool gather) {
+  return stage_slots(nr, gather) * kStageSlotBytes > stage_copies(es, nr, gather) * kStageCopyBytes
+             ? stage_slots(nr, gather) * kStageSlotBytes
+             : stage_copies(es, nr, gather) * kStageCopyBytes;
+}
+// Resident blocks per SM: as many as shared memory allows, since the tiles
+// in flight are what keeps HBM busy (three at 66 KB, six at 33 KB with 40
+// registers and no spills).  Measured, 2-byte elements at eight offsets:
+// 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 / 89.3 / 83.9 us
+// at four / five / six blocks; 8 x 128 MiB 446.7 us at two, 351.4 at three
+// (before the bulk stores).
+__host__ __device__ constexpr int stage_min_blocks(int nr, int es, bool gather) {
+  return stage_smem_bytes(nr, es, gather) > 48 * 1024 ? 3 : 6;
 }
 
 // The double binary tree's in-order fold (see inorder_root) over G groups
@@ -117,18 +123,20 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
 
 // NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 0 = the table's rank count
 // (ring).  Every order folds the ranks in increasing position order, so
-// each is folded as soon as its copies have landed.
-template <class ARGS, int DT, int OP, int ORDER, int NR>
-__global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage_kernel(const __grid_constant__ ARGS a) {
+// each is folded as soon as its copies have landed.  GATHER: no fold, the
+// segment's owner (its chunk id) is copied to every other rank.
+template <class ARGS, int DT, int OP, int ORDER, int NR, bool GATHER>
+__global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>::value, GATHER))
+    fused_stage_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
   constexpr int VEC = 16 / ES;
   constexpr int TV = kStageTileVecs;
   constexpr int G = TV * 4 / kStageBlock / 4;  // groups of 4 frame words per thread
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
-  constexpr int NS = stage_slots(NR);
-  constexpr bool kStream = NR == 0 || NR > kStageSlots;  // ranks stream through the slots
+  constexpr int NS = stage_slots(NR, GATHER);
+  constexpr bool kStream = !GATHER && (NR == 0 || NR > kStageSlots);  // ranks stream through the slots
   static_assert(NR == 0 ? ORDER == RING : NR <= 64 && (NR & (NR - 1)) == 0, "no staged form");
-  constexpr bool kHalfCopies = stage_copies(ES, NR) == 8;
+  constexpr bool kHalfCopies = stage_copies(ES, NR, GATHER) == 8;
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
   const auto& T = a.tab;
@@ -152,7 +160,8 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
       // into slot p (mod the slot count), one commit group each
       const int rank_shift = ORDER == DBTREE && c != 0 ? 1 : 0;
       auto rank_at = [&](int p) -> int {
-        if constexpr (ORDER == RING) return rot(c + 1 + p, n);
+        if constexpr (GATHER) return c;
+        else if constexpr (ORDER == RING) return rot(c + 1 + p, n);
         else if constexpr (ORDER == DBTREE) return rot(p + rank_shift, n);
         else return p;
       };
@@ -166,7 +175,9 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         for (int i = tid; i < nw; i += kStageBlock) cp_async16(d + i * 16, g + i * 16);
         cp_async_commit();
       };
-      if constexpr (kStream) {
+      if constexpr (GATHER) {
+        issue(0);
+      } else if constexpr (kStream) {
         const int first = n < NS ? n : NS;
         for (int p = 0; p < first; ++p) issue(p);
       } else {
@@ -194,7 +205,12 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
         if (kStream && p == 0 && later > NS - 1) later = NS - 1;
         return later;
       };
-      if constexpr (ORDER == DBTREE) {
+      if constexpr (GATHER) {
+        cp_async_wait_all();
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < G; ++j) res[j] = group(0, j);
+      } else if constexpr (ORDER == DBTREE) {
         // the in-order tree visits positions in increasing order too
         auto take = [&](int p, uint4 (&v)[G]) {
           cp_async_wait_pending(later_than(p));
@@ -329,7 +345,11 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
           }
         }
       };
-      if (a.owner_only || a.to_root) {
+      if constexpr (GATHER) {
+#pragma unroll 1
+        for (int r = 0; r < n; ++r)
+          if (r != c) put(r);
+      } else if (a.owner_only || a.to_root) {
         put(a.owner_only ? c : a.root);
       } else if constexpr (NR > 0 && NR <= kStageSlots) {
 #pragma unroll
@@ -344,12 +364,18 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
     // elements of the segment outside its full vectors
     if (ti == 0 && tid < sh.head + sh.tail) {
       const int64_t e = scalar_elem<VEC>(s, sh, tid, shift);
-      uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
-      if (a.avg) r = div_word<DT>(r, a.fn);
-      if (a.owner_only || a.to_root) {
-        st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
+      if constexpr (GATHER) {
+        const uint32_t v = ld_elem<ES>(P[c], e);
+        for (int q = 0; q < n; ++q)
+          if (q != c) st_elem<ES>(const_cast<void*>(P[q]), e, v);
       } else {
-        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+        uint32_t r = fold_scalar<DT, OP, ORDER>(P, n, c, e);
+        if (a.avg) r = div_word<DT>(r, a.fn);
+        if (a.owner_only || a.to_root) {
+          st_elem<ES>(const_cast<void*>(P[a.owner_only ? c : a.root]), e, r);
+        } else {
+          for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, r);
+        }
       }
     }
     // the next tile's copies overwrite shared memory every thread and every
@@ -362,10 +388,10 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR)) fused_stage
   if (tid == 0) bulk_wait_all();
 }
 
-template <int DT, int OP, int ORDER, int NR, class ARGS>
+template <int DT, int OP, int ORDER, int NR, bool GATHER = false, class ARGS>
 cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
-  constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value);
-  auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR>;
+  constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value, GATHER);
+  auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR, GATHER>;
   // opened once per device to the shared memory the kernel uses
   static std::atomic<bool> opened[256];
   int dev = 0;
@@ -416,6 +442,13 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
 }
 
 }  // namespace ar
+
+// AllGather / Broadcast of rows whose buffers sit at different addresses
+// modulo 16 (element size of DT; the table's chunk ids name the owners).
+#define AR_DEFINE_STAGE_GATHER(NAME, DT)                                                            \
+  namespace ar {                                                                                      \
+  cudaError_t NAME(FusedArgs& a, cudaStream_t s) { return launch_fused_stage<DT, SUM, RING, 0, true>(a, s); } \
+  }
 
 #define AR_DEFINE_STAGE(NAME, DT, OP)                                                                \
   namespace ar {                                                                                      \

@@ -3,3 +3,4 @@
 #include "ar_stage.cuh"
 AR_DEFINE_STAGE(launch_stage_bf16_sum, BF16, SUM)
 AR_DEFINE_STAGE(launch_stage_bf16_max, BF16, MAX)
+AR_DEFINE_STAGE_GATHER(launch_stage_gather2, BF16)

@@ -3,3 +3,4 @@
 #include "ar_stage.cuh"
 AR_DEFINE_STAGE(launch_stage_f32_sum, F32, SUM)
 AR_DEFINE_STAGE(launch_stage_f32_max, F32, MAX)
+AR_DEFINE_STAGE_GATHER(launch_stage_gather4, F32)
