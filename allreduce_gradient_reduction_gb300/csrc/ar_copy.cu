@@ -14,9 +14,11 @@ namespace ar {
 // registers): 1-4% faster alone than four positions without the cap.
 constexpr int kGatherUnroll = 2;
 
-template <int ES, bool VECTOR>
+// Rows whose buffers share their address modulo 16: 16-byte vectors cut at
+// that offset, the segment's scalar ends one element per thread.
+template <int ES>
 __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_constant__ SegTable T) {
-  constexpr int VEC = VECTOR ? 16 / ES : 1;
+  constexpr int VEC = 16 / ES;
   constexpr int TILE = kFusedBlock * kGatherUnroll;
   pdl_prologue();
   const int n = T.nranks;
@@ -26,51 +28,39 @@ __global__ void __launch_bounds__(kFusedBlock, 4) gather_kernel(const __grid_con
     const void* const* P = T.ptr + (size_t)s.tensor * n;
     const char* src = static_cast<const char*>(P[c]);
     const int64_t ti = tile - s.tile_begin;
-    if constexpr (VECTOR) {
-      const int shift = row_shift(P[0], ES);  // the row's buffers share it
-      const SegShape sh = seg_shape<VEC>(s, shift);
-      uint4 x[kGatherUnroll];
-      int64_t off[kGatherUnroll];
-      bool ok[kGatherUnroll];
+    const int shift = row_shift(P[0], ES);  // the row's buffers share it
+    const SegShape sh = seg_shape<VEC>(s, shift);
+    uint4 x[kGatherUnroll];
+    int64_t off[kGatherUnroll];
+    bool ok[kGatherUnroll];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int64_t v = sh.vb + ti * TILE + u * kFusedBlock + threadIdx.x;
-        ok[u] = v < sh.ve;
-        off[u] = v * 16 - shift * ES;
-        if (ok[u]) x[u] = ld_stream(src + off[u]);
-      }
-      for (int r = 0; r < n; ++r) {
-        if (r == c) continue;
-        char* dst = static_cast<char*>(const_cast<void*>(P[r]));
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int64_t v = sh.vb + ti * TILE + u * kFusedBlock + threadIdx.x;
+      ok[u] = v < sh.ve;
+      off[u] = v * 16 - shift * ES;
+      if (ok[u]) x[u] = ld_stream(src + off[u]);
+    }
+    for (int r = 0; r < n; ++r) {
+      if (r == c) continue;
+      char* dst = static_cast<char*>(const_cast<void*>(P[r]));
 #pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u)
-          if (ok[u]) st_stream(dst + off[u], x[u]);
-      }
-      if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
-        const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x, shift);
-        const uint32_t v = ld_elem<ES>(src, e);
-        for (int r = 0; r < n; ++r)
-          if (r != c) st_elem<ES>(const_cast<void*>(P[r]), e, v);
-      }
-    } else {
-      const int64_t e = s.begin + ti * TILE + threadIdx.x;
-#pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int64_t eu = e + u * kFusedBlock;
-        if (eu >= s.end) continue;
-        const uint32_t v = ld_elem<ES>(src, eu);
-        for (int r = 0; r < n; ++r)
-          if (r != c) st_elem<ES>(const_cast<void*>(P[r]), eu, v);
-      }
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (ok[u]) st_stream(dst + off[u], x[u]);
+    }
+    if (ti == 0 && (int)threadIdx.x < sh.head + sh.tail) {
+      const int64_t e = scalar_elem<VEC>(s, sh, threadIdx.x, shift);
+      const uint32_t v = ld_elem<ES>(src, e);
+      for (int r = 0; r < n; ++r)
+        if (r != c) st_elem<ES>(const_cast<void*>(P[r]), e, v);
     }
   }
 }
 
-template <int ES, bool VECTOR>
+template <int ES>
 static cudaError_t launch_gather_typed(SegTable& t, cudaStream_t stream) {
-  if (fill_tiles(t, VECTOR ? 16 / ES : 1, (int64_t)kFusedBlock * kGatherUnroll, VECTOR) == 0) return cudaSuccess;
+  if (fill_tiles(t, 16 / ES, (int64_t)kFusedBlock * kGatherUnroll, true) == 0) return cudaSuccess;
   count_launch();
-  return launch_pdl(gather_kernel<ES, VECTOR>, grid_for(t.ntiles), kFusedBlock, stream, t);
+  return launch_pdl(gather_kernel<ES>, grid_for(t.ntiles), kFusedBlock, stream, t);
 }
 
 cudaError_t launch_stage_gather4(FusedArgs&, cudaStream_t);
@@ -81,7 +71,7 @@ cudaError_t launch_stage_gather2(FusedArgs&, cudaStream_t);
 // staged in shared memory, each destination written by bulk copies at its
 // own offset).
 cudaError_t launch_gather(int esize, bool vec, SegTable& t, cudaStream_t s) {
-  if (vec) return esize == 2 ? launch_gather_typed<2, true>(t, s) : launch_gather_typed<4, true>(t, s);
+  if (vec) return esize == 2 ? launch_gather_typed<2>(t, s) : launch_gather_typed<4>(t, s);
   FusedArgs a;
   a.tab = t;
   a.avg = 0;
