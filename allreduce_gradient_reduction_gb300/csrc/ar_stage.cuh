@@ -225,14 +225,24 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
         // later ranks' copies are still in flight; the tree keeps finished
         // subtrees on a stack (a binary counter over the rank index), which
         // is the same balanced pairwise tree
-        constexpr int kDepth = ORDER == RING ? 1 : (NR >= 64 ? 7 : NR >= 32 ? 6 : NR >= 16 ? 5 : 4);
-        uint4 stk[G][kDepth];
-        int top = 0;
-        auto fold = [&](int p) {
+        auto arrive = [&](int p) {
           cp_async_wait_pending(later_than(p));
           __syncthreads();  // rank p has landed; every thread has folded rank p - 1
           // streaming: rank p - 1's slot is free, refill it
           if (kStream && p > 0 && p - 1 + NS < n) issue(p - 1 + NS);
+        };
+        // 64-rank trees fold subtrees of 8 in a loop (below); measured on
+        // bf16 at eight offsets, 64 x 8 MiB 244.9 -> 200.2 us, while 16 x 32
+        // MiB (164.6 -> 171.7) and 32 x 16 MiB f32 (168.3 -> 179.6) were
+        // faster fully unrolled
+        constexpr bool kWideTree = ORDER == TREE && NR == 64;
+        // entries the counter holds: log2 of the ranks it counts over
+        constexpr int kDepth = ORDER == RING ? 1 : kWideTree || NR <= 16 ? 4 : NR == 32 ? 5 : 6;
+        uint4 stk[G][kDepth];
+        int top = 0;
+        // pos: the rank's place in its subtree (p itself up to 8 ranks)
+        auto fold = [&](int p, int pos) {
+          arrive(p);
 #pragma unroll
           for (int j = 0; j < G; ++j) {
             uint4 v = group(p, j);
@@ -241,24 +251,49 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
             } else {
               int t = top;
 #pragma unroll
-              for (int k = p; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[j][--t], v);
+              for (int k = pos; k & 1; k >>= 1) v = step_vec<DT, OP>(stk[j][--t], v);
               stk[j][t] = v;
             }
           }
           if constexpr (ORDER != RING) {
-            for (int k = p; k & 1; k >>= 1) --top;
+            for (int k = pos; k & 1; k >>= 1) --top;
             ++top;
           }
         };
-        if constexpr (NR > 0) {
+        if constexpr (kWideTree) {
+          // subtrees of 8 consecutive ranks, each folded by the unrolled
+          // counter above, merged by a counter over the subtree index in a
+          // loop that is not unrolled (unrolled over 64 ranks the kernel is
+          // much larger and slower)
+          uint4 done[G][3];
+#pragma unroll 1
+          for (int g = 0; g < NR / kStageSlots; ++g) {
+            top = 0;
 #pragma unroll
-          for (int p = 0; p < NR; ++p) fold(p);
+            for (int q = 0; q < kStageSlots; ++q) fold(q + kStageSlots * g, q);
+            int t = 0;
+            for (int k = g; k & 1; k >>= 1) ++t;  // subtrees merged now
+            const int base_top = __popc(g) - t;  // finished subtrees below them
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              uint4 v = stk[j][0];
+              for (int k = 0; k < t; ++k) v = step_vec<DT, OP>(done[j][base_top + t - 1 - k], v);
+              done[j][base_top] = v;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < G; ++j) res[j] = done[j][0];
+        } else if constexpr (NR > 0) {
+#pragma unroll
+          for (int p = 0; p < NR; ++p) fold(p, p);
+#pragma unroll
+          for (int j = 0; j < G; ++j) res[j] = stk[j][0];
         } else {
 #pragma unroll 1
-          for (int p = 0; p < n; ++p) fold(p);
-        }
+          for (int p = 0; p < n; ++p) fold(p, p);
 #pragma unroll
-        for (int j = 0; j < G; ++j) res[j] = stk[j][0];
+          for (int j = 0; j < G; ++j) res[j] = stk[j][0];
+        }
       }
       if (a.avg) {
 #pragma unroll

@@ -306,7 +306,7 @@ def test_unaligned_buffers(ar, algo, dtype):
             assert np.array_equal(from_dev([big[r][:shifts[r]]], dtype)[0], x[r, :shifts[r]])
 
 
-@pytest.mark.parametrize("n", [2, 3, 4, 5, 16, 64])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 32, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_mixed_phase_rows(ar, n, dtype):
     """Rank buffers at different addresses modulo 16 (the staged kernel:
