@@ -1030,6 +1030,27 @@ def other_workloads(dev, torch, np, W, ar, stream, clocks, peak):
                                "algorithmic_bytes": nbytes, "clocks": clocks.summary(*win)}
     del bufs
 
+    # the headline configuration with every rank buffer at a different address
+    # modulo 16 (rank r starts (3r + 1) mod 8 elements into its allocation):
+    # the staged kernel
+    n, count = W.LARGE["nranks"], W.LARGE["count"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(W.BASE_SEED + 1000 * W.CONFIG_LARGE + 7)
+    bufs = rank_buffers(n, count, torch.bfloat16, dev, 2, "mixed")
+    for b in bufs:
+        b.copy_(torch.randn(count, device=dev, generator=gen).to(torch.bfloat16))
+    nbytes = 2 * n * count * 2
+    ms, win = timed_calls(lambda: chk(ar.ar_allreduce(bufs, count=count, dtype="bf16", op="sum", algo="ring",
+                                                      stream=sid), "large mixed"), 200, stream, torch)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["large_mixed_offsets"] = {
+        "workload": "ring AllReduce SUM, 8 ranks x 67,108,864 bf16, rank buffers at eight different addresses "
+                    "modulo 16 (element offsets " + ", ".join(str(o) for o in rank_offsets(n, 2, "mixed")) + ")",
+        "ms_per_step": ms, "effective_gbs": gbs, "frac": gbs / peak, "algorithmic_bytes": nbytes,
+        "clocks": clocks.summary(*win)}
+    del bufs
+    torch.cuda.empty_cache()
+
     # GPT-2 small gradients in 25 MiB reverse-order buckets, AVG: fused and literal
     counts = W.gpt2_small_counts()
     total = int(counts.sum())
@@ -1063,8 +1084,8 @@ def other_workloads(dev, torch, np, W, ar, stream, clocks, peak):
     del flats, grads, ws
     torch.cuda.empty_cache()
     out["note"] = ("each timed like the headline (CUDA events over back-to-back calls); bucket and small inputs "
-                   "from the seeded host recipe, GPT-2 gradients drawn on the device (normal(0, 1e-4)); frac is "
-                   "of the measured copy bandwidth")
+                   "from the seeded host recipe, GPT-2 gradients and the mixed-offset rows drawn on the device "
+                   "(normal(0, 1e-4); normal(0, 1)); frac is of the measured copy bandwidth")
     return out
 
 
