@@ -71,31 +71,35 @@ __device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, 
 constexpr int kStageBlock = 256;
 constexpr int kStageSlots = 8;
 // Rank slots a block holds: one per rank up to eight ranks; NR = 0 (a
-// runtime rank count) and more ranks stream through eight.  The gather form
-// (AllGather, Broadcast: one owner's words copied to the other ranks) holds
-// one.
-__host__ __device__ constexpr int stage_slots(int nr, bool gather) {
+// runtime rank count) and more ranks stream through eight.  The gather forms
+// (AllGather, Broadcast: one owner's words copied to the other ranks; GATHER
+// 1 for up to eight ranks, 2 beyond) hold one.
+__host__ __device__ constexpr int stage_slots(int nr, int gather) {
   return gather ? 1 : nr > 0 && nr < kStageSlots ? nr : kStageSlots;
 }
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
-__host__ __device__ constexpr int stage_copies(int es, int nr, bool gather) {
-  return es == 2 && (gather || stage_slots(nr, gather) == kStageSlots) ? 8 : 4;
+__host__ __device__ constexpr int stage_copies(int es, int nr, int gather) {
+  return gather == 1 ? 2 : es == 2 && (gather == 2 || stage_slots(nr, gather) == kStageSlots) ? 8 : 4;
 }
-__host__ __device__ constexpr int stage_smem_bytes(int nr, int es, bool gather) {
-  return stage_slots(nr, gather) * kStageSlotBytes > stage_copies(es, nr, gather) * kStageCopyBytes
+// Gather form 1 keeps its slot and two copy buffers apart (it builds one
+// destination's copy while the bulk copy of the previous one reads the
+// other); the other forms reuse the slots for the copies.
+__host__ __device__ constexpr int stage_smem_bytes(int nr, int es, int gather) {
+  return gather == 1 ? kStageSlotBytes + 2 * kStageCopyBytes
+         : stage_slots(nr, gather) * kStageSlotBytes > stage_copies(es, nr, gather) * kStageCopyBytes
              ? stage_slots(nr, gather) * kStageSlotBytes
              : stage_copies(es, nr, gather) * kStageCopyBytes;
 }
 // Resident blocks per SM: as many as shared memory allows, since the tiles
 // in flight are what keeps HBM busy (three at 66 KB, six at 33 KB with 40
-// registers and no spills).  Measured, 2-byte elements at eight offsets:
+// registers and no spills; the gather form eight at 25 KB).  Measured, 2-byte elements at eight offsets:
 // 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 / 89.3 / 83.9 us
 // at four / five / six blocks; 8 x 128 MiB 446.7 us at two, 351.4 at three
 // (before the bulk stores).
-__host__ __device__ constexpr int stage_min_blocks(int nr, int es, bool gather) {
-  return stage_smem_bytes(nr, es, gather) > 48 * 1024 ? 3 : 6;
+__host__ __device__ constexpr int stage_min_blocks(int nr, int es, int gather) {
+  return gather == 1 ? 8 : stage_smem_bytes(nr, es, gather) > 48 * 1024 ? 3 : 6;
 }
 
 // The double binary tree's in-order fold (see inorder_root) over G groups
@@ -124,8 +128,10 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
 // NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 0 = the table's rank count
 // (ring).  Every order folds the ranks in increasing position order, so
 // each is folded as soon as its copies have landed.  GATHER: no fold, the
-// segment's owner (its chunk id) is copied to every other rank.
-template <class ARGS, int DT, int OP, int ORDER, int NR, bool GATHER>
+// segment's owner (its chunk id) is copied to every other rank, a copy built
+// per destination in turn (1: up to eight ranks, whose phases seldom
+// repeat) or all eight phases at once (2: more ranks).
+template <class ARGS, int DT, int OP, int ORDER, int NR, int GATHER>
 __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>::value, GATHER))
     fused_stage_kernel(const __grid_constant__ ARGS a) {
   constexpr int ES = ElemSize<DT>::value;
@@ -301,6 +307,56 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
       }
       __syncthreads();  // every slot has been read
 
+      if constexpr (GATHER == 1) {
+        // (3+4) per destination: a copy of the owner's words in its phase
+        // (word m at index m + k + 4, for h = 2 the stream one element
+        // earlier), built while the bulk copy of the destination before
+        // reads the other buffer
+        const int offc = byte_phase(P[c], P[0]);
+        const uint32_t* own = reinterpret_cast<const uint32_t*>(S) + (offc >> 2);  // the staged slot
+        int idx = 0;
+#pragma unroll 1
+        for (int r = 0; r < n; ++r) {
+          if (r == c) continue;
+          const int off = byte_phase(P[r], P[0]);
+          const int k = off >> 2;
+          const bool h = ES == 2 && (off & 2);
+          uint32_t* cw = reinterpret_cast<uint32_t*>(S + kStageSlotBytes + (idx & 1) * kStageCopyBytes);
+          if (idx >= 2) {
+            if (tid == 0) bulk_wait_read_but_one();  // the buffer's previous bulk copy has read it
+            __syncthreads();
+          }
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            const uint32_t f[4] = {res[j].x, res[j].y, res[j].z, res[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int m = tid + (4 * j + q) * kStageBlock;
+              uint32_t v = f[q];
+              if (h) {
+                uint32_t below = __shfl_up_sync(0xffffffffu, f[q], 1);
+                if (lane == 0 && m > 0) {
+                  below = own[m - 1];
+                  if constexpr (ES == 2) below = __funnelshift_r(below, own[m], (uint32_t)(offc & 2) * 8);
+                }
+                v = __funnelshift_l(below, f[q], 16);
+              }
+              cw[k + 4 + m] = v;
+            }
+          }
+          if (h && tid == kStageBlock - 1) cw[k + 4 + 4 * TV] = __funnelshift_l(res[G - 1].w, 0u, 16);
+          fence_proxy_async_shared();
+          __syncthreads();
+          const uint4* cp = reinterpret_cast<const uint4*>(cw);
+          char* g = static_cast<char*>(const_cast<void*>(P[r])) + base - off;
+          const int lo = off != 0;
+          if (tid == 0 && nv > lo) bulk_store(g + 16 * lo, cp + lo + 1, 16 * (nv - lo));
+          if (off != 0 && tid == 32) st_stream_part(g, cp[1], off, 16);
+          if (off != 0 && tid == 64) st_stream_part(g + 16 * (int64_t)nv, cp[nv + 1], 0, off);
+          if (tid == 0) bulk_commit();
+          ++idx;
+        }
+      } else {
       // (3) copy k holds frame word m at word index m + k + 4
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -380,7 +436,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
           }
         }
       };
-      if constexpr (GATHER) {
+      if constexpr (GATHER == 2) {
 #pragma unroll 1
         for (int r = 0; r < n; ++r)
           if (r != c) put(r);
@@ -394,6 +450,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
         for (int r = 0; r < n; ++r) put(r);
       }
       if (tid == 0) bulk_commit();
+      }
     }
 
     // elements of the segment outside its full vectors
@@ -423,7 +480,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
   if (tid == 0) bulk_wait_all();
 }
 
-template <int DT, int OP, int ORDER, int NR, bool GATHER = false, class ARGS>
+template <int DT, int OP, int ORDER, int NR, int GATHER = 0, class ARGS>
 cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
   constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value, GATHER);
   auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR, GATHER>;
@@ -482,7 +539,10 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
 // modulo 16 (element size of DT; the table's chunk ids name the owners).
 #define AR_DEFINE_STAGE_GATHER(NAME, DT)                                                            \
   namespace ar {                                                                                      \
-  cudaError_t NAME(FusedArgs& a, cudaStream_t s) { return launch_fused_stage<DT, SUM, RING, 0, true>(a, s); } \
+  cudaError_t NAME(FusedArgs& a, cudaStream_t s) {                                                    \
+    return a.tab.nranks <= kStageSlots ? launch_fused_stage<DT, SUM, RING, 0, 1>(a, s)                \
+                                       : launch_fused_stage<DT, SUM, RING, 0, 2>(a, s);               \
+  }                                                                                                   \
   }
 
 #define AR_DEFINE_STAGE(NAME, DT, OP)                                                                \

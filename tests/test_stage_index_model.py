@@ -7,7 +7,8 @@ of each segment, the aligned 16-byte words staged per rank (one slot per rank
 up to eight, eight slots streamed beyond that, one for the gather form), the
 4-byte frame words read from a slot at a rank's offset, the fold in the
 schedule's position order, the shifted result copies (four word shifts, four
-more moved by one 2-byte element), and the stores: one bulk copy of whole
+more moved by one 2-byte element; the gather form of up to 8 ranks builds
+one copy per destination, in two buffers used in turn), and the stores: one bulk copy of whole
 entries per destination plus the two partial edge words, or, for 2- and
 4-rank rows of 2-byte elements, words shifted in registers.  The fold step is
 a stand-in operation that is neither commutative nor associative, so any
@@ -35,11 +36,21 @@ def slots(nr, gather):
     return 1 if gather else nr if nr < 8 else 8
 
 
+def gather_form(nr):
+    """1: a copy per destination in two buffers used in turn (up to 8 ranks);
+    2: all shifted copies at once (more ranks)."""
+    return 1 if nr <= 8 else 2
+
+
 def copies(es, nr, gather):
+    if gather and gather_form(nr) == 1:
+        return 2
     return 8 if es == 2 and (gather or slots(nr, gather) == 8) else 4
 
 
 def smem_bytes(nr, es, gather):
+    if gather and gather_form(nr) == 1:  # the slot, then the two copy buffers
+        return SLOT + 2 * COPY
     return max(slots(nr, gather) * SLOT, copies(es, nr, gather) * COPY)
 
 
@@ -248,9 +259,32 @@ def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000
                 F = fold(order, [vals[(p - (c + 1)) % nr] if order == "ring" else
                                  vals[(p - (1 if c else 0)) % nr] if order == "dbtree" else vals[p]
                                  for p in range(nr)], c, nr, f)
+            if gather and gather_form(nr) == 1:
+                for idx, r0 in enumerate(r for r in range(nr) if r != c):
+                    off = (P[r0] - P[0]) & 15
+                    k, h = off >> 2, es == 2 and off & 2
+                    cb = SLOT + (idx & 1) * COPY
+                    assert cb + COPY <= smem
+                    buf = words(S[cb:cb + COPY]).copy()
+                    if h:
+                        below = np.concatenate(([F[0]], F[:-1]))  # m = 0: a value no stored byte uses
+                        buf[k + 4:k + 4 + 4 * TV] = fshl(below, F, 16)
+                        buf[k + 4 + 4 * TV] = fshl(F[-1], np.uint64(0), 16)
+                    else:
+                        buf[k + 4:k + 4 + 4 * TV] = F
+                    S[cb:cb + COPY] = buf.astype("<u4").view(np.uint8)
+                    for r in (r0,):
+                        g = P[r] + base - off
+                        lo = 1 if off else 0
+                        if nv > lo:
+                            stores.append((g + 16 * lo, S[cb + 16 * (lo + 1):cb + 16 * (nv + 1)].copy()))
+                        if off:
+                            stores.append((g + off, S[cb + 16:cb + 32][off:].copy()))
+                            stores.append((g + 16 * nv, S[cb + 16 * (nv + 1):cb + 16 * (nv + 2)][:off].copy()))
             # the shifted copies: copy k holds frame word m at word index m + k + 4
-            C = [words(S[k * COPY:(k + 1) * COPY]).copy() for k in range(copies(es, nr, gather))]
-            for k in range(4):
+            form1 = gather and gather_form(nr) == 1
+            C = [] if form1 else [words(S[k * COPY:(k + 1) * COPY]).copy() for k in range(copies(es, nr, gather))]
+            for k in range(len(C) and 4):
                 C[k][k + 4:k + 4 + 4 * TV] = F
             if len(C) == 8:
                 below = np.concatenate(([C[0][3]], F[:-1]))   # lane 0 reads copy 0's word below
@@ -261,7 +295,7 @@ def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000
                         C[4 + k][k + 4 + 4 * TV] = fshl(F[-1], np.uint64(0), 16)
             for k, ck in enumerate(C):
                 S[k * COPY:(k + 1) * COPY] = ck.astype("<u4").view(np.uint8)
-            dests = [r for r in range(nr) if r != c] if gather else [c] if owner_only else range(nr)
+            dests = [] if form1 else [r for r in range(nr) if r != c] if gather else [c] if owner_only else range(nr)
             for r in dests:
                 off = (P[r] - P[0]) & 15
                 k, hs = off >> 2, off & 2
@@ -345,6 +379,8 @@ CASES = [
     (8, 2, "ring", False, True, (512 * 8 * 8 + 21,)),
     (5, 4, "broadcast", False, True, (512 * 4 + 999,)),
     (8, 2, "broadcast", False, True, (3, 5000)),
+    (16, 2, "ring", False, True, (16 * 8 * 60 + 3,)),
+    (16, 4, "broadcast", False, True, (7000,)),
 ]
 
 
