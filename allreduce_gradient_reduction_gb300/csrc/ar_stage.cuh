@@ -94,12 +94,17 @@ __host__ __device__ constexpr int stage_smem_bytes(int nr, int es, int gather) {
 }
 // Resident blocks per SM: as many as shared memory allows, since the tiles
 // in flight are what keeps HBM busy (three at 66 KB, six at 33 KB with 40
-// registers and no spills; the gather form eight at 25 KB).  Measured, 2-byte elements at eight offsets:
+// registers and no spills; the gather form eight at 25 KB; 5-, 6- and 7-rank
+// rings five, four and three).  Measured, 2-byte elements at eight offsets:
 // 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 / 89.3 / 83.9 us
 // at four / five / six blocks; 8 x 128 MiB 446.7 us at two, 351.4 at three
 // (before the bulk stores).
 __host__ __device__ constexpr int stage_min_blocks(int nr, int es, int gather) {
-  return gather == 1 ? 8 : stage_smem_bytes(nr, es, gather) > 48 * 1024 ? 3 : 6;
+  // what an SM's 228 KB of shared memory (1 KB reserved per block) holds,
+  // at most 8 for the gather form and 6 for the folds
+  return (gather == 1 ? 8 : 6) < 233472 / (stage_smem_bytes(nr, es, gather) + 1024)
+             ? (gather == 1 ? 8 : 6)
+             : 233472 / (stage_smem_bytes(nr, es, gather) + 1024);
 }
 
 // The double binary tree's in-order fold (see inorder_root) over G groups
@@ -125,8 +130,8 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
   }
 }
 
-// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 0 = the table's rank count
-// (ring).  Every order folds the ranks in increasing position order, so
+// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 3, 5, 6 or 7 (ring), 0 =
+// the table's rank count (ring).  Every order folds the ranks in increasing position order, so
 // each is folded as soon as its copies have landed.  GATHER: no fold, the
 // segment's owner (its chunk id) is copied to every other rank, a copy built
 // per destination in turn (1: up to eight ranks, whose phases seldom
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
   constexpr int NS = stage_slots(NR, GATHER);
   constexpr bool kStream = !GATHER && (NR == 0 || NR > kStageSlots);  // ranks stream through the slots
-  static_assert(NR == 0 ? ORDER == RING : NR <= 64 && (NR & (NR - 1)) == 0, "no staged form");
+  static_assert(NR == 0 ? ORDER == RING : NR <= 64 && ((NR & (NR - 1)) == 0 || ORDER == RING), "no staged form");
   constexpr bool kHalfCopies = stage_copies(ES, NR, GATHER) == 8;
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
@@ -513,7 +518,11 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
   switch (order * 100 + n) {
     case RING * 100 + 2: return launch_fused_stage<DT, OP, RING, 2>(a, stream);
+    case RING * 100 + 3: return launch_fused_stage<DT, OP, RING, 3>(a, stream);
     case RING * 100 + 4: return launch_fused_stage<DT, OP, RING, 4>(a, stream);
+    case RING * 100 + 5: return launch_fused_stage<DT, OP, RING, 5>(a, stream);
+    case RING * 100 + 6: return launch_fused_stage<DT, OP, RING, 6>(a, stream);
+    case RING * 100 + 7: return launch_fused_stage<DT, OP, RING, 7>(a, stream);
     case RING * 100 + 8: return launch_fused_stage<DT, OP, RING, 8>(a, stream);
     case TREE * 100 + 2: return launch_fused_stage<DT, OP, TREE, 2>(a, stream);
     case TREE * 100 + 4: return launch_fused_stage<DT, OP, TREE, 4>(a, stream);

@@ -1,0 +1,4 @@
+// Fused kernels for bf16 rows whose buffers sit at different addresses modulo
+// 16, max: one translation unit per dtype and op, compiled in parallel.
+#include "ar_stage.cuh"
+AR_DEFINE_STAGE(launch_stage_bf16_max, BF16, MAX)
