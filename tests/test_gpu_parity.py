@@ -306,17 +306,18 @@ def test_unaligned_buffers(ar, algo, dtype):
             assert np.array_equal(from_dev([big[r][:shifts[r]]], dtype)[0], x[r, :shifts[r]])
 
 
-@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 32, 64])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 6, 7, 8, 16, 24, 32, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
 def test_mixed_phase_rows(ar, n, dtype):
     """Rank buffers at different addresses modulo 16 (the staged kernel:
     aligned words of every rank copied to shared memory, through eight slots
     beyond eight ranks, folded in the first buffer's frame, stored back at
-    each rank's phase; double binary trees of 3 or 5 ranks one element per
+    each rank's phase; double binary trees of other rank counts one element per
     thread), in every order the rank count allows, for AllReduce,
     ReduceScatter (owner store) and Reduce (root store), over a size whose
-    chunks span several tiles and end ragged.  Nothing outside the buffers
-    may change."""
+    chunks span several tiles and end ragged.  Every rank count the kernel
+    is compiled for (2-8, 16, 32, 64) and the runtime-rank ring (24).
+    Nothing outside the buffers may change."""
     vec = 8 if dtype in HALF else 4
     count = 3 * 512 * vec * min(n, 8) + 2048 * n + 13
     x = inputs(n, count, dtype, "values", seed=41 + n)
