@@ -61,6 +61,9 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 // Grid-wide barrier with a bounded wait.  Returns false when the kernel must
 // stop: this block timed out (it then raises `abort` for the others and
 // records AR_ERR_TIMEOUT in the sticky status) or another block already did.
+// The abort flag and the clock are read every 32 polls, and the poll backs
+// off only after 1024 (measured: 64 ranks x 64 KiB bf16 ring 279.6 -> 260.9
+// us, 2.2 -> 2.1 us a step; never backing off made no further difference).
 // The block's stores are ordered before its arrival by the CTA barrier and
 // the gpu-scope release of the arrival (release is cumulative); the acquire
 // load that sees the last arrival orders every later load after all of them.
@@ -73,17 +76,19 @@ __device__ bool grid_barrier(SyncBlock* sb, unsigned target, bool arrive, int64_
     const uint64_t t0 = global_ns();
     unsigned spins = 0;
     while (ld_acquire_u32(&sb->counter) < target) {
-      if (ld_relaxed_s32(&sb->abort)) {
-        ok = 0;
-        break;
+      if ((++spins & 31) == 0) {
+        if (ld_relaxed_s32(&sb->abort)) {
+          ok = 0;
+          break;
+        }
+        if (spins > kMaxSpin || global_ns() - t0 > (uint64_t)timeout_ns) {
+          atomicExch(&sb->abort, 1);
+          atomicCAS(&sb->status, 0, kTimeoutStatus);
+          ok = 0;
+          break;
+        }
       }
-      if (++spins > kMaxSpin || global_ns() - t0 > (uint64_t)timeout_ns) {
-        atomicExch(&sb->abort, 1);
-        atomicCAS(&sb->status, 0, kTimeoutStatus);
-        ok = 0;
-        break;
-      }
-      if (spins > 32) __nanosleep(64);
+      if (spins > 1024) __nanosleep(64);
     }
     s_ok = ok;
   }
