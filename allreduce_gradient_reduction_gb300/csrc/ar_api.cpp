@@ -554,6 +554,25 @@ int check_common(int nranks, int64_t count, int dtype, int op, int algo) {
 }
 int current_context_id(unsigned long long* id) { return context_id(id); }
 
+cudaError_t open_kernel(const void* kernel, int smem_bytes, bool big_clusters,
+                        std::atomic<unsigned long long>* tag) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  if (context_id(&ctx) != AR_OK) return cudaErrorDeviceUninitialized;
+  if (ctx != 0 && tag[dev].load() == ctx) return cudaSuccess;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
+    return e;
+  if (big_clusters && (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  // the first runtime call on this thread may have made the device's context current
+  if (ctx == 0 && context_id(&ctx) != AR_OK) return cudaErrorDeviceUninitialized;
+  tag[dev].store(ctx);
+  return cudaSuccess;
+}
+
 std::atomic<int64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace ar

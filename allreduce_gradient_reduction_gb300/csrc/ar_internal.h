@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ar {
 
 enum Dtype { F32 = 0, BF16 = 1, I32 = 2, F16 = 3 };
@@ -182,6 +184,15 @@ int note_cuda_failure(cudaError_t e);
 // Device addresses the library caches per device are keyed by it, so a
 // context that was torn down (cudaDeviceReset) and replaced is noticed.
 int current_context_id(unsigned long long* id);
+// Applies a kernel's per-function settings -- the opt-in to `smem_bytes` of
+// dynamic shared memory and, with `big_clusters`, to clusters past the
+// portable eight blocks -- once per context.  `tag` has one entry per device
+// ordinal holding the id of the context they were last applied in: function
+// attributes belong to the module as loaded in one context, and a context
+// torn down and replaced (cudaDeviceReset) loads the module anew with the
+// defaults.
+cudaError_t open_kernel(const void* kernel, int smem_bytes, bool big_clusters,
+                        std::atomic<unsigned long long>* tag);
 
 // Counts every kernel launch the library enqueues (ar_kernel_launches).
 void count_launch();

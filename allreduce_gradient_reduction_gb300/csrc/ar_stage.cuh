@@ -489,17 +489,10 @@ template <int DT, int OP, int ORDER, int NR, int GATHER = 0, class ARGS>
 cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
   constexpr int kSmem = stage_smem_bytes(NR, ElemSize<DT>::value, GATHER);
   auto kernel = fused_stage_kernel<ARGS, DT, OP, ORDER, NR, GATHER>;
-  // opened once per device to the shared memory the kernel uses
-  static std::atomic<bool> opened[256];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // opened once per context to the shared memory the kernel uses
+  static std::atomic<unsigned long long> opened[256];
+  cudaError_t e = open_kernel(reinterpret_cast<const void*>(kernel), kSmem, false, opened);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-  if (!opened[dev].load()) {
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess)
-      return e;
-    opened[dev].store(true);
-  }
   if (fill_tiles(a.tab, 16 / ElemSize<DT>::value, kStageTileVecs, true) == 0) return cudaSuccess;
   count_launch();
   return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kStageBlock, stream, a, (size_t)kSmem);

@@ -30,18 +30,11 @@ static cudaError_t launch_step_op(bool vec, StepArgs& a, cudaStream_t s) {
 
 template <int DT, int OP>
 static cudaError_t launch_smem_typed(SmemStepArgs& a, cudaStream_t stream) {
-  // opened once per device to the largest shared memory the path uses
-  static std::atomic<bool> opened[256];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // opened once per context to the largest shared memory the path uses
+  static std::atomic<unsigned long long> opened[256];
+  cudaError_t e = open_kernel(reinterpret_cast<const void*>(stepwise_smem_kernel<DT, OP>), (int)kSmemStepBytes,
+                              false, opened);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-  if (!opened[dev].load()) {
-    e = cudaFuncSetAttribute(stepwise_smem_kernel<DT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemStepBytes);
-    if (e != cudaSuccess) return e;
-    opened[dev].store(true);
-  }
   const size_t bytes = (size_t)smem_step_bytes(a.nranks, a.count, ElemSize<DT>::value);
   stepwise_smem_kernel<DT, OP><<<1, kSmemStepBlock, bytes, stream>>>(a);
   count_launch();
@@ -52,19 +45,10 @@ static cudaError_t launch_smem_typed(SmemStepArgs& a, cudaStream_t stream) {
 
 template <int DT, int OP>
 static cudaError_t launch_cluster_typed(SmemStepArgs& a, int csize, cudaStream_t stream) {
-  static std::atomic<bool> opened[256];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  static std::atomic<unsigned long long> opened[256];  // once per context
   auto kernel = stepwise_cluster_kernel<DT, OP>;
-  if (!opened[dev].load()) {
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemStepBytes)) !=
-        cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
-    opened[dev].store(true);
-  }
+  cudaError_t e = open_kernel(reinterpret_cast<const void*>(kernel), (int)kSmemStepBytes, true, opened);
+  if (e != cudaSuccess) return e;
   const int es = ElemSize<DT>::value;
   const int64_t stride = (a.count * es + 15) / 16 * 16;
   const size_t bytes = (size_t)(((int64_t)a.nranks + csize - 1) / csize * stride);
