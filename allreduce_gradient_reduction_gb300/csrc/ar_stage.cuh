@@ -130,8 +130,8 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
   }
 }
 
-// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 3, 5, 6 or 7 (ring), 0 =
-// the table's rank count (ring).  Every order folds the ranks in increasing position order, so
+// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 3, 5, 6 or 7 (ring and
+// double binary tree), 0 = the table's rank count (ring).  Every order folds the ranks in increasing position order, so
 // each is folded as soon as its copies have landed.  GATHER: no fold, the
 // segment's owner (its chunk id) is copied to every other rank, a copy built
 // per destination in turn (1: up to eight ranks, whose phases seldom
@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
   constexpr int NS = stage_slots(NR, GATHER);
   constexpr bool kStream = !GATHER && (NR == 0 || NR > kStageSlots);  // ranks stream through the slots
-  static_assert(NR == 0 ? ORDER == RING : NR <= 64 && ((NR & (NR - 1)) == 0 || ORDER == RING), "no staged form");
+  static_assert(NR == 0 ? ORDER == RING
+                        : NR <= 64 && ((NR & (NR - 1)) == 0 || ORDER == RING || (ORDER == DBTREE && NR < kStageSlots)),
+                "no staged form");
   constexpr bool kHalfCopies = stage_copies(ES, NR, GATHER) == 8;
   extern __shared__ __align__(16) unsigned char S[];
   pdl_prologue();
@@ -499,11 +501,12 @@ cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
 }
 
 // Rows whose buffers sit at different addresses modulo 16: the staged
-// kernel for rings of any size and trees and double binary trees of 2 to 64
-// ranks.  Returns cudaErrorNotSupported otherwise (double binary trees of
-// other rank counts), for the element-wise kernel to take.
+// kernel for rings of any size, trees of 2 to 64 ranks and double binary
+// trees of 2 to 8, 16, 32 or 64 ranks.  Returns cudaErrorNotSupported
+// otherwise (double binary trees of other rank counts), for the element-wise
+// kernel to take.
 __host__ __forceinline__ bool stage_form_exists(int order, int n) {
-  return order == RING || order == TREE || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+  return order == RING || order == TREE || (n >= 2 && n <= kStageSlots) || n == 16 || n == 32 || n == 64;
 }
 
 template <int DT, int OP, class ARGS>
@@ -524,7 +527,11 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
     case TREE * 100 + 32: return launch_fused_stage<DT, OP, TREE, 32>(a, stream);
     case TREE * 100 + 64: return launch_fused_stage<DT, OP, TREE, 64>(a, stream);
     case DBTREE * 100 + 2: return launch_fused_stage<DT, OP, DBTREE, 2>(a, stream);
+    case DBTREE * 100 + 3: return launch_fused_stage<DT, OP, DBTREE, 3>(a, stream);
     case DBTREE * 100 + 4: return launch_fused_stage<DT, OP, DBTREE, 4>(a, stream);
+    case DBTREE * 100 + 5: return launch_fused_stage<DT, OP, DBTREE, 5>(a, stream);
+    case DBTREE * 100 + 6: return launch_fused_stage<DT, OP, DBTREE, 6>(a, stream);
+    case DBTREE * 100 + 7: return launch_fused_stage<DT, OP, DBTREE, 7>(a, stream);
     case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
     case DBTREE * 100 + 16: return launch_fused_stage<DT, OP, DBTREE, 16>(a, stream);
     case DBTREE * 100 + 32: return launch_fused_stage<DT, OP, DBTREE, 32>(a, stream);

@@ -316,7 +316,8 @@ def test_mixed_phase_rows(ar, n, dtype):
     thread), in every order the rank count allows, for AllReduce,
     ReduceScatter (owner store) and Reduce (root store), over a size whose
     chunks span several tiles and end ragged.  Every rank count the kernel
-    is compiled for (2-8, 16, 32, 64) and the runtime-rank ring (24).
+    is compiled for (2-8, 16, 32, 64), the runtime-rank ring and the
+    element-wise double binary tree (24).
     Nothing outside the buffers may change."""
     vec = 8 if dtype in HALF else 4
     count = 3 * 512 * vec * min(n, 8) + 2048 * n + 13

@@ -381,6 +381,8 @@ CASES = [
     (8, 2, "broadcast", False, True, (3, 5000)),
     (16, 2, "ring", False, True, (16 * 8 * 60 + 3,)),
     (16, 4, "broadcast", False, True, (7000,)),
+    (7, 2, "dbtree", False, False, (2 * 512 * 8 + 301,)),
+    (3, 4, "dbtree", False, False, (3 * 512 * 4 + 6, 9)),
 ]
 
 
