@@ -317,64 +317,6 @@ __global__ void __launch_bounds__(kFusedBlock, fused_min_blocks(ORDER, NR))
   }
 }
 
-// Same computation element by element, for rows whose buffers sit at
-// different addresses modulo 16.  Each thread takes kScalarUnroll elements of
-// a tile, kFusedBlock apart.  In ring order (the naive order too) it walks the
-// ranks once for all of them, so their loads from each rank are in flight
-// together; the trees fold each element on its own.  Measured with every rank
-// at a different offset: 8 x 128 MiB bf16 SUM 1030 us at one element per
-// thread, 623 at two, 560 at four, 1052 at eight; 8 x 25 MiB f32 AVG 118.8,
-// 86.0, 83.0 and 139.6 us.
-constexpr int kScalarUnroll = 4;
-
-template <class ARGS, int DT, int OP, int ORDER>
-__global__ void __launch_bounds__(kFusedBlock) fused_scalar_kernel(const __grid_constant__ ARGS a) {
-  constexpr int ES = ElemSize<DT>::value;
-  constexpr int SU = kScalarUnroll;
-  pdl_prologue();
-  const auto& T = a.tab;
-  const int n = T.nranks;
-  for (int64_t tile = blockIdx.x; tile < T.ntiles; tile += gridDim.x) {
-    const Seg& s = T.seg[find_seg(T, tile)];
-    const int64_t e0 = s.begin + (tile - s.tile_begin) * (int64_t)kFusedBlock * SU + threadIdx.x;
-    if (e0 >= s.end) continue;
-    const void* const* P = T.ptr + (size_t)s.tensor * n;
-    uint32_t r[SU];
-    bool ok[SU];
-#pragma unroll
-    for (int u = 0; u < SU; ++u) ok[u] = e0 + (int64_t)u * kFusedBlock < s.end;
-    if constexpr (ORDER == RING) {
-      const void* src = P[rot(s.chunk + 1, n)];
-#pragma unroll
-      for (int u = 0; u < SU; ++u)
-        if (ok[u]) r[u] = ld_elem<ES>(src, e0 + (int64_t)u * kFusedBlock);
-#pragma unroll 1
-      for (int p = 1; p < n; ++p) {
-        src = P[rot(s.chunk + 1 + p, n)];
-#pragma unroll
-        for (int u = 0; u < SU; ++u)
-          if (ok[u]) r[u] = step_word<DT, OP>(r[u], ld_elem<ES>(src, e0 + (int64_t)u * kFusedBlock));
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < SU; ++u)
-        if (ok[u]) r[u] = fold_scalar<DT, OP, ORDER>(P, n, s.chunk, e0 + (int64_t)u * kFusedBlock);
-    }
-#pragma unroll
-    for (int u = 0; u < SU; ++u) {
-      if (!ok[u]) continue;
-      const int64_t e = e0 + (int64_t)u * kFusedBlock;
-      uint32_t v = r[u];
-      if (a.avg) v = div_word<DT>(v, a.fn);
-      if (a.owner_only || a.to_root) {
-        st_elem<ES>(const_cast<void*>(P[a.owner_only ? s.chunk : a.root]), e, v);
-      } else {
-        for (int q = 0; q < n; ++q) st_elem<ES>(const_cast<void*>(P[q]), e, v);
-      }
-    }
-  }
-}
-
 // ---- host side ---------------------------------------------------------------
 
 // Tiles of `tile_elems` vectors (or elements) per segment; a segment with
@@ -450,33 +392,23 @@ cudaError_t launch_fused_vec(ARGS& a, cudaStream_t stream) {
                     stream, a);
 }
 
-template <int DT, int OP, int ORDER, class ARGS>
-cudaError_t launch_fused_scalar(ARGS& a, cudaStream_t stream) {
-  if (fill_tiles(a.tab, 1, (int64_t)kFusedBlock * kScalarUnroll) == 0) return cudaSuccess;
-  count_launch();
-  return launch_pdl(fused_scalar_kernel<ARGS, DT, OP, ORDER>, grid_for(a.tab.ntiles, a.max_grid), kFusedBlock, stream,
-                    a);
-}
-
-// Dispatch on order and rank count for one (dtype, op).
+// Dispatch on order and rank count for one (dtype, op), rows whose buffers
+// share their address modulo 16.  Double binary trees of other rank counts
+// than these, and rows whose buffers do not, take the staged kernel.
 template <int DT, int OP, class ARGS>
-cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream) {
+cudaError_t launch_fused_typed(int order, ARGS& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
   if (order == DBTREE) {
-    // register-resident trees for the common rank counts, the element-wise
-    // kernel (recursive fold) for the others
-    if (vec) switch (n) {
-        case 2: return launch_fused_vec<DT, OP, DBTREE, 2>(a, stream);
-        case 4: return launch_fused_vec<DT, OP, DBTREE, 4>(a, stream);
-        case 8: return launch_fused_vec<DT, OP, DBTREE, 8>(a, stream);
-        case 16: return launch_fused_vec<DT, OP, DBTREE, 16>(a, stream);
-        case 32: return launch_fused_vec<DT, OP, DBTREE, 32>(a, stream);
-        case 64: return launch_fused_vec<DT, OP, DBTREE, 64>(a, stream);
-        default: break;
-      }
-    return launch_fused_scalar<DT, OP, DBTREE>(a, stream);
+    switch (n) {
+      case 2: return launch_fused_vec<DT, OP, DBTREE, 2>(a, stream);
+      case 4: return launch_fused_vec<DT, OP, DBTREE, 4>(a, stream);
+      case 8: return launch_fused_vec<DT, OP, DBTREE, 8>(a, stream);
+      case 16: return launch_fused_vec<DT, OP, DBTREE, 16>(a, stream);
+      case 32: return launch_fused_vec<DT, OP, DBTREE, 32>(a, stream);
+      case 64: return launch_fused_vec<DT, OP, DBTREE, 64>(a, stream);
+      default: return cudaErrorNotSupported;
+    }
   }
-  if (!vec) return order == RING ? launch_fused_scalar<DT, OP, RING>(a, stream) : launch_fused_scalar<DT, OP, TREE>(a, stream);
   if (order == RING) {
     switch (n) {
       case 2: return launch_fused_vec<DT, OP, RING, 2>(a, stream);
@@ -503,10 +435,6 @@ cudaError_t launch_fused_typed(int order, bool vec, ARGS& a, cudaStream_t stream
 
 #define AR_DEFINE_FUSED(NAME, DT, OP)                                                              \
   namespace ar {                                                                                  \
-  cudaError_t NAME(int order, bool vec, FusedArgs& a, cudaStream_t s) {                           \
-    return launch_fused_typed<DT, OP>(order, vec, a, s);                                          \
-  }                                                                                               \
-  cudaError_t NAME(int order, bool vec, SmallFusedArgs& a, cudaStream_t s) {                      \
-    return launch_fused_typed<DT, OP>(order, vec, a, s);                                          \
-  }                                                                                               \
+  cudaError_t NAME(int order, FusedArgs& a, cudaStream_t s) { return launch_fused_typed<DT, OP>(order, a, s); }      \
+  cudaError_t NAME(int order, SmallFusedArgs& a, cudaStream_t s) { return launch_fused_typed<DT, OP>(order, a, s); } \
   }

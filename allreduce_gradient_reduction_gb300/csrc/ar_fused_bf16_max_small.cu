@@ -2,7 +2,7 @@
 #include "ar_fused.cuh"
 
 namespace ar {
-cudaError_t launch_fused_bf16_max(int order, bool vec, SmallFusedArgs& a, cudaStream_t s) {
-  return launch_fused_typed<BF16, MAX>(order, vec, a, s);
+cudaError_t launch_fused_bf16_max(int order, SmallFusedArgs& a, cudaStream_t s) {
+  return launch_fused_typed<BF16, MAX>(order, a, s);
 }
 }  // namespace ar

@@ -2,7 +2,7 @@
 #include "ar_fused.cuh"
 
 namespace ar {
-cudaError_t launch_fused_f32_max(int order, bool vec, SmallFusedArgs& a, cudaStream_t s) {
-  return launch_fused_typed<F32, MAX>(order, vec, a, s);
+cudaError_t launch_fused_f32_max(int order, SmallFusedArgs& a, cudaStream_t s) {
+  return launch_fused_typed<F32, MAX>(order, a, s);
 }
 }  // namespace ar

@@ -159,8 +159,10 @@ struct Int8Args {
 };
 
 // Launchers.  Each fills tab.seg[*].tile_begin and tab.ntiles for its own
-// tile shape, then enqueues on `stream`.  `vec` selects the 16-byte path
-// (every pointer 16-byte aligned); otherwise one element per thread.
+// tile shape, then enqueues on `stream`.  `vec`: every row's buffers share
+// their address modulo 16, so 16-byte vectors line up across ranks; rows
+// that do not take the staged kernel (launch_fused, launch_gather) or one
+// element per thread (launch_stepwise).
 cudaError_t launch_fused(int dtype, int op, int order, bool vec, FusedArgs& args, cudaStream_t stream);
 cudaError_t launch_fused(int dtype, int op, int order, bool vec, SmallFusedArgs& args, cudaStream_t stream);
 cudaError_t launch_gather(int esize, bool vec, SegTable& tab, cudaStream_t stream);

@@ -1,6 +1,7 @@
 // Fused AllReduce / ReduceScatter / Reduce for rows whose rank buffers sit
-// at different addresses modulo 16: the same fold, in the same order, as the
-// fused kernels in ar_fused.cuh, with every rank's words staged in shared
+// at different addresses modulo 16, and double binary trees of the rank
+// counts the kernels in ar_fused.cuh are not compiled for: the same fold, in
+// the same order, as those kernels, with every rank's words staged in shared
 // memory and realigned there.
 #pragma once
 
@@ -130,8 +131,12 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
   }
 }
 
-// NR: 2, 4, 8, 16, 32 or 64 ranks (every order), 3, 5, 6 or 7 (ring and
-// double binary tree), 0 = the table's rank count (ring).  Every order folds the ranks in increasing position order, so
+// NR: 2, 4, 8, 16, 32 or 64 ranks (rings and trees), 2 to 8, 16 or 32
+// (double binary trees), 3, 5, 6 or 7 (rings), 0 = the table's rank count
+// (rings and double binary trees).  The double binary tree's unrolled fold
+// beats the run-time one up to 32 ranks and loses at 64 (bf16 at eight
+// offsets: 16 x 32 MiB 161.5 against 216.8 us, 32 x 16 MiB f32 164.9
+// against 186.3, 64 x 8 MiB 262.7 against 228.7).  Every order folds the ranks in increasing position order, so
 // each is folded as soon as its copies have landed.  GATHER: no fold, the
 // segment's owner (its chunk id) is copied to every other rank, a copy built
 // per destination in turn (1: up to eight ranks, whose phases seldom
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
   constexpr int NS = stage_slots(NR, GATHER);
   constexpr bool kStream = !GATHER && (NR == 0 || NR > kStageSlots);  // ranks stream through the slots
-  static_assert(NR == 0 ? ORDER == RING
+  static_assert(NR == 0 ? ORDER == RING || ORDER == DBTREE
                         : NR <= 64 && ((NR & (NR - 1)) == 0 || ORDER == RING || (ORDER == DBTREE && NR < kStageSlots)),
                 "no staged form");
   constexpr bool kHalfCopies = stage_copies(ES, NR, GATHER) == 8;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < G; ++j) res[j] = group(0, j);
-      } else if constexpr (ORDER == DBTREE) {
+      } else if constexpr (ORDER == DBTREE && NR > 0) {
         // the in-order tree visits positions in increasing order too
         auto take = [&](int p, uint4 (&v)[G]) {
           cp_async_wait_pending(later_than(p));
@@ -273,7 +278,62 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
             ++top;
           }
         };
-        if constexpr (kWideTree) {
+        if constexpr (ORDER == DBTREE) {
+          // a rank count known at run time.  In the in-order tree over
+          // positions 1..n (see inorder_root) position q sits at level
+          // tz(q): odd positions are leaves, and node q of level l >= 1 has
+          // the 2^l - 1 positions before it as its left subtree.  A leaf
+          // completes at once and, while the subtree it completes is a right
+          // child (the bits of q above bit 0 are ones), completes its parent
+          // too, whose held value takes it in.  Node q of level l >= 1 holds
+          // (its left subtree) (+) x_q until then.  Subtrees whose parent
+          // would lie past n fold in at the end, right-nested from the
+          // lowest open level up.  Every index into `hold` is a constant.
+          constexpr int kLevels = 6;  // 64 positions: levels 1..6
+          uint4 hold[kLevels][G], cur[G];
+          unsigned open = 0;  // bit l: node of level l holding
+          bool pend = false;  // cur: a finished subtree waiting for its parent
+#pragma unroll 1
+          for (int p = 0; p < n; ++p) {
+            arrive(p);
+            const unsigned q = p + 1;
+            if (q & 1) {
+              const int casc = __ffs(~(q >> 1)) - 1;  // levels of the parents it completes
+#pragma unroll
+              for (int j = 0; j < G; ++j) cur[j] = group(p, j);
+#pragma unroll
+              for (int l = 1; l <= kLevels; ++l)
+                if (l <= casc) {
+#pragma unroll
+                  for (int j = 0; j < G; ++j) cur[j] = step_vec<DT, OP>(hold[l - 1][j], cur[j]);
+                }
+              open &= ~((2u << casc) - 2u);
+              pend = true;
+            } else {
+              const int t = __ffs(q) - 1;
+              uint4 v[G];
+#pragma unroll
+              for (int j = 0; j < G; ++j) v[j] = step_vec<DT, OP>(cur[j], group(p, j));
+#pragma unroll
+              for (int l = 1; l <= kLevels; ++l)
+                if (l == t) {
+#pragma unroll
+                  for (int j = 0; j < G; ++j) hold[l - 1][j] = v[j];
+                }
+              open |= 1u << t;
+              pend = false;
+            }
+          }
+#pragma unroll
+          for (int l = 1; l <= kLevels; ++l)
+            if (open & (1u << l)) {
+#pragma unroll
+              for (int j = 0; j < G; ++j) cur[j] = pend ? step_vec<DT, OP>(hold[l - 1][j], cur[j]) : hold[l - 1][j];
+              pend = true;
+            }
+#pragma unroll
+          for (int j = 0; j < G; ++j) res[j] = cur[j];
+        } else if constexpr (kWideTree) {
           // subtrees of 8 consecutive ranks, each folded by the unrolled
           // counter above, merged by a counter over the subtree index in a
           // loop that is not unrolled (unrolled over 64 ranks the kernel is
@@ -500,15 +560,9 @@ cudaError_t launch_fused_stage(ARGS& a, cudaStream_t stream) {
   return launch_pdl(kernel, grid_for(a.tab.ntiles, a.max_grid), kStageBlock, stream, a, (size_t)kSmem);
 }
 
-// Rows whose buffers sit at different addresses modulo 16: the staged
-// kernel for rings of any size, trees of 2 to 64 ranks and double binary
-// trees of 2 to 8, 16, 32 or 64 ranks.  Returns cudaErrorNotSupported
-// otherwise (double binary trees of other rank counts), for the element-wise
-// kernel to take.
-__host__ __forceinline__ bool stage_form_exists(int order, int n) {
-  return order == RING || order == TREE || (n >= 2 && n <= kStageSlots) || n == 16 || n == 32 || n == 64;
-}
-
+// The staged kernel for one (dtype, op): every order and rank count the
+// order takes (trees: powers of two up to 64).  cudaErrorNotSupported for
+// any other.
 template <int DT, int OP, class ARGS>
 cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
   const int n = a.tab.nranks;
@@ -535,10 +589,10 @@ cudaError_t launch_stage_typed(int order, ARGS& a, cudaStream_t stream) {
     case DBTREE * 100 + 8: return launch_fused_stage<DT, OP, DBTREE, 8>(a, stream);
     case DBTREE * 100 + 16: return launch_fused_stage<DT, OP, DBTREE, 16>(a, stream);
     case DBTREE * 100 + 32: return launch_fused_stage<DT, OP, DBTREE, 32>(a, stream);
-    case DBTREE * 100 + 64: return launch_fused_stage<DT, OP, DBTREE, 64>(a, stream);
     default: break;
   }
   if (order == RING) return launch_fused_stage<DT, OP, RING, 0>(a, stream);
+  if (order == DBTREE) return launch_fused_stage<DT, OP, DBTREE, 0>(a, stream);
   return cudaErrorNotSupported;
 }
 

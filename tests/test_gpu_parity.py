@@ -312,12 +312,11 @@ def test_mixed_phase_rows(ar, n, dtype):
     """Rank buffers at different addresses modulo 16 (the staged kernel:
     aligned words of every rank copied to shared memory, through eight slots
     beyond eight ranks, folded in the first buffer's frame, stored back at
-    each rank's phase; double binary trees of other rank counts one element per
-    thread), in every order the rank count allows, for AllReduce,
+    each rank's phase), in every order the rank count allows, for AllReduce,
     ReduceScatter (owner store) and Reduce (root store), over a size whose
     chunks span several tiles and end ragged.  Every rank count the kernel
-    is compiled for (2-8, 16, 32, 64), the runtime-rank ring and the
-    element-wise double binary tree (24).
+    is compiled for (2-8, 16, 32, 64) and the runtime-rank ring and double
+    binary tree (24).
     Nothing outside the buffers may change."""
     vec = 8 if dtype in HALF else 4
     count = 3 * 512 * vec * min(n, 8) + 2048 * n + 13
@@ -770,8 +769,11 @@ def test_broadcast_copies_bits(ar, dtype):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
-@pytest.mark.parametrize("n", [2, 3, 4, 5, 8, 16, 64])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 6, 7, 8, 12, 16, 64])
 def test_dbtree_matches_oracle(ar, dtype, n):
+    """Aligned rows: the register-resident kernel (2, 4, 8, 16, 64 ranks)
+    and the staged kernel, compiled for the rank count (3, 5, 6, 7) or
+    taking it at run time (12)."""
     for count in [c for c in (1, 2, n + 1, 4099, 2 * 2048 * n + 11) if c > 0]:
         for op in ["sum", "max"] + ([] if dtype == "i32" else ["avg"]):
             x = inputs(n, count, dtype, "bits" if (count % 2 and op != "sum") else "values", seed=2100 + n + count)

@@ -137,8 +137,9 @@ def words(b):
     return b.view("<u4").astype(np.uint64)
 
 
-def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000,), mutation=None):
-    """mutation: a planted mistake in the modelled kernel (see the last test)."""
+def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000,), mutation=None, phase=None):
+    """phase: every buffer at this address modulo 16 (else each at its own);
+    mutation: a planted mistake in the modelled kernel (see the last test)."""
     vec = 16 // es
     mem = Memory()
     ptrs, valid, orig = [], [], []
@@ -146,7 +147,7 @@ def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000
         for r in range(nr):
             base = 0x4000000 * (1 + len(ptrs))
             mem.alloc(base, cnt * es + 64)
-            p = base + rng.randrange(0, 16 // es) * es + 16 * rng.randrange(0, 2)
+            p = base + (rng.randrange(0, 16 // es) * es if phase is None else phase) + 16 * rng.randrange(0, 2)
             data = np.frombuffer(rng.randbytes(cnt * es), np.uint8)
             mem.write(p, data)
             ptrs.append(p)
@@ -383,6 +384,7 @@ CASES = [
     (16, 4, "broadcast", False, True, (7000,)),
     (7, 2, "dbtree", False, False, (2 * 512 * 8 + 301,)),
     (3, 4, "dbtree", False, False, (3 * 512 * 4 + 6, 9)),
+    (12, 2, "dbtree", False, False, (2 * 512 * 8 + 1001,)),
 ]
 
 
@@ -393,6 +395,58 @@ def test_staged_kernel_index_model(case):
     root = rng.randrange(nr)
     tiles = run(rng, nr, es, order, owner_only, gather, root, counts)
     assert tiles >= len(counts)
+
+
+@pytest.mark.parametrize("nr,es,phase", [(5, 2, 6), (7, 4, 0), (3, 2, 0)])
+def test_staged_kernel_index_model_one_phase(nr, es, phase):
+    """Double binary trees of 3, 5 and 7 ranks take the staged kernel even
+    when every buffer sits at the same address modulo 16."""
+    rng = random.Random(nr * 100 + es)
+    run(rng, nr, es, "dbtree", counts=(2 * 512 * 16 // es + 77, 5), phase=phase)
+
+
+def level_counter_fold(xs, f, mutation=None):
+    """The double binary tree's fold as the staged kernel takes it for a rank
+    count known at run time: positions arrive in order; position q sits at
+    level tz(q) of the in-order tree; a leaf (odd q) completes at once and,
+    while the subtree it completes is a right child (the bits of q above bit
+    0 are ones), completes its parents, whose held values take it in; node q
+    of level l >= 1 holds (its left subtree) (+) x_q; at the end the held
+    values fold in right-nested from the lowest level up."""
+    hold, cur, pend, opn = [None] * 7, None, False, 0
+    for q in range(1, len(xs) + 1):
+        if q & 1:
+            casc = ((~(q >> 1)) & -(~(q >> 1))).bit_length() - 1  # ones above bit 0
+            cur = xs[q - 1]
+            for lv in range(1, casc + 1):
+                cur = f(hold[lv], cur)
+            opn &= ~((2 << casc) - 2)
+            pend = True
+        else:
+            t = (q & -q).bit_length() - 1
+            hold[t] = f(cur, xs[q - 1]) if mutation != "operands_swapped" else f(xs[q - 1], cur)
+            opn |= 1 << t
+            pend = False
+    levels = range(1, 7) if mutation != "end_from_the_top" else range(6, 0, -1)
+    for lv in levels:
+        if opn & (1 << lv):
+            cur = f(hold[lv], cur) if pend else hold[lv]
+            pend = True
+    return cur
+
+
+def test_dbtree_level_counter_rule():
+    """The run-time double binary tree fold equals the recursive in-order
+    definition for every rank count up to 64 (a step that keeps its operands
+    as text shows any change of order or grouping), and two planted
+    mistakes make it differ."""
+    f = lambda a, b: f"({a}.{b})"
+    for n in range(1, 65):
+        xs = [f"x{q}" for q in range(1, n + 1)]
+        assert level_counter_fold(xs, f) == inorder_fold(xs, 1, n, f), n
+    for mutation in ("operands_swapped", "end_from_the_top"):
+        assert any(level_counter_fold([f"x{q}" for q in range(1, n + 1)], f, mutation)
+                   != inorder_fold([f"x{q}" for q in range(1, n + 1)], 1, n, f) for n in range(1, 65)), mutation
 
 
 @pytest.mark.parametrize("mutation", ["ring_from_owner", "no_word_past_tile", "bulk_one_entry_late"])
