@@ -31,11 +31,9 @@
  *     cut at that offset.  Buffers at different offsets modulo 16 still move
  *     in aligned 16-byte words in the fused kernels (each rank's words staged
  *     in shared memory, folded there in the first buffer's frame and written
- *     back at each rank's own offset) for rings of any size, trees of 2 to
- *     64 ranks and double binary trees of 2 to 8, 16, 32 or 64 ranks, and
- *     for AllGather and Broadcast; double binary trees of other rank counts
- *     and the step-wise and copy kernels then take a slower
- *     one-element-per-thread path.  (For a bucketed call this holds per
+ *     back at each rank's own offset) for every order and rank count, and
+ *     for AllGather and Broadcast; the step-wise and copy kernels then take
+ *     a slower one-element-per-thread path.  (For a bucketed call this holds per
  *     tensor: each tensor's N buffers.)
  *   - 1 <= nranks <= AR_MAX_RANKS; 0 <= count <= AR_MAX_COUNT (else
  *     AR_ERR_INVALID_ARG, as for a buffer whose end would pass the top of the
