@@ -56,6 +56,8 @@ def parse():
                         "elements into its allocation, so the ranks sit at different addresses modulo 16")
     p.add_argument("--count", type=int, default=0,
                    help="elements per rank (default: the full workload); smaller counts are for profiling")
+    p.add_argument("--nranks", type=int, default=0,
+                   help="ranks of the large workload (default: 8); other counts are for profiling")
     p.add_argument("--variants", action="store_true", help="also time tree and step-wise orders (extra keys)")
     p.add_argument("--workload", choices=["large", "bucket", "gpt2"], default="large",
                    help="large: the headline (default); bucket: 8 x 25 MiB f32 AVG; gpt2: DDP buckets of GPT-2 small")
@@ -491,7 +493,7 @@ class LargeWorkload:
 
     def __init__(self, args, dev, torch, np, W, ar):
         self.ar, self.args = ar, args
-        self.n, self.count = W.LARGE["nranks"], (args.count or W.LARGE["count"])
+        self.n, self.count = (args.nranks or W.LARGE["nranks"]), (args.count or W.LARGE["count"])
         self.bytes_step = 2 * self.n * self.count * 2
         self.host = torch.empty((self.n, self.count), dtype=torch.int16, pin_memory=True)
         for r in range(self.n):
@@ -500,8 +502,9 @@ class LargeWorkload:
         self.bufs = rank_buffers(self.n, self.count, torch.int16, dev, 2, args.rank_offsets)
         self.h2d = [(self.host[r], self.bufs[r]) for r in range(self.n)]
         self.d2h = [(self.bufs[r], self.out[r]) for r in range(self.n)]
-        self.workload = WORKLOAD if self.count == W.LARGE["count"] else (
-            f"ring AllReduce SUM, {self.n} ranks x {self.count:,} bf16 ({self.count * 2 / 2**20:g} MiB per rank)")
+        headline = self.count == W.LARGE["count"] and self.n == W.LARGE["nranks"] and args.algo == "ring"
+        self.workload = WORKLOAD if headline else (
+            f"{args.algo} AllReduce SUM, {self.n} ranks x {self.count:,} bf16 ({self.count * 2 / 2**20:g} MiB per rank)")
         if args.rank_offsets == "mixed":
             self.workload += ", rank buffers at different addresses modulo 16"
         self.config = {"nranks": self.n, "count_per_rank": self.count, "algo": args.algo, "op": self.op,
@@ -1268,7 +1271,9 @@ def main():
             "accuracy": acc, "context": PAGES_CONTEXT,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": profiled_traffic() if isinstance(wl, LargeWorkload) and not args.count else None,
+                         # the capture is of the headline kernel: aligned ring, full size
+                         "traffic": profiled_traffic() if (isinstance(wl, LargeWorkload) and wl.workload == WORKLOAD
+                                                           and args.rank_offsets == "aligned") else None,
                          "algorithmic_bytes_per_launch": nbytes_step},
             "e2e": e2e,
             "gpu_launches": launches,
