@@ -136,7 +136,7 @@ __device__ __forceinline__ void stage_inorder(uint4 (&acc)[G], TAKE& take) {
 // (rings and double binary trees).  The double binary tree's unrolled fold
 // beats the run-time one up to 32 ranks and loses at 64 (bf16 at eight
 // offsets: 16 x 32 MiB 161.5 against 216.8 us, 32 x 16 MiB f32 164.9
-// against 186.3, 64 x 8 MiB 262.7 against 228.7).  Every order folds the ranks in increasing position order, so
+// against 186.3, 64 x 8 MiB 262.7 against 223.1).  Every order folds the ranks in increasing position order, so
 // each is folded as soon as its copies have landed.  GATHER: no fold, the
 // segment's owner (its chunk id) is copied to every other rank, a copy built
 // per destination in turn (1: up to eight ranks, whose phases seldom
@@ -301,12 +301,13 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
               const int casc = __ffs(~(q >> 1)) - 1;  // levels of the parents it completes
 #pragma unroll
               for (int j = 0; j < G; ++j) cur[j] = group(p, j);
+              // a uniform early exit, not predication: 12-64 ranks 2-3% faster
 #pragma unroll
-              for (int l = 1; l <= kLevels; ++l)
-                if (l <= casc) {
+              for (int l = 1; l <= kLevels; ++l) {
+                if (l > casc) break;
 #pragma unroll
-                  for (int j = 0; j < G; ++j) cur[j] = step_vec<DT, OP>(hold[l - 1][j], cur[j]);
-                }
+                for (int j = 0; j < G; ++j) cur[j] = step_vec<DT, OP>(hold[l - 1][j], cur[j]);
+              }
               open &= ~((2u << casc) - 2u);
               pend = true;
             } else {
