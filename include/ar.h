@@ -339,11 +339,10 @@ int ar_bucketed_allreduce(void* const* grads, const int64_t* counts, int ntensor
  * GPU where the library's device code is loaded, until the process exits
  * (with CUDA's default lazy module loading, from the first call on that GPU).
  * The first call on each device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress, no allocation); make that
- * first call before any stream capture.  The address is remembered together
- * with the context it belongs to: after the device's context has been torn
- * down and replaced (cudaDeviceReset), the next call looks it up again (that
- * call, too, should come before any capture).
+ * array's device address (cudaGetSymbolAddress, no allocation).  The address
+ * is remembered together with the context it belongs to: after the device's
+ * context has been torn down and replaced (cudaDeviceReset), the next call
+ * looks it up again.
  */
 #define AR_NOALLOC_SCRATCH_BYTES (32 << 20)
 #define AR_NOALLOC_MAX_TENSORS 1024
