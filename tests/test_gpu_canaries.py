@@ -59,7 +59,7 @@ def sizes(n):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "i32", "f16"])
-@pytest.mark.parametrize("n", [2, 3, 8, 16])
+@pytest.mark.parametrize("n", [2, 3, 8, 12, 16])
 def test_collectives_stay_inside_their_buffers(ar, n, dtype):
     algos = ["ring", "ring_stepwise", "naive", "dbtree"] + (
         ["tree", "tree_stepwise", "binomial_stepwise"] if n & (n - 1) == 0 else [])
