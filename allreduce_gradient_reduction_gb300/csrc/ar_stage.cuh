@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
           // would lie past n fold in at the end, right-nested from the
           // lowest open level up.  Every index into `hold` is a constant.
           constexpr int kLevels = 6;  // 64 positions: levels 1..6
+          static_assert((1 << kLevels) >= kMaxRanks && (1 << kLevels) < 2 * kMaxRanks, "a level per bit of q");
           uint4 hold[kLevels][G], cur[G];
           unsigned open = 0;  // bit l: node of level l holding
           bool pend = false;  // cur: a finished subtree waiting for its parent
