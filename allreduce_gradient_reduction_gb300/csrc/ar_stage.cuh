@@ -75,28 +75,38 @@ constexpr int kStageSlots = 8;
 // runtime rank count) and more ranks stream through eight.  The gather forms
 // (AllGather, Broadcast: one owner's words copied to the other ranks; GATHER
 // 1 for up to eight ranks, 2 beyond) hold one.
-__host__ __device__ constexpr int stage_slots(int nr, int gather) {
-  return gather ? 1 : nr > 0 && nr < kStageSlots ? nr : kStageSlots;
+// Rows of 4-byte elements and 6 to 8 ranks stream through five slots: they
+// keep four result copies, so the slots set the block's shared memory, and
+// five blocks of 41 KB per SM beat three of 66 KB (f32 at four offsets, bit
+// for bit the same: 8 x 25 MiB AVG 66.0 -> 63.8 us, 8 x 64 MiB ring 159.2 ->
+// 156.2, tree 161.6 -> 155.9; four slots 64.1, 156.3 and 156.8).
+constexpr int kStageSlotsF32 = 5;
+__host__ __device__ constexpr int stage_slots(int nr, int gather, int es) {
+  return gather                                                 ? 1
+         : es == 4 && nr > kStageSlotsF32 && nr <= kStageSlots ? kStageSlotsF32
+         : nr > 0 && nr < kStageSlots                          ? nr
+                                                                : kStageSlots;
 }
 constexpr int kStageTileVecs = 512;
 constexpr int kStageSlotBytes = kStageTileVecs * 16 + 16;          // one rank's staged words
 constexpr int kStageCopyBytes = (kStageTileVecs + 2) * 16;         // one shifted copy of the result
 __host__ __device__ constexpr int stage_copies(int es, int nr, int gather) {
-  return gather == 1 ? 2 : es == 2 && (gather == 2 || stage_slots(nr, gather) == kStageSlots) ? 8 : 4;
+  return gather == 1 ? 2 : es == 2 && (gather == 2 || stage_slots(nr, gather, es) == kStageSlots) ? 8 : 4;
 }
 // Gather form 1 keeps its slot and two copy buffers apart (it builds one
 // destination's copy while the bulk copy of the previous one reads the
 // other); the other forms reuse the slots for the copies.
 __host__ __device__ constexpr int stage_smem_bytes(int nr, int es, int gather) {
   return gather == 1 ? kStageSlotBytes + 2 * kStageCopyBytes
-         : stage_slots(nr, gather) * kStageSlotBytes > stage_copies(es, nr, gather) * kStageCopyBytes
-             ? stage_slots(nr, gather) * kStageSlotBytes
+         : stage_slots(nr, gather, es) * kStageSlotBytes > stage_copies(es, nr, gather) * kStageCopyBytes
+             ? stage_slots(nr, gather, es) * kStageSlotBytes
              : stage_copies(es, nr, gather) * kStageCopyBytes;
 }
 // Resident blocks per SM: as many as shared memory allows, since the tiles
 // in flight are what keeps HBM busy (three at 66 KB, six at 33 KB with 40
 // registers and no spills; the gather form eight at 25 KB; 5-, 6- and 7-rank
-// rings five, four and three).  Measured, 2-byte elements at eight offsets:
+// rings of 2-byte elements five, four and three; 4-byte elements of 6 to 8
+// ranks five).  Measured, 2-byte elements at eight offsets:
 // 4 x 128 MiB 162.8 / 158.5 / 157.5 us and 2 x 128 MiB 98.1 / 89.3 / 83.9 us
 // at four / five / six blocks; 8 x 128 MiB 446.7 us at two, 351.4 at three
 // (before the bulk stores).
@@ -149,8 +159,8 @@ __global__ void __launch_bounds__(kStageBlock, stage_min_blocks(NR, ElemSize<DT>
   constexpr int TV = kStageTileVecs;
   constexpr int G = TV * 4 / kStageBlock / 4;  // groups of 4 frame words per thread
   static_assert(G * 4 * kStageBlock == TV * 4, "tile is a whole number of word groups");
-  constexpr int NS = stage_slots(NR, GATHER);
-  constexpr bool kStream = !GATHER && (NR == 0 || NR > kStageSlots);  // ranks stream through the slots
+  constexpr int NS = stage_slots(NR, GATHER, ES);
+  constexpr bool kStream = !GATHER && (NR == 0 || NR > NS);  // ranks stream through the slots
   static_assert(NR == 0 ? ORDER == RING || ORDER == DBTREE
                         : NR <= 64 && ((NR & (NR - 1)) == 0 || ORDER == RING || (ORDER == DBTREE && NR < kStageSlots)),
                 "no staged form");

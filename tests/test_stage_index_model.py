@@ -32,8 +32,10 @@ COPY = (TV + 2) * 16                 # one shifted copy of the result
 M32 = (1 << 32) - 1
 
 
-def slots(nr, gather):
-    return 1 if gather else nr if nr < 8 else 8
+def slots(nr, gather, es):
+    """Rank slots: one per rank up to 8 (4-byte elements of 6 to 8 ranks:
+    five, streamed), eight streamed beyond; the gather form one."""
+    return 1 if gather else 5 if es == 4 and 5 < nr <= 8 else nr if nr < 8 else 8
 
 
 def gather_form(nr):
@@ -45,13 +47,13 @@ def gather_form(nr):
 def copies(es, nr, gather):
     if gather and gather_form(nr) == 1:
         return 2
-    return 8 if es == 2 and (gather or slots(nr, gather) == 8) else 4
+    return 8 if es == 2 and (gather or slots(nr, gather, es) == 8) else 4
 
 
 def smem_bytes(nr, es, gather):
     if gather and gather_form(nr) == 1:  # the slot, then the two copy buffers
         return SLOT + 2 * COPY
-    return max(slots(nr, gather) * SLOT, copies(es, nr, gather) * COPY)
+    return max(slots(nr, gather, es) * SLOT, copies(es, nr, gather) * COPY)
 
 
 def fshr(lo, hi, sh):
@@ -174,7 +176,7 @@ def run(rng, nr, es, order, owner_only=False, gather=False, root=0, counts=(1000
         ntiles += tiles if tiles or not extra else 1
     smem = smem_bytes(nr, es, gather)
     nfold = 1 if gather else nr
-    ns = slots(nr, gather)
+    ns = slots(nr, gather, es)
     written = {}
     for tile in rng.sample(range(ntiles), ntiles):
         sg = max((s for s in segs if s["tile_begin"] <= tile), key=lambda s: s["tile_begin"])
@@ -385,6 +387,8 @@ CASES = [
     (7, 2, "dbtree", False, False, (2 * 512 * 8 + 301,)),
     (3, 4, "dbtree", False, False, (3 * 512 * 4 + 6, 9)),
     (12, 2, "dbtree", False, False, (2 * 512 * 8 + 1001,)),
+    (8, 4, "ring", False, False, (2 * 512 * 4 * 8 + 19,)),
+    (7, 4, "dbtree", False, False, (512 * 4 * 7 + 3001,)),
 ]
 
 
