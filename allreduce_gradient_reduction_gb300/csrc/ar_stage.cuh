@@ -51,12 +51,13 @@ __device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, 
 // rank r's words from the one holding the tile's first byte in buffer r:
 // the tile's bytes then sit off_r = (P[r] - P[0]) mod 16 bytes into its
 // slot.  One commit group per rank, in the order the fold takes them; up to
-// eight ranks each have a slot, more stream through eight slots, a slot
-// refilled as soon as its rank is folded.  (2) Each thread folds 4-byte
-// words of the frame, kStageBlock apart (consecutive threads, consecutive
-// words: no bank conflicts), a rank as soon as its copies have landed: word
-// w of rank r is bytes [4w + off_r, 4w + off_r + 4) of its slot, two word
-// loads and a funnel shift when off_r is 2 mod 4, one load otherwise.
+// eight ranks each have a slot (4-byte elements: up to five ranks), more
+// stream through the slots, a slot refilled as soon as its rank is folded.
+// (2) Each thread folds 4-byte words of the frame, kStageBlock apart
+// (consecutive threads, consecutive words: no bank conflicts), a rank as
+// soon as its copies have landed: word w of rank r is bytes [4w + off_r,
+// 4w + off_r + 4) of its slot, two word loads and a funnel shift when off_r
+// is 2 mod 4, one load otherwise.
 // (3) The results go to shared memory four times, the k-th copy shifted by
 // k words, and for 2-byte elements (with eight slots) four more times moved
 // by one element, so that the 16-byte words a destination at off = 4k + h
@@ -71,8 +72,9 @@ __device__ __forceinline__ void st_stream_part(char* w, const uint4& v, int lo, 
 // the tile are never used.
 constexpr int kStageBlock = 256;
 constexpr int kStageSlots = 8;
-// Rank slots a block holds: one per rank up to eight ranks; NR = 0 (a
-// runtime rank count) and more ranks stream through eight.  The gather forms
+// Rank slots a block holds: one per rank up to eight ranks (but see
+// kStageSlotsF32); NR = 0 (a runtime rank count) and more ranks stream
+// through eight.  The gather forms
 // (AllGather, Broadcast: one owner's words copied to the other ranks; GATHER
 // 1 for up to eight ranks, 2 beyond) hold one.
 // Rows of 4-byte elements and 6 to 8 ranks stream through five slots: they
